@@ -1,0 +1,158 @@
+"""Pins for the oracle's attention over position sets (no GPU).
+
+Covers Force 2's sparse decode attention, Force 1's sink + window attention and
+Force 3's full-cache verification ("TriForce: Hierarchical Speculative Decoding
+for LLMs", "The Three Forces of TriForce").  Pins: torch's float64 scaled-dot-
+product attention as a textbook cross-check, closed forms, a hand-worked
+fixture, the split-K merge identity, set-builder statements of the position
+sets, and the reductions the method implies (sparse == full when the budget
+covers the context, window == full when the context fits the window, verify
+row j == decode attention on the truncated cache).
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import triforce as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bits(t):
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _rand_bf16(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * scale).to(torch.bfloat16)
+
+
+def test_attend_matches_torch_sdpa_float64():
+    rng = np.random.default_rng(0)
+    for n, m, D in [(1, 1, 8), (3, 17, 16), (6, 300, 128), (24, 77, 128)]:
+        q = rng.standard_normal((n, D))
+        K = rng.standard_normal((m, D)) * 2
+        V = rng.standard_normal((m, D))
+        scale = 1 / math.sqrt(D)
+        want = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None], scale=scale)[0].numpy()
+        np.testing.assert_allclose(O.attend(q, K, V, scale), want, rtol=1e-12, atol=1e-12)
+
+
+def test_attend_golden_fixture():
+    with open(os.path.join(GOLDEN, "attention_hand.json")) as f:
+        fx = json.load(f)
+    got = O.attend(np.array(fx["q"], float), np.array(fx["K"], float), np.array(fx["V"], float), fx["scale"])
+    np.testing.assert_allclose(got, np.array(fx["out"]), rtol=1e-14, atol=1e-14)
+
+
+def test_closed_forms():
+    rng = np.random.default_rng(1)
+    D = 128
+    q = rng.standard_normal((2, D))
+    V = rng.standard_normal((9, D))
+    # Identical keys: uniform weights, output = mean of V.
+    K = np.repeat(rng.standard_normal((1, D)), 9, axis=0)
+    np.testing.assert_allclose(O.attend(q, K, V, 0.1), np.repeat(V.mean(0, keepdims=True), 2, 0), atol=1e-12)
+    # A single key: output = its value row.
+    np.testing.assert_allclose(O.attend(q, K[:1], V[:1], 0.1), np.repeat(V[:1], 2, 0), atol=1e-14)
+    # One key dominating by a wide margin: output = that value row.
+    K2 = rng.standard_normal((9, D)) * 0.01
+    K2[4] = q[0] * 100
+    np.testing.assert_allclose(O.attend(q[:1], K2, V, 1.0), V[4:5], atol=1e-12)
+    # Empty key set: zeros.
+    assert np.all(O.attend(q, K[:0], V[:0], 1.0) == 0)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_split_merge_identity(seed):
+    rng = np.random.default_rng(seed)
+    n, m, D = 6, 257, 128
+    q = rng.standard_normal((n, D))
+    K = rng.standard_normal((m, D))
+    V = rng.standard_normal((m, D))
+    full = O.attend(q, K, V, 0.09)
+    for nsplit in [1, 2, 5, 64]:
+        cuts = np.sort(rng.choice(np.arange(1, m), size=nsplit - 1, replace=False)) if nsplit > 1 else []
+        bounds = [0, *cuts, m]
+        parts = [O.attend_partial(q, K[a:b], V[a:b], 0.09) for a, b in zip(bounds[:-1], bounds[1:])]
+        parts.append(O.attend_partial(q, K[:0], V[:0], 0.09))  # an empty split changes nothing
+        np.testing.assert_allclose(O.merge_partials(parts), full, rtol=1e-12, atol=1e-12)
+
+
+def test_position_sets_against_set_builder():
+    for L in [0, 1, 3, 4, 5, 100, 255, 256, 257, 300, 4096]:
+        for ns, W in [(4, 252), (0, 8), (4, 0), (8, 3)]:
+            want = sorted({t for t in range(L) if t < ns or t >= L - W})
+            assert O.window_positions(L, ns, W).tolist() == want
+        for T in [1, 5, 6]:
+            for j in range(T):
+                assert O.verify_positions(L, T, j).tolist() == [t for t in range(L) if t <= L - T + j]
+    idx = np.array([3, 0, 7, -1, 99])
+    for L in [0, 5, 20, 31, 64]:
+        want = [t for c in [3, 0, 7] if c < -(-L // 4) for t in range(4 * c, 4 * c + 4) if t < L]
+        assert O.sparse_positions(idx, 5, L, 4, 64).tolist() == want
+
+
+def test_sparse_equals_full_when_budget_covers_context():
+    B, Hq, Hkv, L, D, chunk = 2, 4, 2, 61, 128, 8
+    q = _rand_bf16((B, Hq, D), 1)
+    K = _rand_bf16((B, Hkv, L, D), 2)
+    V = _rand_bf16((B, Hkv, L, D), 3)
+    seq = np.array([61, 40])
+    M = O.build_chunk_means(_bits(K), seq, chunk)
+    kc = 8  # 8 chunks x 8 tokens >= 61
+    idx, n_sel, *_ = O.chunk_scores_topk(_bits(q), M, seq, L, chunk, kc, Hkv)
+    sp = O.sparse_decode_attn(_bits(q), _bits(K), _bits(V), seq, idx, n_sel, chunk, 0.088)
+    # Full decode attention = verification with a single query token.
+    full = O.verify_attn(_bits(q)[:, :, None, :], _bits(K), _bits(V), seq, 0.088)[:, :, 0]
+    np.testing.assert_allclose(sp, full, rtol=1e-12, atol=1e-12)
+
+
+def test_window_equals_full_when_context_fits():
+    B, Hq, Hkv, L, D = 1, 2, 1, 200, 128
+    q = _rand_bf16((B, Hq, D), 4)
+    K = _rand_bf16((B, Hkv, L, D), 5)
+    V = _rand_bf16((B, Hkv, L, D), 6)
+    for Lb in [1, 100, 200]:
+        seq = np.array([Lb])
+        win = O.stream_window_attn(_bits(q), _bits(K), _bits(V), seq, 4, 252, 0.088)
+        full = O.verify_attn(_bits(q)[:, :, None, :], _bits(K), _bits(V), seq, 0.088)[:, :, 0]
+        np.testing.assert_allclose(win, full, rtol=1e-12, atol=1e-12)
+
+
+def test_verify_row_equals_decode_on_truncated_cache():
+    B, Hq, Hkv, L, D, T = 1, 4, 2, 90, 128, 5
+    Q = _rand_bf16((B, Hq, T, D), 7)
+    K = _rand_bf16((B, Hkv, L, D), 8)
+    V = _rand_bf16((B, Hkv, L, D), 9)
+    out = O.verify_attn(_bits(Q), _bits(K), _bits(V), np.array([L]), 0.088)
+    for j in range(T):
+        Lj = L - T + 1 + j
+        dec = O.verify_attn(_bits(Q)[:, :, j : j + 1], _bits(K), _bits(V), np.array([Lj]), 0.088)[:, :, 0]
+        np.testing.assert_allclose(out[:, :, j], dec, rtol=1e-12, atol=1e-12)
+    # Rows with no visible key (context shorter than the candidate count) are zero.
+    short = O.verify_attn(_bits(Q), _bits(K), _bits(V), np.array([2]), 0.088)
+    assert np.all(short[:, :, :2] == 0) and np.all(np.isfinite(short))
+
+
+def test_positions_beyond_length_are_never_read():
+    B, Hq, Hkv, L, D = 1, 2, 2, 48, 128
+    q = _rand_bf16((B, Hq, D), 10)
+    K = _rand_bf16((B, Hkv, L, D), 11)
+    V = _rand_bf16((B, Hkv, L, D), 12)
+    K[:, :, 37:] = float("nan")
+    V[:, :, 37:] = float("nan")
+    seq = np.array([37])
+    M = O.build_chunk_means(_bits(K), seq, 8)
+    idx, n_sel, *_ = O.chunk_scores_topk(_bits(q), M, seq, L, 8, 6, Hkv)
+    assert np.all(np.isfinite(O.bf16_to_f64(M)[:, :, :5]))
+    assert np.all(np.isfinite(O.sparse_decode_attn(_bits(q), _bits(K), _bits(V), seq, idx, n_sel, 8, 0.1)))
+    assert np.all(np.isfinite(O.stream_window_attn(_bits(q), _bits(K), _bits(V), seq, 4, 16, 0.1)))
+    Q = _rand_bf16((B, Hq, 3, D), 13)
+    assert np.all(np.isfinite(O.verify_attn(_bits(Q), _bits(K), _bits(V), seq, 0.1)))
