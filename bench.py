@@ -1,0 +1,426 @@
+"""Benchmark: draft+verify attention steps/s of the TriForce decode step at 128K.
+
+One step = for every layer, in order: chunk scores + top-k (Force 2 retrieval),
+sparse decode attention over the retrieved chunks (Force 2), sink + window
+attention (Force 1), full-cache verification of gamma+1 = 6 queries (Force 3).
+Workload: the full 32-layer Llama2-7B-128K KV cache (32 heads x 128 dims x
+131072 tokens, bf16, 64 GiB), seeded synthetic data with 1% planted chunks.
+
+Default (impl=triforce): the CUDA library, inputs resident in HBM; prints one
+JSON line with steps/s, the verify kernel's roofline, an end-to-end number
+(queries copied from pinned host memory and outputs copied back inside the
+timed region) and the float64 oracle timed on a bounded sample of host cores.
+impl=reference: the oracle alone, on host cores, one bounded sample per step.
+
+Multi-GPU (torchrun): each rank runs an independent replica of the step on its
+own GPU (the path has no exchange step); value = all ranks' steps / max time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "draft+verify attn steps/s at 128K (Llama2-7B shape); achieved HBM GB/s vs peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="triforce", choices=["triforce", "reference"])
+    ap.add_argument("--workload", default="llama2-7b-128k-32layer")
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling runs only)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+
+
+def dist_setup(n_gpus):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash(name):
+    path = os.path.join(ROOT, "hierarchical_speculative_decoding_gb300", "csrc", name)
+    h = hashlib.sha256()
+    with open(path, "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_file):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash(kernel_file)
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and parts[0] == kernel_file and parts[1] == want:
+                return float(parts[2])
+    return None
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+
+
+def cpu_sample_worker(w_name, n_units, seed):
+    """Time the float64 oracle on n_units (layer, KV head) units of the workload,
+    each a full-length single-head slice.  Runs in a fresh single-threaded process."""
+    import numpy as np
+    import torch
+
+    sys.path.insert(0, ROOT)
+    from hierarchical_speculative_decoding_gb300 import synth
+    from oracle import triforce as O
+
+    w = synth.WORKLOADS[w_name]
+    unit_w = synth.Workload(w.name + "-unit", 1, w.G, 1, w.D, w.L, 1, w.chunk, w.budget, w.n_sink, w.window, w.T,
+                            w.gamma, w.vocab, w.planted_frac, seed)
+    scale = w.D ** -0.5
+    total = 0.0
+    for u in range(n_units):
+        seq = synth.seq_lens_for(unit_w)
+        q, Q = synth.decode_queries(unit_w, u)
+        K, V, _ = synth.kv_cache(unit_w, u, q, seq)
+        kb = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+        qb, Qb, Kb, Vb, sl = kb(q), kb(Q), kb(K), kb(V), seq.numpy()
+        M = O.build_chunk_means(Kb, sl, w.chunk)  # prefill-time index, not part of the step
+        t0 = time.perf_counter()
+        idx, nsel, *_ = O.chunk_scores_topk(qb, M, sl, w.L, w.chunk, w.kc, 1)
+        O.sparse_decode_attn(qb, Kb, Vb, sl, idx, nsel, w.chunk, scale)
+        O.stream_window_attn(qb, Kb, Vb, sl, w.n_sink, w.window, scale)
+        O.verify_attn(Qb, Kb, Vb, sl, scale)
+        total += time.perf_counter() - t0
+    return total / n_units
+
+
+def cpu_baseline(w, n_units=4):
+    """The oracle, as it stands, on a bounded sample of the workload, in a fresh
+    single-threaded process; scaled to one full step (units x layers)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import sys, json; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.cpu_sample_worker(%r, %d, 7)))" % (ROOT, w.name, n_units))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError("cpu baseline failed: " + r.stderr[-2000:])
+    per_unit = float(r.stdout.strip().splitlines()[-1])
+    units_per_step = w.B * w.Hkv * w.layers
+    step_s = per_unit * units_per_step
+    return {"value": 1.0 / step_s, "unit": "steps/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{n_units} (layer, KV head) units at full context {w.L}, float64 numpy oracle, "
+                       f"{per_unit:.3f} s per unit, scaled by {units_per_step} units per step")}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+
+def run_gpu(args):
+    import torch
+
+    sys.path.insert(0, ROOT)
+    from hierarchical_speculative_decoding_gb300 import binding as tf
+    from hierarchical_speculative_decoding_gb300 import synth
+
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    tf.load()
+    w = synth.WORKLOADS[args.workload]
+    layers = args.layers or w.layers
+    B, Hq, Hkv, L, D, T = w.B, w.Hq, w.Hkv, w.L, w.D, w.T
+    Cmax = -(-L // w.chunk)
+    scale = D ** -0.5
+
+    # ---- resident state: KV cache, chunk means, per-layer queries
+    Kc = torch.empty((layers, B, Hkv, L, D), dtype=torch.bfloat16, device=dev)
+    Vc = torch.empty_like(Kc)
+    Mc = torch.empty((layers, B, Hkv, Cmax, D), dtype=torch.bfloat16, device=dev)
+    seq_cpu = synth.seq_lens_for(w)
+    seq = seq_cpu.to(dev)
+    qs, Qs = [], []
+    for l in range(layers):
+        q, Q = synth.decode_queries(w, l, device=dev)
+        synth.kv_cache(w, l, q, seq_cpu, device=dev, K_out=Kc[l], V_out=Vc[l])
+        qs.append(q)
+        Qs.append(Q)
+    q_all = torch.stack(qs)
+    Q_all = torch.stack(Qs)
+    del qs, Qs
+    # chunk-mean index (prefill-time; timed once for its own bandwidth)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for l in range(layers):
+        tf.tf_build_chunk_means(Kc[l], seq, Mc[l])
+    torch.cuda.synchronize()
+    ev0.record()
+    tf.tf_build_chunk_means(Kc[0], seq, Mc[0])
+    ev1.record()
+    torch.cuda.synchronize()
+    means_ms = ev0.elapsed_time(ev1)
+    means_bytes = B * Hkv * L * D * 2 + B * Hkv * Cmax * D * 2
+
+    # ---- outputs and workspaces (zeroed once; every call leaves them reusable)
+    idx = torch.empty((layers, B, Hkv, w.kc), dtype=torch.int32, device=dev)
+    nsel = torch.empty((layers, B, Hkv), dtype=torch.int32, device=dev)
+    o_sp = torch.empty((layers, B, Hq, D), dtype=torch.float32, device=dev)
+    o_win = torch.empty((layers, B, Hq, D), dtype=torch.float32, device=dev)
+    o_ver = torch.empty((layers, B, Hq, T, D), dtype=torch.float32, device=dev)
+    ws_topk = tf.workspace(tf.tf_chunk_scores_topk_workspace(B, Hkv, L), dev)
+    ws_sp = tf.workspace(tf.tf_sparse_decode_attn_workspace(B, Hq, Hkv, w.kc), dev)
+    ws_win = tf.workspace(tf.tf_stream_window_attn_workspace(B, Hq, Hkv, w.n_sink, w.window), dev)
+    ws_ver = tf.workspace(tf.tf_verify_attn_workspace(B, Hq, Hkv, L, T), dev)
+
+    stream = torch.cuda.current_stream()
+    kinds = ("topk", "sparse", "window", "verify")
+
+    def step(evs=None):
+        for l in range(layers):
+            if evs is not None:
+                evs[l][0].record(stream)
+            tf.tf_chunk_scores_topk(q_all[l], Mc[l], seq, L, w.kc, idx[l], nsel[l], ws=ws_topk)
+            if evs is not None:
+                evs[l][1].record(stream)
+            tf.tf_sparse_decode_attn(q_all[l], Kc[l], Vc[l], seq, idx[l], nsel[l], scale, out=o_sp[l], ws=ws_sp)
+            if evs is not None:
+                evs[l][2].record(stream)
+            tf.tf_stream_window_attn(q_all[l], Kc[l], Vc[l], seq, w.n_sink, w.window, scale, out=o_win[l],
+                                     ws=ws_win)
+            if evs is not None:
+                evs[l][3].record(stream)
+            tf.tf_verify_attn(Q_all[l], Kc[l], Vc[l], seq, scale, out=o_ver[l], ws=ws_ver)
+            if evs is not None:
+                evs[l][4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: device-resident inputs (64 GiB of KV >> 129 MB L2)
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(layers)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_start.record(stream)
+        for s in range(args.steps):
+            step(evs[s])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed_s = t_start.elapsed_time(t_end) / 1e3
+    elapsed_s = max_over_ranks(elapsed_s, world)
+    per_kind = {k: [] for k in kinds}
+    for s in range(args.steps):
+        for l in range(layers):
+            for i, k in enumerate(kinds):
+                per_kind[k].append(evs[s][l][i].elapsed_time(evs[s][l][i + 1]))
+
+    # ---- algorithmic bytes per launch (one layer)
+    kv_row = D * 2
+    bytes_topk = B * Hkv * Cmax * D * 2 + B * Hq * D * 2 + B * Hkv * w.kc * 4
+    bytes_sparse = 2 * B * Hkv * w.kc * w.chunk * kv_row + B * Hkv * w.kc * 4 + B * Hq * D * (2 + 4)
+    bytes_window = 2 * B * Hkv * min(L, w.n_sink + w.window) * kv_row + B * Hq * D * (2 + 4)
+    bytes_verify = 2 * B * Hkv * L * kv_row + B * Hq * T * D * (2 + 4)
+    kbytes = {"topk": bytes_topk, "sparse": bytes_sparse, "window": bytes_window, "verify": bytes_verify}
+    peak, peak_kind = measured_peaks()
+    kernels = {}
+    for k in kinds:
+        ms = statistics.mean(per_kind[k])
+        kernels[k] = {"ms": round(ms, 5), "GBps": round(kbytes[k] / (ms / 1e3) / 1e9, 1),
+                      "frac_hbm": round(kbytes[k] / (ms / 1e3) / 1e9 / peak, 4)}
+    draft_ms = statistics.mean(per_kind["topk"]) + statistics.mean(per_kind["sparse"])
+    kernels["retrieval_draft"] = {
+        "ms": round(draft_ms, 5),
+        "GBps": round((bytes_topk + bytes_sparse) / (draft_ms / 1e3) / 1e9, 1),
+        "frac_hbm": round((bytes_topk + bytes_sparse) / (draft_ms / 1e3) / 1e9 / peak, 4)}
+    kernels["chunk_means_prefill_1layer"] = {"ms": round(means_ms, 4),
+                                             "GBps": round(means_bytes / (means_ms / 1e3) / 1e9, 1)}
+    ver_ms = statistics.mean(per_kind["verify"])
+    achieved = bytes_verify / (ver_ms / 1e3) / 1e9
+    traffic = recorded_traffic("verify_attn.cu")
+
+    value = world * args.steps / elapsed_s
+    result = {
+        "metric": METRIC, "value": round(value, 4), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_s / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "head_dim": D, "context": L, "layers": layers,
+                   "chunk": w.chunk, "budget_tokens": w.budget, "window": f"{w.n_sink}+{w.window}",
+                   "verify_tokens": T, "l2": "inputs larger than L2: 2 GiB of K+V per layer, no flush needed"},
+        "roofline": {"bound": "hbm", "kernel": "tf_verify_attn", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": bytes_verify, "peak_source": peak_kind},
+        "kernels": kernels,
+        "gpu_launches": args.steps * layers * 4,
+        "clocks": clocks.summary(),
+    }
+
+    # ---- end to end through the public API with host buffers
+    if not args.no_e2e:
+        q_host = q_all.cpu().pin_memory()
+        Q_host = Q_all.cpu().pin_memory()
+        outs_host = [t.cpu().pin_memory() for t in (o_sp, o_win, o_ver)]
+        h2d = q_host.numel() * 2 + Q_host.numel() * 2
+        d2h = sum(t.numel() * 4 for t in outs_host)
+        e_steps = max(3, args.steps // 2)
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e_steps):
+            q_all.copy_(q_host, non_blocking=True)
+            Q_all.copy_(Q_host, non_blocking=True)
+            step()
+            for h, d in zip(outs_host, (o_sp, o_win, o_ver)):
+                h.copy_(d, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        e_s = max_over_ranks(time.perf_counter() - t0, world)
+        result["e2e"] = {"value": round(world * e_steps / e_s, 4), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                         "d2h_bytes_per_step": d2h}
+
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        del Kc, Vc, Mc
+        torch.cuda.empty_cache()
+        result["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm
+
+
+def run_reference(args):
+    """The float64 oracle on host cores; each step is one (layer, KV head) unit
+    of the workload, scaled to a full step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    sys.path.insert(0, ROOT)
+    from hierarchical_speculative_decoding_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm state; warm-up steps would only repeat the sample
+    cb = cpu_baseline(w, n_units=max(1, args.steps))
+    step_s = 1.0 / cb["value"]
+    out = {"metric": METRIC, "value": cb["value"], "unit": "steps/s", "n_gpus": args.gpus, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+           "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D, "context": w.L,
+                      "layers": w.layers, "chunk": w.chunk, "budget_tokens": w.budget,
+                      "window": f"{w.n_sink}+{w.window}", "verify_tokens": w.T},
+           "cpu_baseline": cb,
+           "e2e": {"value": cb["value"], "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_gpu(a)

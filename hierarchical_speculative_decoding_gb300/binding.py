@@ -1,0 +1,246 @@
+"""Thin ctypes binding over libtriforce_attn.so (argument marshalling only).
+
+Every function has the C entry point's name, checks dtypes/shapes/devices,
+passes raw device pointers plus torch's current CUDA stream, and raises on a
+non-zero status.  All arithmetic happens in the CUDA kernels; there is no CPU
+path.  The library is built in-tree on first use (nvcc, sm_103a) and loading
+fails loudly if it cannot be built or loaded.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+_c = ctypes
+_P = _c.c_void_p
+_I = _c.c_int
+_F = _c.c_float
+_S = _c.c_size_t
+
+_SIGS = {
+    "tf_status_string": (_c.c_char_p, [_I]),
+    "tf_abi_version": (_I, []),
+    "tf_build_chunk_means": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "tf_chunk_scores_topk_workspace": (_S, [_I, _I, _I, _I]),
+    "tf_chunk_scores_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P]),
+    "tf_sparse_decode_attn_workspace": (_S, [_I, _I, _I, _I]),
+    "tf_sparse_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
+    "tf_stream_window_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
+    "tf_stream_window_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
+    "tf_verify_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
+    "tf_verify_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
+    "tf_spec_accept": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_needed: bool = True):
+    """Load (building first if needed) the CUDA library; raises if impossible."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_needed and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"CUDA library missing: {_build.LIB} (run build())")
+    lib = ctypes.CDLL(_build.LIB)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+class TFError(RuntimeError):
+    pass
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = load().tf_status_string(status).decode()
+        raise TFError(f"{what} failed: status {status} ({msg})")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else _c.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return _c.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-filled scratch buffer (the library requires zeroed workspace once)."""
+    return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def _ws(ws, need, device):
+    if need == 0:
+        return ws, 0
+    if ws is None:
+        ws = workspace(need, device)
+    _need(ws, torch.uint8, "ws")
+    return ws, ws.numel()
+
+
+# ------------------------------------------------------------------ calls
+
+
+def tf_build_chunk_means(K, seq_lens, M, chunk=8, c_begin=0, c_end=None, stream=None):
+    _need(K, torch.bfloat16, "K", 4)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(M, torch.bfloat16, "M", 4)
+    B, Hkv, Lmax, D = K.shape
+    Cmax = -(-Lmax // chunk)
+    if tuple(M.shape) != (B, Hkv, Cmax, D):
+        raise ValueError(f"M must be {(B, Hkv, Cmax, D)}")
+    c_end = Cmax if c_end is None else c_end
+    _check(load().tf_build_chunk_means(_ptr(K), _ptr(seq_lens), B, Hkv, Lmax, D, chunk, c_begin, c_end, _ptr(M),
+                                       _stream(stream)), "tf_build_chunk_means")
+    return M
+
+
+def tf_chunk_scores_topk_workspace(B, Hkv, Lmax, chunk=8):
+    return int(load().tf_chunk_scores_topk_workspace(B, Hkv, Lmax, chunk))
+
+
+def tf_chunk_scores_topk(q, M, seq_lens, Lmax, kc, idx=None, n_sel=None, s_cut=None, ws=None, chunk=8,
+                         stream=None):
+    _need(q, torch.bfloat16, "q", 3)
+    _need(M, torch.bfloat16, "M", 4)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, Hq, D = q.shape
+    Hkv = M.shape[1]
+    if idx is None:
+        idx = torch.empty((B, Hkv, kc), dtype=torch.int32, device=q.device)
+    if n_sel is None:
+        n_sel = torch.empty((B, Hkv), dtype=torch.int32, device=q.device)
+    _need(idx, torch.int32, "idx", 3)
+    _need(n_sel, torch.int32, "n_sel", 2)
+    if s_cut is not None:
+        _need(s_cut, torch.float32, "s_cut", 2)
+    ws, nbytes = _ws(ws, tf_chunk_scores_topk_workspace(B, Hkv, Lmax, chunk), q.device)
+    _check(load().tf_chunk_scores_topk(_ptr(q), _ptr(M), _ptr(seq_lens), B, Hq, Hkv, Lmax, D, chunk, kc, _ptr(idx),
+                                       _ptr(n_sel), _ptr(s_cut), _ptr(ws), nbytes, _stream(stream)),
+           "tf_chunk_scores_topk")
+    return idx, n_sel
+
+
+def tf_sparse_decode_attn_workspace(B, Hq, Hkv, kc):
+    return int(load().tf_sparse_decode_attn_workspace(B, Hq, Hkv, kc))
+
+
+def tf_sparse_decode_attn(q, K, V, seq_lens, idx, n_sel, scale, out=None, ws=None, chunk=8, stream=None):
+    _need(q, torch.bfloat16, "q", 3)
+    _need(K, torch.bfloat16, "K", 4)
+    _need(V, torch.bfloat16, "V", 4)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(idx, torch.int32, "idx", 3)
+    _need(n_sel, torch.int32, "n_sel", 2)
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = K.shape
+    kc = idx.shape[2]
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, "out", 3)
+    ws, nbytes = _ws(ws, tf_sparse_decode_attn_workspace(B, Hq, Hkv, kc), q.device)
+    _check(load().tf_sparse_decode_attn(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(idx), _ptr(n_sel), B, Hq,
+                                        Hkv, Lmax, D, chunk, kc, float(scale), _ptr(out), _ptr(ws), nbytes,
+                                        _stream(stream)), "tf_sparse_decode_attn")
+    return out
+
+
+def tf_stream_window_attn_workspace(B, Hq, Hkv, n_sink, window):
+    return int(load().tf_stream_window_attn_workspace(B, Hq, Hkv, n_sink, window))
+
+
+def tf_stream_window_attn(q, K, V, seq_lens, n_sink, window, scale, out=None, ws=None, stream=None):
+    _need(q, torch.bfloat16, "q", 3)
+    _need(K, torch.bfloat16, "K", 4)
+    _need(V, torch.bfloat16, "V", 4)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = K.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, "out", 3)
+    ws, nbytes = _ws(ws, tf_stream_window_attn_workspace(B, Hq, Hkv, n_sink, window), q.device)
+    _check(load().tf_stream_window_attn(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax, D, n_sink,
+                                        window, float(scale), _ptr(out), _ptr(ws), nbytes, _stream(stream)),
+           "tf_stream_window_attn")
+    return out
+
+
+def tf_verify_attn_workspace(B, Hq, Hkv, Lmax, T):
+    return int(load().tf_verify_attn_workspace(B, Hq, Hkv, Lmax, T))
+
+
+def tf_verify_attn(Q, K, V, seq_lens, scale, out=None, ws=None, stream=None):
+    _need(Q, torch.bfloat16, "Q", 4)
+    _need(K, torch.bfloat16, "K", 4)
+    _need(V, torch.bfloat16, "V", 4)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, Hq, T, D = Q.shape
+    _, Hkv, Lmax, _ = K.shape
+    if out is None:
+        out = torch.empty((B, Hq, T, D), dtype=torch.float32, device=Q.device)
+    _need(out, torch.float32, "out", 4)
+    ws, nbytes = _ws(ws, tf_verify_attn_workspace(B, Hq, Hkv, Lmax, T), Q.device)
+    _check(load().tf_verify_attn(_ptr(Q), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax, D, T, float(scale),
+                                 _ptr(out), _ptr(ws), nbytes, _stream(stream)), "tf_verify_attn")
+    return out
+
+
+def tf_spec_accept(tgt_logits, drf_logits, drf_tokens, u_acc, u_res, temperature=1.0, n_acc=None, next_token=None,
+                   out_tokens=None, stream=None):
+    _need(tgt_logits, torch.float32, "tgt_logits", 3)
+    B, g1, Vn = tgt_logits.shape
+    gamma = g1 - 1
+    _need(u_res, torch.float32, "u_res", 1)
+    if gamma > 0:
+        _need(drf_logits, torch.float32, "drf_logits", 3)
+        _need(drf_tokens, torch.int32, "drf_tokens", 2)
+        _need(u_acc, torch.float32, "u_acc", 2)
+        if tuple(drf_logits.shape) != (B, gamma, Vn) or tuple(drf_tokens.shape) != (B, gamma):
+            raise ValueError("draft shapes must be [B, gamma, V] and [B, gamma]")
+    dev = tgt_logits.device
+    if n_acc is None:
+        n_acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    _check(load().tf_spec_accept(_ptr(tgt_logits), _ptr(drf_logits if gamma > 0 else None),
+                                 _ptr(drf_tokens if gamma > 0 else None), _ptr(u_acc if gamma > 0 else None),
+                                 _ptr(u_res), B, gamma, Vn, float(temperature), _ptr(n_acc), _ptr(next_token),
+                                 _ptr(out_tokens), _stream(stream)), "tf_spec_accept")
+    return n_acc, next_token, out_tokens

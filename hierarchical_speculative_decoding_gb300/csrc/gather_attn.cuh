@@ -1,0 +1,36 @@
+// Decode attention over a gathered position set (sparse chunks, sink+window,
+// or a causal prefix); shared by the sparse, window and verify entry points.
+#pragma once
+
+#include "tf_common.cuh"
+
+namespace tf {
+
+constexpr int kGatherThreads = 256;
+constexpr int kModeChunks = 0;  // positions of the selected chunks (Force 2)
+constexpr int kModeWindow = 1;  // attention sinks + recent window (Force 1)
+constexpr int kModePrefix = 2;  // positions [0, L - T + j] for query j (Force 3)
+
+struct GatherParams {
+  const uint16_t* q;  // [B, Hq, T, D]
+  const uint16_t* K;  // [B, Hkv, Lmax, D]
+  const uint16_t* V;
+  const int32_t* seq_lens;
+  const int32_t* idx;    // [B, Hkv, kc] (chunks mode)
+  const int32_t* n_sel;  // [B, Hkv]     (chunks mode)
+  int Hq, Hkv, Lmax, T, kc, n_sink, window;
+  float scale_log2;  // softmax scale * log2(e)
+  int ngroups;       // query-row groups per unit
+  int splits;        // CTAs per (unit, group)
+  int splits_cap;    // partial-buffer stride
+  float* out;        // [B, Hq, T, D]
+  int* tickets;      // [units * ngroups]
+  float* part_ml;    // [units * ngroups, splits_cap, NQ, 2]
+  float* part_o;     // [units * ngroups, splits_cap, NQ, D]
+};
+
+size_t gather_workspace(int units, int rows, int P_max);
+tf_status gather_launch(int mode, GatherParams p, int units, int rows, int P_max, void* ws, size_t ws_bytes,
+                        cudaStream_t stream);
+
+}  // namespace tf

@@ -1,0 +1,186 @@
+/*
+ * triforce_attn.h -- C ABI of the TriForce decode-step attention library (sm_103a).
+ *
+ * The calls below are the data-parallel work of one hierarchical speculative
+ * decoding step as described in "TriForce: Hierarchical Speculative Decoding
+ * for LLMs" (section "The Architecture" / "The Three Forces of TriForce" and
+ * section "Dual Rejection Sampling: Mathematical Losslessness") and in the
+ * arXiv abstract of "TriForce: Lossless Acceleration of Long Sequence
+ * Generation with Hierarchical Speculative Decoding":
+ *   Force 1  the streaming drafter attends to attention sinks + a recent window;
+ *   Force 2  the target model attends to the top-k KV blocks retrieved by
+ *            key-query similarity (retrieval-sparse cache);
+ *   Force 3  the target model verifies all candidates against the full cache;
+ *   then each level accepts or resamples the drafted tokens losslessly.
+ *
+ * Conventions shared by every call
+ *   - Tensor arguments are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or keeps them; it keeps no global state.
+ *   - bf16 tensors are passed as uint16_t bit patterns (IEEE fp32 top half).
+ *   - Layouts are dense row-major:  K, V  [B, Hkv, Lmax, D];
+ *     chunk means M [B, Hkv, Cmax, D] with Cmax = ceil(Lmax / chunk);
+ *     decode query q [B, Hq, D]; verify queries Q [B, Hq, T, D].
+ *     Query head h reads KV head h / (Hq / Hkv) (grouped-query attention).
+ *   - D must be 128 and chunk must be 8 (TF_ERR_UNSUPPORTED otherwise).
+ *     Tensor pointers must be 16-byte aligned (TF_ERR_INVALID_ARG otherwise).
+ *   - seq_lens [B] int32 on the device holds each sequence's valid length L_b;
+ *     values are clamped to [0, Lmax].  Positions >= L_b are never read into a
+ *     result (they may hold anything, including NaN).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  On error nothing is launched, except TF_ERR_CUDA,
+ *     which reports a failed launch.
+ *   - Workspace: calls that take `ws` need scratch of at least the size the
+ *     matching *_workspace() query returns.  The buffer must be zero-filled
+ *     once after allocation (cudaMemset); every call leaves its counters at
+ *     zero again, so one buffer serves any sequence of calls that are ordered
+ *     on the GPU.  Calls that may run concurrently need separate workspaces.
+ */
+#ifndef TRIFORCE_ATTN_H
+#define TRIFORCE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TF_API __attribute__((visibility("default")))
+#else
+#define TF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* tf_stream_t; /* same type as cudaStream_t */
+
+typedef enum tf_status {
+  TF_OK = 0,
+  TF_ERR_INVALID_ARG = 1,  /* null/misaligned pointer or inconsistent sizes; nothing launched */
+  TF_ERR_UNSUPPORTED = 2,  /* valid but unsupported shape (D != 128, chunk != 8, ...) */
+  TF_ERR_WORKSPACE = 3,    /* ws missing or ws_bytes below the *_workspace() size */
+  TF_ERR_CUDA = 4          /* a kernel launch failed (cudaGetLastError) */
+} tf_status;
+
+/* Static, human-readable text for a status code. */
+TF_API const char* tf_status_string(tf_status s);
+
+/* Library ABI version (major * 100 + minor). */
+TF_API int tf_abi_version(void);
+
+/*
+ * a1 -- chunk-mean retrieval index.
+ * The retrieval-sparse cache of Force 2 selects KV blocks by key-query
+ * similarity and keeps an on-demand sparse index ("The Three Forces of
+ * TriForce"; "Production Advantages").  A block is `chunk` consecutive tokens,
+ * represented by the mean of its keys:
+ *   M[b,g,c,:] = bf16_round_nearest_even( (1/n_c) * sum_{t in chunk c, t < L_b} K[b,g,t,:] )
+ * with n_c the number of valid tokens of chunk c (8, fewer for the last partial
+ * chunk).  Chunks with no valid token are written as zeros.  Only chunks
+ * c_begin <= c < c_end are written (0 <= c_begin <= c_end <= Cmax), so a
+ * decode step can refresh just the chunk that changed.
+ * The mean is rounded once: the sum is carried as an unevaluated pair of fp32
+ * values, exact for any eight bf16 values whose magnitudes span < 2^40.
+ */
+TF_API tf_status tf_build_chunk_means(const uint16_t* K, const int32_t* seq_lens,
+                               int B, int Hkv, int Lmax, int D, int chunk,
+                               int c_begin, int c_end,
+                               uint16_t* M, tf_stream_t stream);
+
+/*
+ * a2 + a3 -- chunk scores and top-k selection (Force 2 retrieval).
+ * Score of chunk c for (b, g): s = sum_d (sum_{h in group g} q[b,h,d]) * M[b,g,c,d],
+ * accumulated in fp32 (no softmax scale: it does not change the order).
+ * Selection keeps the kc highest-scoring chunks among C_b = ceil(L_b / chunk);
+ * equal scores go to the lower chunk id; output ids are ascending.
+ *   idx   [B, Hkv, kc] int32   selected chunk ids, slots >= n_sel hold -1
+ *   n_sel [B, Hkv]     int32   min(kc, C_b)
+ *   s_cut [B, Hkv]     float   smallest selected score (nullable; -inf if none)
+ * Scores must be finite (NaN scores rank above every number).
+ * Workspace: tf_chunk_scores_topk_workspace(B, Hkv, Lmax, chunk) bytes.
+ */
+TF_API size_t tf_chunk_scores_topk_workspace(int B, int Hkv, int Lmax, int chunk);
+TF_API tf_status tf_chunk_scores_topk(const uint16_t* q, const uint16_t* M, const int32_t* seq_lens,
+                               int B, int Hq, int Hkv, int Lmax, int D, int chunk, int kc,
+                               int32_t* idx, int32_t* n_sel, float* s_cut,
+                               void* ws, size_t ws_bytes, tf_stream_t stream);
+
+/*
+ * a4 (+ a5) -- retrieval-sparse decode attention (Force 2).
+ * For query head h of group g:  out[b,h,:] = softmax(scale * q_h . K_S) V_S
+ * where S is the valid tokens (t < L_b) of the chunks idx[b,g,0:n_sel[b,g]].
+ * Ids outside [0, C_b) are skipped; a repeated id is attended once per
+ * occurrence.  An empty set gives a zero output row.  fp32 accumulation,
+ * split over the selected chunks and merged with the log-sum-exp identity.
+ *   out [B, Hq, D] float32
+ * Workspace: tf_sparse_decode_attn_workspace(B, Hq, Hkv, kc) bytes.
+ */
+TF_API size_t tf_sparse_decode_attn_workspace(int B, int Hq, int Hkv, int kc);
+TF_API tf_status tf_sparse_decode_attn(const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                                const int32_t* seq_lens, const int32_t* idx, const int32_t* n_sel,
+                                int B, int Hq, int Hkv, int Lmax, int D, int chunk, int kc,
+                                float scale, float* out,
+                                void* ws, size_t ws_bytes, tf_stream_t stream);
+
+/*
+ * a6 (+ a5) -- StreamingLLM sink + window attention (Force 1 drafter).
+ * Positions P = [0, min(n_sink, L)) U [max(n_sink, L - window), L): the first
+ * n_sink tokens plus the most recent `window` tokens, de-duplicated.
+ *   out [B, Hq, D] float32 = softmax(scale * q_h . K_P) V_P
+ * Workspace: tf_stream_window_attn_workspace(B, Hq, Hkv, n_sink, window) bytes.
+ */
+TF_API size_t tf_stream_window_attn_workspace(int B, int Hq, int Hkv, int n_sink, int window);
+TF_API tf_status tf_stream_window_attn(const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                                const int32_t* seq_lens,
+                                int B, int Hq, int Hkv, int Lmax, int D, int n_sink, int window,
+                                float scale, float* out,
+                                void* ws, size_t ws_bytes, tf_stream_t stream);
+
+/*
+ * a7 (+ a5) -- full-cache verification attention (Force 3).
+ * The cache already holds the T candidates' keys/values at positions
+ * L-T .. L-1 and the candidates form a chain, so verify query j (0 <= j < T)
+ * attends to positions [0, L - T + j]:
+ *   out[b,h,j,:] = softmax(scale * Q[b,h,j] . K_{0..L-T+j}) V_{0..L-T+j}
+ * Rows with no visible position (L - T + j < 0) are zero.  1 <= T <= 16.
+ *   out [B, Hq, T, D] float32
+ * Workspace: tf_verify_attn_workspace(B, Hq, Hkv, Lmax, T) bytes.
+ */
+TF_API size_t tf_verify_attn_workspace(int B, int Hq, int Hkv, int Lmax, int T);
+TF_API tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                         const int32_t* seq_lens,
+                         int B, int Hq, int Hkv, int Lmax, int D, int T,
+                         float scale, float* out,
+                         void* ws, size_t ws_bytes, tf_stream_t stream);
+
+/*
+ * a8 -- lossless speculative accept / resample of one verification level
+ * ("Dual Rejection Sampling: Mathematical Losslessness").
+ * With p_i = softmax(tgt_logits[b,i,:] / temperature) (the verifier) and
+ * q_i = softmax(drf_logits[b,i,:] / temperature) (the drafter), drafted token
+ * x_i is accepted when u_acc[b,i] <= p_i(x_i) / q_i(x_i) (always when
+ * q_i(x_i) == 0).  At the first rejection j the next token is drawn from
+ * max(0, p_j - q_j) normalised (from p_j if that residual is all zero); if
+ * all g drafted tokens are accepted, a bonus token is drawn from p_g.  Draws
+ * use the index-order inverse CDF with u_res[b]: the first t whose cumulative
+ * weight exceeds u_res * total.
+ * The same call serves both levels of the hierarchy: tiny drafter -> retrieval
+ * drafter, then retrieval drafter -> target (pass the first level's
+ * out_tokens as the second level's drf_tokens).
+ *   tgt_logits [B, gamma+1, V] f32, drf_logits [B, gamma, V] f32
+ *   drf_tokens [B, gamma] int32; an entry outside [0, V) ends the draft
+ *   u_acc [B, gamma] f32, u_res [B] f32, uniforms in [0, 1)
+ *   n_acc [B] int32 (accepted count), next_token [B] int32
+ *   out_tokens [B, gamma+1] int32 (nullable): accepted drafts, next token, -1 pad
+ * temperature > 0.  gamma >= 0, V >= 1.  No workspace.
+ */
+TF_API tf_status tf_spec_accept(const float* tgt_logits, const float* drf_logits, const int32_t* drf_tokens,
+                         const float* u_acc, const float* u_res,
+                         int B, int gamma, int V, float temperature,
+                         int32_t* n_acc, int32_t* next_token, int32_t* out_tokens,
+                         tf_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRIFORCE_ATTN_H */

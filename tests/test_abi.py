@@ -1,0 +1,90 @@
+"""The C-ABI library builds, loads and exports every declared symbol (no GPU).
+
+Only calls that return before touching the GPU are made here: status strings,
+the ABI version, workspace-size queries and host-side argument validation.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from hierarchical_speculative_decoding_gb300 import binding, build
+
+HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+
+
+def declared_symbols():
+    names = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if fn.endswith(".h"):
+            with open(os.path.join(HEADER_DIR, fn)) as f:
+                names += re.findall(r"^TF_API\s+[\w\s\*]+?\b(tf_\w+)\s*\(", f.read(), flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load(build_if_needed=False)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(binding.exported_symbols())
+
+
+def test_version_and_status_strings(lib):
+    assert lib.tf_abi_version() == 100
+    for s in range(5):
+        assert len(lib.tf_status_string(s)) > 0
+    assert lib.tf_status_string(99) == b"unknown status"
+
+
+def test_workspace_sizes(lib):
+    units, cmax = 32, 16384
+    assert lib.tf_chunk_scores_topk_workspace(1, 32, 131072, 8) >= units * cmax * 4
+    assert lib.tf_chunk_scores_topk_workspace(1, 32, 131072, 7) == 0  # unsupported chunk
+    assert lib.tf_sparse_decode_attn_workspace(1, 32, 32, 512) > 0
+    assert lib.tf_sparse_decode_attn_workspace(1, 32, 5, 512) == 0  # Hq % Hkv != 0
+    assert lib.tf_stream_window_attn_workspace(4, 32, 8, 4, 252) > 0
+    assert lib.tf_verify_attn_workspace(4, 32, 8, 131072, 6) > 0
+    # workspace grows with the problem
+    assert lib.tf_verify_attn_workspace(8, 32, 8, 131072, 6) > lib.tf_verify_attn_workspace(1, 32, 8, 131072, 6)
+
+
+def test_host_validation_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced: every call below fails validation first
+    odd = P(0x10008)  # not 16-byte aligned
+    null = None
+    INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 3
+    assert lib.tf_build_chunk_means(null, fake, 1, 1, 64, 128, 8, 0, 8, fake, None) == INVALID
+    assert lib.tf_build_chunk_means(odd, fake, 1, 1, 64, 128, 8, 0, 8, fake, None) == INVALID
+    assert lib.tf_build_chunk_means(fake, fake, 1, 1, 64, 64, 8, 0, 8, fake, None) == UNSUPPORTED
+    assert lib.tf_build_chunk_means(fake, fake, 1, 1, 64, 128, 8, 0, 9, fake, None) == INVALID
+    assert lib.tf_chunk_scores_topk(fake, fake, fake, 1, 6, 4, 64, 128, 8, 4, fake, fake, null, null, 0,
+                                    None) == INVALID  # Hq % Hkv
+    assert lib.tf_chunk_scores_topk(fake, fake, fake, 1, 8, 4, 64, 128, 8, 4, fake, fake, null, null, 0,
+                                    None) == WORKSPACE
+    assert lib.tf_sparse_decode_attn(fake, fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 16, 4, 0.1, fake, null,
+                                     0, None) == UNSUPPORTED
+    assert lib.tf_stream_window_attn(fake, fake, fake, fake, 1, 8, 2, 64, 128, -1, 4, 0.1, fake, null, 0,
+                                     None) == INVALID
+    assert lib.tf_verify_attn(fake, fake, fake, fake, 1, 8, 2, 64, 128, 0, 0.1, fake, null, 0, None) == INVALID
+    assert lib.tf_verify_attn(fake, fake, fake, fake, 1, 8, 2, 64, 128, 17, 0.1, fake, null, 0, None) == UNSUPPORTED
+    assert lib.tf_spec_accept(fake, fake, fake, fake, fake, 1, 4, 100, 0.0, fake, fake, null, None) == INVALID
+    assert lib.tf_spec_accept(fake, null, fake, fake, fake, 1, 4, 100, 1.0, fake, fake, null, None) == INVALID
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+
+    K = torch.zeros((1, 1, 8, 128), dtype=torch.bfloat16)
+    with pytest.raises(TypeError, match="CUDA"):
+        binding.tf_build_chunk_means(K, torch.zeros(1, dtype=torch.int32), torch.zeros((1, 1, 1, 128),
+                                                                                      dtype=torch.bfloat16))

@@ -1,0 +1,304 @@
+"""GPU parity of every library call against the float64 oracle.
+
+Inputs come from the seeded generators (never from the CUDA path); both sides
+read the same bf16 bits.  Tolerances:
+  * chunk means: bit-exact (the definition rounds once; the kernel sums exactly);
+  * top-k ids: identical except where the oracle's score gap at the cut is
+    below 1e-4 (counted, and every swapped chunk must sit within 1e-4 of the cut);
+  * attention outputs: max abs error <= 2e-3 (bf16 inputs, fp32 accumulation);
+  * accept/resample: n_acc / next / out_tokens bit-exact except sequences whose
+    uniforms fall within 1e-6 of a decision boundary (counted).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from hierarchical_speculative_decoding_gb300 import synth
+from oracle import triforce as O
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 2e-3
+GAP = 1e-4
+EDGE = 1e-6
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def scale_for(D):
+    return D ** -0.5
+
+
+def make_case(w, layer=0, fill_invalid=None, device="cuda"):
+    seq = synth.seq_lens_for(w)
+    q, Q = synth.decode_queries(w, layer)
+    K, V, planted = synth.kv_cache(w, layer, q, seq, fill_invalid=fill_invalid)
+    return dict(seq_cpu=seq, q_cpu=q, Q_cpu=Q, K_cpu=K, V_cpu=V, planted=planted,
+                seq=seq.to(device), q=q.to(device), Q=Q.to(device), K=K.to(device), V=V.to(device))
+
+
+def small_workload(**kw):
+    base = dict(name="small", B=2, Hq=8, Hkv=2, D=128, L=1000, layers=1, chunk=8, budget=256, n_sink=4,
+                window=60, T=6, gamma=4, vocab=1000, planted_frac=0.02, seed=21, ragged=True, L_min=200)
+    base.update(kw)
+    return synth.Workload(**base)
+
+
+def check_topk(idx_g, nsel_g, idx_o, nsel_o, gap_o, scores_o):
+    """Top-k parity: identical sets except at near-ties of the cut."""
+    near_ties = 0
+    B, Hkv, _ = idx_o.shape
+    for b in range(B):
+        for g in range(Hkv):
+            assert nsel_g[b, g] == nsel_o[b, g]
+            n = nsel_o[b, g]
+            a = idx_g[b, g, :n]
+            assert np.all(np.diff(a) > 0), "ids must be ascending and distinct"
+            assert np.all(idx_g[b, g, n:] == -1)
+            o = idx_o[b, g, :n]
+            if np.array_equal(a, o):
+                continue
+            assert gap_o[b, g] < GAP, f"top-k mismatch at (b={b}, g={g}) with oracle gap {gap_o[b, g]}"
+            s = scores_o[b][g]
+            cut = min(s[o])
+            for c in set(a.tolist()) ^ set(o.tolist()):
+                assert abs(s[c] - cut) < GAP
+            near_ties += 1
+    return near_ties
+
+
+# ------------------------------------------------------------------ a1
+
+
+@pytest.mark.parametrize("w", [synth.TINY, small_workload()], ids=["tiny", "ragged-gqa"])
+def test_chunk_means_bit_exact(cuda_lib, w):
+    c = make_case(w, fill_invalid=float("nan"))
+    Cmax = -(-w.L // w.chunk)
+    M = torch.full((w.B, w.Hkv, Cmax, w.D), 7.0, dtype=torch.bfloat16, device="cuda")
+    cuda_lib.tf_build_chunk_means(c["K"], c["seq"], M)
+    want = O.build_chunk_means(bits(c["K_cpu"]), c["seq_cpu"].numpy(), w.chunk)
+    got = bits(M)
+    assert np.array_equal(got, want), f"{(got != want).sum()} mismatching means"
+
+
+def test_chunk_means_subrange_only(cuda_lib):
+    w = small_workload(ragged=False, B=1)
+    c = make_case(w)
+    Cmax = -(-w.L // w.chunk)
+    M = torch.full((w.B, w.Hkv, Cmax, w.D), 7.0, dtype=torch.bfloat16, device="cuda")
+    cuda_lib.tf_build_chunk_means(c["K"], c["seq"], M, c_begin=10, c_end=37)
+    got = bits(M)
+    want = O.build_chunk_means(bits(c["K_cpu"]), c["seq_cpu"].numpy(), w.chunk, 10, 37)
+    assert np.array_equal(got[:, :, 10:37], want[:, :, 10:37])
+    seven = bits(torch.tensor([7.0], dtype=torch.bfloat16))[0]
+    assert np.all(got[:, :, :10] == seven) and np.all(got[:, :, 37:] == seven)
+
+
+# ------------------------------------------------------------------ a2 + a3
+
+
+def run_topk(cuda_lib, w, c, M_bits, kc=None):
+    kc = kc or w.kc
+    M = torch.from_numpy(M_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    s_cut = torch.empty((w.B, w.Hkv), dtype=torch.float32, device="cuda")
+    idx, n_sel = cuda_lib.tf_chunk_scores_topk(c["q"], M, c["seq"], w.L, kc, s_cut=s_cut)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), n_sel.cpu().numpy(), s_cut.cpu().numpy()
+
+
+@pytest.mark.parametrize("w", [synth.TINY, small_workload(), small_workload(budget=8 * 2000)],
+                         ids=["tiny", "ragged-gqa", "budget-covers-all"])
+def test_scores_topk(cuda_lib, w):
+    c = make_case(w)
+    M_bits = O.build_chunk_means(bits(c["K_cpu"]), c["seq_cpu"].numpy(), w.chunk)
+    idx, nsel, s_cut = run_topk(cuda_lib, w, c, M_bits)
+    idx_o, nsel_o, cut_o, gap_o, scores_o = O.chunk_scores_topk(
+        bits(c["q_cpu"]), M_bits, c["seq_cpu"].numpy(), w.L, w.chunk, w.kc, w.Hkv)
+    check_topk(idx, nsel, idx_o, nsel_o, gap_o, scores_o)
+    np.testing.assert_allclose(s_cut, cut_o, rtol=1e-5, atol=1e-4)
+    # planted relevant chunks are all retrieved
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            assert set(c["planted"][b][g].tolist()) <= set(idx[b, g, : nsel[b, g]].tolist())
+
+
+def test_topk_ties_go_to_lower_ids(cuda_lib):
+    w = small_workload(B=1, ragged=False, L=8 * 3000)
+    c = make_case(w)
+    Cmax = w.L // 8
+    M_bits = np.zeros((1, w.Hkv, Cmax, 128), dtype=np.uint16)  # every score is exactly 0
+    qsum = c["q_cpu"].double().reshape(w.Hkv, w.G, 128).sum(1)[1]
+    winner = torch.where(qsum >= 0, 1.0, -1.0).to(torch.bfloat16)  # a strictly positive score
+    M_bits[0, 1, 2999] = bits(winner)
+    idx, nsel, _ = run_topk(cuda_lib, w, c, M_bits, kc=100)
+    assert idx[0, 0].tolist() == list(range(100))
+    assert idx[0, 1].tolist() == list(range(99)) + [2999]
+
+
+def test_topk_empty_and_tiny_contexts(cuda_lib):
+    w = small_workload(B=3, ragged=False, L=64)
+    c = make_case(w)
+    c["seq"] = torch.tensor([0, 1, 64], dtype=torch.int32, device="cuda")
+    seq = np.array([0, 1, 64])
+    M_bits = O.build_chunk_means(bits(c["K_cpu"]), seq, 8)
+    idx, nsel, _ = run_topk(cuda_lib, w, c, M_bits, kc=4)
+    idx_o, nsel_o, _, gap_o, scores_o = O.chunk_scores_topk(bits(c["q_cpu"]), M_bits, seq, 64, 8, 4, w.Hkv)
+    check_topk(idx, nsel, idx_o, nsel_o, gap_o, scores_o)
+    assert nsel[0].tolist() == [0, 0] and nsel[1].tolist() == [1, 1]
+
+
+# ------------------------------------------------------------------ a4
+
+
+def oracle_idx(w, c):
+    M_bits = O.build_chunk_means(bits(c["K_cpu"]), c["seq_cpu"].numpy(), w.chunk)
+    idx_o, nsel_o, *_ = O.chunk_scores_topk(bits(c["q_cpu"]), M_bits, c["seq_cpu"].numpy(), w.L, w.chunk, w.kc,
+                                            w.Hkv)
+    return idx_o, nsel_o
+
+
+@pytest.mark.parametrize("w", [synth.TINY, small_workload()], ids=["tiny", "ragged-gqa"])
+def test_sparse_decode_attn(cuda_lib, w):
+    c = make_case(w, fill_invalid=float("nan"))
+    idx_o, nsel_o = oracle_idx(w, c)
+    idx = torch.from_numpy(idx_o.astype(np.int32)).cuda()
+    nsel = torch.from_numpy(nsel_o.astype(np.int32)).cuda()
+    out = cuda_lib.tf_sparse_decode_attn(c["q"], c["K"], c["V"], c["seq"], idx, nsel, scale_for(w.D))
+    want = O.sparse_decode_attn(bits(c["q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), c["seq_cpu"].numpy(), idx_o,
+                                nsel_o, w.chunk, scale_for(w.D))
+    err = np.abs(out.cpu().double().numpy() - want).max()
+    assert err <= ATOL, err
+
+
+def test_sparse_edge_cases(cuda_lib):
+    w = small_workload(B=2, ragged=False, L=200, budget=64)
+    c = make_case(w)
+    kc = w.kc
+    idx_o = np.full((2, w.Hkv, kc), -1, dtype=np.int64)
+    nsel_o = np.zeros((2, w.Hkv), dtype=np.int64)
+    idx_o[0, 0, :3] = [24, 0, 5]  # L=200: chunks 0..24; any order is accepted
+    nsel_o[0, 0] = 3
+    idx_o[0, 1, :4] = [1, 999, -5, 2]  # invalid ids are skipped
+    nsel_o[0, 1] = 4
+    idx_o[1, 0, :kc] = np.arange(kc)  # full list
+    nsel_o[1, 0] = kc
+    nsel_o[1, 1] = 0  # empty set -> zeros
+    out = cuda_lib.tf_sparse_decode_attn(c["q"], c["K"], c["V"], c["seq"],
+                                         torch.from_numpy(idx_o.astype(np.int32)).cuda(),
+                                         torch.from_numpy(nsel_o.astype(np.int32)).cuda(), 0.05)
+    want = O.sparse_decode_attn(bits(c["q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), c["seq_cpu"].numpy(), idx_o,
+                                nsel_o, 8, 0.05)
+    assert np.abs(out.cpu().double().numpy() - want).max() <= ATOL
+
+
+# ------------------------------------------------------------------ a6
+
+
+@pytest.mark.parametrize("w", [synth.TINY, small_workload(), small_workload(L=150, L_min=1)],
+                         ids=["tiny", "ragged-gqa", "short-contexts"])
+def test_stream_window_attn(cuda_lib, w):
+    c = make_case(w, fill_invalid=float("nan"))
+    out = cuda_lib.tf_stream_window_attn(c["q"], c["K"], c["V"], c["seq"], w.n_sink, w.window, scale_for(w.D))
+    want = O.stream_window_attn(bits(c["q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), c["seq_cpu"].numpy(),
+                                w.n_sink, w.window, scale_for(w.D))
+    assert np.abs(out.cpu().double().numpy() - want).max() <= ATOL
+
+
+# ------------------------------------------------------------------ a7
+
+
+@pytest.mark.parametrize("w", [synth.TINY, small_workload(), small_workload(Hkv=8, T=6, L=3000, L_min=2000),
+                               synth.LLAMA2_7B_32K_1LAYER],
+                         ids=["tiny", "ragged-gqa", "mha-6", "llama2-7b-32k-1layer"])
+def test_verify_attn(cuda_lib, w):
+    c = make_case(w, fill_invalid=float("nan") if w.ragged else None)
+    out = cuda_lib.tf_verify_attn(c["Q"], c["K"], c["V"], c["seq"], scale_for(w.D))
+    want = O.verify_attn(bits(c["Q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), c["seq_cpu"].numpy(), scale_for(w.D))
+    assert np.abs(out.cpu().double().numpy() - want).max() <= ATOL
+
+
+def test_verify_context_shorter_than_candidates(cuda_lib):
+    w = small_workload(B=2, ragged=False, L=16, T=6)
+    c = make_case(w)
+    c["seq"] = torch.tensor([3, 0], dtype=torch.int32, device="cuda")
+    out = cuda_lib.tf_verify_attn(c["Q"], c["K"], c["V"], c["seq"], 0.1)
+    want = O.verify_attn(bits(c["Q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), np.array([3, 0]), 0.1)
+    got = out.cpu().double().numpy()
+    assert np.all(got[1] == 0) and np.all(got[0, :, :3] == 0)
+    assert np.abs(got - want).max() <= ATOL
+
+
+# ------------------------------------------------------------------ a8
+
+
+def run_accept(cuda_lib, tgt, drf, x, ua, ur, temperature=1.0):
+    n_acc, nxt, out = cuda_lib.tf_spec_accept(tgt.cuda(), drf.cuda(), x.cuda(), ua.cuda(), ur.cuda(), temperature)
+    torch.cuda.synchronize()
+    return n_acc.cpu().numpy(), nxt.cpu().numpy(), out.cpu().numpy()
+
+
+def compare_accept(got, want):
+    n_acc, nxt, out = got
+    same = (n_acc == want["n_acc"]) & (nxt == want["next"]) & np.all(out == want["out_tokens"], axis=1)
+    bad = ~same
+    assert np.all(want["margin"][bad] < EDGE), f"{bad.sum()} mismatches not explained by boundary draws"
+    return int(bad.sum())
+
+
+@pytest.mark.parametrize("B,gamma,V,temp", [(1, 4, 32000, 1.0), (64, 4, 32000, 1.0), (256, 5, 1000, 0.7),
+                                            (512, 3, 7, 1.3)])
+def test_spec_accept_parity(cuda_lib, B, gamma, V, temp):
+    tgt, drf, x, ua, ur = synth.accept_inputs(B, gamma, V, seed=B + V)
+    got = run_accept(cuda_lib, tgt, drf, x, ua, ur, temp)
+    want = O.spec_accept(tgt.double().numpy(), drf.double().numpy(), x.numpy(), ua.double().numpy(),
+                         ur.double().numpy(), temp)
+    compare_accept(got, want)
+
+
+def test_spec_accept_short_and_empty_drafts(cuda_lib):
+    tgt, drf, x, ua, ur = synth.accept_inputs(32, 4, 500, seed=77)
+    x[0:8, 2] = -1  # drafts of length 2
+    x[8:16, 0] = -1  # empty drafts
+    x[16:24, 3] = 500  # out-of-range token ends the draft
+    got = run_accept(cuda_lib, tgt, drf, x, ua, ur)
+    want = O.spec_accept(tgt.double().numpy(), drf.double().numpy(), x.numpy(), ua.double().numpy(),
+                         ur.double().numpy())
+    compare_accept(got, want)
+
+
+def test_spec_accept_identical_distributions(cuda_lib):
+    tgt, drf, x, ua, ur = synth.accept_inputs(128, 4, 300, seed=5)
+    drf = tgt[:, :4].clone()
+    got = run_accept(cuda_lib, tgt, drf, x, ua, ur)
+    assert np.all(got[0] == 4)
+
+
+def _chi2_ok(tokens, p):
+    from scipy import stats
+    counts = np.bincount(tokens, minlength=len(p))
+    return stats.chisquare(counts, p * counts.sum()).pvalue > 1e-3
+
+
+def test_spec_accept_lossless_chi_square_gpu(cuda_lib):
+    """10^6 independent sequences in one call: the first emitted token follows p0,
+    for one level and for the two-level r -> q -> p composition."""
+    N, V, g1 = 1_000_000, 16, 4
+    d = synth.two_level_inputs(1, g1, V, seed=99)
+    gen = synth.generator(1234, "cuda")
+    p, q, r = d["p"].cuda(), d["q"].cuda(), d["r"].cuda()
+    pN, qN, rN = p.expand(N, -1, -1).contiguous(), q.expand(N, -1, -1).contiguous(), r.expand(N, -1, -1).contiguous()
+    x = synth.sample_tokens(rN, gen)
+    u1 = torch.rand((N, g1), generator=gen, device="cuda")
+    ur1 = torch.rand((N,), generator=gen, device="cuda")
+    n1, nx1, y = cuda_lib.tf_spec_accept(qN[:, : g1 + 1].contiguous(), rN, x, u1, ur1)
+    u2 = torch.rand((N, g1 + 1), generator=gen, device="cuda")
+    ur2 = torch.rand((N,), generator=gen, device="cuda")
+    n2, nx2, z = cuda_lib.tf_spec_accept(pN, qN, y, u2, ur2)
+    torch.cuda.synchronize()
+    q0 = torch.softmax(q[0, 0].double(), -1).cpu().numpy()
+    p0 = torch.softmax(p[0, 0].double(), -1).cpu().numpy()
+    assert _chi2_ok(y[:, 0].cpu().numpy(), q0)
+    assert _chi2_ok(z[:, 0].cpu().numpy(), p0)
