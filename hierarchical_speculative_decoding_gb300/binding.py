@@ -32,6 +32,7 @@ _SIGS = {
     "tf_chunk_scores_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P]),
     "tf_sparse_decode_attn_workspace": (_S, [_I, _I, _I, _I]),
     "tf_sparse_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
+    "tf_sparse_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
     "tf_stream_window_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
     "tf_stream_window_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_verify_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
@@ -176,6 +177,26 @@ def tf_sparse_decode_attn(q, K, V, seq_lens, idx, n_sel, scale, out=None, ws=Non
     _check(load().tf_sparse_decode_attn(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(idx), _ptr(n_sel), B, Hq,
                                         Hkv, Lmax, D, chunk, kc, float(scale), _ptr(out), _ptr(ws), nbytes,
                                         _stream(stream)), "tf_sparse_decode_attn")
+    return out
+
+
+def tf_sparse_decode_attn_noalloc(q, K, V, seq_lens, idx, n_sel, scale, out, chunk=8, stream=None):
+    """tf_sparse_decode_attn for callers that cannot allocate: no workspace, the
+    scratch is the library's static per-device buffer.  `out` must be given
+    (preallocated by the caller); this wrapper allocates nothing either."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(K, torch.bfloat16, "K", 4)
+    _need(V, torch.bfloat16, "V", 4)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(idx, torch.int32, "idx", 3)
+    _need(n_sel, torch.int32, "n_sel", 2)
+    _need(out, torch.float32, "out", 3)
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = K.shape
+    kc = idx.shape[2]
+    _check(load().tf_sparse_decode_attn_noalloc(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(idx), _ptr(n_sel),
+                                                B, Hq, Hkv, Lmax, D, chunk, kc, float(scale), _ptr(out),
+                                                _stream(stream)), "tf_sparse_decode_attn_noalloc")
     return out
 
 

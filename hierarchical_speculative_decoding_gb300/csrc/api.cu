@@ -8,6 +8,7 @@ extern "C" const char* tf_status_string(tf_status s) {
     case TF_ERR_UNSUPPORTED: return "unsupported shape (head dim must be 128, chunk must be 8)";
     case TF_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than the *_workspace() size";
     case TF_ERR_CUDA: return "CUDA launch failed";
+    case TF_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the static buffer of the no-allocation entry point";
   }
   return "unknown status";
 }

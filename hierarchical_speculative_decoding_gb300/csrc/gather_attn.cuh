@@ -29,6 +29,7 @@ struct GatherParams {
   float* part_o;     // [units * ngroups, splits_cap, NQ, D]
 };
 
+int gather_nq(int rows);  // query rows per CTA for `rows` rows per unit
 size_t gather_workspace(int units, int rows, int P_max);
 tf_status gather_launch(int mode, GatherParams p, int units, int rows, int P_max, void* ws, size_t ws_bytes,
                         cudaStream_t stream);

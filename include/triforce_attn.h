@@ -58,7 +58,8 @@ typedef enum tf_status {
   TF_ERR_INVALID_ARG = 1,  /* null/misaligned pointer or inconsistent sizes; nothing launched */
   TF_ERR_UNSUPPORTED = 2,  /* valid but unsupported shape (D != 128, chunk != 8, ...) */
   TF_ERR_WORKSPACE = 3,    /* ws missing or ws_bytes below the *_workspace() size */
-  TF_ERR_CUDA = 4          /* a kernel launch failed (cudaGetLastError) */
+  TF_ERR_CUDA = 4,         /* a kernel launch failed (cudaGetLastError) */
+  TF_ERR_SCRATCH_LIMIT = 5 /* the no-allocation entry point's static scratch is too small */
 } tf_status;
 
 /* Static, human-readable text for a status code. */
@@ -120,6 +121,31 @@ TF_API tf_status tf_sparse_decode_attn(const uint16_t* q, const uint16_t* K, con
                                 int B, int Hq, int Hkv, int Lmax, int D, int chunk, int kc,
                                 float scale, float* out,
                                 void* ws, size_t ws_bytes, tf_stream_t stream);
+
+/*
+ * tf_sparse_decode_attn without a workspace, for callers that cannot allocate
+ * device memory (the paper has no counterpart; this is a deployment aid).
+ * Some hosts cannot call cudaMalloc: an engine that owns every device
+ * allocation, a plugin loaded into such an engine, or a latency-critical loop
+ * where allocating (and the synchronisation it may bring) is not allowed.
+ * Same inputs, outputs and result as tf_sparse_decode_attn; the split-K
+ * scratch is a 16 MiB file-scope device array instead of `ws`, held by every
+ * GPU that loads this library until the process exits.  The tickets use its
+ * first 64 KiB and the partial results the rest (about 8.5 MB for batch 8 x
+ * 8 KV heads x 4 query heads per group at kc = 512); problems whose partial
+ * results exceed 16 MiB - 64 KiB return TF_ERR_SCRATCH_LIMIT without
+ * launching anything.
+ * The first call on each device sets up that device's copy (looks up its
+ * address with cudaGetSymbolAddress and zeroes the ticket area with a
+ * synchronous cudaMemset), so make it before any stream capture.  All calls
+ * share the one array and leave their contents in it: calls that may overlap
+ * on the GPU (unordered streams) race and give wrong results.  It allocates
+ * nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+TF_API tf_status tf_sparse_decode_attn_noalloc(const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                                const int32_t* seq_lens, const int32_t* idx, const int32_t* n_sel,
+                                int B, int Hq, int Hkv, int Lmax, int D, int chunk, int kc,
+                                float scale, float* out, tf_stream_t stream);
 
 /*
  * a6 (+ a5) -- StreamingLLM sink + window attention (Force 1 drafter).
