@@ -45,12 +45,10 @@ __global__ void __launch_bounds__(kGatherThreads) gather_attn_kernel(GatherParam
     nsel = nsel < 0 ? 0 : (nsel > p.kc ? p.kc : nsel);
     sel = p.idx + (size_t)unit * p.kc;
     P = nsel * kChunk;
-  } else if (MODE == kModeWindow) {
+  } else {
     ns_eff = min(p.n_sink, L);
     w0 = max(p.n_sink, L - p.window);
     P = ns_eff + max(0, L - w0);
-  } else {
-    P = L;
   }
   const int C = (L + kChunk - 1) / kChunk;
 
@@ -63,8 +61,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_attn_kernel(GatherParam
     const int rr = grp * NQ + r;
     row_on[r] = rr < rows;
     const int hh = row_on[r] ? rr / p.T : 0, j = row_on[r] ? rr % p.T : 0;
-    lim[r] = (MODE == kModePrefix) ? (L - p.T + j) : 0x7fffffff;
-    if (!row_on[r]) lim[r] = -1;
+    lim[r] = row_on[r] ? 0x7fffffff : -1;
     const uint16_t* qrow = p.q + (((size_t)b * p.Hq + (size_t)g * G + hh) * p.T + j) * kHeadDim + l16 * 8;
     float f[8];
     unpack8(row_on[r] ? *reinterpret_cast<const uint4*>(qrow) : make_uint4(0, 0, 0, 0), f);
@@ -101,10 +98,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_attn_kernel(GatherParam
           const int c = sel[v >> 3];
           t = (c >= 0 && c < C) ? c * kChunk + (v & 7) : -1;
           if (t >= L) t = -1;
-        } else if (MODE == kModeWindow) {
-          t = (v < ns_eff) ? v : w0 + (v - ns_eff);
         } else {
-          t = v;
+          t = (v < ns_eff) ? v : w0 + (v - ns_eff);
         }
       }
       pos[i] = t;
@@ -267,8 +262,7 @@ template <int NQ>
 static void launch_nq(int mode, const GatherParams& p, dim3 grid, cudaStream_t s) {
   switch (mode) {
     case kModeChunks: gather_attn_kernel<NQ, kModeChunks><<<grid, kGatherThreads, 0, s>>>(p); break;
-    case kModeWindow: gather_attn_kernel<NQ, kModeWindow><<<grid, kGatherThreads, 0, s>>>(p); break;
-    default: gather_attn_kernel<NQ, kModePrefix><<<grid, kGatherThreads, 0, s>>>(p); break;
+    default: gather_attn_kernel<NQ, kModeWindow><<<grid, kGatherThreads, 0, s>>>(p); break;
   }
 }
 

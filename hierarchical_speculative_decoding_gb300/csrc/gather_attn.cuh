@@ -1,5 +1,5 @@
-// Decode attention over a gathered position set (sparse chunks, sink+window,
-// or a causal prefix); shared by the sparse, window and verify entry points.
+// Decode attention over a gathered position set (sparse chunks or sink +
+// window); shared by the sparse and window entry points.
 #pragma once
 
 #include "tf_common.cuh"
@@ -9,7 +9,6 @@ namespace tf {
 constexpr int kGatherThreads = 256;
 constexpr int kModeChunks = 0;  // positions of the selected chunks (Force 2)
 constexpr int kModeWindow = 1;  // attention sinks + recent window (Force 1)
-constexpr int kModePrefix = 2;  // positions [0, L - T + j] for query j (Force 3)
 
 struct GatherParams {
   const uint16_t* q;  // [B, Hq, T, D]

@@ -9,11 +9,14 @@
 //
 // Design: one kernel.  The (b, g) units are few (32 at batch 1) while each
 // holds up to ~16K chunks, so every unit is split over several CTAs that stream
-// the chunk means (a half-warp per 256-byte mean row, 16-byte loads) and write
-// fp32 scores to the workspace.  The last CTA of a unit to finish (an atomic
-// ticket; no CTA ever waits) runs an exact radix select on order-preserving
-// uint32 keys (11 + 11 + 10 bits), then compacts the winners in id order with a
-// block-wide scan, so ties resolve to the lower id without any sort.
+// the chunk means (a half-warp per 256-byte mean row, 16-byte loads), write fp32
+// scores to the workspace and add the top 11 bits of each order-preserving
+// uint32 score key to a per-unit histogram.  The last CTA of a unit to finish
+// (an atomic ticket; no CTA ever waits) reads that histogram to find the bin
+// holding the kc-th largest key, pulls the unit's keys into shared memory while
+// collecting the few keys of that bin, resolves the remaining 21 bits on those
+// candidates alone, and then compacts the winners in id order with two
+// warp-segmented ballot walks, so ties resolve to the lower id without a sort.
 #include "tf_common.cuh"
 
 namespace tf {
@@ -22,98 +25,148 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 4;
+constexpr int kBins = 2048;       // histogram over the top 11 key bits
+constexpr int kSmemKeys = 16384;  // keys the selecting CTA keeps in shared memory (128K tokens)
+constexpr int kCandCap = 2048;    // keys of the threshold bin resolved in shared memory
 
 inline size_t tickets_bytes(int units) { return align_up((size_t)units * sizeof(int), 256); }
+inline size_t hist_bytes(int units) { return (size_t)units * kBins * sizeof(uint32_t); }
 
-// Exclusive block scan of two 0/1 flags; returns the block totals.
-__device__ __forceinline__ void block_scan2(bool a, bool b, int& a_ex, int& b_ex, int& a_tot, int& b_tot,
-                                            int* sa, int* sb) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned ba = __ballot_sync(0xffffffffu, a), bb = __ballot_sync(0xffffffffu, b);
-  const unsigned below = (1u << lane) - 1u;
-  if (lane == 0) {
-    sa[warp] = __popc(ba);
-    sb[warp] = __popc(bb);
-  }
-  __syncthreads();
-  int pa = 0, pb = 0, ta = 0, tb = 0;
+// Warp 0 scans hist[0, nb) from the top and finds the bin holding the krem-th
+// largest key; writes the bin and how many keys are still needed from it.
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int krem, int* s_bin, int* s_krem) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int seg = nb / 32;
+    const int top = nb - lane * seg;  // lane 0 owns the highest bins
+    int segsum = 0;
+    for (int i = top - seg; i < top; ++i) segsum += (int)hist[i];
+    int incl = segsum;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const int xa = sa[w], xb = sb[w];
-    if (w < warp) { pa += xa; pb += xb; }
-    ta += xa;
-    tb += xb;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int excl = incl - segsum;
+    if (excl < krem && krem <= incl) {
+      int run = excl;
+      for (int i = top - 1; i >= top - seg; --i) {
+        const int h = (int)hist[i];
+        if (run + h >= krem) {
+          *s_bin = i;
+          *s_krem = krem - run;
+          break;
+        }
+        run += h;
+      }
+    }
   }
-  a_ex = pa + __popc(ba & below);
-  b_ex = pb + __popc(bb & below);
-  a_tot = ta;
-  b_tot = tb;
-  __syncthreads();
 }
 
-// Radix-select the kc-th largest key among keys[0, C) (C > kc); returns the
-// threshold key and how many keys equal to it are to be taken.
-__device__ void radix_select(const float* __restrict__ scores, int C, int kc, unsigned* hist,
-                             uint32_t& thresh, int& take_eq) {
-  __shared__ int s_bin, s_krem;
-  uint32_t prefix = 0, pmask = 0;
-  int krem = kc;
-  const int shifts[3] = {21, 10, 0};
-  const int nbits[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = shifts[pass];
-    const int nb = 1 << nbits[pass];
+template <bool kSmem>
+__device__ __forceinline__ uint32_t key_at(const uint32_t* keys, const float* scores, int c) {
+  return kSmem ? keys[c] : score_key(__ldcg(scores + c));
+}
+
+// Select the kc largest of C > kc keys (ties to the lower id) and write their ids
+// ascending.  hist holds the unit's top-11-bit histogram on entry.
+template <bool kSmem>
+__device__ __noinline__ void select_and_compact(const uint32_t* keys, const float* scores, int C, int kc, uint32_t* hist,
+                                   uint32_t* cand, int32_t* out, uint32_t* thresh_out) {
+  __shared__ int s_bin, s_krem, s_ncand;
+  __shared__ int s_wgt[kWarps], s_weq[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  // 1. the top-11-bit bin of the kc-th largest key
+  find_bin(hist, kBins, kc, &s_bin, &s_krem);
+  if (threadIdx.x == 0) s_ncand = 0;
+  __syncthreads();
+  const uint32_t b1 = (uint32_t)s_bin;
+  int krem = s_krem;
+
+  // 2. collect the keys of that bin
+  for (int c = threadIdx.x; c < C; c += kThreads) {
+    const uint32_t key = key_at<kSmem>(keys, scores, c);
+    if ((key >> 21) == b1) {
+      const int slot = atomicAdd(&s_ncand, 1);
+      if (slot < kCandCap) cand[slot] = key;
+    }
+  }
+  __syncthreads();
+  const int ncand = s_ncand;
+  const bool in_cand = ncand <= kCandCap;
+
+  // 3. remaining 11 + 10 bits, on the candidates (or on all keys if the bin is huge)
+  uint32_t prefix = b1 << 21, pmask = 0xFFE00000u;
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = pass == 0 ? 10 : 0, nb = pass == 0 ? 2048 : 1024;
     const uint32_t mask = (uint32_t)nb - 1u;
     for (int i = threadIdx.x; i < nb; i += kThreads) hist[i] = 0;
     __syncthreads();
-    for (int c = threadIdx.x; c < C; c += kThreads) {
-      const uint32_t key = score_key(__ldcg(scores + c));
+    const int n = in_cand ? ncand : C;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t key = in_cand ? cand[i] : key_at<kSmem>(keys, scores, i);
       if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & mask], 1u);
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      const int seg = nb / 32;
-      const int top = nb - lane * seg;  // lane 0 owns the highest bins
-      int segsum = 0;
-      for (int i = top - seg; i < top; ++i) segsum += (int)hist[i];
-      int incl = segsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const int excl = incl - segsum;
-      if (excl < krem && krem <= incl) {
-        int run = excl;
-        for (int i = top - 1; i >= top - seg; --i) {
-          const int h = (int)hist[i];
-          if (run + h >= krem) {
-            s_bin = i;
-            s_krem = krem - run;
-            break;
-          }
-          run += h;
-        }
-      }
-    }
+    find_bin(hist, nb, krem, &s_bin, &s_krem);
     __syncthreads();
     prefix |= (uint32_t)s_bin << shift;
     pmask |= mask << shift;
     krem = s_krem;
     __syncthreads();
   }
-  thresh = prefix;
-  take_eq = krem;
+  const uint32_t T = prefix;
+  const int take_eq = krem;
+
+  // 4. id-order compaction: warp w owns ids [w * seg, (w + 1) * seg)
+  const int seg = ((C + kWarps - 1) / kWarps + 31) & ~31;
+  const int w0 = warp * seg, w1 = min(C, w0 + seg);
+  const unsigned lt = (1u << lane) - 1u;
+  int ngt = 0, neq = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int c = base + lane;
+    const uint32_t key = c < w1 ? key_at<kSmem>(keys, scores, c) : 0u;
+    ngt += __popc(__ballot_sync(0xffffffffu, c < w1 && key > T));
+    neq += __popc(__ballot_sync(0xffffffffu, c < w1 && key == T));
+  }
+  if (lane == 0) {
+    s_wgt[warp] = ngt;
+    s_weq[warp] = neq;
+  }
+  __syncthreads();
+  int eq_base = 0, sel_base = 0;
+  for (int w = 0; w < warp; ++w) {
+    const int take = min(max(take_eq - eq_base, 0), s_weq[w]);
+    sel_base += s_wgt[w] + take;
+    eq_base += s_weq[w];
+  }
+  for (int base = w0; base < w1; base += 32) {
+    const int c = base + lane;
+    const uint32_t key = c < w1 ? key_at<kSmem>(keys, scores, c) : 0u;
+    const bool gt = c < w1 && key > T;
+    const bool eq = c < w1 && key == T;
+    const unsigned beq = __ballot_sync(0xffffffffu, eq);
+    const bool sel = gt || (eq && eq_base + __popc(beq & lt) < take_eq);
+    const unsigned bsel = __ballot_sync(0xffffffffu, sel);
+    const int pos = sel_base + __popc(bsel & lt);
+    if (sel && pos < kc) out[pos] = c;
+    eq_base += __popc(beq);
+    sel_base += __popc(bsel);
+  }
+  *thresh_out = T;
 }
 
-__global__ void __launch_bounds__(kThreads) scores_topk_kernel(
+__global__ void __launch_bounds__(kThreads, 2) scores_topk_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ M, const int32_t* __restrict__ seq_lens,
-    int Hq, int Hkv, int Lmax, int kc, int splits, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel,
-    float* __restrict__ s_cut, int* __restrict__ tickets, float* __restrict__ scores_ws) {
+    int Hq, int Hkv, int Lmax, int kc, int splits, int smem_keys, int32_t* __restrict__ idx,
+    int32_t* __restrict__ n_sel, float* __restrict__ s_cut, int* __restrict__ tickets,
+    uint32_t* __restrict__ hist_ws, float* __restrict__ scores_ws) {
+  extern __shared__ uint32_t keys_smem[];
   __shared__ float qs[kHeadDim];
-  __shared__ unsigned hist[2048];
-  __shared__ int scan_a[kWarps], scan_b[kWarps];
+  __shared__ uint32_t hist[kBins];
+  __shared__ uint32_t cand[kCandCap];
   __shared__ int s_last;
   __shared__ float s_min[kWarps];
 
@@ -124,6 +177,7 @@ __global__ void __launch_bounds__(kThreads) scores_topk_kernel(
   const int L = clamp_len(seq_lens[b], Lmax);
   const int C = (L + kChunk - 1) / kChunk;
   float* scores = scores_ws + (size_t)unit * Cmax;
+  uint32_t* hist_g = hist_ws + (size_t)unit * kBins;
 
   if (threadIdx.x < kHeadDim) {
     float s = 0.0f;
@@ -131,6 +185,7 @@ __global__ void __launch_bounds__(kThreads) scores_topk_kernel(
       s += __uint_as_float((uint32_t)q[((size_t)b * Hq + (size_t)g * G + h) * kHeadDim + threadIdx.x] << 16);
     qs[threadIdx.x] = s;
   }
+  for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
   __syncthreads();
 
   // ---- scoring: this CTA's slice of the unit's chunks
@@ -165,9 +220,15 @@ __global__ void __launch_bounds__(kThreads) scores_topk_kernel(
       s += __shfl_xor_sync(0xffffffffu, s, 2);
       s += __shfl_xor_sync(0xffffffffu, s, 1);
       const int c = cb + u * kHalfWarps;
-      if (l16 == 0 && c < c1) scores[c] = s;
+      if (l16 == 0 && c < c1) {
+        scores[c] = s;
+        atomicAdd(&hist[score_key(s) >> 21], 1u);
+      }
     }
   }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kBins; i += kThreads)
+    if (hist[i]) atomicAdd(&hist_g[i], hist[i]);
 
   // ---- ticket: the last CTA of this unit selects
   __threadfence();
@@ -176,6 +237,13 @@ __global__ void __launch_bounds__(kThreads) scores_topk_kernel(
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+
+  // the unit's histogram -> shared memory; leave the workspace copy zeroed
+  for (int i = threadIdx.x; i < kBins; i += kThreads) {
+    hist[i] = __ldcg(hist_g + i);
+    hist_g[i] = 0u;
+  }
+  __syncthreads();
 
   int32_t* out = idx + (size_t)unit * kc;
   if (C <= kc) {
@@ -198,24 +266,13 @@ __global__ void __launch_bounds__(kThreads) scores_topk_kernel(
     return;
   }
 
-  uint32_t T;
-  int take_eq;
-  radix_select(scores, C, kc, hist, T, take_eq);
-
-  int run_out = 0, run_eq = 0;
-  for (int base = 0; base < C; base += kThreads) {
-    const int c = base + threadIdx.x;
-    const uint32_t key = (c < C) ? score_key(__ldcg(scores + c)) : 0u;
-    const bool gt = (c < C) && key > T;
-    const bool eq = (c < C) && key == T;
-    int eq_ex, dummy_ex, eq_tot, dummy_tot;
-    block_scan2(eq, false, eq_ex, dummy_ex, eq_tot, dummy_tot, scan_a, scan_b);
-    const bool sel = gt || (eq && (run_eq + eq_ex) < take_eq);
-    int sel_ex, sel_tot;
-    block_scan2(sel, false, sel_ex, dummy_ex, sel_tot, dummy_tot, scan_a, scan_b);
-    if (sel && run_out + sel_ex < kc) out[run_out + sel_ex] = c;
-    run_out += sel_tot;
-    run_eq += eq_tot;
+  uint32_t T = 0;
+  if (C <= smem_keys) {
+    for (int c = threadIdx.x; c < C; c += kThreads) keys_smem[c] = score_key(__ldcg(scores + c));
+    __syncthreads();
+    select_and_compact<true>(keys_smem, scores, C, kc, hist, cand, out, &T);
+  } else {
+    select_and_compact<false>(keys_smem, scores, C, kc, hist, cand, out, &T);
   }
   if (threadIdx.x == 0) {
     n_sel[unit] = kc;
@@ -241,7 +298,7 @@ extern "C" size_t tf_chunk_scores_topk_workspace(int B, int Hkv, int Lmax, int c
   if (B <= 0 || Hkv <= 0 || Lmax <= 0 || chunk != tf::kChunk) return 0;
   const size_t units = (size_t)B * Hkv;
   const size_t Cmax = (size_t)(Lmax + chunk - 1) / chunk;
-  return tf::tickets_bytes((int)units) + units * Cmax * sizeof(float);
+  return tf::tickets_bytes((int)units) + tf::hist_bytes((int)units) + units * Cmax * sizeof(float);
 }
 
 extern "C" tf_status tf_chunk_scores_topk(const uint16_t* q, const uint16_t* M, const int32_t* seq_lens, int B,
@@ -259,10 +316,21 @@ extern "C" tf_status tf_chunk_scores_topk(const uint16_t* q, const uint16_t* M, 
   const int units = B * Hkv;
   const int Cmax = (Lmax + kChunk - 1) / kChunk;
   const int splits = scores_splits(units, Cmax);
-  int* tickets = static_cast<int*>(ws);
-  float* scores = reinterpret_cast<float*>(static_cast<char*>(ws) + tickets_bytes(units));
+  const int smem_keys = Cmax <= kSmemKeys ? Cmax : 0;
+  const size_t dyn = (size_t)smem_keys * sizeof(uint32_t);
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(scores_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemKeys * (int)sizeof(uint32_t)) != cudaSuccess)
+      return TF_ERR_CUDA;
+    configured = true;
+  }
+  char* w = static_cast<char*>(ws);
+  int* tickets = reinterpret_cast<int*>(w);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(w + tickets_bytes(units));
+  float* scores = reinterpret_cast<float*>(w + tickets_bytes(units) + hist_bytes(units));
   dim3 grid(splits, units);
-  scores_topk_kernel<<<grid, kThreads, 0, stream>>>(q, M, seq_lens, Hq, Hkv, Lmax, kc, splits, idx, n_sel, s_cut,
-                                                    tickets, scores);
+  scores_topk_kernel<<<grid, kThreads, dyn, stream>>>(q, M, seq_lens, Hq, Hkv, Lmax, kc, splits, smem_keys, idx,
+                                                      n_sel, s_cut, tickets, hist, scores);
   return launch_status();
 }

@@ -1,14 +1,502 @@
-// a7 (+ a5) -- full-cache verification attention (Force 3).
+// a7 (+ a5) -- full-cache verification attention (Force 3) on the 5th-generation
+// tensor cores.
 //
 // "TriForce: Hierarchical Speculative Decoding for LLMs", "The Three Forces of
-// TriForce": the target model with the complete KV cache checks all drafted
-// candidates in one parallel pass.  The candidates form a chain whose keys
-// already sit at positions L-T .. L-1, so query j sees positions [0, L-T+j].
-#include "gather_attn.cuh"
+// TriForce": the target model with the complete KV cache checks every drafted
+// candidate in one parallel pass.  The candidates form a chain whose keys sit at
+// positions L-T .. L-1, so verify query j sees positions [0, L-T+j].
+//
+// The whole cache is read once per step, so the kernel is HBM-bound (6 flop/B for
+// MHA, 24 flop/B for a GQA group of 4); the tensor cores only have to keep up.
+// Per CTA: one (sequence, KV head) unit, one group of <= 32 query rows (the
+// GQA heads x gamma+1 tokens, padded to N = 16 or 32) and one contiguous key
+// range (split-K).  Warp roles:
+//   warp 0    TMA producer: 128-key tiles of K and V (2 x 32 KB, 128-byte
+//             swizzle) into a 3-stage shared-memory ring;
+//   warp 1    tcgen05 issuer: S^T[key, n] = K Q^T into TMEM (M = 128 keys),
+//             then O^T[d, n] = V^T P^T into TMEM (M = 128 head dims, V read
+//             MN-major straight from the TMA tile);
+//   warps 2-5 softmax on TMEM lane = key (online, log2 domain, rescaled only
+//             when the running max grows by > 2^8), P written to shared memory
+//             as bf16; then the O tile of the previous key tile is read back
+//             (TMEM lane = head dim) and accumulated in fp32 registers.
+// S, P and O are double-buffered so the MMA of tile t+1 overlaps the softmax of
+// tile t.  Splits are merged with the log-sum-exp identity by the last CTA of
+// each unit (atomic ticket).  Every mbarrier wait is bounded; on a timeout the
+// CTA records a nonzero status word at the start of the workspace and leaves.
+#include <cuda_bf16.h>
+
+#include "sm100_ptx.cuh"
+#include "tf_common.cuh"
+
+namespace tf {
+namespace {
+
+using namespace sm100;
+
+constexpr int kTile = 128;          // keys per tile (MMA M)
+constexpr int kStages = 3;          // K/V ring depth
+constexpr int kStageBytes = 2 * kTile * kHeadDim * 2;  // K + V tile
+constexpr int kThreads = 192;       // 6 warps
+constexpr int kSoftmaxThreads = 128;
+constexpr int kMaxRows = 32;        // query rows per CTA (N <= 32)
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint32_t kTmemCols = 128;
+
+
+struct VerifyParams {
+  const uint16_t* Q;
+  const int32_t* seq_lens;
+  float* out;
+  int* status;    // workspace status word
+  int* tickets;   // [units * ngroups]
+  float* part_ml; // [units * ngroups, splits_cap, kMaxRows, 2]
+  float* part_o;  // [units * ngroups, splits_cap, kMaxRows, D]
+  int Hq, Hkv, Lmax, T, ngroups, splits, splits_cap;
+  float scale_log2;
+};
+
+template <int NPAD>
+struct Smem {
+  static constexpr int kQBytes = 2 * NPAD * 128;     // two 64-column halves of [NPAD x 128] bf16
+  static constexpr int kPHalf = 2 * NPAD * 128;      // one bf16 copy of P [NPAD x 128 keys]
+  static constexpr int kPBuf = 2 * kPHalf;           // P split into hi + lo bf16 parts
+  static constexpr int kNumPBuf = NPAD <= 16 ? 2 : 1;  // double-buffer P when it fits
+  static constexpr int kOffQ = kStages * kStageBytes;
+  static constexpr int kOffP = kOffQ + kQBytes;
+  static constexpr int kBytes = kOffP + kNumPBuf * kPBuf;
+  static constexpr int kDynamic = kBytes + 1024;     // slack for 1024-byte alignment
+};
+
+__device__ __forceinline__ bool named_bar_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(kSoftmaxThreads));
+  return r != 0;
+}
+
+__device__ __forceinline__ void named_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
+}
+
+template <int NPAD>
+__global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_constant__ CUtensorMap mapK,
+                                                                  const __grid_constant__ CUtensorMap mapV,
+                                                                  VerifyParams p) {
+  using S = Smem<NPAD>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages];
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_o_full[2], bar_o_free[2];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ float red[4][NPAD];
+  __shared__ float alpha_s[2][NPAD];
+  __shared__ int rescaled_s[2];
+  __shared__ int s_last, s_abort;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + S::kOffQ;
+  uint8_t* sP = smem + S::kOffP;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ug = blockIdx.y;
+  const int unit = ug / p.ngroups, grp = ug % p.ngroups;
+  const int b = unit / p.Hkv, g = unit % p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const int rows_all = G * p.T;
+  const int row0 = grp * kMaxRows;
+  const int rows = min(kMaxRows, rows_all - row0);
+  const int L = clamp_len(p.seq_lens[b], p.Lmax);
+
+  // key range of this split: whole tiles
+  const int tiles_all = (L + kTile - 1) / kTile;
+  const int tiles_per = (tiles_all + p.splits - 1) / p.splits;
+  const int k0 = blockIdx.x * tiles_per * kTile;
+  const int k1 = min(L, k0 + tiles_per * kTile);
+  const int ntiles = k1 > k0 ? (k1 - k0 + kTile - 1) / kTile : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_s_full[i], 1);
+      mbar_init(&bar_p_full[i], kSoftmaxThreads);
+      mbar_init(&bar_o_full[i], 1);
+      mbar_init(&bar_o_free[i], kSoftmaxThreads);
+    }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&mapK);
+    prefetch_tensormap(&mapV);
+  }
+  // Q rows of this group -> shared memory, [NPAD x 128] bf16 in two swizzled halves.
+  {
+    const uint16_t* Qg = p.Q + (((size_t)b * p.Hq + (size_t)g * G) * p.T + row0) * kHeadDim;
+    for (int e = tid; e < NPAD * 16; e += kThreads) {
+      const int r = e >> 4, c8 = (e & 15) * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < rows) v = *reinterpret_cast<const uint4*>(Qg + (size_t)r * kHeadDim + c8);
+      const uint32_t off = (c8 >> 6) * (NPAD * 128) + sw128_offset(r, c8 & 63);
+      *reinterpret_cast<uint4*>(sQ + off) = v;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;  // columns: S0 [0,32) S1 [32,64) O0 [64,96) O1 [96,128)
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const int row_base = unit * p.Lmax + k0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kStages;
+        if (t >= kStages && !mbar_wait(&bar_empty[s], ((t / kStages) - 1) & 1)) {
+          atomicExch(&s_abort, 1);
+          break;
+        }
+        if (*(volatile int*)&s_abort) break;
+        uint8_t* sk = smem + s * kStageBytes;
+        uint8_t* sv = sk + kTile * kHeadDim * 2;
+        mbar_arrive_expect_tx(&bar_full[s], kStageBytes);
+        const int y = row_base + t * kTile;
+        tma_load_2d(sk, &mapK, &bar_full[s], 0, y);
+        tma_load_2d(sk + 16384, &mapK, &bar_full[s], 64, y);
+        tma_load_2d(sv, &mapV, &bar_full[s], 0, y);
+        tma_load_2d(sv + 16384, &mapV, &bar_full[s], 64, y);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16_f32(128, NPAD, false, false);
+      const uint32_t idO = idesc_bf16_f32(128, NPAD, true, false);
+      const uint32_t q_addr = smem_u32(sQ);
+      for (int t = 0; t <= ntiles; ++t) {
+        if (t < ntiles) {
+          const int s = t % kStages;
+          if (!mbar_wait(&bar_full[s], (t / kStages) & 1)) { atomicExch(&s_abort, 1); break; }
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(smem + s * kStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t a = smem_desc(k_addr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc(q_addr + (kk >> 2) * (NPAD * 128) + (kk & 3) * 32, 16, 1024);
+            mma_bf16(tmem + (t & 1) * 32, a, bd, idS, kk > 0);
+          }
+          mma_commit(&bar_s_full[t & 1]);
+        }
+        if (t >= 1) {
+          const int u = t - 1;
+          if (!mbar_wait(&bar_p_full[u & 1], (u >> 1) & 1)) { atomicExch(&s_abort, 1); break; }
+          if (u >= 2 && !mbar_wait(&bar_o_free[u & 1], ((u - 2) >> 1) & 1)) { atomicExch(&s_abort, 1); break; }
+          tc_fence_after();
+          const uint32_t v_addr = smem_u32(smem + (u % kStages) * kStageBytes + kTile * kHeadDim * 2);
+          const uint32_t p_addr = smem_u32(sP + (u % S::kNumPBuf) * S::kPBuf);
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {
+            // A = V^T (M = head dim, K = key), MN-major: 64-dim atoms 16 KB apart,
+            // 8-key groups 1 KB apart.  B = P (N = query row, K = key), K-major;
+            // the hi part (kk < 8) and then the lo part (kk >= 8) of P.
+            const int k8 = kk & 7;
+            const uint64_t a = smem_desc(v_addr + k8 * 2048, 16384, 1024);
+            const uint64_t bd = smem_desc(p_addr + (kk >> 3) * S::kPHalf + (k8 >> 2) * (NPAD * 128) + (k8 & 3) * 32,
+                                          16, 1024);
+            mma_bf16(tmem + 64 + (u & 1) * 32, a, bd, idO, kk > 0);
+          }
+          mma_commit(&bar_o_full[u & 1]);
+          mma_commit(&bar_empty[u % kStages]);
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax + correction
+    const int q4 = warp & 3;               // TMEM lane quarter of this warp
+    const int my = q4 * 32 + lane;         // key index in the tile / head dim of O
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    float m_run[NPAD], l_part[NPAD], acc[NPAD];
+    int lim[NPAD];
+#pragma unroll
+    for (int n = 0; n < NPAD; ++n) {
+      m_run[n] = -INFINITY;
+      l_part[n] = 0.0f;
+      acc[n] = 0.0f;
+      const int rr = row0 + n;
+      lim[n] = (n < rows) ? (L - p.T + (rr % p.T)) : -1;
+    }
+    // Every wait is followed by a vote over the 128 threads so that a timeout
+    // makes all of them leave the loop together (named barriers stay matched).
+    for (int t = 0; t <= ntiles; ++t) {
+      float sc[NPAD];  // scores, then softmax weights of tile t
+      if (t < ntiles) {
+        const bool timed_out = !mbar_wait(&bar_s_full[t & 1], (t >> 1) & 1);
+        if (named_bar_or(timed_out)) {
+          if (my == 0) atomicExch(&s_abort, 1);
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < NPAD; c += 8) tmem_ld8(tmem + (t & 1) * 32 + lane_off + c, sc + c);
+        tmem_ld_wait();
+        const int pos = k0 + t * kTile + my;
+        bool need = false;
+#pragma unroll
+        for (int n = 0; n < NPAD; ++n) {
+          const bool valid = pos < k1 && pos <= lim[n];
+          sc[n] = valid ? sc[n] * p.scale_log2 : -INFINITY;
+          need |= sc[n] > m_run[n] + kRescaleThreshold;
+        }
+        need = named_bar_or(need);
+        if (need) {
+          // tile max per row, then a new reference max for every row that grew
+#pragma unroll
+          for (int n = 0; n < NPAD; ++n) {
+            float v = sc[n];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) red[q4][n] = v;
+          }
+          named_bar_sync();
+#pragma unroll
+          for (int n = 0; n < NPAD; ++n) {
+            const float tmax = fmaxf(fmaxf(red[0][n], red[1][n]), fmaxf(red[2][n], red[3][n]));
+            const float mn = fmaxf(m_run[n], tmax);
+            const float a = merge_scale(m_run[n], mn);
+            l_part[n] *= a;
+            if (my == 0) alpha_s[t & 1][n] = a;
+            m_run[n] = mn;
+          }
+          named_bar_sync();  // red[] is reused by the next rescale
+        }
+        if (my == 0) rescaled_s[t & 1] = need ? 1 : 0;
+#pragma unroll
+        for (int n = 0; n < NPAD; ++n) sc[n] = (sc[n] == -INFINITY) ? 0.0f : exp2f(sc[n] - m_run[n]);
+      }
+      if (t >= 1) {
+        // O of the previous tile: after this, P V of tile t-1 has finished, so
+        // its P buffer may be overwritten (a single P buffer suffices).
+        const int u = t - 1;
+        const bool timed_out = !mbar_wait(&bar_o_full[u & 1], (u >> 1) & 1);
+        if (named_bar_or(timed_out)) {  // also orders alpha_s / rescaled_s of tile u
+          if (my == 0) atomicExch(&s_abort, 1);
+          break;
+        }
+        tc_fence_after();
+        float ov[NPAD];
+#pragma unroll
+        for (int c = 0; c < NPAD; c += 8) tmem_ld8(tmem + 64 + (u & 1) * 32 + lane_off + c, ov + c);
+        tmem_ld_wait();
+        const bool resc = rescaled_s[u & 1] != 0;
+#pragma unroll
+        for (int n = 0; n < NPAD; ++n) acc[n] = (resc ? acc[n] * alpha_s[u & 1][n] : acc[n]) + ov[n];
+        tc_fence_before();
+        mbar_arrive(&bar_o_free[u & 1]);
+      }
+      if (t < ntiles) {
+        // P for this tile as hi + lo bf16 parts (P V error ~2^-17 instead of
+        // 2^-9 relative); row n, column = key.
+        const int pos = k0 + t * kTile + my;
+        uint8_t* pbuf = sP + (t % S::kNumPBuf) * S::kPBuf;
+        const uint32_t off_key = (uint32_t)(my >> 6) * (NPAD * 128);
+#pragma unroll
+        for (int n = 0; n < NPAD; ++n) {
+          const float pv = sc[n];
+          const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
+          l_part[n] += pv;
+          const uint32_t o = off_key + sw128_offset(n, my & 63);
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + o) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + S::kPHalf + o) = lo;
+        }
+        if (t == ntiles - 1 && pos >= k1) {
+          // Rows past the key range may hold anything (even NaN): zero them in
+          // the V tile so 0 * V stays 0 in the MMA.  Waiting on the (already
+          // completed) TMA barrier orders these writes after the tile landed.
+          const int s = t % kStages;
+          mbar_wait(&bar_full[s], (t / kStages) & 1);
+          uint8_t* sv = smem + s * kStageBytes + kTile * kHeadDim * 2;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(sv + h * 16384 + my * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar_p_full[t & 1]);
+      }
+    }
+
+    // ---- row sums across the 128 key lanes
+#pragma unroll
+    for (int n = 0; n < NPAD; ++n) {
+      float v = l_part[n];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) red[q4][n] = v;
+    }
+    named_bar_sync();
+    const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
+    if (p.splits == 1) {
+#pragma unroll
+      for (int n = 0; n < NPAD; ++n) {
+        if (n < rows) {
+          const float l = (red[0][n] + red[1][n]) + (red[2][n] + red[3][n]);
+          p.out[(out_row0 + n) * kHeadDim + my] = (l > 0.0f) ? acc[n] / l : 0.0f;
+        }
+      }
+    } else {
+      float* ml = p.part_ml + ((size_t)ug * p.splits_cap + blockIdx.x) * kMaxRows * 2;
+      float* po = p.part_o + ((size_t)ug * p.splits_cap + blockIdx.x) * kMaxRows * kHeadDim;
+#pragma unroll
+      for (int n = 0; n < NPAD; ++n) {
+        if (n < rows) {
+          if (my == 0) {
+            ml[n * 2 + 0] = m_run[n];
+            ml[n * 2 + 1] = (red[0][n] + red[1][n]) + (red[2][n] + red[3][n]);
+          }
+          po[n * kHeadDim + my] = acc[n];
+        }
+      }
+    }
+  }
+
+  // ---- teardown (all warps)
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (s_abort) {
+    if (tid == 0) atomicExch(p.status, 1);
+    // Let any TMA copy still in flight land before the CTA's shared memory goes away.
+    if (tid == 0)
+      for (int s = 0; s < kStages; ++s) mbar_wait(&bar_full[s], 0, 1u << 16);
+    return;
+  }
+  if (p.splits == 1) return;
+
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&p.tickets[ug], 1) == p.splits - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float* ml0 = p.part_ml + (size_t)ug * p.splits_cap * kMaxRows * 2;
+  const float* o0 = p.part_o + (size_t)ug * p.splits_cap * kMaxRows * kHeadDim;
+  const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
+  for (int e = tid; e < rows * kHeadDim; e += kThreads) {
+    const int n = e / kHeadDim, d = e % kHeadDim;
+    float mx = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) mx = fmaxf(mx, __ldcg(ml0 + ((size_t)s * kMaxRows + n) * 2));
+    float ls = 0.0f, os = 0.0f;
+    for (int s = 0; s < p.splits; ++s) {
+      const float f = merge_scale(__ldcg(ml0 + ((size_t)s * kMaxRows + n) * 2), mx);
+      ls = fmaf(f, __ldcg(ml0 + ((size_t)s * kMaxRows + n) * 2 + 1), ls);
+      os = fmaf(f, __ldcg(o0 + ((size_t)s * kMaxRows + n) * kHeadDim + d), os);
+    }
+    p.out[(out_row0 + n) * kHeadDim + d] = (ls > 0.0f) ? os / ls : 0.0f;
+  }
+  if (tid == 0) p.tickets[ug] = 0;
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// [rows, 128] bf16 rows of 256 bytes; boxes of 128 rows x 64 columns, 128-byte swizzle.
+bool make_kv_map(CUtensorMap* m, const void* base, long long rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kTile};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int verify_splits_cap(int Lmax) {
+  int tiles = (Lmax + kTile - 1) / kTile;
+  int cap = (tiles + 3) / 4;  // at least 4 tiles per split
+  if (cap > 256) cap = 256;
+  return cap < 1 ? 1 : cap;
+}
+
+// Pick the split count so that (units x groups x splits) CTAs, one per SM,
+// fill whole waves with at least 4 tiles per CTA.
+int verify_splits(int ug, int Lmax, int sms) {
+  const int cap = verify_splits_cap(Lmax);
+  int best = 1;
+  double best_eff = -1.0;
+  for (int waves = 1; waves <= 16; ++waves) {
+    int s = (waves * sms + ug / 2) / ug;
+    if (s < 1) s = 1;
+    if (s > cap) s = cap;
+    const long long ctas = (long long)ug * s;
+    const long long full = (ctas + sms - 1) / sms * sms;
+    const double eff = (double)ctas / (double)full;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
+    if (eff > 0.97) break;
+  }
+  return best;
+}
+
+size_t verify_ws(int units, int rows_all, int Lmax) {
+  const int ngroups = (rows_all + kMaxRows - 1) / kMaxRows;
+  const size_t ug = (size_t)units * ngroups;
+  const size_t cap = (size_t)verify_splits_cap(Lmax);
+  return 256 + align_up(ug * sizeof(int), 256) + align_up(ug * cap * kMaxRows * 2 * sizeof(float), 256) +
+         ug * cap * kMaxRows * kHeadDim * sizeof(float);
+}
+
+template <int NPAD>
+tf_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParams& p, dim3 grid,
+                 cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(verify_umma_kernel<NPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Smem<NPAD>::kDynamic) != cudaSuccess)
+      return TF_ERR_CUDA;
+    configured = true;
+  }
+  verify_umma_kernel<NPAD><<<grid, kThreads, Smem<NPAD>::kDynamic, stream>>>(mk, mv, p);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace tf
 
 extern "C" size_t tf_verify_attn_workspace(int B, int Hq, int Hkv, int Lmax, int T) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lmax <= 0 || T <= 0 || Hq % Hkv) return 0;
-  return tf::gather_workspace(B * Hkv, (Hq / Hkv) * T, Lmax);
+  return tf::verify_ws(B * Hkv, (Hq / Hkv) * T, Lmax);
 }
 
 extern "C" tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
@@ -19,10 +507,35 @@ extern "C" tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const 
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || Hq % Hkv || T < 1) return TF_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return TF_ERR_INVALID_ARG;
   if (D != kHeadDim || T > 16) return TF_ERR_UNSUPPORTED;
-  if (B == 0) return TF_OK;
-  GatherParams p{};
-  p.q = Q; p.K = K; p.V = V; p.seq_lens = seq_lens;
-  p.Hq = Hq; p.Hkv = Hkv; p.Lmax = Lmax; p.T = T;
-  p.scale_log2 = scale * kLog2e; p.out = out;
-  return gather_launch(kModePrefix, p, B * Hkv, (Hq / Hkv) * T, Lmax, ws, ws_bytes, stream);
+  if (B == 0 || Lmax == 0) return TF_OK;
+  const long long rows_total = (long long)B * Hkv * Lmax;
+  if (rows_total >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
+  const size_t need = verify_ws(B * Hkv, (Hq / Hkv) * T, Lmax);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
+  CUtensorMap mk, mv;
+  if (!make_kv_map(&mk, K, rows_total) || !make_kv_map(&mv, V, rows_total)) return TF_ERR_CUDA;
+
+  VerifyParams p{};
+  const int rows_all = (Hq / Hkv) * T;
+  p.Q = Q;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Lmax = Lmax;
+  p.T = T;
+  p.ngroups = (rows_all + kMaxRows - 1) / kMaxRows;
+  p.splits_cap = verify_splits_cap(Lmax);
+  const int ug = B * Hkv * p.ngroups;
+  p.splits = verify_splits(ug, Lmax, num_sms());
+  p.scale_log2 = scale * kLog2e;
+  char* w = static_cast<char*>(ws);
+  p.status = reinterpret_cast<int*>(w);
+  p.tickets = reinterpret_cast<int*>(w + 256);
+  p.part_ml = reinterpret_cast<float*>(w + 256 + align_up((size_t)ug * sizeof(int), 256));
+  p.part_o = reinterpret_cast<float*>(w + 256 + align_up((size_t)ug * sizeof(int), 256) +
+                                      align_up((size_t)ug * p.splits_cap * kMaxRows * 2 * sizeof(float), 256));
+  dim3 grid(p.splits, ug);
+  const int rows_max = rows_all < kMaxRows ? rows_all : kMaxRows;
+  return rows_max <= 16 ? launch<16>(mk, mv, p, grid, stream) : launch<32>(mk, mv, p, grid, stream);
 }

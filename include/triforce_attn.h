@@ -167,9 +167,16 @@ TF_API tf_status tf_stream_window_attn(const uint16_t* q, const uint16_t* K, con
  * L-T .. L-1 and the candidates form a chain, so verify query j (0 <= j < T)
  * attends to positions [0, L - T + j]:
  *   out[b,h,j,:] = softmax(scale * Q[b,h,j] . K_{0..L-T+j}) V_{0..L-T+j}
- * Rows with no visible position (L - T + j < 0) are zero.  1 <= T <= 16.
+ * Rows with no visible position (L - T + j < 0) are zero.  1 <= T <= 16;
+ * B * Hkv * Lmax < 2^31.  Tensor-core kernel: K and V tiles stream in by TMA,
+ * S = K Q^T and O = P V run as tcgen05 MMAs (bf16 in, fp32 accumulate; the
+ * softmax weights P are rounded to bf16 and the row sums use the same rounded
+ * weights).
  *   out [B, Hq, T, D] float32
- * Workspace: tf_verify_attn_workspace(B, Hq, Hkv, Lmax, T) bytes.
+ * Workspace: tf_verify_attn_workspace(B, Hq, Hkv, Lmax, T) bytes.  Its first
+ * int32 is a status word: nonzero means a pipeline wait timed out (which only a
+ * hardware fault can cause) and the output is invalid; re-zero the workspace
+ * before reusing it.
  */
 TF_API size_t tf_verify_attn_workspace(int B, int Hq, int Hkv, int Lmax, int T);
 TF_API tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V,

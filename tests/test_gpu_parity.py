@@ -215,8 +215,24 @@ def test_stream_window_attn(cuda_lib, w):
                          ids=["tiny", "ragged-gqa", "mha-6", "llama2-7b-32k-1layer"])
 def test_verify_attn(cuda_lib, w):
     c = make_case(w, fill_invalid=float("nan") if w.ragged else None)
-    out = cuda_lib.tf_verify_attn(c["Q"], c["K"], c["V"], c["seq"], scale_for(w.D))
-    want = O.verify_attn(bits(c["Q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), c["seq_cpu"].numpy(), scale_for(w.D))
+    ws = cuda_lib.workspace(cuda_lib.tf_verify_attn_workspace(w.B, w.Hq, w.Hkv, w.L, w.T), "cuda")
+    for _ in range(2):  # a second call on the same workspace (tickets reset by the first)
+        out = cuda_lib.tf_verify_attn(c["Q"], c["K"], c["V"], c["seq"], scale_for(w.D), ws=ws)
+        torch.cuda.synchronize()
+        assert int(ws[:4].view(torch.int32).item()) == 0, "pipeline status word set"
+        want = O.verify_attn(bits(c["Q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), c["seq_cpu"].numpy(),
+                             scale_for(w.D))
+        assert np.abs(out.cpu().double().numpy() - want).max() <= ATOL
+
+
+@pytest.mark.parametrize("G,T", [(1, 1), (1, 16), (2, 16), (8, 4), (4, 9)], ids=lambda v: str(v))
+def test_verify_row_groups(cuda_lib, G, T):
+    """Query-row groups: N = G * T padded to 16 or 32, and more than 32 rows split
+    into several groups per KV head."""
+    w = small_workload(B=1, Hq=2 * G, Hkv=2, T=T, L=700, ragged=False)
+    c = make_case(w)
+    out = cuda_lib.tf_verify_attn(c["Q"], c["K"], c["V"], c["seq"], 0.09)
+    want = O.verify_attn(bits(c["Q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), c["seq_cpu"].numpy(), 0.09)
     assert np.abs(out.cpu().double().numpy() - want).max() <= ATOL
 
 
