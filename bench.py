@@ -69,15 +69,23 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """Largest value over all ranks (the slowest replica sets the job time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(steps, elapsed_local_s, world, device="cuda"):
+    """Whole-job steps/s: every rank runs `steps` steps of its own replica; the
+    job ends when the slowest rank does.  Returns (steps/s, max elapsed)."""
+    el = max_over_ranks(elapsed_local_s, world, device)
+    return world * steps / el, el
 
 
 class ClockSampler:
@@ -146,9 +154,9 @@ def kernel_source_hash(name):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_file):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel (else None)."""
+def recorded_traffic(kernel_file, workload):
+    """DRAM bytes per launch of the kernel on this workload from the committed ncu
+    summary, if it was taken on the current source of the kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
@@ -156,8 +164,8 @@ def recorded_traffic(kernel_file):
     with open(path) as f:
         for line in f:
             parts = line.split()
-            if len(parts) >= 3 and parts[0] == kernel_file and parts[1] == want:
-                return float(parts[2])
+            if len(parts) >= 4 and parts[0] == kernel_file and parts[1] == want and parts[2] == workload:
+                return float(parts[3])
     return None
 
 
@@ -308,8 +316,7 @@ def run_gpu(args):
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
-    elapsed_s = t_start.elapsed_time(t_end) / 1e3
-    elapsed_s = max_over_ranks(elapsed_s, world)
+    value, elapsed_s = job_throughput(args.steps, t_start.elapsed_time(t_end) / 1e3, world)
     per_kind = {k: [] for k in kinds}
     for s in range(args.steps):
         for l in range(layers):
@@ -338,9 +345,8 @@ def run_gpu(args):
                                              "GBps": round(means_bytes / (means_ms / 1e3) / 1e9, 1)}
     ver_ms = statistics.mean(per_kind["verify"])
     achieved = bytes_verify / (ver_ms / 1e3) / 1e9
-    traffic = recorded_traffic("verify_attn.cu")
+    traffic = recorded_traffic("verify_attn.cu", w.name)
 
-    value = world * args.steps / elapsed_s
     result = {
         "metric": METRIC, "value": round(value, 4), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(elapsed_s / args.steps * 1e3, 4), "higher_is_better": True,
@@ -355,6 +361,34 @@ def run_gpu(args):
         "gpu_launches": args.steps * layers * 4,
         "clocks": clocks.summary(),
     }
+
+    # ---- accept / resample (latency-bound; reported in microseconds per call):
+    # the two-level step of a batch of 8 over vocabulary 32000, gamma 4 then 5.
+    acc = synth.two_level_inputs(8, 4, w.vocab, seed=4, device=dev)
+    q_lvl1 = acc["q"][:, :5].contiguous()
+    ws_a1 = tf.workspace(tf.tf_spec_accept_workspace(8, 4), dev)
+    ws_a2 = tf.workspace(tf.tf_spec_accept_workspace(8, 5), dev)
+    outs1 = [torch.empty(8, dtype=torch.int32, device=dev) for _ in range(2)] + [
+        torch.empty((8, 5), dtype=torch.int32, device=dev)]
+    outs2 = [torch.empty(8, dtype=torch.int32, device=dev) for _ in range(2)] + [
+        torch.empty((8, 6), dtype=torch.int32, device=dev)]
+
+    def two_level():
+        tf.tf_spec_accept(q_lvl1, acc["r"], acc["x"], acc["u1"], acc["ur1"], n_acc=outs1[0], next_token=outs1[1],
+                          out_tokens=outs1[2], ws=ws_a1)
+        tf.tf_spec_accept(acc["p"], acc["q"], outs1[2], acc["u2"], acc["ur2"], n_acc=outs2[0], next_token=outs2[1],
+                          out_tokens=outs2[2], ws=ws_a2)
+    for _ in range(3):
+        two_level()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(20):
+        two_level()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    kernels["spec_accept_two_level_b8_v32000"] = {"us_per_step": round(a0.elapsed_time(a1) / 20 * 1e3, 2),
+                                                  "launches_per_step": 4}
 
     # ---- end to end through the public API with host buffers
     if not args.no_e2e:
@@ -374,8 +408,8 @@ def run_gpu(args):
             for h, d in zip(outs_host, (o_sp, o_win, o_ver)):
                 h.copy_(d, non_blocking=True)
             torch.cuda.current_stream().synchronize()
-        e_s = max_over_ranks(time.perf_counter() - t0, world)
-        result["e2e"] = {"value": round(world * e_steps / e_s, 4), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+        e_value, _ = job_throughput(e_steps, time.perf_counter() - t0, world)
+        result["e2e"] = {"value": round(e_value, 4), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                          "d2h_bytes_per_step": d2h}
 
     if rank == 0 and not args.no_cpu_baseline and world == 1:

@@ -37,7 +37,8 @@ _SIGS = {
     "tf_stream_window_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_verify_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
     "tf_verify_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
-    "tf_spec_accept": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P]),
+    "tf_spec_accept_workspace": (_S, [_I, _I]),
+    "tf_spec_accept": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _S, _P]),
 }
 
 
@@ -241,8 +242,12 @@ def tf_verify_attn(Q, K, V, seq_lens, scale, out=None, ws=None, stream=None):
     return out
 
 
+def tf_spec_accept_workspace(B, gamma):
+    return int(load().tf_spec_accept_workspace(B, gamma))
+
+
 def tf_spec_accept(tgt_logits, drf_logits, drf_tokens, u_acc, u_res, temperature=1.0, n_acc=None, next_token=None,
-                   out_tokens=None, stream=None):
+                   out_tokens=None, ws=None, stream=None):
     _need(tgt_logits, torch.float32, "tgt_logits", 3)
     B, g1, Vn = tgt_logits.shape
     gamma = g1 - 1
@@ -260,8 +265,9 @@ def tf_spec_accept(tgt_logits, drf_logits, drf_tokens, u_acc, u_res, temperature
         next_token = torch.empty((B,), dtype=torch.int32, device=dev)
     if out_tokens is None:
         out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    ws, nbytes = _ws(ws, tf_spec_accept_workspace(B, gamma), dev)
     _check(load().tf_spec_accept(_ptr(tgt_logits), _ptr(drf_logits if gamma > 0 else None),
                                  _ptr(drf_tokens if gamma > 0 else None), _ptr(u_acc if gamma > 0 else None),
                                  _ptr(u_res), B, gamma, Vn, float(temperature), _ptr(n_acc), _ptr(next_token),
-                                 _ptr(out_tokens), _stream(stream)), "tf_spec_accept")
+                                 _ptr(out_tokens), _ptr(ws), nbytes, _stream(stream)), "tf_spec_accept")
     return n_acc, next_token, out_tokens

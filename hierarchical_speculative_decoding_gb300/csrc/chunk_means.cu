@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(256) chunk_means_kernel(const uint16_t* __rest
                                                           int Hkv, int Lmax, int c_begin, int n_chunks,
                                                           long long total, uint16_t* __restrict__ M) {
   const int Cmax = (Lmax + kChunk - 1) / kChunk;
+  pdl_wait();
   for (long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x; item < total;
        item += (long long)gridDim.x * blockDim.x) {
     const int slice = (int)(item & 15);
@@ -128,6 +129,8 @@ extern "C" tf_status tf_build_chunk_means(const uint16_t* K, const int32_t* seq_
   long long blocks = (total + threads - 1) / threads;
   const long long cap = (long long)num_sms() * 8;
   if (blocks > cap) blocks = cap;
-  chunk_means_kernel<<<(unsigned)blocks, threads, 0, stream>>>(K, seq_lens, Hkv, Lmax, c_begin, n_chunks, total, M);
+  if (launch_pdl(chunk_means_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, K, seq_lens, Hkv, Lmax,
+                 c_begin, n_chunks, total, M) != cudaSuccess)
+    return TF_ERR_CUDA;
   return launch_status();
 }

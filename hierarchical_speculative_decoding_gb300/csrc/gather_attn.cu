@@ -6,203 +6,267 @@
 //     blocks retrieved by key-query similarity (the selected chunk list);
 //   Force 1 (streaming drafter): attention sinks plus the most recent window.
 // Both are one query token per head attending to a small, irregular subset of
-// a long cache, so both run through one kernel parameterised by how a
-// "virtual row" (the i-th position of the set) maps to a cache position.
+// a long cache.  Both are served by one kernel whose unit of work is an 8-row
+// "chunk" of K and V: a selected chunk id, or a piece of the sink / window
+// ranges (the sinks form one chunk, the window is cut into 8-row pieces).
 //
-// Design (HBM-bound, ~1 flop/byte): split-K over the position set.  Each warp
-// walks groups of 8 virtual rows; a half-warp owns a row and each lane reads 16
-// bytes (8 head dims) of K and of V with L1-bypassing vector loads, so one
-// load instruction moves 2 x 256 contiguous bytes and each lane keeps 8 loads
-// in flight.  Scores are reduced over the half-warp with 4 shuffles, the
-// online softmax runs in the log2 domain in fp32, warps merge in shared
-// memory, and splits merge with the log-sum-exp identity in the last CTA of
-// each unit to finish (atomic ticket, no waiting).
+// Design (HBM-bound, ~1 flop/byte; latency matters because a layer moves only
+// 64 MiB): split-K over the chunk list.  A producer warp stages chunks into a
+// 16-slot shared-memory ring with untiled bulk copies (cp.async.bulk: a chunk's
+// K rows and V rows are each one contiguous run of n x 256 bytes; mbarrier
+// complete-tx), 32 chunk ids resolved per batch so no copy waits on an id.
+// Four compute warps take chunks in turn: lane (row r, quarter dq) forms
+// 32-dim partial dot products, visiting its four 16-byte pieces in a rotated
+// order that keeps the shared-memory reads conflict-free; the row score is
+// reduced over the 4 quarters, the online softmax runs in the log2 domain in
+// fp32, and for P V each lane owns 4 head dims across all rows.  Warps merge in
+// shared memory; splits merge with the log-sum-exp identity in the last CTA of
+// each unit to finish (atomic ticket, no waiting).  All waits are bounded; a
+// timeout (only a hardware fault can cause one) leaves NaN in the outputs.
 #include "gather_attn.cuh"
+#include "sm100_ptx.cuh"
 
 namespace tf {
 
+using namespace sm100;
+
+constexpr int kComputeWarps = 4;
+constexpr int kSlots = 16;
+constexpr int kSlotBytes = 4096;  // K rows [0, 2 KB), V rows [2 KB, 4 KB)
+constexpr int kGatherSmem = kSlots * kSlotBytes + 128;  // + alignment slack
+
+// The i-th chunk of a unit's position set: first position y and valid rows n.
+template <int MODE>
+__device__ __forceinline__ void chunk_at(int e, const int32_t* sel, int C, int L, int has_sink, int ns_eff, int w0,
+                                         int& y, int& n) {
+  if (MODE == kModeChunks) {
+    const int c = sel[e];
+    const bool ok = c >= 0 && c < C;
+    y = ok ? c * kChunk : 0;
+    n = ok ? min(kChunk, L - c * kChunk) : 0;
+  } else {
+    if (has_sink && e == 0) {
+      y = 0;
+      n = ns_eff;
+    } else {
+      y = w0 + (e - has_sink) * kChunk;
+      n = min(kChunk, L - y);
+    }
+  }
+}
+
 template <int NQ, int MODE>
-__global__ void __launch_bounds__(kGatherThreads) gather_attn_kernel(GatherParams p) {
-  constexpr int kW = kGatherThreads / 32;
-  __shared__ float sm_m[kW][NQ], sm_l[kW][NQ];
-  __shared__ float sm_o[kW][NQ][kHeadDim];
-  __shared__ int s_last;
+__global__ void __launch_bounds__(kGatherThreads, 1) gather_attn_kernel(GatherParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[kSlots], bar_empty[kSlots];
+  __shared__ int slot_n[kSlots];
+  __shared__ float sm_m[kComputeWarps][NQ], sm_l[kComputeWarps][NQ];
+  __shared__ float sm_o[kComputeWarps][NQ][kHeadDim];
+  __shared__ int s_last, s_abort;
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
   const int unit_grp = blockIdx.y;
   const int unit = unit_grp / p.ngroups, grp = unit_grp % p.ngroups;
   const int b = unit / p.Hkv, g = unit % p.Hkv;
   const int G = p.Hq / p.Hkv;
-  const int rows = G * p.T;
-  const int L = clamp_len(p.seq_lens[b], p.Lmax);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sub = lane >> 4, l16 = lane & 15;
+  const int rows = G - grp * NQ < NQ ? G - grp * NQ : NQ;  // heads of this group
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  const int L = clamp_len(p.seq_lens[b], p.Lmax);
+  const int C = (L + kChunk - 1) / kChunk;
 
-  // ---- the position set of this unit
-  int P = 0, ns_eff = 0, w0 = 0, nsel = 0;
+  // ---- this CTA's slice of the unit's chunk list.  For the chunk list the
+  // slice bounds come from kc alone, so the ids and n_sel load together.
+  int nch = 0, ns_eff = 0, w0 = 0, has_sink = 0, per = 0;
   const int32_t* sel = nullptr;
   if (MODE == kModeChunks) {
-    nsel = p.n_sel[unit];
-    nsel = nsel < 0 ? 0 : (nsel > p.kc ? p.kc : nsel);
     sel = p.idx + (size_t)unit * p.kc;
-    P = nsel * kChunk;
+    per = (p.kc + p.splits - 1) / p.splits;
+    nch = p.n_sel[unit];
+    nch = nch < 0 ? 0 : (nch > p.kc ? p.kc : nch);
   } else {
     ns_eff = min(p.n_sink, L);
     w0 = max(p.n_sink, L - p.window);
-    P = ns_eff + max(0, L - w0);
+    has_sink = ns_eff > 0 ? 1 : 0;
+    nch = has_sink + (max(0, L - w0) + kChunk - 1) / kChunk;
+    per = (nch + p.splits - 1) / p.splits;
   }
-  const int C = (L + kChunk - 1) / kChunk;
+  const int e0 = blockIdx.x * per;
+  const int cnt = max(0, min(nch, e0 + per) - e0);
 
-  // ---- this CTA's query rows: r = hh * T + j, head h = g * G + hh
-  float qv[NQ][8];
-  int lim[NQ];
-  bool row_on[NQ];
+  if (warp == kComputeWarps) {
+    // ---------------------------------------------------------------- producer
+    const uint16_t* Ku = p.K + (size_t)unit * p.Lmax * kHeadDim;
+    const uint16_t* Vu = p.V + (size_t)unit * p.Lmax * kHeadDim;
+    for (int base = 0; base < cnt; base += 32) {
+      int y = 0, n = 0;
+      if (base + lane < cnt) chunk_at<MODE>(e0 + base + lane, sel, C, L, has_sink, ns_eff, w0, y, n);
+      const int m = min(32, cnt - base);
+      for (int i = 0; i < m; ++i) {
+        const int yi = __shfl_sync(0xffffffffu, y, i);
+        const int ni = __shfl_sync(0xffffffffu, n, i);
+        if (lane == 0 && !s_abort) {
+          const int k = base + i, slot = k % kSlots;
+          if (k >= kSlots && !mbar_wait(&bar_empty[slot], ((k / kSlots) - 1) & 1)) {
+            atomicExch(&s_abort, 1);
+          } else {
+            slot_n[slot] = ni;
+            uint8_t* dst = ring + slot * kSlotBytes;
+            const uint32_t bytes = (uint32_t)ni * kHeadDim * 2;
+            mbar_arrive_expect_tx(&bar_full[slot], 2 * bytes);
+            if (ni > 0) {
+              bulk_load(dst, Ku + (size_t)yi * kHeadDim, bytes, &bar_full[slot]);
+              bulk_load(dst + 2048, Vu + (size_t)yi * kHeadDim, bytes, &bar_full[slot]);
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- compute warps
+    // Score phase: lane = (row r, quarter dq) reads 16-byte pieces j of dims
+    // [32 dq, 32 dq + 32) in the rotated order jr(j) (conflict-free banks).
+    const int r = lane >> 2, dq = lane & 3;
+    const int rot = (dq >> 1) + 2 * (r & 1);
+    float qv[NQ][32];
 #pragma unroll
-  for (int r = 0; r < NQ; ++r) {
-    const int rr = grp * NQ + r;
-    row_on[r] = rr < rows;
-    const int hh = row_on[r] ? rr / p.T : 0, j = row_on[r] ? rr % p.T : 0;
-    lim[r] = row_on[r] ? 0x7fffffff : -1;
-    const uint16_t* qrow = p.q + (((size_t)b * p.Hq + (size_t)g * G + hh) * p.T + j) * kHeadDim + l16 * 8;
-    float f[8];
-    unpack8(row_on[r] ? *reinterpret_cast<const uint4*>(qrow) : make_uint4(0, 0, 0, 0), f);
+    for (int h = 0; h < NQ; ++h) {
+      const bool on = h < rows;
+      const uint16_t* qrow = p.q + ((size_t)b * p.Hq + (size_t)g * G + grp * NQ + (on ? h : 0)) * kHeadDim + dq * 32;
 #pragma unroll
-    for (int d = 0; d < 8; ++d) qv[r][d] = f[d] * p.scale_log2;
-  }
-
-  // ---- split range over virtual rows (whole groups of 8)
-  int vper = (P + p.splits - 1) / p.splits;
-  vper = (vper + 7) & ~7;
-  const int v_begin = blockIdx.x * vper;
-  const int v_end = min(P, v_begin + vper);
-
-  float m[NQ], l[NQ], o[NQ][8];
+      for (int j = 0; j < 4; ++j) {
+        const int jr = (j + rot) & 3;
+        float f[8];
+        unpack8(on ? *reinterpret_cast<const uint4*>(qrow + jr * 8) : make_uint4(0, 0, 0, 0), f);
 #pragma unroll
-  for (int r = 0; r < NQ; ++r) {
-    m[r] = -INFINITY;
-    l[r] = 0.0f;
+        for (int d = 0; d < 8; ++d) qv[h][j * 8 + d] = f[d] * p.scale_log2;
+      }
+    }
+    float m[NQ], l[NQ], o[NQ][4];
 #pragma unroll
-    for (int d = 0; d < 8; ++d) o[r][d] = 0.0f;
-  }
-
-  const size_t kv_base = (size_t)unit * p.Lmax;
-  for (int gv = v_begin + warp * 8; gv < v_end; gv += kW * 8) {
-    uint4 kr[4], vr[4];
-    int pos[4];
-    bool ok[4];
+    for (int h = 0; h < NQ; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int v = gv + sub + 2 * i;
-      int t = -1;
-      if (v < v_end) {
-        if (MODE == kModeChunks) {
-          const int c = sel[v >> 3];
-          t = (c >= 0 && c < C) ? c * kChunk + (v & 7) : -1;
-          if (t >= L) t = -1;
-        } else {
-          t = (v < ns_eff) ? v : w0 + (v - ns_eff);
+      for (int i = 0; i < 4; ++i) o[h][i] = 0.0f;
+    }
+    for (int k = warp; k < cnt; k += kComputeWarps) {
+      const int slot = k % kSlots;
+      if (!mbar_wait(&bar_full[slot], (k / kSlots) & 1)) {
+        if (lane == 0) atomicExch(&s_abort, 1);
+        break;
+      }
+      const int n = slot_n[slot];
+      const uint8_t* kb = ring + slot * kSlotBytes;
+      const uint8_t* vb = kb + 2048;
+      float s[NQ], s4[NQ][4];  // four independent partial sums per head (short FMA chains)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int jr = (j + rot) & 3;
+        const uint4 kv = *reinterpret_cast<const uint4*>(kb + r * 256 + dq * 64 + jr * 16);
+        float f[8];
+        unpack8(kv, f);
+#pragma unroll
+        for (int h = 0; h < NQ; ++h) {
+          float a = qv[h][j * 8] * f[0];
+#pragma unroll
+          for (int d = 1; d < 8; ++d) a = fmaf(qv[h][j * 8 + d], f[d], a);
+          s4[h][j] = a;
         }
       }
-      pos[i] = t;
-      ok[i] = t >= 0;
-      const size_t off = (kv_base + (size_t)(ok[i] ? t : 0)) * kHeadDim + l16 * 8;
-      kr[i] = ok[i] ? ld_stream16(p.K + off) : make_uint4(0, 0, 0, 0);
-      vr[i] = ok[i] ? ld_stream16(p.V + off) : make_uint4(0, 0, 0, 0);
-    }
-    float s[4][NQ];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float kf[8];
-      unpack8(kr[i], kf);
+      for (int h = 0; h < NQ; ++h) s[h] = (s4[h][0] + s4[h][1]) + (s4[h][2] + s4[h][3]);
+      const bool valid = r < n;
 #pragma unroll
-      for (int r = 0; r < NQ; ++r) {
-        float a = 0.0f;
-#pragma unroll
-        for (int d = 0; d < 8; ++d) a = fmaf(qv[r][d], kf[d], a);
-        a += __shfl_xor_sync(0xffffffffu, a, 8);
-        a += __shfl_xor_sync(0xffffffffu, a, 4);
-        a += __shfl_xor_sync(0xffffffffu, a, 2);
-        a += __shfl_xor_sync(0xffffffffu, a, 1);
-        s[i][r] = (ok[i] && pos[i] <= lim[r]) ? a : -INFINITY;
+      for (int h = 0; h < NQ; ++h) {
+        s[h] += __shfl_xor_sync(0xffffffffu, s[h], 1);
+        s[h] += __shfl_xor_sync(0xffffffffu, s[h], 2);
+        s[h] = valid ? s[h] : -INFINITY;
       }
-    }
-    float vf[4][8];
+      float pr[NQ];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) unpack8(vr[i], vf[i]);
+      for (int h = 0; h < NQ; ++h) {
+        float cm = s[h];
+        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
+        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
+        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
+        const float mn = fmaxf(m[h], cm);
+        const float alpha = merge_scale(m[h], mn);
+        pr[h] = (s[h] == -INFINITY) ? 0.0f : exp2f(s[h] - mn);
+        float ps = pr[h];
+        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+        l[h] = l[h] * alpha + ps;
+        m[h] = mn;
 #pragma unroll
-    for (int r = 0; r < NQ; ++r) {
-      const float mx = fmaxf(fmaxf(s[0][r], s[1][r]), fmaxf(s[2][r], s[3][r]));
-      const float mn = fmaxf(m[r], mx);
-      if (mn == -INFINITY) continue;
-      const float alpha = merge_scale(m[r], mn);
-      float pr[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) pr[i] = exp2f(s[i][r] - mn);
-      l[r] = l[r] * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
-#pragma unroll
-      for (int d = 0; d < 8; ++d) {
-        float acc = o[r][d] * alpha;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc = fmaf(pr[i], vf[i][d], acc);
-        o[r][d] = acc;
+        for (int i = 0; i < 4; ++i) o[h][i] *= alpha;
       }
-      m[r] = mn;
+      // P V: lane owns head dims [4 lane, 4 lane + 4) of every row
+      for (int rr = 0; rr < n; ++rr) {
+        const uint2 vv = *reinterpret_cast<const uint2*>(vb + rr * 256 + lane * 8);
+        const float v0 = __uint_as_float(vv.x << 16), v1 = __uint_as_float(vv.x & 0xffff0000u);
+        const float v2 = __uint_as_float(vv.y << 16), v3 = __uint_as_float(vv.y & 0xffff0000u);
+#pragma unroll
+        for (int h = 0; h < NQ; ++h) {
+          const float pw = __shfl_sync(0xffffffffu, pr[h], rr * 4);  // lane 4 rr holds row rr
+          o[h][0] = fmaf(pw, v0, o[h][0]);
+          o[h][1] = fmaf(pw, v1, o[h][1]);
+          o[h][2] = fmaf(pw, v2, o[h][2]);
+          o[h][3] = fmaf(pw, v3, o[h][3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_empty[slot]);
     }
-  }
-
-  // ---- merge the two half-warps (different rows, same query rows)
 #pragma unroll
-  for (int r = 0; r < NQ; ++r) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m[r], 16);
-    const float l2 = __shfl_xor_sync(0xffffffffu, l[r], 16);
-    const float mn = fmaxf(m[r], m2);
-    const float a1 = merge_scale(m[r], mn), a2 = merge_scale(m2, mn);
-    l[r] = l[r] * a1 + l2 * a2;
-#pragma unroll
-    for (int d = 0; d < 8; ++d) {
-      const float o2 = __shfl_xor_sync(0xffffffffu, o[r][d], 16);
-      o[r][d] = o[r][d] * a1 + o2 * a2;
-    }
-    m[r] = mn;
-  }
-  if (sub == 0) {
-#pragma unroll
-    for (int r = 0; r < NQ; ++r) {
-      if (l16 == 0) {
-        sm_m[warp][r] = m[r];
-        sm_l[warp][r] = l[r];
+    for (int h = 0; h < NQ; ++h) {
+      if (lane == 0) {
+        sm_m[warp][h] = m[h];
+        sm_l[warp][h] = l[h];
       }
 #pragma unroll
-      for (int d = 0; d < 8; ++d) sm_o[warp][r][l16 * 8 + d] = o[r][d];
+      for (int i = 0; i < 4; ++i) sm_o[warp][h][lane * 4 + i] = o[h][i];
     }
   }
   __syncthreads();
 
-  // ---- merge warps: thread handles (r, d) pairs
-  const int out_rows = min(NQ, rows - grp * NQ);
+  // ---- merge the compute warps: thread handles (h, d) pairs
+  const bool bad = s_abort != 0;
   float* part_ml = p.part_ml + ((size_t)unit_grp * p.splits_cap + blockIdx.x) * NQ * 2;
   float* part_o = p.part_o + ((size_t)unit_grp * p.splits_cap + blockIdx.x) * NQ * kHeadDim;
-  for (int pr = threadIdx.x; pr < out_rows * kHeadDim; pr += kGatherThreads) {
-    const int r = pr / kHeadDim, d = pr % kHeadDim;
+  for (int e = threadIdx.x; e < rows * kHeadDim; e += kGatherThreads) {
+    const int h = e / kHeadDim, d = e % kHeadDim;
     float mx = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kW; ++w) mx = fmaxf(mx, sm_m[w][r]);
+    for (int w = 0; w < kComputeWarps; ++w) mx = fmaxf(mx, sm_m[w][h]);
     float ls = 0.0f, os = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kW; ++w) {
-      const float f = merge_scale(sm_m[w][r], mx);
-      ls = fmaf(f, sm_l[w][r], ls);
-      os = fmaf(f, sm_o[w][r][d], os);
+    for (int w = 0; w < kComputeWarps; ++w) {
+      const float f = merge_scale(sm_m[w][h], mx);
+      ls = fmaf(f, sm_l[w][h], ls);
+      os = fmaf(f, sm_o[w][h][d], os);
     }
+    if (bad) os = NAN;
     if (p.splits == 1) {
-      const int rr = grp * NQ + r;
-      const int hh = rr / p.T, j = rr % p.T;
-      p.out[(((size_t)b * p.Hq + (size_t)g * G + hh) * p.T + j) * kHeadDim + d] = (ls > 0.0f) ? os / ls : 0.0f;
+      p.out[((size_t)b * p.Hq + (size_t)g * G + grp * NQ + h) * kHeadDim + d] =
+          (ls > 0.0f) ? os / ls : (bad ? NAN : 0.0f);
     } else {
       if (d == 0) {
-        part_ml[r * 2 + 0] = mx;
-        part_ml[r * 2 + 1] = ls;
+        part_ml[h * 2 + 0] = mx;
+        part_ml[h * 2 + 1] = ls;
       }
-      part_o[r * kHeadDim + d] = os;
+      part_o[h * kHeadDim + d] = os;
     }
   }
   if (p.splits == 1) return;
@@ -216,19 +280,17 @@ __global__ void __launch_bounds__(kGatherThreads) gather_attn_kernel(GatherParam
 
   const float* ml0 = p.part_ml + (size_t)unit_grp * p.splits_cap * NQ * 2;
   const float* o0 = p.part_o + (size_t)unit_grp * p.splits_cap * NQ * kHeadDim;
-  for (int pr = threadIdx.x; pr < out_rows * kHeadDim; pr += kGatherThreads) {
-    const int r = pr / kHeadDim, d = pr % kHeadDim;
+  for (int e = threadIdx.x; e < rows * kHeadDim; e += kGatherThreads) {
+    const int h = e / kHeadDim, d = e % kHeadDim;
     float mx = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) mx = fmaxf(mx, __ldcg(ml0 + ((size_t)s * NQ + r) * 2));
+    for (int s = 0; s < p.splits; ++s) mx = fmaxf(mx, __ldcg(ml0 + ((size_t)s * NQ + h) * 2));
     float ls = 0.0f, os = 0.0f;
     for (int s = 0; s < p.splits; ++s) {
-      const float f = merge_scale(__ldcg(ml0 + ((size_t)s * NQ + r) * 2), mx);
-      ls = fmaf(f, __ldcg(ml0 + ((size_t)s * NQ + r) * 2 + 1), ls);
-      os = fmaf(f, __ldcg(o0 + ((size_t)s * NQ + r) * kHeadDim + d), os);
+      const float f = merge_scale(__ldcg(ml0 + ((size_t)s * NQ + h) * 2), mx);
+      ls = fmaf(f, __ldcg(ml0 + ((size_t)s * NQ + h) * 2 + 1), ls);
+      os = fmaf(f, __ldcg(o0 + ((size_t)s * NQ + h) * kHeadDim + d), os);
     }
-    const int rr = grp * NQ + r;
-    const int hh = rr / p.T, j = rr % p.T;
-    p.out[(((size_t)b * p.Hq + (size_t)g * G + hh) * p.T + j) * kHeadDim + d] = (ls > 0.0f) ? os / ls : 0.0f;
+    p.out[((size_t)b * p.Hq + (size_t)g * G + grp * NQ + h) * kHeadDim + d] = (ls > 0.0f) ? os / ls : 0.0f;
   }
   if (threadIdx.x == 0) p.tickets[unit_grp] = 0;
 }
@@ -238,13 +300,14 @@ __global__ void __launch_bounds__(kGatherThreads) gather_attn_kernel(GatherParam
 int gather_nq(int rows) {
   if (rows <= 1) return 1;
   if (rows <= 2) return 2;
-  if (rows <= 4) return 4;
-  if (rows <= 6) return 6;
-  return 8;
+  return 4;
 }
 
+// Chunk-list length bound: P_max positions in 8-row chunks plus the sink chunk.
+static int gather_max_chunks(int P_max) { return (P_max + kChunk - 1) / kChunk + 1; }
+
 int gather_splits_cap(int P_max) {
-  int s = (P_max + 63) / 64;
+  int s = (gather_max_chunks(P_max) + 3) / 4;  // at least 4 chunks per split
   if (s > 256) s = 256;
   return s < 1 ? 1 : s;
 }
@@ -258,40 +321,53 @@ size_t gather_workspace(int units, int rows, int P_max) {
          ug * cap * nq * kHeadDim * sizeof(float);
 }
 
-template <int NQ>
-static void launch_nq(int mode, const GatherParams& p, dim3 grid, cudaStream_t s) {
-  switch (mode) {
-    case kModeChunks: gather_attn_kernel<NQ, kModeChunks><<<grid, kGatherThreads, 0, s>>>(p); break;
-    default: gather_attn_kernel<NQ, kModeWindow><<<grid, kGatherThreads, 0, s>>>(p); break;
+template <int NQ, int MODE>
+static int configure() {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    if (cudaFuncSetAttribute(gather_attn_kernel<NQ, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kGatherSmem) != cudaSuccess)
+      return 0;
+    per_sm = occupancy_blocks((const void*)gather_attn_kernel<NQ, MODE>, kGatherThreads, kGatherSmem);
   }
+  return per_sm;
+}
+
+template <int NQ, int MODE>
+static tf_status launch(GatherParams p, int ug, cudaStream_t s) {
+  const int per_sm = configure<NQ, MODE>();
+  if (per_sm == 0) return TF_ERR_CUDA;
+  p.splits = wave_splits(ug, num_sms() * per_sm, p.splits_cap);
+  dim3 grid(p.splits, ug);
+  if (launch_pdl(gather_attn_kernel<NQ, MODE>, grid, dim3(kGatherThreads), kGatherSmem, s, p) != cudaSuccess)
+    return TF_ERR_CUDA;
+  return launch_status();
+}
+
+template <int NQ>
+static tf_status launch_mode(int mode, const GatherParams& p, int ug, cudaStream_t s) {
+  return mode == kModeChunks ? launch<NQ, kModeChunks>(p, ug, s) : launch<NQ, kModeWindow>(p, ug, s);
 }
 
 tf_status gather_launch(int mode, GatherParams p, int units, int rows, int P_max, void* ws, size_t ws_bytes,
                         cudaStream_t stream) {
+  if (p.T != 1) return TF_ERR_UNSUPPORTED;
   const int nq = gather_nq(rows);
   p.ngroups = (rows + nq - 1) / nq;
   p.splits_cap = gather_splits_cap(P_max);
   const int ug = units * p.ngroups;
-  const int target = num_sms() * 4;
-  int splits = (target + ug - 1) / ug;
-  if (splits > p.splits_cap) splits = p.splits_cap;
-  p.splits = splits < 1 ? 1 : splits;
   const size_t need = gather_workspace(units, rows, P_max);
-  if (p.splits > 1 && (!ws || ws_bytes < need || !aligned16(ws))) return TF_ERR_WORKSPACE;
+  if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
   char* w = static_cast<char*>(ws);
   p.tickets = reinterpret_cast<int*>(w);
   p.part_ml = reinterpret_cast<float*>(w + align_up((size_t)ug * sizeof(int), 256));
   p.part_o = reinterpret_cast<float*>(w + align_up((size_t)ug * sizeof(int), 256) +
                                       align_up((size_t)ug * p.splits_cap * nq * 2 * sizeof(float), 256));
-  dim3 grid(p.splits, ug);
   switch (nq) {
-    case 1: launch_nq<1>(mode, p, grid, stream); break;
-    case 2: launch_nq<2>(mode, p, grid, stream); break;
-    case 4: launch_nq<4>(mode, p, grid, stream); break;
-    case 6: launch_nq<6>(mode, p, grid, stream); break;
-    default: launch_nq<8>(mode, p, grid, stream); break;
+    case 1: return launch_mode<1>(mode, p, ug, stream);
+    case 2: return launch_mode<2>(mode, p, ug, stream);
+    default: return launch_mode<4>(mode, p, ug, stream);
   }
-  return launch_status();
 }
 
 }  // namespace tf

@@ -6,7 +6,7 @@
 
 namespace tf {
 
-constexpr int kGatherThreads = 256;
+constexpr int kGatherThreads = 160;  // 4 compute warps + 1 bulk-copy producer warp
 constexpr int kModeChunks = 0;  // positions of the selected chunks (Force 2)
 constexpr int kModeWindow = 1;  // attention sinks + recent window (Force 1)
 
@@ -19,7 +19,7 @@ struct GatherParams {
   const int32_t* n_sel;  // [B, Hkv]     (chunks mode)
   int Hq, Hkv, Lmax, T, kc, n_sink, window;
   float scale_log2;  // softmax scale * log2(e)
-  int ngroups;       // query-row groups per unit
+  int ngroups;       // query-head groups per unit (<= 4 heads each)
   int splits;        // CTAs per (unit, group)
   int splits_cap;    // partial-buffer stride
   float* out;        // [B, Hq, T, D]

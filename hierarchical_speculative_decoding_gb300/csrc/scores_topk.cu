@@ -7,177 +7,122 @@
 // Selection: the kc largest scores, equal scores to the lower chunk id, ids
 // written in ascending order.
 //
-// Design: one kernel.  The (b, g) units are few (32 at batch 1) while each
-// holds up to ~16K chunks, so every unit is split over several CTAs that stream
-// the chunk means (a half-warp per 256-byte mean row, 16-byte loads), write fp32
-// scores to the workspace and add the top 11 bits of each order-preserving
-// uint32 score key to a per-unit histogram.  The last CTA of a unit to finish
-// (an atomic ticket; no CTA ever waits) reads that histogram to find the bin
-// holding the kc-th largest key, pulls the unit's keys into shared memory while
-// collecting the few keys of that bin, resolves the remaining 21 bits on those
-// candidates alone, and then compacts the winners in id order with two
-// warp-segmented ballot walks, so ties resolve to the lower id without a sort.
+// Design: one thread-block cluster per (b, g) unit, S <= 8 CTAs, CTA r owning
+// the r-th contiguous slice of the unit's chunks.  Each CTA streams its chunk
+// means (a half-warp per 256-byte mean row, 16-byte loads, several in flight)
+// and keeps its scores in shared memory as order-preserving uint32 keys with a
+// histogram of their top 11 bits.  The selection then runs on the whole
+// cluster at once through distributed shared memory: every CTA sums the S
+// histograms and finds the bin holding the kc-th largest key (all CTAs reach
+// the same answer); each CTA publishes its keys of that bin and its count of
+// keys above it; every CTA gathers those few keys, resolves the remaining 21
+// bits and every CTA's output offset by itself, and writes its own winners in
+// id order.  Three cluster barriers in all; scores never leave the chip and no
+// CTA waits on another except at those barriers (hardware, no spinning).
+#include "sm100_ptx.cuh"
 #include "tf_common.cuh"
 
 namespace tf {
 namespace {
 
+using namespace sm100;
+
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 4;
-constexpr int kBins = 2048;       // histogram over the top 11 key bits
-constexpr int kSmemKeys = 16384;  // keys the selecting CTA keeps in shared memory (128K tokens)
-constexpr int kCandCap = 2048;    // keys of the threshold bin resolved in shared memory
+constexpr int kUnroll = 6;
+constexpr int kMaxCluster = 8;
+constexpr int kMaxSliceKeys = 16384;  // keys per CTA held in shared memory (64 KB)
+constexpr int kCandCap = 4096;        // keys of the threshold bin gathered on every CTA
 
-inline size_t tickets_bytes(int units) { return align_up((size_t)units * sizeof(int), 256); }
-inline size_t hist_bytes(int units) { return (size_t)units * kBins * sizeof(uint32_t); }
-
-// Warp 0 scans hist[0, nb) from the top and finds the bin holding the krem-th
-// largest key; writes the bin and how many keys are still needed from it.
-__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int krem, int* s_bin, int* s_krem) {
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const int seg = nb / 32;
-    const int top = nb - lane * seg;  // lane 0 owns the highest bins
-    int segsum = 0;
-    for (int i = top - seg; i < top; ++i) segsum += (int)hist[i];
-    int incl = segsum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const int excl = incl - segsum;
-    if (excl < krem && krem <= incl) {
-      int run = excl;
-      for (int i = top - 1; i >= top - seg; --i) {
-        const int h = (int)hist[i];
-        if (run + h >= krem) {
-          *s_bin = i;
-          *s_krem = krem - run;
-          break;
-        }
-        run += h;
-      }
-    }
-  }
-}
-
-template <bool kSmem>
-__device__ __forceinline__ uint32_t key_at(const uint32_t* keys, const float* scores, int c) {
-  return kSmem ? keys[c] : score_key(__ldcg(scores + c));
-}
-
-// Select the kc largest of C > kc keys (ties to the lower id) and write their ids
-// ascending.  hist holds the unit's top-11-bit histogram on entry.
-template <bool kSmem>
-__device__ __noinline__ void select_and_compact(const uint32_t* keys, const float* scores, int C, int kc, uint32_t* hist,
-                                   uint32_t* cand, int32_t* out, uint32_t* thresh_out) {
-  __shared__ int s_bin, s_krem, s_ncand;
-  __shared__ int s_wgt[kWarps], s_weq[kWarps];
+// Thread t owns nb / kThreads bins of h (thread 0 the highest); find the bin
+// holding the krem-th largest key.  All threads; result in s_bin / s_krem.
+__device__ __forceinline__ void find_bin(const uint32_t* h, int nb, int krem, int* s_wsum, int* s_bin,
+                                         int* s_krem) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-
-  // 1. the top-11-bit bin of the kc-th largest key
-  find_bin(hist, kBins, kc, &s_bin, &s_krem);
-  if (threadIdx.x == 0) s_ncand = 0;
-  __syncthreads();
-  const uint32_t b1 = (uint32_t)s_bin;
-  int krem = s_krem;
-
-  // 2. collect the keys of that bin
-  for (int c = threadIdx.x; c < C; c += kThreads) {
-    const uint32_t key = key_at<kSmem>(keys, scores, c);
-    if ((key >> 21) == b1) {
-      const int slot = atomicAdd(&s_ncand, 1);
-      if (slot < kCandCap) cand[slot] = key;
-    }
-  }
-  __syncthreads();
-  const int ncand = s_ncand;
-  const bool in_cand = ncand <= kCandCap;
-
-  // 3. remaining 11 + 10 bits, on the candidates (or on all keys if the bin is huge)
-  uint32_t prefix = b1 << 21, pmask = 0xFFE00000u;
+  const int k = nb / kThreads;
+  const int top = nb - (int)threadIdx.x * k;
+  int segsum = 0;
+  for (int i = top - k; i < top; ++i) segsum += (int)h[i];
+  int incl = segsum;
 #pragma unroll
-  for (int pass = 0; pass < 2; ++pass) {
-    const int shift = pass == 0 ? 10 : 0, nb = pass == 0 ? 2048 : 1024;
-    const uint32_t mask = (uint32_t)nb - 1u;
-    for (int i = threadIdx.x; i < nb; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    const int n = in_cand ? ncand : C;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      const uint32_t key = in_cand ? cand[i] : key_at<kSmem>(keys, scores, i);
-      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & mask], 1u);
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
+  incl += wbase;
+  const int excl = incl - segsum;
+  if (excl < krem && krem <= incl) {
+    int run = excl;
+    for (int i = top - 1; i >= top - k; --i) {
+      const int c = (int)h[i];
+      if (run + c >= krem) {
+        *s_bin = i;
+        *s_krem = krem - run;
+        break;
+      }
+      run += c;
     }
-    __syncthreads();
-    find_bin(hist, nb, krem, &s_bin, &s_krem);
-    __syncthreads();
-    prefix |= (uint32_t)s_bin << shift;
-    pmask |= mask << shift;
-    krem = s_krem;
-    __syncthreads();
-  }
-  const uint32_t T = prefix;
-  const int take_eq = krem;
-
-  // 4. id-order compaction: warp w owns ids [w * seg, (w + 1) * seg)
-  const int seg = ((C + kWarps - 1) / kWarps + 31) & ~31;
-  const int w0 = warp * seg, w1 = min(C, w0 + seg);
-  const unsigned lt = (1u << lane) - 1u;
-  int ngt = 0, neq = 0;
-  for (int base = w0; base < w1; base += 32) {
-    const int c = base + lane;
-    const uint32_t key = c < w1 ? key_at<kSmem>(keys, scores, c) : 0u;
-    ngt += __popc(__ballot_sync(0xffffffffu, c < w1 && key > T));
-    neq += __popc(__ballot_sync(0xffffffffu, c < w1 && key == T));
-  }
-  if (lane == 0) {
-    s_wgt[warp] = ngt;
-    s_weq[warp] = neq;
   }
   __syncthreads();
-  int eq_base = 0, sel_base = 0;
-  for (int w = 0; w < warp; ++w) {
-    const int take = min(max(take_eq - eq_base, 0), s_weq[w]);
-    sel_base += s_wgt[w] + take;
-    eq_base += s_weq[w];
+}
+
+// tot[i] = sum over the cluster's CTAs of their local[i], i < nb (nb a multiple
+// of 4, arrays 16-byte aligned): 16-byte remote loads, all ranks in flight.
+__device__ __forceinline__ void cluster_sum(const uint32_t* local, uint32_t* tot, int nb, int S) {
+  for (int i = 4 * threadIdx.x; i < nb; i += 4 * kThreads) {
+    uint4 v[kMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) v[r] = r < S ? dsmem_ld_v4(local + i, (uint32_t)r) : make_uint4(0, 0, 0, 0);
+    uint4 t = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+      t.x += v[r].x;
+      t.y += v[r].y;
+      t.z += v[r].z;
+      t.w += v[r].w;
+    }
+    *reinterpret_cast<uint4*>(tot + i) = t;
   }
-  for (int base = w0; base < w1; base += 32) {
-    const int c = base + lane;
-    const uint32_t key = c < w1 ? key_at<kSmem>(keys, scores, c) : 0u;
-    const bool gt = c < w1 && key > T;
-    const bool eq = c < w1 && key == T;
-    const unsigned beq = __ballot_sync(0xffffffffu, eq);
-    const bool sel = gt || (eq && eq_base + __popc(beq & lt) < take_eq);
-    const unsigned bsel = __ballot_sync(0xffffffffu, sel);
-    const int pos = sel_base + __popc(bsel & lt);
-    if (sel && pos < kc) out[pos] = c;
-    eq_base += __popc(beq);
-    sel_base += __popc(bsel);
-  }
-  *thresh_out = T;
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads, 2) scores_topk_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ M, const int32_t* __restrict__ seq_lens,
-    int Hq, int Hkv, int Lmax, int kc, int splits, int smem_keys, int32_t* __restrict__ idx,
-    int32_t* __restrict__ n_sel, float* __restrict__ s_cut, int* __restrict__ tickets,
-    uint32_t* __restrict__ hist_ws, float* __restrict__ scores_ws) {
-  extern __shared__ uint32_t keys_smem[];
+    int Hq, int Hkv, int Lmax, int kc, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel,
+    float* __restrict__ s_cut) {
+  extern __shared__ uint32_t keys[];  // this CTA's slice of score keys
   __shared__ float qs[kHeadDim];
-  __shared__ uint32_t hist[kBins];
-  __shared__ uint32_t cand[kCandCap];
-  __shared__ int s_last;
-  __shared__ float s_min[kWarps];
+  __shared__ __align__(16) uint32_t hist1[2048], hist2[2048], hist3[1024], tot[2048];
+  __shared__ uint32_t cand[kCandCap];   // this CTA's keys of the threshold bin (read by the cluster)
+  __shared__ uint32_t gcand[kCandCap];  // the cluster's keys of the threshold bin
+  __shared__ int s_ncand, s_above, s_roff[kMaxCluster + 1], s_rgt[kMaxCluster], s_req[kMaxCluster];
+  __shared__ int s_wsum[kWarps], s_bin, s_krem;
+  __shared__ uint32_t s_counts[2];  // keys > T and keys == T in this slice (or the slice's min key)
+  __shared__ int s_wgt[kWarps], s_weq[kWarps];
 
+  const int S = (int)gridDim.x;  // the cluster spans grid x
+  const uint32_t rank = cluster_ctarank();
   const int unit = blockIdx.y;
   const int b = unit / Hkv, g = unit % Hkv;
   const int G = Hq / Hkv;
   const int Cmax = (Lmax + kChunk - 1) / kChunk;
+
+  for (int i = threadIdx.x; i < 2048; i += kThreads) {
+    hist1[i] = 0;
+    hist2[i] = 0;
+  }
+  for (int i = threadIdx.x; i < 1024; i += kThreads) hist3[i] = 0;
+  pdl_wait();
   const int L = clamp_len(seq_lens[b], Lmax);
   const int C = (L + kChunk - 1) / kChunk;
-  float* scores = scores_ws + (size_t)unit * Cmax;
-  uint32_t* hist_g = hist_ws + (size_t)unit * kBins;
+  const int per = (C + S - 1) / S;
+  const int c0 = min(C, (int)rank * per);
+  const int c1 = min(C, c0 + per);
+  const int n = c1 - c0;
 
   if (threadIdx.x < kHeadDim) {
     float s = 0.0f;
@@ -185,120 +130,261 @@ __global__ void __launch_bounds__(kThreads, 2) scores_topk_kernel(
       s += __uint_as_float((uint32_t)q[((size_t)b * Hq + (size_t)g * G + h) * kHeadDim + threadIdx.x] << 16);
     qs[threadIdx.x] = s;
   }
-  for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
   __syncthreads();
 
-  // ---- scoring: this CTA's slice of the unit's chunks
-  const int per = (C + splits - 1) / splits;
-  const int c0 = blockIdx.x * per;
-  const int c1 = min(C, c0 + per);
-  const int half = (threadIdx.x >> 4) & 1, l16 = threadIdx.x & 15, wid = threadIdx.x >> 5;
-  float qv[8];
+  // ---- scoring of this CTA's slice into shared memory
+  {
+    const int half = (threadIdx.x >> 4) & 1, l16 = threadIdx.x & 15, wid = threadIdx.x >> 5;
+    float qv[8];
 #pragma unroll
-  for (int d = 0; d < 8; ++d) qv[d] = qs[l16 * 8 + d];
-  const uint16_t* Mu = M + (size_t)unit * Cmax * kHeadDim + l16 * 8;
-  constexpr int kHalfWarps = kThreads / 16;
-  // The loop bound is warp-uniform (the shuffles below need the whole warp);
-  // each half-warp owns chunk base + half + u * kHalfWarps.
-  for (int base = c0 + 2 * wid; base < c1; base += kHalfWarps * kUnroll) {
-    const int cb = base + half;
-    uint4 v[kUnroll];
+    for (int d = 0; d < 8; ++d) qv[d] = qs[l16 * 8 + d];
+    const uint16_t* Mu = M + (size_t)unit * Cmax * kHeadDim + l16 * 8;
+    constexpr int kHalfWarps = kThreads / 16;
+    // The loop bound is warp-uniform (the shuffles need the whole warp); each
+    // half-warp owns chunk base + half + u * kHalfWarps.
+    for (int base = c0 + 2 * wid; base < c1; base += kHalfWarps * kUnroll) {
+      const int cb = base + half;
+      uint4 v[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int c = cb + u * kHalfWarps;
-      v[u] = (c < c1) ? ld_stream16(Mu + (size_t)c * kHeadDim) : make_uint4(0, 0, 0, 0);
-    }
+      for (int u = 0; u < kUnroll; ++u) {
+        const int c = cb + u * kHalfWarps;
+        v[u] = (c < c1) ? ld_stream16(Mu + (size_t)c * kHeadDim) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      float f[8];
-      unpack8(v[u], f);
-      float s = 0.0f;
+      for (int u = 0; u < kUnroll; ++u) {
+        float f[8];
+        unpack8(v[u], f);
+        float s = 0.0f;
 #pragma unroll
-      for (int d = 0; d < 8; ++d) s = fmaf(qv[d], f[d], s);
-      s += __shfl_xor_sync(0xffffffffu, s, 8);
-      s += __shfl_xor_sync(0xffffffffu, s, 4);
-      s += __shfl_xor_sync(0xffffffffu, s, 2);
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      const int c = cb + u * kHalfWarps;
-      if (l16 == 0 && c < c1) {
-        scores[c] = s;
-        atomicAdd(&hist[score_key(s) >> 21], 1u);
+        for (int d = 0; d < 8; ++d) s = fmaf(qv[d], f[d], s);
+        s += __shfl_xor_sync(0xffffffffu, s, 8);
+        s += __shfl_xor_sync(0xffffffffu, s, 4);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        const int c = cb + u * kHalfWarps;
+        if (l16 == 0 && c < c1) {
+          const uint32_t key = score_key(s);
+          keys[c - c0] = key;
+          atomicAdd(&hist1[key >> 21], 1u);
+        }
       }
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < kBins; i += kThreads)
-    if (hist[i]) atomicAdd(&hist_g[i], hist[i]);
-
-  // ---- ticket: the last CTA of this unit selects
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(&tickets[unit], 1) == splits - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // the unit's histogram -> shared memory; leave the workspace copy zeroed
-  for (int i = threadIdx.x; i < kBins; i += kThreads) {
-    hist[i] = __ldcg(hist_g + i);
-    hist_g[i] = 0u;
-  }
-  __syncthreads();
-
   int32_t* out = idx + (size_t)unit * kc;
+
   if (C <= kc) {
-    float mn = INFINITY;
-    for (int c = threadIdx.x; c < kc; c += kThreads) {
-      out[c] = (c < C) ? c : -1;
-      if (c < C) mn = fminf(mn, __ldcg(scores + c));
+    // Every chunk is selected: ids in order, slots past C hold -1, s_cut = min score.
+    uint32_t mn = 0xffffffffu;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      out[c0 + i] = c0 + i;
+      mn = min(mn, keys[i]);
     }
+    if (rank == 0)
+      for (int i = C + (int)threadIdx.x; i < kc; i += kThreads) out[i] = -1;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    if ((threadIdx.x & 31) == 0) s_min[threadIdx.x >> 5] = mn;
+    for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    if (threadIdx.x == 0) s_counts[0] = 0xffffffffu;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      float m = INFINITY;
-      for (int w = 0; w < kWarps; ++w) m = fminf(m, s_min[w]);
+    if ((threadIdx.x & 31) == 0) atomicMin(&s_counts[0], mn);
+    cluster_sync();
+    if (rank == 0 && threadIdx.x == 0) {
+      uint32_t m = 0xffffffffu;
+      for (int r = 0; r < S; ++r) m = min(m, dsmem_ld_u32(&s_counts[0], (uint32_t)r));
       n_sel[unit] = C;
-      if (s_cut) s_cut[unit] = (C > 0) ? m : -INFINITY;
-      tickets[unit] = 0;
+      if (s_cut) s_cut[unit] = (C > 0) ? key_score(m) : -INFINITY;
     }
+    cluster_sync();  // keep shared memory alive until rank 0 has read it
     return;
   }
 
-  uint32_t T = 0;
-  if (C <= smem_keys) {
-    for (int c = threadIdx.x; c < C; c += kThreads) keys_smem[c] = score_key(__ldcg(scores + c));
+  // ---- round 1: the cluster's histogram of the top 11 key bits -> bin b1
+  cluster_sync();
+  cluster_sum(hist1, tot, 2048, S);
+  find_bin(tot, 2048, kc, s_wsum, &s_bin, &s_krem);
+  const uint32_t b1 = (uint32_t)s_bin;
+  const int krem1 = s_krem;
+  const int ncand_tot = (int)tot[b1];  // keys of bin b1 over the cluster (same on every CTA)
+
+  uint32_t T;
+  int take_eq;
+  int cta_eq = 0, cta_sel = 0;  // equal keys and selected ids in the CTAs before this one
+  if (ncand_tot <= kCandCap) {
+    // ---- round 2: publish this slice's keys of bin b1 and its count of keys
+    // above the bin; every CTA gathers all lists and resolves the last 21 bits
+    // and all output offsets by itself.
+    if (threadIdx.x == 0) {
+      s_ncand = 0;
+      s_above = 0;
+    }
     __syncthreads();
-    select_and_compact<true>(keys_smem, scores, C, kc, hist, cand, out, &T);
+    {
+      int above = 0;
+      constexpr int k4 = 2048 / kThreads;
+      for (int i = threadIdx.x * k4; i < ((int)threadIdx.x + 1) * k4; ++i) above += (uint32_t)i > b1 ? (int)hist1[i] : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
+      if ((threadIdx.x & 31) == 0) atomicAdd(&s_above, above);
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint32_t key = keys[i];
+        if ((key >> 21) == b1) cand[atomicAdd(&s_ncand, 1)] = key;  // at most ncand_tot <= kCandCap
+      }
+    }
+    cluster_sync();
+    if (threadIdx.x < 32) {
+      const int r = threadIdx.x;
+      const int nc = r < S ? (int)dsmem_ld_u32(&s_ncand, (uint32_t)r) : 0;
+      int incl = nc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (r >= o) incl += v;
+      }
+      if (r < S) {
+        s_roff[r] = incl - nc;
+        s_rgt[r] = (int)dsmem_ld_u32(&s_above, (uint32_t)r);
+        s_req[r] = 0;
+      }
+      if (r == S - 1) s_roff[S] = incl;
+    }
+    __syncthreads();
+    for (int r = 0; r < S; ++r) {
+      const int off = s_roff[r], nc = s_roff[r + 1] - off;
+      for (int i = threadIdx.x; i < nc; i += kThreads) gcand[off + i] = dsmem_ld_u32(cand + i, (uint32_t)r);
+    }
+    __syncthreads();
+    // bits 20..10, then 9..0, among the gathered keys (all of them are in bin b1)
+    for (int i = threadIdx.x; i < ncand_tot; i += kThreads) atomicAdd(&hist2[(gcand[i] >> 10) & 2047u], 1u);
+    __syncthreads();
+    find_bin(hist2, 2048, krem1, s_wsum, &s_bin, &s_krem);
+    const uint32_t pre2 = (b1 << 11) | (uint32_t)s_bin;
+    const int krem2 = s_krem;
+    for (int i = threadIdx.x; i < ncand_tot; i += kThreads) {
+      const uint32_t key = gcand[i];
+      if ((key >> 10) == pre2) atomicAdd(&hist3[key & 1023u], 1u);
+    }
+    __syncthreads();
+    find_bin(hist3, 1024, krem2, s_wsum, &s_bin, &s_krem);
+    T = (pre2 << 10) | (uint32_t)s_bin;
+    take_eq = s_krem;
+    // per-CTA counts of keys > T and == T among the gathered keys
+    for (int i = threadIdx.x; i < ncand_tot; i += kThreads) {
+      const uint32_t key = gcand[i];
+      int r = 0;
+      while (r + 1 < S && i >= s_roff[r + 1]) ++r;
+      if (key > T) atomicAdd(&s_rgt[r], 1);
+      if (key == T) atomicAdd(&s_req[r], 1);
+    }
+    __syncthreads();
+    for (int r = 0; r < (int)rank; ++r) {
+      cta_sel += s_rgt[r] + min(max(take_eq - cta_eq, 0), s_req[r]);
+      cta_eq += s_req[r];
+    }
   } else {
-    select_and_compact<false>(keys_smem, scores, C, kc, hist, cand, out, &T);
+    // ---- rare (huge ties or a flat score range): resolve the last 21 bits with
+    // two more cluster-wide histogram rounds, then exchange exact counts.
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t key = keys[i];
+      if ((key >> 21) == b1) atomicAdd(&hist2[(key >> 10) & 2047u], 1u);
+    }
+    cluster_sync();
+    cluster_sum(hist2, tot, 2048, S);
+    find_bin(tot, 2048, krem1, s_wsum, &s_bin, &s_krem);
+    const uint32_t pre2 = (b1 << 11) | (uint32_t)s_bin;
+    const int krem2 = s_krem;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t key = keys[i];
+      if ((key >> 10) == pre2) atomicAdd(&hist3[key & 1023u], 1u);
+    }
+    cluster_sync();
+    cluster_sum(hist3, tot, 1024, S);
+    find_bin(tot, 1024, krem2, s_wsum, &s_bin, &s_krem);
+    T = (pre2 << 10) | (uint32_t)s_bin;
+    take_eq = s_krem;
+    {
+      int ngt = 0, neq = 0;
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint32_t key = keys[i];
+        ngt += key > T;
+        neq += key == T;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        ngt += __shfl_xor_sync(0xffffffffu, ngt, o);
+        neq += __shfl_xor_sync(0xffffffffu, neq, o);
+      }
+      if (threadIdx.x == 0) {
+        s_counts[0] = 0;
+        s_counts[1] = 0;
+      }
+      __syncthreads();
+      if ((threadIdx.x & 31) == 0) {
+        atomicAdd(&s_counts[0], (uint32_t)ngt);
+        atomicAdd(&s_counts[1], (uint32_t)neq);
+      }
+    }
+    cluster_sync();
+    for (int r = 0; r < (int)rank; ++r) {
+      const int gt_r = (int)dsmem_ld_u32(&s_counts[0], (uint32_t)r);
+      const int eq_r = (int)dsmem_ld_u32(&s_counts[1], (uint32_t)r);
+      cta_sel += gt_r + min(max(take_eq - cta_eq, 0), eq_r);
+      cta_eq += eq_r;
+    }
   }
-  if (threadIdx.x == 0) {
+
+  // ---- id-order compaction of this slice: warp w owns local ids [w * seg, (w + 1) * seg)
+  {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
+    const int w0 = warp * seg, w1 = min(n, w0 + seg);
+    const unsigned lt = (1u << lane) - 1u;
+    int ngt = 0, neq = 0;
+    for (int base = w0; base < w1; base += 32) {
+      const int i = base + lane;
+      const uint32_t key = i < w1 ? keys[i] : 0u;
+      ngt += __popc(__ballot_sync(0xffffffffu, i < w1 && key > T));
+      neq += __popc(__ballot_sync(0xffffffffu, i < w1 && key == T));
+    }
+    if (lane == 0) {
+      s_wgt[warp] = ngt;
+      s_weq[warp] = neq;
+    }
+    __syncthreads();
+    int eq_base = cta_eq, sel_base = cta_sel;
+    for (int w = 0; w < warp; ++w) {
+      sel_base += s_wgt[w] + min(max(take_eq - eq_base, 0), s_weq[w]);
+      eq_base += s_weq[w];
+    }
+    for (int base = w0; base < w1; base += 32) {
+      const int i = base + lane;
+      const uint32_t key = i < w1 ? keys[i] : 0u;
+      const bool gt = i < w1 && key > T;
+      const bool eq = i < w1 && key == T;
+      const unsigned beq = __ballot_sync(0xffffffffu, eq);
+      const bool sel = gt || (eq && eq_base + __popc(beq & lt) < take_eq);
+      const unsigned bsel = __ballot_sync(0xffffffffu, sel);
+      const int pos = sel_base + __popc(bsel & lt);
+      if (sel && pos < kc) out[pos] = c0 + i;
+      eq_base += __popc(beq);
+      sel_base += __popc(bsel);
+    }
+  }
+  if (rank == 0 && threadIdx.x == 0) {
     n_sel[unit] = kc;
     if (s_cut) s_cut[unit] = key_score(T);
-    tickets[unit] = 0;
   }
+  cluster_sync();  // no CTA leaves while another may still read its counts
 }
 
 }  // namespace
 }  // namespace tf
 
-namespace {
-int scores_splits(int units, int Cmax) {
-  const int target = tf::num_sms() * 2;
-  int s = (target + units - 1) / units;
-  const int max_s = (Cmax + 63) / 64;
-  if (s > max_s) s = max_s;
-  return s < 1 ? 1 : s;
-}
-}  // namespace
-
 extern "C" size_t tf_chunk_scores_topk_workspace(int B, int Hkv, int Lmax, int chunk) {
-  if (B <= 0 || Hkv <= 0 || Lmax <= 0 || chunk != tf::kChunk) return 0;
-  const size_t units = (size_t)B * Hkv;
-  const size_t Cmax = (size_t)(Lmax + chunk - 1) / chunk;
-  return tf::tickets_bytes((int)units) + tf::hist_bytes((int)units) + units * Cmax * sizeof(float);
+  (void)B;
+  (void)Hkv;
+  (void)Lmax;
+  (void)chunk;
+  return 0;  // scores and the selection stay in (distributed) shared memory
 }
 
 extern "C" tf_status tf_chunk_scores_topk(const uint16_t* q, const uint16_t* M, const int32_t* seq_lens, int B,
@@ -306,31 +392,61 @@ extern "C" tf_status tf_chunk_scores_topk(const uint16_t* q, const uint16_t* M, 
                                           int32_t* n_sel, float* s_cut, void* ws, size_t ws_bytes,
                                           tf_stream_t stream) {
   using namespace tf;
+  (void)ws;
+  (void)ws_bytes;
   if (!q || !M || !seq_lens || !idx || !n_sel) return TF_ERR_INVALID_ARG;
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || kc <= 0 || Hq % Hkv != 0) return TF_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(M)) return TF_ERR_INVALID_ARG;
   if (D != kHeadDim || chunk != kChunk) return TF_ERR_UNSUPPORTED;
   if (B == 0 || Lmax == 0) return TF_OK;
-  const size_t need = tf_chunk_scores_topk_workspace(B, Hkv, Lmax, chunk);
-  if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
   const int units = B * Hkv;
+  if (units > 65535) return TF_ERR_UNSUPPORTED;
   const int Cmax = (Lmax + kChunk - 1) / kChunk;
-  const int splits = scores_splits(units, Cmax);
-  const int smem_keys = Cmax <= kSmemKeys ? Cmax : 0;
-  const size_t dyn = (size_t)smem_keys * sizeof(uint32_t);
+
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(scores_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemKeys * (int)sizeof(uint32_t)) != cudaSuccess)
+                             kMaxSliceKeys * (int)sizeof(uint32_t)) != cudaSuccess)
       return TF_ERR_CUDA;
     configured = true;
   }
-  char* w = static_cast<char*>(ws);
-  int* tickets = reinterpret_cast<int*>(w);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(w + tickets_bytes(units));
-  float* scores = reinterpret_cast<float*>(w + tickets_bytes(units) + hist_bytes(units));
-  dim3 grid(splits, units);
-  scores_topk_kernel<<<grid, kThreads, dyn, stream>>>(q, M, seq_lens, Hq, Hkv, Lmax, kc, splits, smem_keys, idx,
-                                                      n_sel, s_cut, tickets, hist, scores);
+  // Cluster size: the largest S <= 8 (at most one CTA per 64 chunks) whose
+  // units x S CTAs fit one wave at the occupancy their slice size allows; at
+  // least enough CTAs that every slice fits on chip.
+  const int sms = num_sms();
+  const int need = (Cmax + kMaxSliceKeys - 1) / kMaxSliceKeys;
+  if (need > kMaxCluster) return TF_ERR_UNSUPPORTED;  // context beyond 8 x 16384 chunks
+  int most = (Cmax + 63) / 64;
+  if (most > kMaxCluster) most = kMaxCluster;
+  int S = need;
+  for (int cand_s = most; cand_s >= need; --cand_s) {
+    const int sl = (Cmax + cand_s - 1) / cand_s;
+    const int occ = occupancy_blocks((const void*)scores_topk_kernel, kThreads, (size_t)sl * sizeof(uint32_t));
+    if ((long long)units * cand_s <= (long long)sms * occ) {
+      S = cand_s;
+      break;
+    }
+  }
+  if (S < 1) S = 1;
+  const int slice = (Cmax + S - 1) / S;
+  const size_t dyn = (size_t)slice * sizeof(uint32_t);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S, units);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, scores_topk_kernel, q, M, seq_lens, Hq, Hkv, Lmax, kc, idx, n_sel, s_cut) !=
+      cudaSuccess)
+    return TF_ERR_CUDA;
   return launch_status();
 }

@@ -6,23 +6,29 @@
 // max(0, p - q) normalised; the two levels (tiny drafter -> retrieval drafter,
 // retrieval drafter -> target) compose to the target distribution.
 //
-// Design: latency-bound, one CTA per sequence.  The CTA computes the softmax
-// normaliser (max, sum of exponentials) of every row it may need, runs the
-// sequential ratio tests on one thread in fp64, then draws the next token
-// with an index-order inverse CDF: each thread owns a contiguous slice of the
-// vocabulary, slice sums are scanned across the block in fp64, and the one
-// thread whose slice holds the crossing walks it.
+// Design: latency-bound, two short kernels chained with programmatic dependent
+// launch.  (1) Every logit row that may be needed (gamma + 1 verifier rows and
+// gamma drafter rows per sequence) gets its softmax normaliser -- max and sum of
+// exponentials in the log2 domain -- from its own group of threads (a warp for
+// small vocabularies, 512 threads otherwise), with all loads of a thread issued
+// together.  (2) One group per sequence runs the ratio tests on one thread in
+// fp64 from those normalisers and the drafted tokens' own logits, then draws the
+// next token with an index-order inverse CDF: each thread owns a contiguous
+// slice of the vocabulary, the slice sums are scanned across the group in fp64,
+// and the thread whose slice holds the crossing walks it again.
 #include "tf_common.cuh"
 
 namespace tf {
 namespace {
 
-constexpr int kMaxThreads = 1024;
+constexpr int kBlockRow = 512;   // threads per row normaliser for large vocabularies
+constexpr int kBlockSeq = 1024;  // threads per sequence for large vocabularies
+constexpr int kSmallV = 1024;    // up to this vocabulary a warp handles a row / a sequence
+constexpr int kBatch = 8;        // loads in flight per thread
 
-// Softmax normaliser of a row in the log2 domain: x_t = logit_t * log2(e) / temperature.
-struct RowNorm {
-  float m;   // max_t x_t
-  double z;  // sum_t 2^(x_t - m)
+struct NormWs {
+  float* m;   // [B, R] max of x = logit * log2(e) / temperature
+  double* z;  // [B, R] sum of 2^(x - m)
 };
 
 __device__ __forceinline__ void combine(float& m, float& z, float m2, float z2) {
@@ -32,205 +38,320 @@ __device__ __forceinline__ void combine(float& m, float& z, float m2, float z2) 
   m = mn;
 }
 
-// Block-wide softmax normaliser of one row.  scratch: >= 2 * 32 floats.
-__device__ RowNorm row_norm(const float* __restrict__ row, int V, float inv_t, float* s_m, double* s_z) {
-  float m = -INFINITY, z = 0.0f;
-  for (int t = threadIdx.x; t < V; t += blockDim.x) {
-    const float x = row[t] * inv_t;
-    if (x > m) {
-      z = z * merge_scale(m, x) + 1.0f;
-      m = x;
-    } else {
-      z += exp2f(x - m);
+// Per-thread (max, sum) over elements t = start, start + stride, ... < V.
+__device__ __forceinline__ void thread_norm(const float* __restrict__ row, int V, int start, int stride, float inv_t,
+                                            float& m, float& z) {
+  m = -INFINITY;
+  z = 0.0f;
+  for (int t0 = start; t0 < V; t0 += stride * kBatch) {
+    float x[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int t = t0 + k * stride;
+      x[k] = t < V ? __ldg(row + t) * inv_t : -INFINITY;
     }
+    float bm = x[0];
+#pragma unroll
+    for (int k = 1; k < kBatch; ++k) bm = fmaxf(bm, x[k]);
+    if (bm == -INFINITY) continue;
+    float bz = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) bz += exp2f(x[k] - bm);
+    combine(m, z, bm, bz);
   }
-  // Warp combine in fp32 (few terms), block combine in fp64.
+}
+
+// (1) Normaliser of every row.  Rows are numbered [b][r] with r < gamma+1 the
+// verifier rows and r >= gamma+1 the drafter rows.  WARP: one warp per row.
+template <bool WARP>
+__global__ void __launch_bounds__(WARP ? 256 : kBlockRow) row_norm_kernel(const float* __restrict__ tgt,
+                                                                          const float* __restrict__ drf, int B,
+                                                                          int gamma, int V, float inv_t, NormWs ws) {
+  pdl_wait();
+  const int R = 2 * gamma + 1;
+  long long row;
+  int start, stride;
+  if (WARP) {
+    row = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    start = threadIdx.x & 31;
+    stride = 32;
+  } else {
+    row = blockIdx.x;
+    start = threadIdx.x;
+    stride = blockDim.x;
+  }
+  if (row >= (long long)B * R) return;  // a whole warp (or block) leaves together
+  const int b = (int)(row / R), r = (int)(row % R);
+  const float* src = r <= gamma ? tgt + ((size_t)b * (gamma + 1) + r) * V
+                                : drf + ((size_t)b * gamma + (r - gamma - 1)) * V;
+  float m, z;
+  thread_norm(src, V, start, stride, inv_t, m, z);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
     const float z2 = __shfl_xor_sync(0xffffffffu, z, o);
     combine(m, z, m2, z2);
   }
-  const int warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-  __syncthreads();
+  if (WARP) {
+    if ((threadIdx.x & 31) == 0) {
+      ws.m[row] = m;
+      ws.z[row] = (double)z;
+    }
+    return;
+  }
+  __shared__ float s_m[32];
+  __shared__ double s_z[32];
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   if ((threadIdx.x & 31) == 0) {
     s_m[warp] = m;
     s_z[warp] = (double)z;
   }
   __syncthreads();
-  RowNorm r;
-  float mm = -INFINITY;
-  for (int w = 0; w < nw; ++w) mm = fmaxf(mm, s_m[w]);
-  double zz = 0.0;
-  for (int w = 0; w < nw; ++w)
-    if (s_m[w] != -INFINITY) zz += s_z[w] * exp2((double)s_m[w] - (double)mm);
-  r.m = mm;
-  r.z = zz;
-  __syncthreads();
-  return r;
+  if (threadIdx.x == 0) {
+    float mm = -INFINITY;
+    for (int w = 0; w < nw; ++w) mm = fmaxf(mm, s_m[w]);
+    double zz = 0.0;
+    for (int w = 0; w < nw; ++w)
+      if (s_m[w] != -INFINITY) zz += s_z[w] * exp2((double)s_m[w] - (double)mm);
+    ws.m[row] = mm;
+    ws.z[row] = zz;
+  }
 }
 
-__global__ void __launch_bounds__(kMaxThreads) spec_accept_kernel(
-    const float* __restrict__ tgt, const float* __restrict__ drf, const int32_t* __restrict__ tokens,
-    const float* __restrict__ u_acc, const float* __restrict__ u_res, int gamma, int V, float inv_t,
-    double inv_t_d,
-    int32_t* __restrict__ n_acc, int32_t* __restrict__ next_token, int32_t* __restrict__ out_tokens) {
-  __shared__ float s_m[32];
-  __shared__ double s_z[32];
-  __shared__ double s_scan[32];
-  __shared__ int s_g, s_nacc, s_next, s_found, s_last;
-  const int b = blockIdx.x;
-  const float* P = tgt + (size_t)b * (gamma + 1) * V;
-  const float* Q = drf + (size_t)b * gamma * V;
-  const int32_t* x = tokens + (size_t)b * gamma;
-
-  if (threadIdx.x == 0) {
-    int g = gamma;
-    for (int i = 0; i < gamma; ++i)
-      if (x[i] < 0 || x[i] >= V) { g = i; break; }
-    s_g = g;
+// Weight of token t in the sampling row: p_t, or max(0, p_t - q_t) for a residual.
+struct RowWeights {
+  const float* pr;
+  const float* qr;
+  float pm, qm, inv_zp, inv_zq, inv_t;
+  bool resid;
+  __device__ __forceinline__ float operator()(int t) const {
+    const float pt = exp2f(__ldg(pr + t) * inv_t - pm) * inv_zp;
+    if (!resid) return pt;
+    return fmaxf(pt - exp2f(__ldg(qr + t) * inv_t - qm) * inv_zq, 0.0f);
   }
-  __syncthreads();
-  const int g = s_g;
+};
 
-  // ---- sequential ratio tests (normalisers computed block-wide per row)
-  int nacc = g;
-  for (int i = 0; i < g; ++i) {
-    const RowNorm np = row_norm(P + (size_t)i * V, V, inv_t, s_m, s_z);
-    const RowNorm nq = row_norm(Q + (size_t)i * V, V, inv_t, s_m, s_z);
-    if (threadIdx.x == 0) {
+// (2) Tests and draw.  GS threads per sequence (a warp, or a whole block).
+template <int GS>
+__global__ void __launch_bounds__(GS == 32 ? 256 : GS) accept_kernel(
+    const float* __restrict__ tgt, const float* __restrict__ drf, const int32_t* __restrict__ tokens,
+    const float* __restrict__ u_acc, const float* __restrict__ u_res, int B, int gamma, int V, float inv_t,
+    double inv_t_d, NormWs ws, int32_t* __restrict__ n_acc, int32_t* __restrict__ next_token,
+    int32_t* __restrict__ out_tokens) {
+  __shared__ double s_scan[32];
+  __shared__ int s_found[32], s_lastv[32];
+  __shared__ int s_g, s_nacc;
+  pdl_wait();
+  const int gid = threadIdx.x % GS;  // thread index inside the sequence's group
+  const int b = GS == 32 ? (int)(blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) : (int)blockIdx.x;
+  const bool live = b < B;  // (warp groups only) groups past B just follow along
+  const int R = 2 * gamma + 1;
+  const int lane = threadIdx.x & 31;
+
+  // ---- draft length and the sequential ratio tests (group thread 0, fp64)
+  int nacc = 0, g = 0;
+  if (live && gid == 0) {
+    const int32_t* x = tokens + (size_t)b * gamma;
+    g = gamma;
+    for (int i = 0; i < gamma; ++i)
+      if (x[i] < 0 || x[i] >= V) {
+        g = i;
+        break;
+      }
+    nacc = g;
+    for (int i = 0; i < g; ++i) {
       const int xi = x[i];
-      // The drafted token's own terms in fp64 from the raw logits.
-      const double lp = (double)P[(size_t)i * V + xi] * inv_t_d - (double)np.m;
-      const double lq = (double)Q[(size_t)i * V + xi] * inv_t_d - (double)nq.m;
-      const double qx = exp2(lq) / nq.z;
-      const double ratio = exp2(lp - lq) * (nq.z / np.z);
+      const double mp = ws.m[(size_t)b * R + i], zp = ws.z[(size_t)b * R + i];
+      const double mq = ws.m[(size_t)b * R + gamma + 1 + i], zq = ws.z[(size_t)b * R + gamma + 1 + i];
+      const double lp = (double)tgt[((size_t)b * (gamma + 1) + i) * V + xi] * inv_t_d - mp;
+      const double lq = (double)drf[((size_t)b * gamma + i) * V + xi] * inv_t_d - mq;
+      const double qx = exp2(lq) / zq;
+      const double ratio = exp2(lp - lq) * (zq / zp);
       const bool accept = (qx == 0.0) || ((double)u_acc[(size_t)b * gamma + i] <= ratio);
-      s_nacc = accept ? -1 : i;
+      if (!accept) {
+        nacc = i;
+        break;
+      }
+    }
+  }
+  if (GS == 32) {
+    g = __shfl_sync(0xffffffffu, g, 0);
+    nacc = __shfl_sync(0xffffffffu, nacc, 0);
+  } else {
+    if (gid == 0) {
+      s_g = g;
+      s_nacc = nacc;
     }
     __syncthreads();
-    if (s_nacc >= 0) { nacc = s_nacc; break; }
+    g = s_g;
+    nacc = s_nacc;
   }
 
   // ---- the sampling row: residual at the first rejection, else the bonus row
   const bool rejected = nacc < g;
   const int j = nacc;
-  const RowNorm np = row_norm(P + (size_t)j * V, V, inv_t, s_m, s_z);
-  RowNorm nq = np;
-  if (rejected) nq = row_norm(Q + (size_t)j * V, V, inv_t, s_m, s_z);
-  const float* pr = P + (size_t)j * V;
-  const float* qr = Q + (size_t)j * V;
-  const float inv_zp = (float)(1.0 / np.z), inv_zq = (float)(1.0 / nq.z);
+  const int bb = live ? b : 0;
+  RowWeights w;
+  w.inv_t = inv_t;
+  w.pr = tgt + ((size_t)bb * (gamma + 1) + j) * V;
+  w.qr = rejected ? drf + ((size_t)bb * gamma + j) * V : w.pr;
+  w.pm = ws.m[(size_t)bb * R + j];
+  w.inv_zp = (float)(1.0 / ws.z[(size_t)bb * R + j]);
+  w.qm = rejected ? ws.m[(size_t)bb * R + gamma + 1 + j] : 0.0f;
+  w.inv_zq = rejected ? (float)(1.0 / ws.z[(size_t)bb * R + gamma + 1 + j]) : 0.0f;
+  const double u = live ? (double)u_res[b] : 0.0;
+  const int seg = (V + GS - 1) / GS;
+  const int t0 = min(V, gid * seg), t1 = min(V, t0 + seg);
 
-  const int seg = (V + blockDim.x - 1) / blockDim.x;
-  const int t0 = min(V, (int)threadIdx.x * seg), t1 = min(V, t0 + seg);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-  const double u = (double)u_res[b];
-
+  int next = 0;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    // attempt 0: residual (if rejected) or p_g; attempt 1: p_j when the residual is all zero
-    const bool use_resid = rejected && attempt == 0;
+    w.resid = rejected && attempt == 0;
+    // slice sum, loads in batches
     float run = 0.0f;
-    for (int t = t0; t < t1; ++t) {
-      const float pt = exp2f(pr[t] * inv_t - np.m) * inv_zp;
-      float w = pt;
-      if (use_resid) w = fmaxf(pt - exp2f(qr[t] * inv_t - nq.m) * inv_zq, 0.0f);
-      run += w;
+    for (int t = t0; t < t1; t += kBatch) {
+      float v[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) v[k] = (t + k < t1) ? w(t + k) : 0.0f;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) run += v[k];
     }
-    // fp64 exclusive scan of the slice sums
+    // fp64 scan of the slice sums over the group
     double incl = (double)run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const double v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
     }
-    if (lane == 31) s_scan[warp] = incl;
-    __syncthreads();
-    double wpre = 0.0, total = 0.0;
-    for (int w = 0; w < nw; ++w) {
-      const double v = s_scan[w];
-      if (w < warp) wpre += v;
-      total += v;
+    double excl, total;
+    if (GS == 32) {
+      total = __shfl_sync(0xffffffffu, incl, 31);
+      excl = incl - (double)run;
+    } else {
+      const int warp = threadIdx.x >> 5, nw = GS / 32;
+      __syncthreads();
+      if (lane == 31) s_scan[warp] = incl;
+      __syncthreads();
+      double wpre = 0.0;
+      total = 0.0;
+      for (int k = 0; k < nw; ++k) {
+        const double v = s_scan[k];
+        if (k < warp) wpre += v;
+        total += v;
+      }
+      excl = wpre + incl - (double)run;
     }
-    const double excl = wpre + incl - (double)run;
-    if (threadIdx.x == 0) {
-      s_found = 0x7fffffff;
-      s_last = -1;
+    if (!(total > 0.0)) {
+      if (w.resid) continue;  // p == q: the residual is empty, draw from p_j instead
+      break;                  // (not reachable for finite logits)
     }
-    __syncthreads();
-    if (total > 0.0) {
-      const double target = u * total;
-      if (excl <= target && excl + (double)run > target) {
-        float r2 = 0.0f;
-        for (int t = t0; t < t1; ++t) {
-          const float pt = exp2f(pr[t] * inv_t - np.m) * inv_zp;
-          float w = pt;
-          if (use_resid) w = fmaxf(pt - exp2f(qr[t] * inv_t - nq.m) * inv_zq, 0.0f);
-          r2 += w;
-          if (excl + (double)r2 > target) {
-            atomicMin(&s_found, t);
-            break;
-          }
+    // the slice holding the crossing walks it again, in the same order
+    const double target = u * total;
+    int found = 0x7fffffff, last = -1;
+    if (excl <= target && excl + (double)run > target) {
+      float r2 = 0.0f;
+      for (int t = t0; t < t1; ++t) {
+        r2 += w(t);
+        if (excl + (double)r2 > target) {
+          found = t;
+          break;
         }
       }
+    }
+    // rounding can leave no crossing: then the last index with positive weight
+    bool any;
+    if (GS == 32) {
+      any = __any_sync(0xffffffffu, found != 0x7fffffff);
+    } else {
+      any = __syncthreads_or(found != 0x7fffffff);
+    }
+    if (!any) {
+      for (int t = t0; t < t1; ++t)
+        if (w(t) > 0.0f) last = t;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
+      last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    }
+    if (GS != 32) {
+      const int warp = threadIdx.x >> 5, nw = GS / 32;
       __syncthreads();
-      if (s_found == 0x7fffffff) {
-        // Rounding left no crossing: take the last index with positive weight.
-        int last = -1;
-        for (int t = t0; t < t1; ++t) {
-          const float pt = exp2f(pr[t] * inv_t - np.m) * inv_zp;
-          float w = pt;
-          if (use_resid) w = fmaxf(pt - exp2f(qr[t] * inv_t - nq.m) * inv_zq, 0.0f);
-          if (w > 0.0f) last = t;
-        }
-        if (last >= 0) atomicMax(&s_last, last);
-        __syncthreads();
-        if (threadIdx.x == 0) s_found = s_last < 0 ? 0 : s_last;
+      if (lane == 0) {
+        s_found[warp] = found;
+        s_lastv[warp] = last;
       }
       __syncthreads();
-      if (threadIdx.x == 0) s_next = s_found;
-      __syncthreads();
-      break;
+      for (int k = 0; k < nw; ++k) {
+        found = min(found, s_found[k]);
+        last = max(last, s_lastv[k]);
+      }
     }
-    __syncthreads();
-    if (!use_resid) {
-      if (threadIdx.x == 0) s_next = 0;
-      __syncthreads();
-      break;
-    }
+    next = found != 0x7fffffff ? found : (last >= 0 ? last : 0);
+    break;
   }
 
-  if (threadIdx.x == 0) {
-    n_acc[b] = nacc;
-    next_token[b] = s_next;
-  }
-  if (out_tokens) {
-    for (int c = threadIdx.x; c <= gamma; c += blockDim.x) {
-      int v = -1;
-      if (c < nacc) v = x[c];
-      else if (c == nacc) v = s_next;
-      out_tokens[(size_t)b * (gamma + 1) + c] = v;
+  if (live) {
+    if (gid == 0) {
+      n_acc[b] = nacc;
+      next_token[b] = next;
+    }
+    if (out_tokens) {
+      const int32_t* x = tokens + (size_t)b * gamma;
+      for (int c = gid; c <= gamma; c += GS) {
+        int v = -1;
+        if (c < nacc)
+          v = x[c];
+        else if (c == nacc)
+          v = next;
+        out_tokens[(size_t)b * (gamma + 1) + c] = v;
+      }
     }
   }
+}
+
+size_t norm_bytes(int B, int gamma) {
+  const size_t rows = (size_t)B * (2 * gamma + 1);
+  return align_up(rows * sizeof(float), 256) + rows * sizeof(double);
 }
 
 }  // namespace
 }  // namespace tf
 
+extern "C" size_t tf_spec_accept_workspace(int B, int gamma) {
+  if (B <= 0 || gamma < 0) return 0;
+  return tf::norm_bytes(B, gamma);
+}
+
 extern "C" tf_status tf_spec_accept(const float* tgt_logits, const float* drf_logits, const int32_t* drf_tokens,
                                     const float* u_acc, const float* u_res, int B, int gamma, int V,
                                     float temperature, int32_t* n_acc, int32_t* next_token, int32_t* out_tokens,
-                                    tf_stream_t stream) {
+                                    void* ws, size_t ws_bytes, tf_stream_t stream) {
   using namespace tf;
   if (!tgt_logits || !u_res || !n_acc || !next_token) return TF_ERR_INVALID_ARG;
   if (gamma > 0 && (!drf_logits || !drf_tokens || !u_acc)) return TF_ERR_INVALID_ARG;
   if (B < 0 || gamma < 0 || V < 1 || !(temperature > 0.0f)) return TF_ERR_INVALID_ARG;
   if (B == 0) return TF_OK;
-  int threads = ((V / 8 + 31) / 32) * 32;
-  if (threads < 32) threads = 32;
-  if (threads > kMaxThreads) threads = kMaxThreads;
+  if (!ws || ws_bytes < norm_bytes(B, gamma) || !aligned16(ws)) return TF_ERR_WORKSPACE;
+  const long long rows = (long long)B * (2 * gamma + 1);
+  if (rows >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
+  NormWs nws;
+  nws.m = static_cast<float*>(ws);
+  nws.z = reinterpret_cast<double*>(static_cast<char*>(ws) + align_up((size_t)rows * sizeof(float), 256));
   const double inv_t_d = 1.4426950408889634 / (double)temperature;  // log2(e) / temperature
-  spec_accept_kernel<<<B, threads, 0, stream>>>(tgt_logits, drf_logits, drf_tokens, u_acc, u_res, gamma, V,
-                                                (float)inv_t_d, inv_t_d, n_acc, next_token, out_tokens);
-  return launch_status();
+  const float inv_t = (float)inv_t_d;
+  cudaError_t e;
+  if (V <= kSmallV) {
+    e = launch_pdl(row_norm_kernel<true>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, stream, tgt_logits,
+                   drf_logits, B, gamma, V, inv_t, nws);
+    if (e == cudaSuccess)
+      e = launch_pdl(accept_kernel<32>, dim3((unsigned)((B + 7) / 8)), dim3(256), 0, stream, tgt_logits, drf_logits,
+                     drf_tokens, u_acc, u_res, B, gamma, V, inv_t, inv_t_d, nws, n_acc, next_token, out_tokens);
+  } else {
+    e = launch_pdl(row_norm_kernel<false>, dim3((unsigned)rows), dim3(kBlockRow), 0, stream, tgt_logits, drf_logits,
+                   B, gamma, V, inv_t, nws);
+    if (e == cudaSuccess)
+      e = launch_pdl(accept_kernel<kBlockSeq>, dim3(B), dim3(kBlockSeq), 0, stream, tgt_logits, drf_logits,
+                     drf_tokens, u_acc, u_res, B, gamma, V, inv_t, inv_t_d, nws, n_acc, next_token, out_tokens);
+  }
+  return e == cudaSuccess ? launch_status() : TF_ERR_CUDA;
 }

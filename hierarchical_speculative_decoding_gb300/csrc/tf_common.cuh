@@ -23,6 +23,41 @@ inline int num_sms() {
   return n;
 }
 
+// Resident CTAs per SM for a kernel (at least 1).
+inline int occupancy_blocks(const void* fn, int threads, size_t dyn_smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, dyn_smem) != cudaSuccess || n < 1) return 1;
+  return n;
+}
+
+// Split count that fills whole waves: the largest s <= cap with units * s
+// CTAs fitting the resident slots, or one wave's worth rounded down.
+inline int wave_splits(int units, int slots, int cap) {
+  int s = slots / (units > 0 ? units : 1);
+  if (s > cap) s = cap;
+  return s < 1 ? 1 : s;
+}
+
+// Launch with programmatic dependent launch: the grid may be scheduled while
+// the previous kernel on the stream drains, so its on-chip set-up overlaps that
+// tail.  Every kernel launched this way calls pdl_wait() before it touches
+// global memory that earlier work on the stream writes or reads.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 inline tf_status launch_status() {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TF_OK : TF_ERR_CUDA;
@@ -31,6 +66,10 @@ inline tf_status launch_status() {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ---------------------------------------------------------------- device side
+
+// Wait until the previous kernel on the stream has completed and its writes are
+// visible (a no-op when the launch had no programmatic dependency).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ int clamp_len(int L, int Lmax) { return L < 0 ? 0 : (L > Lmax ? Lmax : L); }
 

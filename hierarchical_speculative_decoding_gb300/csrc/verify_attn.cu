@@ -28,6 +28,7 @@
 
 #include "sm100_ptx.cuh"
 #include "tf_common.cuh"
+#include "tma_host.cuh"
 
 namespace tf {
 namespace {
@@ -107,14 +108,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   const int rows_all = G * p.T;
   const int row0 = grp * kMaxRows;
   const int rows = min(kMaxRows, rows_all - row0);
-  const int L = clamp_len(p.seq_lens[b], p.Lmax);
-
-  // key range of this split: whole tiles
-  const int tiles_all = (L + kTile - 1) / kTile;
-  const int tiles_per = (tiles_all + p.splits - 1) / p.splits;
-  const int k0 = blockIdx.x * tiles_per * kTile;
-  const int k1 = min(L, k0 + tiles_per * kTile);
-  const int ntiles = k1 > k0 ? (k1 - k0 + kTile - 1) / kTile : 0;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -138,6 +131,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     prefetch_tensormap(&mapK);
     prefetch_tensormap(&mapV);
   }
+  pdl_wait();  // everything above is on-chip set-up that may overlap the previous kernel
+  const int L = clamp_len(p.seq_lens[b], p.Lmax);
+
+  // key range of this split: whole tiles
+  const int tiles_all = (L + kTile - 1) / kTile;
+  const int tiles_per = (tiles_all + p.splits - 1) / p.splits;
+  const int k0 = blockIdx.x * tiles_per * kTile;
+  const int k1 = min(L, k0 + tiles_per * kTile);
+  const int ntiles = k1 > k0 ? (k1 - k0 + kTile - 1) / kTile : 0;
   // Q rows of this group -> shared memory, [NPAD x 128] bf16 in two swizzled halves.
   {
     const uint16_t* Qg = p.Q + (((size_t)b * p.Hq + (size_t)g * G) * p.T + row0) * kHeadDim;
@@ -410,36 +412,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
 
 // ------------------------------------------------------------------ host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
-  return fn;
-}
-
-// [rows, 128] bf16 rows of 256 bytes; boxes of 128 rows x 64 columns, 128-byte swizzle.
-bool make_kv_map(CUtensorMap* m, const void* base, long long rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kTile};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int verify_splits_cap(int Lmax) {
   int tiles = (Lmax + kTile - 1) / kTile;
   int cap = (tiles + 3) / 4;  // at least 4 tiles per split
@@ -487,7 +459,9 @@ tf_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParam
       return TF_ERR_CUDA;
     configured = true;
   }
-  verify_umma_kernel<NPAD><<<grid, kThreads, Smem<NPAD>::kDynamic, stream>>>(mk, mv, p);
+  if (launch_pdl(verify_umma_kernel<NPAD>, grid, dim3(kThreads), Smem<NPAD>::kDynamic, stream, mk, mv, p) !=
+      cudaSuccess)
+    return TF_ERR_CUDA;
   return launch_status();
 }
 
@@ -513,7 +487,7 @@ extern "C" tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const 
   const size_t need = verify_ws(B * Hkv, (Hq / Hkv) * T, Lmax);
   if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
   CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, K, rows_total) || !make_kv_map(&mv, V, rows_total)) return TF_ERR_CUDA;
+  if (!make_kv_map(&mk, K, rows_total, kTile) || !make_kv_map(&mv, V, rows_total, kTile)) return TF_ERR_CUDA;
 
   VerifyParams p{};
   const int rows_all = (Hq / Hkv) * T;

@@ -96,8 +96,11 @@ TF_API tf_status tf_build_chunk_means(const uint16_t* K, const int32_t* seq_lens
  *   idx   [B, Hkv, kc] int32   selected chunk ids, slots >= n_sel hold -1
  *   n_sel [B, Hkv]     int32   min(kc, C_b)
  *   s_cut [B, Hkv]     float   smallest selected score (nullable; -inf if none)
- * Scores must be finite (NaN scores rank above every number).
- * Workspace: tf_chunk_scores_topk_workspace(B, Hkv, Lmax, chunk) bytes.
+ * Scores must be finite (NaN scores rank above every number).  Contexts up to
+ * 8 x 16384 chunks (1,048,576 tokens) per sequence.
+ * Workspace: none; tf_chunk_scores_topk_workspace() returns 0 and ws may be
+ * NULL (scores and the selection stay in on-chip shared memory of one
+ * thread-block cluster per (b, g)).
  */
 TF_API size_t tf_chunk_scores_topk_workspace(int B, int Hkv, int Lmax, int chunk);
 TF_API tf_status tf_chunk_scores_topk(const uint16_t* q, const uint16_t* M, const int32_t* seq_lens,
@@ -204,13 +207,18 @@ TF_API tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const uint
  *   u_acc [B, gamma] f32, u_res [B] f32, uniforms in [0, 1)
  *   n_acc [B] int32 (accepted count), next_token [B] int32
  *   out_tokens [B, gamma+1] int32 (nullable): accepted drafts, next token, -1 pad
- * temperature > 0.  gamma >= 0, V >= 1.  No workspace.
+ * temperature > 0.  gamma >= 0, V >= 1.  Probabilities use fp32 exponentials,
+ * fp64 sums and an fp64 ratio test, so a decision can differ from exact
+ * arithmetic only when a uniform lies within ~1e-6 of its boundary.
+ * Workspace: tf_spec_accept_workspace(B, gamma) bytes (per-row normalisers;
+ * needs no zeroing).  Two kernel launches.
  */
+TF_API size_t tf_spec_accept_workspace(int B, int gamma);
 TF_API tf_status tf_spec_accept(const float* tgt_logits, const float* drf_logits, const int32_t* drf_tokens,
                          const float* u_acc, const float* u_res,
                          int B, int gamma, int V, float temperature,
                          int32_t* n_acc, int32_t* next_token, int32_t* out_tokens,
-                         tf_stream_t stream);
+                         void* ws, size_t ws_bytes, tf_stream_t stream);
 
 #ifdef __cplusplus
 }

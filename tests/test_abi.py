@@ -46,13 +46,12 @@ def test_version_and_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    units, cmax = 32, 16384
-    assert lib.tf_chunk_scores_topk_workspace(1, 32, 131072, 8) >= units * cmax * 4
-    assert lib.tf_chunk_scores_topk_workspace(1, 32, 131072, 7) == 0  # unsupported chunk
+    assert lib.tf_chunk_scores_topk_workspace(1, 32, 131072, 8) == 0  # selection stays on chip
     assert lib.tf_sparse_decode_attn_workspace(1, 32, 32, 512) > 0
     assert lib.tf_sparse_decode_attn_workspace(1, 32, 5, 512) == 0  # Hq % Hkv != 0
     assert lib.tf_stream_window_attn_workspace(4, 32, 8, 4, 252) > 0
     assert lib.tf_verify_attn_workspace(4, 32, 8, 131072, 6) > 0
+    assert lib.tf_spec_accept_workspace(8, 5) >= 8 * 11 * 12
     # workspace grows with the problem
     assert lib.tf_verify_attn_workspace(8, 32, 8, 131072, 6) > lib.tf_verify_attn_workspace(1, 32, 8, 131072, 6)
 
@@ -69,16 +68,22 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.tf_build_chunk_means(fake, fake, 1, 1, 64, 128, 8, 0, 9, fake, None) == INVALID
     assert lib.tf_chunk_scores_topk(fake, fake, fake, 1, 6, 4, 64, 128, 8, 4, fake, fake, null, null, 0,
                                     None) == INVALID  # Hq % Hkv
-    assert lib.tf_chunk_scores_topk(fake, fake, fake, 1, 8, 4, 64, 128, 8, 4, fake, fake, null, null, 0,
-                                    None) == WORKSPACE
+    assert lib.tf_chunk_scores_topk(fake, fake, fake, 1, 8, 4, 64, 128, 8, 0, fake, fake, null, null, 0,
+                                    None) == INVALID  # kc = 0
+    assert lib.tf_sparse_decode_attn(fake, fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 4, 0.1, fake, null,
+                                     0, None) == WORKSPACE
     assert lib.tf_sparse_decode_attn(fake, fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 16, 4, 0.1, fake, null,
                                      0, None) == UNSUPPORTED
     assert lib.tf_stream_window_attn(fake, fake, fake, fake, 1, 8, 2, 64, 128, -1, 4, 0.1, fake, null, 0,
                                      None) == INVALID
     assert lib.tf_verify_attn(fake, fake, fake, fake, 1, 8, 2, 64, 128, 0, 0.1, fake, null, 0, None) == INVALID
     assert lib.tf_verify_attn(fake, fake, fake, fake, 1, 8, 2, 64, 128, 17, 0.1, fake, null, 0, None) == UNSUPPORTED
-    assert lib.tf_spec_accept(fake, fake, fake, fake, fake, 1, 4, 100, 0.0, fake, fake, null, None) == INVALID
-    assert lib.tf_spec_accept(fake, null, fake, fake, fake, 1, 4, 100, 1.0, fake, fake, null, None) == INVALID
+    assert lib.tf_spec_accept(fake, fake, fake, fake, fake, 1, 4, 100, 0.0, fake, fake, null, fake, 4096,
+                              None) == INVALID
+    assert lib.tf_spec_accept(fake, null, fake, fake, fake, 1, 4, 100, 1.0, fake, fake, null, fake, 4096,
+                              None) == INVALID
+    assert lib.tf_spec_accept(fake, fake, fake, fake, fake, 1, 4, 100, 1.0, fake, fake, null, null, 0,
+                              None) == WORKSPACE
 
 
 def test_binding_rejects_cpu_tensors():

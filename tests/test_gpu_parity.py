@@ -138,6 +138,18 @@ def test_topk_ties_go_to_lower_ids(cuda_lib):
     assert idx[0, 1].tolist() == list(range(99)) + [2999]
 
 
+def test_topk_all_equal_scores_many_chunks(cuda_lib):
+    """6000 equal scores per unit: the threshold bin holds more keys than the
+    on-chip candidate gather takes, so the cluster resolves it bin by bin."""
+    w = small_workload(B=1, ragged=False, L=8 * 6000)
+    c = make_case(w)
+    M_bits = np.zeros((1, w.Hkv, 6000, 128), dtype=np.uint16)
+    idx, nsel, s_cut = run_topk(cuda_lib, w, c, M_bits, kc=512)
+    for g in range(w.Hkv):
+        assert idx[0, g].tolist() == list(range(512))
+        assert nsel[0, g] == 512 and s_cut[0, g] == 0.0
+
+
 def test_topk_empty_and_tiny_contexts(cuda_lib):
     w = small_workload(B=3, ragged=False, L=64)
     c = make_case(w)
