@@ -105,31 +105,31 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_attn_kernel(GatherPa
 
   if (warp == kComputeWarps) {
     // ---------------------------------------------------------------- producer
+    // Lane l < kSlots owns ring slot l and stages chunks l, l + kSlots, ... on
+    // its own, so the copies of different slots are issued in parallel.
     const uint16_t* Ku = p.K + (size_t)unit * p.Lmax * kHeadDim;
     const uint16_t* Vu = p.V + (size_t)unit * p.Lmax * kHeadDim;
-    for (int base = 0; base < cnt; base += 32) {
+    if (lane < kSlots) {
+      const int slot = lane;
       int y = 0, n = 0;
-      if (base + lane < cnt) chunk_at<MODE>(e0 + base + lane, sel, C, L, has_sink, ns_eff, w0, y, n);
-      const int m = min(32, cnt - base);
-      for (int i = 0; i < m; ++i) {
-        const int yi = __shfl_sync(0xffffffffu, y, i);
-        const int ni = __shfl_sync(0xffffffffu, n, i);
-        if (lane == 0 && !s_abort) {
-          const int k = base + i, slot = k % kSlots;
-          if (k >= kSlots && !mbar_wait(&bar_empty[slot], ((k / kSlots) - 1) & 1)) {
-            atomicExch(&s_abort, 1);
-          } else {
-            slot_n[slot] = ni;
-            uint8_t* dst = ring + slot * kSlotBytes;
-            const uint32_t bytes = (uint32_t)ni * kHeadDim * 2;
-            mbar_arrive_expect_tx(&bar_full[slot], 2 * bytes);
-            if (ni > 0) {
-              bulk_load(dst, Ku + (size_t)yi * kHeadDim, bytes, &bar_full[slot]);
-              bulk_load(dst + 2048, Vu + (size_t)yi * kHeadDim, bytes, &bar_full[slot]);
-            }
-          }
+      if (slot < cnt) chunk_at<MODE>(e0 + slot, sel, C, L, has_sink, ns_eff, w0, y, n);
+      for (int k = slot, j = 0; k < cnt; k += kSlots, ++j) {
+        int yn = 0, nn = 0;  // next chunk's id resolved while this one is in flight
+        if (k + kSlots < cnt) chunk_at<MODE>(e0 + k + kSlots, sel, C, L, has_sink, ns_eff, w0, yn, nn);
+        if (j > 0 && !mbar_wait(&bar_empty[slot], (j - 1) & 1)) {
+          atomicExch(&s_abort, 1);
+          break;
         }
-        __syncwarp();
+        slot_n[slot] = n;
+        uint8_t* dst = ring + slot * kSlotBytes;
+        const uint32_t bytes = (uint32_t)n * kHeadDim * 2;
+        mbar_arrive_expect_tx(&bar_full[slot], 2 * bytes);
+        if (n > 0) {
+          bulk_load(dst, Ku + (size_t)y * kHeadDim, bytes, &bar_full[slot]);
+          bulk_load(dst + 2048, Vu + (size_t)y * kHeadDim, bytes, &bar_full[slot]);
+        }
+        y = yn;
+        n = nn;
       }
     }
   } else {
@@ -280,18 +280,10 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_attn_kernel(GatherPa
 
   const float* ml0 = p.part_ml + (size_t)unit_grp * p.splits_cap * NQ * 2;
   const float* o0 = p.part_o + (size_t)unit_grp * p.splits_cap * NQ * kHeadDim;
-  for (int e = threadIdx.x; e < rows * kHeadDim; e += kGatherThreads) {
-    const int h = e / kHeadDim, d = e % kHeadDim;
-    float mx = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) mx = fmaxf(mx, __ldcg(ml0 + ((size_t)s * NQ + h) * 2));
-    float ls = 0.0f, os = 0.0f;
-    for (int s = 0; s < p.splits; ++s) {
-      const float f = merge_scale(__ldcg(ml0 + ((size_t)s * NQ + h) * 2), mx);
-      ls = fmaf(f, __ldcg(ml0 + ((size_t)s * NQ + h) * 2 + 1), ls);
-      os = fmaf(f, __ldcg(o0 + ((size_t)s * NQ + h) * kHeadDim + d), os);
-    }
-    p.out[((size_t)b * p.Hq + (size_t)g * G + grp * NQ + h) * kHeadDim + d] = (ls > 0.0f) ? os / ls : 0.0f;
-  }
+  float* outp = p.out + ((size_t)b * p.Hq + (size_t)g * G + grp * NQ) * kHeadDim;
+  // The chunk ring is idle now: it serves as the merge scratch.
+  merge_splits(ml0, o0, p.splits, rows, NQ, reinterpret_cast<float*>(ring),
+               [&](int h, int d, float v) { outp[h * kHeadDim + d] = v; });
   if (threadIdx.x == 0) p.tickets[unit_grp] = 0;
 }
 

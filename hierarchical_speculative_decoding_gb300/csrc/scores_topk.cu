@@ -248,9 +248,11 @@ __global__ void __launch_bounds__(kThreads, 2) scores_topk_kernel(
       if (r == S - 1) s_roff[S] = incl;
     }
     __syncthreads();
-    for (int r = 0; r < S; ++r) {
-      const int off = s_roff[r], nc = s_roff[r + 1] - off;
-      for (int i = threadIdx.x; i < nc; i += kThreads) gcand[off + i] = dsmem_ld_u32(cand + i, (uint32_t)r);
+    // one remote load per gathered key, all ranks at once
+    for (int i = threadIdx.x; i < ncand_tot; i += kThreads) {
+      int r = 0;
+      while (r + 1 < S && i >= s_roff[r + 1]) ++r;
+      gcand[i] = dsmem_ld_u32(cand + (i - s_roff[r]), (uint32_t)r);
     }
     __syncthreads();
     // bits 20..10, then 9..0, among the gathered keys (all of them are in bin b1)

@@ -36,22 +36,25 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
+// One poll: the thread may stay suspended (issuing nothing) for up to
+// `suspend_ns` while the phase is incomplete, and resumes as soon as it completes.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase, uint32_t suspend_ns) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(phase)
+      : "r"(smem_u32(bar)), "r"(phase), "r"(suspend_ns)
       : "memory");
   return ok != 0;
 }
 
-// Bounded wait on a phase parity.  Returns false after `limit` polls (each poll
-// itself suspends for a hardware-chosen time slice), so a lost arrival ends in
-// an error status instead of a hung GPU.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, uint32_t limit = (1u << 24)) {
+// Bounded wait on a phase parity.  Waiting threads sleep inside try_wait rather
+// than spinning, so they do not steal issue slots from the warps doing the work.
+// Returns false after `limit` polls of at most 20 us each (about 1.3 s), so a
+// lost arrival ends in an error status instead of a hung GPU.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, uint32_t limit = (1u << 16)) {
   for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, phase)) return true;
+    if (mbar_try_wait(bar, phase, 20000u)) return true;
   return false;
 }
 

@@ -128,4 +128,56 @@ __device__ __forceinline__ float merge_scale(float m_self, float m_new) {
   return (m_self == -INFINITY) ? 0.0f : exp2f(m_self - m_new);
 }
 
+// Final log-sum-exp merge of split-K partial states, run by one CTA.
+// ml: [splits][stride][2] (m, l) and o: [splits][stride][D] in global memory
+// (written by other CTAs; read with L1-bypassing loads); scratch: shared
+// memory for 2 * splits * rows + rows floats.  out(n, d) receives
+// sum_s e^{m_s - m} o_s / sum_s e^{m_s - m} l_s  (0 when every split is empty).
+// The (m, l) pairs are staged first so that every global load below is
+// independent of the others (no chain of round trips per split).
+template <typename Out>
+__device__ void merge_splits(const float* __restrict__ ml, const float* __restrict__ o, int splits, int rows,
+                             int stride, float* scratch, Out out) {
+  float* sm_w = scratch;                  // [splits][rows]: m, then the weight e^{m_s - m}
+  float* sm_l = scratch + splits * rows;  // [splits][rows]
+  float* sm_L = sm_l + splits * rows;     // [rows]
+  for (int i = threadIdx.x; i < splits * rows; i += blockDim.x) {
+    const int sp = i / rows, n = i % rows;
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(ml) + (size_t)sp * stride + n);
+    sm_w[i] = v.x;
+    sm_l[i] = v.y;
+  }
+  __syncthreads();
+  for (int n = threadIdx.x; n < rows; n += blockDim.x) {
+    float mx = -INFINITY;
+    for (int sp = 0; sp < splits; ++sp) mx = fmaxf(mx, sm_w[sp * rows + n]);
+    float L = 0.0f;
+    for (int sp = 0; sp < splits; ++sp) {
+      const float w = merge_scale(sm_w[sp * rows + n], mx);
+      sm_w[sp * rows + n] = w;
+      L = fmaf(w, sm_l[sp * rows + n], L);
+    }
+    sm_L[n] = L;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < rows * kHeadDim; e += blockDim.x) {
+    const int n = e / kHeadDim, d = e % kHeadDim;
+    const float* on = o + (size_t)n * kHeadDim + d;
+    const size_t sstride = (size_t)stride * kHeadDim;
+    float acc = 0.0f;
+    int sp = 0;
+    for (; sp + 4 <= splits; sp += 4) {
+      const float v0 = __ldcg(on + (sp + 0) * sstride), v1 = __ldcg(on + (sp + 1) * sstride);
+      const float v2 = __ldcg(on + (sp + 2) * sstride), v3 = __ldcg(on + (sp + 3) * sstride);
+      acc = fmaf(sm_w[(sp + 0) * rows + n], v0, acc);
+      acc = fmaf(sm_w[(sp + 1) * rows + n], v1, acc);
+      acc = fmaf(sm_w[(sp + 2) * rows + n], v2, acc);
+      acc = fmaf(sm_w[(sp + 3) * rows + n], v3, acc);
+    }
+    for (; sp < splits; ++sp) acc = fmaf(sm_w[sp * rows + n], __ldcg(on + sp * sstride), acc);
+    const float L = sm_L[n];
+    out(n, d, L > 0.0f ? acc / L : 0.0f);
+  }
+}
+
 }  // namespace tf

@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     if (tid == 0) atomicExch(p.status, 1);
     // Let any TMA copy still in flight land before the CTA's shared memory goes away.
     if (tid == 0)
-      for (int s = 0; s < kStages; ++s) mbar_wait(&bar_full[s], 0, 1u << 16);
+      for (int s = 0; s < kStages; ++s) mbar_wait(&bar_full[s], 0, 1u << 8);
     return;
   }
   if (p.splits == 1) return;
@@ -395,18 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   const float* ml0 = p.part_ml + (size_t)ug * p.splits_cap * kMaxRows * 2;
   const float* o0 = p.part_o + (size_t)ug * p.splits_cap * kMaxRows * kHeadDim;
   const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
-  for (int e = tid; e < rows * kHeadDim; e += kThreads) {
-    const int n = e / kHeadDim, d = e % kHeadDim;
-    float mx = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) mx = fmaxf(mx, __ldcg(ml0 + ((size_t)s * kMaxRows + n) * 2));
-    float ls = 0.0f, os = 0.0f;
-    for (int s = 0; s < p.splits; ++s) {
-      const float f = merge_scale(__ldcg(ml0 + ((size_t)s * kMaxRows + n) * 2), mx);
-      ls = fmaf(f, __ldcg(ml0 + ((size_t)s * kMaxRows + n) * 2 + 1), ls);
-      os = fmaf(f, __ldcg(o0 + ((size_t)s * kMaxRows + n) * kHeadDim + d), os);
-    }
-    p.out[(out_row0 + n) * kHeadDim + d] = (ls > 0.0f) ? os / ls : 0.0f;
-  }
+  float* out = p.out;
+  // The K/V ring is idle now: it serves as the merge scratch.
+  merge_splits(ml0, o0, p.splits, rows, kMaxRows, reinterpret_cast<float*>(smem),
+               [&](int n, int d, float v) { out[(out_row0 + n) * kHeadDim + d] = v; });
   if (tid == 0) p.tickets[ug] = 0;
 }
 
