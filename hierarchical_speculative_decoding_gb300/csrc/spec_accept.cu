@@ -148,31 +148,39 @@ __global__ void __launch_bounds__(GS == 32 ? 256 : GS) accept_kernel(
   const int R = 2 * gamma + 1;
   const int lane = threadIdx.x & 31;
 
-  // ---- draft length and the sequential ratio tests (group thread 0, fp64)
+  // ---- draft length and the ratio tests (fp64)
+  // The group's first warp takes 32 draft positions at a time: lane i loads
+  // everything test i needs (all loads in flight together) and decides it; the
+  // first position outside the draft and the first rejection come from ballots.
   int nacc = 0, g = 0;
-  if (live && gid == 0) {
-    const int32_t* x = tokens + (size_t)b * gamma;
+  if (live && gid < 32) {
     g = gamma;
-    for (int i = 0; i < gamma; ++i)
-      if (x[i] < 0 || x[i] >= V) {
-        g = i;
-        break;
+    int first_rej = gamma;
+    for (int base = 0; base < gamma; base += 32) {
+      const int i = base + gid;
+      bool in_draft = false, accept = false;
+      if (i < gamma) {
+        const int xi = tokens[(size_t)b * gamma + i];
+        in_draft = xi >= 0 && xi < V;
+        if (in_draft) {
+          const double zp = ws.z[(size_t)b * R + i];
+          const double zq = ws.z[(size_t)b * R + gamma + 1 + i];
+          const double lp =
+              (double)tgt[((size_t)b * (gamma + 1) + i) * V + xi] * inv_t_d - (double)ws.m[(size_t)b * R + i];
+          const double lq = (double)drf[((size_t)b * gamma + i) * V + xi] * inv_t_d -
+                            (double)ws.m[(size_t)b * R + gamma + 1 + i];
+          const double ua = (double)u_acc[(size_t)b * gamma + i];
+          accept = (exp2(lq) / zq == 0.0) || ua <= exp2(lp - lq) * (zq / zp);
+        }
       }
-    nacc = g;
-    for (int i = 0; i < g; ++i) {
-      const int xi = x[i];
-      const double mp = ws.m[(size_t)b * R + i], zp = ws.z[(size_t)b * R + i];
-      const double mq = ws.m[(size_t)b * R + gamma + 1 + i], zq = ws.z[(size_t)b * R + gamma + 1 + i];
-      const double lp = (double)tgt[((size_t)b * (gamma + 1) + i) * V + xi] * inv_t_d - mp;
-      const double lq = (double)drf[((size_t)b * gamma + i) * V + xi] * inv_t_d - mq;
-      const double qx = exp2(lq) / zq;
-      const double ratio = exp2(lp - lq) * (zq / zp);
-      const bool accept = (qx == 0.0) || ((double)u_acc[(size_t)b * gamma + i] <= ratio);
-      if (!accept) {
-        nacc = i;
-        break;
-      }
+      const unsigned outside = __ballot_sync(0xffffffffu, i < gamma && !in_draft);
+      const unsigned rej = __ballot_sync(0xffffffffu, in_draft && !accept);
+      if (outside) g = base + __ffs(outside) - 1;
+      if (rej) first_rej = base + __ffs(rej) - 1;
+      if (outside || rej) break;  // the first of the two ends the tests (warp-uniform)
     }
+    // a rejection past the end of the draft is no rejection
+    nacc = min(g, first_rej);
   }
   if (GS == 32) {
     g = __shfl_sync(0xffffffffu, g, 0);

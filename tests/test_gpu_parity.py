@@ -297,6 +297,19 @@ def test_spec_accept_short_and_empty_drafts(cuda_lib):
     compare_accept(got, want)
 
 
+@pytest.mark.parametrize("gamma,V", [(33, 500), (70, 2048)])
+def test_spec_accept_long_drafts(cuda_lib, gamma, V):
+    """Drafts longer than one warp of tests: a close drafter keeps most tokens,
+    so acceptance runs past position 32; some drafts also end early."""
+    tgt, drf, x, ua, ur = synth.accept_inputs(96, gamma, V, seed=gamma + V, drf_noise=0.02)
+    x[0:8, 40 % gamma] = -1
+    got = run_accept(cuda_lib, tgt, drf, x, ua, ur)
+    want = O.spec_accept(tgt.double().numpy(), drf.double().numpy(), x.numpy(), ua.double().numpy(),
+                         ur.double().numpy())
+    assert np.any(want["n_acc"] > 32)
+    compare_accept(got, want)
+
+
 def test_spec_accept_identical_distributions(cuda_lib):
     tgt, drf, x, ua, ur = synth.accept_inputs(128, 4, 300, seed=5)
     drf = tgt[:, :4].clone()
