@@ -1,8 +1,10 @@
 """Benchmark: draft+verify attention steps/s of the TriForce decode step at 128K.
 
-One step = for every layer, in order: chunk scores + top-k (Force 2 retrieval),
-sparse decode attention over the retrieved chunks (Force 2), sink + window
-attention (Force 1), full-cache verification of gamma+1 = 6 queries (Force 3).
+One step = for every layer, in order: chunk scores + top-k + sparse decode
+attention over the retrieved chunks (the Force 2 retrieval drafter, one fused
+launch; --two-call-draft runs it as the separate top-k and sparse-attention
+calls), sink + window attention (Force 1), full-cache verification of
+gamma+1 = 6 queries (Force 3).
 Workload: the full 32-layer Llama2-7B-128K KV cache (32 heads x 128 dims x
 131072 tokens, bf16, 64 GiB), seeded synthetic data with 1% planted chunks.
 
@@ -42,6 +44,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (profiling runs only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--two-call-draft", action="store_true",
+                    help="run the retrieval drafter as tf_chunk_scores_topk + tf_sparse_decode_attn")
     return ap.parse_args()
 
 
@@ -280,25 +284,30 @@ def run_gpu(args):
     ws_ver = tf.workspace(tf.tf_verify_attn_workspace(B, Hq, Hkv, L, T), dev)
 
     stream = torch.cuda.current_stream()
-    kinds = ("topk", "sparse", "window", "verify")
+    kinds = ("draft", "window", "verify")
+
+    def draft(l):
+        if args.two_call_draft:
+            tf.tf_chunk_scores_topk(q_all[l], Mc[l], seq, L, w.kc, idx[l], nsel[l], ws=ws_topk)
+            tf.tf_sparse_decode_attn(q_all[l], Kc[l], Vc[l], seq, idx[l], nsel[l], scale, out=o_sp[l], ws=ws_sp)
+        else:
+            tf.tf_retrieval_draft_attn(q_all[l], Mc[l], Kc[l], Vc[l], seq, w.kc, scale, idx=idx[l], n_sel=nsel[l],
+                                       out=o_sp[l])
 
     def step(evs=None):
         for l in range(layers):
             if evs is not None:
                 evs[l][0].record(stream)
-            tf.tf_chunk_scores_topk(q_all[l], Mc[l], seq, L, w.kc, idx[l], nsel[l], ws=ws_topk)
+            draft(l)
             if evs is not None:
                 evs[l][1].record(stream)
-            tf.tf_sparse_decode_attn(q_all[l], Kc[l], Vc[l], seq, idx[l], nsel[l], scale, out=o_sp[l], ws=ws_sp)
-            if evs is not None:
-                evs[l][2].record(stream)
             tf.tf_stream_window_attn(q_all[l], Kc[l], Vc[l], seq, w.n_sink, w.window, scale, out=o_win[l],
                                      ws=ws_win)
             if evs is not None:
-                evs[l][3].record(stream)
+                evs[l][2].record(stream)
             tf.tf_verify_attn(Q_all[l], Kc[l], Vc[l], seq, scale, out=o_ver[l], ws=ws_ver)
             if evs is not None:
-                evs[l][4].record(stream)
+                evs[l][3].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -322,7 +331,7 @@ def run_gpu(args):
     # ---- second timed region for the per-kernel breakdown and the verify
     # roofline: an event before and after every launch.
     k_steps = max(3, args.steps // 2)
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(layers)] for _ in range(k_steps)]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(layers)] for _ in range(k_steps)]
     torch.cuda.synchronize()
     for s in range(k_steps):
         step(evs[s])
@@ -339,18 +348,34 @@ def run_gpu(args):
     bytes_sparse = 2 * B * Hkv * w.kc * w.chunk * kv_row + B * Hkv * w.kc * 4 + B * Hq * D * (2 + 4)
     bytes_window = 2 * B * Hkv * min(L, w.n_sink + w.window) * kv_row + B * Hq * D * (2 + 4)
     bytes_verify = 2 * B * Hkv * L * kv_row + B * Hq * T * D * (2 + 4)
-    kbytes = {"topk": bytes_topk, "sparse": bytes_sparse, "window": bytes_window, "verify": bytes_verify}
+    # fused retrieval drafter: means, queries, the selection written, selected K/V rows, outputs
+    bytes_draft = (B * Hkv * Cmax * D * 2 + B * Hq * D * 2 + B * Hkv * w.kc * 4 +
+                   2 * B * Hkv * w.kc * w.chunk * kv_row + B * Hq * D * 4)
+    kbytes = {"draft": bytes_draft, "window": bytes_window, "verify": bytes_verify}
     peak, peak_kind = measured_peaks()
     kernels = {}
     for k in kinds:
         ms = statistics.mean(per_kind[k])
-        kernels[k] = {"ms": round(ms, 5), "GBps": round(kbytes[k] / (ms / 1e3) / 1e9, 1),
-                      "frac_hbm": round(kbytes[k] / (ms / 1e3) / 1e9 / peak, 4)}
-    draft_ms = statistics.mean(per_kind["topk"]) + statistics.mean(per_kind["sparse"])
-    kernels["retrieval_draft"] = {
-        "ms": round(draft_ms, 5),
-        "GBps": round((bytes_topk + bytes_sparse) / (draft_ms / 1e3) / 1e9, 1),
-        "frac_hbm": round((bytes_topk + bytes_sparse) / (draft_ms / 1e3) / 1e9 / peak, 4)}
+        name = "retrieval_draft" if k == "draft" else k
+        kernels[name] = {"ms": round(ms, 5), "GBps": round(kbytes[k] / (ms / 1e3) / 1e9, 1),
+                         "frac_hbm": round(kbytes[k] / (ms / 1e3) / 1e9 / peak, 4)}
+    kernels["retrieval_draft"]["calls"] = ("tf_chunk_scores_topk + tf_sparse_decode_attn" if args.two_call_draft
+                                           else "tf_retrieval_draft_attn")
+    # the two-call form of the retrieval drafter, for comparison (events around each call)
+    if not args.two_call_draft:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(layers)]
+        torch.cuda.synchronize()
+        for l in range(layers):
+            ev[l][0].record(stream)
+            tf.tf_chunk_scores_topk(q_all[l], Mc[l], seq, L, w.kc, idx[l], nsel[l], ws=ws_topk)
+            ev[l][1].record(stream)
+            tf.tf_sparse_decode_attn(q_all[l], Kc[l], Vc[l], seq, idx[l], nsel[l], scale, out=o_sp[l], ws=ws_sp)
+            ev[l][2].record(stream)
+        torch.cuda.synchronize()
+        for i, (k, nb) in enumerate((("topk", bytes_topk), ("sparse", bytes_sparse))):
+            ms = statistics.mean(ev[l][i].elapsed_time(ev[l][i + 1]) for l in range(layers))
+            kernels["two_call_" + k] = {"ms": round(ms, 5), "GBps": round(nb / (ms / 1e3) / 1e9, 1),
+                                        "frac_hbm": round(nb / (ms / 1e3) / 1e9 / peak, 4)}
     kernels["chunk_means_prefill_1layer"] = {"ms": round(means_ms, 4),
                                              "GBps": round(means_bytes / (means_ms / 1e3) / 1e9, 1)}
     ver_ms = statistics.mean(per_kind["verify"])
@@ -369,7 +394,7 @@ def run_gpu(args):
                      "algorithmic_bytes": bytes_verify, "peak_source": peak_kind},
         "kernels": kernels,
         "kernel_timing": f"CUDA events around every launch, {k_steps} further steps after the timed region",
-        "gpu_launches": args.steps * layers * 4,
+        "gpu_launches": args.steps * layers * (4 if args.two_call_draft else 3),
         "clocks": clocks.summary(),
     }
 

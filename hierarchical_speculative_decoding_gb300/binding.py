@@ -33,6 +33,7 @@ _SIGS = {
     "tf_sparse_decode_attn_workspace": (_S, [_I, _I, _I, _I]),
     "tf_sparse_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_sparse_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
+    "tf_retrieval_draft_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
     "tf_stream_window_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
     "tf_stream_window_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_verify_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
@@ -179,6 +180,34 @@ def tf_sparse_decode_attn(q, K, V, seq_lens, idx, n_sel, scale, out=None, ws=Non
                                         Hkv, Lmax, D, chunk, kc, float(scale), _ptr(out), _ptr(ws), nbytes,
                                         _stream(stream)), "tf_sparse_decode_attn")
     return out
+
+
+def tf_retrieval_draft_attn(q, M, K, V, seq_lens, kc, scale, idx=None, n_sel=None, s_cut=None, out=None, chunk=8,
+                            stream=None):
+    """Scores, top-k and sparse attention of the retrieval drafter in one launch.
+    Returns (idx, n_sel, out); s_cut is filled when given."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(M, torch.bfloat16, "M", 4)
+    _need(K, torch.bfloat16, "K", 4)
+    _need(V, torch.bfloat16, "V", 4)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = K.shape
+    if idx is None:
+        idx = torch.empty((B, Hkv, kc), dtype=torch.int32, device=q.device)
+    if n_sel is None:
+        n_sel = torch.empty((B, Hkv), dtype=torch.int32, device=q.device)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(idx, torch.int32, "idx", 3)
+    _need(n_sel, torch.int32, "n_sel", 2)
+    _need(out, torch.float32, "out", 3)
+    if s_cut is not None:
+        _need(s_cut, torch.float32, "s_cut", 2)
+    _check(load().tf_retrieval_draft_attn(_ptr(q), _ptr(M), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax, D,
+                                          chunk, kc, float(scale), _ptr(idx), _ptr(n_sel), _ptr(s_cut), _ptr(out),
+                                          _stream(stream)), "tf_retrieval_draft_attn")
+    return idx, n_sel, out
 
 
 def tf_sparse_decode_attn_noalloc(q, K, V, seq_lens, idx, n_sel, scale, out, chunk=8, stream=None):

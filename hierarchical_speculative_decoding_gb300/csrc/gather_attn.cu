@@ -14,7 +14,8 @@
 // 64 MiB): split-K over the chunk list.  A producer warp stages chunks into a
 // 16-slot shared-memory ring with untiled bulk copies (cp.async.bulk: a chunk's
 // K rows and V rows are each one contiguous run of n x 256 bytes; mbarrier
-// complete-tx), 32 chunk ids resolved per batch so no copy waits on an id.
+// complete-tx), chunk ids resolved 32 at a time so no copy waits on an id;
+// only one lane of the producer warp ever waits on a barrier.
 // Four compute warps take chunks in turn: lane (row r, quarter dq) forms
 // 32-dim partial dot products, visiting its four 16-byte pieces in a rotated
 // order that keeps the shared-memory reads conflict-free; the row score is
@@ -34,6 +35,10 @@ constexpr int kComputeWarps = 4;
 constexpr int kSlots = 16;
 constexpr int kSlotBytes = 4096;  // K rows [0, 2 KB), V rows [2 KB, 4 KB)
 constexpr int kGatherSmem = kSlots * kSlotBytes + 128;  // + alignment slack
+// Chunk k sits in slot k % 16 and is consumed by compute warp k % 4: every use
+// of a slot is consumed by the same warp, so a phase-parity wait never runs two
+// phases ahead of its barrier.
+static_assert(kSlots % kComputeWarps == 0, "a slot must always be consumed by the same warp");
 
 // The i-th chunk of a unit's position set: first position y and valid rows n.
 template <int MODE>
@@ -62,7 +67,7 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_attn_kernel(GatherPa
   __shared__ int slot_n[kSlots];
   __shared__ float sm_m[kComputeWarps][NQ], sm_l[kComputeWarps][NQ];
   __shared__ float sm_o[kComputeWarps][NQ][kHeadDim];
-  __shared__ int s_last, s_abort;
+  __shared__ int s_last, s_abort, s_issued;
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
   const int unit_grp = blockIdx.y;
@@ -77,6 +82,7 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_attn_kernel(GatherPa
       mbar_init(&bar_empty[s], 1);
     }
     s_abort = 0;
+    s_issued = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -105,33 +111,48 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_attn_kernel(GatherPa
 
   if (warp == kComputeWarps) {
     // ---------------------------------------------------------------- producer
-    // Lane l < kSlots owns ring slot l and stages chunks l, l + kSlots, ... on
-    // its own, so the copies of different slots are issued in parallel.
+    // Chunk positions are resolved 32 at a time, one per lane.  The first use
+    // of every ring slot needs no wait, so those lanes issue at once; every
+    // later chunk is issued in order by lane 0 alone, so that no two lanes of
+    // this warp ever wait on different barriers (diverged lanes need not be
+    // scheduled fairly, and a wait that starves another lane could time out).
     const uint16_t* Ku = p.K + (size_t)unit * p.Lmax * kHeadDim;
     const uint16_t* Vu = p.V + (size_t)unit * p.Lmax * kHeadDim;
-    if (lane < kSlots) {
-      const int slot = lane;
+    auto issue = [&](int slot, int y, int n) {
+      slot_n[slot] = n;
+      uint8_t* dst = ring + slot * kSlotBytes;
+      const uint32_t bytes = (uint32_t)n * kHeadDim * 2;
+      mbar_arrive_expect_tx(&bar_full[slot], 2 * bytes);
+      if (n > 0) {
+        bulk_load(dst, Ku + (size_t)y * kHeadDim, bytes, &bar_full[slot]);
+        bulk_load(dst + 2048, Vu + (size_t)y * kHeadDim, bytes, &bar_full[slot]);
+      }
+    };
+    int issued = 0;  // chunks [0, issued) have been staged
+    for (int base = 0; base < cnt; base += 32) {
       int y = 0, n = 0;
-      if (slot < cnt) chunk_at<MODE>(e0 + slot, sel, C, L, has_sink, ns_eff, w0, y, n);
-      for (int k = slot, j = 0; k < cnt; k += kSlots, ++j) {
-        int yn = 0, nn = 0;  // next chunk's id resolved while this one is in flight
-        if (k + kSlots < cnt) chunk_at<MODE>(e0 + k + kSlots, sel, C, L, has_sink, ns_eff, w0, yn, nn);
-        if (j > 0 && !mbar_wait(&bar_empty[slot], (j - 1) & 1)) {
-          atomicExch(&s_abort, 1);
-          break;
+      if (base + lane < cnt) chunk_at<MODE>(e0 + base + lane, sel, C, L, has_sink, ns_eff, w0, y, n);
+      if (base + lane < cnt && base + lane < kSlots) issue(base + lane, y, n);
+      bool ok = true;
+      for (int t = 0; t < 32 && base + t < cnt; ++t) {  // warp-uniform
+        const int k = base + t;
+        const int yk = __shfl_sync(0xffffffffu, y, t), nk = __shfl_sync(0xffffffffu, n, t);
+        if (k >= kSlots) {
+          if (lane == 0) {
+            ok = mbar_wait(&bar_empty[k % kSlots], (k / kSlots - 1) & 1);
+            if (ok) issue(k % kSlots, yk, nk);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
         }
-        slot_n[slot] = n;
-        uint8_t* dst = ring + slot * kSlotBytes;
-        const uint32_t bytes = (uint32_t)n * kHeadDim * 2;
-        mbar_arrive_expect_tx(&bar_full[slot], 2 * bytes);
-        if (n > 0) {
-          bulk_load(dst, Ku + (size_t)y * kHeadDim, bytes, &bar_full[slot]);
-          bulk_load(dst + 2048, Vu + (size_t)y * kHeadDim, bytes, &bar_full[slot]);
-        }
-        y = yn;
-        n = nn;
+        issued = k + 1;
+      }
+      if (!ok) {
+        if (lane == 0) atomicExch(&s_abort, 1);
+        break;
       }
     }
+    if (lane == 0) s_issued = issued;
   } else {
     // ---------------------------------------------------------------- compute warps
     // Score phase: lane = (row r, quarter dq) reads 16-byte pieces j of dims
@@ -237,6 +258,15 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_attn_kernel(GatherPa
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) sm_o[warp][h][lane * 4 + i] = o[h][i];
+    }
+  }
+  __syncthreads();
+  if (s_abort && threadIdx.x == 0) {
+    // (only after a timeout) let every copy still in flight land before the
+    // ring is reused or the CTA exits
+    for (int sl = 0; sl < kSlots && sl < s_issued; ++sl) {
+      const int klast = sl + (s_issued - 1 - sl) / kSlots * kSlots;
+      mbar_wait(&bar_full[sl], (klast / kSlots) & 1, 1u << 8);
     }
   }
   __syncthreads();

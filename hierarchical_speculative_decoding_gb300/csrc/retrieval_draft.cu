@@ -1,0 +1,513 @@
+// a2 + a3 + a4 (+ a5) fused -- the Force 2 retrieval drafter's decode attention
+// in one launch: chunk scores, top-k selection and attention over the selected
+// chunks.
+//
+// "TriForce: Hierarchical Speculative Decoding for LLMs", "The Three Forces of
+// TriForce": the retrieval drafter is the target model attending only to the
+// KV blocks whose key-query similarity is highest, within a fixed budget.
+// Outputs are those of the top-k call (idx, n_sel, s_cut) and of the sparse
+// attention call over that selection (out), computed in one pass.
+//
+// Design: the top-k cluster (one cluster of S <= 8 CTAs per (b, g) unit, CTA r
+// scoring the r-th slice of the chunk means; see topk_select.cuh) keeps going
+// after the cut: each CTA attends the chunks it selected itself, so no chunk
+// list goes through global memory and no second launch waits for the first.
+//  * As soon as the first cluster histogram round fixes the bin b1 of the cut,
+//    every key in a bin above b1 is known to be selected; the CTA lists those
+//    chunks and starts bulk copies (cp.async.bulk, complete-tx on an mbarrier)
+//    of the first eight into the part of the ring that the selection does not
+//    use, so HBM keeps working while the cut is resolved.
+//  * After the id-order compaction, warp 15 stages the rest of the list into
+//    the 15-slot ring (one lane per slot for the first round, then in list
+//    order as slots free up), and warp w of 0..14 takes chunks w, w + 15, ...
+//    from its own slot: lane (row r,
+//    quarter dq) forms 32-dim dot products with the query rows held in shared
+//    memory in a bank-conflict-free permuted layout, the online softmax runs in
+//    the log2 domain in fp32, and each lane owns 4 head dims of P V.
+//  * Warps merge in shared memory, then CTA rank 0 merges the S partial states
+//    of the cluster through distributed shared memory (log-sum-exp identity)
+//    and writes the output.
+// All waits are bounded; a timeout (only a hardware fault can cause one)
+// leaves NaN in the outputs.
+#include "topk_select.cuh"
+
+namespace tf {
+namespace {
+
+using namespace sm100;
+using topk::kMaxCluster;
+using topk::kMaxSliceKeys;
+using topk::kThreads;
+using topk::kWarps;
+
+constexpr int kProducerWarp = kWarps - 1;
+constexpr int kComputeWarps = kWarps - 1;
+// One ring slot per compute warp: chunk k sits in slot k % 15 and is consumed
+// by warp k % 15, so every use of a slot is waited for by the warp that
+// consumed the previous one and a phase-parity wait can never run two phases
+// ahead of its barrier.
+constexpr int kRingSlots = kComputeWarps;
+constexpr int kEarlySlots = 8;   // ring slots that do not overlay the selection arrays
+constexpr int kSlotBytes = 4096;  // K rows [0, 2 KB), V rows [2 KB, 4 KB)
+constexpr int kCandCap = 2048;    // keys of the threshold bin gathered on every CTA
+constexpr int kMaxList = 2048;    // selected chunks per CTA (kc <= kMaxList)
+
+// Dynamic shared memory (bytes).  The histograms overlay ring slots 8..14,
+// which are first written after the cut; the candidate buffers (cand is read
+// by the other CTAs until the last cluster barrier) and the chunk list have
+// their own space.
+constexpr int kOffHist1 = kEarlySlots * kSlotBytes;  // 32768
+constexpr int kOffHist2 = kOffHist1 + 2048 * 4;
+constexpr int kOffHist3 = kOffHist2 + 2048 * 4;
+constexpr int kOffTot = kOffHist3 + 1024 * 4;
+constexpr int kOffGcand = kOffTot + 2048 * 4;      // 61440 = end of the ring
+constexpr int kOffCand = kOffGcand + kCandCap * 4;  // 69632
+constexpr int kOffList = kOffCand + kCandCap * 4;   // 77824
+constexpr int kOffKeys = kOffList + kMaxList * 4;   // 86016
+static_assert(kOffGcand >= kRingSlots * kSlotBytes, "the candidate buffers must not overlay the ring");
+
+struct DraftParams {
+  const uint16_t* q;  // [B, Hq, 128]
+  const uint16_t* M;  // [B, Hkv, Cmax, 128]
+  const uint16_t* K;  // [B, Hkv, Lmax, 128]
+  const uint16_t* V;
+  const int32_t* seq_lens;
+  int Hq, Hkv, Lmax, kc;
+  float scale_log2;  // softmax scale * log2(e)
+  int32_t* idx;      // [B, Hkv, kc]
+  int32_t* n_sel;    // [B, Hkv]
+  float* s_cut;      // [B, Hkv] or null
+  float* out;        // [B, Hq, 128]
+};
+
+size_t draft_smem(int slice) { return (size_t)kOffKeys + (size_t)slice * sizeof(uint32_t); }
+
+template <int NQ>
+__global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(16) float qsm[NQ * kHeadDim];  // scaled query rows, permuted (see below)
+  __shared__ float qs[kHeadDim];                      // the group's summed query (scores)
+  __shared__ __align__(8) uint64_t bar_full[kRingSlots], bar_empty[kRingSlots];
+  __shared__ int slot_n[kRingSlots];
+  __shared__ float wm[kComputeWarps][NQ], wl[kComputeWarps][NQ];
+  __shared__ float cpart[NQ][kHeadDim], cm[NQ], cl[NQ];
+  __shared__ uint32_t s_min;
+  __shared__ int s_na, s_ntot, s_abort, s_issued, s_wcnt[kWarps];
+
+  uint8_t* ring = smem;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kOffKeys);
+  int32_t* alist = reinterpret_cast<int32_t*>(smem + kOffList);
+  const topk::Arrays a{keys,
+                       reinterpret_cast<uint32_t*>(smem + kOffHist1),
+                       reinterpret_cast<uint32_t*>(smem + kOffHist2),
+                       reinterpret_cast<uint32_t*>(smem + kOffHist3),
+                       reinterpret_cast<uint32_t*>(smem + kOffTot),
+                       reinterpret_cast<uint32_t*>(smem + kOffCand),
+                       reinterpret_cast<uint32_t*>(smem + kOffGcand),
+                       kCandCap};
+
+  const int S = (int)gridDim.x;  // the cluster spans grid x
+  const uint32_t rank = cluster_ctarank();
+  const int unit = blockIdx.y;
+  const int b = unit / p.Hkv, g = unit % p.Hkv;
+  const int G = p.Hq / p.Hkv;  // <= NQ
+  const int Cmax = (p.Lmax + kChunk - 1) / kChunk;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRingSlots; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    s_abort = 0;
+    s_issued = 0;
+    s_min = 0xffffffffu;
+    fence_mbar_init();
+  }
+  topk::zero_hists(a);
+  pdl_wait();
+  const int L = clamp_len(p.seq_lens[b], p.Lmax);
+  const int C = (L + kChunk - 1) / kChunk;
+  const int per = (C + S - 1) / S;
+  const int c0 = min(C, (int)rank * per);
+  const int c1 = min(C, c0 + per);
+  const int n = c1 - c0;
+
+  // Queries.  Head h's scaled row is stored so that the 16-byte piece of dims
+  // [32 dq + 8 jr + 4 hf, +4) sits at 16-byte unit hf * 16 + 4 dq + jr: the
+  // eight (dq, jr) pairs read together by a quarter-warp below then fall in
+  // eight different bank groups.
+  const uint16_t* qg = p.q + ((size_t)b * p.Hq + (size_t)g * G) * kHeadDim;
+  if (threadIdx.x < kHeadDim) {
+    float s = 0.0f;
+    for (int h = 0; h < G; ++h) s += __uint_as_float((uint32_t)qg[h * kHeadDim + threadIdx.x] << 16);
+    qs[threadIdx.x] = s;
+  }
+  for (int e = threadIdx.x; e < NQ * kHeadDim; e += kThreads) {
+    const int h = e / kHeadDim, d = e % kHeadDim;
+    const float v = h < G ? __uint_as_float((uint32_t)qg[h * kHeadDim + d] << 16) * p.scale_log2 : 0.0f;
+    const int u = ((d >> 2) & 1) * 16 + 4 * (d >> 5) + ((d >> 3) & 3);
+    qsm[h * kHeadDim + u * 4 + (d & 3)] = v;
+  }
+  __syncthreads();
+  topk::score_slice(qs, p.M + (size_t)unit * Cmax * kHeadDim, c0, c1, a);
+  __syncthreads();
+
+  const uint16_t* Ku = p.K + (size_t)unit * p.Lmax * kHeadDim;
+  const uint16_t* Vu = p.V + (size_t)unit * p.Lmax * kHeadDim;
+  // Stage chunk c (its valid rows of K and of V) into a ring slot.  An id
+  // outside [0, C) cannot come out of the selection; it is refused all the
+  // same (the slot completes empty and the outputs are poisoned) rather than
+  // turned into a copy from outside the cache.
+  auto issue = [&](int slot, int c) {
+    if (c < 0 || c >= C) {
+      atomicExch(&s_abort, 1);
+      slot_n[slot] = 0;
+      mbar_arrive(&bar_full[slot]);
+      return;
+    }
+    const int y = c * kChunk;
+    const int nr = min(kChunk, L - y);
+    slot_n[slot] = nr;
+    const uint32_t bytes = (uint32_t)nr * kHeadDim * 2;
+    uint8_t* dst = ring + slot * kSlotBytes;
+    mbar_arrive_expect_tx(&bar_full[slot], 2 * bytes);
+    bulk_load(dst, Ku + (size_t)y * kHeadDim, bytes, &bar_full[slot]);
+    bulk_load(dst + 2048, Vu + (size_t)y * kHeadDim, bytes, &bar_full[slot]);
+  };
+
+  int32_t* out_idx = p.idx + (size_t)unit * p.kc;
+  uint32_t T = 0;
+  if (C <= p.kc) {
+    // Every chunk is selected: ids in order, slots past C hold -1, s_cut = min score.
+    uint32_t mn = 0xffffffffu;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      out_idx[c0 + i] = c0 + i;
+      alist[i] = c0 + i;
+      mn = min(mn, keys[i]);
+    }
+    if (rank == 0)
+      for (int i = C + (int)threadIdx.x; i < p.kc; i += kThreads) out_idx[i] = -1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    if (lane == 0) atomicMin(&s_min, mn);
+    if (threadIdx.x == 0) {
+      s_na = n;
+      s_ntot = n;
+    }
+    __syncthreads();
+    if ((int)threadIdx.x < min(kEarlySlots, n)) issue(threadIdx.x, alist[threadIdx.x]);
+  } else {
+    // List the chunks above bin b1 (selected whatever the rest of the cut) and
+    // start copying the first of them while the cut is resolved.
+    auto early = [&](uint32_t b1) {
+      const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
+      const int w0 = warp * seg, w1 = min(n, w0 + seg);
+      const unsigned lt = (1u << lane) - 1u;
+      int cnt = 0;
+      for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        cnt += __popc(__ballot_sync(0xffffffffu, i < w1 && (keys[i] >> 21) > b1));
+      }
+      if (lane == 0) s_wcnt[warp] = cnt;
+      __syncthreads();
+      int pos = 0;
+      for (int w = 0; w < warp; ++w) pos += s_wcnt[w];
+      if (warp == kWarps - 1 && lane == 0) {
+        s_na = pos + cnt;
+        s_ntot = pos + cnt;
+      }
+      for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        const bool sel = i < w1 && (keys[i] >> 21) > b1;
+        const unsigned bs = __ballot_sync(0xffffffffu, sel);
+        if (sel) alist[pos + __popc(bs & lt)] = c0 + i;
+        pos += __popc(bs);
+      }
+      __syncthreads();
+      if ((int)threadIdx.x < min(kEarlySlots, s_na)) issue(threadIdx.x, alist[threadIdx.x]);
+    };
+    const topk::Cut cut = topk::find_cut(a, n, p.kc, S, rank, early);
+    T = cut.T;
+    topk::compact<true>(a, n, p.kc, cut, s_na, [&](int i, int pos, int upos) {
+      out_idx[pos] = c0 + i;
+      if (upos >= 0 && upos < kMaxList) {
+        alist[upos] = c0 + i;
+        atomicMax(&s_ntot, upos + 1);
+      }
+    });
+    __syncthreads();
+  }
+  const int ntot = s_ntot;
+  const int n_pre = min(kEarlySlots, s_na);
+
+  // ---------------------------------------------------------------- attention
+  constexpr int rows_cap = NQ;
+  const int rows = G < rows_cap ? G : rows_cap;
+  float m[NQ], l[NQ], o[NQ][4];
+#pragma unroll
+  for (int h = 0; h < NQ; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[h][i] = 0.0f;
+  }
+  if (warp == kProducerWarp) {
+    // Slots 8..14 held the histograms (generic-proxy writes): order those
+    // before the bulk copies that now overwrite them.
+    fence_proxy_async_smem();
+    // First use of every slot needs no wait: one lane per slot issues at once.
+    const int first = min(kRingSlots, ntot);
+    if (lane >= n_pre && lane < first) issue(lane, alist[lane]);
+    // Every later chunk in list order: lane 0 waits for the slot and issues,
+    // the whole warp steps through the loop together (a lane left looping on
+    // its own would not hold back the block barrier below).
+    int k = first;
+    for (; k < ntot; ++k) {
+      const int slot = k % kRingSlots;
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(&bar_empty[slot], (k / kRingSlots - 1) & 1);
+        if (ok) issue(slot, alist[k]);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) atomicExch(&s_abort, 1);
+        break;
+      }
+    }
+    if (lane == 0) s_issued = k;
+  } else {
+    // lane = (row r, quarter dq); pieces visited in the rotated order jr(j)
+    const int r = lane >> 2, dq = lane & 3;
+    const int rot = (dq >> 1) + 2 * (r & 1);
+    const float4* q4 = reinterpret_cast<const float4*>(qsm);
+    for (int k = warp; k < ntot; k += kComputeWarps) {
+      const int slot = warp;  // == k % kRingSlots
+      if (!mbar_wait(&bar_full[slot], (k / kRingSlots) & 1)) {
+        if (lane == 0) atomicExch(&s_abort, 1);
+        break;
+      }
+      const int nr = slot_n[slot];
+      const uint8_t* kb = ring + slot * kSlotBytes;
+      const uint8_t* vb = kb + 2048;
+      float sa[NQ], sb[NQ];  // two independent partial sums per head
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int jr = (j + rot) & 3;
+        const uint4 kv = *reinterpret_cast<const uint4*>(kb + r * 256 + dq * 64 + jr * 16);
+        float f[8];
+        unpack8(kv, f);
+#pragma unroll
+        for (int h = 0; h < NQ; ++h) {
+          const float4 qa = q4[h * 32 + 4 * dq + jr];
+          const float4 qb = q4[h * 32 + 16 + 4 * dq + jr];
+          float t = qa.x * f[0];
+          t = fmaf(qa.y, f[1], t);
+          t = fmaf(qa.z, f[2], t);
+          t = fmaf(qa.w, f[3], t);
+          t = fmaf(qb.x, f[4], t);
+          t = fmaf(qb.y, f[5], t);
+          t = fmaf(qb.z, f[6], t);
+          t = fmaf(qb.w, f[7], t);
+          if (j == 0) sa[h] = t;
+          else if (j == 1) sb[h] = t;
+          else if (j == 2) sa[h] += t;
+          else sb[h] += t;
+        }
+      }
+      const bool valid = r < nr;
+      float pr[NQ];
+#pragma unroll
+      for (int h = 0; h < NQ; ++h) {
+        float s = sa[h] + sb[h];
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        s = valid ? s : -INFINITY;
+        float cmx = s;
+        cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 4));
+        cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 8));
+        cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 16));
+        const float mn = fmaxf(m[h], cmx);
+        const float alpha = merge_scale(m[h], mn);
+        pr[h] = (s == -INFINITY) ? 0.0f : exp2f(s - mn);
+        float ps = pr[h];
+        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+        l[h] = l[h] * alpha + ps;
+        m[h] = mn;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[h][i] *= alpha;
+      }
+      // P V: lane owns head dims [4 lane, 4 lane + 4) of every row
+      for (int rr = 0; rr < nr; ++rr) {
+        const uint2 vv = *reinterpret_cast<const uint2*>(vb + rr * 256 + lane * 8);
+        const float v0 = __uint_as_float(vv.x << 16), v1 = __uint_as_float(vv.x & 0xffff0000u);
+        const float v2 = __uint_as_float(vv.y << 16), v3 = __uint_as_float(vv.y & 0xffff0000u);
+#pragma unroll
+        for (int h = 0; h < NQ; ++h) {
+          const float pw = __shfl_sync(0xffffffffu, pr[h], rr * 4);  // lane 4 rr holds row rr
+          o[h][0] = fmaf(pw, v0, o[h][0]);
+          o[h][1] = fmaf(pw, v1, o[h][1]);
+          o[h][2] = fmaf(pw, v2, o[h][2]);
+          o[h][3] = fmaf(pw, v3, o[h][3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_empty[slot]);
+    }
+  }
+  __syncthreads();  // every chunk consumed: the ring is idle and serves as scratch
+  if (s_abort && threadIdx.x == 0) {
+    // (only after a timeout) let every copy still in flight land before the
+    // ring is reused or the CTA exits
+    for (int sl = 0; sl < kRingSlots && sl < s_issued; ++sl) {
+      const int klast = sl + (s_issued - 1 - sl) / kRingSlots * kRingSlots;
+      mbar_wait(&bar_full[sl], (klast / kRingSlots) & 1, 1u << 8);
+    }
+  }
+  __syncthreads();
+  float* wo = reinterpret_cast<float*>(ring);  // [kComputeWarps][NQ][128]
+  if (warp != kProducerWarp) {
+#pragma unroll
+    for (int h = 0; h < NQ; ++h) {
+      if (lane == 0) {
+        wm[warp][h] = m[h];
+        wl[warp][h] = l[h];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) wo[(warp * NQ + h) * kHeadDim + lane * 4 + i] = o[h][i];
+    }
+  }
+  __syncthreads();
+
+  // ---- this CTA's partial state: merge the compute warps
+  for (int e = threadIdx.x; e < rows * kHeadDim; e += kThreads) {
+    const int h = e / kHeadDim, d = e % kHeadDim;
+    float mx = -INFINITY;
+    for (int w = 0; w < kComputeWarps; ++w) mx = fmaxf(mx, wm[w][h]);
+    float ls = 0.0f, os = 0.0f;
+    for (int w = 0; w < kComputeWarps; ++w) {
+      const float f = merge_scale(wm[w][h], mx);
+      ls = fmaf(f, wl[w][h], ls);
+      os = fmaf(f, wo[(w * NQ + h) * kHeadDim + d], os);
+    }
+    cpart[h][d] = os;
+    if (d == 0) {
+      cm[h] = mx;
+      cl[h] = ls;
+    }
+  }
+  cluster_sync();
+
+  // ---- rank 0 merges the cluster's partial states and writes the outputs
+  if (rank == 0) {
+    bool bad = false;
+    for (int rr = 0; rr < S; ++rr) bad |= dsmem_ld_u32(&s_abort, (uint32_t)rr) != 0;
+    float* outp = p.out + ((size_t)b * p.Hq + (size_t)g * G) * kHeadDim;
+    for (int e = threadIdx.x; e < rows * kHeadDim; e += kThreads) {
+      const int h = e / kHeadDim, d = e % kHeadDim;
+      float mr[kMaxCluster];
+#pragma unroll
+      for (int rr = 0; rr < kMaxCluster; ++rr)
+        mr[rr] = rr < S ? __uint_as_float(dsmem_ld_u32(&cm[h], (uint32_t)rr)) : -INFINITY;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int rr = 0; rr < kMaxCluster; ++rr) mx = fmaxf(mx, mr[rr]);
+      float ls = 0.0f, os = 0.0f;
+#pragma unroll
+      for (int rr = 0; rr < kMaxCluster; ++rr) {
+        if (rr < S) {
+          const float f = merge_scale(mr[rr], mx);
+          ls = fmaf(f, __uint_as_float(dsmem_ld_u32(&cl[h], (uint32_t)rr)), ls);
+          os = fmaf(f, __uint_as_float(dsmem_ld_u32(&cpart[h][d], (uint32_t)rr)), os);
+        }
+      }
+      outp[h * kHeadDim + d] = bad ? NAN : (ls > 0.0f ? os / ls : 0.0f);
+    }
+    if (threadIdx.x == 0) {
+      if (C <= p.kc) {
+        uint32_t mn = 0xffffffffu;
+        for (int rr = 0; rr < S; ++rr) mn = min(mn, dsmem_ld_u32(&s_min, (uint32_t)rr));
+        p.n_sel[unit] = C;
+        if (p.s_cut) p.s_cut[unit] = (C > 0) ? key_score(mn) : -INFINITY;
+      } else {
+        p.n_sel[unit] = p.kc;
+        if (p.s_cut) p.s_cut[unit] = key_score(T);
+      }
+    }
+  }
+  cluster_sync();  // keep shared memory alive until rank 0 has read it
+}
+
+template <int NQ>
+tf_status launch_draft(const DraftParams& p, int units, int Cmax, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(retrieval_draft_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)draft_smem(kMaxSliceKeys)) != cudaSuccess)
+      return TF_ERR_CUDA;
+    configured = true;
+  }
+  // Cluster size: the largest S <= 8 (at most one CTA per 64 chunks) whose
+  // units x S CTAs fit one wave at the occupancy their slice size allows; at
+  // least enough CTAs that every slice fits on chip.
+  const int sms = num_sms();
+  const int need = (Cmax + kMaxSliceKeys - 1) / kMaxSliceKeys;
+  if (need > kMaxCluster) return TF_ERR_UNSUPPORTED;
+  int most = (Cmax + 63) / 64;
+  if (most > kMaxCluster) most = kMaxCluster;
+  int S = need < 1 ? 1 : need;
+  for (int cand_s = most; cand_s >= need && cand_s >= 1; --cand_s) {
+    const int sl = (Cmax + cand_s - 1) / cand_s;
+    const int occ = occupancy_blocks((const void*)retrieval_draft_kernel<NQ>, kThreads, draft_smem(sl));
+    if ((long long)units * cand_s <= (long long)sms * occ) {
+      S = cand_s;
+      break;
+    }
+  }
+  const int slice = (Cmax + S - 1) / S;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S, units);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = draft_smem(slice);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, retrieval_draft_kernel<NQ>, p) != cudaSuccess) return TF_ERR_CUDA;
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace tf
+
+extern "C" tf_status tf_retrieval_draft_attn(const uint16_t* q, const uint16_t* M, const uint16_t* K,
+                                             const uint16_t* V, const int32_t* seq_lens, int B, int Hq, int Hkv,
+                                             int Lmax, int D, int chunk, int kc, float scale, int32_t* idx,
+                                             int32_t* n_sel, float* s_cut, float* out, tf_stream_t stream) {
+  using namespace tf;
+  if (!q || !M || !K || !V || !seq_lens || !idx || !n_sel || !out) return TF_ERR_INVALID_ARG;
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || kc <= 0 || Hq % Hkv != 0) return TF_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(M) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return TF_ERR_INVALID_ARG;
+  if (D != kHeadDim || chunk != kChunk) return TF_ERR_UNSUPPORTED;
+  if (kc > kMaxList || Hq / Hkv > 4) return TF_ERR_UNSUPPORTED;
+  if (B == 0) return TF_OK;
+  const int units = B * Hkv;
+  if (units > 65535) return TF_ERR_UNSUPPORTED;
+  const int Cmax = (Lmax + kChunk - 1) / kChunk;
+  DraftParams p{q, M, K, V, seq_lens, Hq, Hkv, Lmax, kc, scale * kLog2e, idx, n_sel, s_cut, out};
+  const int G = Hq / Hkv;
+  switch (G) {
+    case 1: return launch_draft<1>(p, units, Cmax < 1 ? 1 : Cmax, stream);
+    case 2: return launch_draft<2>(p, units, Cmax < 1 ? 1 : Cmax, stream);
+    default: return launch_draft<4>(p, units, Cmax < 1 ? 1 : Cmax, stream);
+  }
+}

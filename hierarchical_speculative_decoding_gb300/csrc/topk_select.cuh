@@ -1,0 +1,372 @@
+// a2 + a3 building blocks -- chunk scoring and cluster-wide top-k selection.
+//
+// "TriForce: Hierarchical Speculative Decoding for LLMs", "The Three Forces of
+// TriForce": Force 2 keeps a small top-k subset of the KV blocks, chosen by
+// key-query similarity.  Score of chunk c for (sequence b, KV head g):
+//   s = (sum of the group's query heads) . M[b, g, c, :]   (fp32 accumulation)
+// Selection: the kc largest scores, equal scores to the lower chunk id.
+//
+// One thread-block cluster of S <= 8 CTAs serves one (b, g) unit; CTA r owns
+// the r-th contiguous slice of the unit's chunks and keeps its scores in shared
+// memory as order-preserving uint32 keys with a histogram of their top 11 bits.
+// The cut is found on the whole cluster through distributed shared memory: the
+// S histograms are summed on every CTA and give the bin b1 holding the kc-th
+// largest key; each CTA publishes its keys of that bin and every CTA gathers
+// them and resolves the remaining 21 bits by itself (a rare overflow of the
+// candidate buffer falls back to two more cluster histogram rounds).  Every
+// key in a bin above b1 is selected, which callers can act on before the cut
+// is final.  Used by the top-k call and by the fused retrieval-draft call.
+#pragma once
+
+#include "sm100_ptx.cuh"
+#include "tf_common.cuh"
+
+namespace tf {
+namespace topk {
+
+using namespace sm100;
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnroll = 6;
+constexpr int kMaxCluster = 8;
+constexpr int kMaxSliceKeys = 16384;  // keys per CTA held in shared memory (64 KB)
+
+// Shared-memory arrays of the selection.  hist*, tot 16-byte aligned.
+struct Arrays {
+  uint32_t* keys;   // [n] this CTA's score keys
+  uint32_t* hist1;  // [2048] top 11 key bits of this slice (read by the cluster)
+  uint32_t* hist2;  // [2048]
+  uint32_t* hist3;  // [1024]
+  uint32_t* tot;    // [2048] cluster sums
+  uint32_t* cand;   // [cap] this CTA's keys of bin b1 (read by the cluster)
+  uint32_t* gcand;  // [cap] the cluster's keys of bin b1
+  int cap;
+};
+
+// The cut: keys > T are selected, and of the keys == T the first take_eq in
+// chunk-id order over the cluster.
+struct Cut {
+  uint32_t b1;   // top 11 bits of T
+  uint32_t T;
+  int take_eq;
+  int cta_eq;    // keys == T in the CTAs before this one
+  int cta_sel;   // selected chunks in the CTAs before this one
+};
+
+__device__ __forceinline__ void zero_hists(const Arrays& a) {
+  for (int i = threadIdx.x; i < 2048; i += kThreads) {
+    a.hist1[i] = 0;
+    a.hist2[i] = 0;
+  }
+  for (int i = threadIdx.x; i < 1024; i += kThreads) a.hist3[i] = 0;
+}
+
+// Thread t owns nb / kThreads bins of h (thread 0 the highest); find the bin
+// holding the krem-th largest key.  All threads; result in s_bin / s_krem.
+__device__ __forceinline__ void find_bin(const uint32_t* h, int nb, int krem, int* s_wsum, int* s_bin,
+                                         int* s_krem) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int k = nb / kThreads;
+  const int top = nb - (int)threadIdx.x * k;
+  int segsum = 0;
+  for (int i = top - k; i < top; ++i) segsum += (int)h[i];
+  int incl = segsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
+  incl += wbase;
+  const int excl = incl - segsum;
+  if (excl < krem && krem <= incl) {
+    int run = excl;
+    for (int i = top - 1; i >= top - k; --i) {
+      const int c = (int)h[i];
+      if (run + c >= krem) {
+        *s_bin = i;
+        *s_krem = krem - run;
+        break;
+      }
+      run += c;
+    }
+  }
+  __syncthreads();
+}
+
+// tot[i] = sum over the cluster's CTAs of their local[i], i < nb (nb a multiple
+// of 4, arrays 16-byte aligned): 16-byte remote loads, all ranks in flight.
+__device__ __forceinline__ void cluster_sum(const uint32_t* local, uint32_t* tot, int nb, int S) {
+  for (int i = 4 * threadIdx.x; i < nb; i += 4 * kThreads) {
+    uint4 v[kMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) v[r] = r < S ? dsmem_ld_v4(local + i, (uint32_t)r) : make_uint4(0, 0, 0, 0);
+    uint4 t = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+      t.x += v[r].x;
+      t.y += v[r].y;
+      t.z += v[r].z;
+      t.w += v[r].w;
+    }
+    *reinterpret_cast<uint4*>(tot + i) = t;
+  }
+  __syncthreads();
+}
+
+// Scores of chunks [c0, c1) of one unit into keys[c - c0] and hist1.  qs: the
+// group's summed query (128 floats in shared memory); Mu: the unit's means.
+// A half-warp reads one 256-byte mean row with 16-byte loads, kUnroll rows in
+// flight per half-warp.
+__device__ __forceinline__ void score_slice(const float* qs, const uint16_t* __restrict__ Mu, int c0, int c1,
+                                            const Arrays& a) {
+  const int half = (threadIdx.x >> 4) & 1, l16 = threadIdx.x & 15, wid = threadIdx.x >> 5;
+  float qv[8];
+#pragma unroll
+  for (int d = 0; d < 8; ++d) qv[d] = qs[l16 * 8 + d];
+  const uint16_t* Ml = Mu + l16 * 8;
+  constexpr int kHalfWarps = kThreads / 16;
+  // The loop bound is warp-uniform (the shuffles need the whole warp); each
+  // half-warp owns chunk base + half + u * kHalfWarps.
+  for (int base = c0 + 2 * wid; base < c1; base += kHalfWarps * kUnroll) {
+    const int cb = base + half;
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int c = cb + u * kHalfWarps;
+      v[u] = (c < c1) ? ld_stream16(Ml + (size_t)c * kHeadDim) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      float f[8];
+      unpack8(v[u], f);
+      float s = 0.0f;
+#pragma unroll
+      for (int d = 0; d < 8; ++d) s = fmaf(qv[d], f[d], s);
+      s += __shfl_xor_sync(0xffffffffu, s, 8);
+      s += __shfl_xor_sync(0xffffffffu, s, 4);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      const int c = cb + u * kHalfWarps;
+      if (l16 == 0 && c < c1) {
+        const uint32_t key = score_key(s);
+        a.keys[c - c0] = key;
+        atomicAdd(&a.hist1[key >> 21], 1u);
+      }
+    }
+  }
+}
+
+// The cut over the cluster (requires C > kc; all threads of all CTAs call it
+// after score_slice and a __syncthreads).  after_round1(b1) is called by all
+// threads once b1 is known: every key with (key >> 21) > b1 is selected.
+template <typename Hook>
+__device__ Cut find_cut(const Arrays& a, int n, int kc, int S, uint32_t rank, Hook after_round1) {
+  __shared__ int s_ncand, s_above, s_roff[kMaxCluster + 1], s_rgt[kMaxCluster], s_req[kMaxCluster];
+  __shared__ int s_wsum[kWarps], s_bin, s_krem;
+  __shared__ uint32_t s_counts[2];  // keys > T and keys == T in this slice
+
+  // ---- round 1: the cluster's histogram of the top 11 key bits -> bin b1
+  cluster_sync();
+  cluster_sum(a.hist1, a.tot, 2048, S);
+  find_bin(a.tot, 2048, kc, s_wsum, &s_bin, &s_krem);
+  Cut cut;
+  cut.b1 = (uint32_t)s_bin;
+  const uint32_t b1 = cut.b1;
+  const int krem1 = s_krem;
+  const int ncand_tot = (int)a.tot[b1];  // keys of bin b1 over the cluster (same on every CTA)
+  after_round1(b1);
+
+  cut.cta_eq = 0;
+  cut.cta_sel = 0;
+  if (ncand_tot <= a.cap) {
+    // ---- round 2: publish this slice's keys of bin b1 and its count of keys
+    // above the bin; every CTA gathers all lists and resolves the last 21 bits
+    // and all output offsets by itself.
+    if (threadIdx.x == 0) {
+      s_ncand = 0;
+      s_above = 0;
+    }
+    __syncthreads();
+    {
+      int above = 0;
+      constexpr int k4 = 2048 / kThreads;
+      for (int i = threadIdx.x * k4; i < ((int)threadIdx.x + 1) * k4; ++i)
+        above += (uint32_t)i > b1 ? (int)a.hist1[i] : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
+      if ((threadIdx.x & 31) == 0) atomicAdd(&s_above, above);
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint32_t key = a.keys[i];
+        if ((key >> 21) == b1) a.cand[atomicAdd(&s_ncand, 1)] = key;  // at most ncand_tot <= cap
+      }
+    }
+    cluster_sync();
+    if (threadIdx.x < 32) {
+      const int r = threadIdx.x;
+      const int nc = r < S ? (int)dsmem_ld_u32(&s_ncand, (uint32_t)r) : 0;
+      int incl = nc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (r >= o) incl += v;
+      }
+      if (r < S) {
+        s_roff[r] = incl - nc;
+        s_rgt[r] = (int)dsmem_ld_u32(&s_above, (uint32_t)r);
+        s_req[r] = 0;
+      }
+      if (r == S - 1) s_roff[S] = incl;
+    }
+    __syncthreads();
+    // one remote load per gathered key, all ranks at once
+    for (int i = threadIdx.x; i < ncand_tot; i += kThreads) {
+      int r = 0;
+      while (r + 1 < S && i >= s_roff[r + 1]) ++r;
+      a.gcand[i] = dsmem_ld_u32(a.cand + (i - s_roff[r]), (uint32_t)r);
+    }
+    __syncthreads();
+    // bits 20..10, then 9..0, among the gathered keys (all of them are in bin b1)
+    for (int i = threadIdx.x; i < ncand_tot; i += kThreads) atomicAdd(&a.hist2[(a.gcand[i] >> 10) & 2047u], 1u);
+    __syncthreads();
+    find_bin(a.hist2, 2048, krem1, s_wsum, &s_bin, &s_krem);
+    const uint32_t pre2 = (b1 << 11) | (uint32_t)s_bin;
+    const int krem2 = s_krem;
+    for (int i = threadIdx.x; i < ncand_tot; i += kThreads) {
+      const uint32_t key = a.gcand[i];
+      if ((key >> 10) == pre2) atomicAdd(&a.hist3[key & 1023u], 1u);
+    }
+    __syncthreads();
+    find_bin(a.hist3, 1024, krem2, s_wsum, &s_bin, &s_krem);
+    cut.T = (pre2 << 10) | (uint32_t)s_bin;
+    cut.take_eq = s_krem;
+    // per-CTA counts of keys > T and == T among the gathered keys
+    for (int i = threadIdx.x; i < ncand_tot; i += kThreads) {
+      const uint32_t key = a.gcand[i];
+      int r = 0;
+      while (r + 1 < S && i >= s_roff[r + 1]) ++r;
+      if (key > cut.T) atomicAdd(&s_rgt[r], 1);
+      if (key == cut.T) atomicAdd(&s_req[r], 1);
+    }
+    __syncthreads();
+    for (int r = 0; r < (int)rank; ++r) {
+      cut.cta_sel += s_rgt[r] + min(max(cut.take_eq - cut.cta_eq, 0), s_req[r]);
+      cut.cta_eq += s_req[r];
+    }
+  } else {
+    // ---- rare (huge ties or a flat score range): resolve the last 21 bits with
+    // two more cluster-wide histogram rounds, then exchange exact counts.
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t key = a.keys[i];
+      if ((key >> 21) == b1) atomicAdd(&a.hist2[(key >> 10) & 2047u], 1u);
+    }
+    cluster_sync();
+    cluster_sum(a.hist2, a.tot, 2048, S);
+    find_bin(a.tot, 2048, krem1, s_wsum, &s_bin, &s_krem);
+    const uint32_t pre2 = (b1 << 11) | (uint32_t)s_bin;
+    const int krem2 = s_krem;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t key = a.keys[i];
+      if ((key >> 10) == pre2) atomicAdd(&a.hist3[key & 1023u], 1u);
+    }
+    cluster_sync();
+    cluster_sum(a.hist3, a.tot, 1024, S);
+    find_bin(a.tot, 1024, krem2, s_wsum, &s_bin, &s_krem);
+    cut.T = (pre2 << 10) | (uint32_t)s_bin;
+    cut.take_eq = s_krem;
+    {
+      int ngt = 0, neq = 0;
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint32_t key = a.keys[i];
+        ngt += key > cut.T;
+        neq += key == cut.T;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        ngt += __shfl_xor_sync(0xffffffffu, ngt, o);
+        neq += __shfl_xor_sync(0xffffffffu, neq, o);
+      }
+      if (threadIdx.x == 0) {
+        s_counts[0] = 0;
+        s_counts[1] = 0;
+      }
+      __syncthreads();
+      if ((threadIdx.x & 31) == 0) {
+        atomicAdd(&s_counts[0], (uint32_t)ngt);
+        atomicAdd(&s_counts[1], (uint32_t)neq);
+      }
+    }
+    cluster_sync();
+    for (int r = 0; r < (int)rank; ++r) {
+      const int gt_r = (int)dsmem_ld_u32(&s_counts[0], (uint32_t)r);
+      const int eq_r = (int)dsmem_ld_u32(&s_counts[1], (uint32_t)r);
+      cut.cta_sel += gt_r + min(max(cut.take_eq - cut.cta_eq, 0), eq_r);
+      cut.cta_eq += eq_r;
+    }
+  }
+  return cut;
+}
+
+// Id-order compaction of this CTA's selected chunks: warp w owns local ids
+// [w * seg, (w + 1) * seg).  emit(i, pos, upos) is called for every selected
+// local id i with its output position pos (< kc); when LIST, upos numbers the
+// selected keys of bin b1 (those after_round1 could not know) in id order,
+// starting at list_base, and is -1 for the others.
+template <bool LIST, typename Emit>
+__device__ void compact(const Arrays& a, int n, int kc, const Cut& cut, int list_base, Emit emit) {
+  __shared__ int s_wgt[kWarps], s_weq[kWarps], s_wcert[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
+  const int w0 = warp * seg, w1 = min(n, w0 + seg);
+  const unsigned lt = (1u << lane) - 1u;
+  const uint32_t T = cut.T;
+  const int take_eq = cut.take_eq;
+  int ngt = 0, neq = 0, ncert = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w1 ? a.keys[i] : 0u;
+    ngt += __popc(__ballot_sync(0xffffffffu, i < w1 && key > T));
+    neq += __popc(__ballot_sync(0xffffffffu, i < w1 && key == T));
+    if (LIST) ncert += __popc(__ballot_sync(0xffffffffu, i < w1 && (key >> 21) > cut.b1));
+  }
+  if (lane == 0) {
+    s_wgt[warp] = ngt;
+    s_weq[warp] = neq;
+    s_wcert[warp] = ncert;
+  }
+  __syncthreads();
+  int eq_base = cut.cta_eq, sel_base = cut.cta_sel, unc_base = list_base;
+  for (int w = 0; w < warp; ++w) {
+    const int sel_w = s_wgt[w] + min(max(take_eq - eq_base, 0), s_weq[w]);
+    sel_base += sel_w;
+    unc_base += sel_w - s_wcert[w];
+    eq_base += s_weq[w];
+  }
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w1 ? a.keys[i] : 0u;
+    const bool gt = i < w1 && key > T;
+    const bool eq = i < w1 && key == T;
+    const unsigned beq = __ballot_sync(0xffffffffu, eq);
+    const bool sel = gt || (eq && eq_base + __popc(beq & lt) < take_eq);
+    const unsigned bsel = __ballot_sync(0xffffffffu, sel);
+    const int pos = sel_base + __popc(bsel & lt);
+    int upos = -1;
+    if (LIST) {
+      const bool unc = sel && (key >> 21) <= cut.b1;
+      const unsigned bunc = __ballot_sync(0xffffffffu, unc);
+      if (unc) upos = unc_base + __popc(bunc & lt);
+      unc_base += __popc(bunc);
+    }
+    if (sel && pos < kc) emit(i, pos, upos);
+    eq_base += __popc(beq);
+    sel_base += __popc(bsel);
+  }
+}
+
+}  // namespace topk
+}  // namespace tf

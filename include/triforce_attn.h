@@ -151,6 +151,26 @@ TF_API tf_status tf_sparse_decode_attn_noalloc(const uint16_t* q, const uint16_t
                                 float scale, float* out, tf_stream_t stream);
 
 /*
+ * a2 + a3 + a4 (+ a5) fused -- the whole Force 2 retrieval drafter step of one
+ * layer in one launch ("TriForce: Hierarchical Speculative Decoding for LLMs",
+ * "The Three Forces of TriForce": attention over only the KV blocks of highest
+ * key-query similarity, within a fixed budget).  Computes exactly what
+ * tf_chunk_scores_topk followed by tf_sparse_decode_attn compute:
+ *   idx, n_sel, s_cut  as tf_chunk_scores_topk (s_cut may be NULL);
+ *   out [B, Hq, D] float32  as tf_sparse_decode_attn over that selection.
+ * Scores, the selection and the split-K partial states stay on chip (one
+ * thread-block cluster per (b, g)), so there is no workspace.  Limits:
+ * kc <= 2048, Hq / Hkv <= 4, contexts up to 8 x 16384 chunks (else
+ * TF_ERR_UNSUPPORTED; the two separate calls have no such limits).  Device
+ * pointers, 16-byte aligned q, M, K, V and out.
+ */
+TF_API tf_status tf_retrieval_draft_attn(const uint16_t* q, const uint16_t* M, const uint16_t* K,
+                                  const uint16_t* V, const int32_t* seq_lens,
+                                  int B, int Hq, int Hkv, int Lmax, int D, int chunk, int kc,
+                                  float scale, int32_t* idx, int32_t* n_sel, float* s_cut,
+                                  float* out, tf_stream_t stream);
+
+/*
  * a6 (+ a5) -- StreamingLLM sink + window attention (Force 1 drafter).
  * Positions P = [0, min(n_sink, L)) U [max(n_sink, L - window), L): the first
  * n_sink tokens plus the most recent `window` tokens, de-duplicated.

@@ -78,6 +78,17 @@ def test_host_validation_rejects_before_launch(lib):
                                      None) == INVALID
     assert lib.tf_verify_attn(fake, fake, fake, fake, 1, 8, 2, 64, 128, 0, 0.1, fake, null, 0, None) == INVALID
     assert lib.tf_verify_attn(fake, fake, fake, fake, 1, 8, 2, 64, 128, 17, 0.1, fake, null, 0, None) == UNSUPPORTED
+    # fused retrieval drafter: q, M, K, V, seq_lens, B, Hq, Hkv, Lmax, D, chunk, kc, scale, idx, n_sel, s_cut, out
+    assert lib.tf_retrieval_draft_attn(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 2049, 0.1, fake, fake, null,
+                                       fake, None) == UNSUPPORTED  # kc above the on-chip list
+    assert lib.tf_retrieval_draft_attn(fake, fake, fake, fake, fake, 1, 16, 2, 64, 128, 8, 64, 0.1, fake, fake, null,
+                                       fake, None) == UNSUPPORTED  # 8 query heads per group
+    assert lib.tf_retrieval_draft_attn(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 64, 0.1, fake, fake, null,
+                                       null, None) == INVALID  # no output
+    assert lib.tf_retrieval_draft_attn(fake, odd, fake, fake, fake, 1, 8, 2, 64, 128, 8, 64, 0.1, fake, fake, null,
+                                       fake, None) == INVALID  # misaligned means
+    assert lib.tf_retrieval_draft_attn(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 16, 64, 0.1, fake, fake, null,
+                                       fake, None) == UNSUPPORTED  # chunk 16
     assert lib.tf_spec_accept(fake, fake, fake, fake, fake, 1, 4, 100, 0.0, fake, fake, null, fake, 4096,
                               None) == INVALID
     assert lib.tf_spec_accept(fake, null, fake, fake, fake, 1, 4, 100, 1.0, fake, fake, null, fake, 4096,

@@ -50,7 +50,12 @@ def test_full_size_layer(cuda_lib, w):
     sp = cuda_lib.tf_sparse_decode_attn(q, K, V, seq, idx, nsel, scale)
     wi = cuda_lib.tf_stream_window_attn(q, K, V, seq, w.n_sink, w.window, scale)
     ve = cuda_lib.tf_verify_attn(Q, K, V, seq, scale)
+    fidx, fnsel, fsp = cuda_lib.tf_retrieval_draft_attn(q, M, K, V, seq, w.kc, scale)
     torch.cuda.synchronize()
+    # the fused retrieval drafter selects exactly what the top-k call selects
+    assert np.array_equal(fidx.cpu().numpy(), idx.cpu().numpy())
+    assert np.array_equal(fnsel.cpu().numpy(), nsel.cpu().numpy())
+    fsp_h = fsp.cpu().double().numpy()
     M_h, idx_h, nsel_h = bits(M), idx.cpu().numpy(), nsel.cpu().numpy()
     sp_h, wi_h, ve_h = sp.cpu().double().numpy(), wi.cpu().double().numpy(), ve.cpu().double().numpy()
     q_h, Q_h = bits(q), bits(Q)
@@ -76,6 +81,7 @@ def test_full_size_layer(cuda_lib, w):
         sp_o = O.sparse_decode_attn(qg, Kb, Vb, sl, idx_h[b : b + 1, g : g + 1], nsel_h[b : b + 1, g : g + 1],
                                     w.chunk, scale)
         assert np.abs(sp_h[b, g * G : (g + 1) * G] - sp_o[0]).max() <= ATOL
+        assert np.abs(fsp_h[b, g * G : (g + 1) * G] - sp_o[0]).max() <= ATOL
         # a6
         wi_o = O.stream_window_attn(qg, Kb, Vb, sl, w.n_sink, w.window, scale)
         assert np.abs(wi_h[b, g * G : (g + 1) * G] - wi_o[0]).max() <= ATOL

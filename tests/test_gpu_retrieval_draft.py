@@ -1,0 +1,105 @@
+"""GPU parity of the fused retrieval-drafter call (scores + top-k + sparse
+attention in one launch) against the float64 oracle.
+
+The selection must pass the same checks as the top-k call (identical ids
+except at oracle cut gaps below 1e-4) and must equal the separate top-k call's
+selection exactly (same scores, same rule); the attention output is checked
+against the oracle's sparse attention over the selection the call made
+(max abs error <= 2e-3) and against the separate sparse-attention call.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from hierarchical_speculative_decoding_gb300 import synth
+from oracle import triforce as O
+
+from test_gpu_parity import ATOL, bits, check_topk, make_case, scale_for, small_workload
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fused(cuda_lib, w, c, M, kc=None, scale=None):
+    kc = kc or w.kc
+    scale = scale if scale is not None else scale_for(w.D)
+    s_cut = torch.empty((w.B, w.Hkv), dtype=torch.float32, device="cuda")
+    idx, nsel, out = cuda_lib.tf_retrieval_draft_attn(c["q"], M, c["K"], c["V"], c["seq"], kc, scale, s_cut=s_cut)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), nsel.cpu().numpy(), s_cut.cpu().numpy(), out.cpu().double().numpy()
+
+
+def check_against_oracle(cuda_lib, w, c, M_bits, kc=None, scale=None):
+    kc = kc or w.kc
+    scale = scale if scale is not None else scale_for(w.D)
+    seq = c["seq_cpu"].numpy()
+    M = torch.from_numpy(M_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    idx, nsel, s_cut, out = run_fused(cuda_lib, w, c, M, kc, scale)
+    idx_o, nsel_o, cut_o, gap_o, scores_o = O.chunk_scores_topk(bits(c["q_cpu"]), M_bits, seq, w.L, w.chunk, kc,
+                                                                w.Hkv)
+    check_topk(idx, nsel, idx_o, nsel_o, gap_o, scores_o)
+    np.testing.assert_allclose(s_cut, cut_o, rtol=1e-5, atol=1e-4)
+    want = O.sparse_decode_attn(bits(c["q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), seq, idx, nsel, w.chunk,
+                                scale)
+    err = np.abs(out - want).max()
+    assert err <= ATOL, err
+    # the two-call path on the same inputs: same selection, same attention
+    idx2, nsel2 = cuda_lib.tf_chunk_scores_topk(c["q"], M, c["seq"], w.L, kc)
+    out2 = cuda_lib.tf_sparse_decode_attn(c["q"], c["K"], c["V"], c["seq"], idx2, nsel2, scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx2.cpu().numpy(), idx) and np.array_equal(nsel2.cpu().numpy(), nsel)
+    assert np.abs(out2.cpu().double().numpy() - out).max() <= ATOL
+    return idx, nsel, out
+
+
+@pytest.mark.parametrize("w", [
+    synth.TINY,
+    small_workload(),
+    small_workload(budget=8 * 2000),
+    small_workload(B=1, Hq=8, Hkv=8, L=32768, budget=4096, ragged=False, planted_frac=0.01),
+    small_workload(B=2, Hq=8, Hkv=4, L=20000, budget=8 * 2048, L_min=17000),
+    small_workload(B=3, Hq=6, Hkv=2, L=5000, budget=8 * 37, L_min=9),
+], ids=["tiny", "ragged-gqa", "budget-covers-all", "mha-32k", "kc-2048", "g3-odd-budget"])
+def test_retrieval_draft_parity(cuda_lib, w):
+    c = make_case(w, fill_invalid=float("nan"))
+    M_bits = O.build_chunk_means(bits(c["K_cpu"]), c["seq_cpu"].numpy(), w.chunk)
+    idx, nsel, _ = check_against_oracle(cuda_lib, w, c, M_bits)
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            assert set(c["planted"][b][g].tolist()) <= set(idx[b, g, : nsel[b, g]].tolist())
+
+
+def test_retrieval_draft_empty_and_tiny_contexts(cuda_lib):
+    w = small_workload(B=3, ragged=False, L=64)
+    c = make_case(w)
+    c["seq"] = torch.tensor([0, 1, 64], dtype=torch.int32, device="cuda")
+    c["seq_cpu"] = torch.tensor([0, 1, 64], dtype=torch.int32)
+    M_bits = O.build_chunk_means(bits(c["K_cpu"]), c["seq_cpu"].numpy(), 8)
+    for kc in (4, 8, 100):
+        idx, nsel, out = check_against_oracle(cuda_lib, w, c, M_bits, kc=kc)
+        assert nsel[0].tolist() == [0, 0] and np.all(out[0] == 0)
+
+
+def test_retrieval_draft_all_equal_scores(cuda_lib):
+    """6000 equal scores per unit: more threshold-bin keys than the on-chip
+    candidate buffer holds, so the cut is resolved bin by bin; ties go to the
+    lowest ids and the attention covers exactly chunks 0..511."""
+    w = small_workload(B=1, ragged=False, L=8 * 6000)
+    c = make_case(w)
+    M_bits = np.zeros((1, w.Hkv, 6000, 128), dtype=np.uint16)
+    idx, nsel, out = check_against_oracle(cuda_lib, w, c, M_bits, kc=512)
+    for g in range(w.Hkv):
+        assert idx[0, g].tolist() == list(range(512)) and nsel[0, g] == 512
+
+
+def test_retrieval_draft_repeated_calls_agree(cuda_lib):
+    """No state survives a call: the same inputs give bit-identical outputs."""
+    w = small_workload(B=2, Hq=8, Hkv=2, L=30000, budget=4096, L_min=20000)
+    c = make_case(w)
+    Cmax = -(-w.L // w.chunk)
+    M = torch.empty((w.B, w.Hkv, Cmax, w.D), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.tf_build_chunk_means(c["K"], c["seq"], M)
+    a = run_fused(cuda_lib, w, c, M)
+    b = run_fused(cuda_lib, w, c, M)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
