@@ -361,6 +361,8 @@ def run_gpu(args):
                          "frac_hbm": round(kbytes[k] / (ms / 1e3) / 1e9 / peak, 4)}
     kernels["retrieval_draft"]["calls"] = ("tf_chunk_scores_topk + tf_sparse_decode_attn" if args.two_call_draft
                                            else "tf_retrieval_draft_attn")
+    kernels["retrieval_draft"]["traffic"] = (None if args.two_call_draft
+                                             else recorded_traffic("retrieval_draft.cu", w.name))
     # the two-call form of the retrieval drafter, for comparison (events around each call)
     if not args.two_call_draft:
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(layers)]
