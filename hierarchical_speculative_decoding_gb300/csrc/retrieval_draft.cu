@@ -12,18 +12,23 @@
 // scoring the r-th slice of the chunk means; see topk_select.cuh) keeps going
 // after the cut: each CTA attends the chunks it selected itself, so no chunk
 // list goes through global memory and no second launch waits for the first.
-//  * As soon as the first cluster histogram round fixes the bin b1 of the cut,
-//    every key in a bin above b1 is known to be selected; the CTA lists those
-//    chunks and starts bulk copies (cp.async.bulk, complete-tx on an mbarrier)
-//    of the first eight into the part of the ring that the selection does not
-//    use, so HBM keeps working while the cut is resolved.
-//  * After the id-order compaction, warp 15 stages the rest of the list into
-//    the 15-slot ring (one lane per slot for the first round, then in list
-//    order as slots free up), and warp w of 0..14 takes chunks w, w + 15, ...
-//    from its own slot: lane (row r,
-//    quarter dq) forms 32-dim dot products with the query rows held in shared
-//    memory in a bank-conflict-free permuted layout, the online softmax runs in
-//    the log2 domain in fp32, and each lane owns 4 head dims of P V.
+//  * After the first cluster histogram round fixes the bin b1 of the cut,
+//    every chunk whose key lies above b1 is selected whatever the rest of the
+//    cut.  The CTA lists those chunks and splits: warps 0..3 finish the cut
+//    (candidate gather, last 21 bits, id-order output, the chunks of bin b1
+//    appended to the list) on a named barrier, while warp 15 stages listed
+//    chunks (K and V rows, cp.async.bulk into a ring of 4 KB slots) and warps
+//    4..14 attend them.  When the cut is done, warps 0..3 join as consumers.
+//    HBM keeps streaming while the cut is resolved.
+//  * Each consumer warp owns one ring slot; the producer hands the next listed
+//    chunk to whichever slot its consumer has released (non-blocking polls in
+//    a warp-uniform loop), and an empty marker ends a consumer's loop.  A slot
+//    only ever has one producer and one consumer, so every wait on its
+//    barriers is for the very next phase.
+//  * Consumer lane (row r, quarter dq) forms 32-dim dot products with the
+//    query rows held in shared memory in a bank-conflict-free permuted layout;
+//    the online softmax runs in the log2 domain in fp32 and each lane owns 4
+//    head dims of P V.
 //  * Warps merge in shared memory, then CTA rank 0 merges the S partial states
 //    of the cluster through distributed shared memory (log-sum-exp identity)
 //    and writes the output.
@@ -42,29 +47,32 @@ using topk::kWarps;
 
 constexpr int kProducerWarp = kWarps - 1;
 constexpr int kComputeWarps = kWarps - 1;
-// One ring slot per compute warp: chunk k sits in slot k % 15 and is consumed
-// by warp k % 15, so every use of a slot is waited for by the warp that
-// consumed the previous one and a phase-parity wait can never run two phases
-// ahead of its barrier.
-constexpr int kRingSlots = kComputeWarps;
-constexpr int kEarlySlots = 8;   // ring slots that do not overlay the selection arrays
+constexpr int kCutWarps = 4;                            // warps 0..3 finish the cut
+constexpr int kRingSlots = kComputeWarps;               // one slot per consumer warp
+constexpr int kEarlySlots = kComputeWarps - kCutWarps;  // slots of warps 4..14
 constexpr int kSlotBytes = 4096;  // K rows [0, 2 KB), V rows [2 KB, 4 KB)
 constexpr int kCandCap = 2048;    // keys of the threshold bin gathered on every CTA
 constexpr int kMaxList = 2048;    // selected chunks per CTA (kc <= kMaxList)
+constexpr uint32_t kIdleLimit = 1u << 22;  // producer polls without progress before it gives up
 
-// Dynamic shared memory (bytes).  The histograms overlay ring slots 8..14,
-// which are first written after the cut; the candidate buffers (cand is read
-// by the other CTAs until the last cluster barrier) and the chunk list have
-// their own space.
-constexpr int kOffHist1 = kEarlySlots * kSlotBytes;  // 32768
-constexpr int kOffHist2 = kOffHist1 + 2048 * 4;
-constexpr int kOffHist3 = kOffHist2 + 2048 * 4;
-constexpr int kOffTot = kOffHist3 + 1024 * 4;
-constexpr int kOffGcand = kOffTot + 2048 * 4;      // 61440 = end of the ring
-constexpr int kOffCand = kOffGcand + kCandCap * 4;  // 69632
-constexpr int kOffList = kOffCand + kCandCap * 4;   // 77824
-constexpr int kOffKeys = kOffList + kMaxList * 4;   // 86016
-static_assert(kOffGcand >= kRingSlots * kSlotBytes, "the candidate buffers must not overlay the ring");
+// Dynamic shared memory (bytes).
+//  [0, 45056)      ring slots 0..10 (consumers 4..14); during round 1 it holds
+//                  tot, which only this CTA reads
+//  [45056, 65536)  hist2, hist3, gcand: the cut group's scratch; ring slots
+//                  11..14 (consumers 0..3) once the cut is done
+//  hist1, cand     read by the other CTAs of the cluster: never overlaid
+//  alist           this CTA's selected chunks (certain ones first)
+//  keys            this CTA's score keys
+constexpr int kOffTot = 0;
+constexpr int kOffHist2 = kEarlySlots * kSlotBytes;  // 45056
+constexpr int kOffHist3 = kOffHist2 + 2048 * 4;      // 53248
+constexpr int kOffGcand = kOffHist3 + 1024 * 4;      // 57344
+constexpr int kOffHist1 = kOffGcand + kCandCap * 4;  // 65536
+constexpr int kOffCand = kOffHist1 + 2048 * 4;       // 73728
+constexpr int kOffList = kOffCand + kCandCap * 4;    // 81920
+constexpr int kOffKeys = kOffList + kMaxList * 4;    // 90112
+static_assert(kRingSlots * kSlotBytes <= kOffHist1, "the ring must not reach the arrays other CTAs read");
+static_assert(kOffTot + 2048 * 4 <= kOffHist2, "tot must stay inside the early slots");
 
 struct DraftParams {
   const uint16_t* q;  // [B, Hq, 128]
@@ -82,17 +90,22 @@ struct DraftParams {
 
 size_t draft_smem(int slice) { return (size_t)kOffKeys + (size_t)slice * sizeof(uint32_t); }
 
+// Ring slot of consumer warp w: warps 4..14 take slots 0..10, warps 0..3 (the
+// cut group) slots 11..14.
+__device__ __forceinline__ int slot_of(int warp) { return (warp + kEarlySlots) % kRingSlots; }
+
 template <int NQ>
 __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) float qsm[NQ * kHeadDim];  // scaled query rows, permuted (see below)
   __shared__ float qs[kHeadDim];                      // the group's summed query (scores)
   __shared__ __align__(8) uint64_t bar_full[kRingSlots], bar_empty[kRingSlots];
-  __shared__ int slot_n[kRingSlots];
+  __shared__ int slot_n[kRingSlots], slot_uses[kRingSlots];
   __shared__ float wm[kComputeWarps][NQ], wl[kComputeWarps][NQ];
   __shared__ float cpart[NQ][kHeadDim], cm[NQ], cl[NQ];
   __shared__ uint32_t s_min;
-  __shared__ int s_na, s_ntot, s_abort, s_issued, s_wcnt[kWarps];
+  __shared__ int s_na, s_ntot, s_abort;
+  __shared__ volatile int s_cut_done;
 
   uint8_t* ring = smem;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kOffKeys);
@@ -120,7 +133,8 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
       mbar_init(&bar_empty[s], 1);
     }
     s_abort = 0;
-    s_issued = 0;
+    s_na = 0;
+    s_cut_done = 0;
     s_min = 0xffffffffu;
     fence_mbar_init();
   }
@@ -178,6 +192,8 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
 
   int32_t* out_idx = p.idx + (size_t)unit * p.kc;
   uint32_t T = 0;
+  bool split = false;  // warps 0..3 finish the cut while the others attend
+  topk::Round1 r1{};
   if (C <= p.kc) {
     // Every chunk is selected: ids in order, slots past C hold -1, s_cut = min score.
     uint32_t mn = 0xffffffffu;
@@ -195,55 +211,32 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
       s_na = n;
       s_ntot = n;
     }
-    __syncthreads();
-    if ((int)threadIdx.x < min(kEarlySlots, n)) issue(threadIdx.x, alist[threadIdx.x]);
   } else {
-    // List the chunks above bin b1 (selected whatever the rest of the cut) and
-    // start copying the first of them while the cut is resolved.
-    auto early = [&](uint32_t b1) {
-      const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
-      const int w0 = warp * seg, w1 = min(n, w0 + seg);
-      const unsigned lt = (1u << lane) - 1u;
-      int cnt = 0;
-      for (int base = w0; base < w1; base += 32) {
-        const int i = base + lane;
-        cnt += __popc(__ballot_sync(0xffffffffu, i < w1 && (keys[i] >> 21) > b1));
-      }
-      if (lane == 0) s_wcnt[warp] = cnt;
-      __syncthreads();
-      int pos = 0;
-      for (int w = 0; w < warp; ++w) pos += s_wcnt[w];
-      if (warp == kWarps - 1 && lane == 0) {
-        s_na = pos + cnt;
-        s_ntot = pos + cnt;
-      }
-      for (int base = w0; base < w1; base += 32) {
-        const int i = base + lane;
-        const bool sel = i < w1 && (keys[i] >> 21) > b1;
-        const unsigned bs = __ballot_sync(0xffffffffu, sel);
-        if (sel) alist[pos + __popc(bs & lt)] = c0 + i;
-        pos += __popc(bs);
-      }
-      __syncthreads();
-      if ((int)threadIdx.x < min(kEarlySlots, s_na)) issue(threadIdx.x, alist[threadIdx.x]);
-    };
-    const topk::Cut cut = topk::find_cut(a, n, p.kc, S, rank, early);
-    T = cut.T;
-    topk::compact<true>(a, n, p.kc, cut, s_na, [&](int i, int pos, int upos) {
-      out_idx[pos] = c0 + i;
-      if (upos >= 0 && upos < kMaxList) {
-        alist[upos] = c0 + i;
-        atomicMax(&s_ntot, upos + 1);
-      }
-    });
+    r1 = topk::round1(a, p.kc, S);
+    // chunks above bin b1: selected whatever the rest of the cut (list order is free)
+    for (int i = threadIdx.x; i < n; i += kThreads)
+      if ((keys[i] >> 21) > r1.b1) alist[atomicAdd(&s_na, 1)] = c0 + i;
     __syncthreads();
+    if (threadIdx.x == 0) s_ntot = s_na;
+    split = r1.ncand_tot <= kCandCap;
+    if (!split) {
+      // rare: resolve the cut with every warp, attend afterwards
+      __syncthreads();
+      const topk::Cut cut = topk::fallback_cut(a, n, S, rank, r1);
+      T = cut.T;
+      topk::compact(a, n, p.kc, cut, topk::CtaBar(), [&](int i, int pos, bool unc) {
+        out_idx[pos] = c0 + i;
+        if (unc) {
+          const int at = atomicAdd(&s_ntot, 1);
+          if (at < kMaxList) alist[at] = c0 + i;
+        }
+      });
+    }
   }
-  const int ntot = s_ntot;
-  const int n_pre = min(kEarlySlots, s_na);
+  __syncthreads();
 
   // ---------------------------------------------------------------- attention
-  constexpr int rows_cap = NQ;
-  const int rows = G < rows_cap ? G : rows_cap;
+  const int rows = G < NQ ? G : NQ;
   float m[NQ], l[NQ], o[NQ][4];
 #pragma unroll
   for (int h = 0; h < NQ; ++h) {
@@ -252,44 +245,104 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[h][i] = 0.0f;
   }
-  if (warp == kProducerWarp) {
-    // Slots 8..14 held the histograms (generic-proxy writes): order those
-    // before the bulk copies that now overwrite them.
-    fence_proxy_async_smem();
-    // First use of every slot needs no wait: one lane per slot issues at once.
-    const int first = min(kRingSlots, ntot);
-    if (lane >= n_pre && lane < first) issue(lane, alist[lane]);
-    // Every later chunk in list order: lane 0 waits for the slot and issues,
-    // the whole warp steps through the loop together (a lane left looping on
-    // its own would not hold back the block barrier below).
-    int k = first;
-    for (; k < ntot; ++k) {
-      const int slot = k % kRingSlots;
-      bool ok = true;
-      if (lane == 0) {
-        ok = mbar_wait(&bar_empty[slot], (k / kRingSlots - 1) & 1);
-        if (ok) issue(slot, alist[k]);
+  const bool cut_group = split && warp < kCutWarps;
+  if (cut_group) {
+    // ---- warps 0..3: the rest of the cut, then consumers of slots 11..14
+    const topk::Cut cut = topk::fast_cut(a, n, S, rank, r1, topk::Warps0to3Bar());
+    T = cut.T;
+    topk::compact(a, n, p.kc, cut, topk::Warps0to3Bar(), [&](int i, int pos, bool unc) {
+      out_idx[pos] = c0 + i;
+      if (unc) {
+        const int at = atomicAdd(&s_ntot, 1);
+        if (at < kMaxList) alist[at] = c0 + i;
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+    });
+    topk::Warps0to3Bar()();
+    if (threadIdx.x == 0) {
+      __threadfence_block();
+      s_cut_done = 1;
+    }
+  } else if (split) {
+    cluster_arrive();  // the cut group's one cluster barrier; waited for below
+  }
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- producer
+    // Lane s < 15 tracks ring slot s: the chunks issued into it (uses) and
+    // whether its end marker went out.  A slot is free once its consumer has
+    // released its last chunk; free slots take the next listed chunks in lane
+    // order.  Non-blocking polls keep the whole warp in step.
+    fence_proxy_async_smem();  // slots 0..10 held tot (generic-proxy writes)
+    const unsigned lt = (1u << lane) - 1u;
+    int nact = split ? kEarlySlots : kRingSlots;
+    bool fin = !split;
+    int list_len = min(s_ntot, kMaxList);
+    int next = 0;
+    uint32_t uses = 0;
+    bool marked = false;
+    uint32_t idle = 0;
+    while (true) {
+      if (!fin && s_cut_done) {
+        __threadfence_block();
+        list_len = min(*(volatile int*)&s_ntot, kMaxList);
+        fin = true;
+        nact = kRingSlots;
+        fence_proxy_async_smem();  // slots 11..14 held the cut's scratch
+      }
+      const bool active = lane < nact && !marked;
+      const bool free_slot = active && (uses == 0 || mbar_test(&bar_empty[lane], (uses - 1) & 1));
+      const unsigned fm = __ballot_sync(0xffffffffu, free_slot);
+      const int avail = max(list_len - next, 0);
+      const int take = min(__popc(fm), avail);
+      const int rk = __popc(fm & lt);
+      if (free_slot && rk < take) {
+        issue(lane, alist[next + rk]);
+        ++uses;
+      }
+      next += take;
+      bool progress = take > 0;
+      if (fin && next >= list_len) {
+        if (free_slot && rk >= take) {  // nothing left for this slot: end marker
+          slot_n[lane] = -1;
+          mbar_arrive(&bar_full[lane]);
+          marked = true;
+          progress = true;
+        }
+        if (__ballot_sync(0xffffffffu, lane < kRingSlots && !marked) == 0) break;
+      }
+      if (progress) {
+        idle = 0;
+      } else if (++idle > kIdleLimit) {
         if (lane == 0) atomicExch(&s_abort, 1);
         break;
+      } else {
+        __nanosleep(64);
       }
     }
-    if (lane == 0) s_issued = k;
+    if (lane < kRingSlots) slot_uses[lane] = uses;
+    if (s_abort && lane < kRingSlots && !marked) {
+      // (only after a timeout) let this slot's last copy land, then release
+      // its consumer
+      if (uses > 0) mbar_wait(&bar_full[lane], (uses - 1) & 1, 1u << 8);
+      slot_n[lane] = -1;
+      mbar_arrive(&bar_full[lane]);
+    }
   } else {
+    // ---------------------------------------------------------------- consumers
     // lane = (row r, quarter dq); pieces visited in the rotated order jr(j)
+    const int slot = slot_of(warp);
     const int r = lane >> 2, dq = lane & 3;
     const int rot = (dq >> 1) + 2 * (r & 1);
     const float4* q4 = reinterpret_cast<const float4*>(qsm);
-    for (int k = warp; k < ntot; k += kComputeWarps) {
-      const int slot = warp;  // == k % kRingSlots
-      if (!mbar_wait(&bar_full[slot], (k / kRingSlots) & 1)) {
+    const uint8_t* kb = ring + slot * kSlotBytes;
+    const uint8_t* vb = kb + 2048;
+    for (uint32_t u = 0;; ++u) {
+      if (!mbar_wait(&bar_full[slot], u & 1)) {
         if (lane == 0) atomicExch(&s_abort, 1);
         break;
       }
       const int nr = slot_n[slot];
-      const uint8_t* kb = ring + slot * kSlotBytes;
-      const uint8_t* vb = kb + 2048;
+      if (nr < 0) break;  // end marker
       float sa[NQ], sb[NQ];  // two independent partial sums per head
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -357,14 +410,13 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
       if (lane == 0) mbar_arrive(&bar_empty[slot]);
     }
   }
+  if (split && !cut_group) cluster_wait();
   __syncthreads();  // every chunk consumed: the ring is idle and serves as scratch
   if (s_abort && threadIdx.x == 0) {
     // (only after a timeout) let every copy still in flight land before the
     // ring is reused or the CTA exits
-    for (int sl = 0; sl < kRingSlots && sl < s_issued; ++sl) {
-      const int klast = sl + (s_issued - 1 - sl) / kRingSlots * kRingSlots;
-      mbar_wait(&bar_full[sl], (klast / kRingSlots) & 1, 1u << 8);
-    }
+    for (int sl = 0; sl < kRingSlots; ++sl)
+      if (slot_uses[sl] > 0) mbar_wait(&bar_full[sl], (slot_uses[sl] - 1) & 1, 1u << 8);
   }
   __syncthreads();
   float* wo = reinterpret_cast<float*>(ring);  // [kComputeWarps][NQ][128]

@@ -94,8 +94,10 @@ __global__ void __launch_bounds__(kThreads, 2) scores_topk_kernel(
     return;
   }
 
-  const topk::Cut cut = topk::find_cut(a, n, kc, S, rank, [](uint32_t) {});
-  topk::compact<false>(a, n, kc, cut, 0, [&](int i, int pos, int) { out[pos] = c0 + i; });
+  const topk::Round1 r1 = topk::round1(a, kc, S);
+  const topk::Cut cut = r1.ncand_tot <= kCandCap ? topk::fast_cut(a, n, S, rank, r1, topk::CtaBar())
+                                                 : topk::fallback_cut(a, n, S, rank, r1);
+  topk::compact(a, n, kc, cut, topk::CtaBar(), [&](int i, int pos, bool) { out[pos] = c0 + i; });
   if (rank == 0 && threadIdx.x == 0) {
     n_sel[unit] = kc;
     if (s_cut) s_cut[unit] = key_score(cut.T);

@@ -48,6 +48,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase, uin
   return ok != 0;
 }
 
+// Non-blocking test of a phase parity (true once that phase has completed).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on a phase parity.  Waiting threads sleep inside try_wait rather
 // than spinning, so they do not steal issue slots from the warps doing the work.
 // Returns false after `limit` polls of at most 20 us each (about 1.3 s), so a
@@ -190,6 +201,10 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The two halves of cluster_sync, for warps that arrive at a cluster barrier
+// early and wait for its completion later (whole warps, in the same order).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // 32-bit load from the same shared-memory variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t dsmem_ld_u32(const void* local_ptr, uint32_t rank) {

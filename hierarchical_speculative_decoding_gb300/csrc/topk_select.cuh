@@ -15,7 +15,9 @@
 // them and resolves the remaining 21 bits by itself (a rare overflow of the
 // candidate buffer falls back to two more cluster histogram rounds).  Every
 // key in a bin above b1 is selected, which callers can act on before the cut
-// is final.  Used by the top-k call and by the fused retrieval-draft call.
+// is final; the steps after round 1 can run on a group of four warps while the
+// rest of the CTA does other work.  Used by the top-k call and by the fused
+// retrieval-draft call.
 #pragma once
 
 #include "sm100_ptx.cuh"
@@ -62,12 +64,26 @@ __device__ __forceinline__ void zero_hists(const Arrays& a) {
   for (int i = threadIdx.x; i < 1024; i += kThreads) a.hist3[i] = 0;
 }
 
-// Thread t owns nb / kThreads bins of h (thread 0 the highest); find the bin
-// holding the krem-th largest key.  All threads; result in s_bin / s_krem.
-__device__ __forceinline__ void find_bin(const uint32_t* h, int nb, int krem, int* s_wsum, int* s_bin,
-                                         int* s_krem) {
+// Barriers for the group of threads running a step: the whole CTA, or warps
+// 0..3 on named barrier 1 while the other warps do something else.
+struct CtaBar {
+  static constexpr int kNT = kThreads;
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+struct Warps0to3Bar {
+  static constexpr int kNT = 128;
+  __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+};
+
+// Thread t of the group owns nb / NT bins of h (thread 0 the highest); find the
+// bin holding the krem-th largest key.  All threads of the group; result in
+// s_bin / s_krem; s_wsum holds NT / 32 ints.
+template <class Bar>
+__device__ __forceinline__ void find_bin(const uint32_t* h, int nb, int krem, int* s_wsum, int* s_bin, int* s_krem,
+                                         Bar bar) {
+  constexpr int NT = Bar::kNT;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int k = nb / kThreads;
+  const int k = nb / NT;
   const int top = nb - (int)threadIdx.x * k;
   int segsum = 0;
   for (int i = top - k; i < top; ++i) segsum += (int)h[i];
@@ -78,7 +94,7 @@ __device__ __forceinline__ void find_bin(const uint32_t* h, int nb, int krem, in
     if (lane >= o) incl += v;
   }
   if (lane == 31) s_wsum[warp] = incl;
-  __syncthreads();
+  bar();
   int wbase = 0;
   for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
   incl += wbase;
@@ -95,7 +111,7 @@ __device__ __forceinline__ void find_bin(const uint32_t* h, int nb, int krem, in
       run += c;
     }
   }
-  __syncthreads();
+  bar();
 }
 
 // tot[i] = sum over the cluster's CTAs of their local[i], i < nb (nb a multiple
@@ -161,189 +177,207 @@ __device__ __forceinline__ void score_slice(const float* qs, const uint16_t* __r
   }
 }
 
-// The cut over the cluster (requires C > kc; all threads of all CTAs call it
-// after score_slice and a __syncthreads).  after_round1(b1) is called by all
-// threads once b1 is known: every key with (key >> 21) > b1 is selected.
-template <typename Hook>
-__device__ Cut find_cut(const Arrays& a, int n, int kc, int S, uint32_t rank, Hook after_round1) {
-  __shared__ int s_ncand, s_above, s_roff[kMaxCluster + 1], s_rgt[kMaxCluster], s_req[kMaxCluster];
-  __shared__ int s_wsum[kWarps], s_bin, s_krem;
-  __shared__ uint32_t s_counts[2];  // keys > T and keys == T in this slice
+// Round 1 of the cut (requires C > kc; all threads of all CTAs, after
+// score_slice and a __syncthreads): the cluster's histogram of the top 11 key
+// bits gives the bin b1 holding the kc-th largest key.  Every key with
+// (key >> 21) > b1 is selected whatever the rest of the cut.
+struct Round1 {
+  uint32_t b1;
+  int krem1;      // rank of the cut inside bin b1
+  int ncand_tot;  // keys of bin b1 over the cluster
+};
 
-  // ---- round 1: the cluster's histogram of the top 11 key bits -> bin b1
+__device__ __forceinline__ Round1 round1(const Arrays& a, int kc, int S) {
+  __shared__ int s_wsum[kWarps], s_bin, s_krem;
   cluster_sync();
   cluster_sum(a.hist1, a.tot, 2048, S);
-  find_bin(a.tot, 2048, kc, s_wsum, &s_bin, &s_krem);
-  Cut cut;
-  cut.b1 = (uint32_t)s_bin;
-  const uint32_t b1 = cut.b1;
-  const int krem1 = s_krem;
-  const int ncand_tot = (int)a.tot[b1];  // keys of bin b1 over the cluster (same on every CTA)
-  after_round1(b1);
+  find_bin(a.tot, 2048, kc, s_wsum, &s_bin, &s_krem, CtaBar());
+  Round1 r;
+  r.b1 = (uint32_t)s_bin;
+  r.krem1 = s_krem;
+  r.ncand_tot = (int)a.tot[r.b1];
+  return r;
+}
 
+// Rest of the cut when the cluster's keys of bin b1 fit the candidate buffer
+// (ncand_tot <= cap), run by the group of Bar: each CTA publishes its keys of
+// bin b1 and its count of keys above the bin (one cluster barrier, which the
+// threads outside the group must also arrive at); every CTA gathers those few
+// keys and resolves the remaining 21 bits and every CTA's output offset by
+// itself.  hist2 and hist3 must be zero.
+template <class Bar>
+__device__ Cut fast_cut(const Arrays& a, int n, int S, uint32_t rank, const Round1& r1, Bar bar) {
+  constexpr int NT = Bar::kNT;
+  __shared__ int s_ncand, s_above, s_roff[kMaxCluster + 1], s_rgt[kMaxCluster], s_req[kMaxCluster];
+  __shared__ int s_wsum[NT / 32], s_bin, s_krem;
+  const uint32_t b1 = r1.b1;
+  const int ncand_tot = r1.ncand_tot;
+  Cut cut;
+  cut.b1 = b1;
   cut.cta_eq = 0;
   cut.cta_sel = 0;
-  if (ncand_tot <= a.cap) {
-    // ---- round 2: publish this slice's keys of bin b1 and its count of keys
-    // above the bin; every CTA gathers all lists and resolves the last 21 bits
-    // and all output offsets by itself.
-    if (threadIdx.x == 0) {
-      s_ncand = 0;
-      s_above = 0;
-    }
-    __syncthreads();
-    {
-      int above = 0;
-      constexpr int k4 = 2048 / kThreads;
-      for (int i = threadIdx.x * k4; i < ((int)threadIdx.x + 1) * k4; ++i)
-        above += (uint32_t)i > b1 ? (int)a.hist1[i] : 0;
+  if (threadIdx.x == 0) {
+    s_ncand = 0;
+    s_above = 0;
+  }
+  bar();
+  {
+    int above = 0;
+    constexpr int k4 = 2048 / NT;
+    for (int i = threadIdx.x * k4; i < ((int)threadIdx.x + 1) * k4; ++i) above += (uint32_t)i > b1 ? (int)a.hist1[i] : 0;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
-      if ((threadIdx.x & 31) == 0) atomicAdd(&s_above, above);
-      for (int i = threadIdx.x; i < n; i += kThreads) {
-        const uint32_t key = a.keys[i];
-        if ((key >> 21) == b1) a.cand[atomicAdd(&s_ncand, 1)] = key;  // at most ncand_tot <= cap
-      }
-    }
-    cluster_sync();
-    if (threadIdx.x < 32) {
-      const int r = threadIdx.x;
-      const int nc = r < S ? (int)dsmem_ld_u32(&s_ncand, (uint32_t)r) : 0;
-      int incl = nc;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (r >= o) incl += v;
-      }
-      if (r < S) {
-        s_roff[r] = incl - nc;
-        s_rgt[r] = (int)dsmem_ld_u32(&s_above, (uint32_t)r);
-        s_req[r] = 0;
-      }
-      if (r == S - 1) s_roff[S] = incl;
-    }
-    __syncthreads();
-    // one remote load per gathered key, all ranks at once
-    for (int i = threadIdx.x; i < ncand_tot; i += kThreads) {
-      int r = 0;
-      while (r + 1 < S && i >= s_roff[r + 1]) ++r;
-      a.gcand[i] = dsmem_ld_u32(a.cand + (i - s_roff[r]), (uint32_t)r);
-    }
-    __syncthreads();
-    // bits 20..10, then 9..0, among the gathered keys (all of them are in bin b1)
-    for (int i = threadIdx.x; i < ncand_tot; i += kThreads) atomicAdd(&a.hist2[(a.gcand[i] >> 10) & 2047u], 1u);
-    __syncthreads();
-    find_bin(a.hist2, 2048, krem1, s_wsum, &s_bin, &s_krem);
-    const uint32_t pre2 = (b1 << 11) | (uint32_t)s_bin;
-    const int krem2 = s_krem;
-    for (int i = threadIdx.x; i < ncand_tot; i += kThreads) {
-      const uint32_t key = a.gcand[i];
-      if ((key >> 10) == pre2) atomicAdd(&a.hist3[key & 1023u], 1u);
-    }
-    __syncthreads();
-    find_bin(a.hist3, 1024, krem2, s_wsum, &s_bin, &s_krem);
-    cut.T = (pre2 << 10) | (uint32_t)s_bin;
-    cut.take_eq = s_krem;
-    // per-CTA counts of keys > T and == T among the gathered keys
-    for (int i = threadIdx.x; i < ncand_tot; i += kThreads) {
-      const uint32_t key = a.gcand[i];
-      int r = 0;
-      while (r + 1 < S && i >= s_roff[r + 1]) ++r;
-      if (key > cut.T) atomicAdd(&s_rgt[r], 1);
-      if (key == cut.T) atomicAdd(&s_req[r], 1);
-    }
-    __syncthreads();
-    for (int r = 0; r < (int)rank; ++r) {
-      cut.cta_sel += s_rgt[r] + min(max(cut.take_eq - cut.cta_eq, 0), s_req[r]);
-      cut.cta_eq += s_req[r];
-    }
-  } else {
-    // ---- rare (huge ties or a flat score range): resolve the last 21 bits with
-    // two more cluster-wide histogram rounds, then exchange exact counts.
-    for (int i = threadIdx.x; i < n; i += kThreads) {
+    for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&s_above, above);
+    for (int i = threadIdx.x; i < n; i += NT) {
       const uint32_t key = a.keys[i];
-      if ((key >> 21) == b1) atomicAdd(&a.hist2[(key >> 10) & 2047u], 1u);
+      if ((key >> 21) == b1) a.cand[atomicAdd(&s_ncand, 1)] = key;  // at most ncand_tot <= cap
     }
-    cluster_sync();
-    cluster_sum(a.hist2, a.tot, 2048, S);
-    find_bin(a.tot, 2048, krem1, s_wsum, &s_bin, &s_krem);
-    const uint32_t pre2 = (b1 << 11) | (uint32_t)s_bin;
-    const int krem2 = s_krem;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      const uint32_t key = a.keys[i];
-      if ((key >> 10) == pre2) atomicAdd(&a.hist3[key & 1023u], 1u);
-    }
-    cluster_sync();
-    cluster_sum(a.hist3, a.tot, 1024, S);
-    find_bin(a.tot, 1024, krem2, s_wsum, &s_bin, &s_krem);
-    cut.T = (pre2 << 10) | (uint32_t)s_bin;
-    cut.take_eq = s_krem;
-    {
-      int ngt = 0, neq = 0;
-      for (int i = threadIdx.x; i < n; i += kThreads) {
-        const uint32_t key = a.keys[i];
-        ngt += key > cut.T;
-        neq += key == cut.T;
-      }
+  }
+  cluster_sync();
+  if (threadIdx.x < 32) {
+    const int r = threadIdx.x;
+    const int nc = r < S ? (int)dsmem_ld_u32(&s_ncand, (uint32_t)r) : 0;
+    int incl = nc;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        ngt += __shfl_xor_sync(0xffffffffu, ngt, o);
-        neq += __shfl_xor_sync(0xffffffffu, neq, o);
-      }
-      if (threadIdx.x == 0) {
-        s_counts[0] = 0;
-        s_counts[1] = 0;
-      }
-      __syncthreads();
-      if ((threadIdx.x & 31) == 0) {
-        atomicAdd(&s_counts[0], (uint32_t)ngt);
-        atomicAdd(&s_counts[1], (uint32_t)neq);
-      }
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (r >= o) incl += v;
     }
-    cluster_sync();
-    for (int r = 0; r < (int)rank; ++r) {
-      const int gt_r = (int)dsmem_ld_u32(&s_counts[0], (uint32_t)r);
-      const int eq_r = (int)dsmem_ld_u32(&s_counts[1], (uint32_t)r);
-      cut.cta_sel += gt_r + min(max(cut.take_eq - cut.cta_eq, 0), eq_r);
-      cut.cta_eq += eq_r;
+    if (r < S) {
+      s_roff[r] = incl - nc;
+      s_rgt[r] = (int)dsmem_ld_u32(&s_above, (uint32_t)r);
+      s_req[r] = 0;
     }
+    if (r == S - 1) s_roff[S] = incl;
+  }
+  bar();
+  // one remote load per gathered key, all ranks at once
+  for (int i = threadIdx.x; i < ncand_tot; i += NT) {
+    int r = 0;
+    while (r + 1 < S && i >= s_roff[r + 1]) ++r;
+    a.gcand[i] = dsmem_ld_u32(a.cand + (i - s_roff[r]), (uint32_t)r);
+  }
+  bar();
+  // bits 20..10, then 9..0, among the gathered keys (all of them are in bin b1)
+  for (int i = threadIdx.x; i < ncand_tot; i += NT) atomicAdd(&a.hist2[(a.gcand[i] >> 10) & 2047u], 1u);
+  bar();
+  find_bin(a.hist2, 2048, r1.krem1, s_wsum, &s_bin, &s_krem, bar);
+  const uint32_t pre2 = (b1 << 11) | (uint32_t)s_bin;
+  const int krem2 = s_krem;
+  for (int i = threadIdx.x; i < ncand_tot; i += NT) {
+    const uint32_t key = a.gcand[i];
+    if ((key >> 10) == pre2) atomicAdd(&a.hist3[key & 1023u], 1u);
+  }
+  bar();
+  find_bin(a.hist3, 1024, krem2, s_wsum, &s_bin, &s_krem, bar);
+  cut.T = (pre2 << 10) | (uint32_t)s_bin;
+  cut.take_eq = s_krem;
+  // per-CTA counts of keys > T and == T among the gathered keys
+  for (int i = threadIdx.x; i < ncand_tot; i += NT) {
+    const uint32_t key = a.gcand[i];
+    int r = 0;
+    while (r + 1 < S && i >= s_roff[r + 1]) ++r;
+    if (key > cut.T) atomicAdd(&s_rgt[r], 1);
+    if (key == cut.T) atomicAdd(&s_req[r], 1);
+  }
+  bar();
+  for (int r = 0; r < (int)rank; ++r) {
+    cut.cta_sel += s_rgt[r] + min(max(cut.take_eq - cut.cta_eq, 0), s_req[r]);
+    cut.cta_eq += s_req[r];
   }
   return cut;
 }
 
-// Id-order compaction of this CTA's selected chunks: warp w owns local ids
-// [w * seg, (w + 1) * seg).  emit(i, pos, upos) is called for every selected
-// local id i with its output position pos (< kc); when LIST, upos numbers the
-// selected keys of bin b1 (those after_round1 could not know) in id order,
-// starting at list_base, and is -1 for the others.
-template <bool LIST, typename Emit>
-__device__ void compact(const Arrays& a, int n, int kc, const Cut& cut, int list_base, Emit emit) {
-  __shared__ int s_wgt[kWarps], s_weq[kWarps], s_wcert[kWarps];
+// Rest of the cut when bin b1 holds more keys than the candidate buffer (huge
+// ties or a flat score range): two more cluster-wide histogram rounds resolve
+// the last 21 bits, then the CTAs exchange exact counts.  All threads.
+static __device__ Cut fallback_cut(const Arrays& a, int n, int S, uint32_t rank, const Round1& r1) {
+  __shared__ int s_wsum[kWarps], s_bin, s_krem;
+  __shared__ uint32_t s_counts[2];  // keys > T and keys == T in this slice
+  const uint32_t b1 = r1.b1;
+  Cut cut;
+  cut.b1 = b1;
+  cut.cta_eq = 0;
+  cut.cta_sel = 0;
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const uint32_t key = a.keys[i];
+    if ((key >> 21) == b1) atomicAdd(&a.hist2[(key >> 10) & 2047u], 1u);
+  }
+  cluster_sync();
+  cluster_sum(a.hist2, a.tot, 2048, S);
+  find_bin(a.tot, 2048, r1.krem1, s_wsum, &s_bin, &s_krem, CtaBar());
+  const uint32_t pre2 = (b1 << 11) | (uint32_t)s_bin;
+  const int krem2 = s_krem;
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const uint32_t key = a.keys[i];
+    if ((key >> 10) == pre2) atomicAdd(&a.hist3[key & 1023u], 1u);
+  }
+  cluster_sync();
+  cluster_sum(a.hist3, a.tot, 1024, S);
+  find_bin(a.tot, 1024, krem2, s_wsum, &s_bin, &s_krem, CtaBar());
+  cut.T = (pre2 << 10) | (uint32_t)s_bin;
+  cut.take_eq = s_krem;
+  {
+    int ngt = 0, neq = 0;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t key = a.keys[i];
+      ngt += key > cut.T;
+      neq += key == cut.T;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ngt += __shfl_xor_sync(0xffffffffu, ngt, o);
+      neq += __shfl_xor_sync(0xffffffffu, neq, o);
+    }
+    if (threadIdx.x == 0) {
+      s_counts[0] = 0;
+      s_counts[1] = 0;
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) {
+      atomicAdd(&s_counts[0], (uint32_t)ngt);
+      atomicAdd(&s_counts[1], (uint32_t)neq);
+    }
+  }
+  cluster_sync();
+  for (int r = 0; r < (int)rank; ++r) {
+    const int gt_r = (int)dsmem_ld_u32(&s_counts[0], (uint32_t)r);
+    const int eq_r = (int)dsmem_ld_u32(&s_counts[1], (uint32_t)r);
+    cut.cta_sel += gt_r + min(max(cut.take_eq - cut.cta_eq, 0), eq_r);
+    cut.cta_eq += eq_r;
+  }
+  return cut;
+}
+
+// Id-order compaction of this CTA's selected chunks by the group of Bar: warp
+// w of the group owns local ids [w * seg, (w + 1) * seg).  emit(i, pos, unc)
+// is called for every selected local id i with its output position pos (< kc)
+// and whether its key lies in bin b1 (a chunk round 1 could not know).
+template <class Bar, typename Emit>
+__device__ void compact(const Arrays& a, int n, int kc, const Cut& cut, Bar bar, Emit emit) {
+  constexpr int NW = Bar::kNT / 32;
+  __shared__ int s_wgt[NW], s_weq[NW];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
+  const int seg = ((n + NW - 1) / NW + 31) & ~31;
   const int w0 = warp * seg, w1 = min(n, w0 + seg);
   const unsigned lt = (1u << lane) - 1u;
   const uint32_t T = cut.T;
   const int take_eq = cut.take_eq;
-  int ngt = 0, neq = 0, ncert = 0;
+  int ngt = 0, neq = 0;
   for (int base = w0; base < w1; base += 32) {
     const int i = base + lane;
     const uint32_t key = i < w1 ? a.keys[i] : 0u;
     ngt += __popc(__ballot_sync(0xffffffffu, i < w1 && key > T));
     neq += __popc(__ballot_sync(0xffffffffu, i < w1 && key == T));
-    if (LIST) ncert += __popc(__ballot_sync(0xffffffffu, i < w1 && (key >> 21) > cut.b1));
   }
   if (lane == 0) {
     s_wgt[warp] = ngt;
     s_weq[warp] = neq;
-    s_wcert[warp] = ncert;
   }
-  __syncthreads();
-  int eq_base = cut.cta_eq, sel_base = cut.cta_sel, unc_base = list_base;
+  bar();
+  int eq_base = cut.cta_eq, sel_base = cut.cta_sel;
   for (int w = 0; w < warp; ++w) {
-    const int sel_w = s_wgt[w] + min(max(take_eq - eq_base, 0), s_weq[w]);
-    sel_base += sel_w;
-    unc_base += sel_w - s_wcert[w];
+    sel_base += s_wgt[w] + min(max(take_eq - eq_base, 0), s_weq[w]);
     eq_base += s_weq[w];
   }
   for (int base = w0; base < w1; base += 32) {
@@ -355,14 +389,7 @@ __device__ void compact(const Arrays& a, int n, int kc, const Cut& cut, int list
     const bool sel = gt || (eq && eq_base + __popc(beq & lt) < take_eq);
     const unsigned bsel = __ballot_sync(0xffffffffu, sel);
     const int pos = sel_base + __popc(bsel & lt);
-    int upos = -1;
-    if (LIST) {
-      const bool unc = sel && (key >> 21) <= cut.b1;
-      const unsigned bunc = __ballot_sync(0xffffffffu, unc);
-      if (unc) upos = unc_base + __popc(bunc & lt);
-      unc_base += __popc(bunc);
-    }
-    if (sel && pos < kc) emit(i, pos, upos);
+    if (sel && pos < kc) emit(i, pos, (key >> 21) <= cut.b1);
     eq_base += __popc(beq);
     sel_base += __popc(bsel);
   }

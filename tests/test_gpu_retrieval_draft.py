@@ -93,7 +93,9 @@ def test_retrieval_draft_all_equal_scores(cuda_lib):
 
 
 def test_retrieval_draft_repeated_calls_agree(cuda_lib):
-    """No state survives a call: the same inputs give bit-identical outputs."""
+    """No state survives a call: the same inputs give the same selection
+    (bit-identical) and the same attention up to the summation order, which
+    follows the order in which chunks reach the consumer warps."""
     w = small_workload(B=2, Hq=8, Hkv=2, L=30000, budget=4096, L_min=20000)
     c = make_case(w)
     Cmax = -(-w.L // w.chunk)
@@ -101,5 +103,6 @@ def test_retrieval_draft_repeated_calls_agree(cuda_lib):
     cuda_lib.tf_build_chunk_means(c["K"], c["seq"], M)
     a = run_fused(cuda_lib, w, c, M)
     b = run_fused(cuda_lib, w, c, M)
-    for x, y in zip(a, b):
+    for x, y in zip(a[:3], b[:3]):
         assert np.array_equal(x, y)
+    np.testing.assert_allclose(a[3], b[3], rtol=1e-5, atol=1e-6)
