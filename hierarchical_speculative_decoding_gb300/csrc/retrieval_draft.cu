@@ -14,11 +14,11 @@
 // list goes through global memory and no second launch waits for the first.
 //  * After the first cluster histogram round fixes the bin b1 of the cut,
 //    every chunk whose key lies above b1 is selected whatever the rest of the
-//    cut.  The CTA lists those chunks and splits: warps 0..3 finish the cut
+//    cut.  The CTA lists those chunks and splits: warps 0..7 finish the cut
 //    (candidate gather, last 21 bits, id-order output, the chunks of bin b1
 //    appended to the list) on a named barrier, while warp 15 stages listed
 //    chunks (K and V rows, cp.async.bulk into a ring of 4 KB slots) and warps
-//    4..14 attend them.  When the cut is done, warps 0..3 join as consumers.
+//    8..14 attend them.  When the cut is done, warps 0..7 join as consumers.
 //    HBM keeps streaming while the cut is resolved.
 //  * Each consumer warp owns one ring slot; the producer hands the next listed
 //    chunk to whichever slot its consumer has released (non-blocking polls in
@@ -47,31 +47,33 @@ using topk::kWarps;
 
 constexpr int kProducerWarp = kWarps - 1;
 constexpr int kComputeWarps = kWarps - 1;
-constexpr int kCutWarps = 4;                            // warps 0..3 finish the cut
+constexpr int kCutWarps = 8;                            // warps 0..7 finish the cut
 constexpr int kRingSlots = kComputeWarps;               // one slot per consumer warp
-constexpr int kEarlySlots = kComputeWarps - kCutWarps;  // slots of warps 4..14
+constexpr int kEarlySlots = kComputeWarps - kCutWarps;  // slots of warps 8..14
 constexpr int kSlotBytes = 4096;  // K rows [0, 2 KB), V rows [2 KB, 4 KB)
 constexpr int kCandCap = 2048;    // keys of the threshold bin gathered on every CTA
 constexpr int kMaxList = 2048;    // selected chunks per CTA (kc <= kMaxList)
 constexpr uint32_t kIdleLimit = 1u << 22;  // producer polls without progress before it gives up
 
 // Dynamic shared memory (bytes).
-//  [0, 45056)      ring slots 0..10 (consumers 4..14); during round 1 it holds
+//  [0, 28672)      ring slots 0..6 (consumers 8..14); during round 1 they hold
 //                  tot, which only this CTA reads
-//  [45056, 65536)  hist2, hist3, gcand: the cut group's scratch; ring slots
-//                  11..14 (consumers 0..3) once the cut is done
-//  hist1, cand     read by the other CTAs of the cluster: never overlaid
+//  [28672, 61440)  ring slots 7..14 (consumers 0..7) once the cut is done;
+//                  until then hist2, hist3, gcand (the cut group's scratch)
+//                  and hist1 (read by the other CTAs in round 1, which they
+//                  finish before the cut's cluster barrier)
+//  cand            read by the other CTAs until the end of their cut: never overlaid
 //  alist           this CTA's selected chunks (certain ones first)
 //  keys            this CTA's score keys
 constexpr int kOffTot = 0;
-constexpr int kOffHist2 = kEarlySlots * kSlotBytes;  // 45056
-constexpr int kOffHist3 = kOffHist2 + 2048 * 4;      // 53248
-constexpr int kOffGcand = kOffHist3 + 1024 * 4;      // 57344
-constexpr int kOffHist1 = kOffGcand + kCandCap * 4;  // 65536
-constexpr int kOffCand = kOffHist1 + 2048 * 4;       // 73728
-constexpr int kOffList = kOffCand + kCandCap * 4;    // 81920
-constexpr int kOffKeys = kOffList + kMaxList * 4;    // 90112
-static_assert(kRingSlots * kSlotBytes <= kOffHist1, "the ring must not reach the arrays other CTAs read");
+constexpr int kOffHist2 = kEarlySlots * kSlotBytes;  // 28672
+constexpr int kOffHist3 = kOffHist2 + 2048 * 4;      // 36864
+constexpr int kOffGcand = kOffHist3 + 1024 * 4;      // 40960
+constexpr int kOffHist1 = kOffGcand + kCandCap * 4;  // 49152
+constexpr int kOffCand = kRingSlots * kSlotBytes;    // 61440
+constexpr int kOffList = kOffCand + kCandCap * 4;    // 69632
+constexpr int kOffKeys = kOffList + kMaxList * 4;    // 77824
+static_assert(kOffHist1 + 2048 * 4 <= kOffCand, "the cut's scratch must fit the late slots");
 static_assert(kOffTot + 2048 * 4 <= kOffHist2, "tot must stay inside the early slots");
 
 struct DraftParams {
@@ -90,8 +92,8 @@ struct DraftParams {
 
 size_t draft_smem(int slice) { return (size_t)kOffKeys + (size_t)slice * sizeof(uint32_t); }
 
-// Ring slot of consumer warp w: warps 4..14 take slots 0..10, warps 0..3 (the
-// cut group) slots 11..14.
+// Ring slot of consumer warp w: warps 8..14 take slots 0..6, warps 0..7 (the
+// cut group) slots 7..14.
 __device__ __forceinline__ int slot_of(int warp) { return (warp + kEarlySlots) % kRingSlots; }
 
 template <int NQ>
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
 
   int32_t* out_idx = p.idx + (size_t)unit * p.kc;
   uint32_t T = 0;
-  bool split = false;  // warps 0..3 finish the cut while the others attend
+  bool split = false;  // warps 0..7 finish the cut while the others attend
   topk::Round1 r1{};
   if (C <= p.kc) {
     // Every chunk is selected: ids in order, slots past C hold -1, s_cut = min score.
@@ -247,17 +249,17 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
   }
   const bool cut_group = split && warp < kCutWarps;
   if (cut_group) {
-    // ---- warps 0..3: the rest of the cut, then consumers of slots 11..14
-    const topk::Cut cut = topk::fast_cut(a, n, S, rank, r1, topk::Warps0to3Bar());
+    // ---- warps 0..7: the rest of the cut, then consumers of slots 7..14
+    const topk::Cut cut = topk::fast_cut(a, n, S, rank, r1, topk::Warps0to7Bar());
     T = cut.T;
-    topk::compact(a, n, p.kc, cut, topk::Warps0to3Bar(), [&](int i, int pos, bool unc) {
+    topk::compact(a, n, p.kc, cut, topk::Warps0to7Bar(), [&](int i, int pos, bool unc) {
       out_idx[pos] = c0 + i;
       if (unc) {
         const int at = atomicAdd(&s_ntot, 1);
         if (at < kMaxList) alist[at] = c0 + i;
       }
     });
-    topk::Warps0to3Bar()();
+    topk::Warps0to7Bar()();
     if (threadIdx.x == 0) {
       __threadfence_block();
       s_cut_done = 1;
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
     // whether its end marker went out.  A slot is free once its consumer has
     // released its last chunk; free slots take the next listed chunks in lane
     // order.  Non-blocking polls keep the whole warp in step.
-    fence_proxy_async_smem();  // slots 0..10 held tot (generic-proxy writes)
+    fence_proxy_async_smem();  // slots 0..6 held tot (generic-proxy writes)
     const unsigned lt = (1u << lane) - 1u;
     int nact = split ? kEarlySlots : kRingSlots;
     bool fin = !split;
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
         list_len = min(*(volatile int*)&s_ntot, kMaxList);
         fin = true;
         nact = kRingSlots;
-        fence_proxy_async_smem();  // slots 11..14 held the cut's scratch
+        fence_proxy_async_smem();  // slots 7..14 held the cut's scratch
       }
       const bool active = lane < nact && !marked;
       const bool free_slot = active && (uses == 0 || mbar_test(&bar_empty[lane], (uses - 1) & 1));

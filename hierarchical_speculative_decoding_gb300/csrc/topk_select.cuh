@@ -15,8 +15,8 @@
 // them and resolves the remaining 21 bits by itself (a rare overflow of the
 // candidate buffer falls back to two more cluster histogram rounds).  Every
 // key in a bin above b1 is selected, which callers can act on before the cut
-// is final; the steps after round 1 can run on a group of four warps while the
-// rest of the CTA does other work.  Used by the top-k call and by the fused
+// is final; the steps after round 1 can run on a group of eight warps while
+// the rest of the CTA does other work.  Used by the top-k call and by the fused
 // retrieval-draft call.
 #pragma once
 
@@ -65,14 +65,14 @@ __device__ __forceinline__ void zero_hists(const Arrays& a) {
 }
 
 // Barriers for the group of threads running a step: the whole CTA, or warps
-// 0..3 on named barrier 1 while the other warps do something else.
+// 0..7 on named barrier 1 while the other warps do something else.
 struct CtaBar {
   static constexpr int kNT = kThreads;
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
 };
-struct Warps0to3Bar {
-  static constexpr int kNT = 128;
-  __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+struct Warps0to7Bar {
+  static constexpr int kNT = 256;
+  __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 };
 
 // Thread t of the group owns nb / NT bins of h (thread 0 the highest); find the
@@ -251,11 +251,21 @@ __device__ Cut fast_cut(const Arrays& a, int n, int S, uint32_t rank, const Roun
     if (r == S - 1) s_roff[S] = incl;
   }
   bar();
-  // one remote load per gathered key, all ranks at once
-  for (int i = threadIdx.x; i < ncand_tot; i += NT) {
-    int r = 0;
-    while (r + 1 < S && i >= s_roff[r + 1]) ++r;
-    a.gcand[i] = dsmem_ld_u32(a.cand + (i - s_roff[r]), (uint32_t)r);
+  // one remote load per gathered key, all ranks at once; each thread's loads
+  // are issued together before any is used
+  for (int base = threadIdx.x; base < ncand_tot; base += 4 * NT) {
+    uint32_t v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * NT;
+      int r = 0;
+      if (i < ncand_tot)
+        while (r + 1 < S && i >= s_roff[r + 1]) ++r;
+      v[u] = i < ncand_tot ? dsmem_ld_u32(a.cand + (i - s_roff[r]), (uint32_t)r) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (base + u * NT < ncand_tot) a.gcand[base + u * NT] = v[u];
   }
   bar();
   // bits 20..10, then 9..0, among the gathered keys (all of them are in bin b1)
