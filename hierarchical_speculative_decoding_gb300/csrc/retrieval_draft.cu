@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
     qsm[h * kHeadDim + u * 4 + (d & 3)] = v;
   }
   __syncthreads();
-  topk::score_slice(qs, p.M + (size_t)unit * Cmax * kHeadDim, c0, c1, a);
+  topk::score_slice<8>(qs, p.M + (size_t)unit * Cmax * kHeadDim, c0, c1, a);
   __syncthreads();
 
   const uint16_t* Ku = p.K + (size_t)unit * p.Lmax * kHeadDim;

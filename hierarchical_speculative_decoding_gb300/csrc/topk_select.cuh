@@ -136,8 +136,9 @@ __device__ __forceinline__ void cluster_sum(const uint32_t* local, uint32_t* tot
 
 // Scores of chunks [c0, c1) of one unit into keys[c - c0] and hist1.  qs: the
 // group's summed query (128 floats in shared memory); Mu: the unit's means.
-// A half-warp reads one 256-byte mean row with 16-byte loads, kUnroll rows in
-// flight per half-warp.
+// A half-warp reads one 256-byte mean row with 16-byte loads, U rows in flight
+// per half-warp (kUnroll unless given).
+template <int U = kUnroll>
 __device__ __forceinline__ void score_slice(const float* qs, const uint16_t* __restrict__ Mu, int c0, int c1,
                                             const Arrays& a) {
   const int half = (threadIdx.x >> 4) & 1, l16 = threadIdx.x & 15, wid = threadIdx.x >> 5;
@@ -148,16 +149,16 @@ __device__ __forceinline__ void score_slice(const float* qs, const uint16_t* __r
   constexpr int kHalfWarps = kThreads / 16;
   // The loop bound is warp-uniform (the shuffles need the whole warp); each
   // half-warp owns chunk base + half + u * kHalfWarps.
-  for (int base = c0 + 2 * wid; base < c1; base += kHalfWarps * kUnroll) {
+  for (int base = c0 + 2 * wid; base < c1; base += kHalfWarps * U) {
     const int cb = base + half;
-    uint4 v[kUnroll];
+    uint4 v[U];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int c = cb + u * kHalfWarps;
       v[u] = (c < c1) ? ld_stream16(Ml + (size_t)c * kHeadDim) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       float f[8];
       unpack8(v[u], f);
       float s = 0.0f;
