@@ -353,6 +353,46 @@ def verify_attn(Q_bits, K_bits, V_bits, seq_lens, scale):
     return out
 
 
+def sparse_verify_positions(idx_row, n_sel, L, T, j, chunk, Lmax):
+    """Keys seen by query j (0 <= j < T) of the retrieval drafter's verification.
+
+    Reading of the level-1 check (blog page, "The Three Forces of TriForce":
+    the retrieval drafter, i.e. the target model over the retrieved KV blocks,
+    verifies the tiny drafter's candidates; "Dual Rejection Sampling:
+    Mathematical Losslessness": the candidates are checked in one pass): the
+    cache already holds the T candidates' keys at positions L-T .. L-1; the
+    drafter's own cache is the retrieved chunks of the context before them, so
+    query j sees the valid tokens of the selected chunks that lie before L-T,
+    then candidates 0..j (chain-causal).  List order: selection, then candidates.
+    """
+    start = max(L - T, 0)
+    pre = [t for t in sparse_positions(idx_row, n_sel, L, chunk, Lmax) if t < start]
+    return np.array(pre + list(range(start, max(L - T + j + 1, start))), dtype=np.int64)
+
+
+def sparse_verify_attn(Q_bits, K_bits, V_bits, seq_lens, idx, n_sel, chunk, scale):
+    """Level-1 verification attention over the retrieval cache plus the candidates.
+
+    Q [B, Hq, T, D] bf16 bits, idx [B, Hkv, kc], n_sel [B, Hkv] -> float64
+    [B, Hq, T, D]; query j of head h attends to sparse_verify_positions.
+    """
+    Q = bf16_to_f64(Q_bits)
+    K = bf16_to_f64(K_bits)
+    V = bf16_to_f64(V_bits)
+    B, Hq, T, D = Q.shape
+    Hkv, Lmax = K.shape[1], K.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, T, D))
+    for b in range(B):
+        L = valid_len(seq_lens[b], Lmax)
+        for g in range(Hkv):
+            for j in range(T):
+                pos = sparse_verify_positions(idx[b, g], n_sel[b, g], L, T, j, chunk, Lmax)
+                for h in range(g * G, (g + 1) * G):
+                    out[b, h, j] = attend(Q[b, h, j], K[b, g, pos], V[b, g, pos], scale)[0]
+    return out
+
+
 # ---------------------------------------------------------------------------
 # a8: lossless accept / resample
 # ---------------------------------------------------------------------------

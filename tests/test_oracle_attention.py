@@ -156,3 +156,71 @@ def test_positions_beyond_length_are_never_read():
     assert np.all(np.isfinite(O.stream_window_attn(_bits(q), _bits(K), _bits(V), seq, 4, 16, 0.1)))
     Q = _rand_bf16((B, Hq, 3, D), 13)
     assert np.all(np.isfinite(O.verify_attn(_bits(Q), _bits(K), _bits(V), seq, 0.1)))
+
+
+# ---------------------------------------------------------------- level-1 verification over the retrieval cache
+
+
+def _compacted_verify(Q, K, V, b, g, rows_pre, L, T, scale):
+    """Verification over a cache rebuilt as [retrieved prefix rows, the T candidate
+    rows]: query j then sees the prefix and candidates 0..j by verify_positions."""
+    cand = list(range(max(L - T, 0), L))
+    keep = list(rows_pre) + cand
+    Kc = K[b : b + 1, g : g + 1, keep]
+    Vc = V[b : b + 1, g : g + 1, keep]
+    return O.verify_attn(_bits(Q[b : b + 1]), _bits(Kc), _bits(Vc), np.array([len(keep)]), scale)[0]
+
+
+def test_sparse_verify_equals_verify_when_every_prefix_chunk_is_selected():
+    B, Hq, Hkv, L, D, T, chunk = 2, 4, 2, 77, 128, 5, 8
+    Q = _rand_bf16((B, Hq, T, D), 31)
+    K = _rand_bf16((B, Hkv, L, D), 32)
+    V = _rand_bf16((B, Hkv, L, D), 33)
+    seq = np.array([77, 50])
+    kc = 10
+    idx = np.full((B, Hkv, kc), -1)
+    n_sel = np.zeros((B, Hkv), dtype=np.int64)
+    for b in range(B):
+        C = -(-seq[b] // chunk)
+        for g in range(Hkv):
+            ids = np.random.default_rng(b * 7 + g).permutation(C)  # any order
+            idx[b, g, :C] = ids
+            n_sel[b, g] = C
+    sv = O.sparse_verify_attn(_bits(Q), _bits(K), _bits(V), seq, idx, n_sel, chunk, 0.088)
+    full = O.verify_attn(_bits(Q), _bits(K), _bits(V), seq, 0.088)
+    np.testing.assert_allclose(sv, full, rtol=1e-12, atol=1e-12)
+
+
+def test_sparse_verify_equals_verify_on_the_compacted_cache():
+    """A selection with a chunk straddling the candidates, an invalid id and a
+    partial last chunk: the result is verification over [retrieved prefix rows,
+    candidates] (rows of selected chunks at or past L-T are not counted twice)."""
+    B, Hq, Hkv, L, D, T, chunk = 1, 6, 2, 90, 128, 6, 8
+    Q = _rand_bf16((B, Hq, T, D), 34)
+    K = _rand_bf16((B, Hkv, L, D), 35)
+    V = _rand_bf16((B, Hkv, L, D), 36)
+    seq = np.array([86])  # candidates at 80..85; chunk 10 holds 80..85 (partial), chunk 9 72..79
+    idx = np.array([[[3, 10, 0, 99, 9], [5, -1, 7, 1, 2]]])
+    n_sel = np.array([[5, 5]])
+    sv = O.sparse_verify_attn(_bits(Q), _bits(K), _bits(V), seq, idx, n_sel, chunk, 0.07)
+    for g in range(Hkv):
+        rows = []
+        for c in idx[0, g]:
+            if 0 <= c < -(-seq[0] // chunk):
+                rows += [t for t in range(c * chunk, min(c * chunk + chunk, seq[0])) if t < seq[0] - T]
+        ref = _compacted_verify(Q[:, g * 3 : (g + 1) * 3], K, V, 0, g, rows, seq[0], T, 0.07)
+        np.testing.assert_allclose(sv[0, g * 3 : (g + 1) * 3], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_sparse_verify_with_an_empty_selection_sees_only_the_candidates():
+    B, Hq, Hkv, L, D, T = 1, 2, 1, 40, 128, 4
+    Q = _rand_bf16((B, Hq, T, D), 37)
+    K = _rand_bf16((B, Hkv, L, D), 38)
+    V = _rand_bf16((B, Hkv, L, D), 39)
+    seq = np.array([40])
+    sv = O.sparse_verify_attn(_bits(Q), _bits(K), _bits(V), seq, np.full((1, 1, 4), -1), np.zeros((1, 1)), 8, 0.1)
+    tail = O.verify_attn(_bits(Q), _bits(K[:, :, 36:]), _bits(V[:, :, 36:]), np.array([4]), 0.1)
+    np.testing.assert_allclose(sv, tail, rtol=1e-12, atol=1e-12)
+    # the first candidate sees only itself: its output is its own V row
+    np.testing.assert_allclose(sv[0, :, 0], np.broadcast_to(O.bf16_to_f64(_bits(V))[0, 0, 36], (Hq, D)), rtol=0,
+                               atol=0)
