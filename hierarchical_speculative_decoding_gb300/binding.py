@@ -36,6 +36,8 @@ _SIGS = {
     "tf_retrieval_draft_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
     "tf_stream_window_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
     "tf_stream_window_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
+    "tf_sparse_verify_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
+    "tf_sparse_verify_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_verify_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
     "tf_verify_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_spec_accept_workspace": (_S, [_I, _I]),
@@ -208,6 +210,32 @@ def tf_retrieval_draft_attn(q, M, K, V, seq_lens, kc, scale, idx=None, n_sel=Non
                                           chunk, kc, float(scale), _ptr(idx), _ptr(n_sel), _ptr(s_cut), _ptr(out),
                                           _stream(stream)), "tf_retrieval_draft_attn")
     return idx, n_sel, out
+
+
+def tf_sparse_verify_attn_workspace(B, Hq, Hkv, kc, T):
+    return int(load().tf_sparse_verify_attn_workspace(B, Hq, Hkv, kc, T))
+
+
+def tf_sparse_verify_attn(Q, K, V, seq_lens, idx, n_sel, scale, out=None, ws=None, chunk=8, stream=None):
+    """Level-1 verification: T candidate queries over the retrieved chunks before
+    the candidates plus the candidates themselves (chain-causal).  Q [B, Hq, T, D]."""
+    _need(Q, torch.bfloat16, "Q", 4)
+    _need(K, torch.bfloat16, "K", 4)
+    _need(V, torch.bfloat16, "V", 4)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(idx, torch.int32, "idx", 3)
+    _need(n_sel, torch.int32, "n_sel", 2)
+    B, Hq, T, D = Q.shape
+    _, Hkv, Lmax, _ = K.shape
+    kc = idx.shape[2]
+    if out is None:
+        out = torch.empty((B, Hq, T, D), dtype=torch.float32, device=Q.device)
+    _need(out, torch.float32, "out", 4)
+    ws, nbytes = _ws(ws, tf_sparse_verify_attn_workspace(B, Hq, Hkv, kc, T), Q.device)
+    _check(load().tf_sparse_verify_attn(_ptr(Q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(idx), _ptr(n_sel), B, Hq,
+                                        Hkv, Lmax, D, chunk, kc, T, float(scale), _ptr(out), _ptr(ws), nbytes,
+                                        _stream(stream)), "tf_sparse_verify_attn")
+    return out
 
 
 def tf_sparse_decode_attn_noalloc(q, K, V, seq_lens, idx, n_sel, scale, out, chunk=8, stream=None):

@@ -24,6 +24,15 @@
 // tile t.  Splits are merged with the log-sum-exp identity by the last CTA of
 // each unit (atomic ticket).  Every mbarrier wait is bounded; on a timeout the
 // CTA records a nonzero status word at the start of the workspace and leaves.
+//
+// The same kernel (GATHER) serves the retrieval drafter's check of the tiny
+// drafter's candidates ("The Three Forces of TriForce": the target model over
+// the retrieved KV blocks verifies the drafts): query j sees the valid rows of
+// the selected 8-token chunks before the candidates (positions < L-T) and
+// candidates 0..j.  A key tile is then sixteen 8-row pieces (the selected
+// chunks in list order, then the candidate rows), each loaded by an 8-row TMA
+// box that lands on one 1 KB swizzle atom of the tile; the softmax warps take
+// every key's position from a per-CTA piece table for the masks.
 #include <cuda_bf16.h>
 
 #include "sm100_ptx.cuh"
@@ -41,6 +50,9 @@ constexpr int kStageBytes = 2 * kTile * kHeadDim * 2;  // K + V tile
 constexpr int kThreads = 192;       // 6 warps
 constexpr int kSoftmaxThreads = 128;
 constexpr int kMaxRows = 32;        // query rows per CTA (N <= 32)
+constexpr int kPiece = 8;           // rows per gathered piece (one chunk, one swizzle atom)
+constexpr int kPiecesPerTile = kTile / kPiece;
+constexpr int kMaxTilesPerCta = 16;  // gathered tiles per split (piece table size)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kTmemCols = 128;
 
@@ -55,6 +67,10 @@ struct VerifyParams {
   float* part_o;  // [units * ngroups, splits_cap, kMaxRows, D]
   int Hq, Hkv, Lmax, T, ngroups, splits, splits_cap;
   float scale_log2;
+  // gathered mode only
+  const int32_t* idx;    // [B * Hkv, kc] selected chunk ids
+  const int32_t* n_sel;  // [B * Hkv]
+  int kc, tiles_per;     // tiles per split
 };
 
 template <int NPAD>
@@ -82,7 +98,7 @@ __device__ __forceinline__ void named_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
 }
 
-template <int NPAD>
+template <int NPAD, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_constant__ CUtensorMap mapK,
                                                                   const __grid_constant__ CUtensorMap mapV,
                                                                   VerifyParams p) {
@@ -95,6 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   __shared__ float alpha_s[2][NPAD];
   __shared__ int rescaled_s[2];
   __shared__ int s_last, s_abort;
+  __shared__ int s_pstart[GATHER ? kPiecesPerTile * kMaxTilesPerCta : 1];  // first position, -1: none
+  __shared__ int s_pcand[GATHER ? kPiecesPerTile * kMaxTilesPerCta : 1];   // 1: candidate rows
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + S::kOffQ;
@@ -134,12 +152,38 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   pdl_wait();  // everything above is on-chip set-up that may overlap the previous kernel
   const int L = clamp_len(p.seq_lens[b], p.Lmax);
 
-  // key range of this split: whole tiles
-  const int tiles_all = (L + kTile - 1) / kTile;
-  const int tiles_per = (tiles_all + p.splits - 1) / p.splits;
-  const int k0 = blockIdx.x * tiles_per * kTile;
-  const int k1 = min(L, k0 + tiles_per * kTile);
-  const int ntiles = k1 > k0 ? (k1 - k0 + kTile - 1) / kTile : 0;
+  // key range of this split: whole tiles (contiguous), or tiles of the piece
+  // list (gathered: selected chunks, then the candidate rows)
+  int k0 = 0, k1 = 0, ntiles = 0;
+  const int cstart = max(0, L - p.T);  // first candidate position
+  if (!GATHER) {
+    const int tiles_all = (L + kTile - 1) / kTile;
+    const int tiles_per = (tiles_all + p.splits - 1) / p.splits;
+    k0 = blockIdx.x * tiles_per * kTile;
+    k1 = min(L, k0 + tiles_per * kTile);
+    ntiles = k1 > k0 ? (k1 - k0 + kTile - 1) / kTile : 0;
+  } else {
+    const int C = (L + kChunk - 1) / kChunk;
+    const int nsel = min(max(p.n_sel[unit], 0), p.kc);
+    const int npieces = nsel + (L - cstart + kPiece - 1) / kPiece;
+    const int tiles_all = (npieces + kPiecesPerTile - 1) / kPiecesPerTile;
+    const int t0 = blockIdx.x * p.tiles_per;
+    ntiles = max(0, min(tiles_all, t0 + p.tiles_per) - t0);
+    const int32_t* sel = p.idx + (size_t)unit * p.kc;
+    for (int e = tid; e < kPiecesPerTile * ntiles; e += kThreads) {
+      const int gp = t0 * kPiecesPerTile + e;
+      int st = -1, cand = 0;
+      if (gp < nsel) {
+        const int c = sel[gp];
+        if (c >= 0 && c < C) st = c * kChunk;
+      } else if (gp < npieces) {
+        st = cstart + (gp - nsel) * kPiece;
+        cand = 1;
+      }
+      s_pstart[e] = st;
+      s_pcand[e] = cand;
+    }
+  }
   // Q rows of this group -> shared memory, [NPAD x 128] bf16 in two swizzled halves.
   {
     const uint16_t* Qg = p.Q + (((size_t)b * p.Hq + (size_t)g * G) * p.T + row0) * kHeadDim;
@@ -159,6 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
+    // lane 0 issues; the other lanes wait at the __syncwarp below so that the
+    // warp reaches the block barrier only once lane 0 has left its loop
     if (lane == 0) {
       const int row_base = unit * p.Lmax + k0;
       for (int t = 0; t < ntiles; ++t) {
@@ -170,16 +216,35 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         if (*(volatile int*)&s_abort) break;
         uint8_t* sk = smem + s * kStageBytes;
         uint8_t* sv = sk + kTile * kHeadDim * 2;
-        mbar_arrive_expect_tx(&bar_full[s], kStageBytes);
-        const int y = row_base + t * kTile;
-        tma_load_2d(sk, &mapK, &bar_full[s], 0, y);
-        tma_load_2d(sk + 16384, &mapK, &bar_full[s], 64, y);
-        tma_load_2d(sv, &mapV, &bar_full[s], 0, y);
-        tma_load_2d(sv + 16384, &mapV, &bar_full[s], 64, y);
+        if (!GATHER) {
+          mbar_arrive_expect_tx(&bar_full[s], kStageBytes);
+          const int y = row_base + t * kTile;
+          tma_load_2d(sk, &mapK, &bar_full[s], 0, y);
+          tma_load_2d(sk + 16384, &mapK, &bar_full[s], 64, y);
+          tma_load_2d(sv, &mapV, &bar_full[s], 0, y);
+          tma_load_2d(sv + 16384, &mapV, &bar_full[s], 64, y);
+        } else {
+          int cnt = 0;
+          for (int i = 0; i < kPiecesPerTile; ++i) cnt += s_pstart[t * kPiecesPerTile + i] >= 0 ? 1 : 0;
+          mbar_arrive_expect_tx(&bar_full[s], (uint32_t)cnt * (kStageBytes / kPiecesPerTile));
+          for (int i = 0; i < kPiecesPerTile; ++i) {
+            const int st = s_pstart[t * kPiecesPerTile + i];
+            if (st < 0) continue;
+            const int y = unit * p.Lmax + st;
+            const int off = i * kPiece * 128;  // rows 8i..8i+7 of each 64-column half
+            tma_load_2d(sk + off, &mapK, &bar_full[s], 0, y);
+            tma_load_2d(sk + 16384 + off, &mapK, &bar_full[s], 64, y);
+            tma_load_2d(sv + off, &mapV, &bar_full[s], 0, y);
+            tma_load_2d(sv + 16384 + off, &mapV, &bar_full[s], 64, y);
+          }
+        }
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
+    // lane 0 issues; the __syncwarp below keeps the warp together for the
+    // block barrier and the warp-wide TMEM release at the end
     if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(128, NPAD, false, false);
       const uint32_t idO = idesc_bf16_f32(128, NPAD, true, false);
@@ -221,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         }
       }
     }
+    __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax + correction
     const int q4 = warp & 3;               // TMEM lane quarter of this warp
@@ -238,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     }
     // Every wait is followed by a vote over the 128 threads so that a timeout
     // makes all of them leave the loop together (named barriers stay matched).
+    bool zero_v = false;  // this key row of the tile must be zeroed in V
     for (int t = 0; t <= ntiles; ++t) {
       float sc[NPAD];  // scores, then softmax weights of tile t
       if (t < ntiles) {
@@ -250,11 +317,27 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
 #pragma unroll
         for (int c = 0; c < NPAD; c += 8) tmem_ld8(tmem + (t & 1) * 32 + lane_off + c, sc + c);
         tmem_ld_wait();
-        const int pos = k0 + t * kTile + my;
+        // this key's position and whether it may be seen at all; candidate
+        // rows (every row of the contiguous range) are also chain-limited
+        int pos;
+        bool key_ok, chain;
+        if (!GATHER) {
+          pos = k0 + t * kTile + my;
+          key_ok = pos < k1;
+          chain = true;
+          zero_v = t == ntiles - 1 && !key_ok;  // rows past the range in the last tile
+        } else {
+          const int li = t * kPiecesPerTile + (my >> 3);
+          const int st = s_pstart[li];
+          chain = s_pcand[li] != 0;
+          pos = st + (my & 7);
+          key_ok = st >= 0 && pos < L && (chain ? pos >= cstart : pos < cstart);
+          zero_v = !key_ok;  // rows of empty pieces, past L, or counted elsewhere
+        }
         bool need = false;
 #pragma unroll
         for (int n = 0; n < NPAD; ++n) {
-          const bool valid = pos < k1 && pos <= lim[n];
+          const bool valid = key_ok && (!chain || pos <= lim[n]);
           sc[n] = valid ? sc[n] * p.scale_log2 : -INFINITY;
           need |= sc[n] > m_run[n] + kRescaleThreshold;
         }
@@ -307,7 +390,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
       if (t < ntiles) {
         // P for this tile as hi + lo bf16 parts (P V error ~2^-17 instead of
         // 2^-9 relative); row n, column = key.
-        const int pos = k0 + t * kTile + my;
         uint8_t* pbuf = sP + (t % S::kNumPBuf) * S::kPBuf;
         const uint32_t off_key = (uint32_t)(my >> 6) * (NPAD * 128);
 #pragma unroll
@@ -320,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           *reinterpret_cast<__nv_bfloat16*>(pbuf + o) = hi;
           *reinterpret_cast<__nv_bfloat16*>(pbuf + S::kPHalf + o) = lo;
         }
-        if (t == ntiles - 1 && pos >= k1) {
-          // Rows past the key range may hold anything (even NaN): zero them in
+        if (zero_v) {
+          // Rows nobody may see can hold anything (even NaN): zero them in
           // the V tile so 0 * V stays 0 in the MMA.  Waiting on the (already
           // completed) TMA barrier orders these writes after the tile landed.
           const int s = t % kStages;
@@ -441,20 +523,62 @@ size_t verify_ws(int units, int rows_all, int Lmax) {
          ug * cap * kMaxRows * kHeadDim * sizeof(float);
 }
 
-template <int NPAD>
+template <int NPAD, bool GATHER>
 tf_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParams& p, dim3 grid,
                  cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(verify_umma_kernel<NPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(verify_umma_kernel<NPAD, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<NPAD>::kDynamic) != cudaSuccess)
       return TF_ERR_CUDA;
     configured = true;
   }
-  if (launch_pdl(verify_umma_kernel<NPAD>, grid, dim3(kThreads), Smem<NPAD>::kDynamic, stream, mk, mv, p) !=
+  if (launch_pdl(verify_umma_kernel<NPAD, GATHER>, grid, dim3(kThreads), Smem<NPAD>::kDynamic, stream, mk, mv, p) !=
       cudaSuccess)
     return TF_ERR_CUDA;
   return launch_status();
+}
+
+// Gathered mode: tiles of the longest possible piece list (kc chunks and at most
+// two 8-row pieces of candidates), and the split count: the work per unit is
+// short, so one wave of CTAs with as many tiles each as the piece table holds
+// beats more, shorter splits (each split pays the pipeline ramp and a merge);
+// when one wave cannot hold the units, the splits that fill whole waves.
+int sparse_verify_tiles(int kc) { return (kc + 2 + kPiecesPerTile - 1) / kPiecesPerTile; }
+
+int sparse_verify_splits(int ug, int tiles, int sms) {
+  const int lo = (tiles + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
+  if ((long long)ug * lo <= sms) {
+    int s = sms / ug;  // one wave
+    if (s > tiles) s = tiles;
+    // fewest splits that keep the per-CTA tile count within one of the one-wave count
+    const int per = (tiles + s - 1) / s;
+    return (tiles + per - 1) / per;
+  }
+  int best = lo;
+  double best_eff = -1.0;
+  for (int waves = 1; waves <= 16; ++waves) {
+    int s = (waves * sms + ug / 2) / ug;
+    if (s < lo) s = lo;
+    if (s > tiles) s = tiles;
+    const long long ctas = (long long)ug * s;
+    const long long full = (ctas + sms - 1) / sms * sms;
+    const double eff = (double)ctas / (double)full;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
+    if (eff > 0.97) break;
+  }
+  return best;
+}
+
+size_t sparse_verify_ws(int units, int rows_all, int kc) {
+  const int ngroups = (rows_all + kMaxRows - 1) / kMaxRows;
+  const size_t ug = (size_t)units * ngroups;
+  const size_t cap = (size_t)sparse_verify_tiles(kc);
+  return 256 + align_up(ug * sizeof(int), 256) + align_up(ug * cap * kMaxRows * 2 * sizeof(float), 256) +
+         ug * cap * kMaxRows * kHeadDim * sizeof(float);
 }
 
 }  // namespace
@@ -503,5 +627,57 @@ extern "C" tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const 
                                       align_up((size_t)ug * p.splits_cap * kMaxRows * 2 * sizeof(float), 256));
   dim3 grid(p.splits, ug);
   const int rows_max = rows_all < kMaxRows ? rows_all : kMaxRows;
-  return rows_max <= 16 ? launch<16>(mk, mv, p, grid, stream) : launch<32>(mk, mv, p, grid, stream);
+  return rows_max <= 16 ? launch<16, false>(mk, mv, p, grid, stream) : launch<32, false>(mk, mv, p, grid, stream);
+}
+
+extern "C" size_t tf_sparse_verify_attn_workspace(int B, int Hq, int Hkv, int kc, int T) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || kc <= 0 || T <= 0 || Hq % Hkv) return 0;
+  return tf::sparse_verify_ws(B * Hkv, (Hq / Hkv) * T, kc);
+}
+
+extern "C" tf_status tf_sparse_verify_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                                           const int32_t* seq_lens, const int32_t* idx, const int32_t* n_sel, int B,
+                                           int Hq, int Hkv, int Lmax, int D, int chunk, int kc, int T, float scale,
+                                           float* out, void* ws, size_t ws_bytes, tf_stream_t stream) {
+  using namespace tf;
+  if (!Q || !K || !V || !seq_lens || !idx || !n_sel || !out) return TF_ERR_INVALID_ARG;
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || Hq % Hkv || T < 1 || kc <= 0) return TF_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return TF_ERR_INVALID_ARG;
+  if (D != kHeadDim || chunk != kChunk || T > 16) return TF_ERR_UNSUPPORTED;
+  if (B == 0 || Lmax == 0) return TF_OK;
+  const long long rows_total = (long long)B * Hkv * Lmax;
+  if (rows_total >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
+  const size_t need = sparse_verify_ws(B * Hkv, (Hq / Hkv) * T, kc);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
+  CUtensorMap mk, mv;
+  if (!make_kv_map(&mk, K, rows_total, kPiece) || !make_kv_map(&mv, V, rows_total, kPiece)) return TF_ERR_CUDA;
+
+  VerifyParams p{};
+  const int rows_all = (Hq / Hkv) * T;
+  p.Q = Q;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Lmax = Lmax;
+  p.T = T;
+  p.ngroups = (rows_all + kMaxRows - 1) / kMaxRows;
+  p.idx = idx;
+  p.n_sel = n_sel;
+  p.kc = kc;
+  const int tiles = sparse_verify_tiles(kc);
+  p.splits_cap = tiles;
+  const int ug = B * Hkv * p.ngroups;
+  p.splits = sparse_verify_splits(ug, tiles, num_sms());
+  p.tiles_per = (tiles + p.splits - 1) / p.splits;
+  p.scale_log2 = scale * kLog2e;
+  char* w = static_cast<char*>(ws);
+  p.status = reinterpret_cast<int*>(w);
+  p.tickets = reinterpret_cast<int*>(w + 256);
+  p.part_ml = reinterpret_cast<float*>(w + 256 + align_up((size_t)ug * sizeof(int), 256));
+  p.part_o = reinterpret_cast<float*>(w + 256 + align_up((size_t)ug * sizeof(int), 256) +
+                                      align_up((size_t)ug * p.splits_cap * kMaxRows * 2 * sizeof(float), 256));
+  dim3 grid(p.splits, ug);
+  const int rows_max = rows_all < kMaxRows ? rows_all : kMaxRows;
+  return rows_max <= 16 ? launch<16, true>(mk, mv, p, grid, stream) : launch<32, true>(mk, mv, p, grid, stream);
 }

@@ -171,6 +171,30 @@ TF_API tf_status tf_retrieval_draft_attn(const uint16_t* q, const uint16_t* M, c
                                   float* out, tf_stream_t stream);
 
 /*
+ * Level-1 verification over the retrieval cache:
+ * the retrieval drafter -- the target model over the retrieved KV blocks --
+ * checks the tiny drafter's candidates in one pass ("TriForce: Hierarchical
+ * Speculative Decoding for LLMs", "The Three Forces of TriForce" and "Dual
+ * Rejection Sampling: Mathematical Losslessness").  The cache already holds
+ * the T candidates' keys/values at positions L-T .. L-1; query j
+ * (0 <= j < T) of head h in group g sees the valid tokens (t < L) of the
+ * chunks idx[b,g,0:n_sel[b,g]] that lie before the candidates (t < L-T), and
+ * candidates 0..j (t in [L-T, L-T+j]):
+ *   out[b,h,j,:] = softmax(scale * Q[b,h,j] . K_P) V_P     (float32)
+ * Ids outside [0, C_b) are skipped; a repeated id is attended once per
+ * occurrence.  Q [B, Hq, T, D] bf16, out [B, Hq, T, D] float32, 1 <= T <= 16.
+ * Tensor-core kernel (tcgen05, bf16 in, fp32 accumulate): each 128-key tile is
+ * gathered from sixteen 8-row pieces by TMA.  Workspace:
+ * tf_sparse_verify_attn_workspace(B, Hq, Hkv, kc, T) bytes, zeroed once; its
+ * first int is a status word (nonzero after a device-side timeout).
+ */
+TF_API size_t tf_sparse_verify_attn_workspace(int B, int Hq, int Hkv, int kc, int T);
+TF_API tf_status tf_sparse_verify_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                                const int32_t* seq_lens, const int32_t* idx, const int32_t* n_sel,
+                                int B, int Hq, int Hkv, int Lmax, int D, int chunk, int kc, int T,
+                                float scale, float* out, void* ws, size_t ws_bytes, tf_stream_t stream);
+
+/*
  * a6 (+ a5) -- StreamingLLM sink + window attention (Force 1 drafter).
  * Positions P = [0, min(n_sink, L)) U [max(n_sink, L - window), L): the first
  * n_sink tokens plus the most recent `window` tokens, de-duplicated.

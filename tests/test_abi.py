@@ -52,6 +52,7 @@ def test_workspace_sizes(lib):
     assert lib.tf_stream_window_attn_workspace(4, 32, 8, 4, 252) > 0
     assert lib.tf_verify_attn_workspace(4, 32, 8, 131072, 6) > 0
     assert lib.tf_spec_accept_workspace(8, 5) >= 8 * 11 * 12
+    assert lib.tf_sparse_verify_attn_workspace(1, 32, 32, 512, 6) > 0
     # workspace grows with the problem
     assert lib.tf_verify_attn_workspace(8, 32, 8, 131072, 6) > lib.tf_verify_attn_workspace(1, 32, 8, 131072, 6)
 
@@ -89,6 +90,17 @@ def test_host_validation_rejects_before_launch(lib):
                                        fake, None) == INVALID  # misaligned means
     assert lib.tf_retrieval_draft_attn(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 16, 64, 0.1, fake, fake, null,
                                        fake, None) == UNSUPPORTED  # chunk 16
+    # sparse verification: Q, K, V, seq, idx, n_sel, B, Hq, Hkv, Lmax, D, chunk, kc, T, scale, out, ws, bytes, s
+    sv = lib.tf_sparse_verify_attn
+    big = 1 << 30
+    assert sv(fake, fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 16, 17, 0.1, fake, fake, big,
+              None) == UNSUPPORTED  # T > 16
+    assert sv(fake, fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 16, 0, 0.1, fake, fake, big,
+              None) == INVALID  # T = 0
+    assert sv(fake, fake, fake, fake, null, fake, 1, 8, 2, 64, 128, 8, 16, 4, 0.1, fake, fake, big,
+              None) == INVALID  # no ids
+    assert sv(fake, fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 16, 4, 0.1, fake, null, 0,
+              None) == WORKSPACE
     assert lib.tf_spec_accept(fake, fake, fake, fake, fake, 1, 4, 100, 0.0, fake, fake, null, fake, 4096,
                               None) == INVALID
     assert lib.tf_spec_accept(fake, null, fake, fake, fake, 1, 4, 100, 1.0, fake, fake, null, fake, 4096,
