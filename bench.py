@@ -378,6 +378,24 @@ def run_gpu(args):
             ms = statistics.mean(ev[l][i].elapsed_time(ev[l][i + 1]) for l in range(layers))
             kernels["two_call_" + k] = {"ms": round(ms, 5), "GBps": round(nb / (ms / 1e3) / 1e9, 1),
                                         "frac_hbm": round(nb / (ms / 1e3) / 1e9 / peak, 4)}
+    # level-1 verification over the retrieval cache (not part of the step): the
+    # step's selection, T verify queries, back-to-back calls over the layers
+    ws_sv = tf.workspace(tf.tf_sparse_verify_attn_workspace(B, Hq, Hkv, w.kc, T), dev)
+    o_sv = torch.empty((B, Hq, T, D), dtype=torch.float32, device=dev)
+    for l in range(min(layers, 4)):
+        tf.tf_sparse_verify_attn(Q_all[l], Kc[l], Vc[l], seq, idx[l], nsel[l], scale, out=o_sv, ws=ws_sv)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for l in range(layers):
+        tf.tf_sparse_verify_attn(Q_all[l], Kc[l], Vc[l], seq, idx[l], nsel[l], scale, out=o_sv, ws=ws_sv)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    sv_ms = s0.elapsed_time(s1) / layers
+    sv_bytes = 2 * B * Hkv * (w.kc * w.chunk + T) * kv_row + B * Hq * T * D * (2 + 4)
+    kernels["sparse_verify_level1"] = {"ms": round(sv_ms, 5), "GBps": round(sv_bytes / (sv_ms / 1e3) / 1e9, 1),
+                                       "frac_hbm": round(sv_bytes / (sv_ms / 1e3) / 1e9 / peak, 4),
+                                       "calls": "tf_sparse_verify_attn", "timing": "back-to-back over the layers"}
     kernels["chunk_means_prefill_1layer"] = {"ms": round(means_ms, 4),
                                              "GBps": round(means_bytes / (means_ms / 1e3) / 1e9, 1)}
     ver_ms = statistics.mean(per_kind["verify"])

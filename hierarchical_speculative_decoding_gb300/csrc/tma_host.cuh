@@ -38,4 +38,19 @@ inline bool make_kv_map(CUtensorMap* m, const void* base, long long rows, int bo
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One 8-row piece of a [rows, 128] bf16 cache as a single box: dims (64
+// columns, rows, two 64-column halves), so the box lands as the piece's two
+// 1 KB swizzle atoms back to back (columns 0..63, then 64..127).
+inline bool make_piece_map(CUtensorMap* m, const void* base, long long rows) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn || rows <= 0) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, 2};
+  cuuint64_t strides[2] = {256, 128};
+  cuuint32_t box[3] = {64, 8, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tf

@@ -53,6 +53,8 @@ constexpr int kMaxRows = 32;        // query rows per CTA (N <= 32)
 constexpr int kPiece = 8;           // rows per gathered piece (one chunk, one swizzle atom)
 constexpr int kPiecesPerTile = kTile / kPiece;
 constexpr int kMaxTilesPerCta = 16;  // gathered tiles per split (piece table size)
+constexpr int kPieceBytes = kPiece * kHeadDim * 2;  // one piece of K (or V): 2 KB
+constexpr int kMaxClusterMerge = 8;  // most splits merged inside one (portable) cluster
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kTmemCols = 128;
 
@@ -71,6 +73,7 @@ struct VerifyParams {
   const int32_t* idx;    // [B * Hkv, kc] selected chunk ids
   const int32_t* n_sel;  // [B * Hkv]
   int kc, tiles_per;     // tiles per split
+  int cmerge;            // 1: the splits of a unit form a cluster and merge through DSMEM
 };
 
 template <int NPAD>
@@ -83,6 +86,12 @@ struct Smem {
   static constexpr int kOffP = kOffQ + kQBytes;
   static constexpr int kBytes = kOffP + kNumPBuf * kPBuf;
   static constexpr int kDynamic = kBytes + 1024;     // slack for 1024-byte alignment
+  // Cluster merge: a split's (m, l) per row and its O rows [NPAD x 128] fp32
+  // reuse the Q and P buffers, which no copy engine writes and the MMAs have
+  // finished reading once the last O has been read back.
+  static constexpr int kOffCm = kOffQ;
+  static constexpr int kOffCo = kOffQ + 256;
+  static_assert(kOffCo + NPAD * kHeadDim * 4 <= kBytes, "cluster merge scratch");
 };
 
 __device__ __forceinline__ bool named_bar_or(bool pred) {
@@ -203,44 +212,58 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    // lane 0 issues; the other lanes wait at the __syncwarp below so that the
-    // warp reaches the block barrier only once lane 0 has left its loop
-    if (lane == 0) {
-      const int row_base = unit * p.Lmax + k0;
-      for (int t = 0; t < ntiles; ++t) {
-        const int s = t % kStages;
-        if (t >= kStages && !mbar_wait(&bar_empty[s], ((t / kStages) - 1) & 1)) {
-          atomicExch(&s_abort, 1);
-          break;
-        }
-        if (*(volatile int*)&s_abort) break;
-        uint8_t* sk = smem + s * kStageBytes;
-        uint8_t* sv = sk + kTile * kHeadDim * 2;
-        if (!GATHER) {
+    if (!GATHER) {
+      // lane 0 issues; the other lanes wait at the __syncwarp below so that the
+      // warp reaches the block barrier only once lane 0 has left its loop
+      if (lane == 0) {
+        const int row_base = unit * p.Lmax + k0;
+        for (int t = 0; t < ntiles; ++t) {
+          const int s = t % kStages;
+          if (t >= kStages && !mbar_wait(&bar_empty[s], ((t / kStages) - 1) & 1)) {
+            atomicExch(&s_abort, 1);
+            break;
+          }
+          if (*(volatile int*)&s_abort) break;
+          uint8_t* sk = smem + s * kStageBytes;
+          uint8_t* sv = sk + kTile * kHeadDim * 2;
           mbar_arrive_expect_tx(&bar_full[s], kStageBytes);
           const int y = row_base + t * kTile;
           tma_load_2d(sk, &mapK, &bar_full[s], 0, y);
           tma_load_2d(sk + 16384, &mapK, &bar_full[s], 64, y);
           tma_load_2d(sv, &mapV, &bar_full[s], 0, y);
           tma_load_2d(sv + 16384, &mapV, &bar_full[s], 64, y);
-        } else {
-          int cnt = 0;
-          for (int i = 0; i < kPiecesPerTile; ++i) cnt += s_pstart[t * kPiecesPerTile + i] >= 0 ? 1 : 0;
-          mbar_arrive_expect_tx(&bar_full[s], (uint32_t)cnt * (kStageBytes / kPiecesPerTile));
-          for (int i = 0; i < kPiecesPerTile; ++i) {
-            const int st = s_pstart[t * kPiecesPerTile + i];
-            if (st < 0) continue;
-            const int y = unit * p.Lmax + st;
-            const int off = i * kPiece * 128;  // rows 8i..8i+7 of each 64-column half
-            tma_load_2d(sk + off, &mapK, &bar_full[s], 0, y);
-            tma_load_2d(sk + 16384 + off, &mapK, &bar_full[s], 64, y);
-            tma_load_2d(sv + off, &mapV, &bar_full[s], 0, y);
-            tma_load_2d(sv + 16384 + off, &mapV, &bar_full[s], 64, y);
+        }
+      }
+      __syncwarp();
+    } else {
+      // Sixteen pieces per tile, one K box and one V box each, issued by the
+      // whole warp after lane 0 has waited for the stage and posted the tile's
+      // bytes; the warp steps through the loop together.  A gathered tile is
+      // laid out piece by piece: [piece][column half][8 rows x 128 B].
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kStages;
+        bool ok = true;
+        if (lane == 0) {
+          if (t >= kStages && !mbar_wait(&bar_empty[s], ((t / kStages) - 1) & 1)) {
+            atomicExch(&s_abort, 1);
+            ok = false;
           }
+          if (*(volatile int*)&s_abort) ok = false;
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const int st = lane < kPiecesPerTile ? s_pstart[t * kPiecesPerTile + lane] : -1;
+        const unsigned have = __ballot_sync(0xffffffffu, st >= 0);
+        if (lane == 0) mbar_arrive_expect_tx(&bar_full[s], (uint32_t)__popc(have) * (kStageBytes / kPiecesPerTile));
+        __syncwarp();
+        // lanes 0..15 fetch the K of piece `lane`, lanes 16..31 its V; a piece
+        // is one 2 KB box that lands as its two 1 KB swizzle atoms
+        const int st_kv = __shfl_sync(0xffffffffu, st, lane & 15);
+        if (st_kv >= 0) {
+          uint8_t* dst = smem + s * kStageBytes + (lane >> 4) * (kTile * kHeadDim * 2) + (lane & 15) * kPieceBytes;
+          tma_load_3d(dst, lane < 16 ? &mapK : &mapV, &bar_full[s], 0, unit * p.Lmax + st_kv, 0);
         }
       }
     }
-    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     // lane 0 issues; the __syncwarp below keeps the warp together for the
@@ -257,7 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           const uint32_t k_addr = smem_u32(smem + s * kStageBytes);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t a = smem_desc(k_addr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+            // K (M = key, K = head dim), K-major: contiguous tiles hold the two
+            // 64-column halves 16 KB apart with 8-key groups 1 KB apart;
+            // gathered tiles hold them 1 KB apart with 8-key groups 2 KB apart
+            const uint64_t a = GATHER ? smem_desc(k_addr + (kk >> 2) * 1024 + (kk & 3) * 32, 16, kPieceBytes)
+                                      : smem_desc(k_addr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
             const uint64_t bd = smem_desc(q_addr + (kk >> 2) * (NPAD * 128) + (kk & 3) * 32, 16, 1024);
             mma_bf16(tmem + (t & 1) * 32, a, bd, idS, kk > 0);
           }
@@ -272,11 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           const uint32_t p_addr = smem_u32(sP + (u % S::kNumPBuf) * S::kPBuf);
 #pragma unroll
           for (int kk = 0; kk < 16; ++kk) {
-            // A = V^T (M = head dim, K = key), MN-major: 64-dim atoms 16 KB apart,
-            // 8-key groups 1 KB apart.  B = P (N = query row, K = key), K-major;
+            // A = V^T (M = head dim, K = key), MN-major: 64-dim atoms 16 KB apart
+            // and 8-key groups 1 KB apart (contiguous), or 1 KB and 2 KB apart
+            // (gathered).  B = P (N = query row, K = key), K-major;
             // the hi part (kk < 8) and then the lo part (kk >= 8) of P.
             const int k8 = kk & 7;
-            const uint64_t a = smem_desc(v_addr + k8 * 2048, 16384, 1024);
+            const uint64_t a = GATHER ? smem_desc(v_addr + k8 * 2 * kPieceBytes, 1024, kPieceBytes)
+                                      : smem_desc(v_addr + k8 * 2048, 16384, 1024);
             const uint64_t bd = smem_desc(p_addr + (kk >> 3) * S::kPHalf + (k8 >> 2) * (NPAD * 128) + (k8 & 3) * 32,
                                           16, 1024);
             mma_bf16(tmem + 64 + (u & 1) * 32, a, bd, idO, kk > 0);
@@ -413,7 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(sv + h * 16384 + my * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(sv + (GATHER ? (my >> 3) * kPieceBytes + h * 1024 + (my & 7) * 128
+                                                     : h * 16384 + my * 128) +
+                                        c * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -437,6 +468,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         if (n < rows) {
           const float l = (red[0][n] + red[1][n]) + (red[2][n] + red[3][n]);
           p.out[(out_row0 + n) * kHeadDim + my] = (l > 0.0f) ? acc[n] / l : 0.0f;
+        }
+      }
+    } else if (p.cmerge) {
+      float* cm = reinterpret_cast<float*>(smem + S::kOffCm);
+      float* co = reinterpret_cast<float*>(smem + S::kOffCo);
+#pragma unroll
+      for (int n = 0; n < NPAD; ++n) {
+        if (n < rows) {
+          if (my == 0) {
+            cm[n * 2 + 0] = m_run[n];
+            cm[n * 2 + 1] = (red[0][n] + red[1][n]) + (red[2][n] + red[3][n]);
+          }
+          co[n * kHeadDim + my] = acc[n];
         }
       }
     } else {
@@ -464,9 +508,66 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     // Let any TMA copy still in flight land before the CTA's shared memory goes away.
     if (tid == 0)
       for (int s = 0; s < kStages; ++s) mbar_wait(&bar_full[s], 0, 1u << 8);
-    return;
+    if (!p.cmerge) return;  // cluster peers still wait for this CTA at the barriers below
   }
   if (p.splits == 1) return;
+
+  if (p.cmerge) {
+    // Every split of the unit has left its partial in shared memory; each rank
+    // of the cluster merges its share of the unit's outputs from all of them.
+    __shared__ float s_w[8 * kMaxRows], s_l[8 * kMaxRows], s_L[kMaxRows];
+    cluster_sync();
+    const int S = p.splits;
+    const uint32_t rank = cluster_ctarank();
+    const float* cm = reinterpret_cast<const float*>(smem + Smem<NPAD>::kOffCm);
+    const float* co = reinterpret_cast<const float*>(smem + Smem<NPAD>::kOffCo);
+    for (int i = tid; i < S * rows; i += kThreads) {
+      const int sp = i / rows, n = i % rows;
+      s_w[i] = __uint_as_float(dsmem_ld_u32(cm + n * 2 + 0, sp));
+      s_l[i] = __uint_as_float(dsmem_ld_u32(cm + n * 2 + 1, sp));
+    }
+    __syncthreads();
+    for (int n = tid; n < rows; n += kThreads) {
+      float mx = -INFINITY;
+      for (int sp = 0; sp < S; ++sp) mx = fmaxf(mx, s_w[sp * rows + n]);
+      float Lsum = 0.0f;
+      for (int sp = 0; sp < S; ++sp) {
+        const float w = merge_scale(s_w[sp * rows + n], mx);
+        s_w[sp * rows + n] = w;
+        Lsum = fmaf(w, s_l[sp * rows + n], Lsum);
+      }
+      s_L[n] = Lsum;
+    }
+    __syncthreads();
+    const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
+    for (int e4 = (int)rank * kThreads + tid; e4 < rows * (kHeadDim / 4); e4 += S * kThreads) {
+      const int n = e4 / (kHeadDim / 4), d = (e4 % (kHeadDim / 4)) * 4;
+      uint4 v[8];
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp)
+        if (sp < S) v[sp] = dsmem_ld_v4(co + n * kHeadDim + d, sp);
+      float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp) {
+        if (sp < S) {
+          const float w = s_w[sp * rows + n];
+          a.x = fmaf(w, __uint_as_float(v[sp].x), a.x);
+          a.y = fmaf(w, __uint_as_float(v[sp].y), a.y);
+          a.z = fmaf(w, __uint_as_float(v[sp].z), a.z);
+          a.w = fmaf(w, __uint_as_float(v[sp].w), a.w);
+        }
+      }
+      const float Lr = s_L[n];
+      const float inv = Lr > 0.0f ? 1.0f / Lr : 0.0f;
+      a.x *= inv;
+      a.y *= inv;
+      a.z *= inv;
+      a.w *= inv;
+      *reinterpret_cast<float4*>(p.out + (out_row0 + n) * kHeadDim + d) = a;
+    }
+    cluster_sync();  // peers keep their shared memory until every rank has read it
+    return;
+  }
 
   __threadfence();
   __syncthreads();
@@ -533,8 +634,21 @@ tf_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParam
       return TF_ERR_CUDA;
     configured = true;
   }
-  if (launch_pdl(verify_umma_kernel<NPAD, GATHER>, grid, dim3(kThreads), Smem<NPAD>::kDynamic, stream, mk, mv, p) !=
-      cudaSuccess)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Smem<NPAD>::kDynamic;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = p.cmerge ? (unsigned)p.splits : 1u;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.cmerge ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, verify_umma_kernel<NPAD, GATHER>, mk, mv, p) != cudaSuccess)
     return TF_ERR_CUDA;
   return launch_status();
 }
@@ -650,7 +764,7 @@ extern "C" tf_status tf_sparse_verify_attn(const uint16_t* Q, const uint16_t* K,
   const size_t need = sparse_verify_ws(B * Hkv, (Hq / Hkv) * T, kc);
   if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
   CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, K, rows_total, kPiece) || !make_kv_map(&mv, V, rows_total, kPiece)) return TF_ERR_CUDA;
+  if (!make_piece_map(&mk, K, rows_total) || !make_piece_map(&mv, V, rows_total)) return TF_ERR_CUDA;
 
   VerifyParams p{};
   const int rows_all = (Hq / Hkv) * T;
@@ -670,6 +784,7 @@ extern "C" tf_status tf_sparse_verify_attn(const uint16_t* Q, const uint16_t* K,
   const int ug = B * Hkv * p.ngroups;
   p.splits = sparse_verify_splits(ug, tiles, num_sms());
   p.tiles_per = (tiles + p.splits - 1) / p.splits;
+  p.cmerge = (p.splits > 1 && p.splits <= kMaxClusterMerge) ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   char* w = static_cast<char*>(ws);
   p.status = reinterpret_cast<int*>(w);
