@@ -79,19 +79,20 @@ struct VerifyParams {
 template <int NPAD>
 struct Smem {
   static constexpr int kQBytes = 2 * NPAD * 128;     // two 64-column halves of [NPAD x 128] bf16
-  static constexpr int kPHalf = 2 * NPAD * 128;      // one bf16 copy of P [NPAD x 128 keys]
-  static constexpr int kPBuf = 2 * kPHalf;           // P split into hi + lo bf16 parts
-  static constexpr int kNumPBuf = NPAD <= 16 ? 2 : 1;  // double-buffer P when it fits
+  // P of tile t (hi and lo bf16 parts of [NPAD x 128 keys]) is written over the
+  // K half of the tile's own stage: K is dead once S = Q K^T has been computed,
+  // and the stage is handed back to the copy engine only after P V has read P.
+  static constexpr int kPHalf = 2 * NPAD * 128;
+  static_assert(2 * kPHalf <= kTile * kHeadDim * 2, "P fits over the K tile");
   static constexpr int kOffQ = kStages * kStageBytes;
-  static constexpr int kOffP = kOffQ + kQBytes;
-  static constexpr int kBytes = kOffP + kNumPBuf * kPBuf;
+  static constexpr int kBytes = kOffQ + kQBytes;
   static constexpr int kDynamic = kBytes + 1024;     // slack for 1024-byte alignment
   // Cluster merge: a split's (m, l) per row and its O rows [NPAD x 128] fp32
-  // reuse the Q and P buffers, which no copy engine writes and the MMAs have
-  // finished reading once the last O has been read back.
-  static constexpr int kOffCm = kOffQ;
-  static constexpr int kOffCo = kOffQ + 256;
-  static_assert(kOffCo + NPAD * kHeadDim * 4 <= kBytes, "cluster merge scratch");
+  // in stage 0, idle once the last O has been read back (every tile landed and
+  // was consumed).
+  static constexpr int kOffCm = 0;
+  static constexpr int kOffCo = 256;
+  static_assert(kOffCo + NPAD * kHeadDim * 4 <= kStageBytes, "cluster merge scratch");
 };
 
 __device__ __forceinline__ bool named_bar_or(bool pred) {
@@ -125,7 +126,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + S::kOffQ;
-  uint8_t* sP = smem + S::kOffP;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ug = blockIdx.y;
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           if (u >= 2 && !mbar_wait(&bar_o_free[u & 1], ((u - 2) >> 1) & 1)) { atomicExch(&s_abort, 1); break; }
           tc_fence_after();
           const uint32_t v_addr = smem_u32(smem + (u % kStages) * kStageBytes + kTile * kHeadDim * 2);
-          const uint32_t p_addr = smem_u32(sP + (u % S::kNumPBuf) * S::kPBuf);
+          const uint32_t p_addr = smem_u32(smem + (u % kStages) * kStageBytes);  // P over K of tile u
 #pragma unroll
           for (int kk = 0; kk < 16; ++kk) {
             // A = V^T (M = head dim, K = key), MN-major: 64-dim atoms 16 KB apart
@@ -396,30 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
 #pragma unroll
         for (int n = 0; n < NPAD; ++n) sc[n] = (sc[n] == -INFINITY) ? 0.0f : exp2f(sc[n] - m_run[n]);
       }
-      if (t >= 1) {
-        // O of the previous tile: after this, P V of tile t-1 has finished, so
-        // its P buffer may be overwritten (a single P buffer suffices).
-        const int u = t - 1;
-        const bool timed_out = !mbar_wait(&bar_o_full[u & 1], (u >> 1) & 1);
-        if (named_bar_or(timed_out)) {  // also orders alpha_s / rescaled_s of tile u
-          if (my == 0) atomicExch(&s_abort, 1);
-          break;
-        }
-        tc_fence_after();
-        float ov[NPAD];
-#pragma unroll
-        for (int c = 0; c < NPAD; c += 8) tmem_ld8(tmem + 64 + (u & 1) * 32 + lane_off + c, ov + c);
-        tmem_ld_wait();
-        const bool resc = rescaled_s[u & 1] != 0;
-#pragma unroll
-        for (int n = 0; n < NPAD; ++n) acc[n] = (resc ? acc[n] * alpha_s[u & 1][n] : acc[n]) + ov[n];
-        tc_fence_before();
-        mbar_arrive(&bar_o_free[u & 1]);
-      }
       if (t < ntiles) {
         // P for this tile as hi + lo bf16 parts (P V error ~2^-17 instead of
         // 2^-9 relative); row n, column = key.
-        uint8_t* pbuf = sP + (t % S::kNumPBuf) * S::kPBuf;
+        uint8_t* pbuf = smem + (t % kStages) * kStageBytes;  // over the K tile
         const uint32_t off_key = (uint32_t)(my >> 6) * (NPAD * 128);
 #pragma unroll
         for (int n = 0; n < NPAD; ++n) {
@@ -449,6 +429,26 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bar_p_full[t & 1]);
+      }
+      if (t >= 1) {
+        // O of the previous tile, folded in after P of this tile has been
+        // handed to the MMA warp (the two use different alpha / rescale slots)
+        const int u = t - 1;
+        const bool timed_out = !mbar_wait(&bar_o_full[u & 1], (u >> 1) & 1);
+        if (named_bar_or(timed_out)) {  // also orders alpha_s / rescaled_s of tile u
+          if (my == 0) atomicExch(&s_abort, 1);
+          break;
+        }
+        tc_fence_after();
+        float ov[NPAD];
+#pragma unroll
+        for (int c = 0; c < NPAD; c += 8) tmem_ld8(tmem + 64 + (u & 1) * 32 + lane_off + c, ov + c);
+        tmem_ld_wait();
+        const bool resc = rescaled_s[u & 1] != 0;
+#pragma unroll
+        for (int n = 0; n < NPAD; ++n) acc[n] = (resc ? acc[n] * alpha_s[u & 1][n] : acc[n]) + ov[n];
+        tc_fence_before();
+        mbar_arrive(&bar_o_free[u & 1]);
       }
     }
 
