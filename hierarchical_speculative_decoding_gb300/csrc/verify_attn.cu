@@ -56,7 +56,10 @@ constexpr int kMaxTilesPerCta = 16;  // gathered tiles per split (piece table si
 constexpr int kPieceBytes = kPiece * kHeadDim * 2;  // one piece of K (or V): 2 KB
 constexpr int kMaxClusterMerge = 8;  // most splits merged inside one (portable) cluster
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr uint32_t kTmemCols = 128;
+// TMEM columns: S of two tiles (32 each), then O of two tiles, 2 x NPAD each
+// (the P_hi V and P_lo V accumulators side by side).
+template <int NPAD>
+__host__ __device__ constexpr uint32_t tmem_cols() { return 64 + 4 * NPAD <= 128 ? 128u : 256u; }
 
 
 struct VerifyParams {
@@ -79,11 +82,12 @@ struct VerifyParams {
 template <int NPAD>
 struct Smem {
   static constexpr int kQBytes = 2 * NPAD * 128;     // two 64-column halves of [NPAD x 128] bf16
-  // P of tile t (hi and lo bf16 parts of [NPAD x 128 keys]) is written over the
-  // K half of the tile's own stage: K is dead once S = Q K^T has been computed,
-  // and the stage is handed back to the copy engine only after P V has read P.
-  static constexpr int kPHalf = 2 * NPAD * 128;
-  static_assert(2 * kPHalf <= kTile * kHeadDim * 2, "P fits over the K tile");
+  // P of tile t, [2 NPAD rows (hi parts, then lo parts) x 128 keys] bf16 in two
+  // 64-key halves, is written over the K half of the tile's own stage: K is
+  // dead once S = Q K^T has been computed, and the stage is handed back to the
+  // copy engine only after P V has read P.
+  static constexpr int kPKeyHalf = 2 * NPAD * 128;
+  static_assert(2 * kPKeyHalf <= kTile * kHeadDim * 2, "P fits over the K tile");
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kBytes = kOffQ + kQBytes;
   static constexpr int kDynamic = kBytes + 1024;     // slack for 1024-byte alignment
@@ -151,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_s, kTmemCols);
+    tmem_alloc(&tmem_base_s, tmem_cols<NPAD>());
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -208,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_base_s;  // columns: S0 [0,32) S1 [32,64) O0 [64,96) O1 [96,128)
+  const uint32_t tmem = tmem_base_s;  // columns: S0 [0,32) S1 [32,64) O0 [64,64+2N) O1 [64+2N,64+4N)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     // block barrier and the warp-wide TMEM release at the end
     if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(128, NPAD, false, false);
-      const uint32_t idO = idesc_bf16_f32(128, NPAD, true, false);
+      const uint32_t idO = idesc_bf16_f32(128, 2 * NPAD, true, false);
       const uint32_t q_addr = smem_u32(sQ);
       for (int t = 0; t <= ntiles; ++t) {
         if (t < ntiles) {
@@ -298,17 +302,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           const uint32_t v_addr = smem_u32(smem + (u % kStages) * kStageBytes + kTile * kHeadDim * 2);
           const uint32_t p_addr = smem_u32(smem + (u % kStages) * kStageBytes);  // P over K of tile u
 #pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
+          for (int k8 = 0; k8 < 8; ++k8) {
             // A = V^T (M = head dim, K = key), MN-major: 64-dim atoms 16 KB apart
             // and 8-key groups 1 KB apart (contiguous), or 1 KB and 2 KB apart
-            // (gathered).  B = P (N = query row, K = key), K-major;
-            // the hi part (kk < 8) and then the lo part (kk >= 8) of P.
-            const int k8 = kk & 7;
+            // (gathered).  B = P (N = 2 NPAD rows: the hi parts of the query rows,
+            // then their lo parts; K = key), K-major, so one pass over V gives
+            // P_hi V and P_lo V in two accumulators.
             const uint64_t a = GATHER ? smem_desc(v_addr + k8 * 2 * kPieceBytes, 1024, kPieceBytes)
                                       : smem_desc(v_addr + k8 * 2048, 16384, 1024);
-            const uint64_t bd = smem_desc(p_addr + (kk >> 3) * S::kPHalf + (k8 >> 2) * (NPAD * 128) + (k8 & 3) * 32,
-                                          16, 1024);
-            mma_bf16(tmem + 64 + (u & 1) * 32, a, bd, idO, kk > 0);
+            const uint64_t bd = smem_desc(p_addr + (k8 >> 2) * S::kPKeyHalf + (k8 & 3) * 32, 16, 1024);
+            mma_bf16(tmem + 64 + (u & 1) * 2 * NPAD, a, bd, idO, k8 > 0);
           }
           mma_commit(&bar_o_full[u & 1]);
           mma_commit(&bar_empty[u % kStages]);
@@ -400,16 +403,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         // P for this tile as hi + lo bf16 parts (P V error ~2^-17 instead of
         // 2^-9 relative); row n, column = key.
         uint8_t* pbuf = smem + (t % kStages) * kStageBytes;  // over the K tile
-        const uint32_t off_key = (uint32_t)(my >> 6) * (NPAD * 128);
+        const uint32_t off_key = (uint32_t)(my >> 6) * S::kPKeyHalf;
 #pragma unroll
         for (int n = 0; n < NPAD; ++n) {
           const float pv = sc[n];
           const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
           const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
           l_part[n] += pv;
-          const uint32_t o = off_key + sw128_offset(n, my & 63);
-          *reinterpret_cast<__nv_bfloat16*>(pbuf + o) = hi;
-          *reinterpret_cast<__nv_bfloat16*>(pbuf + S::kPHalf + o) = lo;
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + off_key + sw128_offset(n, my & 63)) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + off_key + sw128_offset(NPAD + n, my & 63)) = lo;
         }
         if (zero_v) {
           // Rows nobody may see can hold anything (even NaN): zero them in
@@ -440,13 +442,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           break;
         }
         tc_fence_after();
-        float ov[NPAD];
+        float ov[NPAD], ol[NPAD];
+        const uint32_t o_col = tmem + 64 + (u & 1) * 2 * NPAD + lane_off;
 #pragma unroll
-        for (int c = 0; c < NPAD; c += 8) tmem_ld8(tmem + 64 + (u & 1) * 32 + lane_off + c, ov + c);
+        for (int c = 0; c < NPAD; c += 8) {
+          tmem_ld8(o_col + c, ov + c);
+          tmem_ld8(o_col + NPAD + c, ol + c);
+        }
         tmem_ld_wait();
         const bool resc = rescaled_s[u & 1] != 0;
 #pragma unroll
-        for (int n = 0; n < NPAD; ++n) acc[n] = (resc ? acc[n] * alpha_s[u & 1][n] : acc[n]) + ov[n];
+        for (int n = 0; n < NPAD; ++n) acc[n] = (resc ? acc[n] * alpha_s[u & 1][n] : acc[n]) + (ov[n] + ol[n]);
         tc_fence_before();
         mbar_arrive(&bar_o_free[u & 1]);
       }
@@ -502,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   // ---- teardown (all warps)
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, tmem_cols<NPAD>());
   if (s_abort) {
     if (tid == 0) atomicExch(p.status, 1);
     // Let any TMA copy still in flight land before the CTA's shared memory goes away.
