@@ -56,10 +56,6 @@ constexpr int kMaxTilesPerCta = 16;  // gathered tiles per split (piece table si
 constexpr int kPieceBytes = kPiece * kHeadDim * 2;  // one piece of K (or V): 2 KB
 constexpr int kMaxClusterMerge = 8;  // most splits merged inside one (portable) cluster
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-// TMEM columns: S of two tiles (32 each), then O of two tiles, 2 x NPAD each
-// (the P_hi V and P_lo V accumulators side by side).
-template <int NPAD>
-__host__ __device__ constexpr uint32_t tmem_cols() { return 64 + 4 * NPAD <= 128 ? 128u : 256u; }
 
 
 struct VerifyParams {
@@ -79,25 +75,42 @@ struct VerifyParams {
   int cmerge;            // 1: the splits of a unit form a cluster and merge through DSMEM
 };
 
-template <int NPAD>
+// NR = query rows the softmax warps work on (the group's rows rounded up to 8):
+// 8, 16, 24 or 32.  The MMA shapes follow from it.
+template <int NR>
 struct Smem {
-  static constexpr int kQBytes = 2 * NPAD * 128;     // two 64-column halves of [NPAD x 128] bf16
-  // P of tile t, [2 NPAD rows (hi parts, then lo parts) x 128 keys] bf16 in two
-  // 64-key halves, is written over the K half of the tile's own stage: K is
-  // dead once S = Q K^T has been computed, and the stage is handed back to the
-  // copy engine only after P V has read P.
-  static constexpr int kPKeyHalf = 2 * NPAD * 128;
+  static constexpr int kNS = NR <= 16 ? 16 : 32;       // N of S = Q K^T (Q rows, zero-padded)
+  static constexpr int kQBytes = 2 * kNS * 128;       // two 64-column halves of [kNS x 128] bf16
+  // P of tile t is written over the K half of the tile's own stage: K is dead
+  // once S has been computed, and the stage is handed back to the copy engine
+  // only after P V has read P.  P holds hi and lo bf16 parts of every row, as
+  // the B operand of one MMA per 16 keys (N = kNPV): K-major rows [hi 0..NR-1,
+  // lo NR..2NR-1] in two 64-key halves for NR <= 16, else MN-major with one
+  // 128-byte swizzled row per key (hi parts in elements 0..31, lo parts in
+  // 32..63; 8-key groups 1 KB apart), written as 16-byte vectors.
+  static constexpr bool kPMnMajor = NR > 16;
+  static constexpr int kNPV = kPMnMajor ? 64 : 2 * NR;
+  static constexpr int kLoCol = kPMnMajor ? 32 : NR;   // first lo column of O (and of P)
+  static constexpr int kPKeyHalf = kNPV * 128;
   static_assert(2 * kPKeyHalf <= kTile * kHeadDim * 2, "P fits over the K tile");
+  // TMEM columns: S of two tiles (32 each), then O of two tiles (kNPV each).
+  static constexpr uint32_t kTmemCols = 64 + 2 * kNPV <= 128 ? 128u : 256u;
   static constexpr int kOffQ = kStages * kStageBytes;
   static constexpr int kBytes = kOffQ + kQBytes;
   static constexpr int kDynamic = kBytes + 1024;     // slack for 1024-byte alignment
-  // Cluster merge: a split's (m, l) per row and its O rows [NPAD x 128] fp32
+  // Cluster merge: a split's (m, l) per row and its O rows [NR x 128] fp32
   // in stage 0, idle once the last O has been read back (every tile landed and
   // was consumed).
   static constexpr int kOffCm = 0;
   static constexpr int kOffCo = 256;
-  static_assert(kOffCo + NPAD * kHeadDim * 4 <= kStageBytes, "cluster merge scratch");
+  static_assert(kOffCo + NR * kHeadDim * 4 <= kStageBytes, "cluster merge scratch");
 };
+
+__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
+  uint32_t u;
+  memcpy(&u, &v, sizeof(u));
+  return u;
+}
 
 __device__ __forceinline__ bool named_bar_or(bool pred) {
   uint32_t r;
@@ -112,17 +125,17 @@ __device__ __forceinline__ void named_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
 }
 
-template <int NPAD, bool GATHER>
+template <int NR, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_constant__ CUtensorMap mapK,
                                                                   const __grid_constant__ CUtensorMap mapV,
                                                                   VerifyParams p) {
-  using S = Smem<NPAD>;
+  using S = Smem<NR>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_o_full[2], bar_o_free[2];
   __shared__ uint32_t tmem_base_s;
-  __shared__ float red[4][NPAD];
-  __shared__ float alpha_s[2][NPAD];
+  __shared__ float red[4][NR];
+  __shared__ float alpha_s[2][NR];
   __shared__ int rescaled_s[2];
   __shared__ int s_last, s_abort;
   __shared__ int s_pstart[GATHER ? kPiecesPerTile * kMaxTilesPerCta : 1];  // first position, -1: none
@@ -155,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_s, tmem_cols<NPAD>());
+    tmem_alloc(&tmem_base_s, S::kTmemCols);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -197,14 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
       s_pcand[e] = cand;
     }
   }
-  // Q rows of this group -> shared memory, [NPAD x 128] bf16 in two swizzled halves.
+  // Q rows of this group -> shared memory, [kNS x 128] bf16 in two swizzled halves.
   {
     const uint16_t* Qg = p.Q + (((size_t)b * p.Hq + (size_t)g * G) * p.T + row0) * kHeadDim;
-    for (int e = tid; e < NPAD * 16; e += kThreads) {
+    for (int e = tid; e < S::kNS * 16; e += kThreads) {
       const int r = e >> 4, c8 = (e & 15) * 8;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (r < rows) v = *reinterpret_cast<const uint4*>(Qg + (size_t)r * kHeadDim + c8);
-      const uint32_t off = (c8 >> 6) * (NPAD * 128) + sw128_offset(r, c8 & 63);
+      const uint32_t off = (c8 >> 6) * (S::kNS * 128) + sw128_offset(r, c8 & 63);
       *reinterpret_cast<uint4*>(sQ + off) = v;
     }
   }
@@ -273,8 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     // lane 0 issues; the __syncwarp below keeps the warp together for the
     // block barrier and the warp-wide TMEM release at the end
     if (lane == 0) {
-      const uint32_t idS = idesc_bf16_f32(128, NPAD, false, false);
-      const uint32_t idO = idesc_bf16_f32(128, 2 * NPAD, true, false);
+      const uint32_t idS = idesc_bf16_f32(128, S::kNS, false, false);
+      const uint32_t idO = idesc_bf16_f32(128, S::kNPV, true, S::kPMnMajor);
       const uint32_t q_addr = smem_u32(sQ);
       for (int t = 0; t <= ntiles; ++t) {
         if (t < ntiles) {
@@ -289,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
             // gathered tiles hold them 1 KB apart with 8-key groups 2 KB apart
             const uint64_t a = GATHER ? smem_desc(k_addr + (kk >> 2) * 1024 + (kk & 3) * 32, 16, kPieceBytes)
                                       : smem_desc(k_addr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc(q_addr + (kk >> 2) * (NPAD * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc(q_addr + (kk >> 2) * (S::kNS * 128) + (kk & 3) * 32, 16, 1024);
             mma_bf16(tmem + (t & 1) * 32, a, bd, idS, kk > 0);
           }
           mma_commit(&bar_s_full[t & 1]);
@@ -305,13 +318,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           for (int k8 = 0; k8 < 8; ++k8) {
             // A = V^T (M = head dim, K = key), MN-major: 64-dim atoms 16 KB apart
             // and 8-key groups 1 KB apart (contiguous), or 1 KB and 2 KB apart
-            // (gathered).  B = P (N = 2 NPAD rows: the hi parts of the query rows,
-            // then their lo parts; K = key), K-major, so one pass over V gives
-            // P_hi V and P_lo V in two accumulators.
+            // (gathered).  B = P (N = the hi parts of the query rows, then their
+            // lo parts; K = key), so one pass over V gives P_hi V and P_lo V in
+            // two accumulators.
             const uint64_t a = GATHER ? smem_desc(v_addr + k8 * 2 * kPieceBytes, 1024, kPieceBytes)
                                       : smem_desc(v_addr + k8 * 2048, 16384, 1024);
-            const uint64_t bd = smem_desc(p_addr + (k8 >> 2) * S::kPKeyHalf + (k8 & 3) * 32, 16, 1024);
-            mma_bf16(tmem + 64 + (u & 1) * 2 * NPAD, a, bd, idO, k8 > 0);
+            const uint64_t bd = S::kPMnMajor
+                                    ? smem_desc(p_addr + k8 * 2048, 8192, 1024)
+                                    : smem_desc(p_addr + (k8 >> 2) * S::kPKeyHalf + (k8 & 3) * 32, 16, 1024);
+            mma_bf16(tmem + 64 + (u & 1) * S::kNPV, a, bd, idO, k8 > 0);
           }
           mma_commit(&bar_o_full[u & 1]);
           mma_commit(&bar_empty[u % kStages]);
@@ -324,10 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     const int q4 = warp & 3;               // TMEM lane quarter of this warp
     const int my = q4 * 32 + lane;         // key index in the tile / head dim of O
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    float m_run[NPAD], l_part[NPAD], acc[NPAD];
-    int lim[NPAD];
+    float m_run[NR], l_part[NR], acc[NR];
+    int lim[NR];
 #pragma unroll
-    for (int n = 0; n < NPAD; ++n) {
+    for (int n = 0; n < NR; ++n) {
       m_run[n] = -INFINITY;
       l_part[n] = 0.0f;
       acc[n] = 0.0f;
@@ -338,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     // makes all of them leave the loop together (named barriers stay matched).
     bool zero_v = false;  // this key row of the tile must be zeroed in V
     for (int t = 0; t <= ntiles; ++t) {
-      float sc[NPAD];  // scores, then softmax weights of tile t
+      float sc[NR];  // scores, then softmax weights of tile t
       if (t < ntiles) {
         const bool timed_out = !mbar_wait(&bar_s_full[t & 1], (t >> 1) & 1);
         if (named_bar_or(timed_out)) {
@@ -347,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < NPAD; c += 8) tmem_ld8(tmem + (t & 1) * 32 + lane_off + c, sc + c);
+        for (int c = 0; c < NR; c += 8) tmem_ld8(tmem + (t & 1) * 32 + lane_off + c, sc + c);
         tmem_ld_wait();
         // this key's position and whether it may be seen at all; candidate
         // rows (every row of the contiguous range) are also chain-limited
@@ -368,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         }
         bool need = false;
 #pragma unroll
-        for (int n = 0; n < NPAD; ++n) {
+        for (int n = 0; n < NR; ++n) {
           const bool valid = key_ok && (!chain || pos <= lim[n]);
           sc[n] = valid ? sc[n] * p.scale_log2 : -INFINITY;
           need |= sc[n] > m_run[n] + kRescaleThreshold;
@@ -377,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         if (need) {
           // tile max per row, then a new reference max for every row that grew
 #pragma unroll
-          for (int n = 0; n < NPAD; ++n) {
+          for (int n = 0; n < NR; ++n) {
             float v = sc[n];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -385,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           }
           named_bar_sync();
 #pragma unroll
-          for (int n = 0; n < NPAD; ++n) {
+          for (int n = 0; n < NR; ++n) {
             const float tmax = fmaxf(fmaxf(red[0][n], red[1][n]), fmaxf(red[2][n], red[3][n]));
             const float mn = fmaxf(m_run[n], tmax);
             const float a = merge_scale(m_run[n], mn);
@@ -397,21 +412,44 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         }
         if (my == 0) rescaled_s[t & 1] = need ? 1 : 0;
 #pragma unroll
-        for (int n = 0; n < NPAD; ++n) sc[n] = (sc[n] == -INFINITY) ? 0.0f : exp2f(sc[n] - m_run[n]);
+        for (int n = 0; n < NR; ++n) sc[n] = (sc[n] == -INFINITY) ? 0.0f : exp2f(sc[n] - m_run[n]);
       }
       if (t < ntiles) {
         // P for this tile as hi + lo bf16 parts (P V error ~2^-17 instead of
-        // 2^-9 relative); row n, column = key.
+        // 2^-9 relative).
         uint8_t* pbuf = smem + (t % kStages) * kStageBytes;  // over the K tile
-        const uint32_t off_key = (uint32_t)(my >> 6) * S::kPKeyHalf;
+        if constexpr (S::kPMnMajor) {
+          // key `my` owns one 128-byte row: 16-byte chunk c < 4 holds the hi
+          // parts of rows 8c..8c+7, chunk c + 4 their lo parts
+          uint8_t* prow = pbuf + (my >> 3) * 1024 + (my & 7) * 128;
 #pragma unroll
-        for (int n = 0; n < NPAD; ++n) {
-          const float pv = sc[n];
-          const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
-          l_part[n] += pv;
-          *reinterpret_cast<__nv_bfloat16*>(pbuf + off_key + sw128_offset(n, my & 63)) = hi;
-          *reinterpret_cast<__nv_bfloat16*>(pbuf + off_key + sw128_offset(NPAD + n, my & 63)) = lo;
+          for (int c = 0; c < NR / 8; ++c) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float a0 = sc[c * 8 + 2 * j], a1 = sc[c * 8 + 2 * j + 1];
+              l_part[c * 8 + 2 * j] += a0;
+              l_part[c * 8 + 2 * j + 1] += a1;
+              const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(a0 - __low2float(h), a1 - __high2float(h));
+              hw[j] = bf16x2_bits(h);
+              lw[j] = bf16x2_bits(lo);
+            }
+            *reinterpret_cast<uint4*>(prow + ((c ^ (my & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(prow + (((c + 4) ^ (my & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+        } else {
+          // K-major: row n (hi) and row NR + n (lo), column = key
+          const uint32_t off_key = (uint32_t)(my >> 6) * S::kPKeyHalf;
+#pragma unroll
+          for (int n = 0; n < NR; ++n) {
+            const float pv = sc[n];
+            const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
+            l_part[n] += pv;
+            *reinterpret_cast<__nv_bfloat16*>(pbuf + off_key + sw128_offset(n, my & 63)) = hi;
+            *reinterpret_cast<__nv_bfloat16*>(pbuf + off_key + sw128_offset(NR + n, my & 63)) = lo;
+          }
         }
         if (zero_v) {
           // Rows nobody may see can hold anything (even NaN): zero them in
@@ -442,17 +480,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           break;
         }
         tc_fence_after();
-        float ov[NPAD], ol[NPAD];
-        const uint32_t o_col = tmem + 64 + (u & 1) * 2 * NPAD + lane_off;
+        float ov[NR], ol[NR];
+        const uint32_t o_col = tmem + 64 + (u & 1) * S::kNPV + lane_off;
 #pragma unroll
-        for (int c = 0; c < NPAD; c += 8) {
+        for (int c = 0; c < NR; c += 8) {
           tmem_ld8(o_col + c, ov + c);
-          tmem_ld8(o_col + NPAD + c, ol + c);
+          tmem_ld8(o_col + S::kLoCol + c, ol + c);
         }
         tmem_ld_wait();
         const bool resc = rescaled_s[u & 1] != 0;
 #pragma unroll
-        for (int n = 0; n < NPAD; ++n) acc[n] = (resc ? acc[n] * alpha_s[u & 1][n] : acc[n]) + (ov[n] + ol[n]);
+        for (int n = 0; n < NR; ++n) acc[n] = (resc ? acc[n] * alpha_s[u & 1][n] : acc[n]) + (ov[n] + ol[n]);
         tc_fence_before();
         mbar_arrive(&bar_o_free[u & 1]);
       }
@@ -460,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
 
     // ---- row sums across the 128 key lanes
 #pragma unroll
-    for (int n = 0; n < NPAD; ++n) {
+    for (int n = 0; n < NR; ++n) {
       float v = l_part[n];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -470,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
     if (p.splits == 1) {
 #pragma unroll
-      for (int n = 0; n < NPAD; ++n) {
+      for (int n = 0; n < NR; ++n) {
         if (n < rows) {
           const float l = (red[0][n] + red[1][n]) + (red[2][n] + red[3][n]);
           p.out[(out_row0 + n) * kHeadDim + my] = (l > 0.0f) ? acc[n] / l : 0.0f;
@@ -480,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
       float* cm = reinterpret_cast<float*>(smem + S::kOffCm);
       float* co = reinterpret_cast<float*>(smem + S::kOffCo);
 #pragma unroll
-      for (int n = 0; n < NPAD; ++n) {
+      for (int n = 0; n < NR; ++n) {
         if (n < rows) {
           if (my == 0) {
             cm[n * 2 + 0] = m_run[n];
@@ -493,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
       float* ml = p.part_ml + ((size_t)ug * p.splits_cap + blockIdx.x) * kMaxRows * 2;
       float* po = p.part_o + ((size_t)ug * p.splits_cap + blockIdx.x) * kMaxRows * kHeadDim;
 #pragma unroll
-      for (int n = 0; n < NPAD; ++n) {
+      for (int n = 0; n < NR; ++n) {
         if (n < rows) {
           if (my == 0) {
             ml[n * 2 + 0] = m_run[n];
@@ -508,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   // ---- teardown (all warps)
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, tmem_cols<NPAD>());
+  if (warp == 1) tmem_dealloc(tmem, S::kTmemCols);
   if (s_abort) {
     if (tid == 0) atomicExch(p.status, 1);
     // Let any TMA copy still in flight land before the CTA's shared memory goes away.
@@ -525,8 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     cluster_sync();
     const int S = p.splits;
     const uint32_t rank = cluster_ctarank();
-    const float* cm = reinterpret_cast<const float*>(smem + Smem<NPAD>::kOffCm);
-    const float* co = reinterpret_cast<const float*>(smem + Smem<NPAD>::kOffCo);
+    const float* cm = reinterpret_cast<const float*>(smem + Smem<NR>::kOffCm);
+    const float* co = reinterpret_cast<const float*>(smem + Smem<NR>::kOffCo);
     for (int i = tid; i < S * rows; i += kThreads) {
       const int sp = i / rows, n = i % rows;
       s_w[i] = __uint_as_float(dsmem_ld_u32(cm + n * 2 + 0, sp));
@@ -630,20 +668,20 @@ size_t verify_ws(int units, int rows_all, int Lmax) {
          ug * cap * kMaxRows * kHeadDim * sizeof(float);
 }
 
-template <int NPAD, bool GATHER>
+template <int NR, bool GATHER>
 tf_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParams& p, dim3 grid,
                  cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(verify_umma_kernel<NPAD, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<NPAD>::kDynamic) != cudaSuccess)
+    if (cudaFuncSetAttribute(verify_umma_kernel<NR, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Smem<NR>::kDynamic) != cudaSuccess)
       return TF_ERR_CUDA;
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Smem<NPAD>::kDynamic;
+  cfg.dynamicSmemBytes = Smem<NR>::kDynamic;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -654,9 +692,21 @@ tf_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParam
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.cmerge ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, verify_umma_kernel<NPAD, GATHER>, mk, mv, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, verify_umma_kernel<NR, GATHER>, mk, mv, p) != cudaSuccess)
     return TF_ERR_CUDA;
   return launch_status();
+}
+
+// The softmax works on the group's query rows rounded up to 8.
+template <bool GATHER>
+tf_status launch_rows(int rows_max, const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParams& p, dim3 grid,
+                      cudaStream_t stream) {
+  switch ((rows_max + 7) >> 3) {
+    case 1: return launch<8, GATHER>(mk, mv, p, grid, stream);
+    case 2: return launch<16, GATHER>(mk, mv, p, grid, stream);
+    case 3: return launch<24, GATHER>(mk, mv, p, grid, stream);
+    default: return launch<32, GATHER>(mk, mv, p, grid, stream);
+  }
 }
 
 // Gathered mode: tiles of the longest possible piece list (kc chunks and at most
@@ -747,7 +797,7 @@ extern "C" tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const 
                                       align_up((size_t)ug * p.splits_cap * kMaxRows * 2 * sizeof(float), 256));
   dim3 grid(p.splits, ug);
   const int rows_max = rows_all < kMaxRows ? rows_all : kMaxRows;
-  return rows_max <= 16 ? launch<16, false>(mk, mv, p, grid, stream) : launch<32, false>(mk, mv, p, grid, stream);
+  return launch_rows<false>(rows_max, mk, mv, p, grid, stream);
 }
 
 extern "C" size_t tf_sparse_verify_attn_workspace(int B, int Hq, int Hkv, int kc, int T) {
@@ -800,5 +850,5 @@ extern "C" tf_status tf_sparse_verify_attn(const uint16_t* Q, const uint16_t* K,
                                       align_up((size_t)ug * p.splits_cap * kMaxRows * 2 * sizeof(float), 256));
   dim3 grid(p.splits, ug);
   const int rows_max = rows_all < kMaxRows ? rows_all : kMaxRows;
-  return rows_max <= 16 ? launch<16, true>(mk, mv, p, grid, stream) : launch<32, true>(mk, mv, p, grid, stream);
+  return launch_rows<true>(rows_max, mk, mv, p, grid, stream);
 }

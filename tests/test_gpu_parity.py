@@ -237,10 +237,11 @@ def test_verify_attn(cuda_lib, w):
         assert np.abs(out.cpu().double().numpy() - want).max() <= ATOL
 
 
-@pytest.mark.parametrize("G,T", [(1, 1), (1, 16), (2, 16), (8, 4), (4, 9)], ids=lambda v: str(v))
+@pytest.mark.parametrize("G,T", [(1, 1), (2, 3), (1, 16), (2, 5), (3, 7), (4, 6), (2, 16), (8, 4), (4, 9)],
+                         ids=lambda v: str(v))
 def test_verify_row_groups(cuda_lib, G, T):
-    """Query-row groups: N = G * T padded to 16 or 32, and more than 32 rows split
-    into several groups per KV head."""
+    """Query-row groups: the rows of a KV head rounded up to 8, 16, 24 or 32 (full
+    and partly filled), and more than 32 rows split into several groups."""
     w = small_workload(B=1, Hq=2 * G, Hkv=2, T=T, L=700, ragged=False)
     c = make_case(w)
     out = cuda_lib.tf_verify_attn(c["Q"], c["K"], c["V"], c["seq"], 0.09)
