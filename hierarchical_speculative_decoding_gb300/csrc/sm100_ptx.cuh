@@ -100,6 +100,11 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 }
 
 // Make generic-proxy shared-memory writes visible to the async proxy (TMA / tensor core).
+// Orders global memory this thread may read through the generic proxy (for
+// instance data other CTAs published before a ticket) before its later bulk
+// copies of that memory.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

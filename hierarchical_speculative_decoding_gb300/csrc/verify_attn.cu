@@ -75,6 +75,102 @@ struct VerifyParams {
   int cmerge;            // 1: the splits of a unit form a cluster and merge through DSMEM
 };
 
+// Final log-sum-exp merge of a unit's split partials by the CTA that finished
+// last, with its idle K/V ring as the staging area.  The splits' O rows (rows x
+// 128 fp32, contiguous per split) come in by bulk copies, as many splits per
+// batch as fit beside the weights, all in flight at once; meanwhile the
+// threads load every split's (m, l), and the weights e^{m_s - m} and row sums
+// L are formed; each thread then accumulates float4 columns of the output
+// from shared memory and writes them divided by L.
+__device__ void merge_staged(const float* __restrict__ ml, const float* __restrict__ o, int S, int rows,
+                             uint8_t* ring, uint64_t* bar, float* __restrict__ out, int* status) {
+  constexpr int kRing = kStages * kStageBytes;
+  constexpr int kAcc = (kMaxRows * kHeadDim / 4 + kThreads - 1) / kThreads;  // float4 outputs per thread
+  const int tid = threadIdx.x;
+  const int nw = S * rows;
+  const int wbytes = (int)(((size_t)(2 * nw + kMaxRows) * sizeof(float) + 1023) & ~size_t(1023));
+  float* m_w = reinterpret_cast<float*>(ring + kRing - wbytes);  // [S][rows]: m, then the weights
+  float* l_s = m_w + nw;                                          // [S][rows]
+  float* L_s = l_s + nw;                                          // [rows]
+  const uint32_t split_bytes = (uint32_t)rows * kHeadDim * sizeof(float);
+  const int per_batch = max(1, (kRing - wbytes) / (int)split_bytes);
+  auto issue = [&](int sp0) {
+    const int nb = min(per_batch, S - sp0);
+    mbar_arrive_expect_tx(bar, (uint32_t)nb * split_bytes);
+    for (int j = 0; j < nb; ++j)
+      bulk_load(ring + (size_t)j * split_bytes, o + (size_t)(sp0 + j) * kMaxRows * kHeadDim, split_bytes, bar);
+  };
+  if (tid == 0) {
+    fence_proxy_async_global();
+    issue(0);
+  }
+  for (int i = tid; i < nw; i += kThreads) {
+    const int sp = i / rows, n = i % rows;
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(ml) + (size_t)sp * kMaxRows + n);
+    m_w[i] = v.x;
+    l_s[i] = v.y;
+  }
+  __syncthreads();
+  for (int n = tid; n < rows; n += kThreads) {
+    float mx = -INFINITY;
+    for (int sp = 0; sp < S; ++sp) mx = fmaxf(mx, m_w[sp * rows + n]);
+    float Lsum = 0.0f;
+    for (int sp = 0; sp < S; ++sp) {
+      const float w = merge_scale(m_w[sp * rows + n], mx);
+      m_w[sp * rows + n] = w;
+      Lsum = fmaf(w, l_s[sp * rows + n], Lsum);
+    }
+    L_s[n] = Lsum;
+  }
+  __syncthreads();
+  float4 acc[kAcc];
+#pragma unroll
+  for (int k = 0; k < kAcc; ++k) acc[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  const int n4 = rows * (kHeadDim / 4);
+  bool ok = true;
+  for (int sp0 = 0, batch = 0; sp0 < S; sp0 += per_batch, ++batch) {
+    const int nb = min(per_batch, S - sp0);
+    if (!mbar_wait(bar, batch & 1)) {
+      ok = false;  // a bounded wait ran out: report, keep no result
+      if (tid == 0) atomicExch(status, 1);
+      break;
+    }
+    const float4* st = reinterpret_cast<const float4*>(ring);
+#pragma unroll
+    for (int k = 0; k < kAcc; ++k) {
+      const int e4 = tid + k * kThreads;
+      if (e4 < n4) {
+        const int n = e4 / (kHeadDim / 4);
+        for (int j = 0; j < nb; ++j) {
+          const float w = m_w[(sp0 + j) * rows + n];
+          const float4 v = st[(size_t)j * n4 + e4];
+          acc[k].x = fmaf(w, v.x, acc[k].x);
+          acc[k].y = fmaf(w, v.y, acc[k].y);
+          acc[k].z = fmaf(w, v.z, acc[k].z);
+          acc[k].w = fmaf(w, v.w, acc[k].w);
+        }
+      }
+    }
+    if (sp0 + nb < S) {
+      fence_proxy_async_smem();  // these reads of the staging area before the next copies into it
+      __syncthreads();
+      if (tid == 0) issue(sp0 + nb);
+    }
+  }
+  if (!ok) return;
+#pragma unroll
+  for (int k = 0; k < kAcc; ++k) {
+    const int e4 = tid + k * kThreads;
+    if (e4 < n4) {
+      const int n = e4 / (kHeadDim / 4);
+      const float Lr = L_s[n];
+      const float inv = Lr > 0.0f ? 1.0f / Lr : 0.0f;
+      reinterpret_cast<float4*>(out)[e4] =
+          make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
+    }
+  }
+}
+
 // NR = query rows the softmax warps work on (the group's rows rounded up to 8):
 // 8, 16, 24 or 32.  The MMA shapes follow from it.
 template <int NR>
@@ -133,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kStages], bar_empty[kStages];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_o_full[2], bar_o_free[2];
+  __shared__ __align__(8) uint64_t bar_merge;
   __shared__ uint32_t tmem_base_s;
   __shared__ float red[4][NR];
   __shared__ float alpha_s[2][NR];
@@ -164,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
       mbar_init(&bar_o_full[i], 1);
       mbar_init(&bar_o_free[i], kSoftmaxThreads);
     }
+    mbar_init(&bar_merge, 1);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -622,10 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   const float* ml0 = p.part_ml + (size_t)ug * p.splits_cap * kMaxRows * 2;
   const float* o0 = p.part_o + (size_t)ug * p.splits_cap * kMaxRows * kHeadDim;
   const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
-  float* out = p.out;
-  // The K/V ring is idle now: it serves as the merge scratch.
-  merge_splits(ml0, o0, p.splits, rows, kMaxRows, reinterpret_cast<float*>(smem),
-               [&](int n, int d, float v) { out[(out_row0 + n) * kHeadDim + d] = v; });
+  merge_staged(ml0, o0, p.splits, rows, smem, &bar_merge, p.out + out_row0 * kHeadDim, p.status);
   if (tid == 0) p.tickets[ug] = 0;
 }
 
