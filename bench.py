@@ -396,6 +396,20 @@ def run_gpu(args):
     kernels["sparse_verify_level1"] = {"ms": round(sv_ms, 5), "GBps": round(sv_bytes / (sv_ms / 1e3) / 1e9, 1),
                                        "frac_hbm": round(sv_bytes / (sv_ms / 1e3) / 1e9 / peak, 4),
                                        "calls": "tf_sparse_verify_attn", "timing": "back-to-back over the layers"}
+    # the retrieval draft alone, back to back over the layers: consecutive
+    # launches overlap through programmatic dependent launch (no events between
+    # them), and every layer's means and K/V are cold
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for l in range(layers):
+        draft(l)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dr_ms = d0.elapsed_time(d1) / layers
+    kernels["retrieval_draft"]["back_to_back"] = {
+        "ms": round(dr_ms, 5), "GBps": round(bytes_draft / (dr_ms / 1e3) / 1e9, 1),
+        "frac_hbm": round(bytes_draft / (dr_ms / 1e3) / 1e9 / peak, 4)}
     kernels["chunk_means_prefill_1layer"] = {"ms": round(means_ms, 4),
                                              "GBps": round(means_bytes / (means_ms / 1e3) / 1e9, 1)}
     ver_ms = statistics.mean(per_kind["verify"])
