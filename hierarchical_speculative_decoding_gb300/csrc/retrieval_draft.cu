@@ -499,27 +499,48 @@ tf_status launch_draft(const DraftParams& p, int units, int Cmax, cudaStream_t s
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(retrieval_draft_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)draft_smem(kMaxSliceKeys)) != cudaSuccess)
+                             (int)draft_smem(kMaxSliceKeys)) != cudaSuccess ||
+        cudaFuncSetAttribute(retrieval_draft_kernel<NQ>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess)
       return TF_ERR_CUDA;
     configured = true;
   }
-  // Cluster size: the largest S <= 8 (at most one CTA per 64 chunks) whose
-  // units x S CTAs fit one wave at the occupancy their slice size allows; at
-  // least enough CTAs that every slice fits on chip.
-  const int sms = num_sms();
+  // Cluster size: the largest S <= 16 (at most one CTA per 64 chunks) for
+  // which every unit's cluster is resident at once, as the occupancy query for
+  // that cluster shape and slice size reports; at least enough CTAs that every
+  // slice fits on chip.  With 32 units that is S = 9: 288 CTAs, two on each of
+  // 144 SMs, so every slice streams at the same rate (S = 8 leaves some CTAs
+  // alone on an SM and the others paired, and each cluster waits for its
+  // paired members).
   const int need = (Cmax + kMaxSliceKeys - 1) / kMaxSliceKeys;
   if (need > kMaxCluster) return TF_ERR_UNSUPPORTED;
   int most = (Cmax + 63) / 64;
   if (most > kMaxCluster) most = kMaxCluster;
-  int S = need < 1 ? 1 : need;
+  int S = 0;
   for (int cand_s = most; cand_s >= need && cand_s >= 1; --cand_s) {
     const int sl = (Cmax + cand_s - 1) / cand_s;
-    const int occ = occupancy_blocks((const void*)retrieval_draft_kernel<NQ>, kThreads, draft_smem(sl));
-    if ((long long)units * cand_s <= (long long)sms * occ) {
+    cudaLaunchConfig_t qc = {};
+    qc.gridDim = dim3(cand_s, units);
+    qc.blockDim = dim3(kThreads);
+    qc.dynamicSmemBytes = draft_smem(sl);
+    cudaLaunchAttribute qa[1];
+    qa[0].id = cudaLaunchAttributeClusterDimension;
+    qa[0].val.clusterDim.x = cand_s;
+    qa[0].val.clusterDim.y = 1;
+    qa[0].val.clusterDim.z = 1;
+    qc.attrs = qa;
+    qc.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, retrieval_draft_kernel<NQ>, &qc) != cudaSuccess) {
+      (void)cudaGetLastError();  // this shape is not available: try a smaller one
+      continue;
+    }
+    if (clusters >= units) {
       S = cand_s;
       break;
     }
   }
+  if (S == 0) S = need < 1 ? 1 : need;  // more units than one wave holds: smallest clusters
   const int slice = (Cmax + S - 1) / S;
 
   cudaLaunchConfig_t cfg = {};

@@ -144,9 +144,9 @@ extern "C" tf_status tf_chunk_scores_topk(const uint16_t* q, const uint16_t* M, 
   // least enough CTAs that every slice fits on chip.
   const int sms = num_sms();
   const int need = (Cmax + kMaxSliceKeys - 1) / kMaxSliceKeys;
-  if (need > kMaxCluster) return TF_ERR_UNSUPPORTED;  // context beyond 8 x 16384 chunks
+  if (need > topk::kMaxPortableCluster) return TF_ERR_UNSUPPORTED;  // context beyond 8 x 16384 chunks
   int most = (Cmax + 63) / 64;
-  if (most > kMaxCluster) most = kMaxCluster;
+  if (most > topk::kMaxPortableCluster) most = topk::kMaxPortableCluster;
   int S = need;
   for (int cand_s = most; cand_s >= need; --cand_s) {
     const int sl = (Cmax + cand_s - 1) / cand_s;

@@ -31,7 +31,8 @@ using namespace sm100;
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 6;
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 16;         // cluster sizes above 8 need the non-portable opt-in
+constexpr int kMaxPortableCluster = 8;
 constexpr int kMaxSliceKeys = 16384;  // keys per CTA held in shared memory (64 KB)
 
 // Shared-memory arrays of the selection.  hist*, tot 16-byte aligned.
@@ -118,16 +119,19 @@ __device__ __forceinline__ void find_bin(const uint32_t* h, int nb, int krem, in
 // of 4, arrays 16-byte aligned): 16-byte remote loads, all ranks in flight.
 __device__ __forceinline__ void cluster_sum(const uint32_t* local, uint32_t* tot, int nb, int S) {
   for (int i = 4 * threadIdx.x; i < nb; i += 4 * kThreads) {
-    uint4 v[kMaxCluster];
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) v[r] = r < S ? dsmem_ld_v4(local + i, (uint32_t)r) : make_uint4(0, 0, 0, 0);
     uint4 t = make_uint4(0, 0, 0, 0);
+    for (int r0 = 0; r0 < S; r0 += 8) {  // eight ranks in flight at a time
+      uint4 v[8];
 #pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) {
-      t.x += v[r].x;
-      t.y += v[r].y;
-      t.z += v[r].z;
-      t.w += v[r].w;
+      for (int r = 0; r < 8; ++r)
+        v[r] = r0 + r < S ? dsmem_ld_v4(local + i, (uint32_t)(r0 + r)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        t.x += v[r].x;
+        t.y += v[r].y;
+        t.z += v[r].z;
+        t.w += v[r].w;
+      }
     }
     *reinterpret_cast<uint4*>(tot + i) = t;
   }

@@ -59,7 +59,8 @@ def check_against_oracle(cuda_lib, w, c, M_bits, kc=None, scale=None):
     small_workload(B=1, Hq=8, Hkv=8, L=32768, budget=4096, ragged=False, planted_frac=0.01),
     small_workload(B=2, Hq=8, Hkv=4, L=20000, budget=8 * 2048, L_min=17000),
     small_workload(B=3, Hq=6, Hkv=2, L=5000, budget=8 * 37, L_min=9),
-], ids=["tiny", "ragged-gqa", "budget-covers-all", "mha-32k", "kc-2048", "g3-odd-budget"])
+    small_workload(B=1, Hq=2, Hkv=2, L=32768, budget=4096, ragged=False, planted_frac=0.01),
+], ids=["tiny", "ragged-gqa", "budget-covers-all", "mha-32k", "kc-2048", "g3-odd-budget", "two-units-16-ctas"])
 def test_retrieval_draft_parity(cuda_lib, w):
     c = make_case(w, fill_invalid=float("nan"))
     M_bits = O.build_chunk_means(bits(c["K_cpu"]), c["seq_cpu"].numpy(), w.chunk)
