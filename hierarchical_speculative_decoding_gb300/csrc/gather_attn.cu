@@ -35,6 +35,7 @@ constexpr int kComputeWarps = 4;
 constexpr int kSlots = 16;
 constexpr int kSlotBytes = 4096;  // K rows [0, 2 KB), V rows [2 KB, 4 KB)
 constexpr int kGatherSmem = kSlots * kSlotBytes + 128;  // + alignment slack
+constexpr int kMaxClusterSplits = 8;  // splits merged inside one (portable) cluster
 // Chunk k sits in slot k % 16 and is consumed by compute warp k % 4: every use
 // of a slot is consumed by the same warp, so a phase-parity wait never runs two
 // phases ahead of its barrier.
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_attn_kernel(GatherPa
   __shared__ float sm_m[kComputeWarps][NQ], sm_l[kComputeWarps][NQ];
   __shared__ float sm_o[kComputeWarps][NQ][kHeadDim];
   __shared__ int s_last, s_abort, s_issued;
+  __shared__ float c_m[NQ], c_l[NQ], c_o[NQ][kHeadDim];  // this split's state (cluster merge)
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
   const int unit_grp = blockIdx.y;
@@ -291,6 +293,12 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_attn_kernel(GatherPa
     if (p.splits == 1) {
       p.out[((size_t)b * p.Hq + (size_t)g * G + grp * NQ + h) * kHeadDim + d] =
           (ls > 0.0f) ? os / ls : (bad ? NAN : 0.0f);
+    } else if (p.cmerge) {
+      if (d == 0) {
+        c_m[h] = mx;
+        c_l[h] = ls;
+      }
+      c_o[h][d] = os;
     } else {
       if (d == 0) {
         part_ml[h * 2 + 0] = mx;
@@ -300,6 +308,40 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_attn_kernel(GatherPa
     }
   }
   if (p.splits == 1) return;
+
+  if (p.cmerge) {
+    // The splits of this (unit, group) are one cluster: after a cluster
+    // barrier each rank merges its share of the outputs from every rank's
+    // state through DSMEM (log-sum-exp identity); a second barrier keeps the
+    // states alive until every rank has read them.
+    cluster_sync();
+    const int S = p.splits;
+    const uint32_t rank = cluster_ctarank();
+    bool bad_any = false;
+    for (int rr = 0; rr < S; ++rr) bad_any |= dsmem_ld_u32(&s_abort, (uint32_t)rr) != 0;
+    float* outp = p.out + ((size_t)b * p.Hq + (size_t)g * G + grp * NQ) * kHeadDim;
+    for (int e = (int)rank * kGatherThreads + threadIdx.x; e < rows * kHeadDim; e += S * kGatherThreads) {
+      const int h = e / kHeadDim, d = e % kHeadDim;
+      float mr[8];
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) mr[rr] = rr < S ? __uint_as_float(dsmem_ld_u32(&c_m[h], (uint32_t)rr)) : -INFINITY;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) mx = fmaxf(mx, mr[rr]);
+      float ls = 0.0f, os = 0.0f;
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) {
+        if (rr < S) {
+          const float f = merge_scale(mr[rr], mx);
+          ls = fmaf(f, __uint_as_float(dsmem_ld_u32(&c_l[h], (uint32_t)rr)), ls);
+          os = fmaf(f, __uint_as_float(dsmem_ld_u32(&c_o[h][d], (uint32_t)rr)), os);
+        }
+      }
+      outp[h * kHeadDim + d] = bad_any ? NAN : (ls > 0.0f ? os / ls : 0.0f);
+    }
+    cluster_sync();
+    return;
+  }
 
   __threadfence();
   __syncthreads();
@@ -359,10 +401,27 @@ template <int NQ, int MODE>
 static tf_status launch(GatherParams p, int ug, cudaStream_t s) {
   const int per_sm = configure<NQ, MODE>();
   if (per_sm == 0) return TF_ERR_CUDA;
-  p.splits = wave_splits(ug, num_sms() * per_sm, p.splits_cap);
-  dim3 grid(p.splits, ug);
-  if (launch_pdl(gather_attn_kernel<NQ, MODE>, grid, dim3(kGatherThreads), kGatherSmem, s, p) != cudaSuccess)
-    return TF_ERR_CUDA;
+  // The window's few chunks per unit: at most 8 splits, merged inside one
+  // cluster; longer chunk lists keep more splits and the ticketed merge.
+  const int cap = MODE == kModeWindow ? (p.splits_cap < kMaxClusterSplits ? p.splits_cap : kMaxClusterSplits)
+                                      : p.splits_cap;
+  p.splits = wave_splits(ug, num_sms() * per_sm, cap);
+  p.cmerge = (p.splits > 1 && p.splits <= kMaxClusterSplits) ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.splits, ug);
+  cfg.blockDim = dim3(kGatherThreads);
+  cfg.dynamicSmemBytes = kGatherSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = p.cmerge ? (unsigned)p.splits : 1u;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.cmerge ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, gather_attn_kernel<NQ, MODE>, p) != cudaSuccess) return TF_ERR_CUDA;
   return launch_status();
 }
 

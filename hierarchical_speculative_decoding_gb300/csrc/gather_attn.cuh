@@ -26,6 +26,7 @@ struct GatherParams {
   int* tickets;      // [units * ngroups]
   float* part_ml;    // [units * ngroups, splits_cap, NQ, 2]
   float* part_o;     // [units * ngroups, splits_cap, NQ, D]
+  int cmerge;        // 1: the splits of a (unit, group) form a cluster and merge through DSMEM
 };
 
 int gather_nq(int rows);  // query rows per CTA for `rows` rows per unit
