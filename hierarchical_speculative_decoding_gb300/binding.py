@@ -40,6 +40,8 @@ _SIGS = {
     "tf_sparse_verify_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_verify_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
     "tf_verify_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
+    "tf_verify_attn_offload_workspace": (_S, [_I, _I, _I, _I, _I, _I]),
+    "tf_verify_attn_offload": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _S, _P, _P]),
     "tf_spec_accept_workspace": (_S, [_I, _I]),
     "tf_spec_accept": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _S, _P]),
 }
@@ -296,6 +298,36 @@ def tf_verify_attn(Q, K, V, seq_lens, scale, out=None, ws=None, stream=None):
     ws, nbytes = _ws(ws, tf_verify_attn_workspace(B, Hq, Hkv, Lmax, T), Q.device)
     _check(load().tf_verify_attn(_ptr(Q), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax, D, T, float(scale),
                                  _ptr(out), _ptr(ws), nbytes, _stream(stream)), "tf_verify_attn")
+    return out
+
+
+def tf_verify_attn_offload_workspace(B, Hq, Hkv, Lmax, T, seg_rows):
+    return int(load().tf_verify_attn_offload_workspace(B, Hq, Hkv, Lmax, T, seg_rows))
+
+
+def tf_verify_attn_offload(Q, K_host, V_host, seq_lens, L_stream, scale, out=None, ws=None, seg_rows=16384,
+                           stream=None, copy_stream=None):
+    """tf_verify_attn with K and V [B, Hkv, Lmax, D] in host memory (pin it for
+    asynchronous full-rate copies): positions [0, L_stream) stream through two
+    device staging slots on copy_stream while the segments are attended."""
+    _need(Q, torch.bfloat16, "Q", 4)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    for name, t in (("K_host", K_host), ("V_host", V_host)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.dim() != 4:
+            raise TypeError(f"{name} must be a 4-dim bfloat16 torch.Tensor")
+        if t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous host tensor")
+    B, Hq, T, D = Q.shape
+    _, Hkv, Lmax, _ = K_host.shape
+    if out is None:
+        out = torch.empty((B, Hq, T, D), dtype=torch.float32, device=Q.device)
+    _need(out, torch.float32, "out", 4)
+    ws, nbytes = _ws(ws, tf_verify_attn_offload_workspace(B, Hq, Hkv, Lmax, T, seg_rows), Q.device)
+    cs = _stream(stream)
+    xs = cs if copy_stream is None else _stream(copy_stream)
+    _check(load().tf_verify_attn_offload(_ptr(Q), _c.c_void_p(K_host.data_ptr()), _c.c_void_p(V_host.data_ptr()),
+                                         _ptr(seq_lens), int(L_stream), B, Hq, Hkv, Lmax, D, T, float(scale), _ptr(out),
+                                         int(seg_rows), _ptr(ws), nbytes, cs, xs), "tf_verify_attn_offload")
     return out
 
 

@@ -54,7 +54,8 @@ constexpr int kPiece = 8;           // rows per gathered piece (one chunk, one s
 constexpr int kPiecesPerTile = kTile / kPiece;
 constexpr int kMaxTilesPerCta = 16;  // gathered tiles per split (piece table size)
 constexpr int kPieceBytes = kPiece * kHeadDim * 2;  // one piece of K (or V): 2 KB
-constexpr int kMaxClusterMerge = 8;  // most splits merged inside one (portable) cluster
+constexpr int kMaxClusterMerge = 8;
+constexpr int kPartStride = 4 + kHeadDim;  // one row's partial state: m, l, 2 unused, O[128]  // most splits merged inside one (portable) cluster
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 
@@ -73,6 +74,11 @@ struct VerifyParams {
   const int32_t* n_sel;  // [B * Hkv]
   int kc, tiles_per;     // tiles per split
   int cmerge;            // 1: the splits of a unit form a cluster and merge through DSMEM
+  // segment mode (contiguous only): the K/V buffers hold positions [pos0,
+  // pos0 + Lmax) of caches Ltot long; with part_out set, every row's state
+  // (m, l, unnormalised O; kPartStride floats) is written instead of O
+  int pos0, Ltot;
+  float* part_out;
 };
 
 // Final log-sum-exp merge of a unit's split partials by the CTA that finished
@@ -83,15 +89,17 @@ struct VerifyParams {
 // L are formed; each thread then accumulates float4 columns of the output
 // from shared memory and writes them divided by L.
 __device__ void merge_staged(const float* __restrict__ ml, const float* __restrict__ o, int S, int rows,
-                             uint8_t* ring, uint64_t* bar, float* __restrict__ out, int* status) {
+                             uint8_t* ring, uint64_t* bar, float* __restrict__ out, float* __restrict__ part,
+                             int* status) {
   constexpr int kRing = kStages * kStageBytes;
   constexpr int kAcc = (kMaxRows * kHeadDim / 4 + kThreads - 1) / kThreads;  // float4 outputs per thread
   const int tid = threadIdx.x;
   const int nw = S * rows;
-  const int wbytes = (int)(((size_t)(2 * nw + kMaxRows) * sizeof(float) + 1023) & ~size_t(1023));
+  const int wbytes = (int)(((size_t)(2 * nw + 2 * kMaxRows) * sizeof(float) + 1023) & ~size_t(1023));
   float* m_w = reinterpret_cast<float*>(ring + kRing - wbytes);  // [S][rows]: m, then the weights
   float* l_s = m_w + nw;                                          // [S][rows]
-  float* L_s = l_s + nw;                                          // [rows]
+  float* L_s = l_s + nw;                                          // [rows]: row sums
+  float* M_s = L_s + kMaxRows;                                    // [rows]: max m
   const uint32_t split_bytes = (uint32_t)rows * kHeadDim * sizeof(float);
   const int per_batch = max(1, (kRing - wbytes) / (int)split_bytes);
   auto issue = [&](int sp0) {
@@ -121,6 +129,7 @@ __device__ void merge_staged(const float* __restrict__ ml, const float* __restri
       Lsum = fmaf(w, l_s[sp * rows + n], Lsum);
     }
     L_s[n] = Lsum;
+    M_s[n] = mx;
   }
   __syncthreads();
   float4 acc[kAcc];
@@ -158,6 +167,22 @@ __device__ void merge_staged(const float* __restrict__ ml, const float* __restri
     }
   }
   if (!ok) return;
+  if (part) {
+    // the unit's state over this segment: max m, row sum L, O relative to m
+    for (int n = tid; n < rows; n += kThreads) {
+      part[(size_t)n * kPartStride + 0] = M_s[n];
+      part[(size_t)n * kPartStride + 1] = L_s[n];
+    }
+#pragma unroll
+    for (int k = 0; k < kAcc; ++k) {
+      const int e4 = tid + k * kThreads;
+      if (e4 < n4) {
+        const int n = e4 / (kHeadDim / 4), d4 = e4 % (kHeadDim / 4);
+        reinterpret_cast<float4*>(part + (size_t)n * kPartStride + 4)[d4] = acc[k];
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int k = 0; k < kAcc; ++k) {
     const int e4 = tid + k * kThreads;
@@ -274,17 +299,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     prefetch_tensormap(&mapV);
   }
   pdl_wait();  // everything above is on-chip set-up that may overlap the previous kernel
-  const int L = clamp_len(p.seq_lens[b], p.Lmax);
+  const int L = clamp_len(p.seq_lens[b], p.Ltot);
 
   // key range of this split: whole tiles (contiguous), or tiles of the piece
   // list (gathered: selected chunks, then the candidate rows)
   int k0 = 0, k1 = 0, ntiles = 0;
   const int cstart = max(0, L - p.T);  // first candidate position
   if (!GATHER) {
-    const int tiles_all = (L + kTile - 1) / kTile;
+    // rows of the buffer (positions pos0 + row) that the sequence holds
+    const int nloc = min(max(L - p.pos0, 0), p.Lmax);
+    const int tiles_all = (nloc + kTile - 1) / kTile;
     const int tiles_per = (tiles_all + p.splits - 1) / p.splits;
     k0 = blockIdx.x * tiles_per * kTile;
-    k1 = min(L, k0 + tiles_per * kTile);
+    k1 = min(nloc, k0 + tiles_per * kTile);
     ntiles = k1 > k0 ? (k1 - k0 + kTile - 1) / kTile : 0;
   } else {
     const int C = (L + kChunk - 1) / kChunk;
@@ -467,8 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         int pos;
         bool key_ok, chain;
         if (!GATHER) {
-          pos = k0 + t * kTile + my;
-          key_ok = pos < k1;
+          const int row = k0 + t * kTile + my;
+          key_ok = row < k1;
+          pos = p.pos0 + row;  // position in the sequence
           chain = true;
           zero_v = t == ntiles - 1 && !key_ok;  // rows past the range in the last tile
         } else {
@@ -604,7 +632,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     }
     named_bar_sync();
     const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
-    if (p.splits == 1) {
+    if (p.splits == 1 && p.part_out) {
+#pragma unroll
+      for (int n = 0; n < NR; ++n) {
+        if (n < rows) {
+          float* pr = p.part_out + (out_row0 + n) * kPartStride;
+          if (my == 0) {
+            pr[0] = m_run[n];
+            pr[1] = (red[0][n] + red[1][n]) + (red[2][n] + red[3][n]);
+          }
+          pr[4 + my] = acc[n];
+        }
+      }
+    } else if (p.splits == 1) {
 #pragma unroll
       for (int n = 0; n < NR; ++n) {
         if (n < rows) {
@@ -720,7 +760,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   const float* ml0 = p.part_ml + (size_t)ug * p.splits_cap * kMaxRows * 2;
   const float* o0 = p.part_o + (size_t)ug * p.splits_cap * kMaxRows * kHeadDim;
   const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
-  merge_staged(ml0, o0, p.splits, rows, smem, &bar_merge, p.out + out_row0 * kHeadDim, p.status);
+  merge_staged(ml0, o0, p.splits, rows, smem, &bar_merge, p.out + out_row0 * kHeadDim,
+               p.part_out ? p.part_out + out_row0 * kPartStride : nullptr, p.status);
   if (tid == 0) p.tickets[ug] = 0;
 }
 
@@ -854,22 +895,18 @@ extern "C" size_t tf_verify_attn_workspace(int B, int Hq, int Hkv, int Lmax, int
   return tf::verify_ws(B * Hkv, (Hq / Hkv) * T, Lmax);
 }
 
-extern "C" tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
-                                    const int32_t* seq_lens, int B, int Hq, int Hkv, int Lmax, int D, int T,
-                                    float scale, float* out, void* ws, size_t ws_bytes, tf_stream_t stream) {
-  using namespace tf;
-  if (!Q || !K || !V || !seq_lens || !out) return TF_ERR_INVALID_ARG;
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || Hq % Hkv || T < 1) return TF_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return TF_ERR_INVALID_ARG;
-  if (D != kHeadDim || T > 16) return TF_ERR_UNSUPPORTED;
-  if (B == 0 || Lmax == 0) return TF_OK;
+namespace tf {
+namespace {
+
+// The contiguous verify over K/V buffers holding positions [pos0, pos0 + Lmax)
+// of caches Ltot long (the whole cache: pos0 = 0, Ltot = Lmax), writing O, or
+// each row's partial state to part_out when it is set.  Arguments validated.
+tf_status verify_contig(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* seq_lens, int B,
+                        int Hq, int Hkv, int Lmax, int T, float scale, float* out, void* ws, cudaStream_t stream,
+                        int pos0, int Ltot, float* part_out) {
   const long long rows_total = (long long)B * Hkv * Lmax;
-  if (rows_total >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
-  const size_t need = verify_ws(B * Hkv, (Hq / Hkv) * T, Lmax);
-  if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
   CUtensorMap mk, mv;
   if (!make_kv_map(&mk, K, rows_total, kTile) || !make_kv_map(&mv, V, rows_total, kTile)) return TF_ERR_CUDA;
-
   VerifyParams p{};
   const int rows_all = (Hq / Hkv) * T;
   p.Q = Q;
@@ -878,6 +915,9 @@ extern "C" tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const 
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.Lmax = Lmax;
+  p.Ltot = Ltot;
+  p.pos0 = pos0;
+  p.part_out = part_out;
   p.T = T;
   p.ngroups = (rows_all + kMaxRows - 1) / kMaxRows;
   p.splits_cap = verify_splits_cap(Lmax);
@@ -893,6 +933,144 @@ extern "C" tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const 
   dim3 grid(p.splits, ug);
   const int rows_max = rows_all < kMaxRows ? rows_all : kMaxRows;
   return launch_rows<false>(rows_max, mk, mv, p, grid, stream);
+}
+
+// Log-sum-exp merge of per-segment row states: part [nseg][rows][kPartStride]
+// -> out [rows][128].  One warp per row, 4 head dims per lane.
+__global__ void __launch_bounds__(256) merge_segments_kernel(const float* __restrict__ part, int nseg, int rows,
+                                                             float* __restrict__ out) {
+  pdl_wait();
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const size_t seg_stride = (size_t)rows * kPartStride;
+  const float* pr = part + (size_t)row * kPartStride;
+  float mx = -INFINITY;
+  for (int sg = 0; sg < nseg; ++sg) mx = fmaxf(mx, __ldg(pr + sg * seg_stride));
+  float L = 0.0f;
+  float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int sg = 0; sg < nseg; ++sg) {
+    const float* ps = pr + sg * seg_stride;
+    const float w = merge_scale(__ldg(ps), mx);
+    L = fmaf(w, __ldg(ps + 1), L);
+    const float4 v = __ldg(reinterpret_cast<const float4*>(ps + 4) + lane);
+    o.x = fmaf(w, v.x, o.x);
+    o.y = fmaf(w, v.y, o.y);
+    o.z = fmaf(w, v.z, o.z);
+    o.w = fmaf(w, v.w, o.w);
+  }
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  reinterpret_cast<float4*>(out + (size_t)row * kHeadDim)[lane] = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+}
+
+// Workspace of the offloaded verify: [status + split scratch of one segment
+// launch][partial states of every segment][two staging slots of K and V].
+struct OffloadLayout {
+  size_t verify, parts, slot, total;
+  int nseg_max;
+};
+
+OffloadLayout offload_layout(int B, int Hq, int Hkv, int Lmax, int T, int seg_rows) {
+  OffloadLayout o;
+  const int units = B * Hkv;
+  o.nseg_max = (Lmax + seg_rows - 1) / seg_rows;
+  o.verify = align_up(verify_ws(units, (Hq / Hkv) * T, seg_rows), 1024);
+  o.parts = align_up((size_t)o.nseg_max * B * Hq * T * kPartStride * sizeof(float), 1024);
+  o.slot = align_up((size_t)units * seg_rows * kHeadDim * 2, 1024);  // one tensor's rows of one segment
+  o.total = o.verify + o.parts + 4 * o.slot;
+  return o;
+}
+
+}  // namespace
+}  // namespace tf
+
+extern "C" tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                                    const int32_t* seq_lens, int B, int Hq, int Hkv, int Lmax, int D, int T,
+                                    float scale, float* out, void* ws, size_t ws_bytes, tf_stream_t stream) {
+  using namespace tf;
+  if (!Q || !K || !V || !seq_lens || !out) return TF_ERR_INVALID_ARG;
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || Hq % Hkv || T < 1) return TF_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return TF_ERR_INVALID_ARG;
+  if (D != kHeadDim || T > 16) return TF_ERR_UNSUPPORTED;
+  if (B == 0 || Lmax == 0) return TF_OK;
+  const long long rows_total = (long long)B * Hkv * Lmax;
+  if (rows_total >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
+  const size_t need = verify_ws(B * Hkv, (Hq / Hkv) * T, Lmax);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
+  return verify_contig(Q, K, V, seq_lens, B, Hq, Hkv, Lmax, T, scale, out, ws, stream, 0, Lmax, nullptr);
+}
+
+extern "C" size_t tf_verify_attn_offload_workspace(int B, int Hq, int Hkv, int Lmax, int T, int seg_rows) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lmax <= 0 || T <= 0 || Hq % Hkv || seg_rows <= 0) return 0;
+  return tf::offload_layout(B, Hq, Hkv, Lmax, T, seg_rows).total;
+}
+
+extern "C" tf_status tf_verify_attn_offload(const uint16_t* Q, const uint16_t* K_host, const uint16_t* V_host,
+                                            const int32_t* seq_lens, int L_stream, int B, int Hq, int Hkv, int Lmax,
+                                            int D, int T, float scale, float* out, int seg_rows, void* ws,
+                                            size_t ws_bytes, tf_stream_t stream, tf_stream_t copy_stream) {
+  using namespace tf;
+  if (!Q || !K_host || !V_host || !seq_lens || !out) return TF_ERR_INVALID_ARG;
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || Hq % Hkv || T < 1 || seg_rows <= 0) return TF_ERR_INVALID_ARG;
+  if (L_stream < 0 || L_stream > Lmax) return TF_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(out)) return TF_ERR_INVALID_ARG;
+  if (D != kHeadDim || T > 16) return TF_ERR_UNSUPPORTED;
+  if (B == 0 || Lmax == 0) return TF_OK;
+  if ((long long)B * Hkv * seg_rows >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
+  const OffloadLayout lay = offload_layout(B, Hq, Hkv, Lmax, T, seg_rows);
+  if (!ws || ws_bytes < lay.total || !aligned16(ws)) return TF_ERR_WORKSPACE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream), xs = static_cast<cudaStream_t>(copy_stream);
+  char* w = static_cast<char*>(ws);
+  float* parts = reinterpret_cast<float*>(w + lay.verify);
+  uint16_t* stage[2][2];  // [slot][K, V]
+  for (int sl = 0; sl < 2; ++sl)
+    for (int kv = 0; kv < 2; ++kv)
+      stage[sl][kv] = reinterpret_cast<uint16_t*>(w + lay.verify + lay.parts + (size_t)(2 * sl + kv) * lay.slot);
+  const int units = B * Hkv;
+  const int rows = B * Hq * T;
+  const int nseg = L_stream > 0 ? (L_stream + seg_rows - 1) / seg_rows : 1;
+  const size_t row_bytes = (size_t)kHeadDim * 2;
+
+  cudaEvent_t start, copied[2], computed[2];
+  if (cudaEventCreateWithFlags(&start, cudaEventDisableTiming) != cudaSuccess) return TF_ERR_CUDA;
+  for (int sl = 0; sl < 2; ++sl) {
+    cudaEventCreateWithFlags(&copied[sl], cudaEventDisableTiming);
+    cudaEventCreateWithFlags(&computed[sl], cudaEventDisableTiming);
+  }
+  tf_status st = TF_OK;
+  // the staging slots may still be read by earlier work on the compute stream
+  if (cudaEventRecord(start, cs) != cudaSuccess || cudaStreamWaitEvent(xs, start, 0) != cudaSuccess) st = TF_ERR_CUDA;
+  for (int sg = 0; sg < nseg && st == TF_OK; ++sg) {
+    const int sl = sg & 1;
+    const int pos0 = sg * seg_rows;
+    const int n = L_stream > 0 ? (L_stream - pos0 < seg_rows ? L_stream - pos0 : seg_rows) : 0;
+    if (sg >= 2 && cudaStreamWaitEvent(xs, computed[sl], 0) != cudaSuccess) st = TF_ERR_CUDA;
+    // one copy per tensor: rows [pos0, pos0 + n) of every (b, g) unit
+    for (int kv = 0; kv < 2 && st == TF_OK && n > 0; ++kv) {
+      const uint16_t* src = (kv == 0 ? K_host : V_host) + (size_t)pos0 * kHeadDim;
+      if (cudaMemcpy2DAsync(stage[sl][kv], (size_t)seg_rows * row_bytes, src, (size_t)Lmax * row_bytes,
+                            (size_t)n * row_bytes, (size_t)units, cudaMemcpyHostToDevice, xs) != cudaSuccess)
+        st = TF_ERR_CUDA;
+    }
+    if (st == TF_OK && (cudaEventRecord(copied[sl], xs) != cudaSuccess || cudaStreamWaitEvent(cs, copied[sl], 0) != cudaSuccess))
+      st = TF_ERR_CUDA;
+    if (st == TF_OK)
+      st = verify_contig(Q, stage[sl][0], stage[sl][1], seq_lens, B, Hq, Hkv, seg_rows, T, scale, out, ws, cs, pos0,
+                         L_stream, parts + (size_t)sg * rows * kPartStride);
+    if (st == TF_OK && cudaEventRecord(computed[sl], cs) != cudaSuccess) st = TF_ERR_CUDA;
+  }
+  if (st == TF_OK) {
+    if (launch_pdl(merge_segments_kernel, dim3((rows + 7) / 8), dim3(256), 0, cs, (const float*)parts, nseg, rows,
+                   out) != cudaSuccess)
+      st = TF_ERR_CUDA;
+    else
+      st = launch_status();
+  }
+  cudaEventDestroy(start);
+  for (int sl = 0; sl < 2; ++sl) {
+    cudaEventDestroy(copied[sl]);
+    cudaEventDestroy(computed[sl]);
+  }
+  return st;
 }
 
 extern "C" size_t tf_sparse_verify_attn_workspace(int B, int Hq, int Hkv, int kc, int T) {
@@ -925,6 +1103,7 @@ extern "C" tf_status tf_sparse_verify_attn(const uint16_t* Q, const uint16_t* K,
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.Lmax = Lmax;
+  p.Ltot = Lmax;
   p.T = T;
   p.ngroups = (rows_all + kMaxRows - 1) / kMaxRows;
   p.idx = idx;

@@ -217,8 +217,8 @@ TF_API tf_status tf_stream_window_attn(const uint16_t* q, const uint16_t* K, con
  * Rows with no visible position (L - T + j < 0) are zero.  1 <= T <= 16;
  * B * Hkv * Lmax < 2^31.  Tensor-core kernel: K and V tiles stream in by TMA,
  * S = K Q^T and O = P V run as tcgen05 MMAs (bf16 in, fp32 accumulate; the
- * softmax weights P are rounded to bf16 and the row sums use the same rounded
- * weights).
+ * softmax weights P enter P V as bf16 hi + lo parts, P = hi + lo to 2^-17, and
+ * the row sums use the fp32 weights).
  *   out [B, Hq, T, D] float32
  * Workspace: tf_verify_attn_workspace(B, Hq, Hkv, Lmax, T) bytes.  Its first
  * int32 is a status word: nonzero means a pipeline wait timed out (which only a
@@ -231,6 +231,38 @@ TF_API tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const uint
                          int B, int Hq, int Hkv, int Lmax, int D, int T,
                          float scale, float* out,
                          void* ws, size_t ws_bytes, tf_stream_t stream);
+
+/*
+ * a7 with the cache offloaded to host memory ("TriForce: Lossless Acceleration
+ * of Long Sequence Generation with Hierarchical Speculative Decoding",
+ * "Abstract (arXiv)": the whole cache is read for every generated token;
+ * project summary, "Highlighted Details" / "How It Works": the original
+ * offloads the cache to CPU memory).  Computes exactly what tf_verify_attn
+ * computes; only where K and V live differs.
+ *   K_host, V_host: [B, Hkv, Lmax, D] bf16 in host memory (pinned, so that the
+ *     copies run asynchronously at full link rate; pageable memory works but
+ *     copies synchronously).  Q, seq_lens, out and ws are device memory.
+ *   L_stream: positions [0, L_stream) are streamed; every seq_lens[b] must be
+ *     <= L_stream <= Lmax (lengths are clamped to L_stream).
+ *   seg_rows: positions per segment.  Segment s (positions [s * seg_rows,
+ *     (s + 1) * seg_rows)) is copied on copy_stream into one of two device
+ *     staging slots (one 2-D copy per tensor: every (b, g) unit's rows) while
+ *     the previous segment is attended on `stream`; each segment leaves every
+ *     query row's (max, row sum, unnormalised O) in the workspace and one
+ *     final kernel merges them (log-sum-exp identity).
+ *   Ordering: work queued on `stream` before the call completes before the
+ *   first copy; `out` is ready in `stream` order.  copy_stream may equal
+ *   stream (no overlap).
+ * Workspace: tf_verify_attn_offload_workspace(B, Hq, Hkv, Lmax, T, seg_rows)
+ * bytes, zeroed once before first use; its first int32 is the status word of
+ * tf_verify_attn.  Errors: TF_ERR_INVALID_ARG / UNSUPPORTED / WORKSPACE before
+ * any work is queued; TF_ERR_CUDA if a copy or launch fails.
+ */
+TF_API size_t tf_verify_attn_offload_workspace(int B, int Hq, int Hkv, int Lmax, int T, int seg_rows);
+TF_API tf_status tf_verify_attn_offload(const uint16_t* Q, const uint16_t* K_host, const uint16_t* V_host,
+                                 const int32_t* seq_lens, int L_stream, int B, int Hq, int Hkv, int Lmax,
+                                 int D, int T, float scale, float* out, int seg_rows, void* ws,
+                                 size_t ws_bytes, tf_stream_t stream, tf_stream_t copy_stream);
 
 /*
  * a8 -- lossless speculative accept / resample of one verification level

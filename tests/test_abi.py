@@ -53,6 +53,11 @@ def test_workspace_sizes(lib):
     assert lib.tf_verify_attn_workspace(4, 32, 8, 131072, 6) > 0
     assert lib.tf_spec_accept_workspace(8, 5) >= 8 * 11 * 12
     assert lib.tf_sparse_verify_attn_workspace(1, 32, 32, 512, 6) > 0
+    assert lib.tf_verify_attn_offload_workspace(1, 32, 32, 131072, 6, 16384) > 0
+    assert lib.tf_verify_attn_offload_workspace(1, 32, 32, 131072, 6, 0) == 0
+    # the staging slots and the per-segment states grow with the segment count and size
+    assert (lib.tf_verify_attn_offload_workspace(1, 32, 32, 131072, 6, 8192) <
+            lib.tf_verify_attn_offload_workspace(1, 32, 32, 131072, 6, 16384))
     # workspace grows with the problem
     assert lib.tf_verify_attn_workspace(8, 32, 8, 131072, 6) > lib.tf_verify_attn_workspace(1, 32, 8, 131072, 6)
 
@@ -101,6 +106,14 @@ def test_host_validation_rejects_before_launch(lib):
               None) == INVALID  # no ids
     assert sv(fake, fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 16, 4, 0.1, fake, null, 0,
               None) == WORKSPACE
+    # offloaded verify: Q, K_host, V_host, seq, L_stream, B, Hq, Hkv, Lmax, D, T, scale, out, seg_rows,
+    # ws, bytes, stream, copy_stream
+    ov = lib.tf_verify_attn_offload
+    assert ov(fake, fake, fake, fake, 65, 1, 8, 2, 64, 128, 4, 0.1, fake, 32, fake, big, None, None) == INVALID
+    assert ov(fake, fake, fake, fake, 64, 1, 8, 2, 64, 128, 4, 0.1, fake, 0, fake, big, None, None) == INVALID
+    assert ov(fake, null, fake, fake, 64, 1, 8, 2, 64, 128, 4, 0.1, fake, 32, fake, big, None, None) == INVALID
+    assert ov(fake, fake, fake, fake, 64, 1, 8, 2, 64, 128, 17, 0.1, fake, 32, fake, big, None, None) == UNSUPPORTED
+    assert ov(fake, fake, fake, fake, 64, 1, 8, 2, 64, 128, 4, 0.1, fake, 32, null, 0, None, None) == WORKSPACE
     assert lib.tf_spec_accept(fake, fake, fake, fake, fake, 1, 4, 100, 0.0, fake, fake, null, fake, 4096,
                               None) == INVALID
     assert lib.tf_spec_accept(fake, null, fake, fake, fake, 1, 4, 100, 1.0, fake, fake, null, fake, 4096,
