@@ -410,6 +410,43 @@ def run_gpu(args):
     kernels["retrieval_draft"]["back_to_back"] = {
         "ms": round(dr_ms, 5), "GBps": round(bytes_draft / (dr_ms / 1e3) / 1e9, 1),
         "frac_hbm": round(bytes_draft / (dr_ms / 1e3) / 1e9 / peak, 4)}
+    # the verify with this layer's cache offloaded to pinned host memory,
+    # streamed over the host link in 16K-position segments (not part of the
+    # step); the peak is a plain pinned host-to-device copy of the same bytes
+    Kh = torch.empty(Kc[0].shape, dtype=Kc[0].dtype, pin_memory=True)
+    Vh = torch.empty(Vc[0].shape, dtype=Vc[0].dtype, pin_memory=True)
+    Kh.copy_(Kc[0])
+    Vh.copy_(Vc[0])
+    off_bytes = 2 * Kh.numel() * 2
+    seg_rows = min(16384, L)
+    ws_off = tf.workspace(tf.tf_verify_attn_offload_workspace(B, Hq, Hkv, L, T, seg_rows), dev)
+    o_off = torch.empty((B, Hq, T, D), dtype=torch.float32, device=dev)
+    side = torch.cuda.Stream()
+    tf.tf_verify_attn_offload(Q_all[0], Kh, Vh, seq, L, scale, out=o_off, ws=ws_off, seg_rows=seg_rows,
+                              copy_stream=side)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(3):
+        tf.tf_verify_attn_offload(Q_all[0], Kh, Vh, seq, L, scale, out=o_off, ws=ws_off, seg_rows=seg_rows,
+                                  copy_stream=side)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    off_ms = f0.elapsed_time(f1) / 3
+    stage = torch.empty_like(Kc[0])
+    f0.record(stream)
+    for _ in range(3):
+        stage.copy_(Kh, non_blocking=True)
+        stage.copy_(Vh, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    h2d_ms = f0.elapsed_time(f1) / 3
+    del stage, Kh, Vh
+    kernels["verify_offloaded_1layer"] = {
+        "ms": round(off_ms, 4), "GBps": round(off_bytes / (off_ms / 1e3) / 1e9, 1),
+        "h2d_copy_GBps": round(off_bytes / (h2d_ms / 1e3) / 1e9, 1),
+        "frac_of_h2d_copy": round(h2d_ms / off_ms, 4), "calls": "tf_verify_attn_offload",
+        "timing": "K/V in pinned host memory, 16K-position segments, copies on a second stream"}
     kernels["chunk_means_prefill_1layer"] = {"ms": round(means_ms, 4),
                                              "GBps": round(means_bytes / (means_ms / 1e3) / 1e9, 1)}
     ver_ms = statistics.mean(per_kind["verify"])
