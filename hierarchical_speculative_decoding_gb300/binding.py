@@ -40,6 +40,7 @@ _SIGS = {
     "tf_sparse_verify_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_verify_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
     "tf_verify_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
+    "tf_verify_attn_tree": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_verify_attn_offload_workspace": (_S, [_I, _I, _I, _I, _I, _I]),
     "tf_verify_attn_offload": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _S, _P, _P]),
     "tf_spec_accept_workspace": (_S, [_I, _I]),
@@ -298,6 +299,27 @@ def tf_verify_attn(Q, K, V, seq_lens, scale, out=None, ws=None, stream=None):
     ws, nbytes = _ws(ws, tf_verify_attn_workspace(B, Hq, Hkv, Lmax, T), Q.device)
     _check(load().tf_verify_attn(_ptr(Q), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax, D, T, float(scale),
                                  _ptr(out), _ptr(ws), nbytes, _stream(stream)), "tf_verify_attn")
+    return out
+
+
+def tf_verify_attn_tree(Q, K, V, seq_lens, parent, scale, out=None, ws=None, stream=None):
+    """Verify attention over a candidate tree: parent [B, T] int32 (-1: the prefix)."""
+    _need(Q, torch.bfloat16, "Q", 4)
+    _need(K, torch.bfloat16, "K", 4)
+    _need(V, torch.bfloat16, "V", 4)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(parent, torch.int32, "parent", 2)
+    B, Hq, T, D = Q.shape
+    _, Hkv, Lmax, _ = K.shape
+    if tuple(parent.shape) != (B, T):
+        raise ValueError(f"parent must be [B, T] = [{B}, {T}], got {tuple(parent.shape)}")
+    if out is None:
+        out = torch.empty((B, Hq, T, D), dtype=torch.float32, device=Q.device)
+    _need(out, torch.float32, "out", 4)
+    ws, nbytes = _ws(ws, tf_verify_attn_workspace(B, Hq, Hkv, Lmax, T), Q.device)
+    _check(load().tf_verify_attn_tree(_ptr(Q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(parent), B, Hq, Hkv, Lmax, D,
+                                      T, float(scale), _ptr(out), _ptr(ws), nbytes, _stream(stream)),
+           "tf_verify_attn_tree")
     return out
 
 

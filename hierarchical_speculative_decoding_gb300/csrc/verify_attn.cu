@@ -79,6 +79,9 @@ struct VerifyParams {
   // (m, l, unnormalised O; kPartStride floats) is written instead of O
   int pos0, Ltot;
   float* part_out;
+  // candidate tree [B, T]: parent[b * T + j] is the candidate that j extends
+  // (-1: the prefix); null: a chain (parent j - 1)
+  const int32_t* parent;
 };
 
 // Final log-sum-exp merge of a unit's split partials by the CTA that finished
@@ -246,7 +249,7 @@ __device__ __forceinline__ void named_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
 }
 
-template <int NR, bool GATHER>
+template <int NR, bool GATHER, bool TREE = false>
 __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_constant__ CUtensorMap mapK,
                                                                   const __grid_constant__ CUtensorMap mapV,
                                                                   VerifyParams p) {
@@ -262,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   __shared__ int s_last, s_abort;
   __shared__ int s_pstart[GATHER ? kPiecesPerTile * kMaxTilesPerCta : 1];  // first position, -1: none
   __shared__ int s_pcand[GATHER ? kPiecesPerTile * kMaxTilesPerCta : 1];   // 1: candidate rows
+  __shared__ uint32_t s_vis[16];  // candidate i -> bit n set: query row n of this CTA sees it
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + S::kOffQ;
@@ -334,6 +338,23 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
       s_pstart[e] = st;
       s_pcand[e] = cand;
     }
+  }
+  // Tree: which candidates each query row sees, its own and its ancestors'.
+  // Parents outside [0, j) end the walk.
+  if (TREE && tid < p.T) {
+    uint32_t vis = 0;
+    for (int n = 0; n < rows; ++n) {
+      int x = (row0 + n) % p.T;
+      for (int k = 0; k <= p.T && x >= 0; ++k) {
+        if (x == tid) {
+          vis |= 1u << n;
+          break;
+        }
+        const int px = p.parent ? p.parent[(size_t)b * p.T + x] : x - 1;
+        x = (px >= 0 && px < x) ? px : -1;
+      }
+    }
+    s_vis[tid] = vis;
   }
   // Q rows of this group -> shared memory, [kNS x 128] bf16 in two swizzled halves.
   {
@@ -465,15 +486,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     const int my = q4 * 32 + lane;         // key index in the tile / head dim of O
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     float m_run[NR], l_part[NR], acc[NR];
-    int lim[NR];
+    int lim[TREE ? 1 : NR];  // chain: query row n sees positions <= lim[n]
 #pragma unroll
     for (int n = 0; n < NR; ++n) {
       m_run[n] = -INFINITY;
       l_part[n] = 0.0f;
       acc[n] = 0.0f;
-      const int rr = row0 + n;
-      lim[n] = (n < rows) ? (L - p.T + (rr % p.T)) : -1;
+      if (!TREE) lim[n] = (n < rows) ? (L - p.T + ((row0 + n) % p.T)) : -1;
     }
+    const uint32_t all_rows = rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u);
+    const int cbase = L - p.T;  // position of candidate 0
     // Every wait is followed by a vote over the 128 threads so that a timeout
     // makes all of them leave the loop together (named barriers stay matched).
     bool zero_v = false;  // this key row of the tile must be zeroed in V
@@ -489,8 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
 #pragma unroll
         for (int c = 0; c < NR; c += 8) tmem_ld8(tmem + (t & 1) * 32 + lane_off + c, sc + c);
         tmem_ld_wait();
-        // this key's position and whether it may be seen at all; candidate
-        // rows (every row of the contiguous range) are also chain-limited
+        // this key's position and whether it may be seen at all; a candidate
+        // key (position >= L - T) only by the rows whose candidate extends it
         int pos;
         bool key_ok, chain;
         if (!GATHER) {
@@ -507,10 +529,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           key_ok = st >= 0 && pos < L && (chain ? pos >= cstart : pos < cstart);
           zero_v = !key_ok;  // rows of empty pieces, past L, or counted elsewhere
         }
+        uint32_t vis = 0;
+        if (TREE) {
+          const int ci = pos - cbase;
+          vis = !key_ok ? 0u : (chain && ci >= 0) ? s_vis[ci < 16 ? ci : 15] : all_rows;
+        }
         bool need = false;
 #pragma unroll
         for (int n = 0; n < NR; ++n) {
-          const bool valid = key_ok && (!chain || pos <= lim[n]);
+          const bool valid = TREE ? ((vis >> n) & 1u) != 0u : (key_ok && (!chain || pos <= lim[TREE ? 0 : n]));
           sc[n] = valid ? sc[n] * p.scale_log2 : -INFINITY;
           need |= sc[n] > m_run[n] + kRescaleThreshold;
         }
@@ -804,12 +831,12 @@ size_t verify_ws(int units, int rows_all, int Lmax) {
          ug * cap * kMaxRows * kHeadDim * sizeof(float);
 }
 
-template <int NR, bool GATHER>
+template <int NR, bool GATHER, bool TREE>
 tf_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParams& p, dim3 grid,
                  cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(verify_umma_kernel<NR, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(verify_umma_kernel<NR, GATHER, TREE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<NR>::kDynamic) != cudaSuccess)
       return TF_ERR_CUDA;
     configured = true;
@@ -828,20 +855,20 @@ tf_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParam
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.cmerge ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, verify_umma_kernel<NR, GATHER>, mk, mv, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, verify_umma_kernel<NR, GATHER, TREE>, mk, mv, p) != cudaSuccess)
     return TF_ERR_CUDA;
   return launch_status();
 }
 
 // The softmax works on the group's query rows rounded up to 8.
-template <bool GATHER>
+template <bool GATHER, bool TREE = false>
 tf_status launch_rows(int rows_max, const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParams& p, dim3 grid,
                       cudaStream_t stream) {
   switch ((rows_max + 7) >> 3) {
-    case 1: return launch<8, GATHER>(mk, mv, p, grid, stream);
-    case 2: return launch<16, GATHER>(mk, mv, p, grid, stream);
-    case 3: return launch<24, GATHER>(mk, mv, p, grid, stream);
-    default: return launch<32, GATHER>(mk, mv, p, grid, stream);
+    case 1: return launch<8, GATHER, TREE>(mk, mv, p, grid, stream);
+    case 2: return launch<16, GATHER, TREE>(mk, mv, p, grid, stream);
+    case 3: return launch<24, GATHER, TREE>(mk, mv, p, grid, stream);
+    default: return launch<32, GATHER, TREE>(mk, mv, p, grid, stream);
   }
 }
 
@@ -903,7 +930,7 @@ namespace {
 // each row's partial state to part_out when it is set.  Arguments validated.
 tf_status verify_contig(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* seq_lens, int B,
                         int Hq, int Hkv, int Lmax, int T, float scale, float* out, void* ws, cudaStream_t stream,
-                        int pos0, int Ltot, float* part_out) {
+                        int pos0, int Ltot, float* part_out, const int32_t* parent = nullptr) {
   const long long rows_total = (long long)B * Hkv * Lmax;
   CUtensorMap mk, mv;
   if (!make_kv_map(&mk, K, rows_total, kTile) || !make_kv_map(&mv, V, rows_total, kTile)) return TF_ERR_CUDA;
@@ -918,6 +945,7 @@ tf_status verify_contig(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
   p.Ltot = Ltot;
   p.pos0 = pos0;
   p.part_out = part_out;
+  p.parent = parent;
   p.T = T;
   p.ngroups = (rows_all + kMaxRows - 1) / kMaxRows;
   p.splits_cap = verify_splits_cap(Lmax);
@@ -932,7 +960,8 @@ tf_status verify_contig(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
                                       align_up((size_t)ug * p.splits_cap * kMaxRows * 2 * sizeof(float), 256));
   dim3 grid(p.splits, ug);
   const int rows_max = rows_all < kMaxRows ? rows_all : kMaxRows;
-  return launch_rows<false>(rows_max, mk, mv, p, grid, stream);
+  return parent ? launch_rows<false, true>(rows_max, mk, mv, p, grid, stream)
+                : launch_rows<false, false>(rows_max, mk, mv, p, grid, stream);
 }
 
 // Log-sum-exp merge of per-segment row states: part [nseg][rows][kPartStride]
@@ -997,6 +1026,23 @@ extern "C" tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const 
   const size_t need = verify_ws(B * Hkv, (Hq / Hkv) * T, Lmax);
   if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
   return verify_contig(Q, K, V, seq_lens, B, Hq, Hkv, Lmax, T, scale, out, ws, stream, 0, Lmax, nullptr);
+}
+
+extern "C" tf_status tf_verify_attn_tree(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                                         const int32_t* seq_lens, const int32_t* parent, int B, int Hq, int Hkv,
+                                         int Lmax, int D, int T, float scale, float* out, void* ws, size_t ws_bytes,
+                                         tf_stream_t stream) {
+  using namespace tf;
+  if (!parent) return TF_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !seq_lens || !out) return TF_ERR_INVALID_ARG;
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || Hq % Hkv || T < 1) return TF_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return TF_ERR_INVALID_ARG;
+  if (D != kHeadDim || T > 16) return TF_ERR_UNSUPPORTED;
+  if (B == 0 || Lmax == 0) return TF_OK;
+  if ((long long)B * Hkv * Lmax >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
+  const size_t need = verify_ws(B * Hkv, (Hq / Hkv) * T, Lmax);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
+  return verify_contig(Q, K, V, seq_lens, B, Hq, Hkv, Lmax, T, scale, out, ws, stream, 0, Lmax, nullptr, parent);
 }
 
 extern "C" size_t tf_verify_attn_offload_workspace(int B, int Hq, int Hkv, int Lmax, int T, int seg_rows) {

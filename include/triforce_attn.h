@@ -233,6 +233,27 @@ TF_API tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const uint
                          void* ws, size_t ws_bytes, tf_stream_t stream);
 
 /*
+ * a7 over a candidate tree (SURVEY's NEXT row 2; "TriForce: Hierarchical
+ * Speculative Decoding for LLMs", "The Three Forces of TriForce": Force 2
+ * arranges the surviving candidates as a tree and Force 3 checks the whole
+ * tree in one forward pass with tree attention).  The T candidates sit at
+ * positions L-T .. L-1 as for tf_verify_attn; parent[b*T + j] (device int32,
+ * [B, T]) is the candidate that candidate j extends, or -1 when j extends the
+ * prefix directly.  Query j attends to the prefix [0, L-T) and to candidate j
+ * and its ancestors:
+ *   out[b,h,j,:] = softmax(scale * Q[b,h,j] . K_P) V_P,
+ *   P = [0, L-T) U { L-T+i : i = j, parent(j), parent(parent(j)), ... }
+ * parent = j - 1 for every j is the chain of tf_verify_attn (same result).  A
+ * parent outside [-1, j) ends the ancestor walk there (it is read as -1).
+ * Same shapes, workspace and errors as tf_verify_attn; parent may not be null.
+ */
+TF_API tf_status tf_verify_attn_tree(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                              const int32_t* seq_lens, const int32_t* parent,
+                              int B, int Hq, int Hkv, int Lmax, int D, int T,
+                              float scale, float* out,
+                              void* ws, size_t ws_bytes, tf_stream_t stream);
+
+/*
  * a7 with the cache offloaded to host memory ("TriForce: Lossless Acceleration
  * of Long Sequence Generation with Hierarchical Speculative Decoding",
  * "Abstract (arXiv)": the whole cache is read for every generated token;

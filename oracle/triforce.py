@@ -353,6 +353,56 @@ def verify_attn(Q_bits, K_bits, V_bits, seq_lens, scale):
     return out
 
 
+def tree_ancestors(parent_row, j):
+    """Candidate j and its ancestors, following parent links towards the prefix.
+
+    Reading of the candidate tree (blog page, "The Three Forces of TriForce":
+    Force 2 arranges the surviving candidates as a tree, Force 3 checks it in
+    one pass with tree attention): parent_row[j] is the candidate that j
+    extends, -1 when j extends the prefix directly.  A link that does not point
+    to an earlier candidate ends the walk (read as -1).
+    """
+    out = [j]
+    x = j
+    while True:
+        px = int(parent_row[x])
+        if px < 0 or px >= x:
+            return out
+        out.append(px)
+        x = px
+
+
+def tree_verify_positions(L, T, j, parent_row):
+    """Keys seen by tree-verify query j: the prefix [0, L - T) and the positions
+    L - T + i of candidate j's ancestors-or-self i (those inside [0, L))."""
+    pre = list(range(0, max(L - T, 0)))
+    cand = sorted(L - T + i for i in tree_ancestors(parent_row, j) if 0 <= L - T + i < L)
+    return np.array(pre + cand, dtype=np.int64)
+
+
+def tree_verify_attn(Q_bits, K_bits, V_bits, seq_lens, parent, scale):
+    """Force 3 over a candidate tree.  parent [B, T] ints; Q [B, Hq, T, D] -> float64.
+
+    Query j of head h attends to tree_verify_positions; with parent[b, j] = j - 1
+    for every j this is verify_attn.
+    """
+    Q = bf16_to_f64(Q_bits)
+    K = bf16_to_f64(K_bits)
+    V = bf16_to_f64(V_bits)
+    B, Hq, T, D = Q.shape
+    Hkv, Lmax = K.shape[1], K.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, T, D))
+    for b in range(B):
+        L = valid_len(seq_lens[b], Lmax)
+        for h in range(Hq):
+            g = h // G
+            for j in range(T):
+                pos = tree_verify_positions(L, T, j, parent[b])
+                out[b, h, j] = attend(Q[b, h, j], K[b, g, pos], V[b, g, pos], scale)[0]
+    return out
+
+
 def sparse_verify_positions(idx_row, n_sel, L, T, j, chunk, Lmax):
     """Keys seen by query j (0 <= j < T) of the retrieval drafter's verification.
 

@@ -344,3 +344,49 @@ def test_spec_accept_lossless_chi_square_gpu(cuda_lib):
     p0 = torch.softmax(p[0, 0].double(), -1).cpu().numpy()
     assert _chi2_ok(y[:, 0].cpu().numpy(), q0)
     assert _chi2_ok(z[:, 0].cpu().numpy(), p0)
+
+
+# ------------------------------------------------------------------ candidate trees
+
+
+def random_tree(B, T, seed):
+    rng = np.random.default_rng(seed)
+    return np.array([[int(rng.integers(-1, j)) if j > 0 else -1 for j in range(T)] for _ in range(B)], np.int32)
+
+
+@pytest.mark.parametrize("w", [small_workload(), small_workload(Hkv=8, T=6, L=3000, L_min=2000),
+                               small_workload(B=1, Hq=16, Hkv=2, T=9, L=900, ragged=False),
+                               small_workload(B=2, Hq=8, Hkv=2, T=16, L=1300, L_min=600)],
+                         ids=["ragged-gqa", "mha-6", "row-groups-72", "t16"])
+def test_verify_tree(cuda_lib, w):
+    c = make_case(w, fill_invalid=float("nan") if w.ragged else None)
+    parent = random_tree(w.B, w.T, seed=w.T)
+    out = cuda_lib.tf_verify_attn_tree(c["Q"], c["K"], c["V"], c["seq"], torch.from_numpy(parent).cuda(),
+                                       scale_for(w.D))
+    want = O.tree_verify_attn(bits(c["Q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), c["seq_cpu"].numpy(), parent,
+                              scale_for(w.D))
+    assert np.abs(out.cpu().double().numpy() - want).max() <= ATOL
+
+
+def test_verify_tree_special_shapes(cuda_lib):
+    w = small_workload(L=1200, T=6, ragged=False)
+    c = make_case(w)
+    sc = scale_for(w.D)
+    want_of = lambda parent: O.tree_verify_attn(bits(c["Q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]),  # noqa: E731
+                                                c["seq_cpu"].numpy(), parent, sc)
+    run = lambda parent: cuda_lib.tf_verify_attn_tree(c["Q"], c["K"], c["V"], c["seq"],  # noqa: E731
+                                                      torch.from_numpy(parent).cuda(), sc)
+    # the chain is tf_verify_attn, to the bit
+    chain = np.tile(np.arange(w.T, dtype=np.int32) - 1, (w.B, 1))
+    assert torch.equal(run(chain), cuda_lib.tf_verify_attn(c["Q"], c["K"], c["V"], c["seq"], sc))
+    # a star: every candidate extends the prefix
+    star = np.full((w.B, w.T), -1, np.int32)
+    assert np.abs(run(star).cpu().double().numpy() - want_of(star)).max() <= ATOL
+    # links to itself, to later candidates or below -1 end the walk
+    bad = np.array([[-1, 3, 1, -7, 2, 5], [0, 0, 1, 9, 3, 4]], np.int32)
+    assert np.abs(run(bad).cpu().double().numpy() - want_of(bad)).max() <= ATOL
+    # contexts shorter than the candidates (L = 5 < T for the shortest sequence)
+    c["seq"] = torch.tensor([5, 1200], dtype=torch.int32, device="cuda")
+    c["seq_cpu"] = torch.tensor([5, 1200], dtype=torch.int32)
+    tree = random_tree(w.B, w.T, seed=1)
+    assert np.abs(run(tree).cpu().double().numpy() - want_of(tree)).max() <= ATOL

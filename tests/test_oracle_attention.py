@@ -224,3 +224,95 @@ def test_sparse_verify_with_an_empty_selection_sees_only_the_candidates():
     # the first candidate sees only itself: its output is its own V row
     np.testing.assert_allclose(sv[0, :, 0], np.broadcast_to(O.bf16_to_f64(_bits(V))[0, 0, 36], (Hq, D)), rtol=0,
                                atol=0)
+
+
+# ------------------------------------------------------------------ candidate trees
+
+
+def test_tree_ancestors_hand_worked():
+    # 0 and its children 1, 2; 3 under 1: ancestors-or-self of each candidate
+    parent = [-1, 0, 0, 1]
+    assert O.tree_ancestors(parent, 0) == [0]
+    assert O.tree_ancestors(parent, 1) == [1, 0]
+    assert O.tree_ancestors(parent, 2) == [2, 0]
+    assert O.tree_ancestors(parent, 3) == [3, 1, 0]
+    # a link to itself, to a later candidate or below -1 ends the walk
+    bad = [-1, 5, -3, 2, 4]
+    assert O.tree_ancestors(bad, 1) == [1]
+    assert O.tree_ancestors(bad, 2) == [2]
+    assert O.tree_ancestors(bad, 3) == [3, 2]
+    assert O.tree_ancestors(bad, 4) == [4]
+    # positions: prefix, then the candidates in position order, clipped to [0, L)
+    np.testing.assert_array_equal(O.tree_verify_positions(10, 4, 3, parent), [0, 1, 2, 3, 4, 5, 6, 7, 9])
+    np.testing.assert_array_equal(O.tree_verify_positions(2, 4, 3, parent), [1])
+
+
+def _tree_case(B=2, Hq=4, Hkv=2, T=6, L=40, D=32, seed=3):
+    Q = _rand_bf16((B, Hq, T, D), seed)
+    K = _rand_bf16((B, Hkv, L, D), seed + 1)
+    V = _rand_bf16((B, Hkv, L, D), seed + 2)
+    return Q, K, V
+
+
+def test_tree_with_chain_parents_is_the_chain_verify():
+    Q, K, V = _tree_case()
+    B, T = Q.shape[0], Q.shape[2]
+    seq = np.array([40, 23])
+    chain = np.tile(np.arange(T) - 1, (B, 1))
+    got = O.tree_verify_attn(_bits(Q), _bits(K), _bits(V), seq, chain, 0.2)
+    want = O.verify_attn(_bits(Q), _bits(K), _bits(V), seq, 0.2)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_tree_matches_sdpa_with_a_closure_mask():
+    # the mask comes from the transitive closure of the parent adjacency
+    # matrix, not from walking the parent links
+    rng = np.random.default_rng(7)
+    Q, K, V = _tree_case(T=7, L=30, seed=11)
+    B, Hq, T, D = Q.shape
+    Hkv, Lmax = K.shape[1], K.shape[2]
+    seq = np.array([30, 12])
+    parent = np.stack([np.array([rng.integers(-1, j) if j > 0 else -1 for j in range(T)]) for _ in range(B)])
+    got = O.tree_verify_attn(_bits(Q), _bits(K), _bits(V), seq, parent, 0.17)
+    Qf, Kf, Vf = (t.to(torch.float64) for t in (Q, K, V))
+    for b in range(B):
+        L = int(seq[b])
+        A = np.eye(T, dtype=np.int64)  # A[j, i] = 1: i is j or an ancestor of j
+        for j in range(T):
+            if parent[b, j] >= 0:
+                A[j, parent[b, j]] = 1
+        R = A.copy()
+        for _ in range(T):
+            R = np.minimum(R @ A, 1)
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            mask = np.zeros((T, Lmax), dtype=bool)
+            mask[:, : max(L - T, 0)] = True
+            for j in range(T):
+                for i in range(T):
+                    if R[j, i] and 0 <= L - T + i < L:
+                        mask[j, L - T + i] = True
+            want = torch.nn.functional.scaled_dot_product_attention(
+                Qf[b, h][None], Kf[b, g][None], Vf[b, g][None], attn_mask=torch.from_numpy(mask)[None],
+                scale=0.17)[0].numpy()
+            np.testing.assert_allclose(got[b, h], want, rtol=1e-10, atol=1e-12)
+
+
+def test_tree_relabelling_permutes_the_outputs():
+    # the same tree with its candidates renumbered (parents still earlier):
+    # queries, candidate keys and values move together, outputs follow
+    Q, K, V = _tree_case(B=1, Hq=2, Hkv=1, T=5, L=20, seed=21)
+    T, L = 5, 20
+    parent = np.array([[-1, 0, -1, 1, 2]])
+    perm = [0, 2, 1, 4, 3]  # new index -> old index; old parents map to earlier new indices
+    inv = {old: new for new, old in enumerate(perm)}
+    parent2 = np.array([[inv[parent[0, o]] if parent[0, o] >= 0 else -1 for o in perm]])
+    assert all(parent2[0, j] < j for j in range(T))
+    Q2 = Q[:, :, perm]
+    K2, V2 = K.clone(), V.clone()
+    K2[:, :, L - T:] = K[:, :, [L - T + o for o in perm]]
+    V2[:, :, L - T:] = V[:, :, [L - T + o for o in perm]]
+    seq = np.array([L])
+    a = O.tree_verify_attn(_bits(Q), _bits(K), _bits(V), seq, parent, 0.3)
+    b = O.tree_verify_attn(_bits(Q2), _bits(K2), _bits(V2), seq, parent2, 0.3)
+    np.testing.assert_allclose(b, a[:, :, perm], rtol=1e-12, atol=1e-14)
