@@ -9,30 +9,42 @@
 // The whole cache is read once per step, so the kernel is HBM-bound (6 flop/B for
 // MHA, 24 flop/B for a GQA group of 4); the tensor cores only have to keep up.
 // Per CTA: one (sequence, KV head) unit, one group of <= 32 query rows (the
-// GQA heads x gamma+1 tokens, padded to N = 16 or 32) and one contiguous key
-// range (split-K).  Warp roles:
+// GQA heads x gamma+1 tokens; the softmax works on them rounded up to 8) and
+// one contiguous key range (split-K).  Warp roles:
 //   warp 0    TMA producer: 128-key tiles of K and V (2 x 32 KB, 128-byte
 //             swizzle) into a 3-stage shared-memory ring;
-//   warp 1    tcgen05 issuer: S^T[key, n] = K Q^T into TMEM (M = 128 keys),
-//             then O^T[d, n] = V^T P^T into TMEM (M = 128 head dims, V read
-//             MN-major straight from the TMA tile);
+//   warp 1    tcgen05 issuer: S^T[key, n] = K Q^T into TMEM (M = 128 keys,
+//             N = 16 or 32), then O^T = V^T [P_hi; P_lo]^T into TMEM (M = 128
+//             head dims, V read MN-major straight from the TMA tile; the hi
+//             and lo bf16 parts of P as separate rows, so one MMA per 16 keys
+//             reads V once and leaves P_hi V and P_lo V side by side);
 //   warps 2-5 softmax on TMEM lane = key (online, log2 domain, rescaled only
-//             when the running max grows by > 2^8), P written to shared memory
-//             as bf16; then the O tile of the previous key tile is read back
-//             (TMEM lane = head dim) and accumulated in fp32 registers.
-// S, P and O are double-buffered so the MMA of tile t+1 overlaps the softmax of
-// tile t.  Splits are merged with the log-sum-exp identity by the last CTA of
-// each unit (atomic ticket).  Every mbarrier wait is bounded; on a timeout the
-// CTA records a nonzero status word at the start of the workspace and leaves.
+//             when the running max grows by > 2^8), P written over the K half
+//             of the tile's own stage (K is dead once S exists; the stage goes
+//             back to the copy engine after P V), handed over before the O of
+//             the previous tile is read back (TMEM lane = head dim) and
+//             accumulated in fp32 registers.
+// S and O are double-buffered in TMEM and P has one buffer per stage, so the
+// MMAs of tile t+1 overlap the softmax of tile t.  Splits are merged with the
+// log-sum-exp identity by the last CTA of each unit (atomic ticket; the
+// splits' partial rows are bulk-copied into its idle ring), or inside a
+// thread-block cluster through DSMEM when a unit has at most 8 splits.  Every
+// mbarrier wait is bounded; on a timeout the CTA records a nonzero status word
+// at the start of the workspace and leaves.
 //
 // The same kernel (GATHER) serves the retrieval drafter's check of the tiny
 // drafter's candidates ("The Three Forces of TriForce": the target model over
 // the retrieved KV blocks verifies the drafts): query j sees the valid rows of
 // the selected 8-token chunks before the candidates (positions < L-T) and
 // candidates 0..j.  A key tile is then sixteen 8-row pieces (the selected
-// chunks in list order, then the candidate rows), each loaded by an 8-row TMA
-// box that lands on one 1 KB swizzle atom of the tile; the softmax warps take
-// every key's position from a per-CTA piece table for the masks.
+// chunks in list order, then the candidate rows), each one 2 KB box of a 3-D
+// tensor map per tensor that lands as the piece's two 1 KB swizzle atoms; the
+// softmax warps take every key's position from a per-CTA piece table for the
+// masks.  With TREE the candidates form a tree (a parent array) and query j
+// sees candidate j and its ancestors; in segment mode the K/V buffers hold a
+// window of positions of a longer cache (the offloaded verify streams the cache
+// through such windows) and each row's (m, l, O) state is written for a final
+// merge.
 #include <cuda_bf16.h>
 
 #include "sm100_ptx.cuh"
