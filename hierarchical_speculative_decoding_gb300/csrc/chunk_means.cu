@@ -9,9 +9,11 @@
 // Design: a pure HBM stream.  One thread owns one 16-byte column slice (8 head
 // dims) of one chunk: a chunk is 8 rows x 256 B = 2 KiB contiguous, so 16
 // threads cover it and every load instruction of a half-warp reads 256
-// contiguous bytes.  Each thread keeps all 8 row loads in flight.  The sum of
-// the rows is carried as an unevaluated fp32 pair (TwoSum), so the mean is
-// exact before its single rounding to bf16.
+// contiguous bytes.  Each thread keeps all 8 row loads of its next item in
+// flight while it sums the current one (the exact sums cost ~700 instructions
+// per 128 bytes, so without the overlap the stream waits on the arithmetic).
+// The sum of the rows is carried as an unevaluated fp32 pair (TwoSum), so the
+// mean is exact before its single rounding to bf16.
 #include "tf_common.cuh"
 
 namespace tf {
@@ -38,75 +40,119 @@ __device__ __forceinline__ uint16_t round_pair_bf16(float hi, float lo) {
   return (uint16_t)((b + 0x7fffu + lsb) >> 16);
 }
 
+// One item = (unit, chunk, 16-byte column slice): where its rows start and how
+// many of them the sequence holds.
+struct Item {
+  const uint16_t* src;
+  uint16_t* dst;
+  int n;
+};
+
+__device__ __forceinline__ Item item_at(long long item, const uint16_t* K, const int32_t* seq_lens, int Hkv, int Lmax,
+                                        int Cmax, int c_begin, int n_chunks, uint16_t* M) {
+  const int slice = (int)(item & 15);
+  const long long rest = item >> 4;
+  const int c = c_begin + (int)(rest % n_chunks);
+  const long long bg = rest / n_chunks;
+  const int b = (int)(bg / Hkv);
+  const int L = clamp_len(seq_lens[b], Lmax);
+  int n = L - c * kChunk;
+  n = n < 0 ? 0 : (n > kChunk ? kChunk : n);
+  Item it;
+  it.src = K + ((size_t)bg * Lmax + (size_t)c * kChunk) * kHeadDim + slice * 8;
+  it.dst = M + ((size_t)bg * Cmax + c) * kHeadDim + slice * 8;
+  it.n = n;
+  return it;
+}
+
+__device__ __forceinline__ void load_rows(const Item& it, uint4 (&rows)[kChunk]) {
+#pragma unroll
+  for (int r = 0; r < kChunk; ++r)
+    rows[r] = (r < it.n) ? ld_stream16(it.src + (size_t)r * kHeadDim) : make_uint4(0, 0, 0, 0);
+}
+
+// Exact mean of the rows, rounded once to bf16, stored as 8 head dims.
+__device__ __forceinline__ void mean_store(const Item& it, const uint4 (&rows)[kChunk]) {
+  float hi[8], lo[8];
+#pragma unroll
+  for (int d = 0; d < 8; ++d) {
+    hi[d] = 0.0f;
+    lo[d] = 0.0f;
+  }
+#pragma unroll
+  for (int r = 0; r < kChunk; ++r) {
+    float f[8];
+    unpack8(rows[r], f);
+#pragma unroll
+    for (int d = 0; d < 8; ++d) {
+      float s, e;
+      two_sum(hi[d], f[d], s, e);
+      hi[d] = s;
+      lo[d] += e;
+    }
+  }
+  const int n = it.n;
+  uint32_t packed[4];
+#pragma unroll
+  for (int d = 0; d < 8; d += 2) {
+    uint16_t o[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      float h = hi[d + k], l = lo[d + k];
+      float s, e;
+      two_sum(h, l, s, e);  // renormalise the pair
+      h = s;
+      l = e;
+      if (n == 0) {
+        o[k] = 0;
+      } else if (n == kChunk) {
+        o[k] = round_pair_bf16(h * 0.125f, l * 0.125f);  // exact scaling by 2^-3
+      } else {
+        // Pair divided by n: quotient, exact remainder by FMA, corrected low part.
+        const float fn = (float)n;
+        float qh = __fdiv_rn(h, fn);
+        float rem = fmaf(-qh, fn, h);
+        float ql = __fdiv_rn(rem + l, fn);
+        float s2, e2;
+        two_sum(qh, ql, s2, e2);
+        o[k] = round_pair_bf16(s2, e2);
+      }
+    }
+    packed[d / 2] = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
+  }
+  *reinterpret_cast<uint4*>(it.dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
+// Grid-stride over items, software-pipelined: the next item's eight row loads
+// are issued before the current item's sums, so the DRAM round trip overlaps
+// the arithmetic.
 __global__ void __launch_bounds__(256) chunk_means_kernel(const uint16_t* __restrict__ K,
                                                           const int32_t* __restrict__ seq_lens,
                                                           int Hkv, int Lmax, int c_begin, int n_chunks,
                                                           long long total, uint16_t* __restrict__ M) {
   const int Cmax = (Lmax + kChunk - 1) / kChunk;
   pdl_wait();
-  for (long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x; item < total;
-       item += (long long)gridDim.x * blockDim.x) {
-    const int slice = (int)(item & 15);
-    const long long rest = item >> 4;
-    const int c = c_begin + (int)(rest % n_chunks);
-    const long long bg = rest / n_chunks;
-    const int b = (int)(bg / Hkv);
-    const int L = clamp_len(seq_lens[b], Lmax);
-    int n = L - c * kChunk;
-    n = n < 0 ? 0 : (n > kChunk ? kChunk : n);
-
-    const uint16_t* src = K + ((size_t)bg * Lmax + (size_t)c * kChunk) * kHeadDim + slice * 8;
-    uint4 rows[kChunk];
-#pragma unroll
-    for (int r = 0; r < kChunk; ++r)
-      rows[r] = (r < n) ? ld_stream16(src + (size_t)r * kHeadDim) : make_uint4(0, 0, 0, 0);
-
-    float hi[8], lo[8];
-#pragma unroll
-    for (int d = 0; d < 8; ++d) { hi[d] = 0.0f; lo[d] = 0.0f; }
-#pragma unroll
-    for (int r = 0; r < kChunk; ++r) {
-      float f[8];
-      unpack8(rows[r], f);
-#pragma unroll
-      for (int d = 0; d < 8; ++d) {
-        float s, e;
-        two_sum(hi[d], f[d], s, e);
-        hi[d] = s;
-        lo[d] += e;
-      }
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= total) return;
+  Item cur = item_at(item, K, seq_lens, Hkv, Lmax, Cmax, c_begin, n_chunks, M);
+  uint4 rows[kChunk];
+  load_rows(cur, rows);
+  while (true) {
+    const long long nxt_item = item + stride;
+    const bool more = nxt_item < total;
+    Item nxt = cur;
+    uint4 next_rows[kChunk];
+    if (more) {
+      nxt = item_at(nxt_item, K, seq_lens, Hkv, Lmax, Cmax, c_begin, n_chunks, M);
+      load_rows(nxt, next_rows);
     }
-
-    uint32_t packed[4];
+    mean_store(cur, rows);
+    if (!more) break;
 #pragma unroll
-    for (int d = 0; d < 8; d += 2) {
-      uint16_t o[2];
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        float h = hi[d + k], l = lo[d + k];
-        float s, e;
-        two_sum(h, l, s, e);  // renormalise the pair
-        h = s;
-        l = e;
-        if (n == 0) {
-          o[k] = 0;
-        } else if (n == kChunk) {
-          o[k] = round_pair_bf16(h * 0.125f, l * 0.125f);  // exact scaling by 2^-3
-        } else {
-          // Pair divided by n: quotient, exact remainder by FMA, corrected low part.
-          const float fn = (float)n;
-          float qh = __fdiv_rn(h, fn);
-          float rem = fmaf(-qh, fn, h);
-          float ql = __fdiv_rn(rem + l, fn);
-          float s2, e2;
-          two_sum(qh, ql, s2, e2);
-          o[k] = round_pair_bf16(s2, e2);
-        }
-      }
-      packed[d / 2] = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(M + ((size_t)bg * Cmax + c) * kHeadDim + slice * 8);
-    *dst = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    for (int r = 0; r < kChunk; ++r) rows[r] = next_rows[r];
+    cur = nxt;
+    item = nxt_item;
   }
 }
 
