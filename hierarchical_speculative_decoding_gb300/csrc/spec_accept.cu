@@ -25,6 +25,7 @@ constexpr int kBlockRow = 512;   // threads per row normaliser for large vocabul
 constexpr int kBlockSeq = 1024;  // threads per sequence for large vocabularies
 constexpr int kSmallV = 1024;    // up to this vocabulary a warp handles a row / a sequence
 constexpr int kBatch = 8;        // loads in flight per thread
+constexpr size_t kMaxStageBytes = 200 * 1024;  // staged sampling row (vocabularies up to ~48K)
 
 struct NormWs {
   float* m;   // [B, R] max of x = logit * log2(e) / temperature
@@ -38,25 +39,27 @@ __device__ __forceinline__ void combine(float& m, float& z, float m2, float z2) 
   m = mn;
 }
 
-// Per-thread (max, sum) over elements t = start, start + stride, ... < V.
+// Per-thread (max, sum) over elements t = start, start + stride, ... < V, NB
+// loads in flight at a time.
+template <int NB>
 __device__ __forceinline__ void thread_norm(const float* __restrict__ row, int V, int start, int stride, float inv_t,
                                             float& m, float& z) {
   m = -INFINITY;
   z = 0.0f;
-  for (int t0 = start; t0 < V; t0 += stride * kBatch) {
-    float x[kBatch];
+  for (int t0 = start; t0 < V; t0 += stride * NB) {
+    float x[NB];
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
+    for (int k = 0; k < NB; ++k) {
       const int t = t0 + k * stride;
       x[k] = t < V ? __ldg(row + t) * inv_t : -INFINITY;
     }
     float bm = x[0];
 #pragma unroll
-    for (int k = 1; k < kBatch; ++k) bm = fmaxf(bm, x[k]);
+    for (int k = 1; k < NB; ++k) bm = fmaxf(bm, x[k]);
     if (bm == -INFINITY) continue;
     float bz = 0.0f;
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) bz += exp2f(x[k] - bm);
+    for (int k = 0; k < NB; ++k) bz += exp2f(x[k] - bm);
     combine(m, z, bm, bz);
   }
 }
@@ -85,7 +88,10 @@ __global__ void __launch_bounds__(WARP ? 256 : kBlockRow) row_norm_kernel(const 
   const float* src = r <= gamma ? tgt + ((size_t)b * (gamma + 1) + r) * V
                                 : drf + ((size_t)b * gamma + (r - gamma - 1)) * V;
   float m, z;
-  thread_norm(src, V, start, stride, inv_t, m, z);
+  if (WARP)
+    thread_norm<kBatch>(src, V, start, stride, inv_t, m, z);
+  else
+    thread_norm<4 * kBatch>(src, V, start, stride, inv_t, m, z);  // a 32000-entry row in two rounds
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -107,14 +113,20 @@ __global__ void __launch_bounds__(WARP ? 256 : kBlockRow) row_norm_kernel(const 
     s_z[warp] = (double)z;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float mm = -INFINITY;
-    for (int w = 0; w < nw; ++w) mm = fmaxf(mm, s_m[w]);
-    double zz = 0.0;
-    for (int w = 0; w < nw; ++w)
-      if (s_m[w] != -INFINITY) zz += s_z[w] * exp2((double)s_m[w] - (double)mm);
-    ws.m[row] = mm;
-    ws.z[row] = zz;
+  if (warp == 0) {
+    // the warps' states combined by one warp: max, then sum z_w 2^(m_w - max)
+    const int lane = threadIdx.x & 31;
+    const float mw = lane < nw ? s_m[lane] : -INFINITY;
+    float mm = mw;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+    double zz = (mw == -INFINITY) ? 0.0 : s_z[lane] * (double)exp2f(mw - mm);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
+    if (lane == 0) {
+      ws.m[row] = mm;
+      ws.z[row] = zz;
+    }
   }
 }
 
@@ -132,13 +144,18 @@ struct RowWeights {
 };
 
 // (2) Tests and draw.  GS threads per sequence (a warp, or a whole block).
-template <int GS>
+// STAGE (GS = 1024 only): the sampling row's weights are computed once with
+// coalesced loads into shared memory, laid out as every thread's contiguous
+// vocabulary slice (seg floats at a pitch of seg + 1, so slice reads are free
+// of bank conflicts); the slice sums and the walk read them from there.
+template <int GS, bool STAGE = false>
 __global__ void __launch_bounds__(GS == 32 ? 256 : GS) accept_kernel(
     const float* __restrict__ tgt, const float* __restrict__ drf, const int32_t* __restrict__ tokens,
     const float* __restrict__ u_acc, const float* __restrict__ u_res, int B, int gamma, int V, float inv_t,
     double inv_t_d, NormWs ws, int32_t* __restrict__ n_acc, int32_t* __restrict__ next_token,
     int32_t* __restrict__ out_tokens) {
-  __shared__ double s_scan[32];
+  extern __shared__ float s_w[];
+  __shared__ double s_scan[32], s_total;
   __shared__ int s_found[32], s_lastv[32];
   __shared__ int s_g, s_nacc;
   pdl_wait();
@@ -214,14 +231,25 @@ __global__ void __launch_bounds__(GS == 32 ? 256 : GS) accept_kernel(
   int next = 0;
   for (int attempt = 0; attempt < 2; ++attempt) {
     w.resid = rejected && attempt == 0;
-    // slice sum, loads in batches
+    // slice sum (in index order)
     float run = 0.0f;
-    for (int t = t0; t < t1; t += kBatch) {
-      float v[kBatch];
+    const float* mine = s_w + (size_t)gid * (seg + 1);
+    if (STAGE) {
+      __syncthreads();  // (attempt 1) every reader of the previous weights is done
+      for (int e = gid; e < V; e += GS) {
+        const int owner = e / seg;
+        s_w[(size_t)owner * (seg + 1) + (e - owner * seg)] = w(e);
+      }
+      __syncthreads();
+      for (int k = 0; k < t1 - t0; ++k) run += mine[k];
+    } else {
+      for (int t = t0; t < t1; t += kBatch) {
+        float v[kBatch];
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) v[k] = (t + k < t1) ? w(t + k) : 0.0f;
+        for (int k = 0; k < kBatch; ++k) v[k] = (t + k < t1) ? w(t + k) : 0.0f;
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) run += v[k];
+        for (int k = 0; k < kBatch; ++k) run += v[k];
+      }
     }
     // fp64 scan of the slice sums over the group
     double incl = (double)run;
@@ -235,18 +263,26 @@ __global__ void __launch_bounds__(GS == 32 ? 256 : GS) accept_kernel(
       total = __shfl_sync(0xffffffffu, incl, 31);
       excl = incl - (double)run;
     } else {
+      // warp totals -> one warp scans them -> every thread adds its warp's prefix
       const int warp = threadIdx.x >> 5, nw = GS / 32;
       __syncthreads();
       if (lane == 31) s_scan[warp] = incl;
       __syncthreads();
-      double wpre = 0.0;
-      total = 0.0;
-      for (int k = 0; k < nw; ++k) {
-        const double v = s_scan[k];
-        if (k < warp) wpre += v;
-        total += v;
+      if (warp == 0) {
+        const double v = lane < nw ? s_scan[lane] : 0.0;
+        double wi = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double u2 = __shfl_up_sync(0xffffffffu, wi, o);
+          if (lane >= o) wi += u2;
+        }
+        __syncwarp();
+        if (lane < nw) s_scan[lane] = wi - v;  // exclusive prefix of warp `lane`
+        if (lane == 31) s_total = wi;
       }
-      excl = wpre + incl - (double)run;
+      __syncthreads();
+      total = s_total;
+      excl = s_scan[warp] + incl - (double)run;
     }
     if (!(total > 0.0)) {
       if (w.resid) continue;  // p == q: the residual is empty, draw from p_j instead
@@ -258,7 +294,7 @@ __global__ void __launch_bounds__(GS == 32 ? 256 : GS) accept_kernel(
     if (excl <= target && excl + (double)run > target) {
       float r2 = 0.0f;
       for (int t = t0; t < t1; ++t) {
-        r2 += w(t);
+        r2 += STAGE ? mine[t - t0] : w(t);
         if (excl + (double)r2 > target) {
           found = t;
           break;
@@ -274,7 +310,7 @@ __global__ void __launch_bounds__(GS == 32 ? 256 : GS) accept_kernel(
     }
     if (!any) {
       for (int t = t0; t < t1; ++t)
-        if (w(t) > 0.0f) last = t;
+        if ((STAGE ? mine[t - t0] : w(t)) > 0.0f) last = t;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -357,9 +393,23 @@ extern "C" tf_status tf_spec_accept(const float* tgt_logits, const float* drf_lo
   } else {
     e = launch_pdl(row_norm_kernel<false>, dim3((unsigned)rows), dim3(kBlockRow), 0, stream, tgt_logits, drf_logits,
                    B, gamma, V, inv_t, nws);
-    if (e == cudaSuccess)
+    const int seg = (V + kBlockSeq - 1) / kBlockSeq;
+    const size_t stage_bytes = (size_t)kBlockSeq * (seg + 1) * sizeof(float);
+    if (e == cudaSuccess && stage_bytes <= kMaxStageBytes) {
+      static bool configured = false;
+      if (!configured) {
+        if (cudaFuncSetAttribute(accept_kernel<kBlockSeq, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kMaxStageBytes) != cudaSuccess)
+          return TF_ERR_CUDA;
+        configured = true;
+      }
+      e = launch_pdl(accept_kernel<kBlockSeq, true>, dim3(B), dim3(kBlockSeq), stage_bytes, stream, tgt_logits,
+                     drf_logits, drf_tokens, u_acc, u_res, B, gamma, V, inv_t, inv_t_d, nws, n_acc, next_token,
+                     out_tokens);
+    } else if (e == cudaSuccess) {
       e = launch_pdl(accept_kernel<kBlockSeq>, dim3(B), dim3(kBlockSeq), 0, stream, tgt_logits, drf_logits,
                      drf_tokens, u_acc, u_res, B, gamma, V, inv_t, inv_t_d, nws, n_acc, next_token, out_tokens);
+    }
   }
   return e == cudaSuccess ? launch_status() : TF_ERR_CUDA;
 }
