@@ -39,6 +39,17 @@ __device__ __forceinline__ void combine(float& m, float& z, float m2, float z2) 
   m = mn;
 }
 
+// hi + lo += bh + bl for unevaluated fp32 pairs (|lo| <= ulp(hi) / 2): TwoSum of
+// the high parts, the low parts added to its error, renormalised.
+__device__ __forceinline__ void pair_add(float& hi, float& lo, float bh, float bl) {
+  const float s = hi + bh;
+  const float bb = s - hi;
+  float e = (hi - (s - bb)) + (bh - bb);
+  e += lo + bl;
+  hi = s + e;
+  lo = e - (hi - s);
+}
+
 // Per-thread (max, sum) over elements t = start, start + stride, ... < V, NB
 // loads in flight at a time.
 template <int NB>
@@ -155,7 +166,8 @@ __global__ void __launch_bounds__(GS == 32 ? 256 : GS) accept_kernel(
     double inv_t_d, NormWs ws, int32_t* __restrict__ n_acc, int32_t* __restrict__ next_token,
     int32_t* __restrict__ out_tokens) {
   extern __shared__ float s_w[];
-  __shared__ double s_scan[32], s_total;
+  __shared__ float s_ph[32], s_pl[32], s_th, s_tl;
+  __shared__ double s_total;
   __shared__ int s_found[32], s_lastv[32];
   __shared__ int s_g, s_nacc;
   pdl_wait();
@@ -251,51 +263,84 @@ __global__ void __launch_bounds__(GS == 32 ? 256 : GS) accept_kernel(
         for (int k = 0; k < kBatch; ++k) run += v[k];
       }
     }
-    // fp64 scan of the slice sums over the group
-    double incl = (double)run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    double excl, total;
+    // Position of this slice in the row's cumulative sum: excl (before it) and
+    // total, then whether the crossing u * total falls inside it (gap: how far
+    // past excl the crossing lies).  A warp scans in fp64; a block scans
+    // exact fp32 pairs (hi + lo, ~44 bits: fp64 is scarce on this part) and
+    // one thread forms the crossing in fp64.
+    bool holds;
+    float gap;
+    double total;
     if (GS == 32) {
+      double incl = (double)run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
       total = __shfl_sync(0xffffffffu, incl, 31);
-      excl = incl - (double)run;
+      const double excl = incl - (double)run;
+      const double target = u * total;
+      holds = excl <= target && excl + (double)run > target;
+      gap = (float)(target - excl);
     } else {
-      // warp totals -> one warp scans them -> every thread adds its warp's prefix
+      float ih = run, il = 0.0f;  // inclusive prefix inside the warp, as a pair
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float h2 = __shfl_up_sync(0xffffffffu, ih, o), l2 = __shfl_up_sync(0xffffffffu, il, o);
+        if (lane >= o) pair_add(ih, il, h2, l2);
+      }
+      float eh = __shfl_up_sync(0xffffffffu, ih, 1), el = __shfl_up_sync(0xffffffffu, il, 1);
+      if (lane == 0) eh = el = 0.0f;  // exclusive prefix inside the warp
       const int warp = threadIdx.x >> 5, nw = GS / 32;
       __syncthreads();
-      if (lane == 31) s_scan[warp] = incl;
+      if (lane == 31) {
+        s_ph[warp] = ih;
+        s_pl[warp] = il;
+      }
       __syncthreads();
       if (warp == 0) {
-        const double v = lane < nw ? s_scan[lane] : 0.0;
-        double wi = v;
+        const float vh = lane < nw ? s_ph[lane] : 0.0f, vl = lane < nw ? s_pl[lane] : 0.0f;
+        float wh = vh, wl = vl;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const double u2 = __shfl_up_sync(0xffffffffu, wi, o);
-          if (lane >= o) wi += u2;
+          const float h2 = __shfl_up_sync(0xffffffffu, wh, o), l2 = __shfl_up_sync(0xffffffffu, wl, o);
+          if (lane >= o) pair_add(wh, wl, h2, l2);
         }
+        float xh = __shfl_up_sync(0xffffffffu, wh, 1), xl = __shfl_up_sync(0xffffffffu, wl, 1);
+        if (lane == 0) xh = xl = 0.0f;
         __syncwarp();
-        if (lane < nw) s_scan[lane] = wi - v;  // exclusive prefix of warp `lane`
-        if (lane == 31) s_total = wi;
+        if (lane < nw) {
+          s_ph[lane] = xh;  // exclusive prefix of warp `lane`
+          s_pl[lane] = xl;
+        }
+        if (lane == 31) {
+          const double tot = (double)wh + (double)wl;
+          const double tgt = u * tot;
+          s_total = tot;
+          s_th = (float)tgt;
+          s_tl = (float)(tgt - (double)(float)tgt);
+        }
       }
       __syncthreads();
       total = s_total;
-      excl = s_scan[warp] + incl - (double)run;
+      float xh = s_ph[warp], xl = s_pl[warp];
+      pair_add(xh, xl, eh, el);  // excl = the warp's prefix + the prefix inside the warp
+      // gap = target - excl, to fp32 rounding of a value below the slice sum
+      gap = ((s_th - xh) + (s_tl - xl));
+      holds = gap >= 0.0f && run > gap;
     }
     if (!(total > 0.0)) {
       if (w.resid) continue;  // p == q: the residual is empty, draw from p_j instead
       break;                  // (not reachable for finite logits)
     }
     // the slice holding the crossing walks it again, in the same order
-    const double target = u * total;
     int found = 0x7fffffff, last = -1;
-    if (excl <= target && excl + (double)run > target) {
+    if (holds) {
       float r2 = 0.0f;
       for (int t = t0; t < t1; ++t) {
         r2 += STAGE ? mine[t - t0] : w(t);
-        if (excl + (double)r2 > target) {
+        if (r2 > gap) {
           found = t;
           break;
         }
