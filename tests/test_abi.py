@@ -106,6 +106,11 @@ def test_host_validation_rejects_before_launch(lib):
               None) == INVALID  # no ids
     assert sv(fake, fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 16, 4, 0.1, fake, null, 0,
               None) == WORKSPACE
+    # tree verify: Q, K, V, seq, parent, B, Hq, Hkv, Lmax, D, T, scale, out, ws, bytes, stream
+    tv = lib.tf_verify_attn_tree
+    assert tv(fake, fake, fake, fake, null, 1, 8, 2, 64, 128, 4, 0.1, fake, fake, big, None) == INVALID  # no tree
+    assert tv(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 17, 0.1, fake, fake, big, None) == UNSUPPORTED
+    assert tv(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 4, 0.1, fake, null, 0, None) == WORKSPACE
     # offloaded verify: Q, K_host, V_host, seq, L_stream, B, Hq, Hkv, Lmax, D, T, scale, out, seg_rows,
     # ws, bytes, stream, copy_stream
     ov = lib.tf_verify_attn_offload
