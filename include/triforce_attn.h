@@ -305,8 +305,10 @@ TF_API tf_status tf_verify_attn_offload(const uint16_t* Q, const uint16_t* K_hos
  *   n_acc [B] int32 (accepted count), next_token [B] int32
  *   out_tokens [B, gamma+1] int32 (nullable): accepted drafts, next token, -1 pad
  * temperature > 0.  gamma >= 0, V >= 1.  Probabilities use fp32 exponentials,
- * fp64 sums and an fp64 ratio test, so a decision can differ from exact
- * arithmetic only when a uniform lies within ~1e-6 of its boundary.
+ * normalisers summed in fp32 then fp64, an fp64 ratio test, and cumulative
+ * sums carried as exact fp32 pairs (fp64 for a warp-sized vocabulary), so a
+ * decision can differ from exact arithmetic only when a uniform lies within
+ * ~1e-6 of its boundary.
  * Workspace: tf_spec_accept_workspace(B, gamma) bytes (per-row normalisers;
  * needs no zeroing).  Two kernel launches.
  */
