@@ -439,13 +439,14 @@ def run_gpu(args):
                               copy_stream=side)
     torch.cuda.synchronize()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(3):
+    off_ms = float("inf")
+    for _ in range(3):  # the fastest of several calls, like the copy it is compared with
+        f0.record(stream)
         tf.tf_verify_attn_offload(Q_all[0], Kh, Vh, seq, L, scale, out=o_off, ws=ws_off, seg_rows=seg_rows,
                                   copy_stream=side)
-    f1.record(stream)
-    torch.cuda.synchronize()
-    off_ms = f0.elapsed_time(f1) / 3
+        f1.record(stream)
+        torch.cuda.synchronize()
+        off_ms = min(off_ms, f0.elapsed_time(f1))
     stage = torch.empty_like(Kc[0])
     stage.copy_(Kh, non_blocking=True)  # warm the copy path
     torch.cuda.synchronize()
@@ -462,7 +463,8 @@ def run_gpu(args):
         "ms": round(off_ms, 4), "GBps": round(off_bytes / (off_ms / 1e3) / 1e9, 1),
         "h2d_copy_GBps": round(off_bytes / (h2d_ms / 1e3) / 1e9, 1),
         "frac_of_h2d_copy": round(h2d_ms / off_ms, 4), "calls": "tf_verify_attn_offload",
-        "timing": "K/V in pinned host memory, 16K-position segments, copies on a second stream"}
+        "timing": "K/V in pinned host memory, 16K-position segments, copies on a second stream; "
+                  "fastest of 3 calls and of 4 plain copies"}
     kernels["chunk_means_prefill_1layer"] = {"ms": round(means_ms, 4),
                                              "GBps": round(means_bytes / (means_ms / 1e3) / 1e9, 1)}
     ver_ms = statistics.mean(per_kind["verify"])

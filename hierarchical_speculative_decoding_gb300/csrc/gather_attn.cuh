@@ -29,6 +29,14 @@ struct GatherParams {
   int cmerge;        // 1: the splits of a (unit, group) form a cluster and merge through DSMEM
 };
 
+// The retrieval drafter's decode attention on the tensor cores: the gathered
+// verify kernel (verify_attn.cu) with one query token per head and no
+// candidate rows.  Arguments validated by the caller.
+size_t sparse_decode_umma_ws(int B, int Hq, int Hkv, int kc);
+tf_status sparse_decode_umma(const uint16_t* q, const uint16_t* K, const uint16_t* V, const int32_t* seq_lens,
+                             const int32_t* idx, const int32_t* n_sel, int B, int Hq, int Hkv, int Lmax, int kc,
+                             float scale, float* out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 int gather_nq(int rows);  // query rows per CTA for `rows` rows per unit
 size_t gather_workspace(int units, int rows, int P_max);
 tf_status gather_launch(int mode, GatherParams p, int units, int rows, int P_max, void* ws, size_t ws_bytes,

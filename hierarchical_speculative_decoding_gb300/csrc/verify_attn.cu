@@ -85,6 +85,7 @@ struct VerifyParams {
   const int32_t* idx;    // [B * Hkv, kc] selected chunk ids
   const int32_t* n_sel;  // [B * Hkv]
   int kc, tiles_per;     // tiles per split
+  int no_cand;           // 1: no candidate rows, every key comes from the selection (decode)
   int cmerge;            // 1: the splits of a unit form a cluster and merge through DSMEM
   // segment mode (contiguous only): the K/V buffers hold positions [pos0,
   // pos0 + Lmax) of caches Ltot long; with part_out set, every row's state
@@ -320,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   // key range of this split: whole tiles (contiguous), or tiles of the piece
   // list (gathered: selected chunks, then the candidate rows)
   int k0 = 0, k1 = 0, ntiles = 0;
-  const int cstart = max(0, L - p.T);  // first candidate position
+  const int cstart = p.no_cand ? L : max(0, L - p.T);  // first candidate position
   if (!GATHER) {
     // rows of the buffer (positions pos0 + row) that the sequence holds
     const int nloc = min(max(L - p.pos0, 0), p.Lmax);
@@ -1136,23 +1137,18 @@ extern "C" size_t tf_sparse_verify_attn_workspace(int B, int Hq, int Hkv, int kc
   return tf::sparse_verify_ws(B * Hkv, (Hq / Hkv) * T, kc);
 }
 
-extern "C" tf_status tf_sparse_verify_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
-                                           const int32_t* seq_lens, const int32_t* idx, const int32_t* n_sel, int B,
-                                           int Hq, int Hkv, int Lmax, int D, int chunk, int kc, int T, float scale,
-                                           float* out, void* ws, size_t ws_bytes, tf_stream_t stream) {
-  using namespace tf;
-  if (!Q || !K || !V || !seq_lens || !idx || !n_sel || !out) return TF_ERR_INVALID_ARG;
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || Hq % Hkv || T < 1 || kc <= 0) return TF_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return TF_ERR_INVALID_ARG;
-  if (D != kHeadDim || chunk != kChunk || T > 16) return TF_ERR_UNSUPPORTED;
-  if (B == 0 || Lmax == 0) return TF_OK;
+namespace tf {
+
+// The gathered verify over the selected chunks for T query rows per head
+// (arguments validated): with candidates (level-1 verification) or, no_cand,
+// the decode attention of the retrieval drafter (T = 1, every key from the
+// selection).
+tf_status sparse_gather(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* seq_lens,
+                        const int32_t* idx, const int32_t* n_sel, int B, int Hq, int Hkv, int Lmax, int kc, int T,
+                        float scale, float* out, void* ws, cudaStream_t stream, int no_cand) {
   const long long rows_total = (long long)B * Hkv * Lmax;
-  if (rows_total >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
-  const size_t need = sparse_verify_ws(B * Hkv, (Hq / Hkv) * T, kc);
-  if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
   CUtensorMap mk, mv;
   if (!make_piece_map(&mk, K, rows_total) || !make_piece_map(&mv, V, rows_total)) return TF_ERR_CUDA;
-
   VerifyParams p{};
   const int rows_all = (Hq / Hkv) * T;
   p.Q = Q;
@@ -1167,6 +1163,7 @@ extern "C" tf_status tf_sparse_verify_attn(const uint16_t* Q, const uint16_t* K,
   p.idx = idx;
   p.n_sel = n_sel;
   p.kc = kc;
+  p.no_cand = no_cand;
   const int tiles = sparse_verify_tiles(kc);
   p.splits_cap = tiles;
   const int ug = B * Hkv * p.ngroups;
@@ -1183,4 +1180,34 @@ extern "C" tf_status tf_sparse_verify_attn(const uint16_t* Q, const uint16_t* K,
   dim3 grid(p.splits, ug);
   const int rows_max = rows_all < kMaxRows ? rows_all : kMaxRows;
   return launch_rows<true>(rows_max, mk, mv, p, grid, stream);
+}
+
+size_t sparse_decode_umma_ws(int B, int Hq, int Hkv, int kc) { return sparse_verify_ws(B * Hkv, Hq / Hkv, kc); }
+
+tf_status sparse_decode_umma(const uint16_t* q, const uint16_t* K, const uint16_t* V, const int32_t* seq_lens,
+                             const int32_t* idx, const int32_t* n_sel, int B, int Hq, int Hkv, int Lmax, int kc,
+                             float scale, float* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if ((long long)B * Hkv * Lmax >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < sparse_decode_umma_ws(B, Hq, Hkv, kc) || !aligned16(ws)) return TF_ERR_WORKSPACE;
+  return sparse_gather(q, K, V, seq_lens, idx, n_sel, B, Hq, Hkv, Lmax, kc, 1, scale, out, ws, stream, 1);
+}
+
+}  // namespace tf
+
+extern "C" tf_status tf_sparse_verify_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                                           const int32_t* seq_lens, const int32_t* idx, const int32_t* n_sel, int B,
+                                           int Hq, int Hkv, int Lmax, int D, int chunk, int kc, int T, float scale,
+                                           float* out, void* ws, size_t ws_bytes, tf_stream_t stream) {
+  using namespace tf;
+  if (!Q || !K || !V || !seq_lens || !idx || !n_sel || !out) return TF_ERR_INVALID_ARG;
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || Hq % Hkv || T < 1 || kc <= 0) return TF_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return TF_ERR_INVALID_ARG;
+  if (D != kHeadDim || chunk != kChunk || T > 16) return TF_ERR_UNSUPPORTED;
+  if (B == 0 || Lmax == 0) return TF_OK;
+  const long long rows_total = (long long)B * Hkv * Lmax;
+  if (rows_total >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
+  const size_t need = sparse_verify_ws(B * Hkv, (Hq / Hkv) * T, kc);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
+
+  return sparse_gather(Q, K, V, seq_lens, idx, n_sel, B, Hq, Hkv, Lmax, kc, T, scale, out, ws, stream, 0);
 }
