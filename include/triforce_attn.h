@@ -233,8 +233,8 @@ TF_API tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const uint
                          void* ws, size_t ws_bytes, tf_stream_t stream);
 
 /*
- * a7 over a candidate tree (SURVEY's NEXT row 2; "TriForce: Hierarchical
- * Speculative Decoding for LLMs", "The Three Forces of TriForce": Force 2
+ * a7 over a candidate tree ("TriForce: Hierarchical Speculative Decoding for
+ * LLMs", "The Three Forces of TriForce": Force 2
  * arranges the surviving candidates as a tree and Force 3 checks the whole
  * tree in one forward pass with tree attention).  The T candidates sit at
  * positions L-T .. L-1 as for tf_verify_attn; parent[b*T + j] (device int32,
