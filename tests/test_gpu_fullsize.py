@@ -4,7 +4,8 @@ units checked one by one against the float64 oracle.
 Same launch configuration as the benchmark: the whole layer (every unit) goes
 through each call; the oracle recomputes a few units, always including the
 first and last KV head and, for ragged batches, the longest and the shortest
-sequence.  Tolerances as in test_gpu_parity.py.
+sequence.  The offloaded verify streams the same cache from pinned host
+memory in the benchmark's 16K-position segments.  Tolerances as in test_gpu_parity.py.
 """
 
 import numpy as np
@@ -51,13 +52,23 @@ def test_full_size_layer(cuda_lib, w):
     wi = cuda_lib.tf_stream_window_attn(q, K, V, seq, w.n_sink, w.window, scale)
     ve = cuda_lib.tf_verify_attn(Q, K, V, seq, scale)
     fidx, fnsel, fsp = cuda_lib.tf_retrieval_draft_attn(q, M, K, V, seq, w.kc, scale)
+    sv = cuda_lib.tf_sparse_verify_attn(Q, K, V, seq, idx, nsel, scale)
+    # offloaded verify as timed: pinned host K/V, 16K-position segments, copies on a side stream
+    K_host = torch.empty(K.shape, dtype=K.dtype, pin_memory=True).copy_(K)
+    V_host = torch.empty(V.shape, dtype=V.dtype, pin_memory=True).copy_(V)
+    off = cuda_lib.tf_verify_attn_offload(Q, K_host, V_host, seq, int(seq_cpu.max()), scale,
+                                          seg_rows=min(16384, w.L), copy_stream=torch.cuda.Stream())
     torch.cuda.synchronize()
+    del K_host, V_host
+    # every unit of the offloaded verify against the resident one (both oracle-checked on the samples)
+    assert (off - ve).abs().max().item() <= ATOL
     # the fused retrieval drafter selects exactly what the top-k call selects
     assert np.array_equal(fidx.cpu().numpy(), idx.cpu().numpy())
     assert np.array_equal(fnsel.cpu().numpy(), nsel.cpu().numpy())
     fsp_h = fsp.cpu().double().numpy()
     M_h, idx_h, nsel_h = bits(M), idx.cpu().numpy(), nsel.cpu().numpy()
     sp_h, wi_h, ve_h = sp.cpu().double().numpy(), wi.cpu().double().numpy(), ve.cpu().double().numpy()
+    sv_h, off_h = sv.cpu().double().numpy(), off.cpu().double().numpy()
     q_h, Q_h = bits(q), bits(Q)
     G = w.G
     near_ties = 0
@@ -88,6 +99,11 @@ def test_full_size_layer(cuda_lib, w):
         # a7
         ve_o = O.verify_attn(Q_h[b : b + 1, g * G : (g + 1) * G], Kb, Vb, sl, scale)
         assert np.abs(ve_h[b, g * G : (g + 1) * G] - ve_o[0]).max() <= ATOL
+        assert np.abs(off_h[b, g * G : (g + 1) * G] - ve_o[0]).max() <= ATOL
+        # level-1 verify over the GPU's own selection
+        sv_o = O.sparse_verify_attn(Q_h[b : b + 1, g * G : (g + 1) * G], Kb, Vb, sl,
+                                    idx_h[b : b + 1, g : g + 1], nsel_h[b : b + 1, g : g + 1], w.chunk, scale)
+        assert np.abs(sv_h[b, g * G : (g + 1) * G] - sv_o[0]).max() <= ATOL
     assert near_ties <= 1
 
 
