@@ -387,14 +387,13 @@ size_t gather_workspace(int units, int rows, int P_max) {
 
 template <int NQ, int MODE>
 static int configure() {
-  static int per_sm = 0;
-  if (per_sm == 0) {
+  static DeviceCache per_sm;  // resident CTAs per SM on each device, 0 if the setup failed
+  return per_sm.get([] {
     if (cudaFuncSetAttribute(gather_attn_kernel<NQ, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kGatherSmem) != cudaSuccess)
       return 0;
-    per_sm = occupancy_blocks((const void*)gather_attn_kernel<NQ, MODE>, kGatherThreads, kGatherSmem);
-  }
-  return per_sm;
+    return occupancy_blocks((const void*)gather_attn_kernel<NQ, MODE>, kGatherThreads, kGatherSmem);
+  });
 }
 
 template <int NQ, int MODE>

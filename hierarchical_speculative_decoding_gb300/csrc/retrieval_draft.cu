@@ -496,15 +496,14 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
 
 template <int NQ>
 tf_status launch_draft(const DraftParams& p, int units, int Cmax, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(retrieval_draft_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)draft_smem(kMaxSliceKeys)) != cudaSuccess ||
-        cudaFuncSetAttribute(retrieval_draft_kernel<NQ>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess)
-      return TF_ERR_CUDA;
-    configured = true;
-  }
+  static DeviceCache configured;
+  if (!configured.get([] {
+        return cudaFuncSetAttribute(retrieval_draft_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)draft_smem(kMaxSliceKeys)) == cudaSuccess &&
+               cudaFuncSetAttribute(retrieval_draft_kernel<NQ>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                    1) == cudaSuccess;
+      }))
+    return TF_ERR_CUDA;
   // Cluster size: the largest S <= 16 (at most one CTA per 64 chunks) for
   // which every unit's cluster is resident at once, as the occupancy query for
   // that cluster shape and slice size reports; at least enough CTAs that every

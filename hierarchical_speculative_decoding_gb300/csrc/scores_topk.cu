@@ -132,13 +132,12 @@ extern "C" tf_status tf_chunk_scores_topk(const uint16_t* q, const uint16_t* M, 
   if (units > 65535) return TF_ERR_UNSUPPORTED;
   const int Cmax = (Lmax + kChunk - 1) / kChunk;
 
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(scores_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxSliceKeys * (int)sizeof(uint32_t)) != cudaSuccess)
-      return TF_ERR_CUDA;
-    configured = true;
-  }
+  static DeviceCache configured;
+  if (!configured.get([] {
+        return cudaFuncSetAttribute(scores_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kMaxSliceKeys * (int)sizeof(uint32_t)) == cudaSuccess;
+      }))
+    return TF_ERR_CUDA;
   // Cluster size: the largest S <= 8 (at most one CTA per 64 chunks) whose
   // units x S CTAs fit one wave at the occupancy their slice size allows; at
   // least enough CTAs that every slice fits on chip.

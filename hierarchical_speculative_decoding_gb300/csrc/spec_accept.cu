@@ -441,13 +441,12 @@ extern "C" tf_status tf_spec_accept(const float* tgt_logits, const float* drf_lo
     const int seg = (V + kBlockSeq - 1) / kBlockSeq;
     const size_t stage_bytes = (size_t)kBlockSeq * (seg + 1) * sizeof(float);
     if (e == cudaSuccess && stage_bytes <= kMaxStageBytes) {
-      static bool configured = false;
-      if (!configured) {
-        if (cudaFuncSetAttribute(accept_kernel<kBlockSeq, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kMaxStageBytes) != cudaSuccess)
-          return TF_ERR_CUDA;
-        configured = true;
-      }
+      static DeviceCache configured;
+      if (!configured.get([] {
+            return cudaFuncSetAttribute(accept_kernel<kBlockSeq, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kMaxStageBytes) == cudaSuccess;
+          }))
+        return TF_ERR_CUDA;
       e = launch_pdl(accept_kernel<kBlockSeq, true>, dim3(B), dim3(kBlockSeq), stage_bytes, stream, tgt_logits,
                      drf_logits, drf_tokens, u_acc, u_res, B, gamma, V, inv_t, inv_t_d, nws, n_acc, next_token,
                      out_tokens);

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "triforce_attn.h"
 
 namespace tf {
@@ -22,6 +24,32 @@ inline int num_sms() {
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
   return n;
 }
+
+// A kernel's one-time setup, kept per device: function attributes (the
+// dynamic shared-memory limit, non-portable cluster sizes) and the occupancy
+// they allow apply to the current device only.  get() runs `setup` on the
+// first call on each device and keeps its result when positive; a failed
+// setup (0) is not kept, so the next call tries again.  Threads that race on
+// a first call may each run `setup`; it only sets attributes and queries
+// occupancy, so they store the same value, and a thread that reads a stored
+// value sees the attributes already set (release/acquire).
+class DeviceCache {
+ public:
+  static constexpr int kSlots = 64;  // device ordinals served
+  template <class F>
+  int get(F&& setup) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSlots) return 0;
+    int v = vals_[dev].load(std::memory_order_acquire);
+    if (v > 0) return v;
+    v = setup();
+    if (v > 0) vals_[dev].store(v, std::memory_order_release);
+    return v;
+  }
+
+ private:
+  std::atomic<int> vals_[kSlots]{};
+};
 
 // Resident CTAs per SM for a kernel (at least 1).
 inline int occupancy_blocks(const void* fn, int threads, size_t dyn_smem) {

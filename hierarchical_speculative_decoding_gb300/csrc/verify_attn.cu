@@ -847,13 +847,12 @@ size_t verify_ws(int units, int rows_all, int Lmax) {
 template <int NR, bool GATHER, bool TREE>
 tf_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParams& p, dim3 grid,
                  cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(verify_umma_kernel<NR, GATHER, TREE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<NR>::kDynamic) != cudaSuccess)
-      return TF_ERR_CUDA;
-    configured = true;
-  }
+  static DeviceCache configured;
+  if (!configured.get([] {
+        return cudaFuncSetAttribute(verify_umma_kernel<NR, GATHER, TREE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Smem<NR>::kDynamic) == cudaSuccess;
+      }))
+    return TF_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
