@@ -34,6 +34,11 @@
  *     once after allocation (cudaMemset); every call leaves its counters at
  *     zero again, so one buffer serves any sequence of calls that are ordered
  *     on the GPU.  Calls that may run concurrently need separate workspaces.
+ *   - Devices: every call runs on the caller's current CUDA device.  Host
+ *     threads may call in concurrently, on one device or several; kernel
+ *     attributes (shared-memory limits, cluster sizes) are set on each
+ *     device's first call, for device ordinals below 64 (higher ordinals get
+ *     an error status from the calls that need them).
  */
 #ifndef TRIFORCE_ATTN_H
 #define TRIFORCE_ATTN_H
