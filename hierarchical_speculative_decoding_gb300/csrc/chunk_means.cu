@@ -10,7 +10,7 @@
 // dims) of one chunk: a chunk is 8 rows x 256 B = 2 KiB contiguous, so 16
 // threads cover it and every load instruction of a half-warp reads 256
 // contiguous bytes.  Each thread keeps all 8 row loads of its next item in
-// flight while it sums the current one (the exact sums cost ~700 instructions
+// flight while it sums the current one (the exact sums cost ~600 instructions
 // per 128 bytes, so without the overlap the stream waits on the arithmetic).
 // The sum of the rows is carried as an unevaluated fp32 pair (TwoSum), so the
 // mean is exact before its single rounding to bf16.
@@ -48,21 +48,42 @@ struct Item {
   int n;
 };
 
-__device__ __forceinline__ Item item_at(long long item, const uint16_t* K, const int32_t* seq_lens, int Hkv, int Lmax,
-                                        int Cmax, int c_begin, int n_chunks, uint16_t* M) {
-  const int slice = (int)(item & 15);
-  const long long rest = item >> 4;
-  const int c = c_begin + (int)(rest % n_chunks);
-  const long long bg = rest / n_chunks;
-  const int b = (int)(bg / Hkv);
-  const int L = clamp_len(seq_lens[b], Lmax);
+// A thread's walk over the items.  The grid stride is a multiple of 16 items,
+// so a thread keeps its column slice and steps through (b, g, c) by a fixed
+// (db, dg, dc) with carries: no integer division per item.
+struct Walk {
+  int b, g, c;     // sequence, KV head, chunk (from c_begin)
+  int db, dg, dc;  // the step per grid stride
+  int slice;
+};
+
+__device__ __forceinline__ Item item_at(const Walk& w, const uint16_t* K, const int32_t* seq_lens, int Hkv,
+                                        int Lmax, int Cmax, int c_begin, uint16_t* M) {
+  const int c = c_begin + w.c;
+  const size_t bg = (size_t)w.b * Hkv + w.g;
+  const int L = clamp_len(seq_lens[w.b], Lmax);
   int n = L - c * kChunk;
   n = n < 0 ? 0 : (n > kChunk ? kChunk : n);
   Item it;
-  it.src = K + ((size_t)bg * Lmax + (size_t)c * kChunk) * kHeadDim + slice * 8;
-  it.dst = M + ((size_t)bg * Cmax + c) * kHeadDim + slice * 8;
+  it.src = K + (bg * Lmax + (size_t)c * kChunk) * kHeadDim + w.slice * 8;
+  it.dst = M + (bg * Cmax + c) * kHeadDim + w.slice * 8;
   it.n = n;
   return it;
+}
+
+__device__ __forceinline__ void advance(Walk& w, int Hkv, int n_chunks) {
+  w.c += w.dc;
+  int carry = 0;
+  if (w.c >= n_chunks) {
+    w.c -= n_chunks;
+    carry = 1;
+  }
+  w.g += w.dg + carry;  // < 2 Hkv
+  w.b += w.db;
+  if (w.g >= Hkv) {
+    w.g -= Hkv;
+    w.b += 1;
+  }
 }
 
 __device__ __forceinline__ void load_rows(const Item& it, uint4 (&rows)[kChunk]) {
@@ -127,24 +148,34 @@ __device__ __forceinline__ void mean_store(const Item& it, const uint4 (&rows)[k
 // are issued before the current item's sums, so the DRAM round trip overlaps
 // the arithmetic.
 __global__ void __launch_bounds__(256) chunk_means_kernel(const uint16_t* __restrict__ K,
-                                                          const int32_t* __restrict__ seq_lens,
+                                                          const int32_t* __restrict__ seq_lens, int B,
                                                           int Hkv, int Lmax, int c_begin, int n_chunks,
-                                                          long long total, uint16_t* __restrict__ M) {
+                                                          uint16_t* __restrict__ M) {
   const int Cmax = (Lmax + kChunk - 1) / kChunk;
   pdl_wait();
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (item >= total) return;
-  Item cur = item_at(item, K, seq_lens, Hkv, Lmax, Cmax, c_begin, n_chunks, M);
+  const long long item0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long step = (long long)gridDim.x * blockDim.x / 16;  // chunks per grid stride
+  const long long ci = item0 / 16;
+  Walk w;
+  w.slice = (int)(item0 % 16);
+  w.c = (int)(ci % n_chunks);
+  w.g = (int)(ci / n_chunks % Hkv);
+  const long long b0 = ci / n_chunks / Hkv;
+  if (b0 >= B) return;
+  w.b = (int)b0;
+  w.dc = (int)(step % n_chunks);
+  w.dg = (int)(step / n_chunks % Hkv);
+  w.db = (int)(step / n_chunks / Hkv);
+  Item cur = item_at(w, K, seq_lens, Hkv, Lmax, Cmax, c_begin, M);
   uint4 rows[kChunk];
   load_rows(cur, rows);
   while (true) {
-    const long long nxt_item = item + stride;
-    const bool more = nxt_item < total;
+    advance(w, Hkv, n_chunks);
+    const bool more = w.b < B;
     Item nxt = cur;
     uint4 next_rows[kChunk];
     if (more) {
-      nxt = item_at(nxt_item, K, seq_lens, Hkv, Lmax, Cmax, c_begin, n_chunks, M);
+      nxt = item_at(w, K, seq_lens, Hkv, Lmax, Cmax, c_begin, M);
       load_rows(nxt, next_rows);
     }
     mean_store(cur, rows);
@@ -152,7 +183,6 @@ __global__ void __launch_bounds__(256) chunk_means_kernel(const uint16_t* __rest
 #pragma unroll
     for (int r = 0; r < kChunk; ++r) rows[r] = next_rows[r];
     cur = nxt;
-    item = nxt_item;
   }
 }
 
@@ -171,12 +201,13 @@ extern "C" tf_status tf_build_chunk_means(const uint16_t* K, const int32_t* seq_
   const int n_chunks = c_end - c_begin;
   const long long total = (long long)B * Hkv * n_chunks * 16;
   if (total == 0) return TF_OK;
-  const int threads = 256;
+  constexpr int threads = 256;
+  static_assert(threads % 16 == 0, "the grid stride must keep each thread's column slice");
   long long blocks = (total + threads - 1) / threads;
   const long long cap = (long long)num_sms() * 8;
   if (blocks > cap) blocks = cap;
-  if (launch_pdl(chunk_means_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, K, seq_lens, Hkv, Lmax,
-                 c_begin, n_chunks, total, M) != cudaSuccess)
+  if (launch_pdl(chunk_means_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, K, seq_lens, B, Hkv, Lmax,
+                 c_begin, n_chunks, M) != cudaSuccess)
     return TF_ERR_CUDA;
   return launch_status();
 }
