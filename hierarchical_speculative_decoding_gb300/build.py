@@ -2,12 +2,15 @@
 
 Each .cu under csrc/ compiles to an object in parallel, then one shared
 library is linked next to this file.  Rebuilds only when a source or header
-is newer than the library.
+is newer than the library.  Processes that build at the same time (one per
+rank under torchrun) take turns on a file lock; whoever waited finds the
+library fresh and returns it without compiling again.
 """
 
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import glob
 import os
 import shutil
@@ -19,6 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtriforce_attn.so")
+LOCK = os.path.join(BUILD, ".build.lock")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -51,6 +55,17 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    with open(LOCK, "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)  # one build at a time, across processes
+        try:
+            if not force and up_to_date():  # built by another process while this one waited
+                return LIB
+            return _compile_and_link(verbose, extra)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _compile_and_link(verbose: bool, extra: list[str] | None) -> str:
     cc = nvcc()
     extra = extra or []
 
@@ -66,9 +81,11 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + ".tmp"
+    tmp = f"{LIB}.{os.getpid()}.tmp"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
+        if os.path.exists(tmp):
+            os.remove(tmp)
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
     return LIB
