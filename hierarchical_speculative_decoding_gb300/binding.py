@@ -26,6 +26,7 @@ _S = _c.c_size_t
 
 _SIGS = {
     "tf_status_string": (_c.c_char_p, [_I]),
+    "tf_check_status": (_I, [_P, _S, _P]),
     "tf_abi_version": (_I, []),
     "tf_build_chunk_means": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "tf_chunk_scores_topk_workspace": (_S, [_I, _I, _I, _I]),
@@ -109,6 +110,21 @@ def _need(t, dtype, name, ndim=None):
 def workspace(nbytes: int, device) -> torch.Tensor:
     """A zero-filled scratch buffer (the library requires zeroed workspace once)."""
     return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+TF_ERR_DEVICE_DATA = 6
+
+
+def tf_check_status(ws, stream=None) -> int:
+    """Device-side status word of a verify workspace (tf_verify_attn, its tree
+    and offloaded forms, tf_sparse_verify_attn).  Waits for the stream; returns
+    0, or TF_ERR_DEVICE_DATA after zeroing the whole workspace again (the
+    outputs computed with it since the last check are invalid)."""
+    _need(ws, torch.uint8, "ws")
+    status = load().tf_check_status(_ptr(ws), ws.numel(), _stream(stream))
+    if status not in (0, TF_ERR_DEVICE_DATA):
+        _check(status, "tf_check_status")
+    return status
 
 
 def _ws(ws, need, device):

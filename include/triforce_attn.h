@@ -64,7 +64,8 @@ typedef enum tf_status {
   TF_ERR_UNSUPPORTED = 2,  /* valid but unsupported shape (D != 128, chunk != 8, ...) */
   TF_ERR_WORKSPACE = 3,    /* ws missing or ws_bytes below the *_workspace() size */
   TF_ERR_CUDA = 4,         /* a kernel launch failed (cudaGetLastError) */
-  TF_ERR_SCRATCH_LIMIT = 5 /* the no-allocation entry point's static scratch is too small */
+  TF_ERR_SCRATCH_LIMIT = 5, /* the no-allocation entry point's static scratch is too small */
+  TF_ERR_DEVICE_DATA = 6   /* a kernel flagged an error on the device (tf_check_status) */
 } tf_status;
 
 /* Static, human-readable text for a status code. */
@@ -72,6 +73,19 @@ TF_API const char* tf_status_string(tf_status s);
 
 /* Library ABI version (major * 100 + minor). */
 TF_API int tf_abi_version(void);
+
+/* Device-side status of a workspace that starts with a status word: the
+ * workspaces of tf_verify_attn, tf_verify_attn_tree, tf_sparse_verify_attn
+ * and tf_verify_attn_offload.  Their kernels set the word when a pipeline wait
+ * times out (only a hardware fault can cause that), and the outputs of every
+ * call that used the workspace since then are invalid.
+ * Waits for `stream` (work queued on it before this call completes first) and
+ * reads the word.  Zero: returns TF_OK.  Nonzero: zeroes all ws_bytes of the
+ * workspace again, in `stream` order, so the workspace can be reused, and
+ * returns TF_ERR_DEVICE_DATA.  ws is device memory of ws_bytes >= 4 bytes
+ * (TF_ERR_INVALID_ARG otherwise, nothing read); TF_ERR_CUDA if the copy, the
+ * clearing or the wait fails. */
+TF_API tf_status tf_check_status(void* ws, size_t ws_bytes, tf_stream_t stream);
 
 /*
  * a1 -- chunk-mean retrieval index.

@@ -39,8 +39,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.tf_abi_version() == 100
-    for s in range(5):
+    assert lib.tf_abi_version() == 101
+    for s in range(7):
         assert len(lib.tf_status_string(s)) > 0
     assert lib.tf_status_string(99) == b"unknown status"
 
@@ -125,6 +125,9 @@ def test_host_validation_rejects_before_launch(lib):
                               None) == INVALID
     assert lib.tf_spec_accept(fake, fake, fake, fake, fake, 1, 4, 100, 1.0, fake, fake, null, null, 0,
                               None) == WORKSPACE
+    # the status query reads nothing without a workspace of at least one word
+    assert lib.tf_check_status(null, 4096, None) == INVALID
+    assert lib.tf_check_status(fake, 3, None) == INVALID
 
 
 def test_binding_rejects_cpu_tensors():
