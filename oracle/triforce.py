@@ -444,6 +444,81 @@ def sparse_verify_attn(Q_bits, K_bits, V_bits, seq_lens, idx, n_sel, chunk, scal
 
 
 # ---------------------------------------------------------------------------
+# resident caches beside an offloaded full cache
+# ---------------------------------------------------------------------------
+
+
+def compact_retrieval_cache(K_bits, V_bits, seq_lens, idx, n_sel, chunk, kc):
+    """The retrieval drafter's cache as a buffer of its own.
+
+    "TriForce: Lossless Acceleration of Long Sequence Generation with
+    Hierarchical Speculative Decoding", "Abstract (arXiv)": the retrieval-sparse
+    cache is the middle draft level, and the offloading setting keeps the full
+    cache in host memory; project summary, "How It Works": the KV cache can be
+    offloaded to CPU memory.  Reading: when the full cache is offloaded, the
+    drafter keeps a copy of the rows it attends to on the GPU.  For each
+    (b, g) those are the rows of sparse_positions (valid tokens of the selected
+    chunks, list order, invalid ids skipped), packed from row 0 of a
+    [B, Hkv, kc * chunk, D] buffer; rows past the packed count are zero.
+    Returns (Kc_bits, Vc_bits, lens) with lens [B, Hkv] the packed counts.
+    """
+    B, Hkv, Lmax, D = K_bits.shape
+    cap = kc * chunk
+    Kc = np.zeros((B, Hkv, cap, D), dtype=np.uint16)
+    Vc = np.zeros((B, Hkv, cap, D), dtype=np.uint16)
+    lens = np.zeros((B, Hkv), dtype=np.int64)
+    for b in range(B):
+        L = valid_len(seq_lens[b], Lmax)
+        for g in range(Hkv):
+            pos = sparse_positions(idx[b, g], min(int(n_sel[b, g]), kc), L, chunk, Lmax)
+            Kc[b, g, : len(pos)] = K_bits[b, g, pos]
+            Vc[b, g, : len(pos)] = V_bits[b, g, pos]
+            lens[b, g] = len(pos)
+    return Kc, Vc, lens
+
+
+def window_cache(K_bits, V_bits, seq_lens, n_sink, window):
+    """The streaming drafter's cache as a buffer of its own: for each (b, g) the
+    rows of window_positions packed from row 0 of a [B, Hkv, n_sink + window, D]
+    buffer (blog page, "The Three Forces of TriForce", Force 1: the sinks and
+    the recent window are all that drafter reads, so they can stay on the GPU
+    when the full cache is offloaded).  Returns (Kw_bits, Vw_bits, lens [B])."""
+    B, Hkv, Lmax, D = K_bits.shape
+    cap = n_sink + window
+    Kw = np.zeros((B, Hkv, cap, D), dtype=np.uint16)
+    Vw = np.zeros((B, Hkv, cap, D), dtype=np.uint16)
+    lens = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        pos = window_positions(valid_len(seq_lens[b], Lmax), n_sink, window)
+        Kw[b, :, : len(pos)] = K_bits[b][:, pos]
+        Vw[b, :, : len(pos)] = V_bits[b][:, pos]
+        lens[b] = len(pos)
+    return Kw, Vw, lens
+
+
+def prefix_decode_attn(q_bits, Kc_bits, Vc_bits, lens, scale):
+    """Decode attention over a packed cache: query head h of KV group g attends
+    to rows [0, lens[b, g]) of its unit (lens [B, Hkv], or [B] for one length
+    per sequence).  Returns float64 [B, Hq, D]."""
+    q = bf16_to_f64(q_bits)
+    K = bf16_to_f64(Kc_bits)
+    V = bf16_to_f64(Vc_bits)
+    B, Hq, D = q.shape
+    Hkv = K.shape[1]
+    G = Hq // Hkv
+    lens = np.asarray(lens)
+    if lens.ndim == 1:
+        lens = np.repeat(lens[:, None], Hkv, axis=1)
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            n = int(lens[b, g])
+            out[b, h] = attend(q[b, h], K[b, g, :n], V[b, g, :n], scale)[0]
+    return out
+
+
+# ---------------------------------------------------------------------------
 # a8: lossless accept / resample
 # ---------------------------------------------------------------------------
 
