@@ -95,3 +95,28 @@ def test_packed_window_rows_by_hand():
     assert _row_ids(Kw[0, 0], 5) == [0, 1, 9, 10, 11]
     Kw, _, lens = O.window_cache(K, K, np.array([4]), 2, 3)  # the context fits: every row once
     assert lens.tolist() == [4] and _row_ids(Kw[0, 0], 4) == [0, 1, 2, 3]
+
+
+def test_packed_retrieval_cache_as_one_sequence_per_unit():
+    # Viewing each (b, g) unit of the packed buffer as a sequence of its own
+    # (one KV head, its G query heads, length = its packed count) turns the
+    # per-unit prefix attention into the sparse call over consecutive chunk ids.
+    B, Hq, Hkv, Lmax, D, chunk, kc = 2, 8, 4, 45, 128, 8, 3
+    G = Hq // Hkv
+    q = _bits(_rand_bf16((B, Hq, D), 7))
+    K = _bits(_rand_bf16((B, Hkv, Lmax, D), 8, 2.0))
+    V = _bits(_rand_bf16((B, Hkv, Lmax, D), 9))
+    seq = np.array([45, 19])
+    idx = np.array([[[5, 1, 0], [0, 2, 4], [3, 3, -1], [1, 2, 5]],
+                    [[2, 0, 1], [1, 0, 7], [0, 0, 0], [2, 1, 0]]])
+    n_sel = np.array([[3, 3, 2, 3], [3, 3, 0, 3]])
+    scale = D ** -0.5
+    Kc, Vc, lens = O.compact_retrieval_cache(K, V, seq, idx, n_sel, chunk, kc)
+    assert any(int(n) % chunk for n in lens.ravel())  # some unit ends in a partial chunk
+    units = B * Hkv
+    ident = np.tile(np.arange(kc), (units, 1, 1))
+    n_ident = -(-lens.reshape(units, 1) // chunk)
+    got = O.sparse_decode_attn(q.reshape(units, G, D), Kc.reshape(units, 1, kc * chunk, D),
+                               Vc.reshape(units, 1, kc * chunk, D), lens.reshape(units), ident, n_ident, chunk, scale)
+    want = O.sparse_decode_attn(q, K, V, seq, idx, n_sel, chunk, scale)
+    np.testing.assert_allclose(got.reshape(B, Hq, D), want, rtol=1e-13, atol=1e-13)
