@@ -44,6 +44,7 @@ _SIGS = {
     "tf_verify_attn_tree": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_verify_attn_offload_workspace": (_S, [_I, _I, _I, _I, _I, _I]),
     "tf_verify_attn_offload": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _S, _P, _P]),
+    "tf_pack_retrieval_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tf_spec_accept_workspace": (_S, [_I, _I]),
     "tf_spec_accept": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _S, _P]),
 }
@@ -201,6 +202,50 @@ def tf_sparse_decode_attn(q, K, V, seq_lens, idx, n_sel, scale, out=None, ws=Non
                                         Hkv, Lmax, D, chunk, kc, float(scale), _ptr(out), _ptr(ws), nbytes,
                                         _stream(stream)), "tf_sparse_decode_attn")
     return out
+
+
+def tf_pack_retrieval_cache(K, V, seq_lens, idx, n_sel, Kc=None, Vc=None, lens=None, n_chunks=None, chunk=8,
+                            stream=None):
+    """The retrieval drafter's rows packed into a resident buffer: for each
+    (b, g) the valid tokens of the chunks idx[b, g, :n_sel[b, g]], in list
+    order, from row 0 of Kc, Vc [B, Hkv, kc * chunk, D].  K and V may be CUDA
+    tensors or pinned CPU tensors (read over the host link).  Returns
+    (Kc, Vc, lens [B*Hkv], n_chunks [B*Hkv])."""
+    for t, name in ((K, "K"), (V, "V")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.dim() != 4:
+            raise TypeError(f"{name} must be a 4-dim torch.bfloat16 tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if not (t.is_cuda or t.is_pinned()):
+            raise TypeError(f"{name} must be a CUDA tensor or pinned host memory (the library has no CPU path)")
+    if V.shape != K.shape:
+        raise ValueError("K and V must have the same shape")
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(idx, torch.int32, "idx", 3)
+    _need(n_sel, torch.int32, "n_sel", 2)
+    B, Hkv, Lmax, D = K.shape
+    kc = idx.shape[2]
+    dev = idx.device
+    if Kc is None:
+        Kc = torch.empty((B, Hkv, kc * chunk, D), dtype=torch.bfloat16, device=dev)
+    if Vc is None:
+        Vc = torch.empty((B, Hkv, kc * chunk, D), dtype=torch.bfloat16, device=dev)
+    if lens is None:
+        lens = torch.empty(B * Hkv, dtype=torch.int32, device=dev)
+    if n_chunks is None:
+        n_chunks = torch.empty(B * Hkv, dtype=torch.int32, device=dev)
+    _need(Kc, torch.bfloat16, "Kc", 4)
+    _need(Vc, torch.bfloat16, "Vc", 4)
+    _need(lens, torch.int32, "lens", 1)
+    _need(n_chunks, torch.int32, "n_chunks", 1)
+    if Kc.shape != (B, Hkv, kc * chunk, D) or Vc.shape != Kc.shape:
+        raise ValueError(f"Kc and Vc must be {(B, Hkv, kc * chunk, D)}")
+    if lens.numel() != B * Hkv or n_chunks.numel() != B * Hkv:
+        raise ValueError("lens and n_chunks hold one entry per (b, g)")
+    _check(load().tf_pack_retrieval_cache(_ptr(K), _ptr(V), _ptr(seq_lens), _ptr(idx), _ptr(n_sel), B, Hkv, Lmax, D,
+                                          chunk, kc, _ptr(Kc), _ptr(Vc), _ptr(lens), _ptr(n_chunks),
+                                          _stream(stream)), "tf_pack_retrieval_cache")
+    return Kc, Vc, lens, n_chunks
 
 
 def tf_retrieval_draft_attn(q, M, K, V, seq_lens, kc, scale, idx=None, n_sel=None, s_cut=None, out=None, chunk=8,

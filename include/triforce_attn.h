@@ -272,6 +272,31 @@ TF_API tf_status tf_verify_attn_tree(const uint16_t* Q, const uint16_t* K, const
                               float scale, float* out,
                               void* ws, size_t ws_bytes, tf_stream_t stream);
 
+/* Resident retrieval cache: the rows the retrieval drafter attends to, packed
+ * into a buffer of their own ("TriForce: Lossless Acceleration of Long
+ * Sequence Generation with Hierarchical Speculative Decoding", "Abstract
+ * (arXiv)": the retrieval-sparse cache is the middle draft level and, when
+ * offloading, the full cache lives in host memory; project summary, "How It
+ * Works").  For each (b, g) the valid tokens (t < L_b) of the chunks
+ * idx[b,g,0:n_sel[b,g]] are copied in list order to rows 0.. of
+ *   Kc, Vc [B, Hkv, kc * chunk, D]   (device memory; rows at and past the
+ *                                      packed count are not written)
+ *   lens [B * Hkv] int32              packed rows of each (b, g)
+ *   n_chunks [B * Hkv] int32          ceil(lens / chunk)
+ * Ids outside [0, C_b) add no rows; a repeated id is copied once per
+ * occurrence; n_sel is clamped to [0, kc].  K, V [B, Hkv, Lmax, D] are device
+ * memory of the current device or host memory the CUDA runtime pinned or
+ * registered (read over the host link); any other pointer is refused with
+ * TF_ERR_INVALID_ARG before launch.  kc <= 4096.
+ * The packed buffer is attended through tf_sparse_decode_attn viewed as B*Hkv
+ * sequences of one KV head each: q [B*Hkv, G, D], K/V [B*Hkv, 1, kc*chunk, D],
+ * seq_lens = lens, idx[u, 0, i] = i and n_sel = n_chunks, which gives the
+ * attention over the original selection. */
+TF_API tf_status tf_pack_retrieval_cache(const uint16_t* K, const uint16_t* V, const int32_t* seq_lens,
+                                  const int32_t* idx, const int32_t* n_sel, int B, int Hkv, int Lmax,
+                                  int D, int chunk, int kc, uint16_t* Kc, uint16_t* Vc, int32_t* lens,
+                                  int32_t* n_chunks, tf_stream_t stream);
+
 /*
  * a7 with the cache offloaded to host memory ("TriForce: Lossless Acceleration
  * of Long Sequence Generation with Hierarchical Speculative Decoding",

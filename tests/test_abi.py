@@ -125,6 +125,13 @@ def test_host_validation_rejects_before_launch(lib):
                               None) == INVALID
     assert lib.tf_spec_accept(fake, fake, fake, fake, fake, 1, 4, 100, 1.0, fake, fake, null, null, 0,
                               None) == WORKSPACE
+    pk = lib.tf_pack_retrieval_cache
+    assert pk(null, fake, fake, fake, fake, 1, 2, 64, 128, 8, 4, fake, fake, fake, fake, None) == INVALID
+    assert pk(fake, fake, fake, fake, fake, 1, 2, 64, 128, 8, 4, odd, fake, fake, fake, None) == INVALID
+    assert pk(fake, fake, fake, fake, fake, 1, 0, 64, 128, 8, 4, fake, fake, fake, fake, None) == INVALID  # Hkv
+    assert pk(fake, fake, fake, fake, fake, 1, 2, 64, 64, 8, 4, fake, fake, fake, fake, None) == UNSUPPORTED
+    assert pk(fake, fake, fake, fake, fake, 1, 2, 64, 128, 8, 4097, fake, fake, fake, fake, None) == UNSUPPORTED
+    assert pk(fake, fake, fake, fake, fake, 0, 2, 64, 128, 8, 4, fake, fake, fake, fake, None) == 0  # B = 0: no work
     # the status query reads nothing without a workspace of at least one word
     assert lib.tf_check_status(null, 4096, None) == INVALID
     assert lib.tf_check_status(fake, 3, None) == INVALID
