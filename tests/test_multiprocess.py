@@ -51,3 +51,28 @@ def test_reference_arm_is_rank_zero_only(monkeypatch, capsys):
                                     workload="llama2-7b-128k-32layer", layers=None)
     bench.run_reference(args)  # must return without work or output on rank 1
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_json_line(monkeypatch, capsys):
+    """Rank 0's reference line carries the keys of the benchmark contract: the
+    oracle timed on the host cores, its own e2e with no device copies."""
+    import json
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    monkeypatch.setenv("RANK", "0")
+    args = bench.argparse.Namespace(impl="reference", gpus=1, steps=1, warmup=0,
+                                    workload="tiny-1layer-mha8-4k", layers=None)
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "tiny-1layer-mha8-4k"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["ms_per_step"] == pytest.approx(1e3 / line["value"], rel=1e-3)
