@@ -1,0 +1,73 @@
+"""Host logic of bench.py that needs no GPU: the clock sampler's summary of
+nvidia-smi rows (throttle reasons that reject a run), the peak fallback, and
+the rule that recorded ncu traffic is used only for the kernel source it was
+captured on."""
+
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _row(sm, mx, hw="Not Active", hw_th="Not Active", sw_th="Not Active", cap="Not Active"):
+    return ["0", str(sm), str(mx), "900.5", "0x0", hw, hw_th, sw_th, cap]
+
+
+def test_clock_summary_reports_median_max_and_active_reasons():
+    s = bench.ClockSampler(0)
+    s.rows = [_row(2070, 2070), _row(1980, 2070, cap="Active"), _row(2040, 2070)]
+    out = s.summary()
+    assert out["sm_mhz"] == 2040 and out["sm_max_mhz"] == 2070 and out["samples"] == 3
+    assert out["reasons"] == ["sw_power_cap"]
+    s.rows = [_row(1500, 2070, hw="Active", sw_th="Active")]
+    assert s.summary()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+
+
+def test_clock_summary_without_samples():
+    out = bench.ClockSampler(0).summary()
+    assert out["samples"] == 0 and out["reasons"] == ["unsampled"] and out["sm_mhz"] is None
+
+
+def test_clock_summary_skips_unreadable_clock_fields():
+    s = bench.ClockSampler(0)
+    s.rows = [_row("[N/A]", "[N/A]"), _row(2070, 2070)]
+    out = s.summary()
+    assert out["sm_mhz"] == 2070 and out["sm_max_mhz"] == 2070 and out["samples"] == 2
+
+
+def test_measured_peak_and_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_peaks() == (6800.0, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6795.5}))
+    assert bench.measured_peaks() == (6795.5, "measured")
+
+
+def test_recorded_traffic_only_for_the_captured_source(tmp_path, monkeypatch):
+    csrc = tmp_path / "hierarchical_speculative_decoding_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    src = csrc / "verify_attn.cu"
+    src.write_text("// kernel v1\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.kernel_source_hash("verify_attn.cu")
+    (tmp_path / "profiles" / "traffic.txt").write_text(
+        "# kernel-file source-hash workload bytes\n"
+        f"verify_attn.cu {h} llama2-7b-128k-32layer 2149004288\n")
+    assert bench.recorded_traffic("verify_attn.cu", "llama2-7b-128k-32layer") == 2149004288.0
+    assert bench.recorded_traffic("verify_attn.cu", "llama3-8b-gqa-128k-b4") is None  # other workload
+    src.write_text("// kernel v2\n")  # the kernel changed since the capture
+    assert bench.recorded_traffic("verify_attn.cu", "llama2-7b-128k-32layer") is None
+
+
+def test_committed_traffic_lines_name_existing_kernels():
+    with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
+        lines = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    assert lines
+    for parts in lines:
+        assert len(parts) == 4 and len(parts[1]) == 16 and float(parts[3]) > 0
+        assert os.path.exists(os.path.join(ROOT, "hierarchical_speculative_decoding_gb300", "csrc", parts[0]))
