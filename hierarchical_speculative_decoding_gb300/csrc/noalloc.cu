@@ -6,16 +6,22 @@
 // call, or latency-critical loops where an allocation (and the implicit device
 // synchronisation it can bring) is not allowed.  This entry point takes the
 // same inputs and outputs as tf_sparse_decode_attn but no workspace: its
-// split-K scratch lives in one file-scope device array of a fixed size that
-// every GPU loading this library keeps until the process exits.
+// split-K scratch lives in one file-scope device array of a fixed size (32 MiB)
+// that every GPU loading this library keeps until the process exits.  It always
+// runs the CUDA-core gather kernel, also for grouped-query heads, where the
+// workspace entry point runs the tensor-core kernel: the two agree within the
+// attention tolerance (2e-3), not bit for bit.
 //
-// Set-up happens on the first call made on each device (with that device
-// current): the array's device address is looked up with cudaGetSymbolAddress
-// and its ticket area is zeroed with a synchronous cudaMemset.  That first call
-// therefore should come before any stream capture.  Every call shares the
-// array and leaves its last contents behind; the tickets are reset by each
-// call, the partial results are always rewritten before they are read.  Calls
-// that overlap on the GPU (different streams, no ordering) race on the array.
+// Set-up happens on the first successful call made on each device (with that
+// device current): the array's device address is looked up with
+// cudaGetSymbolAddress and its ticket area is zeroed with a synchronous
+// cudaMemset.  That first call therefore must come before any stream capture;
+// made on a stream that is being captured it is refused (TF_ERR_INVALID_ARG)
+// without touching the device, and a set-up that failed is tried again by the
+// next call.  Every call shares the array and leaves its last contents behind;
+// the tickets are reset by each call, the partial results are always rewritten
+// before they are read.  Calls that overlap on the GPU (different streams, no
+// ordering) race on the array.
 #include <mutex>
 
 #include "gather_attn.cuh"
@@ -23,21 +29,24 @@
 namespace tf {
 namespace {
 
-constexpr size_t kScratchBytes = 16u << 20;  // 16 MiB per device
+constexpr size_t kScratchBytes = 32u << 20;  // 32 MiB per device
 constexpr size_t kTicketArea = 64u << 10;    // tickets live in the first 64 KiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_sparse_scratch[kScratchBytes];
 
 struct DeviceScratch {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
+  std::mutex mu;
+  void* ptr = nullptr;  // set once the set-up succeeded
 };
 DeviceScratch g_dev[kMaxDevices];
 
-// Device address of the scratch array on the current device (set up once).
-void* scratch_for_current_device(tf_status* st) {
+// Device address of the scratch array on the current device.  The set-up runs
+// under a per-device lock until it succeeds once; a failed attempt leaves
+// nothing behind, so a later call tries again.  A stream under capture is
+// refused before the device is touched (the synchronous set-up would end the
+// capture).
+void* scratch_for_current_device(cudaStream_t stream, tf_status* st) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     *st = TF_ERR_CUDA;
@@ -48,16 +57,28 @@ void* scratch_for_current_device(tf_status* st) {
     return nullptr;
   }
   DeviceScratch& d = g_dev[dev];
-  std::call_once(d.once, [&d]() {
+  std::lock_guard<std::mutex> lock(d.mu);
+  if (!d.ptr) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+      (void)cudaGetLastError();
+      *st = TF_ERR_CUDA;
+      return nullptr;
+    }
+    if (cap != cudaStreamCaptureStatusNone) {
+      *st = TF_ERR_INVALID_ARG;
+      return nullptr;
+    }
     void* p = nullptr;
-    d.err = cudaGetSymbolAddress(&p, g_sparse_scratch);
-    if (d.err == cudaSuccess) d.err = cudaMemset(p, 0, kTicketArea);
-    if (d.err == cudaSuccess) d.err = cudaDeviceSynchronize();
-    if (d.err == cudaSuccess) d.ptr = p;
-  });
-  if (d.err != cudaSuccess || !d.ptr) {
-    *st = TF_ERR_CUDA;
-    return nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_sparse_scratch);
+    if (e == cudaSuccess) e = cudaMemset(p, 0, kTicketArea);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      *st = TF_ERR_CUDA;
+      return nullptr;
+    }
+    d.ptr = p;
   }
   *st = TF_OK;
   return d.ptr;
@@ -89,7 +110,7 @@ extern "C" tf_status tf_sparse_decode_attn_noalloc(const uint16_t* q, const uint
   if (tickets > kTicketArea || need - tickets > kScratchBytes - kTicketArea) return TF_ERR_SCRATCH_LIMIT;
 
   tf_status st;
-  char* base = static_cast<char*>(scratch_for_current_device(&st));
+  char* base = static_cast<char*>(scratch_for_current_device((cudaStream_t)stream, &st));
   if (!base) return st;
   char* ws = base + (kTicketArea - tickets);
   GatherParams p{};

@@ -150,19 +150,27 @@ TF_API tf_status tf_sparse_decode_attn(const uint16_t* q, const uint16_t* K, con
  * Some hosts cannot call cudaMalloc: an engine that owns every device
  * allocation, a plugin loaded into such an engine, or a latency-critical loop
  * where allocating (and the synchronisation it may bring) is not allowed.
- * Same inputs, outputs and result as tf_sparse_decode_attn; the split-K
- * scratch is a 16 MiB file-scope device array instead of `ws`, held by every
- * GPU that loads this library until the process exits.  The tickets use its
- * first 64 KiB and the partial results the rest (about 8.5 MB for batch 8 x
- * 8 KV heads x 4 query heads per group at kc = 512); problems whose partial
- * results exceed 16 MiB - 64 KiB return TF_ERR_SCRATCH_LIMIT without
- * launching anything.
- * The first call on each device sets up that device's copy (looks up its
- * address with cudaGetSymbolAddress and zeroes the ticket area with a
- * synchronous cudaMemset), so make it before any stream capture.  All calls
- * share the one array and leave their contents in it: calls that may overlap
- * on the GPU (unordered streams) race and give wrong results.  It allocates
- * nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * Same inputs and outputs as tf_sparse_decode_attn.  The result agrees with
+ * tf_sparse_decode_attn within the attention tolerance (max abs error 2e-3),
+ * not bit for bit: this call always runs the CUDA-core gather kernel, while
+ * tf_sparse_decode_attn runs the tensor-core kernel for groups of two or more
+ * query heads per KV head (at 128K, batch 4 x 8 KV heads x 4 heads per group,
+ * about 50 us per call here against about 30 us there).
+ * The split-K scratch is a 32 MiB file-scope device array instead of `ws`,
+ * held by every GPU that loads this library until the process exits.  The
+ * tickets use its first 64 KiB and the partial results the rest: a problem
+ * fits when its partials need at most 32 MiB - 64 KiB, i.e. at kc = 512 up to
+ * B * Hkv = 499 (one query head per KV head), 249 (two), 124 (three or four,
+ * e.g. batch 8 x 8 KV heads x 4 heads per group: 17.2 MB) or 62 (five to
+ * eight).  Larger problems return TF_ERR_SCRATCH_LIMIT without launching.
+ * The first successful call on each device sets up that device's copy (looks
+ * up its address with cudaGetSymbolAddress and zeroes the ticket area with a
+ * synchronous cudaMemset), so make it before any stream capture: on a stream
+ * that is being captured it returns TF_ERR_INVALID_ARG without touching the
+ * device, and a set-up that failed is tried again on the next call.  All
+ * calls share the one array and leave their contents in it: calls that may
+ * overlap on the GPU (unordered streams) race and give wrong results.  It
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  */
 TF_API tf_status tf_sparse_decode_attn_noalloc(const uint16_t* q, const uint16_t* K, const uint16_t* V,
                                 const int32_t* seq_lens, const int32_t* idx, const int32_t* n_sel,
