@@ -630,3 +630,97 @@ def spec_accept(tgt_logits, drf_logits, drf_tokens, u_acc, u_res, temperature=1.
     out_tokens = np.where(col < n_acc[:, None], xpad, -1)
     out_tokens = np.where(col == n_acc[:, None], nxt[:, None], out_tokens)
     return {"n_acc": n_acc, "next": nxt, "out_tokens": out_tokens, "margin": margin}
+
+
+def tree_parent(parent_row, j):
+    """Parent of candidate j as the tree calls read it: parent_row[j] when it
+    points to an earlier candidate or is -1 (the prefix), else -1 (a link
+    outside [-1, j) attaches the candidate to the prefix, as tree_ancestors
+    ends a walk there)."""
+    pj = int(parent_row[j])
+    return pj if -1 <= pj < j else -1
+
+
+def spec_accept_tree(tgt_logits, drf_logits, drf_tokens, parent, u_acc, u_res, temperature=1.0):
+    """Lossless accept / resample over a tree of candidates.
+
+    Blog page, "The Three Forces of TriForce": Force 2 arranges the surviving
+    candidates as a tree and Force 3 verifies the tree in one pass, applying
+    the speculative rejection rule; "Dual Rejection Sampling: Mathematical
+    Losslessness" prints the rule for one candidate: keep x when
+    min(1, p(x)/q(x)) >= u, otherwise draw from max(0, p - q) normalised.  The
+    pages print no rule for several candidates that extend the same node.
+    Reading (the printed rule applied to the siblings one at a time, the only
+    steps it uses are the printed ones): the children of a node are
+    independent draws from the drafter's distribution at that node; they are
+    tested in index order against the current target distribution p', which
+    starts as the verifier's distribution at the node; a child that passes is
+    kept and the walk continues at it with the verifier's distribution there;
+    a child that fails replaces p' by max(0, p' - q) normalised (kept as is
+    when that residual is all zero, as the chain call falls back to p_j) and
+    the next sibling is tested.  When a node has no child left, the next
+    token is drawn from p' with the index-order inverse CDF: the residual
+    after the last rejection, or the verifier's distribution at the node (the
+    bonus token) when nothing there was rejected.  With parent[j] = j - 1 for
+    every j this is spec_accept.
+
+    Shapes (T candidates): tgt_logits [B, T+1, V], row 0 the verifier at the
+    prefix and row 1+j the verifier after candidate j; drf_logits [B, T, V],
+    row j the drafter distribution candidate j was drawn from (its parent's);
+    drf_tokens [B, T] (an entry outside [0, V) removes the candidate and so its
+    subtree); parent [B, T] (read by tree_parent); u_acc [B, T] (the uniform of
+    candidate j's test); u_res [B].  Logit arrays may have a leading 1 to
+    broadcast over B.
+
+    Because a child's index exceeds its parent's, visiting j = 0 .. T-1 once
+    and testing j exactly when its parent is the current node and j is in the
+    draft takes every node's children in index order, each after the walk
+    reached that node.  Returns dict with n_acc [B] (depth of the kept path),
+    next [B], out_tokens [B, T+1] (the kept tokens, the next token, -1 pad),
+    acc_nodes [B, T] (the kept candidates' indices, -1 pad) and the smallest
+    decision margin per sequence (as in spec_accept).
+    """
+    x = np.asarray(drf_tokens, dtype=np.int64)
+    par = np.asarray(parent, dtype=np.int64)
+    u_acc = np.asarray(u_acc, dtype=np.float64)
+    u_res = np.asarray(u_res, dtype=np.float64)
+    B, T = x.shape
+    p = softmax_rows(tgt_logits, temperature)
+    Vn = p.shape[-1]
+    p = np.broadcast_to(p, (B, T + 1, Vn))
+    q = np.broadcast_to(softmax_rows(drf_logits, temperature), (B, T, Vn)) if T > 0 else np.zeros((B, 0, Vn))
+    bidx = np.arange(B)
+
+    node = np.full(B, -1, dtype=np.int64)
+    w = p[:, 0].copy()  # p': the distribution the next test and the final draw use
+    n_acc = np.zeros(B, dtype=np.int64)
+    acc_nodes = np.full((B, T), -1, dtype=np.int64)
+    out_tokens = np.full((B, T + 1), -1, dtype=np.int64)
+    margin = np.full(B, np.inf)
+    for j in range(T):
+        pj = np.array([tree_parent(par[b], j) for b in range(B)], dtype=np.int64)
+        valid = (x[:, j] >= 0) & (x[:, j] < Vn)
+        test = valid & (pj == node)
+        xj = np.clip(x[:, j], 0, Vn - 1)
+        wx = w[bidx, xj]
+        qx = q[bidx, j, xj]
+        ratio = np.where(qx > 0, wx / np.where(qx > 0, qx, 1.0), np.inf)
+        accept = u_acc[:, j] <= ratio
+        margin = np.where(test, np.minimum(margin, np.abs(u_acc[:, j] - ratio)), margin)
+        keep = test & accept
+        drop = test & ~accept
+        # kept: the walk moves to candidate j
+        acc_nodes[bidx[keep], n_acc[keep]] = j
+        out_tokens[bidx[keep], n_acc[keep]] = x[keep, j]
+        n_acc = np.where(keep, n_acc + 1, n_acc)
+        node = np.where(keep, j, node)
+        w = np.where(keep[:, None], p[:, 1 + j], w)
+        # rejected: the residual against this candidate's drafter distribution
+        r = np.maximum(w - q[:, j], 0.0)
+        rs = r.sum(axis=-1)
+        upd = drop & (rs > 0)
+        w = np.where(upd[:, None], r / np.where(rs > 0, rs, 1.0)[:, None], w)
+    nxt, m2 = inverse_cdf(w, u_res)
+    margin = np.minimum(margin, m2)
+    out_tokens[bidx, n_acc] = nxt
+    return {"n_acc": n_acc, "next": nxt, "out_tokens": out_tokens, "acc_nodes": acc_nodes, "margin": margin}
