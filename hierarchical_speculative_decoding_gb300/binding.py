@@ -47,6 +47,8 @@ _SIGS = {
     "tf_pack_retrieval_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tf_spec_accept_workspace": (_S, [_I, _I]),
     "tf_spec_accept": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _S, _P]),
+    "tf_spec_accept_tree_workspace": (_S, [_I, _I, _I]),
+    "tf_spec_accept_tree": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _S, _P]),
 }
 
 
@@ -443,3 +445,44 @@ def tf_spec_accept(tgt_logits, drf_logits, drf_tokens, u_acc, u_res, temperature
                                  _ptr(u_res), B, gamma, Vn, float(temperature), _ptr(n_acc), _ptr(next_token),
                                  _ptr(out_tokens), _ptr(ws), nbytes, _stream(stream)), "tf_spec_accept")
     return n_acc, next_token, out_tokens
+
+
+def tf_spec_accept_tree_workspace(B, T, V):
+    return int(load().tf_spec_accept_tree_workspace(B, T, V))
+
+
+def tf_spec_accept_tree(tgt_logits, drf_logits, drf_tokens, parent, u_acc, u_res, temperature=1.0, n_acc=None,
+                        next_token=None, out_tokens=None, acc_nodes=None, ws=None, stream=None):
+    """Accept / resample over a candidate tree: tgt_logits [B, T+1, V] (row 1+j
+    after candidate j), drf_logits [B, T, V] (row j the distribution candidate j
+    was drawn from), drf_tokens / parent / u_acc [B, T], u_res [B].  Returns
+    (n_acc, next_token, out_tokens [B, T+1], acc_nodes [B, T])."""
+    _need(tgt_logits, torch.float32, "tgt_logits", 3)
+    B, t1, Vn = tgt_logits.shape
+    T = t1 - 1
+    _need(u_res, torch.float32, "u_res", 1)
+    if T > 0:
+        _need(drf_logits, torch.float32, "drf_logits", 3)
+        _need(drf_tokens, torch.int32, "drf_tokens", 2)
+        _need(parent, torch.int32, "parent", 2)
+        _need(u_acc, torch.float32, "u_acc", 2)
+        if tuple(drf_logits.shape) != (B, T, Vn) or tuple(drf_tokens.shape) != (B, T) or \
+                tuple(parent.shape) != (B, T) or tuple(u_acc.shape) != (B, T):
+            raise ValueError("tree shapes must be [B, T, V] for drf_logits and [B, T] for tokens, parent, u_acc")
+    dev = tgt_logits.device
+    if n_acc is None:
+        n_acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, T + 1), dtype=torch.int32, device=dev)
+    if acc_nodes is None:
+        acc_nodes = torch.empty((B, max(T, 1)), dtype=torch.int32, device=dev)
+    ws, nbytes = _ws(ws, tf_spec_accept_tree_workspace(B, T, Vn), dev)
+    g = T > 0
+    _check(load().tf_spec_accept_tree(_ptr(tgt_logits), _ptr(drf_logits if g else None),
+                                      _ptr(drf_tokens if g else None), _ptr(parent if g else None),
+                                      _ptr(u_acc if g else None), _ptr(u_res), B, T, Vn, float(temperature),
+                                      _ptr(n_acc), _ptr(next_token), _ptr(out_tokens), _ptr(acc_nodes), _ptr(ws),
+                                      nbytes, _stream(stream)), "tf_spec_accept_tree")
+    return n_acc, next_token, out_tokens, acc_nodes

@@ -403,6 +403,275 @@ size_t norm_bytes(int B, int gamma) {
   return align_up(rows * sizeof(float), 256) + rows * sizeof(double);
 }
 
+// ---------------------------------------------------------------------------
+// Tree form (candidates with parent links).  The same rule applied to the
+// children of a node one at a time, in index order: a child passes when
+// u <= p'(x) / q(x); a child that fails turns p' into max(0, p' - q)
+// normalised and the next sibling is tested; a child that passes restarts
+// the walk at it with the verifier row after it; a node with no child left
+// draws the next token from p'.
+//
+// One block per sequence.  Warp 0 walks the tree (next child by ballot over
+// the parent links, fp64 ratio tests from the normalisers, as in the chain
+// kernel); only a rejection needs the whole block, for one pass over the
+// vocabulary that writes the residual into one of two workspace rows (the
+// other keeps p' in case the residual is all zero) and sums it.  The final
+// draw scans the row holding p' with the chain kernel's fp32-pair scan.
+struct TreeParams {
+  const float* tgt;      // [B, T+1, V]
+  const float* drf;      // [B, T, V]
+  const int32_t* tokens;  // [B, T]
+  const int32_t* parent;  // [B, T]
+  const float* u_acc;    // [B, T]
+  const float* u_res;    // [B]
+  int T, V, Vpad;
+  float inv_t;
+  double inv_t_d;
+  NormWs ws;    // [B, 2T+1]
+  float* wbuf;  // [B, 2, Vpad]
+  int32_t* n_acc;
+  int32_t* next_token;
+  int32_t* out_tokens;  // [B, T+1] or null
+  int32_t* acc_nodes;   // [B, T] or null
+};
+
+// Index-order inverse CDF over w[0, V) with 1024 threads (every thread of the
+// block): each thread owns a contiguous slice, the slice sums are scanned as
+// exact fp32 pairs, one thread forms the crossing u * total in fp64 and the
+// slice holding it is walked again.  Returns the drawn index (all threads);
+// the last index with positive weight if rounding leaves no crossing.
+__device__ int block_inverse_cdf(const float* __restrict__ w, int V, double u) {
+  constexpr int GS = kBlockSeq;
+  __shared__ float s_ph[32], s_pl[32], s_th, s_tl;
+  __shared__ int s_found[32], s_lastv[32];
+  const int gid = threadIdx.x, lane = gid & 31, warp = gid >> 5, nw = GS / 32;
+  const int seg = (V + GS - 1) / GS;
+  const int t0 = min(V, gid * seg), t1 = min(V, t0 + seg);
+  float run = 0.0f;
+  for (int t = t0; t < t1; ++t) run += w[t];
+  float ih = run, il = 0.0f;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float h2 = __shfl_up_sync(0xffffffffu, ih, o), l2 = __shfl_up_sync(0xffffffffu, il, o);
+    if (lane >= o) pair_add(ih, il, h2, l2);
+  }
+  float eh = __shfl_up_sync(0xffffffffu, ih, 1), el = __shfl_up_sync(0xffffffffu, il, 1);
+  if (lane == 0) eh = el = 0.0f;
+  __syncthreads();
+  if (lane == 31) {
+    s_ph[warp] = ih;
+    s_pl[warp] = il;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const float vh = lane < nw ? s_ph[lane] : 0.0f, vl = lane < nw ? s_pl[lane] : 0.0f;
+    float wh = vh, wl = vl;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float h2 = __shfl_up_sync(0xffffffffu, wh, o), l2 = __shfl_up_sync(0xffffffffu, wl, o);
+      if (lane >= o) pair_add(wh, wl, h2, l2);
+    }
+    float xh = __shfl_up_sync(0xffffffffu, wh, 1), xl = __shfl_up_sync(0xffffffffu, wl, 1);
+    if (lane == 0) xh = xl = 0.0f;
+    __syncwarp();
+    if (lane < nw) {
+      s_ph[lane] = xh;
+      s_pl[lane] = xl;
+    }
+    if (lane == 31) {
+      const double tgt = u * ((double)wh + (double)wl);
+      s_th = (float)tgt;
+      s_tl = (float)(tgt - (double)(float)tgt);
+    }
+  }
+  __syncthreads();
+  float xh = s_ph[warp], xl = s_pl[warp];
+  pair_add(xh, xl, eh, el);
+  const float gap = (s_th - xh) + (s_tl - xl);
+  const bool holds = gap >= 0.0f && run > gap;
+  int found = 0x7fffffff, last = -1;
+  if (holds) {
+    float r2 = 0.0f;
+    for (int t = t0; t < t1; ++t) {
+      r2 += w[t];
+      if (r2 > gap) {
+        found = t;
+        break;
+      }
+    }
+  }
+  if (!__syncthreads_or(found != 0x7fffffff)) {
+    for (int t = t0; t < t1; ++t)
+      if (w[t] > 0.0f) last = t;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
+    last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  }
+  __syncthreads();
+  if (lane == 0) {
+    s_found[warp] = found;
+    s_lastv[warp] = last;
+  }
+  __syncthreads();
+  for (int k = 0; k < nw; ++k) {
+    found = min(found, s_found[k]);
+    last = max(last, s_lastv[k]);
+  }
+  return found != 0x7fffffff ? found : (last >= 0 ? last : 0);
+}
+
+// Parent of candidate j as the tree calls read it (a link outside [-1, j) is -1).
+__device__ __forceinline__ int tree_parent(const int32_t* par, int j) {
+  const int pj = par[j];
+  return (pj >= -1 && pj < j) ? pj : -1;
+}
+
+__global__ void __launch_bounds__(kBlockSeq) tree_accept_kernel(TreeParams p) {
+  __shared__ int s_node, s_staged, s_rej, s_depth;
+  __shared__ double s_Z, s_part[32];
+  pdl_wait();
+  const int b = blockIdx.x, T = p.T, V = p.V, R = 2 * T + 1;
+  const int gid = threadIdx.x, lane = gid & 31, warp = gid >> 5;
+  const int32_t* tok = p.tokens + (size_t)b * T;
+  const int32_t* par = p.parent + (size_t)b * T;
+  float* buf = p.wbuf + (size_t)b * 2 * p.Vpad;
+  // Walk state, kept by thread 0 and published for the block: the current
+  // node (-1: the prefix); which workspace row holds p' (-1: p' is the
+  // verifier row after the node) and its sum.
+  if (gid == 0) {
+    s_node = -1;
+    s_staged = -1;
+    s_depth = 0;
+    s_Z = 0.0;
+  }
+  __syncthreads();
+  int last = -1;  // warp 0: candidates up to here have been visited
+  while (true) {
+    if (warp == 0) {
+      int node = s_node, staged = s_staged, depth = s_depth;
+      const double Z = s_Z;
+      int rej = -1;
+      while (true) {
+        // next child of `node` after `last`, in index order
+        int c = -1;
+        for (int base = last + 1; base < T; base += 32) {
+          const int j = base + lane;
+          bool ok = false;
+          if (j < T) {
+            const int x = tok[j];
+            ok = x >= 0 && x < V && tree_parent(par, j) == node;
+          }
+          const unsigned ball = __ballot_sync(0xffffffffu, ok);
+          if (ball) {
+            c = base + __ffs(ball) - 1;
+            break;
+          }
+        }
+        if (c < 0) break;
+        last = c;
+        bool accept = false;
+        if (lane == 0) {
+          const int x = tok[c];
+          const double lq = (double)p.drf[((size_t)b * T + c) * V + x] * p.inv_t_d -
+                            (double)p.ws.m[(size_t)b * R + T + 1 + c];
+          const double zq = p.ws.z[(size_t)b * R + T + 1 + c];
+          const double ua = (double)p.u_acc[(size_t)b * T + c];
+          if (staged < 0) {
+            const int row = node + 1;
+            const double lp = (double)p.tgt[((size_t)b * (T + 1) + row) * V + x] * p.inv_t_d -
+                              (double)p.ws.m[(size_t)b * R + row];
+            const double zp = p.ws.z[(size_t)b * R + row];
+            accept = (exp2(lq) / zq == 0.0) || ua <= exp2(lp - lq) * (zq / zp);
+          } else {
+            const double wx = (double)buf[(size_t)staged * p.Vpad + x];
+            accept = (exp2(lq) / zq == 0.0) || ua <= (wx / Z) * zq / exp2(lq);
+          }
+          if (accept) {
+            if (p.out_tokens) p.out_tokens[(size_t)b * (T + 1) + depth] = x;
+            if (p.acc_nodes) p.acc_nodes[(size_t)b * T + depth] = c;
+          }
+        }
+        accept = __shfl_sync(0xffffffffu, accept, 0);
+        if (!accept) {
+          rej = c;
+          break;
+        }
+        node = c;
+        staged = -1;
+        ++depth;
+      }
+      if (lane == 0) {
+        s_node = node;
+        s_staged = staged;
+        s_depth = depth;
+        s_rej = rej;
+      }
+    }
+    __syncthreads();
+    const int rej = s_rej;
+    if (rej < 0) break;
+    // ---- residual of p' against the rejected candidate's drafter row
+    const int node = s_node, staged = s_staged;
+    const int dst = staged == 0 ? 1 : 0;
+    const float* qr = p.drf + ((size_t)b * T + rej) * V;
+    const float qm = p.ws.m[(size_t)b * R + T + 1 + rej];
+    const float inv_zq = (float)(1.0 / p.ws.z[(size_t)b * R + T + 1 + rej]);
+    const float* pr = p.tgt + ((size_t)b * (T + 1) + node + 1) * V;
+    const float pm = p.ws.m[(size_t)b * R + node + 1];
+    const float inv_zp = (float)(1.0 / p.ws.z[(size_t)b * R + node + 1]);
+    const float inv_Z = staged >= 0 ? (float)(1.0 / s_Z) : 0.0f;
+    const float* src = buf + (size_t)(staged >= 0 ? staged : 0) * p.Vpad;
+    float* out = buf + (size_t)dst * p.Vpad;
+    double part = 0.0;
+    for (int t = gid; t < V; t += kBlockSeq) {
+      const float cur = staged >= 0 ? src[t] * inv_Z : exp2f(__ldg(pr + t) * p.inv_t - pm) * inv_zp;
+      const float r = fmaxf(cur - exp2f(__ldg(qr + t) * p.inv_t - qm) * inv_zq, 0.0f);
+      out[t] = r;
+      part += (double)r;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) s_part[warp] = part;
+    __syncthreads();
+    if (gid == 0) {
+      double z = 0.0;
+      for (int w = 0; w < kBlockSeq / 32; ++w) z += s_part[w];
+      if (z > 0.0) {  // an all-zero residual leaves p' as it was
+        s_staged = dst;
+        s_Z = z;
+      }
+    }
+    __syncthreads();
+  }
+  // ---- the draw: p' into a workspace row if it is still a verifier row
+  const int node = s_node, depth = s_depth;
+  int staged = s_staged;
+  if (staged < 0) {
+    const float* pr = p.tgt + ((size_t)b * (T + 1) + node + 1) * V;
+    const float pm = p.ws.m[(size_t)b * R + node + 1];
+    const float inv_zp = (float)(1.0 / p.ws.z[(size_t)b * R + node + 1]);
+    for (int t = gid; t < V; t += kBlockSeq) buf[t] = exp2f(__ldg(pr + t) * p.inv_t - pm) * inv_zp;
+    staged = 0;
+    __syncthreads();
+  }
+  const int next = block_inverse_cdf(buf + (size_t)staged * p.Vpad, V, (double)p.u_res[b]);
+  if (gid == 0) {
+    p.n_acc[b] = depth;
+    p.next_token[b] = next;
+  }
+  if (p.out_tokens)
+    for (int c = depth + gid; c <= T; c += kBlockSeq) p.out_tokens[(size_t)b * (T + 1) + c] = c == depth ? next : -1;
+  if (p.acc_nodes)
+    for (int c = depth + gid; c < T; c += kBlockSeq) p.acc_nodes[(size_t)b * T + c] = -1;
+}
+
+size_t tree_bytes(int B, int T, int V) {
+  return align_up(norm_bytes(B, T), 256) + (size_t)B * 2 * align_up((size_t)V, 64) * sizeof(float);
+}
+
+
 }  // namespace
 }  // namespace tf
 
@@ -455,5 +724,56 @@ extern "C" tf_status tf_spec_accept(const float* tgt_logits, const float* drf_lo
                      drf_tokens, u_acc, u_res, B, gamma, V, inv_t, inv_t_d, nws, n_acc, next_token, out_tokens);
     }
   }
+  return e == cudaSuccess ? launch_status() : TF_ERR_CUDA;
+}
+
+extern "C" size_t tf_spec_accept_tree_workspace(int B, int T, int V) {
+  if (B <= 0 || T < 0 || V < 1) return 0;
+  return tf::tree_bytes(B, T, V);
+}
+
+extern "C" tf_status tf_spec_accept_tree(const float* tgt_logits, const float* drf_logits, const int32_t* drf_tokens,
+                                         const int32_t* parent, const float* u_acc, const float* u_res, int B, int T,
+                                         int V, float temperature, int32_t* n_acc, int32_t* next_token,
+                                         int32_t* out_tokens, int32_t* acc_nodes, void* ws, size_t ws_bytes,
+                                         tf_stream_t stream) {
+  using namespace tf;
+  if (!tgt_logits || !u_res || !n_acc || !next_token) return TF_ERR_INVALID_ARG;
+  if (T > 0 && (!drf_logits || !drf_tokens || !parent || !u_acc)) return TF_ERR_INVALID_ARG;
+  if (B < 0 || T < 0 || V < 1 || !(temperature > 0.0f)) return TF_ERR_INVALID_ARG;
+  if (B == 0) return TF_OK;
+  if (!ws || ws_bytes < tree_bytes(B, T, V) || !aligned16(ws)) return TF_ERR_WORKSPACE;
+  const long long rows = (long long)B * (2 * T + 1);
+  if (rows >= (1ll << 31) || (long long)B * (T + 1) * V >= (1ll << 40)) return TF_ERR_UNSUPPORTED;
+  NormWs nws;
+  nws.m = static_cast<float*>(ws);
+  nws.z = reinterpret_cast<double*>(static_cast<char*>(ws) + align_up((size_t)rows * sizeof(float), 256));
+  TreeParams tp;
+  tp.tgt = tgt_logits;
+  tp.drf = drf_logits;
+  tp.tokens = drf_tokens;
+  tp.parent = parent;
+  tp.u_acc = u_acc;
+  tp.u_res = u_res;
+  tp.T = T;
+  tp.V = V;
+  tp.Vpad = (int)align_up((size_t)V, 64);
+  tp.inv_t_d = 1.4426950408889634 / (double)temperature;  // log2(e) / temperature
+  tp.inv_t = (float)tp.inv_t_d;
+  tp.ws = nws;
+  tp.wbuf = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(norm_bytes(B, T), 256));
+  tp.n_acc = n_acc;
+  tp.next_token = next_token;
+  tp.out_tokens = out_tokens;
+  tp.acc_nodes = acc_nodes;
+  cudaError_t e;
+  if (V <= kSmallV)
+    e = launch_pdl(row_norm_kernel<true>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, (cudaStream_t)stream,
+                   tgt_logits, drf_logits, B, T, V, tp.inv_t, nws);
+  else
+    e = launch_pdl(row_norm_kernel<false>, dim3((unsigned)rows), dim3(kBlockRow), 0, (cudaStream_t)stream,
+                   tgt_logits, drf_logits, B, T, V, tp.inv_t, nws);
+  if (e == cudaSuccess)
+    e = launch_pdl(tree_accept_kernel, dim3(B), dim3(kBlockSeq), 0, (cudaStream_t)stream, tp);
   return e == cudaSuccess ? launch_status() : TF_ERR_CUDA;
 }

@@ -189,3 +189,30 @@ def two_level_inputs(B, gamma1, vocab, seed, device="cpu"):
     ur2 = torch.rand((B,), generator=g, device=device)
     return dict(p=p.contiguous(), q=q.contiguous(), r=r.contiguous(), x=x, u1=u1, ur1=ur1, u2=u2, ur2=ur2)
 
+
+
+def tree_accept_inputs(B, T, vocab, seed, device="cpu", tgt_std=2.0, drf_noise=1.0, branching=None):
+    """A candidate tree per sequence: parent [B, T] (candidate j extends a
+    uniformly drawn earlier candidate or the prefix, -1), verifier logits
+    [B, T+1, V] (row 0 the prefix, row 1+j after candidate j), the drafter's
+    logits at every node (the prefix and each candidate) = the verifier's at
+    that node + noise, drf [B, T, V] = the row of candidate j's parent, tokens
+    drawn independently from those rows (siblings are independent draws) and
+    uniforms.  branching=k gives every node up to k children in order instead
+    (a complete k-ary tree laid out breadth first)."""
+    g = generator(seed * 1_000_003 + 17, device)
+    if branching:
+        parent = torch.tensor([(j // branching) - 1 for j in range(T)], dtype=torch.int32, device=device)
+        parent = parent[None].repeat(B, 1)
+    else:
+        span = torch.arange(T, device=device, dtype=torch.float32)[None] + 1.0  # choices -1 .. j-1
+        parent = (torch.rand((B, T), generator=g, device=device) * span).floor().to(torch.int32) - 1
+    tgt = torch.randn((B, T + 1, vocab), generator=g, device=device) * tgt_std
+    node_drf = tgt + torch.randn((B, T + 1, vocab), generator=g, device=device) * drf_noise
+    rows = (parent.long() + 1).clamp(0, T)  # node index of the parent: 0 = prefix, 1 + i = candidate i
+    drf = torch.gather(node_drf, 1, rows[:, :, None].expand(B, T, vocab)) if T > 0 else node_drf[:, :0]
+    x = sample_tokens(drf, g) if T > 0 else torch.zeros((B, 0), dtype=torch.int32, device=device)
+    u_acc = torch.rand((B, T), generator=g, device=device)
+    u_res = torch.rand((B,), generator=g, device=device)
+    return dict(tgt=tgt.contiguous(), drf=drf.contiguous(), x=x.contiguous(), parent=parent.contiguous(),
+                u_acc=u_acc, u_res=u_res)

@@ -371,6 +371,49 @@ TF_API tf_status tf_spec_accept(const float* tgt_logits, const float* drf_logits
                          int32_t* n_acc, int32_t* next_token, int32_t* out_tokens,
                          void* ws, size_t ws_bytes, tf_stream_t stream);
 
+/*
+ * a8 over a candidate tree ("TriForce: Hierarchical Speculative Decoding for
+ * LLMs", "The Three Forces of TriForce": Force 2 arranges the candidates as a
+ * tree and Force 3 verifies the tree in one pass with the speculative
+ * rejection rule; "Dual Rejection Sampling: Mathematical Losslessness": the
+ * per-candidate test and residual).  The pages print no rule for several
+ * candidates extending one node; this call applies the printed rule to them
+ * one at a time: the children of a node, drawn independently from the
+ * drafter's distribution there, are tested in index order against the
+ * current target p' (at first the verifier's distribution at the node); a
+ * child is kept when u_acc <= p'(x) / q(x) (always when q(x) == 0) and the
+ * walk goes on at it with the verifier's distribution after it; a child that
+ * fails replaces p' by max(0, p' - q) normalised (p' is kept when that
+ * residual is all zero) and its next sibling is tested.  When the current
+ * node has no child left, the next token is drawn from p' with the
+ * index-order inverse CDF of tf_spec_accept (u_res): the residual after the
+ * last rejection, or the bonus token from the verifier row after the node.
+ * With parent[j] = j - 1 this is tf_spec_accept, decision for decision.
+ *   tgt_logits [B, T+1, V] f32: row 0 the verifier at the prefix, row 1+j the
+ *     verifier after candidate j (as tf_verify_attn_tree's query j gives it)
+ *   drf_logits [B, T, V] f32: row j the drafter distribution candidate j was
+ *     drawn from (its parent's; siblings share it)
+ *   drf_tokens [B, T] int32: an entry outside [0, V) removes the candidate and
+ *     its subtree
+ *   parent [B, T] int32: the candidate that j extends, -1 for the prefix; a
+ *     link outside [-1, j) is read as -1 (as in tf_verify_attn_tree)
+ *   u_acc [B, T] f32 (the uniform of candidate j's test), u_res [B] f32
+ *   n_acc [B] int32: depth of the kept path; next_token [B] int32
+ *   out_tokens [B, T+1] int32 (nullable): kept tokens, next token, -1 pad
+ *   acc_nodes [B, T] int32 (nullable): indices of the kept candidates, -1 pad
+ * T >= 0 (drf_logits, drf_tokens, parent and u_acc may be NULL when T == 0),
+ * V >= 1, temperature > 0.  Precision as tf_spec_accept; p' after a rejection
+ * is held as fp32 weights.  Workspace: tf_spec_accept_tree_workspace(B, T, V)
+ * bytes (normalisers and two vocabulary rows per sequence; needs no zeroing).
+ * Two kernel launches; a rejection costs one pass over the vocabulary.
+ */
+TF_API size_t tf_spec_accept_tree_workspace(int B, int T, int V);
+TF_API tf_status tf_spec_accept_tree(const float* tgt_logits, const float* drf_logits, const int32_t* drf_tokens,
+                              const int32_t* parent, const float* u_acc, const float* u_res,
+                              int B, int T, int V, float temperature,
+                              int32_t* n_acc, int32_t* next_token, int32_t* out_tokens, int32_t* acc_nodes,
+                              void* ws, size_t ws_bytes, tf_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -52,6 +52,9 @@ def test_workspace_sizes(lib):
     assert lib.tf_stream_window_attn_workspace(4, 32, 8, 4, 252) > 0
     assert lib.tf_verify_attn_workspace(4, 32, 8, 131072, 6) > 0
     assert lib.tf_spec_accept_workspace(8, 5) >= 8 * 11 * 12
+    # normalisers of 2T+1 rows and two vocabulary rows per sequence
+    assert lib.tf_spec_accept_tree_workspace(8, 6, 32000) >= 8 * 13 * 12 + 8 * 2 * 32000 * 4
+    assert lib.tf_spec_accept_tree_workspace(8, -1, 32000) == 0
     assert lib.tf_sparse_verify_attn_workspace(1, 32, 32, 512, 6) > 0
     assert lib.tf_verify_attn_offload_workspace(1, 32, 32, 131072, 6, 16384) > 0
     assert lib.tf_verify_attn_offload_workspace(1, 32, 32, 131072, 6, 0) == 0
@@ -125,6 +128,18 @@ def test_host_validation_rejects_before_launch(lib):
                               None) == INVALID
     assert lib.tf_spec_accept(fake, fake, fake, fake, fake, 1, 4, 100, 1.0, fake, fake, null, null, 0,
                               None) == WORKSPACE
+    # tree accept: tgt, drf, tokens, parent, u_acc, u_res, B, T, V, temperature, n_acc, next, out, nodes, ws, bytes
+    ta = lib.tf_spec_accept_tree
+    assert ta(fake, fake, fake, null, fake, fake, 1, 4, 100, 1.0, fake, fake, null, null, fake, big,
+              None) == INVALID  # no tree
+    assert ta(fake, fake, fake, fake, fake, fake, 1, 4, 100, 0.0, fake, fake, null, null, fake, big,
+              None) == INVALID  # temperature
+    assert ta(fake, fake, fake, fake, fake, fake, 1, -1, 100, 1.0, fake, fake, null, null, fake, big,
+              None) == INVALID  # T < 0
+    assert ta(fake, fake, fake, fake, fake, fake, 1, 4, 100, 1.0, fake, fake, null, null, fake,
+              lib.tf_spec_accept_tree_workspace(1, 4, 100) - 1, None) == WORKSPACE
+    assert ta(fake, fake, fake, fake, fake, fake, 0, 4, 100, 1.0, fake, fake, null, null, null, 0,
+              None) == 0  # B = 0: no work
     pk = lib.tf_pack_retrieval_cache
     assert pk(null, fake, fake, fake, fake, 1, 2, 64, 128, 8, 4, fake, fake, fake, fake, None) == INVALID
     assert pk(fake, fake, fake, fake, fake, 1, 2, 64, 128, 8, 4, odd, fake, fake, fake, None) == INVALID
