@@ -107,3 +107,61 @@ def test_retrieval_draft_repeated_calls_agree(cuda_lib):
     for x, y in zip(a[:3], b[:3]):
         assert np.array_equal(x, y)
     np.testing.assert_allclose(a[3], b[3], rtol=1e-5, atol=1e-6)
+
+
+def _level_means(w, C, levels, seed):
+    """Means that are zero except dimension 0, set to level / 8 (exact in bf16):
+    every score is q_sum[0] * level / 8 exactly, in fp32 and in float64, so
+    equal levels are exact ties on both sides."""
+    M = np.zeros((w.B, w.Hkv, C, 128), dtype=np.float32)
+    M[..., 0] = levels / 8.0
+    return (M.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _exact_topk(scores_bg, kc):
+    order = np.lexsort((np.arange(len(scores_bg)), -scores_bg))  # score descending, then lower id
+    return np.sort(order[:kc])
+
+
+def test_retrieval_draft_exact_ties_at_the_cut(cuda_lib):
+    """Scores on 64 levels (about 256 chunks each): the cut falls inside a
+    level with hundreds of exact ties spread over the CTAs of the cluster,
+    which must go to the lower chunk ids."""
+    C = 16384
+    w = small_workload(B=1, Hq=2, Hkv=2, L=8 * C, ragged=False)
+    c = make_case(w)
+    rng = np.random.default_rng(4)
+    M_bits = _level_means(w, C, rng.integers(0, 64, (w.B, w.Hkv, C)).astype(np.float32), 4)
+    idx, nsel, out = check_against_oracle(cuda_lib, w, c, M_bits, kc=512)
+    scores = O.chunk_scores(bits(c["q_cpu"]), M_bits, c["seq_cpu"].numpy(), w.L, 8, w.Hkv)
+    for g in range(w.Hkv):
+        assert np.array_equal(idx[0, g, :512], _exact_topk(scores[0][g], 512)), g
+
+
+def test_retrieval_draft_top_chunks_fill_the_budget(cuda_lib):
+    """Exactly kc chunks share the top score and the rest score far lower:
+    the tied top level is the whole selection and s_cut its score."""
+    C, kc = 16384, 512
+    w = small_workload(B=1, Hq=2, Hkv=2, L=8 * C, ragged=False)
+    c = make_case(w)
+    rng = np.random.default_rng(6)
+    q0 = bits(c["q_cpu"])  # make q_sum[0] > 0 so the high level scores highest
+    levels = rng.integers(0, 40, (w.B, w.Hkv, C)).astype(np.float32)
+    top = np.stack([rng.choice(C, kc, replace=False) for _ in range(w.Hkv)])
+    for g in range(w.Hkv):
+        levels[0, g, top[g]] = 100.0
+    qs = O.bf16_to_f64(q0).reshape(w.B, w.Hkv, -1, 128).sum(axis=2)[..., 0]
+    levels = np.where(qs[..., None] > 0, levels, -levels)
+    M_bits = _level_means(w, C, levels, 6)
+    idx, nsel, out = check_against_oracle(cuda_lib, w, c, M_bits, kc=kc)
+    for g in range(w.Hkv):
+        assert np.array_equal(idx[0, g], np.sort(top[g]))
+
+
+def test_retrieval_draft_context_just_above_the_budget(cuda_lib):
+    """600 chunks for a budget of 512: nearly every chunk is selected and the
+    cut sits near the bottom of the score range."""
+    w = small_workload(B=2, Hq=8, Hkv=2, L=8 * 600, budget=4096, ragged=False)
+    c = make_case(w, fill_invalid=float("nan"))
+    M_bits = O.build_chunk_means(bits(c["K_cpu"]), c["seq_cpu"].numpy(), w.chunk)
+    check_against_oracle(cuda_lib, w, c, M_bits)
