@@ -7,12 +7,16 @@ calls), sink + window attention (Force 1), full-cache verification of
 gamma+1 = 6 queries (Force 3).
 Workload: the full 32-layer Llama2-7B-128K KV cache (32 heads x 128 dims x
 131072 tokens, bf16, 64 GiB), seeded synthetic data with 1% planted chunks.
+After it, in the same run, the same step on the GQA batch (Llama-3-8B style,
+batch 4, 32/8 heads, 128K, 32 layers) and on the mixed batch (batch 8,
+contexts 16K..128K, 32/8 heads, 16 layers), each reported under "workloads".
 
 Default (impl=triforce): the CUDA library, inputs resident in HBM; prints one
 JSON line with steps/s, the verify kernel's roofline, an end-to-end number
 (queries copied from pinned host memory and outputs copied back inside the
-timed region) and the float64 oracle timed on a bounded sample of host cores.
-impl=reference: the oracle alone, on host cores, one bounded sample per step.
+timed region) and the float64 oracle timed on every host core (one
+single-threaded worker process per core) on a bounded sample of the workload.
+impl=reference: the oracle alone, on the same pool, one bounded sample per step.
 
 Multi-GPU (torchrun): each rank runs an independent replica of the step on its
 own GPU (the path has no exchange step); value = all ranks' steps / max time.
@@ -48,6 +52,8 @@ def parse():
                     help="capture the step (every layer's launches) once as a CUDA graph and replay it")
     ap.add_argument("--two-call-draft", action="store_true",
                     help="run the retrieval drafter as tf_chunk_scores_topk + tf_sparse_decode_attn")
+    ap.add_argument("--extra-workloads", default="llama3-8b-gqa-128k-b4,mixed-b8-gqa-16k-128k",
+                    help="comma-separated workloads timed after the headline one ('none': skip)")
     return ap.parse_args()
 
 
@@ -175,12 +181,30 @@ def recorded_traffic(kernel_file, workload):
     return None
 
 
-# ---------------------------------------------------------------- CPU oracle sample
+# ---------------------------------------------------------------- CPU oracle (every host core)
+
+_ORACLE_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+               "CUDA_VISIBLE_DEVICES": ""}
 
 
-def cpu_sample_worker(w_name, n_units, seed):
-    """Time the float64 oracle on n_units (layer, KV head) units of the workload,
-    each a full-length single-head slice.  Runs in a fresh single-threaded process."""
+def _pool_warm(_):
+    """Import the oracle and the input generators in a pool worker before any
+    unit is timed (and hold the worker briefly so each gets one task)."""
+    sys.path.insert(0, ROOT)
+    import numpy  # noqa: F401
+    import torch  # noqa: F401
+
+    from hierarchical_speculative_decoding_gb300 import synth  # noqa: F401
+    from oracle import triforce  # noqa: F401
+
+    time.sleep(0.3)
+    return os.getpid()
+
+
+def cpu_unit_worker(w_name, unit, seed):
+    """The float64 oracle on one (layer, KV head) unit of the workload at full
+    context: scores + top-k, sparse decode, window and verify attention.
+    Returns the seconds of oracle compute (input generation excluded)."""
     import numpy as np
     import torch
 
@@ -189,45 +213,391 @@ def cpu_sample_worker(w_name, n_units, seed):
     from oracle import triforce as O
 
     w = synth.WORKLOADS[w_name]
-    unit_w = synth.Workload(w.name + "-unit", 1, w.G, 1, w.D, w.L, 1, w.chunk, w.budget, w.n_sink, w.window, w.T,
-                            w.gamma, w.vocab, w.planted_frac, seed)
+    L = int(synth.seq_lens_for(w).max())
+    unit_w = synth.Workload(w.name + "-unit", 1, w.G, 1, w.D, L, 1, w.chunk, w.budget, w.n_sink, w.window, w.T,
+                            w.gamma, w.vocab, w.planted_frac, seed + unit)
     scale = w.D ** -0.5
-    total = 0.0
-    for u in range(n_units):
-        seq = synth.seq_lens_for(unit_w)
-        q, Q = synth.decode_queries(unit_w, u)
-        K, V, _ = synth.kv_cache(unit_w, u, q, seq)
-        kb = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
-        qb, Qb, Kb, Vb, sl = kb(q), kb(Q), kb(K), kb(V), seq.numpy()
-        M = O.build_chunk_means(Kb, sl, w.chunk)  # prefill-time index, not part of the step
-        t0 = time.perf_counter()
-        idx, nsel, *_ = O.chunk_scores_topk(qb, M, sl, w.L, w.chunk, w.kc, 1)
-        O.sparse_decode_attn(qb, Kb, Vb, sl, idx, nsel, w.chunk, scale)
-        O.stream_window_attn(qb, Kb, Vb, sl, w.n_sink, w.window, scale)
-        O.verify_attn(Qb, Kb, Vb, sl, scale)
-        total += time.perf_counter() - t0
-    return total / n_units
+    seq = synth.seq_lens_for(unit_w)
+    q, Q = synth.decode_queries(unit_w, 0)
+    K, V, _ = synth.kv_cache(unit_w, 0, q, seq)
+    kb = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    qb, Qb, Kb, Vb, sl = kb(q), kb(Q), kb(K), kb(V), seq.numpy()
+    M = O.build_chunk_means(Kb, sl, w.chunk)  # prefill-time index, not part of the step
+    t0 = time.perf_counter()
+    idx, nsel, *_ = O.chunk_scores_topk(qb, M, sl, L, w.chunk, w.kc, 1)
+    O.sparse_decode_attn(qb, Kb, Vb, sl, idx, nsel, w.chunk, scale)
+    O.stream_window_attn(qb, Kb, Vb, sl, w.n_sink, w.window, scale)
+    O.verify_attn(Qb, Kb, Vb, sl, scale)
+    return time.perf_counter() - t0
 
 
-def cpu_baseline(w, n_units=4):
-    """The oracle, as it stands, on a bounded sample of the workload, in a fresh
-    single-threaded process; scaled to one full step (units x layers)."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    code = ("import sys, json; sys.path.insert(0, %r); import bench; "
-            "print(json.dumps(bench.cpu_sample_worker(%r, %d, 7)))" % (ROOT, w.name, n_units))
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=1800)
-    if r.returncode != 0:
-        raise RuntimeError("cpu baseline failed: " + r.stderr[-2000:])
-    per_unit = float(r.stdout.strip().splitlines()[-1])
+def cpu_baseline(w, units_per_worker=2):
+    """The oracle, as it stands, on every host core: a spawn process pool (safe
+    beside a CUDA context) with one single-threaded worker per core, each
+    timing whole (layer, KV head) units at full context; all workers run at
+    once, so the per-unit times include their contention.  Throughput =
+    workers / mean unit time, scaled to one full step (units x layers)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+
+    workers = max(1, os.cpu_count() or 1)
+    n_units = units_per_worker * workers
+    saved = {k: os.environ.get(k) for k in _ORACLE_ENV}
+    os.environ.update(_ORACLE_ENV)
+    try:
+        with cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
+            list(ex.map(_pool_warm, range(workers)))
+            t0 = time.perf_counter()
+            times = list(ex.map(cpu_unit_worker, [w.name] * n_units, range(n_units), [7] * n_units))
+            wall = time.perf_counter() - t0
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    per_unit = statistics.mean(times)
     units_per_step = w.B * w.Hkv * w.layers
-    step_s = per_unit * units_per_step
-    return {"value": 1.0 / step_s, "unit": "steps/s", "cores": 1, "kind": "oracle",
-            "sample": (f"{n_units} (layer, KV head) units at full context {w.L}, float64 numpy oracle, "
-                       f"{per_unit:.3f} s per unit, scaled by {units_per_step} units per step")}
+    value = workers / per_unit / units_per_step
+    return {"value": value, "unit": "steps/s", "cores": workers, "host_cpu_count": os.cpu_count(),
+            "kind": "oracle", "threads_per_worker": 1,
+            "sample": (f"{n_units} (layer, KV head) units at full context, float64 numpy oracle, {workers} "
+                       f"single-threaded worker processes at once ({wall:.2f} s wall), {per_unit:.3f} s per unit; "
+                       f"scaled by {units_per_step} units per step")}
 
 
 # ---------------------------------------------------------------- GPU arm
+
+
+def _ev():
+    import torch
+
+    return torch.cuda.Event(enable_timing=True)
+
+
+def _median_call_ms(fn, stream, reps=5, warm=1):
+    """Median duration of fn() with CUDA events on `stream` around each call."""
+    import torch
+
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(reps):
+        a, b = _ev(), _ev()
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        out.append(a.elapsed_time(b))
+    return statistics.median(out)
+
+
+def graph_loop_ms(calls, stream, replays=5):
+    """Per-call device time of a loop of short launches: the loop is captured
+    once as a CUDA graph and replayed, so host launch cost (larger than these
+    kernels through the Python binding) stays out of the measurement."""
+    import torch
+
+    for c in calls:  # first calls outside the capture (per-device set-up)
+        c()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in calls:
+            c()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = _ev(), _ev()
+    a.record(stream)
+    for _ in range(replays):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (replays * len(calls))
+    del g
+    return ms
+
+
+class StepState:
+    """Resident inputs, outputs and workspaces of one workload's decode step."""
+
+    def __init__(self, w, layers, dev, tf, synth):
+        import torch
+
+        self.w, self.layers, self.dev = w, layers, dev
+        B, Hq, Hkv, L, D, T = w.B, w.Hq, w.Hkv, w.L, w.D, w.T
+        self.Cmax = -(-L // w.chunk)
+        self.scale = D ** -0.5
+        self.K = torch.empty((layers, B, Hkv, L, D), dtype=torch.bfloat16, device=dev)
+        self.V = torch.empty_like(self.K)
+        self.M = torch.empty((layers, B, Hkv, self.Cmax, D), dtype=torch.bfloat16, device=dev)
+        self.seq_cpu = synth.seq_lens_for(w)
+        self.seq = self.seq_cpu.to(dev)
+        qs, Qs = [], []
+        for l in range(layers):
+            q, Q = synth.decode_queries(w, l, device=dev)
+            synth.kv_cache(w, l, q, self.seq_cpu, device=dev, K_out=self.K[l], V_out=self.V[l])
+            qs.append(q)
+            Qs.append(Q)
+        self.q = torch.stack(qs)
+        self.Q = torch.stack(Qs)
+        for l in range(layers):
+            tf.tf_build_chunk_means(self.K[l], self.seq, self.M[l])
+        self.idx = torch.empty((layers, B, Hkv, w.kc), dtype=torch.int32, device=dev)
+        self.nsel = torch.empty((layers, B, Hkv), dtype=torch.int32, device=dev)
+        self.o_sp = torch.empty((layers, B, Hq, D), dtype=torch.float32, device=dev)
+        self.o_win = torch.empty((layers, B, Hq, D), dtype=torch.float32, device=dev)
+        self.o_ver = torch.empty((layers, B, Hq, T, D), dtype=torch.float32, device=dev)
+        self.ws_topk = tf.workspace(tf.tf_chunk_scores_topk_workspace(B, Hkv, L), dev)
+        self.ws_sp = tf.workspace(tf.tf_sparse_decode_attn_workspace(B, Hq, Hkv, w.kc), dev)
+        self.ws_win = tf.workspace(tf.tf_stream_window_attn_workspace(B, Hq, Hkv, w.n_sink, w.window), dev)
+        self.ws_ver = tf.workspace(tf.tf_verify_attn_workspace(B, Hq, Hkv, L, T), dev)
+        torch.cuda.synchronize()
+
+    def bytes_per_launch(self):
+        """Algorithmic bytes of one layer's launches, from the actual lengths
+        (and, for the drafter, the valid rows of the chunks it selected)."""
+        import torch
+
+        w = self.w
+        B, Hq, Hkv, D, T = w.B, w.Hq, w.Hkv, w.D, w.T
+        row = D * 2
+        lens = [min(max(int(x), 0), w.L) for x in self.seq_cpu.tolist()]
+        C = [-(-x // w.chunk) for x in lens]
+        sel_rows = 0
+        nsel = self.nsel[0].cpu()
+        idx = self.idx[0].cpu()
+        for b in range(B):
+            for g in range(Hkv):
+                ids = idx[b, g, : int(nsel[b, g])].to(torch.int64)
+                sel_rows += int(torch.clamp(lens[b] - ids * w.chunk, 0, w.chunk).sum())
+        q_io = B * Hq * D * (2 + 4)
+        means = sum(Hkv * c * row for c in C)
+        ids = B * Hkv * w.kc * 4
+        return {
+            "topk": means + B * Hq * D * 2 + ids,
+            "sparse": 2 * sel_rows * row + ids + q_io,
+            "draft": means + ids + 2 * sel_rows * row + q_io,
+            "window": sum(2 * Hkv * min(x, w.n_sink + w.window) * row for x in lens) + q_io,
+            "verify": sum(2 * Hkv * x * row for x in lens) + B * Hq * T * D * (2 + 4),
+        }
+
+
+def make_step(st, tf, two_call, stream):
+    w = st.w
+    kinds = ("draft", "window", "verify")
+
+    def draft(l):
+        if two_call:
+            tf.tf_chunk_scores_topk(st.q[l], st.M[l], st.seq, w.L, w.kc, st.idx[l], st.nsel[l], ws=st.ws_topk)
+            tf.tf_sparse_decode_attn(st.q[l], st.K[l], st.V[l], st.seq, st.idx[l], st.nsel[l], st.scale,
+                                     out=st.o_sp[l], ws=st.ws_sp)
+        else:
+            tf.tf_retrieval_draft_attn(st.q[l], st.M[l], st.K[l], st.V[l], st.seq, w.kc, st.scale, idx=st.idx[l],
+                                       n_sel=st.nsel[l], out=st.o_sp[l])
+
+    def step(evs=None):
+        for l in range(st.layers):
+            if evs is not None:
+                evs[l][0].record(stream)
+            draft(l)
+            if evs is not None:
+                evs[l][1].record(stream)
+            tf.tf_stream_window_attn(st.q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window, st.scale,
+                                     out=st.o_win[l], ws=st.ws_win)
+            if evs is not None:
+                evs[l][2].record(stream)
+            tf.tf_verify_attn(st.Q[l], st.K[l], st.V[l], st.seq, st.scale, out=st.o_ver[l], ws=st.ws_ver)
+            if evs is not None:
+                evs[l][3].record(stream)
+
+    return step, draft, kinds
+
+
+def time_steps(run_step, steps, stream, world, local):
+    """The headline region: a start and an end event only (events between
+    kernels would stop programmatic dependent launch from overlapping them)."""
+    import torch
+
+    t_start, t_end = _ev(), _ev()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_start.record(stream)
+        for _ in range(steps):
+            run_step()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    value, elapsed_s = job_throughput(steps, t_start.elapsed_time(t_end) / 1e3, world)
+    return value, elapsed_s, clocks.summary()
+
+
+def per_kernel_times(step, layers, k_steps, kinds):
+    """A second region with an event before and after every launch."""
+    import torch
+
+    evs = [[[_ev() for _ in range(4)] for _ in range(layers)] for _ in range(k_steps)]
+    torch.cuda.synchronize()
+    for s in range(k_steps):
+        step(evs[s])
+    torch.cuda.synchronize()
+    per_kind = {k: [] for k in kinds}
+    for s in range(k_steps):
+        for l in range(layers):
+            for i, k in enumerate(kinds):
+                per_kind[k].append(evs[s][l][i].elapsed_time(evs[s][l][i + 1]))
+    return per_kind
+
+
+def kernel_entry(nbytes, ms, peak):
+    gbps = nbytes / (ms / 1e3) / 1e9
+    return {"ms": round(ms, 5), "GBps": round(gbps, 1), "frac_hbm": round(gbps / peak, 4)}
+
+
+def measure_extra_workload(w, args, tf, synth, dev, stream, world, local, peak):
+    """The step on another workload: steps/s, the per-kernel breakdown with the
+    verify roofline, and the drafter back to back."""
+    import torch
+
+    st = StepState(w, w.layers, dev, tf, synth)
+    step, draft, kinds = make_step(st, tf, args.two_call_draft, stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    steps = max(3, args.steps // 2)
+    value, elapsed_s, clocks = time_steps(step, steps, stream, world, local)
+    per_kind = per_kernel_times(step, st.layers, max(3, steps // 2), kinds)
+    nb = st.bytes_per_launch()
+    kern = {}
+    for k in kinds:
+        name = "retrieval_draft" if k == "draft" else k
+        kern[name] = kernel_entry(nb[k], statistics.mean(per_kind[k]), peak)
+    d0, d1 = _ev(), _ev()
+    torch.cuda.synchronize()
+    d0.record(stream)
+    for l in range(st.layers):
+        draft(l)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    kern["retrieval_draft"]["back_to_back"] = kernel_entry(nb["draft"], d0.elapsed_time(d1) / st.layers, peak)
+    ver = kern["verify"]
+    out = {"value": round(value, 4), "unit": "steps/s", "steps": steps, "ms_per_step": round(elapsed_s / steps * 1e3, 4),
+           "config": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D, "context": w.L, "layers": w.layers,
+                      "ragged": bool(w.ragged), "seq_lens": st.seq_cpu.tolist(), "budget_tokens": w.budget,
+                      "verify_tokens": w.T},
+           "roofline": {"bound": "hbm", "kernel": "tf_verify_attn", "achieved": ver["GBps"], "peak": peak,
+                        "unit": "GB/s", "frac": ver["frac_hbm"], "algorithmic_bytes": nb["verify"],
+                        "traffic": recorded_traffic("verify_attn.cu", w.name)},
+           "kernels": kern, "clocks": clocks,
+           "gpu_launches": steps * st.layers * (4 if args.two_call_draft else 3)}
+    kern["retrieval_draft"]["traffic"] = None if args.two_call_draft else recorded_traffic("retrieval_draft.cu",
+                                                                                            w.name)
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_offload(st, tf, stream, peak, kernels):
+    """The offloaded setting on one 128K layer: the verify streamed from pinned
+    host memory, the retrieval drafter's cache packed (from device memory and
+    from pinned host memory), and one offloaded layer step."""
+    import torch
+
+    w, dev = st.w, st.dev
+    B, Hq, Hkv, L, D, T = w.B, w.Hq, w.Hkv, w.L, w.D, w.T
+    units, G = B * Hkv, Hq // Hkv
+    Kh = torch.empty(st.K[0].shape, dtype=st.K.dtype, pin_memory=True)
+    Vh = torch.empty(st.V[0].shape, dtype=st.V.dtype, pin_memory=True)
+    Kh.copy_(st.K[0])
+    Vh.copy_(st.V[0])
+    off_bytes = 2 * Kh.numel() * 2
+    seg_rows = min(16384, L)
+    ws_off = tf.workspace(tf.tf_verify_attn_offload_workspace(B, Hq, Hkv, L, T, seg_rows), dev)
+    o_off = torch.empty((B, Hq, T, D), dtype=torch.float32, device=dev)
+    side = torch.cuda.Stream()
+    Lmax_seq = int(st.seq_cpu.max())
+
+    def verify_off():
+        tf.tf_verify_attn_offload(st.Q[0], Kh, Vh, st.seq, Lmax_seq, st.scale, out=o_off, ws=ws_off, seg_rows=seg_rows,
+                                  copy_stream=side)
+
+    off_ms = min(_median_call_ms(verify_off, stream, reps=3), float("inf"))
+    stage = torch.empty_like(st.K[0])
+
+    def h2d():
+        stage.copy_(Kh, non_blocking=True)
+        stage.copy_(Vh, non_blocking=True)
+
+    h2d_ms = _median_call_ms(h2d, stream, reps=4)
+    del stage
+    h2d_gbps = off_bytes / (h2d_ms / 1e3) / 1e9
+    kernels["verify_offloaded_1layer"] = {
+        "ms": round(off_ms, 4), "GBps": round(off_bytes / (off_ms / 1e3) / 1e9, 1), "h2d_copy_GBps": round(h2d_gbps, 1),
+        "frac_of_h2d_copy": round(h2d_ms / off_ms, 4), "calls": "tf_verify_attn_offload",
+        "timing": "K/V in pinned host memory, 16K-position segments, copies on a second stream; median of 3 calls "
+                  "against the median of 4 plain pinned host-to-device copies of the same bytes"}
+
+    # the retrieval drafter's resident cache: this layer's selection packed
+    kc = w.kc
+    Kc = torch.empty((B, Hkv, kc * w.chunk, D), dtype=torch.bfloat16, device=dev)
+    Vc = torch.empty_like(Kc)
+    lens = torch.empty(units, dtype=torch.int32, device=dev)
+    nch = torch.empty(units, dtype=torch.int32, device=dev)
+    nb = st.bytes_per_launch()
+    rows_bytes = nb["sparse"] - B * Hkv * kc * 4 - B * Hq * D * 6  # selected K+V bytes
+    pack_bytes = 2 * rows_bytes + B * Hkv * kc * 4  # read + written, ids
+
+    def pack(src_k, src_v):
+        return lambda: tf.tf_pack_retrieval_cache(src_k, src_v, st.seq, st.idx[0], st.nsel[0], Kc, Vc, lens, nch)
+
+    pk_dev = _median_call_ms(pack(st.K[0], st.V[0]), stream)
+    pk_host = _median_call_ms(pack(Kh, Vh), stream, reps=3)
+    kernels["pack_retrieval_cache_1layer"] = {
+        "device": dict(kernel_entry(pack_bytes, pk_dev, peak), bytes=pack_bytes,
+                       bound="selected K+V rows read and written once (HBM)"),
+        "pinned_host": {"ms": round(pk_host, 5), "GBps_over_link": round(rows_bytes / (pk_host / 1e3) / 1e9, 1),
+                        "frac_of_h2d_copy": round(rows_bytes / (pk_host / 1e3) / 1e9 / h2d_gbps, 4),
+                        "bytes_over_link": rows_bytes,
+                        "bound": "the selected rows over the host link, against a plain pinned copy"},
+        "calls": "tf_pack_retrieval_cache"}
+
+    # one offloaded layer step: refresh the drafter's packed cache from host
+    # memory, the drafter over it, the tiny drafter over its resident window,
+    # and the verify streamed from host memory
+    win = w.n_sink + w.window
+    Kw = torch.empty((B, Hkv, win, D), dtype=torch.bfloat16, device=dev)
+    Vw = torch.empty_like(Kw)
+    for b in range(B):
+        Lb = int(st.seq_cpu[b])
+        pos = list(range(0, min(w.n_sink, Lb))) + list(range(max(w.n_sink, Lb - w.window), Lb))
+        Kw[b, :, : len(pos)] = st.K[0, b][:, pos]
+        Vw[b, :, : len(pos)] = st.V[0, b][:, pos]
+    wlens = torch.tensor([min(win, int(x)) for x in st.seq_cpu], dtype=torch.int32, device=dev)
+    ident = torch.arange(kc, dtype=torch.int32, device=dev).repeat(units, 1, 1).contiguous()
+    o_sp = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    o_w = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws_sp1 = tf.workspace(tf.tf_sparse_decode_attn_workspace(units, G, 1, kc), dev)
+    ws_w1 = tf.workspace(tf.tf_stream_window_attn_workspace(B, Hq, Hkv, w.n_sink, w.window), dev)
+
+    def off_step():
+        tf.tf_pack_retrieval_cache(Kh, Vh, st.seq, st.idx[0], st.nsel[0], Kc, Vc, lens, nch)
+        tf.tf_sparse_decode_attn(st.q[0].view(units, G, D), Kc.view(units, 1, kc * w.chunk, D),
+                                 Vc.view(units, 1, kc * w.chunk, D), lens, ident, nch.view(units, 1), st.scale,
+                                 out=o_sp.view(units, G, D), ws=ws_sp1)
+        tf.tf_stream_window_attn(st.q[0], Kw, Vw, wlens, w.n_sink, w.window, st.scale, out=o_w, ws=ws_w1)
+        verify_off()
+
+    step_ms = _median_call_ms(off_step, stream, reps=3)
+    link = off_bytes + rows_bytes
+    kernels["offloaded_step_1layer"] = {
+        "ms": round(step_ms, 4), "bytes_over_link": link, "GBps_over_link": round(link / (step_ms / 1e3) / 1e9, 1),
+        "frac_of_h2d_copy": round(link / (step_ms / 1e3) / 1e9 / h2d_gbps, 4),
+        "calls": "tf_pack_retrieval_cache (from host) + tf_sparse_decode_attn (packed) + tf_stream_window_attn "
+                 "(resident window) + tf_verify_attn_offload",
+        "steps_per_s_32_layers": round(1e3 / (step_ms * w.layers), 3)}
+    del Kh, Vh
 
 
 def run_gpu(args):
@@ -244,73 +614,15 @@ def run_gpu(args):
     w = synth.WORKLOADS[args.workload]
     layers = args.layers or w.layers
     B, Hq, Hkv, L, D, T = w.B, w.Hq, w.Hkv, w.L, w.D, w.T
-    Cmax = -(-L // w.chunk)
-    scale = D ** -0.5
-
-    # ---- resident state: KV cache, chunk means, per-layer queries
-    Kc = torch.empty((layers, B, Hkv, L, D), dtype=torch.bfloat16, device=dev)
-    Vc = torch.empty_like(Kc)
-    Mc = torch.empty((layers, B, Hkv, Cmax, D), dtype=torch.bfloat16, device=dev)
-    seq_cpu = synth.seq_lens_for(w)
-    seq = seq_cpu.to(dev)
-    qs, Qs = [], []
-    for l in range(layers):
-        q, Q = synth.decode_queries(w, l, device=dev)
-        synth.kv_cache(w, l, q, seq_cpu, device=dev, K_out=Kc[l], V_out=Vc[l])
-        qs.append(q)
-        Qs.append(Q)
-    q_all = torch.stack(qs)
-    Q_all = torch.stack(Qs)
-    del qs, Qs
-    # chunk-mean index (prefill-time; timed once for its own bandwidth)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for l in range(layers):
-        tf.tf_build_chunk_means(Kc[l], seq, Mc[l])
-    torch.cuda.synchronize()
-    ev0.record()
-    tf.tf_build_chunk_means(Kc[0], seq, Mc[0])
-    ev1.record()
-    torch.cuda.synchronize()
-    means_ms = ev0.elapsed_time(ev1)
-    means_bytes = B * Hkv * L * D * 2 + B * Hkv * Cmax * D * 2
-
-    # ---- outputs and workspaces (zeroed once; every call leaves them reusable)
-    idx = torch.empty((layers, B, Hkv, w.kc), dtype=torch.int32, device=dev)
-    nsel = torch.empty((layers, B, Hkv), dtype=torch.int32, device=dev)
-    o_sp = torch.empty((layers, B, Hq, D), dtype=torch.float32, device=dev)
-    o_win = torch.empty((layers, B, Hq, D), dtype=torch.float32, device=dev)
-    o_ver = torch.empty((layers, B, Hq, T, D), dtype=torch.float32, device=dev)
-    ws_topk = tf.workspace(tf.tf_chunk_scores_topk_workspace(B, Hkv, L), dev)
-    ws_sp = tf.workspace(tf.tf_sparse_decode_attn_workspace(B, Hq, Hkv, w.kc), dev)
-    ws_win = tf.workspace(tf.tf_stream_window_attn_workspace(B, Hq, Hkv, w.n_sink, w.window), dev)
-    ws_ver = tf.workspace(tf.tf_verify_attn_workspace(B, Hq, Hkv, L, T), dev)
-
     stream = torch.cuda.current_stream()
-    kinds = ("draft", "window", "verify")
+    peak, peak_kind = measured_peaks()
 
-    def draft(l):
-        if args.two_call_draft:
-            tf.tf_chunk_scores_topk(q_all[l], Mc[l], seq, L, w.kc, idx[l], nsel[l], ws=ws_topk)
-            tf.tf_sparse_decode_attn(q_all[l], Kc[l], Vc[l], seq, idx[l], nsel[l], scale, out=o_sp[l], ws=ws_sp)
-        else:
-            tf.tf_retrieval_draft_attn(q_all[l], Mc[l], Kc[l], Vc[l], seq, w.kc, scale, idx=idx[l], n_sel=nsel[l],
-                                       out=o_sp[l])
+    st = StepState(w, layers, dev, tf, synth)
+    # chunk-mean index (prefill-time; timed once for its own bandwidth)
+    means_ms = _median_call_ms(lambda: tf.tf_build_chunk_means(st.K[0], st.seq, st.M[0]), stream, reps=3)
+    means_bytes = B * Hkv * L * D * 2 + B * Hkv * st.Cmax * D * 2
 
-    def step(evs=None):
-        for l in range(layers):
-            if evs is not None:
-                evs[l][0].record(stream)
-            draft(l)
-            if evs is not None:
-                evs[l][1].record(stream)
-            tf.tf_stream_window_attn(q_all[l], Kc[l], Vc[l], seq, w.n_sink, w.window, scale, out=o_win[l],
-                                     ws=ws_win)
-            if evs is not None:
-                evs[l][2].record(stream)
-            tf.tf_verify_attn(Q_all[l], Kc[l], Vc[l], seq, scale, out=o_ver[l], ws=ws_ver)
-            if evs is not None:
-                evs[l][3].record(stream)
-
+    step, draft, kinds = make_step(st, tf, args.two_call_draft, stream)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -326,149 +638,85 @@ def run_gpu(args):
         torch.cuda.synchronize()
         run_step = graph.replay
 
-    # ---- timed region: device-resident inputs (64 GiB of KV >> 129 MB L2).  Only
-    # a start and an end event: events between kernels would break the
-    # programmatic-dependent-launch overlap of consecutive kernels.
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        t_start.record(stream)
-        for s in range(args.steps):
-            run_step()
-        t_end.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    value, elapsed_s = job_throughput(args.steps, t_start.elapsed_time(t_end) / 1e3, world)
+    # ---- timed region: device-resident inputs (64 GiB of KV >> 129 MB L2)
+    value, elapsed_s, clocks = time_steps(run_step, args.steps, stream, world, local)
 
-    # ---- second timed region for the per-kernel breakdown and the verify
-    # roofline: an event before and after every launch.
+    # ---- per-kernel breakdown and the verify roofline
     k_steps = max(3, args.steps // 2)
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(layers)] for _ in range(k_steps)]
-    torch.cuda.synchronize()
-    for s in range(k_steps):
-        step(evs[s])
-    torch.cuda.synchronize()
-    per_kind = {k: [] for k in kinds}
-    for s in range(k_steps):
-        for l in range(layers):
-            for i, k in enumerate(kinds):
-                per_kind[k].append(evs[s][l][i].elapsed_time(evs[s][l][i + 1]))
-
-    # ---- algorithmic bytes per launch (one layer)
-    kv_row = D * 2
-    bytes_topk = B * Hkv * Cmax * D * 2 + B * Hq * D * 2 + B * Hkv * w.kc * 4
-    bytes_sparse = 2 * B * Hkv * w.kc * w.chunk * kv_row + B * Hkv * w.kc * 4 + B * Hq * D * (2 + 4)
-    bytes_window = 2 * B * Hkv * min(L, w.n_sink + w.window) * kv_row + B * Hq * D * (2 + 4)
-    bytes_verify = 2 * B * Hkv * L * kv_row + B * Hq * T * D * (2 + 4)
-    # fused retrieval drafter: means, queries, the selection written, selected K/V rows, outputs
-    bytes_draft = (B * Hkv * Cmax * D * 2 + B * Hq * D * 2 + B * Hkv * w.kc * 4 +
-                   2 * B * Hkv * w.kc * w.chunk * kv_row + B * Hq * D * 4)
-    kbytes = {"draft": bytes_draft, "window": bytes_window, "verify": bytes_verify}
-    peak, peak_kind = measured_peaks()
+    per_kind = per_kernel_times(step, layers, k_steps, kinds)
+    nb = st.bytes_per_launch()
     kernels = {}
     for k in kinds:
-        ms = statistics.mean(per_kind[k])
         name = "retrieval_draft" if k == "draft" else k
-        kernels[name] = {"ms": round(ms, 5), "GBps": round(kbytes[k] / (ms / 1e3) / 1e9, 1),
-                         "frac_hbm": round(kbytes[k] / (ms / 1e3) / 1e9 / peak, 4)}
+        kernels[name] = kernel_entry(nb[k], statistics.mean(per_kind[k]), peak)
     kernels["retrieval_draft"]["calls"] = ("tf_chunk_scores_topk + tf_sparse_decode_attn" if args.two_call_draft
                                            else "tf_retrieval_draft_attn")
     kernels["retrieval_draft"]["traffic"] = (None if args.two_call_draft
                                              else recorded_traffic("retrieval_draft.cu", w.name))
     # the two-call form of the retrieval drafter, for comparison (events around each call)
     if not args.two_call_draft:
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(layers)]
+        ev = [[_ev() for _ in range(3)] for _ in range(layers)]
         torch.cuda.synchronize()
         for l in range(layers):
             ev[l][0].record(stream)
-            tf.tf_chunk_scores_topk(q_all[l], Mc[l], seq, L, w.kc, idx[l], nsel[l], ws=ws_topk)
+            tf.tf_chunk_scores_topk(st.q[l], st.M[l], st.seq, L, w.kc, st.idx[l], st.nsel[l], ws=st.ws_topk)
             ev[l][1].record(stream)
-            tf.tf_sparse_decode_attn(q_all[l], Kc[l], Vc[l], seq, idx[l], nsel[l], scale, out=o_sp[l], ws=ws_sp)
+            tf.tf_sparse_decode_attn(st.q[l], st.K[l], st.V[l], st.seq, st.idx[l], st.nsel[l], st.scale,
+                                     out=st.o_sp[l], ws=st.ws_sp)
             ev[l][2].record(stream)
         torch.cuda.synchronize()
-        for i, (k, nb) in enumerate((("topk", bytes_topk), ("sparse", bytes_sparse))):
+        for i, k in enumerate(("topk", "sparse")):
             ms = statistics.mean(ev[l][i].elapsed_time(ev[l][i + 1]) for l in range(layers))
-            kernels["two_call_" + k] = {"ms": round(ms, 5), "GBps": round(nb / (ms / 1e3) / 1e9, 1),
-                                        "frac_hbm": round(nb / (ms / 1e3) / 1e9 / peak, 4)}
-    # level-1 verification over the retrieval cache (not part of the step): the
-    # step's selection, T verify queries, back-to-back calls over the layers
-    ws_sv = tf.workspace(tf.tf_sparse_verify_attn_workspace(B, Hq, Hkv, w.kc, T), dev)
-    o_sv = torch.empty((B, Hq, T, D), dtype=torch.float32, device=dev)
-    for l in range(min(layers, 4)):
-        tf.tf_sparse_verify_attn(Q_all[l], Kc[l], Vc[l], seq, idx[l], nsel[l], scale, out=o_sv, ws=ws_sv)
-    torch.cuda.synchronize()
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
-    for l in range(layers):
-        tf.tf_sparse_verify_attn(Q_all[l], Kc[l], Vc[l], seq, idx[l], nsel[l], scale, out=o_sv, ws=ws_sv)
-    s1.record(stream)
-    torch.cuda.synchronize()
-    sv_ms = s0.elapsed_time(s1) / layers
-    sv_bytes = 2 * B * Hkv * (w.kc * w.chunk + T) * kv_row + B * Hq * T * D * (2 + 4)
-    kernels["sparse_verify_level1"] = {"ms": round(sv_ms, 5), "GBps": round(sv_bytes / (sv_ms / 1e3) / 1e9, 1),
-                                       "frac_hbm": round(sv_bytes / (sv_ms / 1e3) / 1e9 / peak, 4),
-                                       "calls": "tf_sparse_verify_attn", "timing": "back-to-back over the layers"}
+            kernels["two_call_" + k] = kernel_entry(nb[k], ms, peak)
     # the retrieval draft alone, back to back over the layers: consecutive
     # launches overlap through programmatic dependent launch (no events between
     # them), and every layer's means and K/V are cold
+    d0, d1 = _ev(), _ev()
     torch.cuda.synchronize()
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     d0.record(stream)
     for l in range(layers):
         draft(l)
     d1.record(stream)
     torch.cuda.synchronize()
-    dr_ms = d0.elapsed_time(d1) / layers
-    kernels["retrieval_draft"]["back_to_back"] = {
-        "ms": round(dr_ms, 5), "GBps": round(bytes_draft / (dr_ms / 1e3) / 1e9, 1),
-        "frac_hbm": round(bytes_draft / (dr_ms / 1e3) / 1e9 / peak, 4)}
-    # the verify with this layer's cache offloaded to pinned host memory,
-    # streamed over the host link in 16K-position segments (not part of the
-    # step); the peak is a plain pinned host-to-device copy of the same bytes
-    Kh = torch.empty(Kc[0].shape, dtype=Kc[0].dtype, pin_memory=True)
-    Vh = torch.empty(Vc[0].shape, dtype=Vc[0].dtype, pin_memory=True)
-    Kh.copy_(Kc[0])
-    Vh.copy_(Vc[0])
-    off_bytes = 2 * Kh.numel() * 2
-    seg_rows = min(16384, L)
-    ws_off = tf.workspace(tf.tf_verify_attn_offload_workspace(B, Hq, Hkv, L, T, seg_rows), dev)
-    o_off = torch.empty((B, Hq, T, D), dtype=torch.float32, device=dev)
-    side = torch.cuda.Stream()
-    tf.tf_verify_attn_offload(Q_all[0], Kh, Vh, seq, L, scale, out=o_off, ws=ws_off, seg_rows=seg_rows,
-                              copy_stream=side)
-    torch.cuda.synchronize()
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    off_ms = float("inf")
-    for _ in range(3):  # the fastest of several calls, like the copy it is compared with
-        f0.record(stream)
-        tf.tf_verify_attn_offload(Q_all[0], Kh, Vh, seq, L, scale, out=o_off, ws=ws_off, seg_rows=seg_rows,
-                                  copy_stream=side)
-        f1.record(stream)
-        torch.cuda.synchronize()
-        off_ms = min(off_ms, f0.elapsed_time(f1))
-    stage = torch.empty_like(Kc[0])
-    stage.copy_(Kh, non_blocking=True)  # warm the copy path
-    torch.cuda.synchronize()
-    h2d_ms = float("inf")
-    for _ in range(4):  # the fastest of several plain copies of the same bytes
-        f0.record(stream)
-        stage.copy_(Kh, non_blocking=True)
-        stage.copy_(Vh, non_blocking=True)
-        f1.record(stream)
-        torch.cuda.synchronize()
-        h2d_ms = min(h2d_ms, f0.elapsed_time(f1))
-    del stage, Kh, Vh
-    kernels["verify_offloaded_1layer"] = {
-        "ms": round(off_ms, 4), "GBps": round(off_bytes / (off_ms / 1e3) / 1e9, 1),
-        "h2d_copy_GBps": round(off_bytes / (h2d_ms / 1e3) / 1e9, 1),
-        "frac_of_h2d_copy": round(h2d_ms / off_ms, 4), "calls": "tf_verify_attn_offload",
-        "timing": "K/V in pinned host memory, 16K-position segments, copies on a second stream; "
-                  "fastest of 3 calls and of 4 plain copies"}
+    kernels["retrieval_draft"]["back_to_back"] = kernel_entry(nb["draft"], d0.elapsed_time(d1) / layers, peak)
+
+    # level-1 verification over the retrieval cache (not part of the step): the
+    # step's selection, T verify queries, back-to-back calls over the layers;
+    # and its fixed cost: the same call over the first 16 selected chunks
+    ws_sv = tf.workspace(tf.tf_sparse_verify_attn_workspace(B, Hq, Hkv, w.kc, T), dev)
+    o_sv = torch.empty((B, Hq, T, D), dtype=torch.float32, device=dev)
+    kv_row = D * 2
+
+    def sv_calls(idx_all, nsel_all):
+        return [lambda l=l: tf.tf_sparse_verify_attn(st.Q[l], st.K[l], st.V[l], st.seq, idx_all[l], nsel_all[l],
+                                                     st.scale, out=o_sv, ws=ws_sv) for l in range(layers)]
+
+    sv_ms = graph_loop_ms(sv_calls(st.idx, st.nsel), stream)
+    sv_bytes = 2 * B * Hkv * (w.kc * w.chunk + T) * kv_row + B * Hq * T * D * (2 + 4)
+    kernels["sparse_verify_level1"] = dict(kernel_entry(sv_bytes, sv_ms, peak), calls="tf_sparse_verify_attn",
+                                           timing="back to back over the layers, replayed as one CUDA graph")
+    idx16 = torch.full_like(st.idx, -1)
+    idx16[:, :, :, :16] = st.idx[:, :, :, :16]
+    nsel16 = torch.clamp(st.nsel, max=16)
+    kernels["sparse_verify_level1"]["floor_kc16_us"] = round(graph_loop_ms(sv_calls(idx16, nsel16), stream) * 1e3, 2)
+    # the window: back to back, and its fixed cost with 4 sinks + 12 recent rows (16 rows) per unit
+    ws_w16 = tf.workspace(tf.tf_stream_window_attn_workspace(B, Hq, Hkv, 4, 12), dev)
+    o_w16 = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    win_ms = graph_loop_ms([lambda l=l: tf.tf_stream_window_attn(st.q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window,
+                                                                 st.scale, out=st.o_win[l], ws=st.ws_win)
+                            for l in range(layers)], stream)
+    kernels["window"]["back_to_back"] = dict(kernel_entry(nb["window"], win_ms, peak),
+                                             timing="replayed as one CUDA graph")
+    kernels["window"]["floor_16rows_us"] = round(graph_loop_ms(
+        [lambda l=l: tf.tf_stream_window_attn(st.q[l], st.K[l], st.V[l], st.seq, 4, 12, st.scale, out=o_w16,
+                                              ws=ws_w16) for l in range(layers)], stream) * 1e3, 2)
+
+    # the offloaded setting (one 128K layer; not part of the step)
+    measure_offload(st, tf, stream, peak, kernels)
     kernels["chunk_means_prefill_1layer"] = {"ms": round(means_ms, 4),
                                              "GBps": round(means_bytes / (means_ms / 1e3) / 1e9, 1)}
     ver_ms = statistics.mean(per_kind["verify"])
-    achieved = bytes_verify / (ver_ms / 1e3) / 1e9
+    achieved = nb["verify"] / (ver_ms / 1e3) / 1e9
     traffic = recorded_traffic("verify_attn.cu", w.name)
 
     result = {
@@ -481,15 +729,16 @@ def run_gpu(args):
                    "launch": "one CUDA graph per step" if args.graph else "stream launches"},
         "roofline": {"bound": "hbm", "kernel": "tf_verify_attn", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes": bytes_verify, "peak_source": peak_kind},
+                     "algorithmic_bytes": nb["verify"], "peak_source": peak_kind},
         "kernels": kernels,
         "kernel_timing": f"CUDA events around every launch, {k_steps} further steps after the timed region",
         "gpu_launches": args.steps * layers * (4 if args.two_call_draft else 3),
-        "clocks": clocks.summary(),
+        "clocks": clocks,
     }
 
     # ---- accept / resample (latency-bound; reported in microseconds per call):
-    # the two-level step of a batch of 8 over vocabulary 32000, gamma 4 then 5.
+    # the two-level step of a batch of 8 over vocabulary 32000, gamma 4 then 5,
+    # and the tree form on a binary tree of 14 candidates
     acc = synth.two_level_inputs(8, 4, w.vocab, seed=4, device=dev)
     q_lvl1 = acc["q"][:, :5].contiguous()
     ws_a1 = tf.workspace(tf.tf_spec_accept_workspace(8, 4), dev)
@@ -504,23 +753,37 @@ def run_gpu(args):
                           out_tokens=outs1[2], ws=ws_a1)
         tf.tf_spec_accept(acc["p"], acc["q"], outs1[2], acc["u2"], acc["ur2"], n_acc=outs2[0], next_token=outs2[1],
                           out_tokens=outs2[2], ws=ws_a2)
-    for _ in range(3):
-        two_level()
-    torch.cuda.synchronize()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    for _ in range(20):
-        two_level()
-    a1.record(stream)
-    torch.cuda.synchronize()
-    kernels["spec_accept_two_level_b8_v32000"] = {"us_per_step": round(a0.elapsed_time(a1) / 20 * 1e3, 2),
-                                                  "launches_per_step": 4}
+
+    def per_call_us(fn, n=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a0, a1 = _ev(), _ev()
+        a0.record(stream)
+        for _ in range(n):
+            fn()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return round(a0.elapsed_time(a1) / n * 1e3, 2)
+
+    kernels["spec_accept_two_level_b8_v32000"] = {"us_per_step": per_call_us(two_level), "launches_per_step": 4}
+    tri = synth.tree_accept_inputs(8, 14, w.vocab, seed=5, device=dev, branching=2)
+    ws_t = tf.workspace(tf.tf_spec_accept_tree_workspace(8, 14, w.vocab), dev)
+    t_out = [torch.empty(8, dtype=torch.int32, device=dev) for _ in range(2)] + [
+        torch.empty((8, 15), dtype=torch.int32, device=dev), torch.empty((8, 14), dtype=torch.int32, device=dev)]
+
+    def tree_accept():
+        tf.tf_spec_accept_tree(tri["tgt"], tri["drf"], tri["x"], tri["parent"], tri["u_acc"], tri["u_res"],
+                               n_acc=t_out[0], next_token=t_out[1], out_tokens=t_out[2], acc_nodes=t_out[3], ws=ws_t)
+
+    kernels["spec_accept_tree_binary_t14_b8_v32000"] = {"us_per_call": per_call_us(tree_accept),
+                                                         "launches_per_call": 2}
 
     # ---- end to end through the public API with host buffers
     if not args.no_e2e:
-        q_host = q_all.cpu().pin_memory()
-        Q_host = Q_all.cpu().pin_memory()
-        outs_host = [t.cpu().pin_memory() for t in (o_sp, o_win, o_ver)]
+        q_host = st.q.cpu().pin_memory()
+        Q_host = st.Q.cpu().pin_memory()
+        outs_host = [t.cpu().pin_memory() for t in (st.o_sp, st.o_win, st.o_ver)]
         h2d = q_host.numel() * 2 + Q_host.numel() * 2
         d2h = sum(t.numel() * 4 for t in outs_host)
         e_steps = max(3, args.steps // 2)
@@ -528,19 +791,30 @@ def run_gpu(args):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(e_steps):
-            q_all.copy_(q_host, non_blocking=True)
-            Q_all.copy_(Q_host, non_blocking=True)
+            st.q.copy_(q_host, non_blocking=True)
+            st.Q.copy_(Q_host, non_blocking=True)
             run_step()
-            for h, d in zip(outs_host, (o_sp, o_win, o_ver)):
+            for h, d in zip(outs_host, (st.o_sp, st.o_win, st.o_ver)):
                 h.copy_(d, non_blocking=True)
             torch.cuda.current_stream().synchronize()
         e_value, _ = job_throughput(e_steps, time.perf_counter() - t0, world)
         result["e2e"] = {"value": round(e_value, 4), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                          "d2h_bytes_per_step": d2h}
 
+    del st, run_step, step, draft
+    if args.graph:
+        del graph
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads, one after the other (each frees its cache)
+    extra = [x for x in args.extra_workloads.split(",") if x and x != "none" and x != w.name]
+    if extra and args.layers is None:
+        result["workloads"] = {}
+        for name in extra:
+            result["workloads"][name] = measure_extra_workload(synth.WORKLOADS[name], args, tf, synth, dev, stream,
+                                                               world, local, peak)
+
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        del Kc, Vc, Mc
-        torch.cuda.empty_cache()
         result["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -554,8 +828,8 @@ def run_gpu(args):
 
 
 def run_reference(args):
-    """The float64 oracle on host cores; each step is one (layer, KV head) unit
-    of the workload, scaled to a full step."""
+    """The float64 oracle on every host core; each step is one batch of
+    (layer, KV head) units (one per worker), scaled to a full step."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
@@ -563,9 +837,9 @@ def run_reference(args):
     from hierarchical_speculative_decoding_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm state; warm-up steps would only repeat the sample
-    cb = cpu_baseline(w, n_units=max(1, args.steps))
+    # the oracle has no warm state; the pool's workers import everything before
+    # the clock starts
+    cb = cpu_baseline(w, units_per_worker=max(1, args.steps))
     step_s = 1.0 / cb["value"]
     out = {"metric": METRIC, "value": cb["value"], "unit": "steps/s", "n_gpus": args.gpus, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True,

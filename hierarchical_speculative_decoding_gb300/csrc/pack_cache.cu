@@ -11,10 +11,12 @@
 // over the host link, from pinned host memory.
 //
 // Design: a grid of (list slices, units) CTAs.  Every CTA of a unit recomputes
-// the unit's packed offsets itself (one warp scans the row counts of the <= kc
-// listed chunks, a few hundred integers), then copies its slice of the list:
-// one chunk (8 rows of K and of V, 4 KiB) per 256-thread step, 16 bytes per
-// thread, two chunks in flight.  No CTA waits on another.
+// the unit's packed offsets itself: each thread loads its run of the <= kc
+// listed ids at once, and one block-wide scan of their valid row counts gives
+// every entry's first packed row (a single round trip, no chain of dependent
+// loads); the CTA keeps those of its own slice of 16 entries.  It then copies
+// that slice: 8 rows of K and of V per chunk (4 KiB), 16 bytes per thread,
+// eight chunks in flight.  No CTA waits on another.
 #include "tf_common.cuh"
 
 namespace tf {
@@ -22,7 +24,9 @@ namespace {
 
 constexpr int kPackThreads = 256;     // 128 threads for a chunk's K rows, 128 for its V rows
 constexpr int kPackMaxList = 4096;    // listed chunks per unit
+constexpr int kPackPerThread = kPackMaxList / kPackThreads;  // ids scanned per thread
 constexpr int kPackChunksPerCta = 16;
+constexpr int kPackInFlight = 8;
 
 // Plain (coherent) 16-byte load: the source may be host memory.
 __device__ __forceinline__ uint4 ld_global16(const void* p) {
@@ -38,76 +42,85 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const uint16_t* K, c
                                                             int kc, uint16_t* __restrict__ Kc,
                                                             uint16_t* __restrict__ Vc, int32_t* __restrict__ lens,
                                                             int32_t* __restrict__ n_chunks) {
-  __shared__ int s_c[kPackMaxList];    // chunk id of each listed entry, -1 if not a valid chunk
-  __shared__ int s_off[kPackMaxList];  // its first packed row
+  __shared__ int s_c[kPackChunksPerCta];    // chunk id of each entry of this CTA's slice, -1 if not a valid chunk
+  __shared__ int s_off[kPackChunksPerCta];  // its first packed row
+  __shared__ int s_wsum[kPackThreads / 32];
   const int unit = blockIdx.y;
   const int b = unit / Hkv;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   pdl_wait();
   const int L = clamp_len(seq_lens[b], Lmax);
   const int C = (L + kChunk - 1) / kChunk;
   int ns = n_sel[unit];
   ns = ns < 0 ? 0 : (ns > kc ? kc : ns);
+  const int i0 = blockIdx.x * kPackChunksPerCta;
+  const int i1 = min(ns, i0 + kPackChunksPerCta);
 
-  if (threadIdx.x < 32) {
-    // Exclusive scan of the entries' valid row counts, 32 entries at a time.
-    const int lane = threadIdx.x;
-    int carry = 0;
-    for (int base = 0; base < ns; base += 32) {
-      const int i = base + lane;
-      int c = -1, rows = 0;
-      if (i < ns) {
-        c = idx[(size_t)unit * kc + i];
-        if (c >= 0 && c < C) rows = min(kChunk, L - c * kChunk);
-        else c = -1;  // an id outside the context contributes no row
-      }
-      int incl = rows;
+  // Exclusive scan of the entries' valid row counts: thread t owns entries
+  // [t * q, (t + 1) * q), all its ids loaded together.
+  const int q = (ns + kPackThreads - 1) / kPackThreads;  // <= kPackPerThread
+  int cid[kPackPerThread], rows[kPackPerThread];
+  int mine = 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      if (i < ns) {
-        s_c[i] = c;
-        s_off[i] = carry + incl - rows;
-      }
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+  for (int k = 0; k < kPackPerThread; ++k) {
+    const int e = t * q + k;
+    cid[k] = (k < q && e < ns) ? idx[(size_t)unit * kc + e] : -1;
+  }
+#pragma unroll
+  for (int k = 0; k < kPackPerThread; ++k) {
+    const int c = cid[k];
+    rows[k] = (c >= 0 && c < C) ? min(kChunk, L - c * kChunk) : 0;  // an id outside the context adds no row
+    mine += rows[k];
+  }
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int run = incl - mine;
+  for (int w = 0; w < warp; ++w) run += s_wsum[w];
+#pragma unroll
+  for (int k = 0; k < kPackPerThread; ++k) {
+    const int e = t * q + k;
+    if (k < q && e >= i0 && e < i1) {
+      s_c[e - i0] = rows[k] > 0 ? cid[k] : -1;
+      s_off[e - i0] = run;
     }
-    if (lane == 0 && blockIdx.x == 0) {
-      lens[unit] = carry;
-      n_chunks[unit] = (carry + kChunk - 1) / kChunk;
-    }
+    run += rows[k];
+  }
+  if (t == kPackThreads - 1 && blockIdx.x == 0) {
+    lens[unit] = run;  // the last thread's running total is the unit's row count
+    n_chunks[unit] = (run + kChunk - 1) / kChunk;
   }
   __syncthreads();
 
-  const int i0 = blockIdx.x * kPackChunksPerCta;
-  const int i1 = min(ns, i0 + kPackChunksPerCta);
-  const int t = threadIdx.x;
   const bool is_v = t >= kPackThreads / 2;
   const int r = (t >> 4) & 7;  // row within the chunk
   const int piece = t & 15;    // 16-byte piece within the row
   const size_t cap = (size_t)kc * kChunk;
   const uint16_t* src = (is_v ? V : K) + (size_t)unit * Lmax * kHeadDim + piece * 8;
   uint16_t* dst = (is_v ? Vc : Kc) + (size_t)unit * cap * kHeadDim + piece * 8;
-  for (int i = i0; i < i1; i += 2) {
-    uint4 v[2];
-    int drow[2];
-    bool ok[2];
+  for (int i = i0; i < i1; i += kPackInFlight) {
+    uint4 v[kPackInFlight];
+    int drow[kPackInFlight];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < kPackInFlight; ++u) {
       const int e = i + u;
-      ok[u] = false;
+      drow[u] = -1;
       if (e < i1) {
-        const int c = s_c[e];
+        const int c = s_c[e - i0];
         if (c >= 0 && r < min(kChunk, L - c * kChunk)) {
-          ok[u] = true;
-          drow[u] = s_off[e] + r;
+          drow[u] = s_off[e - i0] + r;
           v[u] = ld_global16(src + ((size_t)c * kChunk + r) * kHeadDim);
         }
       }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u)
-      if (ok[u]) *reinterpret_cast<uint4*>(dst + (size_t)drow[u] * kHeadDim) = v[u];
+    for (int u = 0; u < kPackInFlight; ++u)
+      if (drow[u] >= 0) *reinterpret_cast<uint4*>(dst + (size_t)drow[u] * kHeadDim) = v[u];
   }
 }
 
