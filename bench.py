@@ -275,15 +275,24 @@ def _ev():
     return torch.cuda.Event(enable_timing=True)
 
 
+_FLUSH = {}
+
+
 def _median_call_ms(fn, stream, reps=5, warm=1):
-    """Median duration of fn() with CUDA events on `stream` around each call."""
+    """Median device time of fn() on `stream`, each call bracketed by CUDA
+    events behind a queued 512 MB memset: the memset keeps the GPU busy while
+    the host enqueues the event, the call and the closing event (so host launch
+    cost is not timed) and leaves L2 cold."""
     import torch
 
+    if "buf" not in _FLUSH:
+        _FLUSH["buf"] = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=torch.cuda.current_device())
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
     out = []
     for _ in range(reps):
+        _FLUSH["buf"].zero_()
         a, b = _ev(), _ev()
         a.record(stream)
         fn()
@@ -755,18 +764,10 @@ def run_gpu(args):
                           out_tokens=outs2[2], ws=ws_a2)
 
     def per_call_us(fn, n=20):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        a0, a1 = _ev(), _ev()
-        a0.record(stream)
-        for _ in range(n):
-            fn()
-        a1.record(stream)
-        torch.cuda.synchronize()
-        return round(a0.elapsed_time(a1) / n * 1e3, 2)
+        return round(graph_loop_ms([fn] * n, stream) * 1e3, 2)
 
-    kernels["spec_accept_two_level_b8_v32000"] = {"us_per_step": per_call_us(two_level), "launches_per_step": 4}
+    kernels["spec_accept_two_level_b8_v32000"] = {"us_per_step": per_call_us(two_level), "launches_per_step": 4,
+                                                  "timing": "20 steps replayed as one CUDA graph"}
     tri = synth.tree_accept_inputs(8, 14, w.vocab, seed=5, device=dev, branching=2)
     ws_t = tf.workspace(tf.tf_spec_accept_tree_workspace(8, 14, w.vocab), dev)
     t_out = [torch.empty(8, dtype=torch.int32, device=dev) for _ in range(2)] + [
@@ -777,7 +778,8 @@ def run_gpu(args):
                                n_acc=t_out[0], next_token=t_out[1], out_tokens=t_out[2], acc_nodes=t_out[3], ws=ws_t)
 
     kernels["spec_accept_tree_binary_t14_b8_v32000"] = {"us_per_call": per_call_us(tree_accept),
-                                                         "launches_per_call": 2}
+                                                         "launches_per_call": 2,
+                                                         "timing": "20 calls replayed as one CUDA graph"}
 
     # ---- end to end through the public API with host buffers
     if not args.no_e2e:

@@ -47,13 +47,20 @@ _SIGS = {
     "tf_pack_retrieval_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tf_spec_accept_workspace": (_S, [_I, _I]),
     "tf_spec_accept": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _S, _P]),
+    "tf_debug_status": (_I, [_P, _I]),
     "tf_spec_accept_tree_workspace": (_S, [_I, _I, _I]),
     "tf_spec_accept_tree": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _S, _P]),
 }
 
 
+def debug_variant() -> bool:
+    """TF_LIBRARY=debug in the environment selects the checked build of the
+    library (every gather index checked, see tf_debug_status)."""
+    return os.environ.get("TF_LIBRARY", "") == "debug"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.library(debug_variant())
 
 
 def load(build_if_needed: bool = True):
@@ -61,11 +68,13 @@ def load(build_if_needed: bool = True):
     global _lib
     if _lib is not None:
         return _lib
-    if build_if_needed and not _build.up_to_date():
-        _build.build()
-    if not os.path.exists(_build.LIB):
-        raise RuntimeError(f"CUDA library missing: {_build.LIB} (run build())")
-    lib = ctypes.CDLL(_build.LIB)
+    dbg = debug_variant()
+    path = _build.library(dbg)
+    if build_if_needed and not _build.up_to_date(dbg):
+        _build.build(debug=dbg)
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library missing: {path} (run build())")
+    lib = ctypes.CDLL(path)
     for name, (res, args) in _SIGS.items():
         fn = getattr(lib, name)
         fn.restype = res
@@ -128,6 +137,14 @@ def tf_check_status(ws, stream=None) -> int:
     if status not in (0, TF_ERR_DEVICE_DATA):
         _check(status, "tf_check_status")
     return status
+
+
+def tf_debug_status(clear: bool = False):
+    """(status, flags): the bounds violations the checked build has recorded on
+    the current device (0: none); status 2 (unsupported) from a release build."""
+    flags = _c.c_uint32(0)
+    status = load().tf_debug_status(_c.byref(flags), 1 if clear else 0)
+    return status, int(flags.value)
 
 
 def _ws(ws, need, device):

@@ -28,3 +28,21 @@ extern "C" tf_status tf_check_status(void* ws, size_t ws_bytes, tf_stream_t stre
   if (cudaMemsetAsync(ws, 0, ws_bytes, s) != cudaSuccess) return TF_ERR_CUDA;
   return TF_ERR_DEVICE_DATA;
 }
+
+extern "C" tf_status tf_debug_status(uint32_t* flags, int clear) {
+  if (!flags) return TF_ERR_INVALID_ARG;
+  *flags = 0;
+#ifdef TF_DEBUG
+  using namespace tf;
+  const uint32_t words[] = {dbg_read_chunk_means(clear), dbg_read_gather(clear), dbg_read_verify(clear),
+                            dbg_read_topk(clear),        dbg_read_draft(clear),  dbg_read_pack(clear)};
+  for (uint32_t w : words) {
+    if (w == ~0u) return TF_ERR_CUDA;
+    *flags |= w;
+  }
+  return TF_OK;
+#else
+  (void)clear;
+  return TF_ERR_UNSUPPORTED;
+#endif
+}

@@ -46,6 +46,7 @@ struct Item {
   const uint16_t* src;
   uint16_t* dst;
   int n;
+  bool ok;  // (debug builds) the chunk lies inside the index and its rows inside the cache
 };
 
 // A thread's walk over the items.  The grid stride is a multiple of 16 items,
@@ -67,7 +68,8 @@ __device__ __forceinline__ Item item_at(const Walk& w, const uint16_t* K, const 
   Item it;
   it.src = K + (bg * Lmax + (size_t)c * kChunk) * kHeadDim + w.slice * 8;
   it.dst = M + (bg * Cmax + c) * kHeadDim + w.slice * 8;
-  it.n = n;
+  it.ok = TF_DBG_OK(c >= 0 && c < Cmax, kDbgIndexRow) && TF_DBG_OK(n == 0 || c * kChunk + n <= L, kDbgCacheRow);
+  it.n = it.ok ? n : 0;
   return it;
 }
 
@@ -94,6 +96,7 @@ __device__ __forceinline__ void load_rows(const Item& it, uint4 (&rows)[kChunk])
 
 // Exact mean of the rows, rounded once to bf16, stored as 8 head dims.
 __device__ __forceinline__ void mean_store(const Item& it, const uint4 (&rows)[kChunk]) {
+  if (!it.ok) return;
   float hi[8], lo[8];
 #pragma unroll
   for (int d = 0; d < 8; ++d) {
@@ -187,6 +190,9 @@ __global__ void __launch_bounds__(256) chunk_means_kernel(const uint16_t* __rest
 }
 
 }  // namespace
+
+TF_DBG_READER(dbg_read_chunk_means)
+
 }  // namespace tf
 
 extern "C" tf_status tf_build_chunk_means(const uint16_t* K, const int32_t* seq_lens, int B, int Hkv,

@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_attn_kernel(GatherPa
     const uint16_t* Ku = p.K + (size_t)unit * p.Lmax * kHeadDim;
     const uint16_t* Vu = p.V + (size_t)unit * p.Lmax * kHeadDim;
     auto issue = [&](int slot, int y, int n) {
+      if (!TF_DBG_OK(n == 0 || (y >= 0 && n <= kChunk && y + n <= L && L <= p.Lmax), kDbgCacheRow)) n = 0;
       slot_n[slot] = n;
       uint8_t* dst = ring + slot * kSlotBytes;
       const uint32_t bytes = (uint32_t)n * kHeadDim * 2;
@@ -449,6 +450,8 @@ tf_status gather_launch(int mode, GatherParams p, int units, int rows, int P_max
     default: return launch_mode<4>(mode, p, ug, stream);
   }
 }
+
+TF_DBG_READER(dbg_read_gather)
 
 }  // namespace tf
 

@@ -14,7 +14,7 @@
 // the unit's packed offsets itself: each thread loads its run of the <= kc
 // listed ids at once, and one block-wide scan of their valid row counts gives
 // every entry's first packed row (a single round trip, no chain of dependent
-// loads); the CTA keeps those of its own slice of 16 entries.  It then copies
+// loads); the CTA keeps those of its own slice of 64 entries.  It then copies
 // that slice: 8 rows of K and of V per chunk (4 KiB), 16 bytes per thread,
 // eight chunks in flight.  No CTA waits on another.
 #include "tf_common.cuh"
@@ -25,7 +25,7 @@ namespace {
 constexpr int kPackThreads = 256;     // 128 threads for a chunk's K rows, 128 for its V rows
 constexpr int kPackMaxList = 4096;    // listed chunks per unit
 constexpr int kPackPerThread = kPackMaxList / kPackThreads;  // ids scanned per thread
-constexpr int kPackChunksPerCta = 16;
+constexpr int kPackChunksPerCta = 64;
 constexpr int kPackInFlight = 8;
 
 // Plain (coherent) 16-byte load: the source may be host memory.
@@ -112,7 +112,8 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const uint16_t* K, c
       drow[u] = -1;
       if (e < i1) {
         const int c = s_c[e - i0];
-        if (c >= 0 && r < min(kChunk, L - c * kChunk)) {
+        if (c >= 0 && r < min(kChunk, L - c * kChunk) && TF_DBG_OK(c * kChunk + r < L && L <= Lmax, kDbgCacheRow) &&
+            TF_DBG_OK(s_off[e - i0] + r < (int)cap, kDbgPacked)) {
           drow[u] = s_off[e - i0] + r;
           v[u] = ld_global16(src + ((size_t)c * kChunk + r) * kHeadDim);
         }
@@ -144,6 +145,9 @@ bool kernel_readable(const void* p) {
 }
 
 }  // namespace
+
+TF_DBG_READER(dbg_read_pack)
+
 }  // namespace tf
 
 extern "C" tf_status tf_pack_retrieval_cache(const uint16_t* K, const uint16_t* V, const int32_t* seq_lens,

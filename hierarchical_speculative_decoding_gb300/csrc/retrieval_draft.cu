@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
     qsm[h * kHeadDim + u * 4 + (d & 3)] = v;
   }
   __syncthreads();
-  topk::score_slice<8>(qs, p.M + (size_t)unit * Cmax * kHeadDim, c0, c1, a);
+  topk::score_slice<8>(qs, p.M + (size_t)unit * Cmax * kHeadDim, c0, c1, a, Cmax);
   __syncthreads();
 
   const uint16_t* Ku = p.K + (size_t)unit * p.Lmax * kHeadDim;
@@ -183,7 +183,8 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
       return;
     }
     const int y = c * kChunk;
-    const int nr = min(kChunk, L - y);
+    int nr = min(kChunk, L - y);
+    if (!TF_DBG_OK(nr > 0 && y + nr <= L && L <= p.Lmax, kDbgCacheRow)) nr = 0;
     slot_n[slot] = nr;
     const uint32_t bytes = (uint32_t)nr * kHeadDim * 2;
     uint8_t* dst = ring + slot * kSlotBytes;
@@ -561,6 +562,9 @@ tf_status launch_draft(const DraftParams& p, int units, int Cmax, cudaStream_t s
 }
 
 }  // namespace
+
+TF_DBG_READER(dbg_read_draft)
+
 }  // namespace tf
 
 extern "C" tf_status tf_retrieval_draft_attn(const uint16_t* q, const uint16_t* M, const uint16_t* K,

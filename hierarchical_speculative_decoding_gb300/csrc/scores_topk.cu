@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kThreads, 2) scores_topk_kernel(
     qs[threadIdx.x] = s;
   }
   __syncthreads();
-  topk::score_slice(qs, M + (size_t)unit * Cmax * kHeadDim, c0, c1, a);
+  topk::score_slice(qs, M + (size_t)unit * Cmax * kHeadDim, c0, c1, a, Cmax);
   __syncthreads();
   int32_t* out = idx + (size_t)unit * kc;
 
@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(kThreads, 2) scores_topk_kernel(
 }
 
 }  // namespace
+TF_DBG_READER(dbg_read_topk)
+
 }  // namespace tf
 
 extern "C" size_t tf_chunk_scores_topk_workspace(int B, int Hkv, int Lmax, int chunk) {

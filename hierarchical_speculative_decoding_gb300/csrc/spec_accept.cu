@@ -413,10 +413,9 @@ size_t norm_bytes(int B, int gamma) {
 //
 // One block per sequence.  Warp 0 walks the tree (next child by ballot over
 // the parent links, fp64 ratio tests from the normalisers, as in the chain
-// kernel); only a rejection needs the whole block, for one pass over the
-// vocabulary that writes the residual into one of two workspace rows (the
-// other keeps p' in case the residual is all zero) and sums it.  The final
-// draw scans the row holding p' with the chain kernel's fp32-pair scan.
+// kernel); only a rejection needs the whole block, for a pass over the
+// vocabulary that forms the residual and sums it.  The final draw scans the
+// row holding p' with the chain kernel's fp32-pair scan.
 struct TreeParams {
   const float* tgt;      // [B, T+1, V]
   const float* drf;      // [B, T, V]
@@ -435,20 +434,23 @@ struct TreeParams {
   int32_t* acc_nodes;   // [B, T] or null
 };
 
-// Index-order inverse CDF over w[0, V) with 1024 threads (every thread of the
-// block): each thread owns a contiguous slice, the slice sums are scanned as
-// exact fp32 pairs, one thread forms the crossing u * total in fp64 and the
-// slice holding it is walked again.  Returns the drawn index (all threads);
-// the last index with positive weight if rounding leaves no crossing.
-__device__ int block_inverse_cdf(const float* __restrict__ w, int V, double u) {
+// Index-order inverse CDF over the weights of tokens [0, V) with 1024 threads
+// (every thread of the block): thread g owns the contiguous slice of tokens
+// [g * seg, (g + 1) * seg), stored at w[g * pitch + k] (pitch = seg: a plain
+// row; seg + 1: the bank-conflict-free shared-memory layout); the slice sums
+// are scanned as exact fp32 pairs, one thread forms the crossing u * total in
+// fp64 and the slice holding it is walked again.  Returns the drawn index (all
+// threads); the last index with positive weight if rounding leaves no crossing.
+__device__ int block_inverse_cdf(const float* __restrict__ w, int V, int pitch, double u) {
   constexpr int GS = kBlockSeq;
   __shared__ float s_ph[32], s_pl[32], s_th, s_tl;
   __shared__ int s_found[32], s_lastv[32];
   const int gid = threadIdx.x, lane = gid & 31, warp = gid >> 5, nw = GS / 32;
   const int seg = (V + GS - 1) / GS;
   const int t0 = min(V, gid * seg), t1 = min(V, t0 + seg);
+  const float* mine = w + (size_t)gid * pitch - t0;  // mine[t]: the weight of token t of this slice
   float run = 0.0f;
-  for (int t = t0; t < t1; ++t) run += w[t];
+  for (int t = t0; t < t1; ++t) run += mine[t];
   float ih = run, il = 0.0f;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -493,7 +495,7 @@ __device__ int block_inverse_cdf(const float* __restrict__ w, int V, double u) {
   if (holds) {
     float r2 = 0.0f;
     for (int t = t0; t < t1; ++t) {
-      r2 += w[t];
+      r2 += mine[t];
       if (r2 > gap) {
         found = t;
         break;
@@ -502,7 +504,7 @@ __device__ int block_inverse_cdf(const float* __restrict__ w, int V, double u) {
   }
   if (!__syncthreads_or(found != 0x7fffffff)) {
     for (int t = t0; t < t1; ++t)
-      if (w[t] > 0.0f) last = t;
+      if (mine[t] > 0.0f) last = t;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -528,18 +530,39 @@ __device__ __forceinline__ int tree_parent(const int32_t* par, int j) {
   return (pj >= -1 && pj < j) ? pj : -1;
 }
 
+// SMEM: p' after a rejection is held in dynamic shared memory (one row, the
+// bank-conflict-free slice layout of the chain kernel's staging: token e at
+// (e / seg) * (seg + 1) + e % seg); each rejection then takes two passes, the
+// residual's sum and, only when that sum is positive, its in-place write, so
+// an all-zero residual still leaves p' as it was.  Otherwise (vocabularies
+// too large for shared memory) p' lives in two workspace rows, the residual
+// written into the row that does not hold p'.
+template <bool SMEM>
 __global__ void __launch_bounds__(kBlockSeq) tree_accept_kernel(TreeParams p) {
+  extern __shared__ float s_w[];
   __shared__ int s_node, s_staged, s_rej, s_depth;
   __shared__ double s_Z, s_part[32];
   pdl_wait();
   const int b = blockIdx.x, T = p.T, V = p.V, R = 2 * T + 1;
   const int gid = threadIdx.x, lane = gid & 31, warp = gid >> 5;
+  const int seg = (V + kBlockSeq - 1) / kBlockSeq;
   const int32_t* tok = p.tokens + (size_t)b * T;
   const int32_t* par = p.parent + (size_t)b * T;
-  float* buf = p.wbuf + (size_t)b * 2 * p.Vpad;
+  float* buf = SMEM ? s_w : p.wbuf + (size_t)b * 2 * p.Vpad;
+  // where token e of the p' row `which` is stored (e / seg as a multiply-high
+  // by the rounded-up reciprocal of seg, exact for e < 2^32 / seg; seg = 1,
+  // whose reciprocal 2^32 does not fit 32 bits, is the identity)
+  const uint32_t recip = seg > 1 ? (uint32_t)((0xffffffffull + (uint32_t)seg) / (uint32_t)seg) : 0u;
+  auto at = [&](int which, int e) -> size_t {
+    if (SMEM) {
+      const int o = seg > 1 ? (int)__umulhi((uint32_t)e, recip) : e;
+      return (size_t)o * (seg + 1) + (e - o * seg);
+    }
+    return (size_t)which * p.Vpad + e;
+  };
   // Walk state, kept by thread 0 and published for the block: the current
-  // node (-1: the prefix); which workspace row holds p' (-1: p' is the
-  // verifier row after the node) and its sum.
+  // node (-1: the prefix); which row holds p' (-1: p' is the verifier row
+  // after the node) and its sum.
   if (gid == 0) {
     s_node = -1;
     s_staged = -1;
@@ -585,7 +608,7 @@ __global__ void __launch_bounds__(kBlockSeq) tree_accept_kernel(TreeParams p) {
             const double zp = p.ws.z[(size_t)b * R + row];
             accept = (exp2(lq) / zq == 0.0) || ua <= exp2(lp - lq) * (zq / zp);
           } else {
-            const double wx = (double)buf[(size_t)staged * p.Vpad + x];
+            const double wx = (double)buf[at(staged, x)];
             accept = (exp2(lq) / zq == 0.0) || ua <= (wx / Z) * zq / exp2(lq);
           }
           if (accept) {
@@ -614,7 +637,7 @@ __global__ void __launch_bounds__(kBlockSeq) tree_accept_kernel(TreeParams p) {
     if (rej < 0) break;
     // ---- residual of p' against the rejected candidate's drafter row
     const int node = s_node, staged = s_staged;
-    const int dst = staged == 0 ? 1 : 0;
+    const int dst = SMEM ? 0 : (staged == 0 ? 1 : 0);
     const float* qr = p.drf + ((size_t)b * T + rej) * V;
     const float qm = p.ws.m[(size_t)b * R + T + 1 + rej];
     const float inv_zq = (float)(1.0 / p.ws.z[(size_t)b * R + T + 1 + rej]);
@@ -622,41 +645,49 @@ __global__ void __launch_bounds__(kBlockSeq) tree_accept_kernel(TreeParams p) {
     const float pm = p.ws.m[(size_t)b * R + node + 1];
     const float inv_zp = (float)(1.0 / p.ws.z[(size_t)b * R + node + 1]);
     const float inv_Z = staged >= 0 ? (float)(1.0 / s_Z) : 0.0f;
-    const float* src = buf + (size_t)(staged >= 0 ? staged : 0) * p.Vpad;
-    float* out = buf + (size_t)dst * p.Vpad;
+    auto resid = [&](int t) {
+      const float cur = staged >= 0 ? buf[at(staged, t)] * inv_Z : exp2f(__ldg(pr + t) * p.inv_t - pm) * inv_zp;
+      return fmaxf(cur - exp2f(__ldg(qr + t) * p.inv_t - qm) * inv_zq, 0.0f);
+    };
     double part = 0.0;
     for (int t = gid; t < V; t += kBlockSeq) {
-      const float cur = staged >= 0 ? src[t] * inv_Z : exp2f(__ldg(pr + t) * p.inv_t - pm) * inv_zp;
-      const float r = fmaxf(cur - exp2f(__ldg(qr + t) * p.inv_t - qm) * inv_zq, 0.0f);
-      out[t] = r;
+      const float r = resid(t);
+      if (!SMEM) buf[at(dst, t)] = r;
       part += (double)r;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     if (lane == 0) s_part[warp] = part;
     __syncthreads();
-    if (gid == 0) {
-      double z = 0.0;
-      for (int w = 0; w < kBlockSeq / 32; ++w) z += s_part[w];
-      if (z > 0.0) {  // an all-zero residual leaves p' as it was
-        s_staged = dst;
-        s_Z = z;
+    double z = 0.0;
+    for (int w = 0; w < kBlockSeq / 32; ++w) z += s_part[w];
+    if (SMEM && z > 0.0) {
+      // the same residual again, now written over p' (each token by one thread)
+      for (int t = gid; t < V; t += kBlockSeq) {
+        const float r = resid(t);
+        buf[at(0, t)] = r;
       }
     }
     __syncthreads();
+    if (gid == 0 && z > 0.0) {  // an all-zero residual leaves p' as it was
+      s_staged = dst;
+      s_Z = z;
+    }
+    __syncthreads();
   }
-  // ---- the draw: p' into a workspace row if it is still a verifier row
+  // ---- the draw: p' into a row if it is still a verifier row
   const int node = s_node, depth = s_depth;
   int staged = s_staged;
   if (staged < 0) {
     const float* pr = p.tgt + ((size_t)b * (T + 1) + node + 1) * V;
     const float pm = p.ws.m[(size_t)b * R + node + 1];
     const float inv_zp = (float)(1.0 / p.ws.z[(size_t)b * R + node + 1]);
-    for (int t = gid; t < V; t += kBlockSeq) buf[t] = exp2f(__ldg(pr + t) * p.inv_t - pm) * inv_zp;
+    for (int t = gid; t < V; t += kBlockSeq) buf[at(0, t)] = exp2f(__ldg(pr + t) * p.inv_t - pm) * inv_zp;
     staged = 0;
     __syncthreads();
   }
-  const int next = block_inverse_cdf(buf + (size_t)staged * p.Vpad, V, (double)p.u_res[b]);
+  const int next = SMEM ? block_inverse_cdf(buf, V, seg + 1, (double)p.u_res[b])
+                        : block_inverse_cdf(buf + (size_t)staged * p.Vpad, V, seg, (double)p.u_res[b]);
   if (gid == 0) {
     p.n_acc[b] = depth;
     p.next_token[b] = next;
@@ -773,7 +804,18 @@ extern "C" tf_status tf_spec_accept_tree(const float* tgt_logits, const float* d
   else
     e = launch_pdl(row_norm_kernel<false>, dim3((unsigned)rows), dim3(kBlockRow), 0, (cudaStream_t)stream,
                    tgt_logits, drf_logits, B, T, V, tp.inv_t, nws);
-  if (e == cudaSuccess)
-    e = launch_pdl(tree_accept_kernel, dim3(B), dim3(kBlockSeq), 0, (cudaStream_t)stream, tp);
+  const int seg = (V + kBlockSeq - 1) / kBlockSeq;
+  const size_t stage_bytes = (size_t)kBlockSeq * (seg + 1) * sizeof(float);
+  if (e == cudaSuccess && stage_bytes <= kMaxStageBytes) {
+    static DeviceCache configured;
+    if (!configured.get([] {
+          return cudaFuncSetAttribute(tree_accept_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kMaxStageBytes) == cudaSuccess;
+        }))
+      return TF_ERR_CUDA;
+    e = launch_pdl(tree_accept_kernel<true>, dim3(B), dim3(kBlockSeq), stage_bytes, (cudaStream_t)stream, tp);
+  } else if (e == cudaSuccess) {
+    e = launch_pdl(tree_accept_kernel<false>, dim3(B), dim3(kBlockSeq), 0, (cudaStream_t)stream, tp);
+  }
   return e == cudaSuccess ? launch_status() : TF_ERR_CUDA;
 }

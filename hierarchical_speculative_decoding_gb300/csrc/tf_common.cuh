@@ -93,6 +93,48 @@ inline tf_status launch_status() {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// ---------------------------------------------------------------- debug build
+// Built with -DTF_DEBUG, every kernel checks the data-dependent indices of its
+// global-memory gathers (rows of the cache, chunks of the index, tiles and
+// pieces of the tensor-core stream, rows of the packed buffer) against the
+// extents of their buffers.  A failed check ORs its bit into a word of this
+// translation unit's device memory and skips the access (no trap, no assert);
+// tf_debug_status() collects the words of every file.  Release builds compile
+// each check to `true`.
+constexpr uint32_t kDbgCacheRow = 1u;   // a row outside [0, L) of its unit, or L > Lmax
+constexpr uint32_t kDbgIndexRow = 2u;   // a chunk-mean row outside [0, Cmax)
+constexpr uint32_t kDbgTile = 4u;       // a tensor-core tile or gathered piece outside its unit's rows
+constexpr uint32_t kDbgPacked = 8u;     // a packed row outside the resident buffer
+
+#ifdef TF_DEBUG
+static __device__ unsigned int g_tf_dbg;  // one word per translation unit
+__device__ __forceinline__ bool dbg_ok(bool ok, uint32_t code) {
+  if (!ok) atomicOr(&g_tf_dbg, code);
+  return ok;
+}
+#define TF_DBG_OK(cond, code) ::tf::dbg_ok((cond), (code))
+#define TF_DBG_READER(name)                                                         \
+  uint32_t name(int clear) {                                                        \
+    unsigned int v = 0;                                                             \
+    if (cudaMemcpyFromSymbol(&v, g_tf_dbg, sizeof(v)) != cudaSuccess) return ~0u;  \
+    if (clear) {                                                                    \
+      const unsigned int z = 0;                                                     \
+      if (cudaMemcpyToSymbol(g_tf_dbg, &z, sizeof(z)) != cudaSuccess) return ~0u;  \
+    }                                                                               \
+    return v;                                                                       \
+  }
+#else
+#define TF_DBG_OK(cond, code) (true)
+#define TF_DBG_READER(name)
+#endif
+// Readers of the files whose kernels gather (defined in debug builds only).
+uint32_t dbg_read_chunk_means(int clear);
+uint32_t dbg_read_gather(int clear);
+uint32_t dbg_read_verify(int clear);
+uint32_t dbg_read_topk(int clear);
+uint32_t dbg_read_draft(int clear);
+uint32_t dbg_read_pack(int clear);
+
 // ---------------------------------------------------------------- device side
 
 // Wait until the previous kernel on the stream has completed and its writes are

@@ -139,12 +139,12 @@ __device__ __forceinline__ void cluster_sum(const uint32_t* local, uint32_t* tot
 }
 
 // Scores of chunks [c0, c1) of one unit into keys[c - c0] and hist1.  qs: the
-// group's summed query (128 floats in shared memory); Mu: the unit's means.
-// A half-warp reads one 256-byte mean row with 16-byte loads, U rows in flight
-// per half-warp (kUnroll unless given).
+// group's summed query (128 floats in shared memory); Mu: the unit's means
+// (cmax rows).  A half-warp reads one 256-byte mean row with 16-byte loads, U
+// rows in flight per half-warp (kUnroll unless given).
 template <int U = kUnroll>
 __device__ __forceinline__ void score_slice(const float* qs, const uint16_t* __restrict__ Mu, int c0, int c1,
-                                            const Arrays& a) {
+                                            const Arrays& a, int cmax) {
   const int half = (threadIdx.x >> 4) & 1, l16 = threadIdx.x & 15, wid = threadIdx.x >> 5;
   float qv[8];
 #pragma unroll
@@ -159,7 +159,8 @@ __device__ __forceinline__ void score_slice(const float* qs, const uint16_t* __r
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int c = cb + u * kHalfWarps;
-      v[u] = (c < c1) ? ld_stream16(Ml + (size_t)c * kHeadDim) : make_uint4(0, 0, 0, 0);
+      v[u] = (c < c1 && TF_DBG_OK(c >= 0 && c < cmax, kDbgIndexRow)) ? ld_stream16(Ml + (size_t)c * kHeadDim)
+                                                                     : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {

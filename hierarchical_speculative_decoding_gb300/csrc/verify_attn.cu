@@ -402,12 +402,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           if (*(volatile int*)&s_abort) break;
           uint8_t* sk = smem + s * kStageBytes;
           uint8_t* sv = sk + kTile * kHeadDim * 2;
-          mbar_arrive_expect_tx(&bar_full[s], kStageBytes);
+          const bool in_unit = TF_DBG_OK(k0 + t * kTile >= 0 && k0 + t * kTile < p.Lmax, kDbgTile);
+          mbar_arrive_expect_tx(&bar_full[s], in_unit ? kStageBytes : 0u);
           const int y = row_base + t * kTile;
-          tma_load_2d(sk, &mapK, &bar_full[s], 0, y);
-          tma_load_2d(sk + 16384, &mapK, &bar_full[s], 64, y);
-          tma_load_2d(sv, &mapV, &bar_full[s], 0, y);
-          tma_load_2d(sv + 16384, &mapV, &bar_full[s], 64, y);
+          if (in_unit) {
+            tma_load_2d(sk, &mapK, &bar_full[s], 0, y);
+            tma_load_2d(sk + 16384, &mapK, &bar_full[s], 64, y);
+            tma_load_2d(sv, &mapV, &bar_full[s], 0, y);
+            tma_load_2d(sv + 16384, &mapV, &bar_full[s], 64, y);
+          }
         }
       }
       __syncwarp();
@@ -427,7 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
           if (*(volatile int*)&s_abort) ok = false;
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        const int st = lane < kPiecesPerTile ? s_pstart[t * kPiecesPerTile + lane] : -1;
+        int st = lane < kPiecesPerTile ? s_pstart[t * kPiecesPerTile + lane] : -1;
+        if (st >= 0 && !TF_DBG_OK(st < p.Lmax, kDbgTile)) st = -1;
         const unsigned have = __ballot_sync(0xffffffffu, st >= 0);
         if (lane == 0) mbar_arrive_expect_tx(&bar_full[s], (uint32_t)__popc(have) * (kStageBytes / kPiecesPerTile));
         __syncwarp();
@@ -927,6 +931,8 @@ size_t sparse_verify_ws(int units, int rows_all, int kc) {
 }
 
 }  // namespace
+TF_DBG_READER(dbg_read_verify)
+
 }  // namespace tf
 
 extern "C" size_t tf_verify_attn_workspace(int B, int Hq, int Hkv, int Lmax, int T) {

@@ -34,6 +34,10 @@
  *     once after allocation (cudaMemset); every call leaves its counters at
  *     zero again, so one buffer serves any sequence of calls that are ordered
  *     on the GPU.  Calls that may run concurrently need separate workspaces.
+ *     Each call has its own size query, taking exactly the shape arguments
+ *     the call takes, rather than one query keyed by an operation code: the
+ *     sizes depend on different arguments per call, and a typed query cannot
+ *     be handed the wrong ones.
  *   - Devices: every call runs on the caller's current CUDA device.  Host
  *     threads may call in concurrently, on one device or several; kernel
  *     attributes (shared-memory limits, cluster sizes) are set on each
@@ -74,7 +78,9 @@ TF_API const char* tf_status_string(tf_status s);
 /* Library ABI version (major * 100 + minor). */
 TF_API int tf_abi_version(void);
 
-/* Device-side status of a workspace that starts with a status word: the
+/* Device-side status of a workspace that starts with a status word (the word
+ * lives in the caller's workspace, since the library keeps no state of its
+ * own, so the query takes that workspace and its size): the
  * workspaces of tf_verify_attn, tf_verify_attn_tree, tf_sparse_verify_attn
  * and tf_verify_attn_offload.  Their kernels set the word when a pipeline wait
  * times out (only a hardware fault can cause that), and the outputs of every
@@ -86,6 +92,20 @@ TF_API int tf_abi_version(void);
  * (TF_ERR_INVALID_ARG otherwise, nothing read); TF_ERR_CUDA if the copy, the
  * clearing or the wait fails. */
 TF_API tf_status tf_check_status(void* ws, size_t ws_bytes, tf_stream_t stream);
+
+/* Bounds violations recorded by the checked build of this library
+ * (libtriforce_attn_debug.so, compiled with TF_DEBUG).  There every kernel
+ * checks the data-dependent indices of its global-memory gathers -- cache
+ * rows against [0, L_b) and Lmax, chunk-mean rows against Cmax, tensor-core
+ * tiles and gathered pieces against their unit's rows, packed rows against
+ * the resident buffer -- and a failed check sets a bit instead of making the
+ * access: 1 cache row, 2 chunk-mean row, 4 tile or piece, 8 packed row.
+ * Writes the OR of the bits recorded on the current device since the last
+ * clearing to *flags (waits for the device's queued work); clear != 0 resets
+ * them.  A release build returns TF_ERR_UNSUPPORTED with *flags = 0.
+ * Ids outside [0, C_b) in a caller's selection are input the calls skip by
+ * contract, not violations. */
+TF_API tf_status tf_debug_status(uint32_t* flags, int clear);
 
 /*
  * a1 -- chunk-mean retrieval index.
@@ -356,6 +376,8 @@ TF_API tf_status tf_verify_attn_offload(const uint16_t* Q, const uint16_t* K_hos
  *   u_acc [B, gamma] f32, u_res [B] f32, uniforms in [0, 1)
  *   n_acc [B] int32 (accepted count), next_token [B] int32
  *   out_tokens [B, gamma+1] int32 (nullable): accepted drafts, next token, -1 pad
+ *     (an output beyond n_acc and next_token so that the second level can take
+ *     the first level's result directly as its draft, with no host step)
  * temperature > 0.  gamma >= 0, V >= 1.  Probabilities use fp32 exponentials,
  * normalisers summed in fp32 then fp64, an fp64 ratio test, and cumulative
  * sums carried as exact fp32 pairs (fp64 for a warp-sized vocabulary), so a

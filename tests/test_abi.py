@@ -147,6 +147,10 @@ def test_host_validation_rejects_before_launch(lib):
     assert pk(fake, fake, fake, fake, fake, 1, 2, 64, 64, 8, 4, fake, fake, fake, fake, None) == UNSUPPORTED
     assert pk(fake, fake, fake, fake, fake, 1, 2, 64, 128, 8, 4097, fake, fake, fake, fake, None) == UNSUPPORTED
     assert pk(fake, fake, fake, fake, fake, 0, 2, 64, 128, 8, 4, fake, fake, fake, fake, None) == 0  # B = 0: no work
+    # the release build keeps no bounds-check words
+    flags = ctypes.c_uint32(7)
+    assert lib.tf_debug_status(ctypes.byref(flags), 0) == UNSUPPORTED and flags.value == 0
+    assert lib.tf_debug_status(null, 0) == INVALID
     # the status query reads nothing without a workspace of at least one word
     assert lib.tf_check_status(null, 4096, None) == INVALID
     assert lib.tf_check_status(fake, 3, None) == INVALID
