@@ -18,12 +18,16 @@
 //             head dims, V read MN-major straight from the TMA tile; the hi
 //             and lo bf16 parts of P as separate rows, so one MMA per 16 keys
 //             reads V once and leaves P_hi V and P_lo V side by side);
-//   warps 2-5 softmax on TMEM lane = key (online, log2 domain, rescaled only
-//             when the running max grows by > 2^8), P written over the K half
-//             of the tile's own stage (K is dead once S exists; the stage goes
-//             back to the copy engine after P V), handed over before the O of
-//             the previous tile is read back (TMEM lane = head dim) and
-//             accumulated in fp32 registers.
+//   warps 2.. softmax, one warpgroup per 8 query rows (1 to 4), on TMEM
+//             lane = key (online, log2 domain, rescaled only when the running
+//             max grows by > 2^8), P written over the K half of the tile's own
+//             stage (K is dead once S exists; the stage goes back to the copy
+//             engine after P V), handed over before the O of the previous tile
+//             is read back (TMEM lane = head dim) and accumulated in fp32
+//             registers.  A stage is held from its copy until P V has read it,
+//             so the softmax latency sets how many tiles are in flight: with
+//             one warpgroup per 8 rows a GQA group's 24 rows take about as
+//             long per tile as MHA's 6.
 // S and O are double-buffered in TMEM and P has one buffer per stage, so the
 // MMAs of tile t+1 overlap the softmax of tile t.  Splits are merged with the
 // log-sum-exp identity by the last CTA of each unit (atomic ticket; the
@@ -59,8 +63,8 @@ using namespace sm100;
 constexpr int kTile = 128;          // keys per tile (MMA M)
 constexpr int kStages = 3;          // K/V ring depth
 constexpr int kStageBytes = 2 * kTile * kHeadDim * 2;  // K + V tile
-constexpr int kThreads = 192;       // 6 warps
-constexpr int kSoftmaxThreads = 128;
+constexpr int kSoftmaxThreads = 128;  // one softmax warpgroup: the four TMEM lane quarters
+constexpr int kGroupRows = 8;         // query rows per softmax warpgroup
 constexpr int kMaxRows = 32;        // query rows per CTA (N <= 32)
 constexpr int kPiece = 8;           // rows per gathered piece (one chunk, one swizzle atom)
 constexpr int kPiecesPerTile = kTile / kPiece;
@@ -69,6 +73,7 @@ constexpr int kPieceBytes = kPiece * kHeadDim * 2;  // one piece of K (or V): 2 
 constexpr int kMaxClusterMerge = 8;
 constexpr int kPartStride = 4 + kHeadDim;  // one row's partial state: m, l, 2 unused, O[128]  // most splits merged inside one (portable) cluster
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kLptMaxSeqs = 64;  // longest-first block order for batches up to this size
 
 
 struct VerifyParams {
@@ -95,6 +100,9 @@ struct VerifyParams {
   // candidate tree [B, T]: parent[b * T + j] is the candidate that j extends
   // (-1: the prefix); null: a chain (parent j - 1)
   const int32_t* parent;
+  // contiguous mode: 1 = block row r serves the sequence with the r-th
+  // longest context (nseq <= kLptMaxSeqs), 0 = batch order
+  int nseq, longest_first;
 };
 
 // Final log-sum-exp merge of a unit's split partials by the CTA that finished
@@ -104,6 +112,7 @@ struct VerifyParams {
 // threads load every split's (m, l), and the weights e^{m_s - m} and row sums
 // L are formed; each thread then accumulates float4 columns of the output
 // from shared memory and writes them divided by L.
+template <int kThreads>
 __device__ void merge_staged(const float* __restrict__ ml, const float* __restrict__ o, int S, int rows,
                              uint8_t* ring, uint64_t* bar, float* __restrict__ out, float* __restrict__ part,
                              int* status) {
@@ -216,6 +225,8 @@ __device__ void merge_staged(const float* __restrict__ ml, const float* __restri
 // 8, 16, 24 or 32.  The MMA shapes follow from it.
 template <int NR>
 struct Smem {
+  static constexpr int kGroups = NR / kGroupRows;                    // softmax warpgroups
+  static constexpr int kThreads = 64 + kSoftmaxThreads * kGroups;    // + producer and MMA warps
   static constexpr int kNS = NR <= 16 ? 16 : 32;       // N of S = Q K^T (Q rows, zero-padded)
   static constexpr int kQBytes = 2 * kNS * 128;       // two 64-column halves of [kNS x 128] bf16
   // P of tile t is written over the K half of the tile's own stage: K is dead
@@ -249,21 +260,22 @@ __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
   return u;
 }
 
-__device__ __forceinline__ bool named_bar_or(bool pred) {
+// Barriers of one softmax warpgroup (id 1 + its index; 0 is the block barrier).
+__device__ __forceinline__ bool named_bar_or(uint32_t id, bool pred) {
   uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %3, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(pred ? 1u : 0u), "r"(kSoftmaxThreads));
+      : "r"(pred ? 1u : 0u), "r"(kSoftmaxThreads), "r"(id));
   return r != 0;
 }
 
-__device__ __forceinline__ void named_bar_sync() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
+__device__ __forceinline__ void named_bar_sync(uint32_t id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kSoftmaxThreads) : "memory");
 }
 
 template <int NR, bool GATHER, bool TREE = false>
-__global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_constant__ CUtensorMap mapK,
+__global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(const __grid_constant__ CUtensorMap mapK,
                                                                   const __grid_constant__ CUtensorMap mapV,
                                                                   VerifyParams p) {
   using S = Smem<NR>;
@@ -274,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   __shared__ uint32_t tmem_base_s;
   __shared__ float red[4][NR];
   __shared__ float alpha_s[2][NR];
-  __shared__ int rescaled_s[2];
+  __shared__ int rescaled_s[S::kGroups][2];
   __shared__ int s_last, s_abort;
   __shared__ int s_pstart[GATHER ? kPiecesPerTile * kMaxTilesPerCta : 1];  // first position, -1: none
   __shared__ int s_pcand[GATHER ? kPiecesPerTile * kMaxTilesPerCta : 1];   // 1: candidate rows
@@ -284,9 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   uint8_t* sQ = smem + S::kOffQ;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ug = blockIdx.y;
-  const int unit = ug / p.ngroups, grp = ug % p.ngroups;
-  const int b = unit / p.Hkv, g = unit % p.Hkv;
+  const int ug = blockIdx.y;  // ticket and partial slots: every split of a unit shares them
+  const int grp = ug % p.ngroups, g = (ug / p.ngroups) % p.Hkv;
+  const int seq_slot = ug / (p.ngroups * p.Hkv);
   const int G = p.Hq / p.Hkv;
   const int rows_all = G * p.T;
   const int row0 = grp * kMaxRows;
@@ -299,9 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_s_full[i], 1);
-      mbar_init(&bar_p_full[i], kSoftmaxThreads);
+      mbar_init(&bar_p_full[i], kSoftmaxThreads * S::kGroups);
       mbar_init(&bar_o_full[i], 1);
-      mbar_init(&bar_o_free[i], kSoftmaxThreads);
+      mbar_init(&bar_o_free[i], kSoftmaxThreads * S::kGroups);
     }
     mbar_init(&bar_merge, 1);
     s_abort = 0;
@@ -316,6 +328,27 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     prefetch_tensormap(&mapV);
   }
   pdl_wait();  // everything above is on-chip set-up that may overlap the previous kernel
+  // Ragged batches: CTAs start in about block order, so block row r takes the
+  // sequence with the r-th longest context (ties in batch order) and the
+  // longest units begin in the first wave instead of stretching the last.
+  // Every warp ranks the (at most 64) lengths itself: lane i holds sequences
+  // i and i + 32, the lengths go round by shuffles, and the one sequence whose
+  // rank is this block row's slot comes out of a ballot (no block barrier).
+  int b = seq_slot;
+  if (p.longest_first) {
+    const int l0 = lane < p.nseq ? clamp_len(p.seq_lens[lane], p.Ltot) : -1;
+    const int l1 = lane + 32 < p.nseq ? clamp_len(p.seq_lens[lane + 32], p.Ltot) : -1;
+    int r0 = 0, r1 = 0;
+    for (int j = 0; j < p.nseq; ++j) {
+      const int lj = __shfl_sync(0xffffffffu, j < 32 ? l0 : l1, j & 31);
+      r0 += (lj > l0 || (lj == l0 && j < lane)) ? 1 : 0;
+      r1 += (lj > l1 || (lj == l1 && j < lane + 32)) ? 1 : 0;
+    }
+    const unsigned m0 = __ballot_sync(0xffffffffu, lane < p.nseq && r0 == seq_slot);
+    const unsigned m1 = __ballot_sync(0xffffffffu, lane + 32 < p.nseq && r1 == seq_slot);
+    b = m0 ? __ffs(m0) - 1 : 32 + __ffs(m1) - 1;
+  }
+  const int unit = b * p.Hkv + g;
   const int L = clamp_len(p.seq_lens[b], p.Ltot);
 
   // key range of this split: whole tiles (contiguous), or tiles of the piece
@@ -338,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     const int t0 = blockIdx.x * p.tiles_per;
     ntiles = max(0, min(tiles_all, t0 + p.tiles_per) - t0);
     const int32_t* sel = p.idx + (size_t)unit * p.kc;
-    for (int e = tid; e < kPiecesPerTile * ntiles; e += kThreads) {
+    for (int e = tid; e < kPiecesPerTile * ntiles; e += S::kThreads) {
       const int gp = t0 * kPiecesPerTile + e;
       int st = -1, cand = 0;
       if (gp < nsel) {
@@ -372,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   // Q rows of this group -> shared memory, [kNS x 128] bf16 in two swizzled halves.
   {
     const uint16_t* Qg = p.Q + (((size_t)b * p.Hq + (size_t)g * G) * p.T + row0) * kHeadDim;
-    for (int e = tid; e < S::kNS * 16; e += kThreads) {
+    for (int e = tid; e < S::kNS * 16; e += S::kThreads) {
       const int r = e >> 4, c8 = (e & 15) * 8;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (r < rows) v = *reinterpret_cast<const uint4*>(Qg + (size_t)r * kHeadDim + c8);
@@ -410,6 +443,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
             tma_load_2d(sk + 16384, &mapK, &bar_full[s], 64, y);
             tma_load_2d(sv, &mapV, &bar_full[s], 0, y);
             tma_load_2d(sv + 16384, &mapV, &bar_full[s], 64, y);
+          }
+          // The next tile into L2 now: its copy into the ring waits for a stage
+          // to come free, and starting the DRAM read here takes that wait off
+          // the ring's turnaround.  (One tile ahead measured best; two to four
+          // ahead were slower.)
+          if (t >= kStages - 1 && t + 1 < ntiles) {
+            const int yn = y + kTile;
+            tma_prefetch_2d(&mapK, 0, yn);
+            tma_prefetch_2d(&mapK, 64, yn);
+            tma_prefetch_2d(&mapV, 0, yn);
+            tma_prefetch_2d(&mapV, 64, yn);
           }
         }
       }
@@ -499,34 +543,41 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax + correction
+    // Warpgroup c (warps 2 + 4c .. 5 + 4c) owns the query rows [8c, 8c + 8);
+    // its four warps cover the four TMEM lane quarters.  The warpgroups share
+    // nothing but the tile hand-overs, so their chains overlap.
+    const int wg = S::kGroups == 1 ? 0 : (warp - 2) >> 2;
+    const int nb = wg * kGroupRows;        // first row of this warpgroup
+    const uint32_t bar_id = 1u + (uint32_t)wg;
     const int q4 = warp & 3;               // TMEM lane quarter of this warp
     const int my = q4 * 32 + lane;         // key index in the tile / head dim of O
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    float m_run[NR], l_part[NR], acc[NR];
-    int lim[TREE ? 1 : NR];  // chain: query row n sees positions <= lim[n]
+    constexpr int R = kGroupRows;
+    float m_run[R], l_part[R], acc[R];
+    int lim[TREE ? 1 : R];  // chain: query row nb + j sees positions <= lim[j]
 #pragma unroll
-    for (int n = 0; n < NR; ++n) {
-      m_run[n] = -INFINITY;
-      l_part[n] = 0.0f;
-      acc[n] = 0.0f;
-      if (!TREE) lim[n] = (n < rows) ? (L - p.T + ((row0 + n) % p.T)) : -1;
+    for (int j = 0; j < R; ++j) {
+      m_run[j] = -INFINITY;
+      l_part[j] = 0.0f;
+      acc[j] = 0.0f;
+      if (!TREE) lim[j] = (nb + j < rows) ? (L - p.T + ((row0 + nb + j) % p.T)) : -1;
     }
     const uint32_t all_rows = rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u);
     const int cbase = L - p.T;  // position of candidate 0
-    // Every wait is followed by a vote over the 128 threads so that a timeout
-    // makes all of them leave the loop together (named barriers stay matched).
+    // Every wait is followed by a vote over the warpgroup so that a timeout
+    // makes all of its threads leave the loop together (its named barriers
+    // stay matched).
     bool zero_v = false;  // this key row of the tile must be zeroed in V
     for (int t = 0; t <= ntiles; ++t) {
-      float sc[NR];  // scores, then softmax weights of tile t
+      float sc[R];  // scores, then softmax weights of tile t
       if (t < ntiles) {
         const bool timed_out = !mbar_wait(&bar_s_full[t & 1], (t >> 1) & 1);
-        if (named_bar_or(timed_out)) {
+        if (named_bar_or(bar_id, timed_out)) {
           if (my == 0) atomicExch(&s_abort, 1);
           break;
         }
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < NR; c += 8) tmem_ld8(tmem + (t & 1) * 32 + lane_off + c, sc + c);
+        tmem_ld8(tmem + (t & 1) * 32 + lane_off + nb, sc);
         tmem_ld_wait();
         // this key's position and whether it may be seen at all; a candidate
         // key (position >= L - T) only by the rows whose candidate extends it
@@ -550,39 +601,41 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         if (TREE) {
           const int ci = pos - cbase;
           vis = !key_ok ? 0u : (chain && ci >= 0) ? s_vis[ci < 16 ? ci : 15] : all_rows;
+          vis >>= nb;
         }
         bool need = false;
 #pragma unroll
-        for (int n = 0; n < NR; ++n) {
-          const bool valid = TREE ? ((vis >> n) & 1u) != 0u : (key_ok && (!chain || pos <= lim[TREE ? 0 : n]));
-          sc[n] = valid ? sc[n] * p.scale_log2 : -INFINITY;
-          need |= sc[n] > m_run[n] + kRescaleThreshold;
+        for (int j = 0; j < R; ++j) {
+          const bool valid = TREE ? ((vis >> j) & 1u) != 0u : (key_ok && (!chain || pos <= lim[TREE ? 0 : j]));
+          sc[j] = valid ? sc[j] * p.scale_log2 : -INFINITY;
+          need |= sc[j] > m_run[j] + kRescaleThreshold;
         }
-        need = named_bar_or(need);
+        need = named_bar_or(bar_id, need);
         if (need) {
           // tile max per row, then a new reference max for every row that grew
 #pragma unroll
-          for (int n = 0; n < NR; ++n) {
-            float v = sc[n];
+          for (int j = 0; j < R; ++j) {
+            float v = sc[j];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0) red[q4][n] = v;
+            if (lane == 0) red[q4][nb + j] = v;
           }
-          named_bar_sync();
+          named_bar_sync(bar_id);
 #pragma unroll
-          for (int n = 0; n < NR; ++n) {
+          for (int j = 0; j < R; ++j) {
+            const int n = nb + j;
             const float tmax = fmaxf(fmaxf(red[0][n], red[1][n]), fmaxf(red[2][n], red[3][n]));
-            const float mn = fmaxf(m_run[n], tmax);
-            const float a = merge_scale(m_run[n], mn);
-            l_part[n] *= a;
+            const float mn = fmaxf(m_run[j], tmax);
+            const float a = merge_scale(m_run[j], mn);
+            l_part[j] *= a;
             if (my == 0) alpha_s[t & 1][n] = a;
-            m_run[n] = mn;
+            m_run[j] = mn;
           }
-          named_bar_sync();  // red[] is reused by the next rescale
+          named_bar_sync(bar_id);  // red[] is reused by the next rescale
         }
-        if (my == 0) rescaled_s[t & 1] = need ? 1 : 0;
+        if (my == 0) rescaled_s[wg][t & 1] = need ? 1 : 0;
 #pragma unroll
-        for (int n = 0; n < NR; ++n) sc[n] = (sc[n] == -INFINITY) ? 0.0f : exp2f(sc[n] - m_run[n]);
+        for (int j = 0; j < R; ++j) sc[j] = (sc[j] == -INFINITY) ? 0.0f : exp2f(sc[j] - m_run[j]);
       }
       if (t < ntiles) {
         // P for this tile as hi + lo bf16 parts (P V error ~2^-17 instead of
@@ -590,38 +643,37 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         uint8_t* pbuf = smem + (t % kStages) * kStageBytes;  // over the K tile
         if constexpr (S::kPMnMajor) {
           // key `my` owns one 128-byte row: 16-byte chunk c < 4 holds the hi
-          // parts of rows 8c..8c+7, chunk c + 4 their lo parts
+          // parts of rows 8c..8c+7, chunk c + 4 their lo parts; this
+          // warpgroup writes chunks wg and wg + 4
           uint8_t* prow = pbuf + (my >> 3) * 1024 + (my & 7) * 128;
+          uint32_t hw[4], lw[4];
 #pragma unroll
-          for (int c = 0; c < NR / 8; ++c) {
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float a0 = sc[c * 8 + 2 * j], a1 = sc[c * 8 + 2 * j + 1];
-              l_part[c * 8 + 2 * j] += a0;
-              l_part[c * 8 + 2 * j + 1] += a1;
-              const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
-              const __nv_bfloat162 lo = __floats2bfloat162_rn(a0 - __low2float(h), a1 - __high2float(h));
-              hw[j] = bf16x2_bits(h);
-              lw[j] = bf16x2_bits(lo);
-            }
-            *reinterpret_cast<uint4*>(prow + ((c ^ (my & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(prow + (((c + 4) ^ (my & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          for (int j = 0; j < 4; ++j) {
+            const float a0 = sc[2 * j], a1 = sc[2 * j + 1];
+            l_part[2 * j] += a0;
+            l_part[2 * j + 1] += a1;
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(a0 - __low2float(h), a1 - __high2float(h));
+            hw[j] = bf16x2_bits(h);
+            lw[j] = bf16x2_bits(lo);
           }
+          *reinterpret_cast<uint4*>(prow + ((wg ^ (my & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(prow + (((wg + 4) ^ (my & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         } else {
           // K-major: row n (hi) and row NR + n (lo), column = key
           const uint32_t off_key = (uint32_t)(my >> 6) * S::kPKeyHalf;
 #pragma unroll
-          for (int n = 0; n < NR; ++n) {
-            const float pv = sc[n];
+          for (int j = 0; j < R; ++j) {
+            const int n = nb + j;
+            const float pv = sc[j];
             const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
             const __nv_bfloat16 lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
-            l_part[n] += pv;
+            l_part[j] += pv;
             *reinterpret_cast<__nv_bfloat16*>(pbuf + off_key + sw128_offset(n, my & 63)) = hi;
             *reinterpret_cast<__nv_bfloat16*>(pbuf + off_key + sw128_offset(NR + n, my & 63)) = lo;
           }
         }
-        if (zero_v) {
+        if (zero_v && wg == 0) {
           // Rows nobody may see can hold anything (even NaN): zero them in
           // the V tile so 0 * V stays 0 in the MMA.  Waiting on the (already
           // completed) TMA barrier orders these writes after the tile landed.
@@ -645,22 +697,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
         // handed to the MMA warp (the two use different alpha / rescale slots)
         const int u = t - 1;
         const bool timed_out = !mbar_wait(&bar_o_full[u & 1], (u >> 1) & 1);
-        if (named_bar_or(timed_out)) {  // also orders alpha_s / rescaled_s of tile u
+        if (named_bar_or(bar_id, timed_out)) {  // also orders alpha_s / rescaled_s of tile u
           if (my == 0) atomicExch(&s_abort, 1);
           break;
         }
         tc_fence_after();
-        float ov[NR], ol[NR];
-        const uint32_t o_col = tmem + 64 + (u & 1) * S::kNPV + lane_off;
-#pragma unroll
-        for (int c = 0; c < NR; c += 8) {
-          tmem_ld8(o_col + c, ov + c);
-          tmem_ld8(o_col + S::kLoCol + c, ol + c);
-        }
+        float ov[R], ol[R];
+        const uint32_t o_col = tmem + 64 + (u & 1) * S::kNPV + lane_off + nb;
+        tmem_ld8(o_col, ov);
+        tmem_ld8(o_col + S::kLoCol, ol);
         tmem_ld_wait();
-        const bool resc = rescaled_s[u & 1] != 0;
+        const bool resc = rescaled_s[wg][u & 1] != 0;
 #pragma unroll
-        for (int n = 0; n < NR; ++n) acc[n] = (resc ? acc[n] * alpha_s[u & 1][n] : acc[n]) + (ov[n] + ol[n]);
+        for (int j = 0; j < R; ++j) acc[j] = (resc ? acc[j] * alpha_s[u & 1][nb + j] : acc[j]) + (ov[j] + ol[j]);
         tc_fence_before();
         mbar_arrive(&bar_o_free[u & 1]);
       }
@@ -668,58 +717,65 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
 
     // ---- row sums across the 128 key lanes
 #pragma unroll
-    for (int n = 0; n < NR; ++n) {
-      float v = l_part[n];
+    for (int j = 0; j < R; ++j) {
+      float v = l_part[j];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) red[q4][n] = v;
+      if (lane == 0) red[q4][nb + j] = v;
     }
-    named_bar_sync();
+    named_bar_sync(bar_id);
     const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
+    auto row_sum = [&](int n) { return (red[0][n] + red[1][n]) + (red[2][n] + red[3][n]); };
     if (p.splits == 1 && p.part_out) {
 #pragma unroll
-      for (int n = 0; n < NR; ++n) {
+      for (int j = 0; j < R; ++j) {
+        const int n = nb + j;
         if (n < rows) {
           float* pr = p.part_out + (out_row0 + n) * kPartStride;
           if (my == 0) {
-            pr[0] = m_run[n];
-            pr[1] = (red[0][n] + red[1][n]) + (red[2][n] + red[3][n]);
+            pr[0] = m_run[j];
+            pr[1] = row_sum(n);
           }
-          pr[4 + my] = acc[n];
+          pr[4 + my] = acc[j];
         }
       }
     } else if (p.splits == 1) {
 #pragma unroll
-      for (int n = 0; n < NR; ++n) {
+      for (int j = 0; j < R; ++j) {
+        const int n = nb + j;
         if (n < rows) {
-          const float l = (red[0][n] + red[1][n]) + (red[2][n] + red[3][n]);
-          p.out[(out_row0 + n) * kHeadDim + my] = (l > 0.0f) ? acc[n] / l : 0.0f;
+          const float l = row_sum(n);
+          p.out[(out_row0 + n) * kHeadDim + my] = (l > 0.0f) ? acc[j] / l : 0.0f;
         }
       }
     } else if (p.cmerge) {
+      // stage 0 is idle: every MMA (and so every copy) has completed once this
+      // warpgroup has read back the last O
       float* cm = reinterpret_cast<float*>(smem + S::kOffCm);
       float* co = reinterpret_cast<float*>(smem + S::kOffCo);
 #pragma unroll
-      for (int n = 0; n < NR; ++n) {
+      for (int j = 0; j < R; ++j) {
+        const int n = nb + j;
         if (n < rows) {
           if (my == 0) {
-            cm[n * 2 + 0] = m_run[n];
-            cm[n * 2 + 1] = (red[0][n] + red[1][n]) + (red[2][n] + red[3][n]);
+            cm[n * 2 + 0] = m_run[j];
+            cm[n * 2 + 1] = row_sum(n);
           }
-          co[n * kHeadDim + my] = acc[n];
+          co[n * kHeadDim + my] = acc[j];
         }
       }
     } else {
       float* ml = p.part_ml + ((size_t)ug * p.splits_cap + blockIdx.x) * kMaxRows * 2;
       float* po = p.part_o + ((size_t)ug * p.splits_cap + blockIdx.x) * kMaxRows * kHeadDim;
 #pragma unroll
-      for (int n = 0; n < NR; ++n) {
+      for (int j = 0; j < R; ++j) {
+        const int n = nb + j;
         if (n < rows) {
           if (my == 0) {
-            ml[n * 2 + 0] = m_run[n];
-            ml[n * 2 + 1] = (red[0][n] + red[1][n]) + (red[2][n] + red[3][n]);
+            ml[n * 2 + 0] = m_run[j];
+            ml[n * 2 + 1] = row_sum(n);
           }
-          po[n * kHeadDim + my] = acc[n];
+          po[n * kHeadDim + my] = acc[j];
         }
       }
     }
@@ -747,13 +803,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     const uint32_t rank = cluster_ctarank();
     const float* cm = reinterpret_cast<const float*>(smem + Smem<NR>::kOffCm);
     const float* co = reinterpret_cast<const float*>(smem + Smem<NR>::kOffCo);
-    for (int i = tid; i < S * rows; i += kThreads) {
+    for (int i = tid; i < S * rows; i += Smem<NR>::kThreads) {
       const int sp = i / rows, n = i % rows;
       s_w[i] = __uint_as_float(dsmem_ld_u32(cm + n * 2 + 0, sp));
       s_l[i] = __uint_as_float(dsmem_ld_u32(cm + n * 2 + 1, sp));
     }
     __syncthreads();
-    for (int n = tid; n < rows; n += kThreads) {
+    for (int n = tid; n < rows; n += Smem<NR>::kThreads) {
       float mx = -INFINITY;
       for (int sp = 0; sp < S; ++sp) mx = fmaxf(mx, s_w[sp * rows + n]);
       float Lsum = 0.0f;
@@ -766,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
     }
     __syncthreads();
     const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
-    for (int e4 = (int)rank * kThreads + tid; e4 < rows * (kHeadDim / 4); e4 += S * kThreads) {
+    for (int e4 = (int)rank * Smem<NR>::kThreads + tid; e4 < rows * (kHeadDim / 4); e4 += S * Smem<NR>::kThreads) {
       const int n = e4 / (kHeadDim / 4), d = (e4 % (kHeadDim / 4)) * 4;
       uint4 v[8];
 #pragma unroll
@@ -804,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_umma_kernel(const __grid_c
   const float* ml0 = p.part_ml + (size_t)ug * p.splits_cap * kMaxRows * 2;
   const float* o0 = p.part_o + (size_t)ug * p.splits_cap * kMaxRows * kHeadDim;
   const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
-  merge_staged(ml0, o0, p.splits, rows, smem, &bar_merge, p.out + out_row0 * kHeadDim,
+  merge_staged<Smem<NR>::kThreads>(ml0, o0, p.splits, rows, smem, &bar_merge, p.out + out_row0 * kHeadDim,
                p.part_out ? p.part_out + out_row0 * kPartStride : nullptr, p.status);
   if (tid == 0) p.tickets[ug] = 0;
 }
@@ -859,7 +915,7 @@ tf_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParam
     return TF_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Smem<NR>::kThreads);
   cfg.dynamicSmemBytes = Smem<NR>::kDynamic;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -965,6 +1021,8 @@ tf_status verify_contig(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
   p.part_out = part_out;
   p.parent = parent;
   p.T = T;
+  p.nseq = B;
+  p.longest_first = (B > 1 && B <= kLptMaxSeqs) ? 1 : 0;
   p.ngroups = (rows_all + kMaxRows - 1) / kMaxRows;
   p.splits_cap = verify_splits_cap(Lmax);
   const int ug = B * Hkv * p.ngroups;

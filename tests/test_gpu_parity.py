@@ -249,6 +249,30 @@ def test_verify_row_groups(cuda_lib, G, T):
     assert np.abs(out.cpu().double().numpy() - want).max() <= ATOL
 
 
+@pytest.mark.parametrize("lens", [[900, 3000, 0, 3000, 17, 2500, 900], [5 + 37 * i for i in range(65)]],
+                         ids=["ties-and-empty", "65-sequences"])
+def test_verify_ragged_batch_order(cuda_lib, lens):
+    """Ragged batches run their longest sequences first (block row r takes the
+    r-th longest context, ties in batch order, up to 64 sequences; larger
+    batches keep the batch order): every sequence's rows still land in its own
+    output slots, with equal, empty and tiny contexts in the mix."""
+    L = max(lens)
+    w = small_workload(B=len(lens), Hq=8, Hkv=2, T=6, L=L, ragged=False)
+    c = make_case(w)
+    seq = np.array(lens, dtype=np.int32)
+    c["seq"] = torch.from_numpy(seq).cuda()
+    for t in ("K", "V"):  # rows past each context hold NaN
+        x = c[t + "_cpu"].clone()
+        for b, n in enumerate(lens):
+            x[b, :, n:] = float("nan")
+        c[t + "_cpu"], c[t] = x, x.cuda()
+    out = cuda_lib.tf_verify_attn(c["Q"], c["K"], c["V"], c["seq"], 0.09)
+    want = O.verify_attn(bits(c["Q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), seq, 0.09)
+    got = out.cpu().double().numpy()
+    assert np.all(np.isfinite(got))
+    assert np.abs(got - want).max() <= ATOL
+
+
 def test_verify_context_shorter_than_candidates(cuda_lib):
     w = small_workload(B=2, ragged=False, L=16, T=6)
     c = make_case(w)
