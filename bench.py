@@ -465,6 +465,34 @@ def kernel_entry(nbytes, ms, peak):
     return {"ms": round(ms, 5), "GBps": round(gbps, 1), "frac_hbm": round(gbps / peak, 4)}
 
 
+def measure_level1(st, w, tf, dev, stream, peak):
+    """Level-1 verification over the retrieval cache (not part of the step):
+    the step's selection, T verify queries, back-to-back calls over the layers
+    replayed as one CUDA graph; and its fixed cost, the same calls over the
+    first 16 selected chunks."""
+    import torch
+
+    B, Hq, Hkv, D, T = w.B, w.Hq, w.Hkv, w.D, w.T
+    ws_sv = tf.workspace(tf.tf_sparse_verify_attn_workspace(B, Hq, Hkv, w.kc, T), dev)
+    o_sv = torch.empty((B, Hq, T, D), dtype=torch.float32, device=dev)
+
+    def sv_calls(idx_all, nsel_all):
+        return [lambda l=l: tf.tf_sparse_verify_attn(st.Q[l], st.K[l], st.V[l], st.seq, idx_all[l], nsel_all[l],
+                                                     st.scale, out=o_sv, ws=ws_sv) for l in range(st.layers)]
+
+    sv_ms = graph_loop_ms(sv_calls(st.idx, st.nsel), stream)
+    # selected chunks (clipped to each context) and the candidate rows, K and V
+    rows = sum(min(w.kc * w.chunk, max(int(n), 0)) + T for n in st.seq_cpu.tolist())
+    sv_bytes = 2 * Hkv * rows * D * 2 + B * Hq * T * D * (2 + 4)
+    out = dict(kernel_entry(sv_bytes, sv_ms, peak), calls="tf_sparse_verify_attn",
+               timing="back to back over the layers, replayed as one CUDA graph")
+    idx16 = torch.full_like(st.idx, -1)
+    idx16[:, :, :, :16] = st.idx[:, :, :, :16]
+    nsel16 = torch.clamp(st.nsel, max=16)
+    out["floor_kc16_us"] = round(graph_loop_ms(sv_calls(idx16, nsel16), stream) * 1e3, 2)
+    return out
+
+
 def measure_extra_workload(w, args, tf, synth, dev, stream, world, local, peak):
     """The step on another workload: steps/s, the per-kernel breakdown with the
     verify roofline, and the drafter back to back."""
@@ -491,6 +519,7 @@ def measure_extra_workload(w, args, tf, synth, dev, stream, world, local, peak):
     d1.record(stream)
     torch.cuda.synchronize()
     kern["retrieval_draft"]["back_to_back"] = kernel_entry(nb["draft"], d0.elapsed_time(d1) / st.layers, peak)
+    kern["sparse_verify_level1"] = measure_level1(st, w, tf, dev, stream, peak)
     ver = kern["verify"]
     out = {"value": round(value, 4), "unit": "steps/s", "steps": steps, "ms_per_step": round(elapsed_s / steps * 1e3, 4),
            "config": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D, "context": w.L, "layers": w.layers,
@@ -689,25 +718,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     kernels["retrieval_draft"]["back_to_back"] = kernel_entry(nb["draft"], d0.elapsed_time(d1) / layers, peak)
 
-    # level-1 verification over the retrieval cache (not part of the step): the
-    # step's selection, T verify queries, back-to-back calls over the layers;
-    # and its fixed cost: the same call over the first 16 selected chunks
-    ws_sv = tf.workspace(tf.tf_sparse_verify_attn_workspace(B, Hq, Hkv, w.kc, T), dev)
-    o_sv = torch.empty((B, Hq, T, D), dtype=torch.float32, device=dev)
-    kv_row = D * 2
-
-    def sv_calls(idx_all, nsel_all):
-        return [lambda l=l: tf.tf_sparse_verify_attn(st.Q[l], st.K[l], st.V[l], st.seq, idx_all[l], nsel_all[l],
-                                                     st.scale, out=o_sv, ws=ws_sv) for l in range(layers)]
-
-    sv_ms = graph_loop_ms(sv_calls(st.idx, st.nsel), stream)
-    sv_bytes = 2 * B * Hkv * (w.kc * w.chunk + T) * kv_row + B * Hq * T * D * (2 + 4)
-    kernels["sparse_verify_level1"] = dict(kernel_entry(sv_bytes, sv_ms, peak), calls="tf_sparse_verify_attn",
-                                           timing="back to back over the layers, replayed as one CUDA graph")
-    idx16 = torch.full_like(st.idx, -1)
-    idx16[:, :, :, :16] = st.idx[:, :, :, :16]
-    nsel16 = torch.clamp(st.nsel, max=16)
-    kernels["sparse_verify_level1"]["floor_kc16_us"] = round(graph_loop_ms(sv_calls(idx16, nsel16), stream) * 1e3, 2)
+    kernels["sparse_verify_level1"] = measure_level1(st, w, tf, dev, stream, peak)
     # the window: back to back, and its fixed cost with 4 sinks + 12 recent rows (16 rows) per unit
     ws_w16 = tf.workspace(tf.tf_stream_window_attn_workspace(B, Hq, Hkv, 4, 12), dev)
     o_w16 = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
