@@ -328,8 +328,16 @@ def graph_loop_ms(calls, stream, replays=5):
     return ms
 
 
+N_QUERY_SETS = 4   # consecutive steps cycle through this many seeded query sets
+HINT_SCALE = 0.7  # the draft's cut bound: the previous step's cut of the layer x 0.7
+
+
 class StepState:
-    """Resident inputs, outputs and workspaces of one workload's decode step."""
+    """Resident inputs, outputs and workspaces of one workload's decode step.
+    Consecutive steps take different seeded queries (N_QUERY_SETS sets per
+    layer; set 0 is the one the planted chunks follow), so the retrieval
+    drafter's cut moves from step to step and the previous step's cut is a
+    bound, not the answer."""
 
     def __init__(self, w, layers, dev, tf, synth):
         import torch
@@ -343,14 +351,19 @@ class StepState:
         self.M = torch.empty((layers, B, Hkv, self.Cmax, D), dtype=torch.bfloat16, device=dev)
         self.seq_cpu = synth.seq_lens_for(w)
         self.seq = self.seq_cpu.to(dev)
-        qs, Qs = [], []
+        qs, Qs = [[] for _ in range(N_QUERY_SETS)], [[] for _ in range(N_QUERY_SETS)]
         for l in range(layers):
-            q, Q = synth.decode_queries(w, l, device=dev)
-            synth.kv_cache(w, l, q, self.seq_cpu, device=dev, K_out=self.K[l], V_out=self.V[l])
-            qs.append(q)
-            Qs.append(Q)
-        self.q = torch.stack(qs)
-        self.Q = torch.stack(Qs)
+            for k in range(N_QUERY_SETS):
+                q, Q = synth.decode_queries(w, l + 1000 * k, device=dev)
+                qs[k].append(q)
+                Qs[k].append(Q)
+            synth.kv_cache(w, l, qs[0][l], self.seq_cpu, device=dev, K_out=self.K[l], V_out=self.V[l])
+        self.q_sets = torch.stack([torch.stack(x) for x in qs])  # [sets, layers, B, Hq, D]
+        self.Q_sets = torch.stack([torch.stack(x) for x in Qs])
+        self.q = self.q_sets[0].clone()  # the live input buffers (host copies land here end to end)
+        self.Q = self.Q_sets[0].clone()
+        self.cut = torch.full((layers, B, Hkv), float("nan"), dtype=torch.float32, device=dev)
+        self.hint = torch.full_like(self.cut, float("nan"))
         for l in range(layers):
             tf.tf_build_chunk_means(self.K[l], self.seq, self.M[l])
         self.idx = torch.empty((layers, B, Hkv, w.kc), dtype=torch.int32, device=dev)
@@ -393,35 +406,59 @@ class StepState:
         }
 
 
-def make_step(st, tf, two_call, stream):
+def make_step(st, tf, two_call, stream, hinted=True):
+    """One decode step over the layers.  step(evs, k) takes query set k (None:
+    the live buffers st.q / st.Q).  With hinted, the fused drafter gets the
+    previous step's cut of each layer x HINT_SCALE as a lower bound (a decode
+    loop has it for free; one elementwise op per step forms it)."""
+    import torch
+
     w = st.w
     kinds = ("draft", "window", "verify")
+    hinted = hinted and not two_call
 
-    def draft(l):
+    def draft(l, q=None):
+        q = st.q if q is None else q
         if two_call:
-            tf.tf_chunk_scores_topk(st.q[l], st.M[l], st.seq, w.L, w.kc, st.idx[l], st.nsel[l], ws=st.ws_topk)
-            tf.tf_sparse_decode_attn(st.q[l], st.K[l], st.V[l], st.seq, st.idx[l], st.nsel[l], st.scale,
+            tf.tf_chunk_scores_topk(q[l], st.M[l], st.seq, w.L, w.kc, st.idx[l], st.nsel[l], ws=st.ws_topk)
+            tf.tf_sparse_decode_attn(q[l], st.K[l], st.V[l], st.seq, st.idx[l], st.nsel[l], st.scale,
                                      out=st.o_sp[l], ws=st.ws_sp)
         else:
-            tf.tf_retrieval_draft_attn(st.q[l], st.M[l], st.K[l], st.V[l], st.seq, w.kc, st.scale, idx=st.idx[l],
-                                       n_sel=st.nsel[l], out=st.o_sp[l])
+            tf.tf_retrieval_draft_attn(q[l], st.M[l], st.K[l], st.V[l], st.seq, w.kc, st.scale, idx=st.idx[l],
+                                       n_sel=st.nsel[l], out=st.o_sp[l], s_cut=st.cut[l],
+                                       cut_hint=st.hint[l] if hinted else None)
 
-    def step(evs=None):
+    def step(evs=None, k=None):
+        q = st.q if k is None else st.q_sets[k % N_QUERY_SETS]
+        Q = st.Q if k is None else st.Q_sets[k % N_QUERY_SETS]
+        if hinted:
+            torch.mul(st.cut, HINT_SCALE, out=st.hint)
         for l in range(st.layers):
             if evs is not None:
                 evs[l][0].record(stream)
-            draft(l)
+            draft(l, q)
             if evs is not None:
                 evs[l][1].record(stream)
-            tf.tf_stream_window_attn(st.q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window, st.scale,
+            tf.tf_stream_window_attn(q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window, st.scale,
                                      out=st.o_win[l], ws=st.ws_win)
             if evs is not None:
                 evs[l][2].record(stream)
-            tf.tf_verify_attn(st.Q[l], st.K[l], st.V[l], st.seq, st.scale, out=st.o_ver[l], ws=st.ws_ver)
+            tf.tf_verify_attn(Q[l], st.K[l], st.V[l], st.seq, st.scale, out=st.o_ver[l], ws=st.ws_ver)
             if evs is not None:
                 evs[l][3].record(stream)
 
     return step, draft, kinds
+
+
+class StepCycle:
+    """Calls step(k=0), step(k=1), ... : every call takes the next query set."""
+
+    def __init__(self, step):
+        self.step, self.k = step, 0
+
+    def __call__(self, evs=None):
+        self.step(evs, self.k)
+        self.k += 1
 
 
 def time_steps(run_step, steps, stream, world, local):
@@ -444,7 +481,8 @@ def time_steps(run_step, steps, stream, world, local):
 
 
 def per_kernel_times(step, layers, k_steps, kinds):
-    """A second region with an event before and after every launch."""
+    """A second region with an event before and after every launch (step: a
+    StepCycle, so these steps too take new queries)."""
     import torch
 
     evs = [[[_ev() for _ in range(4)] for _ in range(layers)] for _ in range(k_steps)]
@@ -493,6 +531,42 @@ def measure_level1(st, w, tf, dev, stream, peak):
     return out
 
 
+def draft_back_to_back_ms(st, draft, cyc, stream):
+    """The retrieval draft alone, back to back over the layers, on the next
+    query set (with the bounds the last step left): consecutive launches
+    overlap through programmatic dependent launch (no events between them),
+    and every layer's means and K/V are cold."""
+    import torch
+
+    q = st.q_sets[cyc.k % N_QUERY_SETS]
+    torch.mul(st.cut, HINT_SCALE, out=st.hint)
+    d0, d1 = _ev(), _ev()
+    torch.cuda.synchronize()
+    d0.record(stream)
+    for l in range(st.layers):
+        draft(l, q)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    return d0.elapsed_time(d1) / st.layers
+
+
+def measure_cold_start(st, tf, args, stream, world, local, steps, k0, nb, peak):
+    """The same step with no cut bounds (the drafter starts every selection
+    from scratch): steps/s, and the drafter per launch and back to back."""
+    step_c, draft_c, kinds = make_step(st, tf, args.two_call_draft, stream, hinted=False)
+    cyc = StepCycle(step_c)
+    cyc.k = k0
+    for _ in range(2):
+        cyc()
+    value, elapsed_s, _ = time_steps(cyc, steps, stream, world, local)
+    per_kind = per_kernel_times(cyc, st.layers, max(3, steps // 2), kinds)
+    draft = kernel_entry(nb["draft"], statistics.mean(per_kind["draft"]), peak)
+    draft["back_to_back"] = kernel_entry(nb["draft"], draft_back_to_back_ms(st, draft_c, cyc, stream), peak)
+    return {"value": round(value, 4), "unit": "steps/s", "steps": steps,
+            "ms_per_step": round(elapsed_s / steps * 1e3, 4), "retrieval_draft": draft,
+            "what": "the same step without the previous step's cut as a bound"}
+
+
 def measure_extra_workload(w, args, tf, synth, dev, stream, world, local, peak):
     """The step on another workload: steps/s, the per-kernel breakdown with the
     verify roofline, and the drafter back to back."""
@@ -500,26 +574,23 @@ def measure_extra_workload(w, args, tf, synth, dev, stream, world, local, peak):
 
     st = StepState(w, w.layers, dev, tf, synth)
     step, draft, kinds = make_step(st, tf, args.two_call_draft, stream)
+    cyc = StepCycle(step)
     for _ in range(max(3, args.warmup)):
-        step()
+        cyc()
     torch.cuda.synchronize()
     steps = max(3, args.steps // 2)
-    value, elapsed_s, clocks = time_steps(step, steps, stream, world, local)
-    per_kind = per_kernel_times(step, st.layers, max(3, steps // 2), kinds)
+    value, elapsed_s, clocks = time_steps(cyc, steps, stream, world, local)
+    per_kind = per_kernel_times(cyc, st.layers, max(3, steps // 2), kinds)
     nb = st.bytes_per_launch()
     kern = {}
     for k in kinds:
         name = "retrieval_draft" if k == "draft" else k
         kern[name] = kernel_entry(nb[k], statistics.mean(per_kind[k]), peak)
-    d0, d1 = _ev(), _ev()
-    torch.cuda.synchronize()
-    d0.record(stream)
-    for l in range(st.layers):
-        draft(l)
-    d1.record(stream)
-    torch.cuda.synchronize()
-    kern["retrieval_draft"]["back_to_back"] = kernel_entry(nb["draft"], d0.elapsed_time(d1) / st.layers, peak)
+    kern["retrieval_draft"]["back_to_back"] = kernel_entry(nb["draft"], draft_back_to_back_ms(st, draft, cyc, stream),
+                                                           peak)
     kern["sparse_verify_level1"] = measure_level1(st, w, tf, dev, stream, peak)
+    cold = None if args.two_call_draft else measure_cold_start(st, tf, args, stream, world, local, steps, cyc.k, nb,
+                                                                peak)
     ver = kern["verify"]
     out = {"value": round(value, 4), "unit": "steps/s", "steps": steps, "ms_per_step": round(elapsed_s / steps * 1e3, 4),
            "config": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D, "context": w.L, "layers": w.layers,
@@ -530,6 +601,8 @@ def measure_extra_workload(w, args, tf, synth, dev, stream, world, local, peak):
                         "traffic": recorded_traffic("verify_attn.cu", w.name)},
            "kernels": kern, "clocks": clocks,
            "gpu_launches": steps * st.layers * (4 if args.two_call_draft else 3)}
+    if cold is not None:
+        out["cold_start"] = cold
     kern["retrieval_draft"]["traffic"] = None if args.two_call_draft else recorded_traffic("retrieval_draft.cu",
                                                                                             w.name)
     del st
@@ -661,27 +734,44 @@ def run_gpu(args):
     means_bytes = B * Hkv * L * D * 2 + B * Hkv * st.Cmax * D * 2
 
     step, draft, kinds = make_step(st, tf, args.two_call_draft, stream)
+    cyc = StepCycle(step)
     for _ in range(args.warmup):
-        step()
+        cyc()
     torch.cuda.synchronize()
-    run_step = step
+    run_step = cyc
+    graphs = []
     if args.graph:
         # the same launches, programmatic-dependent-launch edges included,
-        # captured once; every buffer and workspace is already allocated
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
+        # captured once per query set (and once on the live input buffers,
+        # for the end-to-end loop); every buffer and workspace is already
+        # allocated
+        for k in list(range(N_QUERY_SETS)) + [None]:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(None, k)
+            graphs.append(g)
         torch.cuda.synchronize()
-        graph.replay()
+        for g in graphs:
+            g.replay()
         torch.cuda.synchronize()
-        run_step = graph.replay
+
+        class GraphCycle:
+            def __init__(self):
+                self.k = 0
+
+            def __call__(self):
+                graphs[self.k % N_QUERY_SETS].replay()
+                self.k += 1
+
+        run_step = GraphCycle()
 
     # ---- timed region: device-resident inputs (64 GiB of KV >> 129 MB L2)
     value, elapsed_s, clocks = time_steps(run_step, args.steps, stream, world, local)
 
     # ---- per-kernel breakdown and the verify roofline
     k_steps = max(3, args.steps // 2)
-    per_kind = per_kernel_times(step, layers, k_steps, kinds)
+    cyc.k = getattr(run_step, "k", cyc.k)
+    per_kind = per_kernel_times(cyc, layers, k_steps, kinds)
     nb = st.bytes_per_launch()
     kernels = {}
     for k in kinds:
@@ -706,17 +796,8 @@ def run_gpu(args):
         for i, k in enumerate(("topk", "sparse")):
             ms = statistics.mean(ev[l][i].elapsed_time(ev[l][i + 1]) for l in range(layers))
             kernels["two_call_" + k] = kernel_entry(nb[k], ms, peak)
-    # the retrieval draft alone, back to back over the layers: consecutive
-    # launches overlap through programmatic dependent launch (no events between
-    # them), and every layer's means and K/V are cold
-    d0, d1 = _ev(), _ev()
-    torch.cuda.synchronize()
-    d0.record(stream)
-    for l in range(layers):
-        draft(l)
-    d1.record(stream)
-    torch.cuda.synchronize()
-    kernels["retrieval_draft"]["back_to_back"] = kernel_entry(nb["draft"], d0.elapsed_time(d1) / layers, peak)
+    kernels["retrieval_draft"]["back_to_back"] = kernel_entry(nb["draft"], draft_back_to_back_ms(st, draft, cyc, stream),
+                                                              peak)
 
     kernels["sparse_verify_level1"] = measure_level1(st, w, tf, dev, stream, peak)
     # the window: back to back, and its fixed cost with 4 sinks + 12 recent rows (16 rows) per unit
@@ -746,7 +827,10 @@ def run_gpu(args):
         "config": {"workload": w.name, "B": B, "Hq": Hq, "Hkv": Hkv, "head_dim": D, "context": L, "layers": layers,
                    "chunk": w.chunk, "budget_tokens": w.budget, "window": f"{w.n_sink}+{w.window}",
                    "verify_tokens": T, "l2": "inputs larger than L2: 2 GiB of K+V per layer, no flush needed",
-                   "launch": "one CUDA graph per step" if args.graph else "stream launches"},
+                   "launch": "one CUDA graph per step" if args.graph else "stream launches",
+                   "queries": f"{N_QUERY_SETS} seeded query sets cycled over the steps; the retrieval drafter "
+                              f"takes the previous step's cut x {HINT_SCALE} of each layer as a bound "
+                              f"(cold_start: the same step without it)"},
         "roofline": {"bound": "hbm", "kernel": "tf_verify_attn", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": nb["verify"], "peak_source": peak_kind},
@@ -792,21 +876,23 @@ def run_gpu(args):
                                                          "launches_per_call": 2,
                                                          "timing": "20 calls replayed as one CUDA graph"}
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: every step
+    # copies its query set from pinned host memory into the live buffers
     if not args.no_e2e:
-        q_host = st.q.cpu().pin_memory()
-        Q_host = st.Q.cpu().pin_memory()
+        q_host = st.q_sets.cpu().pin_memory()
+        Q_host = st.Q_sets.cpu().pin_memory()
         outs_host = [t.cpu().pin_memory() for t in (st.o_sp, st.o_win, st.o_ver)]
-        h2d = q_host.numel() * 2 + Q_host.numel() * 2
+        h2d = q_host[0].numel() * 2 + Q_host[0].numel() * 2
         d2h = sum(t.numel() * 4 for t in outs_host)
         e_steps = max(3, args.steps // 2)
+        live = graphs[-1].replay if graphs else (lambda: step(None, None))
         barrier(world)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for _ in range(e_steps):
-            st.q.copy_(q_host, non_blocking=True)
-            st.Q.copy_(Q_host, non_blocking=True)
-            run_step()
+        for i in range(e_steps):
+            st.q.copy_(q_host[i % N_QUERY_SETS], non_blocking=True)
+            st.Q.copy_(Q_host[i % N_QUERY_SETS], non_blocking=True)
+            live()
             for h, d in zip(outs_host, (st.o_sp, st.o_win, st.o_ver)):
                 h.copy_(d, non_blocking=True)
             torch.cuda.current_stream().synchronize()
@@ -814,9 +900,9 @@ def run_gpu(args):
         result["e2e"] = {"value": round(e_value, 4), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                          "d2h_bytes_per_step": d2h}
 
-    del st, run_step, step, draft
-    if args.graph:
-        del graph
+    if not args.two_call_draft:
+        result["cold_start"] = measure_cold_start(st, tf, args, stream, world, local, k_steps, cyc.k + 1, nb, peak)
+    del st, run_step, step, draft, cyc, graphs
     torch.cuda.empty_cache()
 
     # ---- the other workloads, one after the other (each frees its cache)

@@ -35,6 +35,8 @@ _SIGS = {
     "tf_sparse_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_sparse_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
     "tf_retrieval_draft_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
+    "tf_retrieval_draft_attn_hinted": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P,
+                                            _P]),
     "tf_stream_window_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
     "tf_stream_window_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_sparse_verify_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
@@ -268,9 +270,11 @@ def tf_pack_retrieval_cache(K, V, seq_lens, idx, n_sel, Kc=None, Vc=None, lens=N
 
 
 def tf_retrieval_draft_attn(q, M, K, V, seq_lens, kc, scale, idx=None, n_sel=None, s_cut=None, out=None, chunk=8,
-                            stream=None):
+                            stream=None, cut_hint=None):
     """Scores, top-k and sparse attention of the retrieval drafter in one launch.
-    Returns (idx, n_sel, out); s_cut is filled when given."""
+    Returns (idx, n_sel, out); s_cut is filled when given.  cut_hint [B, Hkv]
+    float32 (optional): lower bounds on the cut scores, which change only the
+    time (tf_retrieval_draft_attn_hinted)."""
     _need(q, torch.bfloat16, "q", 3)
     _need(M, torch.bfloat16, "M", 4)
     _need(K, torch.bfloat16, "K", 4)
@@ -289,9 +293,18 @@ def tf_retrieval_draft_attn(q, M, K, V, seq_lens, kc, scale, idx=None, n_sel=Non
     _need(out, torch.float32, "out", 3)
     if s_cut is not None:
         _need(s_cut, torch.float32, "s_cut", 2)
-    _check(load().tf_retrieval_draft_attn(_ptr(q), _ptr(M), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax, D,
-                                          chunk, kc, float(scale), _ptr(idx), _ptr(n_sel), _ptr(s_cut), _ptr(out),
-                                          _stream(stream)), "tf_retrieval_draft_attn")
+    if cut_hint is None:
+        _check(load().tf_retrieval_draft_attn(_ptr(q), _ptr(M), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax,
+                                              D, chunk, kc, float(scale), _ptr(idx), _ptr(n_sel), _ptr(s_cut),
+                                              _ptr(out), _stream(stream)), "tf_retrieval_draft_attn")
+    else:
+        _need(cut_hint, torch.float32, "cut_hint", 2)
+        if tuple(cut_hint.shape) != (B, Hkv):
+            raise ValueError(f"cut_hint must be [B, Hkv] = {(B, Hkv)}, got {tuple(cut_hint.shape)}")
+        _check(load().tf_retrieval_draft_attn_hinted(_ptr(q), _ptr(M), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv,
+                                                     Lmax, D, chunk, kc, float(scale), _ptr(cut_hint), _ptr(idx),
+                                                     _ptr(n_sel), _ptr(s_cut), _ptr(out), _stream(stream)),
+               "tf_retrieval_draft_attn_hinted")
     return idx, n_sel, out
 
 

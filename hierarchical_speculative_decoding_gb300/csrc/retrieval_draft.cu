@@ -52,6 +52,7 @@ constexpr int kRingSlots = kComputeWarps;               // one slot per consumer
 constexpr int kEarlySlots = kComputeWarps - kCutWarps;  // slots of warps 8..14
 constexpr int kSlotBytes = 4096;  // K rows [0, 2 KB), V rows [2 KB, 4 KB)
 constexpr int kCandCap = 2048;    // keys of the threshold bin gathered on every CTA
+constexpr int kHintCap = 4096;    // keys above a cut bound gathered on every CTA (over gcand and hist1)
 constexpr int kMaxList = 2048;    // selected chunks per CTA (kc <= kMaxList)
 constexpr uint32_t kIdleLimit = 1u << 22;  // producer polls without progress before it gives up
 
@@ -61,7 +62,8 @@ constexpr uint32_t kIdleLimit = 1u << 22;  // producer polls without progress be
 //  [28672, 61440)  ring slots 7..14 (consumers 0..7) once the cut is done;
 //                  until then hist2, hist3, gcand (the cut group's scratch)
 //                  and hist1 (read by the other CTAs in round 1, which they
-//                  finish before the cut's cluster barrier)
+//                  finish before the cut's cluster barrier; with a cut bound
+//                  that holds, no round 1 runs and gcand extends over it)
 //  cand            read by the other CTAs until the end of their cut: never overlaid
 //  alist           this CTA's selected chunks (certain ones first)
 //  keys            this CTA's score keys
@@ -74,6 +76,7 @@ constexpr int kOffCand = kRingSlots * kSlotBytes;    // 61440
 constexpr int kOffList = kOffCand + kCandCap * 4;    // 69632
 constexpr int kOffKeys = kOffList + kMaxList * 4;    // 77824
 static_assert(kOffHist1 + 2048 * 4 <= kOffCand, "the cut's scratch must fit the late slots");
+static_assert(kOffGcand + kHintCap * 4 <= kOffCand, "the hinted gather must fit the late slots");
 static_assert(kOffTot + 2048 * 4 <= kOffHist2, "tot must stay inside the early slots");
 
 struct DraftParams {
@@ -88,6 +91,7 @@ struct DraftParams {
   int32_t* n_sel;    // [B, Hkv]
   float* s_cut;      // [B, Hkv] or null
   float* out;        // [B, Hq, 128]
+  const float* hint;  // [B, Hkv] lower bounds on the cut scores, or null (NaN: none for that unit)
 };
 
 size_t draft_smem(int slice) { return (size_t)kOffKeys + (size_t)slice * sizeof(uint32_t); }
@@ -106,7 +110,8 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
   __shared__ float wm[kComputeWarps][NQ], wl[kComputeWarps][NQ];
   __shared__ float cpart[NQ][kHeadDim], cm[NQ], cl[NQ];
   __shared__ uint32_t s_min;
-  __shared__ int s_na, s_ntot, s_abort;
+  __shared__ int s_na, s_ntot, s_abort, s_hcnt;
+  __shared__ int s_hroff[kMaxCluster + 1];
   __shared__ volatile int s_cut_done;
 
   uint8_t* ring = smem;
@@ -135,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
       mbar_init(&bar_empty[s], 1);
     }
     s_abort = 0;
+    s_hcnt = 0;
     s_na = 0;
     s_cut_done = 0;
     s_min = 0xffffffffu;
@@ -197,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
   uint32_t T = 0;
   bool split = false;  // warps 0..7 finish the cut while the others attend
   topk::Round1 r1{};
+  topk::Hinted hinted{};
   if (C <= p.kc) {
     // Every chunk is selected: ids in order, slots past C hold -1, s_cut = min score.
     uint32_t mn = 0xffffffffu;
@@ -215,13 +222,32 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
       s_ntot = n;
     }
   } else {
-    r1 = topk::round1(a, p.kc, S);
+    // With a lower bound on the cut, list the keys that reach it; if the
+    // cluster holds between kc and kHintCap of them, the cut comes from those
+    // keys alone (one cluster barrier, no cluster histogram round, no second
+    // barrier for the rest of the cut).  Otherwise the unhinted path runs,
+    // with the barrier already passed; the selection is the same either way.
+    const float hv = p.hint ? p.hint[unit] : NAN;
+    if (hv == hv) {
+      const uint32_t hkey = score_key(hv);
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint32_t key = keys[i];
+        if (key >= hkey) {
+          const int at = atomicAdd(&s_hcnt, 1);
+          if (at < kCandCap) a.cand[at] = key;
+        }
+      }
+      __syncthreads();
+      hinted = topk::hinted_round1(a, p.kc, S, kHintCap, &s_hcnt, s_hroff);
+    }
+    // after a bound that did not hold, round 1 needs no barrier of its own
+    r1 = hinted.ok ? hinted.r1 : topk::round1(a, p.kc, S, hv == hv);
     // chunks above bin b1: selected whatever the rest of the cut (list order is free)
     for (int i = threadIdx.x; i < n; i += kThreads)
       if ((keys[i] >> 21) > r1.b1) alist[atomicAdd(&s_na, 1)] = c0 + i;
     __syncthreads();
     if (threadIdx.x == 0) s_ntot = s_na;
-    split = r1.ncand_tot <= kCandCap;
+    split = hinted.ok || r1.ncand_tot <= kCandCap;
     if (!split) {
       // rare: resolve the cut with every warp, attend afterwards
       __syncthreads();
@@ -251,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
   const bool cut_group = split && warp < kCutWarps;
   if (cut_group) {
     // ---- warps 0..7: the rest of the cut, then consumers of slots 7..14
-    const topk::Cut cut = topk::fast_cut(a, n, S, rank, r1, topk::Warps0to7Bar());
+    const topk::Cut cut = hinted.ok ? topk::hinted_cut(a, S, rank, hinted, s_hroff, topk::Warps0to7Bar())
+                                    : topk::fast_cut(a, n, S, rank, r1, topk::Warps0to7Bar());
     T = cut.T;
     topk::compact(a, n, p.kc, cut, topk::Warps0to7Bar(), [&](int i, int pos, bool unc) {
       out_idx[pos] = c0 + i;
@@ -265,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
       __threadfence_block();
       s_cut_done = 1;
     }
-  } else if (split) {
+  } else if (split && !hinted.ok) {
     cluster_arrive();  // the cut group's one cluster barrier; waited for below
   }
 
@@ -413,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
       if (lane == 0) mbar_arrive(&bar_empty[slot]);
     }
   }
-  if (split && !cut_group) cluster_wait();
+  if (split && !cut_group && !hinted.ok) cluster_wait();
   __syncthreads();  // every chunk consumed: the ring is idle and serves as scratch
   if (s_abort && threadIdx.x == 0) {
     // (only after a timeout) let every copy still in flight land before the
@@ -567,11 +594,13 @@ TF_DBG_READER(dbg_read_draft)
 
 }  // namespace tf
 
-extern "C" tf_status tf_retrieval_draft_attn(const uint16_t* q, const uint16_t* M, const uint16_t* K,
-                                             const uint16_t* V, const int32_t* seq_lens, int B, int Hq, int Hkv,
-                                             int Lmax, int D, int chunk, int kc, float scale, int32_t* idx,
-                                             int32_t* n_sel, float* s_cut, float* out, tf_stream_t stream) {
-  using namespace tf;
+namespace tf {
+namespace {
+
+tf_status draft_entry(const uint16_t* q, const uint16_t* M, const uint16_t* K, const uint16_t* V,
+                      const int32_t* seq_lens, int B, int Hq, int Hkv, int Lmax, int D, int chunk, int kc, float scale,
+                      int32_t* idx, int32_t* n_sel, float* s_cut, float* out, const float* hint,
+                      cudaStream_t stream) {
   if (!q || !M || !K || !V || !seq_lens || !idx || !n_sel || !out) return TF_ERR_INVALID_ARG;
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || kc <= 0 || Hq % Hkv != 0) return TF_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(M) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return TF_ERR_INVALID_ARG;
@@ -581,11 +610,32 @@ extern "C" tf_status tf_retrieval_draft_attn(const uint16_t* q, const uint16_t* 
   const int units = B * Hkv;
   if (units > 65535) return TF_ERR_UNSUPPORTED;
   const int Cmax = (Lmax + kChunk - 1) / kChunk;
-  DraftParams p{q, M, K, V, seq_lens, Hq, Hkv, Lmax, kc, scale * kLog2e, idx, n_sel, s_cut, out};
+  DraftParams p{q, M, K, V, seq_lens, Hq, Hkv, Lmax, kc, scale * kLog2e, idx, n_sel, s_cut, out, hint};
   const int G = Hq / Hkv;
   switch (G) {
     case 1: return launch_draft<1>(p, units, Cmax < 1 ? 1 : Cmax, stream);
     case 2: return launch_draft<2>(p, units, Cmax < 1 ? 1 : Cmax, stream);
     default: return launch_draft<4>(p, units, Cmax < 1 ? 1 : Cmax, stream);
   }
+}
+
+}  // namespace
+}  // namespace tf
+
+extern "C" tf_status tf_retrieval_draft_attn(const uint16_t* q, const uint16_t* M, const uint16_t* K,
+                                             const uint16_t* V, const int32_t* seq_lens, int B, int Hq, int Hkv,
+                                             int Lmax, int D, int chunk, int kc, float scale, int32_t* idx,
+                                             int32_t* n_sel, float* s_cut, float* out, tf_stream_t stream) {
+  return tf::draft_entry(q, M, K, V, seq_lens, B, Hq, Hkv, Lmax, D, chunk, kc, scale, idx, n_sel, s_cut, out,
+                         nullptr, (cudaStream_t)stream);
+}
+
+extern "C" tf_status tf_retrieval_draft_attn_hinted(const uint16_t* q, const uint16_t* M, const uint16_t* K,
+                                                    const uint16_t* V, const int32_t* seq_lens, int B, int Hq,
+                                                    int Hkv, int Lmax, int D, int chunk, int kc, float scale,
+                                                    const float* cut_hint, int32_t* idx, int32_t* n_sel,
+                                                    float* s_cut, float* out, tf_stream_t stream) {
+  if (!cut_hint) return TF_ERR_INVALID_ARG;
+  return tf::draft_entry(q, M, K, V, seq_lens, B, Hq, Hkv, Lmax, D, chunk, kc, scale, idx, n_sel, s_cut, out,
+                         cut_hint, (cudaStream_t)stream);
 }

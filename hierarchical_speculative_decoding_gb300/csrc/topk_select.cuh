@@ -193,9 +193,9 @@ struct Round1 {
   int ncand_tot;  // keys of bin b1 over the cluster
 };
 
-__device__ __forceinline__ Round1 round1(const Arrays& a, int kc, int S) {
+__device__ __forceinline__ Round1 round1(const Arrays& a, int kc, int S, bool synced = false) {
   __shared__ int s_wsum[kWarps], s_bin, s_krem;
-  cluster_sync();
+  if (!synced) cluster_sync();  // (synced: a cluster barrier since the histograms were built)
   cluster_sum(a.hist1, a.tot, 2048, S);
   find_bin(a.tot, 2048, kc, s_wsum, &s_bin, &s_krem, CtaBar());
   Round1 r;
@@ -203,6 +203,53 @@ __device__ __forceinline__ Round1 round1(const Arrays& a, int kc, int S) {
   r.krem1 = s_krem;
   r.ncand_tot = (int)a.tot[r.b1];
   return r;
+}
+
+// Bits 20..0 of the cut from keys gathered on this CTA, a.gcand[0, ng) (keys
+// outside bin b1 are skipped; the cut is the krem1-th largest key of the bin),
+// then every CTA's counts of keys > T and == T among them (CTA r's keys are
+// gcand[roff[r], roff[r + 1])), added to rgt[r] and req[r], and this CTA's
+// output offsets.  hist2 and hist3 must be zero.  The group of Bar.
+template <class Bar>
+__device__ Cut resolve_gathered(const Arrays& a, int ng, uint32_t b1, int krem1, int S, uint32_t rank,
+                                const int* roff, int* rgt, int* req, Bar bar) {
+  constexpr int NT = Bar::kNT;
+  __shared__ int s_wsum[NT / 32], s_bin, s_krem;
+  Cut cut;
+  cut.b1 = b1;
+  cut.cta_eq = 0;
+  cut.cta_sel = 0;
+  // bits 20..10, then 9..0
+  for (int i = threadIdx.x; i < ng; i += NT) {
+    const uint32_t key = a.gcand[i];
+    if ((key >> 21) == b1) atomicAdd(&a.hist2[(key >> 10) & 2047u], 1u);
+  }
+  bar();
+  find_bin(a.hist2, 2048, krem1, s_wsum, &s_bin, &s_krem, bar);
+  const uint32_t pre2 = (b1 << 11) | (uint32_t)s_bin;
+  const int krem2 = s_krem;
+  for (int i = threadIdx.x; i < ng; i += NT) {
+    const uint32_t key = a.gcand[i];
+    if ((key >> 10) == pre2) atomicAdd(&a.hist3[key & 1023u], 1u);
+  }
+  bar();
+  find_bin(a.hist3, 1024, krem2, s_wsum, &s_bin, &s_krem, bar);
+  cut.T = (pre2 << 10) | (uint32_t)s_bin;
+  cut.take_eq = s_krem;
+  // per-CTA counts of keys > T and == T among the gathered keys
+  for (int i = threadIdx.x; i < ng; i += NT) {
+    const uint32_t key = a.gcand[i];
+    int r = 0;
+    while (r + 1 < S && i >= roff[r + 1]) ++r;
+    if (key > cut.T) atomicAdd(&rgt[r], 1);
+    if (key == cut.T) atomicAdd(&req[r], 1);
+  }
+  bar();
+  for (int r = 0; r < (int)rank; ++r) {
+    cut.cta_sel += rgt[r] + min(max(cut.take_eq - cut.cta_eq, 0), req[r]);
+    cut.cta_eq += req[r];
+  }
+  return cut;
 }
 
 // Rest of the cut when the cluster's keys of bin b1 fit the candidate buffer
@@ -215,13 +262,8 @@ template <class Bar>
 __device__ Cut fast_cut(const Arrays& a, int n, int S, uint32_t rank, const Round1& r1, Bar bar) {
   constexpr int NT = Bar::kNT;
   __shared__ int s_ncand, s_above, s_roff[kMaxCluster + 1], s_rgt[kMaxCluster], s_req[kMaxCluster];
-  __shared__ int s_wsum[NT / 32], s_bin, s_krem;
   const uint32_t b1 = r1.b1;
   const int ncand_tot = r1.ncand_tot;
-  Cut cut;
-  cut.b1 = b1;
-  cut.cta_eq = 0;
-  cut.cta_sel = 0;
   if (threadIdx.x == 0) {
     s_ncand = 0;
     s_above = 0;
@@ -274,34 +316,91 @@ __device__ Cut fast_cut(const Arrays& a, int n, int S, uint32_t rank, const Roun
       if (base + u * NT < ncand_tot) a.gcand[base + u * NT] = v[u];
   }
   bar();
-  // bits 20..10, then 9..0, among the gathered keys (all of them are in bin b1)
-  for (int i = threadIdx.x; i < ncand_tot; i += NT) atomicAdd(&a.hist2[(a.gcand[i] >> 10) & 2047u], 1u);
-  bar();
-  find_bin(a.hist2, 2048, r1.krem1, s_wsum, &s_bin, &s_krem, bar);
-  const uint32_t pre2 = (b1 << 11) | (uint32_t)s_bin;
-  const int krem2 = s_krem;
-  for (int i = threadIdx.x; i < ncand_tot; i += NT) {
-    const uint32_t key = a.gcand[i];
-    if ((key >> 10) == pre2) atomicAdd(&a.hist3[key & 1023u], 1u);
+  return resolve_gathered(a, ncand_tot, b1, r1.krem1, S, rank, s_roff, s_rgt, s_req, bar);
+}
+
+// Round 1 from a lower bound on the cut (a key that every selected chunk
+// reaches, e.g. from the previous decode step's cut): every CTA has listed its
+// keys >= the bound in a.cand (*cnt of them; only the first a.cap are stored).
+// All threads of all CTAs.  One cluster barrier, then every CTA reads the S
+// counts; when the cluster holds between kc and gcap such keys (and no CTA
+// more than a.cap), every CTA gathers all of them into a.gcand (room for gcap;
+// CTA r's at roff[r] ..) and bin b1 of the kc-th largest key follows from a
+// local histogram of those keys (no cluster histogram round; every key of the
+// cluster above the bound is gathered, so the cut is the kc-th largest of
+// them).  Otherwise (the bound lies above the cut, or admits too many keys)
+// nothing that round1 reads has changed, ok is false on every CTA alike, and
+// round1 may skip its own cluster barrier.  a.tot is scratch.
+struct Hinted {
+  bool ok;
+  Round1 r1;
+  int ntot;  // keys gathered
+};
+
+__device__ __forceinline__ Hinted hinted_round1(const Arrays& a, int kc, int S, int gcap, const int* cnt,
+                                                int* roff) {
+  __shared__ int s_wsum[kWarps], s_bin, s_krem, s_over;
+  Hinted h{};
+  cluster_sync();
+  if (threadIdx.x < 32) {
+    const int r = threadIdx.x;
+    const int nc = r < S ? (int)dsmem_ld_u32(cnt, (uint32_t)r) : 0;
+    int incl = nc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (r >= o) incl += v;
+    }
+    if (r < S) roff[r] = incl - nc;
+    if (r == S - 1) roff[S] = incl;
+    const unsigned over = __ballot_sync(0xffffffffu, nc > a.cap);
+    if (r == 0) s_over = over != 0u;
+  }
+  for (int i = threadIdx.x; i < 2048; i += kThreads) a.tot[i] = 0;
+  __syncthreads();
+  const int ntot = roff[S];
+  if (ntot < kc || ntot > gcap || s_over) return h;
+  for (int base = threadIdx.x; base < ntot; base += 4 * kThreads) {
+    uint32_t v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * kThreads;
+      int r = 0;
+      if (i < ntot)
+        while (r + 1 < S && i >= roff[r + 1]) ++r;
+      v[u] = i < ntot ? dsmem_ld_u32(a.cand + (i - roff[r]), (uint32_t)r) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * kThreads;
+      if (i < ntot) {
+        a.gcand[i] = v[u];
+        atomicAdd(&a.tot[v[u] >> 21], 1u);
+      }
+    }
+  }
+  __syncthreads();
+  find_bin(a.tot, 2048, kc, s_wsum, &s_bin, &s_krem, CtaBar());
+  h.ok = true;
+  h.r1.b1 = (uint32_t)s_bin;
+  h.r1.krem1 = s_krem;
+  h.r1.ncand_tot = (int)a.tot[s_bin];
+  h.ntot = ntot;
+  return h;
+}
+
+// Rest of the cut after hinted_round1 succeeded: the gathered keys hold the
+// whole answer, so no cluster barrier.  The group of Bar; hist2 and hist3
+// must be zero.
+template <class Bar>
+__device__ Cut hinted_cut(const Arrays& a, int S, uint32_t rank, const Hinted& h, const int* roff, Bar bar) {
+  __shared__ int s_rgt[kMaxCluster], s_req[kMaxCluster];
+  if (threadIdx.x < kMaxCluster) {
+    s_rgt[threadIdx.x] = 0;
+    s_req[threadIdx.x] = 0;
   }
   bar();
-  find_bin(a.hist3, 1024, krem2, s_wsum, &s_bin, &s_krem, bar);
-  cut.T = (pre2 << 10) | (uint32_t)s_bin;
-  cut.take_eq = s_krem;
-  // per-CTA counts of keys > T and == T among the gathered keys
-  for (int i = threadIdx.x; i < ncand_tot; i += NT) {
-    const uint32_t key = a.gcand[i];
-    int r = 0;
-    while (r + 1 < S && i >= s_roff[r + 1]) ++r;
-    if (key > cut.T) atomicAdd(&s_rgt[r], 1);
-    if (key == cut.T) atomicAdd(&s_req[r], 1);
-  }
-  bar();
-  for (int r = 0; r < (int)rank; ++r) {
-    cut.cta_sel += s_rgt[r] + min(max(cut.take_eq - cut.cta_eq, 0), s_req[r]);
-    cut.cta_eq += s_req[r];
-  }
-  return cut;
+  return resolve_gathered(a, h.ntot, h.r1.b1, h.r1.krem1, S, rank, roff, s_rgt, s_req, bar);
 }
 
 // Rest of the cut when bin b1 holds more keys than the candidate buffer (huge

@@ -218,6 +218,30 @@ TF_API tf_status tf_retrieval_draft_attn(const uint16_t* q, const uint16_t* M, c
                                   float* out, tf_stream_t stream);
 
 /*
+ * tf_retrieval_draft_attn with a lower bound on each (b, g)'s cut score, e.g.
+ * the s_cut of the previous decode step lowered by a margin.  cut_hint
+ * [B, Hkv] float32, device, required (NaN in a slot: no bound for that
+ * (b, g)).  The outputs are exactly those of tf_retrieval_draft_attn on the
+ * same inputs, whatever the bounds: idx, n_sel and s_cut bit for bit, out up
+ * to the fp32 summation order.  Only the time changes.  When between kc and
+ * 4096 chunks of the (b, g) score at least the bound (and no CTA of its
+ * cluster holds more than 2048 of them), the cut is found from those keys
+ * alone: one cluster barrier and a gather of those keys replace the
+ * cluster-wide histogram round and the second barrier of the unhinted path.
+ * Otherwise (a bound above the cut, or one that admits too many chunks) the
+ * count exchange is the only extra cost and the unhinted path runs.  A launch
+ * takes as long as its slowest (b, g), so the bound pays when it holds on
+ * every (b, g): 0.7 x the previous step's s_cut did on every one in the
+ * synthetic decode steps measured here.  Same limits as
+ * tf_retrieval_draft_attn.
+ */
+TF_API tf_status tf_retrieval_draft_attn_hinted(const uint16_t* q, const uint16_t* M, const uint16_t* K,
+                                                const uint16_t* V, const int32_t* seq_lens, int B, int Hq,
+                                                int Hkv, int Lmax, int D, int chunk, int kc, float scale,
+                                                const float* cut_hint, int32_t* idx, int32_t* n_sel,
+                                                float* s_cut, float* out, tf_stream_t stream);
+
+/*
  * Level-1 verification over the retrieval cache:
  * the retrieval drafter -- the target model over the retrieved KV blocks --
  * checks the tiny drafter's candidates in one pass ("TriForce: Hierarchical

@@ -98,6 +98,14 @@ def test_host_validation_rejects_before_launch(lib):
                                        fake, None) == INVALID  # misaligned means
     assert lib.tf_retrieval_draft_attn(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 16, 64, 0.1, fake, fake, null,
                                        fake, None) == UNSUPPORTED  # chunk 16
+    # the same with a cut hint (before idx): required, and the same limits
+    hd = lib.tf_retrieval_draft_attn_hinted
+    assert hd(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 64, 0.1, null, fake, fake, null, fake,
+              None) == INVALID  # no hint array
+    assert hd(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 2049, 0.1, fake, fake, fake, null, fake,
+              None) == UNSUPPORTED
+    assert hd(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 64, 0.1, fake, fake, fake, null, null,
+              None) == INVALID  # no output
     # sparse verification: Q, K, V, seq, idx, n_sel, B, Hq, Hkv, Lmax, D, chunk, kc, T, scale, out, ws, bytes, s
     sv = lib.tf_sparse_verify_attn
     big = 1 << 30

@@ -165,3 +165,102 @@ def test_retrieval_draft_context_just_above_the_budget(cuda_lib):
     c = make_case(w, fill_invalid=float("nan"))
     M_bits = O.build_chunk_means(bits(c["K_cpu"]), c["seq_cpu"].numpy(), w.chunk)
     check_against_oracle(cuda_lib, w, c, M_bits)
+
+
+def _hinted(cuda_lib, w, c, M, hint, kc):
+    s_cut = torch.empty((w.B, w.Hkv), dtype=torch.float32, device="cuda")
+    idx, nsel, out = cuda_lib.tf_retrieval_draft_attn(c["q"], M, c["K"], c["V"], c["seq"], kc, scale_for(w.D),
+                                                      s_cut=s_cut, cut_hint=hint)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), nsel.cpu().numpy(), s_cut.cpu().numpy(), out.cpu().double().numpy()
+
+
+def _hints(scores, s_cut, kc):
+    """Per-unit bounds of every kind: below the cut with kc + 40 keys above it
+    (or with as many as fit 2048), at the cut, one ulp above it, so far below
+    that more than 4096 keys reach it (or every chunk, when there are fewer),
+    and the special values."""
+    B, Hkv = s_cut.shape
+    below = np.full((B, Hkv), np.nan, np.float32)
+    far = np.full((B, Hkv), np.nan, np.float32)
+    for b in range(B):
+        for g in range(Hkv):
+            s = np.sort(np.asarray(scores[b][g], dtype=np.float32))[::-1]
+            if len(s) > kc:
+                below[b, g] = s[min(kc + 40, 2047, len(s) - 1)]
+                far[b, g] = s[min(4200, len(s) - 1)] if len(s) > 4200 else -1e30
+    at = s_cut.astype(np.float32)
+    above = np.nextafter(at, np.float32(np.inf))
+    mixed = np.where((np.arange(B)[:, None] + np.arange(Hkv)[None, :]) % 3 == 0, below,
+                     np.where((np.arange(B)[:, None] + np.arange(Hkv)[None, :]) % 3 == 1, above, np.nan))
+    return {"below": below, "at": at, "above": above, "far-below": far, "nan": np.full_like(at, np.nan),
+            "+inf": np.full_like(at, np.inf), "-inf": np.full_like(at, -np.inf), "mixed": mixed.astype(np.float32)}
+
+
+@pytest.mark.parametrize("w", [
+    small_workload(),
+    small_workload(B=1, Hq=8, Hkv=8, L=32768, budget=4096, ragged=False, planted_frac=0.01),
+    small_workload(B=2, Hq=8, Hkv=4, L=20000, budget=8 * 2048, L_min=17000),
+    small_workload(B=3, Hq=6, Hkv=2, L=5000, budget=8 * 37, L_min=9),
+    small_workload(B=1, Hq=2, Hkv=2, L=32768, budget=4096, ragged=False, planted_frac=0.01),
+], ids=["ragged-gqa", "mha-32k", "kc-2048", "g3-odd-budget", "two-units-16-ctas"])
+def test_retrieval_draft_cut_hint_changes_nothing(cuda_lib, w):
+    """A lower bound on the cut changes only the time: with bounds below, at
+    and just above the cut, admitting more than 4096 keys, NaN, +-inf and a
+    per-unit mix of them, the selection and s_cut equal the unhinted call's
+    bit for bit and the attention matches the oracle over that selection."""
+    c = make_case(w, fill_invalid=float("nan"))
+    M_bits = O.build_chunk_means(bits(c["K_cpu"]), c["seq_cpu"].numpy(), w.chunk)
+    M = torch.from_numpy(M_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    idx0, nsel0, cut0, out0 = run_fused(cuda_lib, w, c, M)
+    scores = O.chunk_scores(bits(c["q_cpu"]), M_bits, c["seq_cpu"].numpy(), w.L, w.chunk, w.Hkv)
+    want = O.sparse_decode_attn(bits(c["q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), c["seq_cpu"].numpy(), idx0,
+                                nsel0, w.chunk, scale_for(w.D))
+    for name, h in _hints(scores, cut0, w.kc).items():
+        idx, nsel, cut, out = _hinted(cuda_lib, w, c, M, torch.from_numpy(h).cuda(), w.kc)
+        assert np.array_equal(idx, idx0) and np.array_equal(nsel, nsel0), name
+        assert np.array_equal(cut.view(np.uint32), cut0.view(np.uint32)), name
+        assert np.abs(out - want).max() <= ATOL, name
+
+
+def test_retrieval_draft_cut_hint_at_exact_ties(cuda_lib):
+    """Scores on 64 levels (hundreds of exact ties per level): a bound equal to
+    the cut level admits the whole tied level, and the ties at the cut still go
+    to the lower chunk ids."""
+    C = 16384
+    w = small_workload(B=1, Hq=2, Hkv=2, L=8 * C, ragged=False)
+    c = make_case(w)
+    rng = np.random.default_rng(4)
+    M_bits = _level_means(w, C, rng.integers(0, 64, (w.B, w.Hkv, C)).astype(np.float32), 4)
+    M = torch.from_numpy(M_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    idx0, nsel0, cut0, out0 = run_fused(cuda_lib, w, c, M, kc=512)
+    scores = O.chunk_scores(bits(c["q_cpu"]), M_bits, c["seq_cpu"].numpy(), w.L, 8, w.Hkv)
+    for h in (cut0, np.nextafter(cut0, np.float32(-np.inf))):
+        idx, nsel, cut, out = _hinted(cuda_lib, w, c, M, torch.from_numpy(h.astype(np.float32)).cuda(), 512)
+        assert np.array_equal(idx, idx0) and np.array_equal(cut.view(np.uint32), cut0.view(np.uint32))
+        for g in range(w.Hkv):
+            assert np.array_equal(idx[0, g, :512], _exact_topk(scores[0][g], 512)), g
+        assert np.abs(out - out0).max() <= ATOL
+
+
+def test_retrieval_draft_cut_hint_one_cta_over_its_list(cuda_lib):
+    """2500 chunks reach the bound, all in the first slice of the cluster:
+    within the 4096 the cluster may gather, but more than one CTA may list,
+    so the unhinted path runs; the selection is unchanged."""
+    C = 40000
+    w = small_workload(B=1, Hq=1, Hkv=1, L=8 * C, ragged=False)
+    c = make_case(w)
+    levels = np.zeros((1, 1, C), dtype=np.float32)
+    levels[0, 0, :2500] = 50.0
+    levels[0, 0, 100:400] = 60.0
+    qs = O.bf16_to_f64(bits(c["q_cpu"])).reshape(1, 1, -1, 128).sum(axis=2)[..., 0]
+    levels = np.where(qs[..., None] > 0, levels, -levels)
+    M_bits = _level_means(w, C, levels, 0)
+    M = torch.from_numpy(M_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    idx0, nsel0, cut0, out0 = run_fused(cuda_lib, w, c, M, kc=512)
+    scores = O.chunk_scores(bits(c["q_cpu"]), M_bits, c["seq_cpu"].numpy(), w.L, 8, w.Hkv)
+    assert np.array_equal(idx0[0, 0, :512], _exact_topk(scores[0][0], 512))
+    bound = np.float32(np.sort(np.asarray(scores[0][0], dtype=np.float32))[::-1][2499])
+    idx, nsel, cut, out = _hinted(cuda_lib, w, c, M, torch.full((1, 1), float(bound)).cuda(), 512)
+    assert np.array_equal(idx, idx0) and np.array_equal(cut.view(np.uint32), cut0.view(np.uint32))
+    assert np.abs(out - out0).max() <= ATOL
