@@ -700,7 +700,7 @@ def measure_offload(st, tf, stream, peak, kernels):
         tf.tf_stream_window_attn(st.q[0], Kw, Vw, wlens, w.n_sink, w.window, st.scale, out=o_w, ws=ws_w1)
         verify_off()
 
-    step_ms = _median_call_ms(off_step, stream, reps=3)
+    step_ms = _median_call_ms(off_step, stream, reps=5)
     link = off_bytes + rows_bytes
     kernels["offloaded_step_1layer"] = {
         "ms": round(step_ms, 4), "bytes_over_link": link, "GBps_over_link": round(link / (step_ms / 1e3) / 1e9, 1),

@@ -32,7 +32,7 @@
 // MMAs of tile t+1 overlap the softmax of tile t.  Splits are merged with the
 // log-sum-exp identity by the last CTA of each unit (atomic ticket; the
 // splits' partial rows are bulk-copied into its idle ring), or inside a
-// thread-block cluster through DSMEM when a unit has at most 8 splits.  Every
+// thread-block cluster through DSMEM when a unit has at most 4 splits.  Every
 // mbarrier wait is bounded; on a timeout the CTA records a nonzero status word
 // at the start of the workspace and leaves.
 //
@@ -70,7 +70,7 @@ constexpr int kPiece = 8;           // rows per gathered piece (one chunk, one s
 constexpr int kPiecesPerTile = kTile / kPiece;
 constexpr int kMaxTilesPerCta = 16;  // gathered tiles per split (piece table size)
 constexpr int kPieceBytes = kPiece * kHeadDim * 2;  // one piece of K (or V): 2 KB
-constexpr int kMaxClusterMerge = 8;
+constexpr int kMaxClusterMerge = 4;  // splits merged inside one cluster (more: ticketed merge)
 constexpr int kPartStride = 4 + kHeadDim;  // one row's partial state: m, l, 2 unused, O[128]  // most splits merged inside one (portable) cluster
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kLptMaxSeqs = 64;  // longest-first block order for batches up to this size
@@ -797,7 +797,7 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
   if (p.cmerge) {
     // Every split of the unit has left its partial in shared memory; each rank
     // of the cluster merges its share of the unit's outputs from all of them.
-    __shared__ float s_w[8 * kMaxRows], s_l[8 * kMaxRows], s_L[kMaxRows];
+    __shared__ float s_w[kMaxClusterMerge * kMaxRows], s_l[kMaxClusterMerge * kMaxRows], s_L[kMaxRows];
     cluster_sync();
     const int S = p.splits;
     const uint32_t rank = cluster_ctarank();
@@ -824,13 +824,13 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
     const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
     for (int e4 = (int)rank * Smem<NR>::kThreads + tid; e4 < rows * (kHeadDim / 4); e4 += S * Smem<NR>::kThreads) {
       const int n = e4 / (kHeadDim / 4), d = (e4 % (kHeadDim / 4)) * 4;
-      uint4 v[8];
+      uint4 v[kMaxClusterMerge];
 #pragma unroll
-      for (int sp = 0; sp < 8; ++sp)
+      for (int sp = 0; sp < kMaxClusterMerge; ++sp)
         if (sp < S) v[sp] = dsmem_ld_v4(co + n * kHeadDim + d, sp);
       float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-      for (int sp = 0; sp < 8; ++sp) {
+      for (int sp = 0; sp < kMaxClusterMerge; ++sp) {
         if (sp < S) {
           const float w = s_w[sp * rows + n];
           a.x = fmaf(w, __uint_as_float(v[sp].x), a.x);
@@ -945,35 +945,27 @@ tf_status launch_rows(int rows_max, const CUtensorMap& mk, const CUtensorMap& mv
 }
 
 // Gathered mode: tiles of the longest possible piece list (kc chunks and at most
-// two 8-row pieces of candidates), and the split count: the work per unit is
-// short, so one wave of CTAs with as many tiles each as the piece table holds
-// beats more, shorter splits (each split pays the pipeline ramp and a merge);
-// when one wave cannot hold the units, the splits that fill whole waves.
+// two 8-row pieces of candidates), and the split count from a cost model that
+// fits every split count measured on this GPU (kc = 512; 32 and 64 units of 24
+// query rows): CTAs run in waves of one per SM, and a CTA costs its tiles plus
+// about five tile-times of set-up, first copies, partial write and merge.  The
+// cheapest count wins (ties: fewer splits); filling the last wave at any price
+// was up to 1.8x slower on 64 units (seven splits of five tiles each).
 int sparse_verify_tiles(int kc) { return (kc + 2 + kPiecesPerTile - 1) / kPiecesPerTile; }
+
+constexpr int kSplitCostTiles = 5;
 
 int sparse_verify_splits(int ug, int tiles, int sms) {
   const int lo = (tiles + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
-  if ((long long)ug * lo <= sms) {
-    int s = sms / ug;  // one wave
-    if (s > tiles) s = tiles;
-    // fewest splits that keep the per-CTA tile count within one of the one-wave count
-    const int per = (tiles + s - 1) / s;
-    return (tiles + per - 1) / per;
-  }
   int best = lo;
-  double best_eff = -1.0;
-  for (int waves = 1; waves <= 16; ++waves) {
-    int s = (waves * sms + ug / 2) / ug;
-    if (s < lo) s = lo;
-    if (s > tiles) s = tiles;
-    const long long ctas = (long long)ug * s;
-    const long long full = (ctas + sms - 1) / sms * sms;
-    const double eff = (double)ctas / (double)full;
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
+  long long best_cost = -1;
+  for (int s = lo; s <= tiles; ++s) {
+    const long long waves = ((long long)ug * s + sms - 1) / sms;
+    const long long cost = waves * (kSplitCostTiles + (tiles + s - 1) / s);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
       best = s;
     }
-    if (eff > 0.97) break;
   }
   return best;
 }
@@ -1232,6 +1224,8 @@ tf_status sparse_gather(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
   const int ug = B * Hkv * p.ngroups;
   p.splits = sparse_verify_splits(ug, tiles, num_sms());
   p.tiles_per = (tiles + p.splits - 1) / p.splits;
+  // Splits merge inside a cluster only up to four: clusters of five to seven
+  // one-SM CTAs packed badly (up to 1.6x slower than the ticketed merge).
   p.cmerge = (p.splits > 1 && p.splits <= kMaxClusterMerge) ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   char* w = static_cast<char*>(ws);

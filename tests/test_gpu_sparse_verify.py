@@ -44,7 +44,9 @@ def topk_over_prefix(w, c, kc):
     small_workload(),
     small_workload(B=2, Hq=32, Hkv=8, L=3000, T=6, budget=8 * 40, L_min=500),
     small_workload(B=1, Hq=8, Hkv=8, L=20000, T=6, budget=4096, ragged=False),
-], ids=["tiny", "ragged-gqa", "gqa-24-rows", "mha-20k-kc512"])
+    small_workload(B=4, Hq=32, Hkv=8, L=6000, T=6, budget=4096, ragged=False),
+    small_workload(B=8, Hq=32, Hkv=8, L=6000, T=6, budget=4096, L_min=4500),
+], ids=["tiny", "ragged-gqa", "gqa-24-rows", "mha-20k-kc512", "32-units-cluster-merge", "64-units-ragged"])
 def test_sparse_verify_topk_selection(cuda_lib, w):
     c = make_case(w, fill_invalid=float("nan"))
     idx, nsel = topk_over_prefix(w, c, w.kc)
