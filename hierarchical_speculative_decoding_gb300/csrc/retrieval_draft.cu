@@ -92,6 +92,8 @@ struct DraftParams {
   float* s_cut;      // [B, Hkv] or null
   float* out;        // [B, Hq, 128]
   const float* hint;  // [B, Hkv] lower bounds on the cut scores, or null (NaN: none for that unit)
+  int nseq;           // B
+  int longest_first;  // 1: block row r serves the sequence with the r-th longest context (B <= 64)
 };
 
 size_t draft_smem(int slice) { return (size_t)kOffKeys + (size_t)slice * sizeof(uint32_t); }
@@ -128,8 +130,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
 
   const int S = (int)gridDim.x;  // the cluster spans grid x
   const uint32_t rank = cluster_ctarank();
-  const int unit = blockIdx.y;
-  const int b = unit / p.Hkv, g = unit % p.Hkv;
+  const int g = (int)blockIdx.y % p.Hkv;
   const int G = p.Hq / p.Hkv;  // <= NQ
   const int Cmax = (p.Lmax + kChunk - 1) / kChunk;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -148,6 +149,26 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
   }
   topk::zero_hists(a);
   pdl_wait();
+  // Ragged batches: clusters start in about block order, so block row r takes
+  // the sequence with the r-th longest context (ties in batch order; every
+  // warp ranks the at most 64 lengths with shuffles and one ballot) and the
+  // longest units do not start in the last wave.
+  int b = (int)blockIdx.y / p.Hkv;
+  if (p.longest_first) {
+    const int slot = b;
+    const int l0 = lane < p.nseq ? clamp_len(p.seq_lens[lane], p.Lmax) : -1;
+    const int l1 = lane + 32 < p.nseq ? clamp_len(p.seq_lens[lane + 32], p.Lmax) : -1;
+    int r0 = 0, r1 = 0;
+    for (int j = 0; j < p.nseq; ++j) {
+      const int lj = __shfl_sync(0xffffffffu, j < 32 ? l0 : l1, j & 31);
+      r0 += (lj > l0 || (lj == l0 && j < lane)) ? 1 : 0;
+      r1 += (lj > l1 || (lj == l1 && j < lane + 32)) ? 1 : 0;
+    }
+    const unsigned m0 = __ballot_sync(0xffffffffu, lane < p.nseq && r0 == slot);
+    const unsigned m1 = __ballot_sync(0xffffffffu, lane + 32 < p.nseq && r1 == slot);
+    b = m0 ? __ffs(m0) - 1 : 32 + __ffs(m1) - 1;
+  }
+  const int unit = b * p.Hkv + g;
   const int L = clamp_len(p.seq_lens[b], p.Lmax);
   const int C = (L + kChunk - 1) / kChunk;
   const int per = (C + S - 1) / S;
@@ -610,7 +631,8 @@ tf_status draft_entry(const uint16_t* q, const uint16_t* M, const uint16_t* K, c
   const int units = B * Hkv;
   if (units > 65535) return TF_ERR_UNSUPPORTED;
   const int Cmax = (Lmax + kChunk - 1) / kChunk;
-  DraftParams p{q, M, K, V, seq_lens, Hq, Hkv, Lmax, kc, scale * kLog2e, idx, n_sel, s_cut, out, hint};
+  DraftParams p{q, M, K, V, seq_lens, Hq, Hkv, Lmax, kc, scale * kLog2e, idx, n_sel, s_cut, out, hint,
+                B, (B > 1 && B <= 64) ? 1 : 0};
   const int G = Hq / Hkv;
   switch (G) {
     case 1: return launch_draft<1>(p, units, Cmax < 1 ? 1 : Cmax, stream);
