@@ -7,6 +7,10 @@ calls), sink + window attention (Force 1), full-cache verification of
 gamma+1 = 6 queries (Force 3).
 Workload: the full 32-layer Llama2-7B-128K KV cache (32 heads x 128 dims x
 131072 tokens, bf16, 64 GiB), seeded synthetic data with 1% planted chunks.
+Consecutive steps take different seeded queries (four sets per layer, cycled),
+and the retrieval drafter gets 0.7 x the previous step's cut of each layer as
+a lower bound on this step's cut (it changes only the time); "cold_start" is
+the same step without the bound.
 After it, in the same run, the same step on the GQA batch (Llama-3-8B style,
 batch 4, 32/8 heads, 128K, 32 layers) and on the mixed batch (batch 8,
 contexts 16K..128K, 32/8 heads, 16 layers), each reported under "workloads".
