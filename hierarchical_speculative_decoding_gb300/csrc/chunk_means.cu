@@ -13,7 +13,9 @@
 // flight while it sums the current one (the exact sums cost ~600 instructions
 // per 128 bytes, so without the overlap the stream waits on the arithmetic).
 // The sum of the rows is carried as an unevaluated fp32 pair (TwoSum), so the
-// mean is exact before its single rounding to bf16.
+// mean is exact before its single rounding to bf16.  Columns whose pair is not
+// finite (infinities or NaNs among the keys, or sums beyond the fp32 range)
+// are redone after the stream with the inputs scaled by 1/8 first.
 #include "tf_common.cuh"
 
 namespace tf {
@@ -94,9 +96,83 @@ __device__ __forceinline__ void load_rows(const Item& it, uint4 (&rows)[kChunk])
     rows[r] = (r < it.n) ? ld_stream16(it.src + (size_t)r * kHeadDim) : make_uint4(0, 0, 0, 0);
 }
 
-// Exact mean of the rows, rounded once to bf16, stored as 8 head dims.
-__device__ __forceinline__ void mean_store(const Item& it, const uint4 (&rows)[kChunk]) {
-  if (!it.ok) return;
+// Exact mean of the n rows at src (pairs of fp32 by TwoSum), rounded once to
+// bf16 and stored at dst.  Out of line and reading its rows again itself, so
+// the rare call leaves the streaming loop's code as it is.
+// Every input is first scaled by 2^-3, which is exact for every bf16 value (its
+// smallest subnormal, 2^-133, stays an fp32 subnormal), so no partial sum can
+// overflow however large the keys.  A column holding an infinity or a NaN
+// takes the IEEE sum's outcome: +-inf, or NaN (0x7fc0) for a NaN or opposite
+// infinities.
+__device__ __noinline__ void exact_means(const uint16_t* __restrict__ src, int n, uint16_t* __restrict__ dst) {
+  uint4 rows[kChunk];
+#pragma unroll
+  for (int r = 0; r < kChunk; ++r)
+    rows[r] = (r < n) ? *reinterpret_cast<const uint4*>(src + (size_t)r * kHeadDim) : make_uint4(0, 0, 0, 0);
+  uint16_t o[8];
+  float hi[8], lo[8], plain[8];
+  bool special[8];
+#pragma unroll
+  for (int d = 0; d < 8; ++d) {
+    hi[d] = 0.0f;
+    lo[d] = 0.0f;
+    plain[d] = 0.0f;
+    special[d] = false;
+  }
+#pragma unroll
+  for (int r = 0; r < kChunk; ++r) {
+    float f[8];
+    unpack8(rows[r], f);
+#pragma unroll
+    for (int d = 0; d < 8; ++d) {
+      const float x = f[d] * 0.125f;
+      special[d] |= !isfinite(f[d]);
+      plain[d] += x;
+      float s, e;
+      two_sum(hi[d], x, s, e);
+      hi[d] = s;
+      lo[d] += e;
+    }
+  }
+#pragma unroll
+  for (int d = 0; d < 8; ++d) {
+    float h = hi[d], l = lo[d];
+    float s, e;
+    two_sum(h, l, s, e);  // renormalise the pair
+    h = s;
+    l = e;
+    if (n == 0) {
+      o[d] = 0;
+    } else if (special[d]) {
+      o[d] = isnan(plain[d]) ? (uint16_t)0x7fc0u : (plain[d] > 0.0f ? (uint16_t)0x7f80u : (uint16_t)0xff80u);
+    } else if (n == kChunk) {
+      o[d] = round_pair_bf16(h, l);  // the scaled sum is the mean
+    } else {
+      // Pair divided by n / 8: quotient, exact remainder by FMA, corrected low part.
+      const float fn = (float)n * 0.125f;
+      float qh = __fdiv_rn(h, fn);
+      float rem = fmaf(-qh, fn, h);
+      float ql = __fdiv_rn(rem + l, fn);
+      float s2, e2;
+      two_sum(qh, ql, s2, e2);
+      o[d] = round_pair_bf16(s2, e2);
+    }
+  }
+  uint32_t packed[4];
+#pragma unroll
+  for (int d = 0; d < 8; d += 2) packed[d / 2] = (uint32_t)o[d] | ((uint32_t)o[d + 1] << 16);
+  *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
+// Exact mean of the rows, rounded once to bf16, stored as 8 head dims: the sum
+// of the rows carried as an unevaluated fp32 pair (TwoSum), renormalised,
+// scaled by 1/8 (or divided by the row count of a partial chunk) and rounded
+// once.  A column whose pair is not finite -- an infinity or NaN among the
+// keys, or partial sums beyond the fp32 range -- returns false; the item is
+// redone after the stream with inputs scaled by 1/8 first and IEEE results
+// for infinities and NaNs.
+__device__ __forceinline__ bool mean_store(const Item& it, const uint4 (&rows)[kChunk]) {
+  if (!it.ok) return true;
   float hi[8], lo[8];
 #pragma unroll
   for (int d = 0; d < 8; ++d) {
@@ -116,36 +192,57 @@ __device__ __forceinline__ void mean_store(const Item& it, const uint4 (&rows)[k
     }
   }
   const int n = it.n;
+  uint16_t o[8];
+  bool finite = true;
+#pragma unroll
+  for (int d = 0; d < 8; ++d) {
+    float h = hi[d], l = lo[d];
+    float s, e;
+    two_sum(h, l, s, e);  // renormalise the pair
+    h = s;
+    l = e;
+    finite &= isfinite(h) && isfinite(l);
+    if (n == 0) {
+      o[d] = 0;
+    } else if (n == kChunk) {
+      o[d] = round_pair_bf16(h * 0.125f, l * 0.125f);  // exact scaling by 2^-3
+    } else {
+      // Pair divided by n: quotient, exact remainder by FMA, corrected low part.
+      const float fn = (float)n;
+      float qh = __fdiv_rn(h, fn);
+      float rem = fmaf(-qh, fn, h);
+      float ql = __fdiv_rn(rem + l, fn);
+      float s2, e2;
+      two_sum(qh, ql, s2, e2);
+      o[d] = round_pair_bf16(s2, e2);
+    }
+  }
+  if (!finite) return false;  // redone after the stream
   uint32_t packed[4];
 #pragma unroll
-  for (int d = 0; d < 8; d += 2) {
-    uint16_t o[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      float h = hi[d + k], l = lo[d + k];
-      float s, e;
-      two_sum(h, l, s, e);  // renormalise the pair
-      h = s;
-      l = e;
-      if (n == 0) {
-        o[k] = 0;
-      } else if (n == kChunk) {
-        o[k] = round_pair_bf16(h * 0.125f, l * 0.125f);  // exact scaling by 2^-3
-      } else {
-        // Pair divided by n: quotient, exact remainder by FMA, corrected low part.
-        const float fn = (float)n;
-        float qh = __fdiv_rn(h, fn);
-        float rem = fmaf(-qh, fn, h);
-        float ql = __fdiv_rn(rem + l, fn);
-        float s2, e2;
-        two_sum(qh, ql, s2, e2);
-        o[k] = round_pair_bf16(s2, e2);
-      }
-    }
-    packed[d / 2] = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
-  }
+  for (int d = 0; d < 8; d += 2) packed[d / 2] = (uint32_t)o[d] | ((uint32_t)o[d + 1] << 16);
   *reinterpret_cast<uint4*>(it.dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  return true;
 }
+
+// Items of one thread whose means are redone exactly after its stream, by
+// their step number in the thread's walk: four slots in registers (constant
+// indices only); more than four (only keys built to sit on rounding midpoints)
+// redo the thread's whole walk.
+struct Deferred {
+  int step[4];
+  int count;
+  __device__ __forceinline__ void add(int k) {
+    switch (count) {
+      case 0: step[0] = k; break;
+      case 1: step[1] = k; break;
+      case 2: step[2] = k; break;
+      case 3: step[3] = k; break;
+      default: break;
+    }
+    ++count;
+  }
+};
 
 // Grid-stride over items, software-pipelined: the next item's eight row loads
 // are issued before the current item's sums, so the DRAM round trip overlaps
@@ -169,6 +266,10 @@ __global__ void __launch_bounds__(256) chunk_means_kernel(const uint16_t* __rest
   w.dc = (int)(step % n_chunks);
   w.dg = (int)(step / n_chunks % Hkv);
   w.db = (int)(step / n_chunks / Hkv);
+  const Walk w0 = w;
+  Deferred later;
+  later.count = 0;
+  int k = 0;  // step of the walk
   Item cur = item_at(w, K, seq_lens, Hkv, Lmax, Cmax, c_begin, M);
   uint4 rows[kChunk];
   load_rows(cur, rows);
@@ -181,11 +282,25 @@ __global__ void __launch_bounds__(256) chunk_means_kernel(const uint16_t* __rest
       nxt = item_at(w, K, seq_lens, Hkv, Lmax, Cmax, c_begin, M);
       load_rows(nxt, next_rows);
     }
-    mean_store(cur, rows);
+    if (!mean_store(cur, rows)) later.add(k);
     if (!more) break;
 #pragma unroll
     for (int r = 0; r < kChunk; ++r) rows[r] = next_rows[r];
     cur = nxt;
+    ++k;
+  }
+  if (later.count == 0) return;
+  // the deferred steps, in increasing order, by walking again
+  int j = 0;
+  w = w0;
+  for (int kk = 0; w.b < B; ++kk, advance(w, Hkv, n_chunks)) {
+    bool redo = later.count > 4;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) redo |= t < later.count && later.step[t] == kk;
+    if (!redo) continue;
+    const Item it = item_at(w, K, seq_lens, Hkv, Lmax, Cmax, c_begin, M);
+    if (it.ok && it.n > 0) exact_means(it.src, it.n, it.dst);
+    if (later.count <= 4 && ++j == later.count) break;
   }
 }
 

@@ -84,6 +84,53 @@ def test_chunk_means_bit_exact(cuda_lib, w):
     assert np.array_equal(got, want), f"{(got != want).sum()} mismatching means"
 
 
+def _bf16_bits(x):
+    return bits(torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16))
+
+
+def test_chunk_means_rounding_edge_cases(cuda_lib):
+    """Chunks whose column sums sit on a bf16 rounding midpoint, a hair off it,
+    behind heavy cancellation, so small that a rounding-error bound would
+    underflow, so large that it would overflow, or hold +-inf and NaN: the
+    exact sum must decide every one of them, bit for bit against the oracle."""
+    rng = np.random.default_rng(11)
+    C, D = 96, 128
+    rows = np.zeros((C, 8, D), dtype=np.float32)
+    for c in range(C):
+        kind = c % 8
+        for d in range(D):
+            if kind == 0:    # sum / 8 exactly a midpoint: 1 + 2^-8 (tie, to even) or 1 + 3 * 2^-8
+                v = [1.0] * 7 + [1.0 + (2 ** -5 if d % 2 else 3 * 2 ** -5)]
+            elif kind == 1:  # sum 8 + 2^-5 + e: the midpoint 1 + 2^-8 plus or minus e / 8
+                e = float(rng.choice([-1, 1])) * 2.0 ** -int(rng.integers(10, 24))
+                v = [1.0] * 5 + [1.0 + 2 ** -5, 2.0, e]
+            elif kind == 2:  # heavy cancellation around a small remainder
+                big = float(2 ** int(rng.integers(4, 12)))
+                v = [big, -big, big, -big] + list(rng.normal(0, 1e-3, 4))
+            elif kind == 3:  # tiny: subnormal means, bounds below the normal range
+                v = list(rng.normal(0, 1e-38, 8))
+            elif kind == 4:  # huge: near the top of the range
+                v = list(rng.normal(0, 1e37, 8))
+            elif kind == 5:  # infinities and NaN
+                v = list(rng.normal(0, 1, 8))
+                v[d % 8] = [np.inf, -np.inf, np.nan][d % 3]
+            elif kind == 6:  # exact zeros and signed zeros
+                v = [0.0, -0.0] * 4
+            else:            # ordinary values with widely spread exponents
+                v = list(rng.normal(0, 1, 8) * 2.0 ** rng.integers(-30, 30, 8))
+            rows[c, :, d] = np.asarray(v, dtype=np.float32)
+    Kb = _bf16_bits(rows.reshape(1, 1, C * 8, D))
+    K = torch.from_numpy(Kb.view(np.int16)).view(torch.bfloat16).cuda()
+    seq = torch.tensor([C * 8], dtype=torch.int32)
+    M = torch.full((1, 1, C, D), 7.0, dtype=torch.bfloat16, device="cuda")
+    cuda_lib.tf_build_chunk_means(K, seq.cuda(), M)
+    want = O.build_chunk_means(Kb, seq.numpy(), 8)
+    got = bits(M)
+    bad = np.argwhere(got[0, 0] != want[0, 0])
+    detail = [(int(c % 8), int(c), int(d), hex(got[0, 0, c, d]), hex(want[0, 0, c, d])) for c, d in bad[:8]]
+    assert len(bad) == 0, f"{len(bad)} mismatching means (kind, chunk, dim, got, want): {detail}"
+
+
 def test_chunk_means_subrange_only(cuda_lib):
     w = small_workload(ragged=False, B=1)
     c = make_case(w)
