@@ -3,8 +3,9 @@
 One step = for every layer, in order: chunk scores + top-k + sparse decode
 attention over the retrieved chunks (the Force 2 retrieval drafter, one fused
 launch; --two-call-draft runs it as the separate top-k and sparse-attention
-calls), sink + window attention (Force 1), full-cache verification of
-gamma+1 = 6 queries (Force 3).
+calls), then full-cache verification of gamma+1 = 6 queries (Force 3)
+with the sink + window attention of the decode queries (Force 1) computed as
+extra query rows of the same launch (tf_verify_window_attn).
 Workload: the full 32-layer Llama2-7B-128K KV cache (32 heads x 128 dims x
 131072 tokens, bf16, 64 GiB), seeded synthetic data with 1% planted chunks.
 Consecutive steps take different seeded queries (four sets per layer, cycled),
@@ -379,6 +380,11 @@ class StepState:
         self.ws_sp = tf.workspace(tf.tf_sparse_decode_attn_workspace(B, Hq, Hkv, w.kc), dev)
         self.ws_win = tf.workspace(tf.tf_stream_window_attn_workspace(B, Hq, Hkv, w.n_sink, w.window), dev)
         self.ws_ver = tf.workspace(tf.tf_verify_attn_workspace(B, Hq, Hkv, L, T), dev)
+        self.ws_vw = tf.workspace(tf.tf_verify_window_attn_workspace(B, Hq, Hkv, L, T, w.n_sink, w.window), dev)
+        G = Hq // Hkv
+        # one launch when the window rows fill padding rows of the verify kernel (the library's rule)
+        fits = (-(-G * (T + 1) // 32) == -(-G * T // 32)) and (-(-min(G * (T + 1), 32) // 8) == -(-min(G * T, 32) // 8))
+        self.vw_launches = 1 if fits else 2
         torch.cuda.synchronize()
 
     def bytes_per_launch(self):
@@ -406,7 +412,9 @@ class StepState:
             "sparse": 2 * sel_rows * row + ids + q_io,
             "draft": means + ids + 2 * sel_rows * row + q_io,
             "window": sum(2 * Hkv * min(x, w.n_sink + w.window) * row for x in lens) + q_io,
-            "verify": sum(2 * Hkv * x * row for x in lens) + B * Hq * T * D * (2 + 4),
+            "verify_only": sum(2 * Hkv * x * row for x in lens) + B * Hq * T * D * (2 + 4),
+            # the window rows read keys the verify rows read anyway: only their queries and outputs add
+            "verify": sum(2 * Hkv * x * row for x in lens) + B * Hq * T * D * (2 + 4) + q_io,
         }
 
 
@@ -418,7 +426,7 @@ def make_step(st, tf, two_call, stream, hinted=True):
     import torch
 
     w = st.w
-    kinds = ("draft", "window", "verify")
+    kinds = ("draft", "verify")  # verify: tf_verify_window_attn, the window rows inside the verify launch
     hinted = hinted and not two_call
 
     def draft(l, q=None):
@@ -443,13 +451,10 @@ def make_step(st, tf, two_call, stream, hinted=True):
             draft(l, q)
             if evs is not None:
                 evs[l][1].record(stream)
-            tf.tf_stream_window_attn(q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window, st.scale,
-                                     out=st.o_win[l], ws=st.ws_win)
+            tf.tf_verify_window_attn(Q[l], q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window, st.scale,
+                                     out=st.o_ver[l], wout=st.o_win[l], ws=st.ws_vw)
             if evs is not None:
                 evs[l][2].record(stream)
-            tf.tf_verify_attn(Q[l], st.K[l], st.V[l], st.seq, st.scale, out=st.o_ver[l], ws=st.ws_ver)
-            if evs is not None:
-                evs[l][3].record(stream)
 
     return step, draft, kinds
 
@@ -489,7 +494,7 @@ def per_kernel_times(step, layers, k_steps, kinds):
     StepCycle, so these steps too take new queries)."""
     import torch
 
-    evs = [[[_ev() for _ in range(4)] for _ in range(layers)] for _ in range(k_steps)]
+    evs = [[[_ev() for _ in range(len(kinds) + 1)] for _ in range(layers)] for _ in range(k_steps)]
     torch.cuda.synchronize()
     for s in range(k_steps):
         step(evs[s])
@@ -600,11 +605,11 @@ def measure_extra_workload(w, args, tf, synth, dev, stream, world, local, peak):
            "config": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D, "context": w.L, "layers": w.layers,
                       "ragged": bool(w.ragged), "seq_lens": st.seq_cpu.tolist(), "budget_tokens": w.budget,
                       "verify_tokens": w.T},
-           "roofline": {"bound": "hbm", "kernel": "tf_verify_attn", "achieved": ver["GBps"], "peak": peak,
+           "roofline": {"bound": "hbm", "kernel": "tf_verify_window_attn", "achieved": ver["GBps"], "peak": peak,
                         "unit": "GB/s", "frac": ver["frac_hbm"], "algorithmic_bytes": nb["verify"],
                         "traffic": recorded_traffic("verify_attn.cu", w.name)},
            "kernels": kern, "clocks": clocks,
-           "gpu_launches": steps * st.layers * (4 if args.two_call_draft else 3)}
+           "gpu_launches": steps * st.layers * ((2 if args.two_call_draft else 1) + st.vw_launches)}
     if cold is not None:
         out["cold_start"] = cold
     kern["retrieval_draft"]["traffic"] = None if args.two_call_draft else recorded_traffic("retrieval_draft.cu",
@@ -810,11 +815,31 @@ def run_gpu(args):
     win_ms = graph_loop_ms([lambda l=l: tf.tf_stream_window_attn(st.q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window,
                                                                  st.scale, out=st.o_win[l], ws=st.ws_win)
                             for l in range(layers)], stream)
-    kernels["window"]["back_to_back"] = dict(kernel_entry(nb["window"], win_ms, peak),
-                                             timing="replayed as one CUDA graph")
+    kernels["window"] = {"in_step": "no: the step computes the window rows inside the verify launch",
+                         "back_to_back": dict(kernel_entry(nb["window"], win_ms, peak),
+                                              timing="replayed as one CUDA graph")}
     kernels["window"]["floor_16rows_us"] = round(graph_loop_ms(
         [lambda l=l: tf.tf_stream_window_attn(st.q[l], st.K[l], st.V[l], st.seq, 4, 12, st.scale, out=o_w16,
                                               ws=ws_w16) for l in range(layers)], stream) * 1e3, 2)
+    # the fused call against verify alone and against the two separate calls, per layer
+    def ver_alone(l):
+        tf.tf_verify_attn(st.Q[l], st.K[l], st.V[l], st.seq, st.scale, out=st.o_ver[l], ws=st.ws_ver)
+
+    def separate(l):
+        tf.tf_stream_window_attn(st.q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window, st.scale, out=st.o_win[l],
+                                 ws=st.ws_win)
+        ver_alone(l)
+
+    def fused(l):
+        tf.tf_verify_window_attn(st.Q[l], st.q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window, st.scale,
+                                 out=st.o_ver[l], wout=st.o_win[l], ws=st.ws_vw)
+
+    kernels["verify"]["back_to_back_us"] = {
+        name: round(graph_loop_ms([lambda l=l, f=f: f(l) for l in range(layers)], stream) * 1e3, 2)
+        for name, f in (("verify_window_one_call", fused), ("verify_alone", ver_alone),
+                        ("window_then_verify", separate))}
+    kernels["verify"]["calls"] = "tf_verify_window_attn (%d launch%s)" % (st.vw_launches,
+                                                                          "" if st.vw_launches == 1 else "es")
 
     # the offloaded setting (one 128K layer; not part of the step)
     measure_offload(st, tf, stream, peak, kernels)
@@ -835,12 +860,12 @@ def run_gpu(args):
                    "queries": f"{N_QUERY_SETS} seeded query sets cycled over the steps; the retrieval drafter "
                               f"takes the previous step's cut x {HINT_SCALE} of each layer as a bound "
                               f"(cold_start: the same step without it)"},
-        "roofline": {"bound": "hbm", "kernel": "tf_verify_attn", "achieved": round(achieved, 1), "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": "tf_verify_window_attn", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": nb["verify"], "peak_source": peak_kind},
         "kernels": kernels,
         "kernel_timing": f"CUDA events around every launch, {k_steps} further steps after the timed region",
-        "gpu_launches": args.steps * layers * (4 if args.two_call_draft else 3),
+        "gpu_launches": args.steps * layers * ((2 if args.two_call_draft else 1) + st.vw_launches),
         "clocks": clocks,
     }
 

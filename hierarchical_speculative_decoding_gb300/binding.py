@@ -35,6 +35,8 @@ _SIGS = {
     "tf_sparse_decode_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_sparse_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
     "tf_retrieval_draft_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
+    "tf_verify_window_attn_workspace": (_S, [_I, _I, _I, _I, _I, _I, _I]),
+    "tf_verify_window_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
     "tf_retrieval_draft_attn_hinted": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P,
                                             _P]),
     "tf_stream_window_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
@@ -393,6 +395,36 @@ def tf_verify_attn(Q, K, V, seq_lens, scale, out=None, ws=None, stream=None):
     _check(load().tf_verify_attn(_ptr(Q), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax, D, T, float(scale),
                                  _ptr(out), _ptr(ws), nbytes, _stream(stream)), "tf_verify_attn")
     return out
+
+
+def tf_verify_window_attn_workspace(B, Hq, Hkv, Lmax, T, n_sink, window):
+    return int(load().tf_verify_window_attn_workspace(B, Hq, Hkv, Lmax, T, n_sink, window))
+
+
+def tf_verify_window_attn(Q, q, K, V, seq_lens, n_sink, window, scale, out=None, wout=None, ws=None, stream=None):
+    """Verify attention of Q and the sink + window attention of the decode queries q
+    in one call (one launch when the window rows fit the verify row groups).
+    Returns (out [B, Hq, T, D], wout [B, Hq, D])."""
+    _need(Q, torch.bfloat16, "Q", 4)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(K, torch.bfloat16, "K", 4)
+    _need(V, torch.bfloat16, "V", 4)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, Hq, T, D = Q.shape
+    _, Hkv, Lmax, _ = K.shape
+    if tuple(q.shape) != (B, Hq, D):
+        raise ValueError(f"q must be [B, Hq, D] = {(B, Hq, D)}, got {tuple(q.shape)}")
+    if out is None:
+        out = torch.empty((B, Hq, T, D), dtype=torch.float32, device=Q.device)
+    if wout is None:
+        wout = torch.empty((B, Hq, D), dtype=torch.float32, device=Q.device)
+    _need(out, torch.float32, "out", 4)
+    _need(wout, torch.float32, "wout", 3)
+    ws, nbytes = _ws(ws, tf_verify_window_attn_workspace(B, Hq, Hkv, Lmax, T, n_sink, window), Q.device)
+    _check(load().tf_verify_window_attn(_ptr(Q), _ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax, D, T,
+                                        int(n_sink), int(window), float(scale), _ptr(out), _ptr(wout), _ptr(ws),
+                                        nbytes, _stream(stream)), "tf_verify_window_attn")
+    return out, wout
 
 
 def tf_verify_attn_tree(Q, K, V, seq_lens, parent, scale, out=None, ws=None, stream=None):

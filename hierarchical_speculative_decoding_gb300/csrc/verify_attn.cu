@@ -103,6 +103,13 @@ struct VerifyParams {
   // contiguous mode: 1 = block row r serves the sequence with the r-th
   // longest context (nseq <= kLptMaxSeqs), 0 = batch order
   int nseq, longest_first;
+  // contiguous chain mode, optional: the decode queries [B, Hq, 128] of the
+  // streaming drafter's window attention, computed as G extra rows per KV
+  // head after the G * T verify rows (keys [0, min(n_sink, L)) and
+  // [max(n_sink, L - window), L)), written to wout [B, Hq, 128]
+  const uint16_t* wq;
+  float* wout;
+  int n_sink, window;
 };
 
 // Final log-sum-exp merge of a unit's split partials by the CTA that finished
@@ -115,7 +122,7 @@ struct VerifyParams {
 template <int kThreads>
 __device__ void merge_staged(const float* __restrict__ ml, const float* __restrict__ o, int S, int rows,
                              uint8_t* ring, uint64_t* bar, float* __restrict__ out, float* __restrict__ part,
-                             int* status) {
+                             int* status, float* __restrict__ wout = nullptr, int nvl = kMaxRows) {
   constexpr int kRing = kStages * kStageBytes;
   constexpr int kAcc = (kMaxRows * kHeadDim / 4 + kThreads - 1) / kThreads;  // float4 outputs per thread
   const int tid = threadIdx.x;
@@ -212,11 +219,12 @@ __device__ void merge_staged(const float* __restrict__ ml, const float* __restri
   for (int k = 0; k < kAcc; ++k) {
     const int e4 = tid + k * kThreads;
     if (e4 < n4) {
-      const int n = e4 / (kHeadDim / 4);
+      const int n = e4 / (kHeadDim / 4), d4 = e4 % (kHeadDim / 4);
       const float Lr = L_s[n];
       const float inv = Lr > 0.0f ? 1.0f / Lr : 0.0f;
-      reinterpret_cast<float4*>(out)[e4] =
-          make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
+      // rows [0, nvl) are contiguous verify rows at out, the rest window rows at wout
+      float* dst = n < nvl ? out + (size_t)n * kHeadDim : wout + (size_t)(n - nvl) * kHeadDim;
+      reinterpret_cast<float4*>(dst)[d4] = make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
     }
   }
 }
@@ -274,7 +282,9 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kSoftmaxThreads) : "memory");
 }
 
-template <int NR, bool GATHER, bool TREE = false>
+// WIN: the G window rows of p.wq follow the G * T verify rows (contiguous
+// chain mode only).
+template <int NR, bool GATHER, bool TREE = false, bool WIN = false>
 __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(const __grid_constant__ CUtensorMap mapK,
                                                                   const __grid_constant__ CUtensorMap mapV,
                                                                   VerifyParams p) {
@@ -300,7 +310,8 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
   const int grp = ug % p.ngroups, g = (ug / p.ngroups) % p.Hkv;
   const int seq_slot = ug / (p.ngroups * p.Hkv);
   const int G = p.Hq / p.Hkv;
-  const int rows_all = G * p.T;
+  const int nv = G * p.T;                          // verify rows per KV head
+  const int rows_all = nv + (WIN ? G : 0);         // + the window rows
   const int row0 = grp * kMaxRows;
   const int rows = min(kMaxRows, rows_all - row0);
 
@@ -350,6 +361,14 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
   }
   const int unit = b * p.Hkv + g;
   const int L = clamp_len(p.seq_lens[b], p.Ltot);
+  // outputs: rows [0, nvl) of this group are verify rows (contiguous from
+  // out_row0 in out), the rest window rows (contiguous from wrow0 in wout)
+  const int nvl = WIN ? min(max(nv - row0, 0), rows) : rows;
+  const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
+  const size_t wrow0 = (size_t)b * p.Hq + (size_t)g * G + (size_t)max(row0 + nvl - nv, 0);
+  auto out_row = [&](int n) -> float* {
+    return (!WIN || n < nvl) ? p.out + (out_row0 + n) * kHeadDim : p.wout + (wrow0 + (n - nvl)) * kHeadDim;
+  };
 
   // key range of this split: whole tiles (contiguous), or tiles of the piece
   // list (gathered: selected chunks, then the candidate rows)
@@ -404,11 +423,14 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
   }
   // Q rows of this group -> shared memory, [kNS x 128] bf16 in two swizzled halves.
   {
-    const uint16_t* Qg = p.Q + (((size_t)b * p.Hq + (size_t)g * G) * p.T + row0) * kHeadDim;
     for (int e = tid; e < S::kNS * 16; e += S::kThreads) {
       const int r = e >> 4, c8 = (e & 15) * 8;
       uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < rows) v = *reinterpret_cast<const uint4*>(Qg + (size_t)r * kHeadDim + c8);
+      if (r < rows) {
+        const uint16_t* src =
+            (!WIN || r < nvl) ? p.Q + (out_row0 + r) * kHeadDim : p.wq + (wrow0 + (r - nvl)) * kHeadDim;
+        v = *reinterpret_cast<const uint4*>(src + c8);
+      }
       const uint32_t off = (c8 >> 6) * (S::kNS * 128) + sw128_offset(r, c8 & 63);
       *reinterpret_cast<uint4*>(sQ + off) = v;
     }
@@ -562,6 +584,20 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
       acc[j] = 0.0f;
       if (!TREE) lim[j] = (nb + j < rows) ? (L - p.T + ((row0 + nb + j) % p.T)) : -1;
     }
+    // window rows of this warpgroup (bit j: row nb + j) and their two key ranges
+    uint32_t wrows = 0;
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if (WIN && nb + j >= nvl && nb + j < rows) wrows |= 1u << j;
+    const int w_sink = min(p.n_sink, L), w_from = max(p.n_sink, L - p.window);
+    // A warpgroup without verify rows (window rows, padding) has P = 0 in
+    // every tile that holds no window key: it skips their scores and O.
+    auto skip_tile = [&](int t) -> bool {
+      if (nb >= rows) return true;
+      if (!WIN || nb < nvl) return false;
+      const int lo = p.pos0 + k0 + t * kTile;  // contiguous mode: window rows exist only there
+      return lo >= w_sink && lo + kTile <= w_from;
+    };
     const uint32_t all_rows = rows >= 32 ? 0xffffffffu : ((1u << rows) - 1u);
     const int cbase = L - p.T;  // position of candidate 0
     // Every wait is followed by a vote over the warpgroup so that a timeout
@@ -577,8 +613,11 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
           break;
         }
         tc_fence_after();
-        tmem_ld8(tmem + (t & 1) * 32 + lane_off + nb, sc);
-        tmem_ld_wait();
+        const bool skip = skip_tile(t);  // uniform over the warpgroup
+        if (!skip) {
+          tmem_ld8(tmem + (t & 1) * 32 + lane_off + nb, sc);
+          tmem_ld_wait();
+        }
         // this key's position and whether it may be seen at all; a candidate
         // key (position >= L - T) only by the rows whose candidate extends it
         int pos;
@@ -597,45 +636,53 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
           key_ok = st >= 0 && pos < L && (chain ? pos >= cstart : pos < cstart);
           zero_v = !key_ok;  // rows of empty pieces, past L, or counted elsewhere
         }
-        uint32_t vis = 0;
-        if (TREE) {
-          const int ci = pos - cbase;
-          vis = !key_ok ? 0u : (chain && ci >= 0) ? s_vis[ci < 16 ? ci : 15] : all_rows;
-          vis >>= nb;
-        }
-        bool need = false;
+        if (skip) {
 #pragma unroll
-        for (int j = 0; j < R; ++j) {
-          const bool valid = TREE ? ((vis >> j) & 1u) != 0u : (key_ok && (!chain || pos <= lim[TREE ? 0 : j]));
-          sc[j] = valid ? sc[j] * p.scale_log2 : -INFINITY;
-          need |= sc[j] > m_run[j] + kRescaleThreshold;
-        }
-        need = named_bar_or(bar_id, need);
-        if (need) {
-          // tile max per row, then a new reference max for every row that grew
+          for (int j = 0; j < R; ++j) sc[j] = 0.0f;
+          if (my == 0) rescaled_s[wg][t & 1] = 0;
+        } else {
+          uint32_t vis = 0;
+          if (TREE) {
+            const int ci = pos - cbase;
+            vis = !key_ok ? 0u : (chain && ci >= 0) ? s_vis[ci < 16 ? ci : 15] : all_rows;
+            vis >>= nb;
+          }
+          bool need = false;
 #pragma unroll
           for (int j = 0; j < R; ++j) {
-            float v = sc[j];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0) red[q4][nb + j] = v;
+            const bool seen = (WIN && ((wrows >> j) & 1u)) ? (pos < w_sink || pos >= w_from)
+                                                            : (!chain || pos <= lim[TREE ? 0 : j]);
+            const bool valid = TREE ? ((vis >> j) & 1u) != 0u : (key_ok && seen);
+            sc[j] = valid ? sc[j] * p.scale_log2 : -INFINITY;
+            need |= sc[j] > m_run[j] + kRescaleThreshold;
           }
-          named_bar_sync(bar_id);
+          need = named_bar_or(bar_id, need);
+          if (need) {
+            // tile max per row, then a new reference max for every row that grew
 #pragma unroll
-          for (int j = 0; j < R; ++j) {
-            const int n = nb + j;
-            const float tmax = fmaxf(fmaxf(red[0][n], red[1][n]), fmaxf(red[2][n], red[3][n]));
-            const float mn = fmaxf(m_run[j], tmax);
-            const float a = merge_scale(m_run[j], mn);
-            l_part[j] *= a;
-            if (my == 0) alpha_s[t & 1][n] = a;
-            m_run[j] = mn;
+            for (int j = 0; j < R; ++j) {
+              float v = sc[j];
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+              if (lane == 0) red[q4][nb + j] = v;
+            }
+            named_bar_sync(bar_id);
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+              const int n = nb + j;
+              const float tmax = fmaxf(fmaxf(red[0][n], red[1][n]), fmaxf(red[2][n], red[3][n]));
+              const float mn = fmaxf(m_run[j], tmax);
+              const float a = merge_scale(m_run[j], mn);
+              l_part[j] *= a;
+              if (my == 0) alpha_s[t & 1][n] = a;
+              m_run[j] = mn;
+            }
+            named_bar_sync(bar_id);  // red[] is reused by the next rescale
           }
-          named_bar_sync(bar_id);  // red[] is reused by the next rescale
+          if (my == 0) rescaled_s[wg][t & 1] = need ? 1 : 0;
+#pragma unroll
+          for (int j = 0; j < R; ++j) sc[j] = (sc[j] == -INFINITY) ? 0.0f : exp2f(sc[j] - m_run[j]);
         }
-        if (my == 0) rescaled_s[wg][t & 1] = need ? 1 : 0;
-#pragma unroll
-        for (int j = 0; j < R; ++j) sc[j] = (sc[j] == -INFINITY) ? 0.0f : exp2f(sc[j] - m_run[j]);
       }
       if (t < ntiles) {
         // P for this tile as hi + lo bf16 parts (P V error ~2^-17 instead of
@@ -702,14 +749,16 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
           break;
         }
         tc_fence_after();
-        float ov[R], ol[R];
-        const uint32_t o_col = tmem + 64 + (u & 1) * S::kNPV + lane_off + nb;
-        tmem_ld8(o_col, ov);
-        tmem_ld8(o_col + S::kLoCol, ol);
-        tmem_ld_wait();
-        const bool resc = rescaled_s[wg][u & 1] != 0;
+        if (!skip_tile(u)) {  // a skipped tile added P V = 0 to these rows
+          float ov[R], ol[R];
+          const uint32_t o_col = tmem + 64 + (u & 1) * S::kNPV + lane_off + nb;
+          tmem_ld8(o_col, ov);
+          tmem_ld8(o_col + S::kLoCol, ol);
+          tmem_ld_wait();
+          const bool resc = rescaled_s[wg][u & 1] != 0;
 #pragma unroll
-        for (int j = 0; j < R; ++j) acc[j] = (resc ? acc[j] * alpha_s[u & 1][nb + j] : acc[j]) + (ov[j] + ol[j]);
+          for (int j = 0; j < R; ++j) acc[j] = (resc ? acc[j] * alpha_s[u & 1][nb + j] : acc[j]) + (ov[j] + ol[j]);
+        }
         tc_fence_before();
         mbar_arrive(&bar_o_free[u & 1]);
       }
@@ -724,7 +773,6 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
       if (lane == 0) red[q4][nb + j] = v;
     }
     named_bar_sync(bar_id);
-    const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
     auto row_sum = [&](int n) { return (red[0][n] + red[1][n]) + (red[2][n] + red[3][n]); };
     if (p.splits == 1 && p.part_out) {
 #pragma unroll
@@ -745,7 +793,7 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
         const int n = nb + j;
         if (n < rows) {
           const float l = row_sum(n);
-          p.out[(out_row0 + n) * kHeadDim + my] = (l > 0.0f) ? acc[j] / l : 0.0f;
+          out_row(n)[my] = (l > 0.0f) ? acc[j] / l : 0.0f;
         }
       }
     } else if (p.cmerge) {
@@ -821,7 +869,6 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
       s_L[n] = Lsum;
     }
     __syncthreads();
-    const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
     for (int e4 = (int)rank * Smem<NR>::kThreads + tid; e4 < rows * (kHeadDim / 4); e4 += S * Smem<NR>::kThreads) {
       const int n = e4 / (kHeadDim / 4), d = (e4 % (kHeadDim / 4)) * 4;
       uint4 v[kMaxClusterMerge];
@@ -845,7 +892,7 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
       a.y *= inv;
       a.z *= inv;
       a.w *= inv;
-      *reinterpret_cast<float4*>(p.out + (out_row0 + n) * kHeadDim + d) = a;
+      *reinterpret_cast<float4*>(out_row(n) + d) = a;
     }
     cluster_sync();  // peers keep their shared memory until every rank has read it
     return;
@@ -859,9 +906,9 @@ __global__ void __launch_bounds__(Smem<NR>::kThreads, 1) verify_umma_kernel(cons
   __threadfence();
   const float* ml0 = p.part_ml + (size_t)ug * p.splits_cap * kMaxRows * 2;
   const float* o0 = p.part_o + (size_t)ug * p.splits_cap * kMaxRows * kHeadDim;
-  const size_t out_row0 = ((size_t)b * p.Hq + (size_t)g * G) * p.T + row0;
   merge_staged<Smem<NR>::kThreads>(ml0, o0, p.splits, rows, smem, &bar_merge, p.out + out_row0 * kHeadDim,
-               p.part_out ? p.part_out + out_row0 * kPartStride : nullptr, p.status);
+               p.part_out ? p.part_out + out_row0 * kPartStride : nullptr, p.status,
+               WIN ? p.wout + wrow0 * kHeadDim : nullptr, nvl);
   if (tid == 0) p.tickets[ug] = 0;
 }
 
@@ -904,13 +951,13 @@ size_t verify_ws(int units, int rows_all, int Lmax) {
          ug * cap * kMaxRows * kHeadDim * sizeof(float);
 }
 
-template <int NR, bool GATHER, bool TREE>
+template <int NR, bool GATHER, bool TREE, bool WIN>
 tf_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParams& p, dim3 grid,
                  cudaStream_t stream) {
   static DeviceCache configured;
   if (!configured.get([] {
-        return cudaFuncSetAttribute(verify_umma_kernel<NR, GATHER, TREE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Smem<NR>::kDynamic) == cudaSuccess;
+        return cudaFuncSetAttribute(verify_umma_kernel<NR, GATHER, TREE, WIN>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<NR>::kDynamic) == cudaSuccess;
       }))
     return TF_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -927,20 +974,20 @@ tf_status launch(const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParam
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.cmerge ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, verify_umma_kernel<NR, GATHER, TREE>, mk, mv, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, verify_umma_kernel<NR, GATHER, TREE, WIN>, mk, mv, p) != cudaSuccess)
     return TF_ERR_CUDA;
   return launch_status();
 }
 
 // The softmax works on the group's query rows rounded up to 8.
-template <bool GATHER, bool TREE = false>
+template <bool GATHER, bool TREE = false, bool WIN = false>
 tf_status launch_rows(int rows_max, const CUtensorMap& mk, const CUtensorMap& mv, const VerifyParams& p, dim3 grid,
                       cudaStream_t stream) {
   switch ((rows_max + 7) >> 3) {
-    case 1: return launch<8, GATHER, TREE>(mk, mv, p, grid, stream);
-    case 2: return launch<16, GATHER, TREE>(mk, mv, p, grid, stream);
-    case 3: return launch<24, GATHER, TREE>(mk, mv, p, grid, stream);
-    default: return launch<32, GATHER, TREE>(mk, mv, p, grid, stream);
+    case 1: return launch<8, GATHER, TREE, WIN>(mk, mv, p, grid, stream);
+    case 2: return launch<16, GATHER, TREE, WIN>(mk, mv, p, grid, stream);
+    case 3: return launch<24, GATHER, TREE, WIN>(mk, mv, p, grid, stream);
+    default: return launch<32, GATHER, TREE, WIN>(mk, mv, p, grid, stream);
   }
 }
 
@@ -996,15 +1043,20 @@ namespace {
 // each row's partial state to part_out when it is set.  Arguments validated.
 tf_status verify_contig(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* seq_lens, int B,
                         int Hq, int Hkv, int Lmax, int T, float scale, float* out, void* ws, cudaStream_t stream,
-                        int pos0, int Ltot, float* part_out, const int32_t* parent = nullptr) {
+                        int pos0, int Ltot, float* part_out, const int32_t* parent = nullptr,
+                        const uint16_t* wq = nullptr, float* wout = nullptr, int n_sink = 0, int window = 0) {
   const long long rows_total = (long long)B * Hkv * Lmax;
   CUtensorMap mk, mv;
   if (!make_kv_map(&mk, K, rows_total, kTile) || !make_kv_map(&mv, V, rows_total, kTile)) return TF_ERR_CUDA;
   VerifyParams p{};
-  const int rows_all = (Hq / Hkv) * T;
+  const int rows_all = (Hq / Hkv) * T + (wq ? Hq / Hkv : 0);
   p.Q = Q;
   p.seq_lens = seq_lens;
   p.out = out;
+  p.wq = wq;
+  p.wout = wout;
+  p.n_sink = n_sink;
+  p.window = window;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.Lmax = Lmax;
@@ -1028,6 +1080,7 @@ tf_status verify_contig(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
                                       align_up((size_t)ug * p.splits_cap * kMaxRows * 2 * sizeof(float), 256));
   dim3 grid(p.splits, ug);
   const int rows_max = rows_all < kMaxRows ? rows_all : kMaxRows;
+  if (wq) return launch_rows<false, false, true>(rows_max, mk, mv, p, grid, stream);
   return parent ? launch_rows<false, true>(rows_max, mk, mv, p, grid, stream)
                 : launch_rows<false, false>(rows_max, mk, mv, p, grid, stream);
 }
@@ -1094,6 +1147,65 @@ extern "C" tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const 
   const size_t need = verify_ws(B * Hkv, (Hq / Hkv) * T, Lmax);
   if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
   return verify_contig(Q, K, V, seq_lens, B, Hq, Hkv, Lmax, T, scale, out, ws, stream, 0, Lmax, nullptr);
+}
+
+namespace tf {
+namespace {
+
+// The window rows ride in the verify launch when they change neither the
+// number of 32-row groups nor the kernel's row count (rows of the widest
+// group rounded up to 8), i.e. when they fill padding rows.  A group of window
+// rows alone would re-read the whole cache for a few hundred keys (128K, G = 8,
+// T = 4: 212.6 us per layer in one launch, 201.2 us in two), and the 32-row
+// kernel (18 warps, so at most 96 registers a thread) in place of the 24-row
+// one cost more inside the decode step than the window launch it saves (128K,
+// batch 4, G = 4, T = 6: 12.99 against 12.63 ms per step); both get two
+// launches.
+bool window_rows_fit(int G, int T) {
+  auto groups = [](int rows) { return (rows + kMaxRows - 1) / kMaxRows; };
+  auto width = [](int rows) { return (min(rows, kMaxRows) + 7) >> 3; };
+  return groups(G * (T + 1)) == groups(G * T) && width(G * (T + 1)) == width(G * T);
+}
+
+}  // namespace
+}  // namespace tf
+
+extern "C" size_t tf_verify_window_attn_workspace(int B, int Hq, int Hkv, int Lmax, int T, int n_sink, int window) {
+  using namespace tf;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lmax <= 0 || T < 1 || n_sink < 0 || window < 0 || Hq % Hkv) return 0;
+  const int G = Hq / Hkv;
+  if (window_rows_fit(G, T)) return verify_ws(B * Hkv, G * (T + 1), Lmax);
+  return align_up(verify_ws(B * Hkv, G * T, Lmax), 256) + tf_stream_window_attn_workspace(B, Hq, Hkv, n_sink, window);
+}
+
+extern "C" tf_status tf_verify_window_attn(const uint16_t* Q, const uint16_t* q, const uint16_t* K,
+                                           const uint16_t* V, const int32_t* seq_lens, int B, int Hq, int Hkv,
+                                           int Lmax, int D, int T, int n_sink, int window, float scale,
+                                           float* out, float* wout, void* ws, size_t ws_bytes,
+                                           tf_stream_t stream) {
+  using namespace tf;
+  if (!Q || !q || !K || !V || !seq_lens || !out || !wout) return TF_ERR_INVALID_ARG;
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || Hq % Hkv || T < 1 || n_sink < 0 || window < 0)
+    return TF_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) || !aligned16(wout))
+    return TF_ERR_INVALID_ARG;
+  if (D != kHeadDim || T > 16) return TF_ERR_UNSUPPORTED;
+  if (B == 0 || Lmax == 0) return TF_OK;
+  const long long rows_total = (long long)B * Hkv * Lmax;
+  if (rows_total >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (!window_rows_fit(G, T)) {
+    const size_t vneed = align_up(verify_ws(B * Hkv, G * T, Lmax), 256);
+    if (!ws || ws_bytes < vneed || !aligned16(ws)) return TF_ERR_WORKSPACE;
+    const tf_status st = tf_stream_window_attn(q, K, V, seq_lens, B, Hq, Hkv, Lmax, D, n_sink, window, scale, wout,
+                                               static_cast<char*>(ws) + vneed, ws_bytes - vneed, stream);
+    if (st != TF_OK) return st;
+    return verify_contig(Q, K, V, seq_lens, B, Hq, Hkv, Lmax, T, scale, out, ws, stream, 0, Lmax, nullptr);
+  }
+  const size_t need = verify_ws(B * Hkv, G * (T + 1), Lmax);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return TF_ERR_WORKSPACE;
+  return verify_contig(Q, K, V, seq_lens, B, Hq, Hkv, Lmax, T, scale, out, ws, stream, 0, Lmax, nullptr, nullptr,
+                       q, wout, n_sink, window);
 }
 
 extern "C" tf_status tf_verify_attn_tree(const uint16_t* Q, const uint16_t* K, const uint16_t* V,

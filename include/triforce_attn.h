@@ -304,6 +304,36 @@ TF_API tf_status tf_verify_attn(const uint16_t* Q, const uint16_t* K, const uint
                          void* ws, size_t ws_bytes, tf_stream_t stream);
 
 /*
+ * a7 and a6 in one call: tf_verify_attn plus tf_stream_window_attn for the
+ * decode queries q [B, Hq, 128] bf16 over the same cache ("TriForce:
+ * Hierarchical Speculative Decoding for LLMs", "The Three Forces of
+ * TriForce": Force 1's attention sinks plus recent window, Force 3's check of
+ * the candidates against the full cache).  With G = Hq / Hkv, when the G
+ * window rows of a KV head fill padding rows of the verify kernel (the
+ * G*(T+1) rows need neither more 32-row groups nor a wider group, rounded up
+ * to 8 rows, than the G*T candidate rows: G = 1 with T = 6, G = 4 with
+ * T = 5; not G = 1 with T = 8, G = 4 with T = 6 nor G = 8 with T = 4), they
+ * ride as extra query rows of the verify launch, masked to the keys
+ * [0, min(n_sink, L)) and [max(n_sink, L - window), L): one launch, the
+ * cache read once.  Otherwise the call makes two launches on the stream
+ * (tf_stream_window_attn, then tf_verify_attn): a wider kernel or a group of
+ * window rows alone costs more than the window launch.
+ * out [B, Hq, T, 128] as tf_verify_attn, wout [B, Hq, 128] as
+ * tf_stream_window_attn (both fp32, within the attention tolerance of the
+ * separate calls).  Workspace from tf_verify_window_attn_workspace (0 for
+ * arguments it refuses); its status word sits where tf_verify_attn's does.
+ * T <= 16.  Device pointers, 16-byte aligned.  Errors: null pointer,
+ * negative size, n_sink or window, Hq % Hkv != 0 or misalignment ->
+ * TF_ERR_INVALID_ARG; D != 128 or T > 16 -> TF_ERR_UNSUPPORTED; a workspace
+ * below the size -> TF_ERR_WORKSPACE; all before any launch.
+ */
+TF_API size_t tf_verify_window_attn_workspace(int B, int Hq, int Hkv, int Lmax, int T, int n_sink, int window);
+TF_API tf_status tf_verify_window_attn(const uint16_t* Q, const uint16_t* q, const uint16_t* K,
+                                       const uint16_t* V, const int32_t* seq_lens, int B, int Hq, int Hkv,
+                                       int Lmax, int D, int T, int n_sink, int window, float scale,
+                                       float* out, float* wout, void* ws, size_t ws_bytes, tf_stream_t stream);
+
+/*
  * a7 over a candidate tree ("TriForce: Hierarchical Speculative Decoding for
  * LLMs", "The Three Forces of TriForce": Force 2
  * arranges the surviving candidates as a tree and Force 3 checks the whole

@@ -98,6 +98,32 @@ def test_host_validation_rejects_before_launch(lib):
                                        fake, None) == INVALID  # misaligned means
     assert lib.tf_retrieval_draft_attn(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 16, 64, 0.1, fake, fake, null,
                                        fake, None) == UNSUPPORTED  # chunk 16
+    # verify + window in one launch: Q, q, K, V, seq, B, Hq, Hkv, Lmax, D, T, n_sink, window, scale, out, wout, ws, bytes, s
+    vw = lib.tf_verify_window_attn
+    assert vw(fake, null, fake, fake, fake, 1, 8, 2, 64, 128, 6, 4, 252, 0.1, fake, fake, fake, 1 << 30,
+              None) == INVALID  # no window queries
+    assert vw(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 6, 4, 252, 0.1, fake, null, fake, 1 << 30,
+              None) == INVALID  # no window output
+    assert vw(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 17, 4, 252, 0.1, fake, fake, fake, 1 << 30,
+              None) == UNSUPPORTED  # T > 16
+    assert vw(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 6, -1, 252, 0.1, fake, fake, fake, 1 << 30,
+              None) == INVALID  # negative sink count
+    assert vw(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 6, 4, 252, 0.1, fake, fake, fake, 0,
+              None) == WORKSPACE
+    # window rows in the verify launch when they fill padding rows: 4 x 6 verify rows -> 4 x 7 (24-row kernel)
+    # and 8 x 5 -> 8 x 6 (two groups, 32-row kernel); not 4 x 6 -> 4 x 7 (24 -> 32 rows) nor 4 x 8 -> 4 x 9
+    # (a second group): the window launched apart, its scratch after the verify's
+    for G, T in ((4, 5), (8, 5), (1, 6), (1, 15)):  # the verify scratch of G * (T + 1) rows
+        assert lib.tf_verify_window_attn_workspace(1, 2 * G, 2, 64, T, 4, 252) == \
+            lib.tf_verify_attn_workspace(1, 2 * G, 2, 64, T + 1)
+    for G, T in ((4, 6), (4, 8), (8, 4), (1, 8), (1, 16)):
+        vsz = lib.tf_verify_attn_workspace(1, 2 * G, 2, 64, T)
+        assert lib.tf_verify_window_attn_workspace(1, 2 * G, 2, 64, T, 4, 252) == \
+            -(-vsz // 256) * 256 + lib.tf_stream_window_attn_workspace(1, 2 * G, 2, 4, 252)
+    vsz = lib.tf_verify_attn_workspace(1, 8, 2, 64, 8)
+    assert vw(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 4, 252, 0.1, fake, fake, fake, vsz,
+              None) == WORKSPACE  # room for the verify scratch only
+    assert lib.tf_verify_window_attn_workspace(1, 8, 2, 64, 6, -1, 252) == 0
     # the same with a cut hint (before idx): required, and the same limits
     hd = lib.tf_retrieval_draft_attn_hinted
     assert hd(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 64, 0.1, null, fake, fake, null, fake,

@@ -270,18 +270,46 @@ def test_stream_window_attn(cuda_lib, w):
 
 
 @pytest.mark.parametrize("w", [synth.TINY, small_workload(), small_workload(Hkv=8, T=6, L=3000, L_min=2000),
-                               synth.LLAMA2_7B_32K_1LAYER],
-                         ids=["tiny", "ragged-gqa", "mha-6", "llama2-7b-32k-1layer"])
-def test_verify_attn(cuda_lib, w):
+                               small_workload(T=5),
+                               small_workload(B=1, Hq=16, Hkv=2, T=4, L=900, ragged=False),
+                               small_workload(B=2, Hq=8, Hkv=2, T=16, L=700, L_min=100),
+                               small_workload(T=5, L=40000, L_min=30000),
+                               small_workload(B=2, Hq=16, Hkv=2, T=5, L=40000, L_min=30000),
+                               small_workload(B=2, Hq=16, Hkv=2, T=4, L=40000, L_min=30000)],
+                         ids=["tiny", "gqa-two-launches", "mha-6", "gqa-t5-padding-rows", "own-group-two-launches",
+                              "three-groups-two-launches", "split", "window-warpgroup-split",
+                              "own-group-two-launches-split"])
+def test_verify_window_attn(cuda_lib, w):
+    """Both outputs against the two oracle calls: window rows after the G*T
+    verify rows in one launch (G*(T+1) rows fit the verify row groups), and the
+    two-launch path where they would need a group of their own."""
     c = make_case(w, fill_invalid=float("nan") if w.ragged else None)
-    ws = cuda_lib.workspace(cuda_lib.tf_verify_attn_workspace(w.B, w.Hq, w.Hkv, w.L, w.T), "cuda")
-    for _ in range(2):  # a second call on the same workspace (tickets reset by the first)
-        out = cuda_lib.tf_verify_attn(c["Q"], c["K"], c["V"], c["seq"], scale_for(w.D), ws=ws)
+    ws = cuda_lib.workspace(cuda_lib.tf_verify_window_attn_workspace(w.B, w.Hq, w.Hkv, w.L, w.T, w.n_sink, w.window), "cuda")
+    want = O.verify_attn(bits(c["Q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), c["seq_cpu"].numpy(), scale_for(w.D))
+    wwant = O.stream_window_attn(bits(c["q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), c["seq_cpu"].numpy(), w.n_sink,
+                                 w.window, scale_for(w.D))
+    for _ in range(2):  # a second call on the same workspace
+        out, wout = cuda_lib.tf_verify_window_attn(c["Q"], c["q"], c["K"], c["V"], c["seq"], w.n_sink, w.window,
+                                                   scale_for(w.D), ws=ws)
         torch.cuda.synchronize()
         assert int(ws[:4].view(torch.int32).item()) == 0, "pipeline status word set"
-        want = O.verify_attn(bits(c["Q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), c["seq_cpu"].numpy(),
-                             scale_for(w.D))
         assert np.abs(out.cpu().double().numpy() - want).max() <= ATOL
+        assert np.abs(wout.cpu().double().numpy() - wwant).max() <= ATOL
+
+
+def test_verify_window_attn_short_contexts(cuda_lib):
+    """Contexts shorter than the candidates, than the sinks and the window, and
+    empty: both outputs follow their oracle position sets."""
+    w = small_workload(B=4, Hq=8, Hkv=2, T=6, L=700, ragged=False)
+    c = make_case(w)
+    seq = np.array([3, 0, 50, 700], dtype=np.int32)
+    c["seq"] = torch.from_numpy(seq).cuda()
+    out, wout = cuda_lib.tf_verify_window_attn(c["Q"], c["q"], c["K"], c["V"], c["seq"], w.n_sink, w.window, 0.1)
+    want = O.verify_attn(bits(c["Q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), seq, 0.1)
+    wwant = O.stream_window_attn(bits(c["q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), seq, w.n_sink, w.window, 0.1)
+    assert np.abs(out.cpu().double().numpy() - want).max() <= ATOL
+    assert np.abs(wout.cpu().double().numpy() - wwant).max() <= ATOL
+    assert np.all(wout.cpu().numpy()[1] == 0)
 
 
 @pytest.mark.parametrize("G,T", [(1, 1), (2, 3), (1, 16), (2, 5), (3, 7), (4, 6), (2, 16), (8, 4), (4, 9)],
