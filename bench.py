@@ -283,11 +283,11 @@ def _ev():
 _FLUSH = {}
 
 
-def _median_call_ms(fn, stream, reps=5, warm=1):
-    """Median device time of fn() on `stream`, each call bracketed by CUDA
-    events behind a queued 512 MB memset: the memset keeps the GPU busy while
-    the host enqueues the event, the call and the closing event (so host launch
-    cost is not timed) and leaves L2 cold."""
+def _median_call_ms(fn, stream, reps=5, warm=1, agg=statistics.median):
+    """Median (or `agg`) device time of fn() on `stream`, each call bracketed
+    by CUDA events behind a queued 512 MB memset: the memset keeps the GPU busy
+    while the host enqueues the event, the call and the closing event (so host
+    launch cost is not timed) and leaves L2 cold."""
     import torch
 
     if "buf" not in _FLUSH:
@@ -304,7 +304,7 @@ def _median_call_ms(fn, stream, reps=5, warm=1):
         b.record(stream)
         torch.cuda.synchronize()
         out.append(a.elapsed_time(b))
-    return statistics.median(out)
+    return agg(out)
 
 
 def graph_loop_ms(calls, stream, replays=5):
@@ -412,21 +412,26 @@ class StepState:
             "sparse": 2 * sel_rows * row + ids + q_io,
             "draft": means + ids + 2 * sel_rows * row + q_io,
             "window": sum(2 * Hkv * min(x, w.n_sink + w.window) * row for x in lens) + q_io,
-            "verify_only": sum(2 * Hkv * x * row for x in lens) + B * Hq * T * D * (2 + 4),
-            # the window rows read keys the verify rows read anyway: only their queries and outputs add
-            "verify": sum(2 * Hkv * x * row for x in lens) + B * Hq * T * D * (2 + 4) + q_io,
+            # in one launch the window rows read keys the verify rows read anyway: only their queries
+            # and outputs add
+            "verify": sum(2 * Hkv * x * row for x in lens) + B * Hq * T * D * (2 + 4) + (
+                q_io if self.vw_launches == 1 else 0),
         }
 
 
-def make_step(st, tf, two_call, stream, hinted=True):
+def make_step(st, tf, two_call, stream, hinted=True, split_window=False):
     """One decode step over the layers.  step(evs, k) takes query set k (None:
     the live buffers st.q / st.Q).  With hinted, the fused drafter gets the
     previous step's cut of each layer x HINT_SCALE as a lower bound (a decode
-    loop has it for free; one elementwise op per step forms it)."""
+    loop has it for free; one elementwise op per step forms it).  Window and
+    verify: one tf_verify_window_attn call; with split_window, where that call
+    makes two launches, the same two launches as two calls (an event between
+    them for the per-kernel breakdown)."""
     import torch
 
     w = st.w
-    kinds = ("draft", "verify")  # verify: tf_verify_window_attn, the window rows inside the verify launch
+    split = split_window and st.vw_launches == 2
+    kinds = ("draft", "window", "verify") if split else ("draft", "verify")
     hinted = hinted and not two_call
 
     def draft(l, q=None):
@@ -451,10 +456,17 @@ def make_step(st, tf, two_call, stream, hinted=True):
             draft(l, q)
             if evs is not None:
                 evs[l][1].record(stream)
-            tf.tf_verify_window_attn(Q[l], q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window, st.scale,
-                                     out=st.o_ver[l], wout=st.o_win[l], ws=st.ws_vw)
+            if split:
+                tf.tf_stream_window_attn(q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window, st.scale,
+                                         out=st.o_win[l], ws=st.ws_win)
+                if evs is not None:
+                    evs[l][2].record(stream)
+                tf.tf_verify_attn(Q[l], st.K[l], st.V[l], st.seq, st.scale, out=st.o_ver[l], ws=st.ws_ver)
+            else:
+                tf.tf_verify_window_attn(Q[l], q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window, st.scale,
+                                         out=st.o_ver[l], wout=st.o_win[l], ws=st.ws_vw)
             if evs is not None:
-                evs[l][2].record(stream)
+                evs[l][len(kinds)].record(stream)
 
     return step, draft, kinds
 
@@ -487,6 +499,21 @@ def time_steps(run_step, steps, stream, world, local):
     barrier(world)
     value, elapsed_s = job_throughput(steps, t_start.elapsed_time(t_end) / 1e3, world)
     return value, elapsed_s, clocks.summary()
+
+
+def breakdown_cycle(st, tf, args, stream, k):
+    """The step for the per-kernel breakdown (window and verify as separate
+    calls where tf_verify_window_attn makes two launches), continuing at
+    query set k.  Returns the cycle and its kinds."""
+    step, _, kinds = make_step(st, tf, args.two_call_draft, stream, split_window=True)
+    cyc = StepCycle(step)
+    cyc.k = k
+    return cyc, kinds
+
+
+def verify_label(st):
+    return ("tf_verify_window_attn (one launch: the window rows inside the verify launch)" if st.vw_launches == 1
+            else "tf_verify_attn, after tf_stream_window_attn (the two launches tf_verify_window_attn makes here)")
 
 
 def per_kernel_times(step, layers, k_steps, kinds):
@@ -589,12 +616,15 @@ def measure_extra_workload(w, args, tf, synth, dev, stream, world, local, peak):
     torch.cuda.synchronize()
     steps = max(3, args.steps // 2)
     value, elapsed_s, clocks = time_steps(cyc, steps, stream, world, local)
-    per_kind = per_kernel_times(cyc, st.layers, max(3, steps // 2), kinds)
+    cyc_k, kinds_k = breakdown_cycle(st, tf, args, stream, cyc.k)
+    per_kind = per_kernel_times(cyc_k, st.layers, max(3, steps // 2), kinds_k)
+    cyc.k = cyc_k.k
     nb = st.bytes_per_launch()
     kern = {}
-    for k in kinds:
+    for k in kinds_k:
         name = "retrieval_draft" if k == "draft" else k
         kern[name] = kernel_entry(nb[k], statistics.mean(per_kind[k]), peak)
+    kern["verify"]["calls"] = verify_label(st)
     kern["retrieval_draft"]["back_to_back"] = kernel_entry(nb["draft"], draft_back_to_back_ms(st, draft, cyc, stream),
                                                            peak)
     kern["sparse_verify_level1"] = measure_level1(st, w, tf, dev, stream, peak)
@@ -605,7 +635,7 @@ def measure_extra_workload(w, args, tf, synth, dev, stream, world, local, peak):
            "config": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D, "context": w.L, "layers": w.layers,
                       "ragged": bool(w.ragged), "seq_lens": st.seq_cpu.tolist(), "budget_tokens": w.budget,
                       "verify_tokens": w.T},
-           "roofline": {"bound": "hbm", "kernel": "tf_verify_window_attn", "achieved": ver["GBps"], "peak": peak,
+           "roofline": {"bound": "hbm", "kernel": verify_label(st), "achieved": ver["GBps"], "peak": peak,
                         "unit": "GB/s", "frac": ver["frac_hbm"], "algorithmic_bytes": nb["verify"],
                         "traffic": recorded_traffic("verify_attn.cu", w.name)},
            "kernels": kern, "clocks": clocks,
@@ -643,21 +673,24 @@ def measure_offload(st, tf, stream, peak, kernels):
         tf.tf_verify_attn_offload(st.Q[0], Kh, Vh, st.seq, Lmax_seq, st.scale, out=o_off, ws=ws_off, seg_rows=seg_rows,
                                   copy_stream=side)
 
-    off_ms = min(_median_call_ms(verify_off, stream, reps=3), float("inf"))
+    # The host link is shared with the machine's other GPUs and jobs: every
+    # figure over it is the fastest of five calls (a median of three once read
+    # 22 ms for a 10.3 ms call, another time the plain copy 3x slow).
+    off_ms = _median_call_ms(verify_off, stream, reps=5, agg=min)
     stage = torch.empty_like(st.K[0])
 
     def h2d():
         stage.copy_(Kh, non_blocking=True)
         stage.copy_(Vh, non_blocking=True)
 
-    h2d_ms = _median_call_ms(h2d, stream, reps=4)
+    h2d_ms = _median_call_ms(h2d, stream, reps=5, agg=min)
     del stage
     h2d_gbps = off_bytes / (h2d_ms / 1e3) / 1e9
     kernels["verify_offloaded_1layer"] = {
         "ms": round(off_ms, 4), "GBps": round(off_bytes / (off_ms / 1e3) / 1e9, 1), "h2d_copy_GBps": round(h2d_gbps, 1),
         "frac_of_h2d_copy": round(h2d_ms / off_ms, 4), "calls": "tf_verify_attn_offload",
-        "timing": "K/V in pinned host memory, 16K-position segments, copies on a second stream; median of 3 calls "
-                  "against the median of 4 plain pinned host-to-device copies of the same bytes"}
+        "timing": "K/V in pinned host memory, 16K-position segments, copies on a second stream; fastest of 5 calls "
+                  "against the fastest of 5 plain pinned host-to-device copies of the same bytes"}
 
     # the retrieval drafter's resident cache: this layer's selection packed
     kc = w.kc
@@ -673,7 +706,7 @@ def measure_offload(st, tf, stream, peak, kernels):
         return lambda: tf.tf_pack_retrieval_cache(src_k, src_v, st.seq, st.idx[0], st.nsel[0], Kc, Vc, lens, nch)
 
     pk_dev = _median_call_ms(pack(st.K[0], st.V[0]), stream)
-    pk_host = _median_call_ms(pack(Kh, Vh), stream, reps=3)
+    pk_host = _median_call_ms(pack(Kh, Vh), stream, reps=5, agg=min)
     kernels["pack_retrieval_cache_1layer"] = {
         "device": dict(kernel_entry(pack_bytes, pk_dev, peak), bytes=pack_bytes,
                        bound="selected K+V rows read and written once (HBM)"),
@@ -709,7 +742,7 @@ def measure_offload(st, tf, stream, peak, kernels):
         tf.tf_stream_window_attn(st.q[0], Kw, Vw, wlens, w.n_sink, w.window, st.scale, out=o_w, ws=ws_w1)
         verify_off()
 
-    step_ms = _median_call_ms(off_step, stream, reps=5)
+    step_ms = _median_call_ms(off_step, stream, reps=5, agg=min)
     link = off_bytes + rows_bytes
     kernels["offloaded_step_1layer"] = {
         "ms": round(step_ms, 4), "bytes_over_link": link, "GBps_over_link": round(link / (step_ms / 1e3) / 1e9, 1),
@@ -779,32 +812,32 @@ def run_gpu(args):
 
     # ---- per-kernel breakdown and the verify roofline
     k_steps = max(3, args.steps // 2)
-    cyc.k = getattr(run_step, "k", cyc.k)
-    per_kind = per_kernel_times(cyc, layers, k_steps, kinds)
+    cyc_k, kinds_k = breakdown_cycle(st, tf, args, stream, getattr(run_step, "k", cyc.k))
+    per_kind = per_kernel_times(cyc_k, layers, k_steps, kinds_k)
+    cyc.k = cyc_k.k
     nb = st.bytes_per_launch()
     kernels = {}
-    for k in kinds:
+    for k in kinds_k:
         name = "retrieval_draft" if k == "draft" else k
         kernels[name] = kernel_entry(nb[k], statistics.mean(per_kind[k]), peak)
     kernels["retrieval_draft"]["calls"] = ("tf_chunk_scores_topk + tf_sparse_decode_attn" if args.two_call_draft
                                            else "tf_retrieval_draft_attn")
     kernels["retrieval_draft"]["traffic"] = (None if args.two_call_draft
                                              else recorded_traffic("retrieval_draft.cu", w.name))
-    # the two-call form of the retrieval drafter, for comparison (events around each call)
+    # the two-call form of the retrieval drafter, for comparison: each call back to back over the
+    # layers as one CUDA graph (eager launches with events between them timed the host's launch gaps)
     if not args.two_call_draft:
-        ev = [[_ev() for _ in range(3)] for _ in range(layers)]
-        torch.cuda.synchronize()
-        for l in range(layers):
-            ev[l][0].record(stream)
+        def topk(l):
             tf.tf_chunk_scores_topk(st.q[l], st.M[l], st.seq, L, w.kc, st.idx[l], st.nsel[l], ws=st.ws_topk)
-            ev[l][1].record(stream)
+
+        def sparse(l):
             tf.tf_sparse_decode_attn(st.q[l], st.K[l], st.V[l], st.seq, st.idx[l], st.nsel[l], st.scale,
                                      out=st.o_sp[l], ws=st.ws_sp)
-            ev[l][2].record(stream)
-        torch.cuda.synchronize()
-        for i, k in enumerate(("topk", "sparse")):
-            ms = statistics.mean(ev[l][i].elapsed_time(ev[l][i + 1]) for l in range(layers))
-            kernels["two_call_" + k] = kernel_entry(nb[k], ms, peak)
+
+        for k, f in (("topk", topk), ("sparse", sparse)):
+            ms = graph_loop_ms([lambda l=l, f=f: f(l) for l in range(layers)], stream)
+            kernels["two_call_" + k] = dict(kernel_entry(nb[k], ms, peak), timing="back to back over the layers, "
+                                                                                   "replayed as one CUDA graph")
     kernels["retrieval_draft"]["back_to_back"] = kernel_entry(nb["draft"], draft_back_to_back_ms(st, draft, cyc, stream),
                                                               peak)
 
@@ -815,9 +848,9 @@ def run_gpu(args):
     win_ms = graph_loop_ms([lambda l=l: tf.tf_stream_window_attn(st.q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window,
                                                                  st.scale, out=st.o_win[l], ws=st.ws_win)
                             for l in range(layers)], stream)
-    kernels["window"] = {"in_step": "no: the step computes the window rows inside the verify launch",
-                         "back_to_back": dict(kernel_entry(nb["window"], win_ms, peak),
-                                              timing="replayed as one CUDA graph")}
+    if "window" not in kernels:
+        kernels["window"] = {"in_step": "no: the step computes the window rows inside the verify launch"}
+    kernels["window"]["back_to_back"] = dict(kernel_entry(nb["window"], win_ms, peak), timing="replayed as one CUDA graph")
     kernels["window"]["floor_16rows_us"] = round(graph_loop_ms(
         [lambda l=l: tf.tf_stream_window_attn(st.q[l], st.K[l], st.V[l], st.seq, 4, 12, st.scale, out=o_w16,
                                               ws=ws_w16) for l in range(layers)], stream) * 1e3, 2)
@@ -838,8 +871,7 @@ def run_gpu(args):
         name: round(graph_loop_ms([lambda l=l, f=f: f(l) for l in range(layers)], stream) * 1e3, 2)
         for name, f in (("verify_window_one_call", fused), ("verify_alone", ver_alone),
                         ("window_then_verify", separate))}
-    kernels["verify"]["calls"] = "tf_verify_window_attn (%d launch%s)" % (st.vw_launches,
-                                                                          "" if st.vw_launches == 1 else "es")
+    kernels["verify"]["calls"] = verify_label(st)
 
     # the offloaded setting (one 128K layer; not part of the step)
     measure_offload(st, tf, stream, peak, kernels)
@@ -860,7 +892,7 @@ def run_gpu(args):
                    "queries": f"{N_QUERY_SETS} seeded query sets cycled over the steps; the retrieval drafter "
                               f"takes the previous step's cut x {HINT_SCALE} of each layer as a bound "
                               f"(cold_start: the same step without it)"},
-        "roofline": {"bound": "hbm", "kernel": "tf_verify_window_attn", "achieved": round(achieved, 1), "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": verify_label(st), "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": nb["verify"], "peak_source": peak_kind},
         "kernels": kernels,
