@@ -16,15 +16,15 @@
 //    every chunk whose key lies above b1 is selected whatever the rest of the
 //    cut.  The CTA lists those chunks and splits: warps 0..7 finish the cut
 //    (candidate gather, last 21 bits, id-order output, the chunks of bin b1
-//    appended to the list) on a named barrier, while warp 15 stages listed
-//    chunks (K and V rows, cp.async.bulk into a ring of 4 KB slots) and warps
-//    8..14 attend them.  When the cut is done, warps 0..7 join as consumers.
-//    HBM keeps streaming while the cut is resolved.
-//  * Each consumer warp owns one ring slot; the producer hands the next listed
-//    chunk to whichever slot its consumer has released (non-blocking polls in
-//    a warp-uniform loop), and an empty marker ends a consumer's loop.  A slot
-//    only ever has one producer and one consumer, so every wait on its
-//    barriers is for the very next phase.
+//    appended to the list) on a named barrier, while warps 8..15 attend the
+//    listed chunks.  When the cut is done, warps 0..7 join them.  HBM keeps
+//    streaming while the cut is resolved.
+//  * Each warp owns one 4 KB ring slot and stages its own chunks: lane 0
+//    claims the next list entry (a shared counter), copies the chunk's K and V
+//    rows into the slot (cp.async.bulk) and the warp waits for them; entries
+//    past the certain ones are read once the cut group has published the final
+//    list.  No hand-over between warps: a slot is free again as soon as its
+//    warp has read it.
 //  * Consumer lane (row r, quarter dq) forms 32-dim dot products with the
 //    query rows held in shared memory in a bank-conflict-free permuted layout;
 //    the online softmax runs in the log2 domain in fp32 and each lane owns 4
@@ -45,21 +45,20 @@ using topk::kMaxSliceKeys;
 using topk::kThreads;
 using topk::kWarps;
 
-constexpr int kProducerWarp = kWarps - 1;
-constexpr int kComputeWarps = kWarps - 1;
+constexpr int kComputeWarps = kWarps;                   // every warp attends
 constexpr int kCutWarps = 8;                            // warps 0..7 finish the cut
-constexpr int kRingSlots = kComputeWarps;               // one slot per consumer warp
-constexpr int kEarlySlots = kComputeWarps - kCutWarps;  // slots of warps 8..14
+constexpr int kRingSlots = kComputeWarps;               // one slot per warp
+constexpr int kEarlySlots = kComputeWarps - kCutWarps;  // slots of warps 8..15
 constexpr int kSlotBytes = 4096;  // K rows [0, 2 KB), V rows [2 KB, 4 KB)
 constexpr int kCandCap = 2048;    // keys of the threshold bin gathered on every CTA
 constexpr int kHintCap = 4096;    // keys above a cut bound gathered on every CTA (over gcand and hist1)
 constexpr int kMaxList = 2048;    // selected chunks per CTA (kc <= kMaxList)
-constexpr uint32_t kIdleLimit = 1u << 22;  // producer polls without progress before it gives up
+constexpr uint32_t kIdleLimit = 1u << 22;  // polls for the final list before a warp gives up
 
 // Dynamic shared memory (bytes).
-//  [0, 28672)      ring slots 0..6 (consumers 8..14); during round 1 they hold
+//  [0, 32768)      ring slots 0..7 (warps 8..15); during round 1 they hold
 //                  tot, which only this CTA reads
-//  [28672, 61440)  ring slots 7..14 (consumers 0..7) once the cut is done;
+//  [32768, 65536)  ring slots 8..15 (warps 0..7) once the cut is done;
 //                  until then hist2, hist3, gcand (the cut group's scratch)
 //                  and hist1 (read by the other CTAs in round 1, which they
 //                  finish before the cut's cluster barrier; with a cut bound
@@ -68,13 +67,13 @@ constexpr uint32_t kIdleLimit = 1u << 22;  // producer polls without progress be
 //  alist           this CTA's selected chunks (certain ones first)
 //  keys            this CTA's score keys
 constexpr int kOffTot = 0;
-constexpr int kOffHist2 = kEarlySlots * kSlotBytes;  // 28672
-constexpr int kOffHist3 = kOffHist2 + 2048 * 4;      // 36864
-constexpr int kOffGcand = kOffHist3 + 1024 * 4;      // 40960
-constexpr int kOffHist1 = kOffGcand + kCandCap * 4;  // 49152
-constexpr int kOffCand = kRingSlots * kSlotBytes;    // 61440
-constexpr int kOffList = kOffCand + kCandCap * 4;    // 69632
-constexpr int kOffKeys = kOffList + kMaxList * 4;    // 77824
+constexpr int kOffHist2 = kEarlySlots * kSlotBytes;  // 32768
+constexpr int kOffHist3 = kOffHist2 + 2048 * 4;      // 40960
+constexpr int kOffGcand = kOffHist3 + 1024 * 4;      // 45056
+constexpr int kOffHist1 = kOffGcand + kCandCap * 4;  // 53248
+constexpr int kOffCand = kRingSlots * kSlotBytes;    // 65536
+constexpr int kOffList = kOffCand + kCandCap * 4;    // 73728
+constexpr int kOffKeys = kOffList + kMaxList * 4;    // 81920
 static_assert(kOffHist1 + 2048 * 4 <= kOffCand, "the cut's scratch must fit the late slots");
 static_assert(kOffGcand + kHintCap * 4 <= kOffCand, "the hinted gather must fit the late slots");
 static_assert(kOffTot + 2048 * 4 <= kOffHist2, "tot must stay inside the early slots");
@@ -98,8 +97,8 @@ struct DraftParams {
 
 size_t draft_smem(int slice) { return (size_t)kOffKeys + (size_t)slice * sizeof(uint32_t); }
 
-// Ring slot of consumer warp w: warps 8..14 take slots 0..6, warps 0..7 (the
-// cut group) slots 7..14.
+// Ring slot of warp w: warps 8..15 take slots 0..7, warps 0..7 (the cut
+// group) slots 8..15.
 __device__ __forceinline__ int slot_of(int warp) { return (warp + kEarlySlots) % kRingSlots; }
 
 template <int NQ>
@@ -107,12 +106,12 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) float qsm[NQ * kHeadDim];  // scaled query rows, permuted (see below)
   __shared__ float qs[kHeadDim];                      // the group's summed query (scores)
-  __shared__ __align__(8) uint64_t bar_full[kRingSlots], bar_empty[kRingSlots];
+  __shared__ __align__(8) uint64_t bar_full[kRingSlots];
   __shared__ int slot_n[kRingSlots], slot_uses[kRingSlots];
   __shared__ float wm[kComputeWarps][NQ], wl[kComputeWarps][NQ];
   __shared__ float cpart[NQ][kHeadDim], cm[NQ], cl[NQ];
   __shared__ uint32_t s_min;
-  __shared__ int s_na, s_ntot, s_abort, s_hcnt;
+  __shared__ int s_na, s_ntot, s_abort, s_hcnt, s_next;
   __shared__ int s_hroff[kMaxCluster + 1];
   __shared__ volatile int s_cut_done;
 
@@ -136,11 +135,9 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kRingSlots; ++s) {
-      mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1);
-    }
+    for (int s = 0; s < kRingSlots; ++s) mbar_init(&bar_full[s], 1);
     s_abort = 0;
+    s_next = 0;
     s_hcnt = 0;
     s_na = 0;
     s_cut_done = 0;
@@ -297,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
   }
   const bool cut_group = split && warp < kCutWarps;
   if (cut_group) {
-    // ---- warps 0..7: the rest of the cut, then consumers of slots 7..14
+    // ---- warps 0..7: the rest of the cut, then attention from slots 8..15
     const topk::Cut cut = hinted.ok ? topk::hinted_cut(a, S, rank, hinted, s_hroff, topk::Warps0to7Bar())
                                     : topk::fast_cut(a, n, S, rank, r1, topk::Warps0to7Bar());
     T = cut.T;
@@ -317,83 +314,56 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
     cluster_arrive();  // the cut group's one cluster barrier; waited for below
   }
 
-  if (warp == kProducerWarp) {
-    // ---------------------------------------------------------------- producer
-    // Lane s < 15 tracks ring slot s: the chunks issued into it (uses) and
-    // whether its end marker went out.  A slot is free once its consumer has
-    // released its last chunk; free slots take the next listed chunks in lane
-    // order.  Non-blocking polls keep the whole warp in step.
-    fence_proxy_async_smem();  // slots 0..6 held tot (generic-proxy writes)
-    const unsigned lt = (1u << lane) - 1u;
-    int nact = split ? kEarlySlots : kRingSlots;
-    bool fin = !split;
-    int list_len = min(s_ntot, kMaxList);
-    int next = 0;
-    uint32_t uses = 0;
-    bool marked = false;
-    uint32_t idle = 0;
-    while (true) {
-      if (!fin && s_cut_done) {
-        __threadfence_block();
-        list_len = min(*(volatile int*)&s_ntot, kMaxList);
-        fin = true;
-        nact = kRingSlots;
-        fence_proxy_async_smem();  // slots 7..14 held the cut's scratch
-      }
-      const bool active = lane < nact && !marked;
-      const bool free_slot = active && (uses == 0 || mbar_test(&bar_empty[lane], (uses - 1) & 1));
-      const unsigned fm = __ballot_sync(0xffffffffu, free_slot);
-      const int avail = max(list_len - next, 0);
-      const int take = min(__popc(fm), avail);
-      const int rk = __popc(fm & lt);
-      if (free_slot && rk < take) {
-        issue(lane, alist[next + rk]);
-        ++uses;
-      }
-      next += take;
-      bool progress = take > 0;
-      if (fin && next >= list_len) {
-        if (free_slot && rk >= take) {  // nothing left for this slot: end marker
-          slot_n[lane] = -1;
-          mbar_arrive(&bar_full[lane]);
-          marked = true;
-          progress = true;
-        }
-        if (__ballot_sync(0xffffffffu, lane < kRingSlots && !marked) == 0) break;
-      }
-      if (progress) {
-        idle = 0;
-      } else if (++idle > kIdleLimit) {
-        if (lane == 0) atomicExch(&s_abort, 1);
-        break;
-      } else {
-        __nanosleep(64);
-      }
-    }
-    if (lane < kRingSlots) slot_uses[lane] = uses;
-    if (s_abort && lane < kRingSlots && !marked) {
-      // (only after a timeout) let this slot's last copy land, then release
-      // its consumer
-      if (uses > 0) mbar_wait(&bar_full[lane], (uses - 1) & 1, 1u << 8);
-      slot_n[lane] = -1;
-      mbar_arrive(&bar_full[lane]);
-    }
-  } else {
-    // ---------------------------------------------------------------- consumers
-    // lane = (row r, quarter dq); pieces visited in the rotated order jr(j)
+  {
+    // ---------------------------------------------------------------- attention
+    // Lane 0 claims the next list entry and stages the chunk into the warp's
+    // slot.  Entries [0, ncert) are final when the attention starts; with the
+    // cut still running, later entries are read once the cut group has
+    // published the final length.
     const int slot = slot_of(warp);
+    const int ncert = split ? s_na : min(s_ntot, kMaxList);
+    // lane = (row r, quarter dq); pieces visited in the rotated order jr(j)
     const int r = lane >> 2, dq = lane & 3;
     const int rot = (dq >> 1) + 2 * (r & 1);
     const float4* q4 = reinterpret_cast<const float4*>(qsm);
     const uint8_t* kb = ring + slot * kSlotBytes;
     const uint8_t* vb = kb + 2048;
-    for (uint32_t u = 0;; ++u) {
-      if (!mbar_wait(&bar_full[slot], u & 1)) {
+    constexpr int kNoChunk = -0x7fffffff - 1;
+    uint32_t u = 0;  // copies issued into the slot
+    while (true) {
+      int c = kNoChunk;
+      if (lane == 0) {
+        const int i = atomicAdd(&s_next, 1);
+        if (i < ncert) {
+          c = alist[i];
+        } else if (split) {
+          uint32_t spins = 0;
+          while (!s_cut_done && !*(volatile int*)&s_abort) {
+            if (++spins > kIdleLimit) {
+              atomicExch(&s_abort, 1);
+              break;
+            }
+            __nanosleep(64);
+          }
+          if (s_cut_done) {
+            __threadfence_block();
+            if (i < min(*(volatile int*)&s_ntot, kMaxList)) c = alist[i];
+          }
+        }
+        if (c != kNoChunk) {
+          fence_proxy_async_smem();  // the slot's earlier generic reads and writes before the copy
+          issue(slot, c);
+        }
+      }
+      c = __shfl_sync(0xffffffffu, c, 0);
+      if (c == kNoChunk) break;
+      const uint32_t ph = u & 1;
+      ++u;
+      if (!mbar_wait(&bar_full[slot], ph)) {
         if (lane == 0) atomicExch(&s_abort, 1);
         break;
       }
       const int nr = slot_n[slot];
-      if (nr < 0) break;  // end marker
       float sa[NQ], sb[NQ];  // two independent partial sums per head
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -458,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_empty[slot]);
     }
+    if (lane == 0) slot_uses[slot] = (int)u;
   }
   if (split && !cut_group && !hinted.ok) cluster_wait();
   __syncthreads();  // every chunk consumed: the ring is idle and serves as scratch
@@ -471,16 +441,14 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
   }
   __syncthreads();
   float* wo = reinterpret_cast<float*>(ring);  // [kComputeWarps][NQ][128]
-  if (warp != kProducerWarp) {
 #pragma unroll
-    for (int h = 0; h < NQ; ++h) {
-      if (lane == 0) {
-        wm[warp][h] = m[h];
-        wl[warp][h] = l[h];
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) wo[(warp * NQ + h) * kHeadDim + lane * 4 + i] = o[h][i];
+  for (int h = 0; h < NQ; ++h) {
+    if (lane == 0) {
+      wm[warp][h] = m[h];
+      wl[warp][h] = l[h];
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) wo[(warp * NQ + h) * kHeadDim + lane * 4 + i] = o[h][i];
   }
   __syncthreads();
 
