@@ -123,6 +123,20 @@ def _need(t, dtype, name, ndim=None):
         raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
 
 
+def _shape(t, shape, name):
+    """The library reads and writes whole buffers from the sizes it is given,
+    which it cannot check against the tensors: every buffer must have exactly
+    the shape those sizes imply."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _kv_shapes(K, V, seq_lens, B, D):
+    _shape(K, (B,) + tuple(K.shape[1:3]) + (D,), "K")
+    _shape(V, tuple(K.shape), "V")
+    _shape(seq_lens, (B,), "seq_lens")
+
+
 def workspace(nbytes: int, device) -> torch.Tensor:
     """A zero-filled scratch buffer (the library requires zeroed workspace once)."""
     return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device)
@@ -196,6 +210,11 @@ def tf_chunk_scores_topk(q, M, seq_lens, Lmax, kc, idx=None, n_sel=None, s_cut=N
     _need(n_sel, torch.int32, "n_sel", 2)
     if s_cut is not None:
         _need(s_cut, torch.float32, "s_cut", 2)
+    _shape(M, (B, Hkv, -(-Lmax // chunk), D), "M")
+    _shape(seq_lens, (B,), "seq_lens")
+    _shape(idx, (B, Hkv, kc), "idx")
+    _shape(n_sel, (B, Hkv), "n_sel")
+    _shape(s_cut, (B, Hkv), "s_cut")
     ws, nbytes = _ws(ws, tf_chunk_scores_topk_workspace(B, Hkv, Lmax, chunk), q.device)
     _check(load().tf_chunk_scores_topk(_ptr(q), _ptr(M), _ptr(seq_lens), B, Hq, Hkv, Lmax, D, chunk, kc, _ptr(idx),
                                        _ptr(n_sel), _ptr(s_cut), _ptr(ws), nbytes, _stream(stream)),
@@ -220,6 +239,10 @@ def tf_sparse_decode_attn(q, K, V, seq_lens, idx, n_sel, scale, out=None, ws=Non
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     _need(out, torch.float32, "out", 3)
+    _kv_shapes(K, V, seq_lens, B, D)
+    _shape(idx, (B, Hkv, kc), "idx")
+    _shape(n_sel, (B, Hkv), "n_sel")
+    _shape(out, (B, Hq, D), "out")
     ws, nbytes = _ws(ws, tf_sparse_decode_attn_workspace(B, Hq, Hkv, kc), q.device)
     _check(load().tf_sparse_decode_attn(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(idx), _ptr(n_sel), B, Hq,
                                         Hkv, Lmax, D, chunk, kc, float(scale), _ptr(out), _ptr(ws), nbytes,
@@ -295,6 +318,12 @@ def tf_retrieval_draft_attn(q, M, K, V, seq_lens, kc, scale, idx=None, n_sel=Non
     _need(out, torch.float32, "out", 3)
     if s_cut is not None:
         _need(s_cut, torch.float32, "s_cut", 2)
+    _kv_shapes(K, V, seq_lens, B, D)
+    _shape(M, (B, Hkv, -(-Lmax // chunk), D), "M")
+    _shape(idx, (B, Hkv, kc), "idx")
+    _shape(n_sel, (B, Hkv), "n_sel")
+    _shape(s_cut, (B, Hkv), "s_cut")
+    _shape(out, (B, Hq, D), "out")
     if cut_hint is None:
         _check(load().tf_retrieval_draft_attn(_ptr(q), _ptr(M), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax,
                                               D, chunk, kc, float(scale), _ptr(idx), _ptr(n_sel), _ptr(s_cut),
@@ -329,6 +358,10 @@ def tf_sparse_verify_attn(Q, K, V, seq_lens, idx, n_sel, scale, out=None, ws=Non
     if out is None:
         out = torch.empty((B, Hq, T, D), dtype=torch.float32, device=Q.device)
     _need(out, torch.float32, "out", 4)
+    _kv_shapes(K, V, seq_lens, B, D)
+    _shape(idx, (B, Hkv, kc), "idx")
+    _shape(n_sel, (B, Hkv), "n_sel")
+    _shape(out, (B, Hq, T, D), "out")
     ws, nbytes = _ws(ws, tf_sparse_verify_attn_workspace(B, Hq, Hkv, kc, T), Q.device)
     _check(load().tf_sparse_verify_attn(_ptr(Q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(idx), _ptr(n_sel), B, Hq,
                                         Hkv, Lmax, D, chunk, kc, T, float(scale), _ptr(out), _ptr(ws), nbytes,
@@ -350,6 +383,10 @@ def tf_sparse_decode_attn_noalloc(q, K, V, seq_lens, idx, n_sel, scale, out, chu
     B, Hq, D = q.shape
     _, Hkv, Lmax, _ = K.shape
     kc = idx.shape[2]
+    _kv_shapes(K, V, seq_lens, B, D)
+    _shape(idx, (B, Hkv, kc), "idx")
+    _shape(n_sel, (B, Hkv), "n_sel")
+    _shape(out, (B, Hq, D), "out")
     _check(load().tf_sparse_decode_attn_noalloc(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(idx), _ptr(n_sel),
                                                 B, Hq, Hkv, Lmax, D, chunk, kc, float(scale), _ptr(out),
                                                 _stream(stream)), "tf_sparse_decode_attn_noalloc")
@@ -370,6 +407,8 @@ def tf_stream_window_attn(q, K, V, seq_lens, n_sink, window, scale, out=None, ws
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     _need(out, torch.float32, "out", 3)
+    _kv_shapes(K, V, seq_lens, B, D)
+    _shape(out, (B, Hq, D), "out")
     ws, nbytes = _ws(ws, tf_stream_window_attn_workspace(B, Hq, Hkv, n_sink, window), q.device)
     _check(load().tf_stream_window_attn(_ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax, D, n_sink,
                                         window, float(scale), _ptr(out), _ptr(ws), nbytes, _stream(stream)),
@@ -391,6 +430,8 @@ def tf_verify_attn(Q, K, V, seq_lens, scale, out=None, ws=None, stream=None):
     if out is None:
         out = torch.empty((B, Hq, T, D), dtype=torch.float32, device=Q.device)
     _need(out, torch.float32, "out", 4)
+    _kv_shapes(K, V, seq_lens, B, D)
+    _shape(out, (B, Hq, T, D), "out")
     ws, nbytes = _ws(ws, tf_verify_attn_workspace(B, Hq, Hkv, Lmax, T), Q.device)
     _check(load().tf_verify_attn(_ptr(Q), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax, D, T, float(scale),
                                  _ptr(out), _ptr(ws), nbytes, _stream(stream)), "tf_verify_attn")
@@ -420,6 +461,9 @@ def tf_verify_window_attn(Q, q, K, V, seq_lens, n_sink, window, scale, out=None,
         wout = torch.empty((B, Hq, D), dtype=torch.float32, device=Q.device)
     _need(out, torch.float32, "out", 4)
     _need(wout, torch.float32, "wout", 3)
+    _kv_shapes(K, V, seq_lens, B, D)
+    _shape(out, (B, Hq, T, D), "out")
+    _shape(wout, (B, Hq, D), "wout")
     ws, nbytes = _ws(ws, tf_verify_window_attn_workspace(B, Hq, Hkv, Lmax, T, n_sink, window), Q.device)
     _check(load().tf_verify_window_attn(_ptr(Q), _ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv, Lmax, D, T,
                                         int(n_sink), int(window), float(scale), _ptr(out), _ptr(wout), _ptr(ws),
@@ -441,6 +485,8 @@ def tf_verify_attn_tree(Q, K, V, seq_lens, parent, scale, out=None, ws=None, str
     if out is None:
         out = torch.empty((B, Hq, T, D), dtype=torch.float32, device=Q.device)
     _need(out, torch.float32, "out", 4)
+    _kv_shapes(K, V, seq_lens, B, D)
+    _shape(out, (B, Hq, T, D), "out")
     ws, nbytes = _ws(ws, tf_verify_attn_workspace(B, Hq, Hkv, Lmax, T), Q.device)
     _check(load().tf_verify_attn_tree(_ptr(Q), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(parent), B, Hq, Hkv, Lmax, D,
                                       T, float(scale), _ptr(out), _ptr(ws), nbytes, _stream(stream)),
@@ -469,6 +515,8 @@ def tf_verify_attn_offload(Q, K_host, V_host, seq_lens, L_stream, scale, out=Non
     if out is None:
         out = torch.empty((B, Hq, T, D), dtype=torch.float32, device=Q.device)
     _need(out, torch.float32, "out", 4)
+    _kv_shapes(K_host, V_host, seq_lens, B, D)
+    _shape(out, (B, Hq, T, D), "out")
     ws, nbytes = _ws(ws, tf_verify_attn_offload_workspace(B, Hq, Hkv, Lmax, T, seg_rows), Q.device)
     cs = _stream(stream)
     xs = cs if copy_stream is None else _stream(copy_stream)
@@ -494,6 +542,8 @@ def tf_spec_accept(tgt_logits, drf_logits, drf_tokens, u_acc, u_res, temperature
         _need(u_acc, torch.float32, "u_acc", 2)
         if tuple(drf_logits.shape) != (B, gamma, Vn) or tuple(drf_tokens.shape) != (B, gamma):
             raise ValueError("draft shapes must be [B, gamma, V] and [B, gamma]")
+        _shape(u_acc, (B, gamma), "u_acc")
+    _shape(u_res, (B,), "u_res")
     dev = tgt_logits.device
     if n_acc is None:
         n_acc = torch.empty((B,), dtype=torch.int32, device=dev)
@@ -501,6 +551,10 @@ def tf_spec_accept(tgt_logits, drf_logits, drf_tokens, u_acc, u_res, temperature
         next_token = torch.empty((B,), dtype=torch.int32, device=dev)
     if out_tokens is None:
         out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    for t, name, shape in ((n_acc, "n_acc", (B,)), (next_token, "next_token", (B,)),
+                           (out_tokens, "out_tokens", (B, gamma + 1))):
+        _need(t, torch.int32, name, len(shape))
+        _shape(t, shape, name)
     ws, nbytes = _ws(ws, tf_spec_accept_workspace(B, gamma), dev)
     _check(load().tf_spec_accept(_ptr(tgt_logits), _ptr(drf_logits if gamma > 0 else None),
                                  _ptr(drf_tokens if gamma > 0 else None), _ptr(u_acc if gamma > 0 else None),
@@ -540,6 +594,11 @@ def tf_spec_accept_tree(tgt_logits, drf_logits, drf_tokens, parent, u_acc, u_res
         out_tokens = torch.empty((B, T + 1), dtype=torch.int32, device=dev)
     if acc_nodes is None:
         acc_nodes = torch.empty((B, max(T, 1)), dtype=torch.int32, device=dev)
+    _shape(u_res, (B,), "u_res")
+    for t, name, shape in ((n_acc, "n_acc", (B,)), (next_token, "next_token", (B,)),
+                           (out_tokens, "out_tokens", (B, T + 1)), (acc_nodes, "acc_nodes", (B, max(T, 1)))):
+        _need(t, torch.int32, name, len(shape))
+        _shape(t, shape, name)
     ws, nbytes = _ws(ws, tf_spec_accept_tree_workspace(B, T, Vn), dev)
     g = T > 0
     _check(load().tf_spec_accept_tree(_ptr(tgt_logits), _ptr(drf_logits if g else None),
