@@ -34,6 +34,8 @@
 //    and writes the output.
 // All waits are bounded; a timeout (only a hardware fault can cause one)
 // leaves NaN in the outputs.
+#include <cuda_bf16.h>
+
 #include "topk_select.cuh"
 
 namespace tf {
@@ -49,16 +51,22 @@ constexpr int kComputeWarps = kWarps;                   // every warp attends
 constexpr int kCutWarps = 8;                            // warps 0..7 finish the cut
 constexpr int kRingSlots = kComputeWarps;               // one slot per warp
 constexpr int kEarlySlots = kComputeWarps - kCutWarps;  // slots of warps 8..15
-constexpr int kSlotBytes = 4096;  // K rows [0, 2 KB), V rows [2 KB, 4 KB)
+// A ring slot holds one chunk's 8 K rows and 8 V rows.  One query head: K
+// rows at [0, 2 KB), V rows at [2 KB, 4 KB), 256 bytes apart.  Two to four
+// heads (tensor-core consumers): rows 272 bytes apart, K from 0 and V from
+// kVOff, so that the eight rows an ldmatrix reads fall in distinct banks.
+constexpr int kPitch = 272;
+constexpr int kVOff = kChunk * kPitch;  // 2176
+constexpr int kSlotBytes = 2 * kVOff;   // 4352
 constexpr int kCandCap = 2048;    // keys of the threshold bin gathered on every CTA
 constexpr int kHintCap = 4096;    // keys above a cut bound gathered on every CTA (over gcand and hist1)
 constexpr int kMaxList = 2048;    // selected chunks per CTA (kc <= kMaxList)
 constexpr uint32_t kIdleLimit = 1u << 22;  // polls for the final list before a warp gives up
 
 // Dynamic shared memory (bytes).
-//  [0, 32768)      ring slots 0..7 (warps 8..15); during round 1 they hold
+//  [0, 34816)      ring slots 0..7 (warps 8..15); during round 1 they hold
 //                  tot, which only this CTA reads
-//  [32768, 65536)  ring slots 8..15 (warps 0..7) once the cut is done;
+//  [34816, 69632)  ring slots 8..15 (warps 0..7) once the cut is done;
 //                  until then hist2, hist3, gcand (the cut group's scratch)
 //                  and hist1 (read by the other CTAs in round 1, which they
 //                  finish before the cut's cluster barrier; with a cut bound
@@ -67,13 +75,13 @@ constexpr uint32_t kIdleLimit = 1u << 22;  // polls for the final list before a 
 //  alist           this CTA's selected chunks (certain ones first)
 //  keys            this CTA's score keys
 constexpr int kOffTot = 0;
-constexpr int kOffHist2 = kEarlySlots * kSlotBytes;  // 32768
-constexpr int kOffHist3 = kOffHist2 + 2048 * 4;      // 40960
-constexpr int kOffGcand = kOffHist3 + 1024 * 4;      // 45056
-constexpr int kOffHist1 = kOffGcand + kCandCap * 4;  // 53248
-constexpr int kOffCand = kRingSlots * kSlotBytes;    // 65536
-constexpr int kOffList = kOffCand + kCandCap * 4;    // 73728
-constexpr int kOffKeys = kOffList + kMaxList * 4;    // 81920
+constexpr int kOffHist2 = kEarlySlots * kSlotBytes;  // 34816
+constexpr int kOffHist3 = kOffHist2 + 2048 * 4;      // 43008
+constexpr int kOffGcand = kOffHist3 + 1024 * 4;      // 47104
+constexpr int kOffHist1 = kOffGcand + kCandCap * 4;  // 55296
+constexpr int kOffCand = kRingSlots * kSlotBytes;    // 69632
+constexpr int kOffList = kOffCand + kCandCap * 4;    // 77824
+constexpr int kOffKeys = kOffList + kMaxList * 4;    // 86016
 static_assert(kOffHist1 + 2048 * 4 <= kOffCand, "the cut's scratch must fit the late slots");
 static_assert(kOffGcand + kHintCap * 4 <= kOffCand, "the hinted gather must fit the late slots");
 static_assert(kOffTot + 2048 * 4 <= kOffHist2, "tot must stay inside the early slots");
@@ -97,6 +105,42 @@ struct DraftParams {
 
 size_t draft_smem(int slice) { return (size_t)kOffKeys + (size_t)slice * sizeof(uint32_t); }
 
+// Warp-level tensor-core fragments (mma.sync: a chunk of 8 keys is far below
+// the 64-row minimum of a tcgen05 tile).  ldsm_x4 / ldsm_x4_t: four 8 x 8
+// 16-bit matrices from shared memory, lane i giving the address of row i % 8
+// of matrix i / 8 (_t: transposed).  mma_s: C += A B for a 16 x 16 A whose
+// rows 8..15 are zero (a0: rows 0..7, k 0..7; a2: k 8..15), B 16 x 8.
+// mma_pv: C += A B for A 16 x 8, B 8 x 8.  bf16 operands, fp32 accumulators.
+__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) {
+  uint32_t u;
+  memcpy(&u, &v, sizeof(u));
+  return u;
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void mma_s(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+               "{%8, %9}, {%0, %1, %2, %3};"
+               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+               : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_pv(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
+               "{%0, %1, %2, %3};"
+               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+               : "r"(a0), "r"(a1), "r"(b0));
+}
+
 // Ring slot of warp w: warps 8..15 take slots 0..7, warps 0..7 (the cut
 // group) slots 8..15.
 __device__ __forceinline__ int slot_of(int warp) { return (warp + kEarlySlots) % kRingSlots; }
@@ -106,6 +150,8 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) float qsm[NQ * kHeadDim];  // scaled query rows, permuted (see below)
   __shared__ float qs[kHeadDim];                      // the group's summed query (scores)
+  // two to four heads: the query rows as bf16, 8 rows (heads past G zero) 272 bytes apart
+  __shared__ __align__(16) uint16_t qbf[NQ >= 2 ? kChunk * kPitch / 2 : 8];
   __shared__ __align__(8) uint64_t bar_full[kRingSlots];
   __shared__ int slot_n[kRingSlots], slot_uses[kRingSlots];
   __shared__ float wm[kComputeWarps][NQ], wl[kComputeWarps][NQ];
@@ -189,6 +235,12 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
     const int u = ((d >> 2) & 1) * 16 + 4 * (d >> 5) + ((d >> 3) & 3);
     qsm[h * kHeadDim + u * 4 + (d & 3)] = v;
   }
+  if constexpr (NQ >= 2) {
+    for (int e = threadIdx.x; e < kChunk * kPitch / 2; e += kThreads) {
+      const int h = e / (kPitch / 2), d = e % (kPitch / 2);
+      qbf[e] = (h < G && d < kHeadDim) ? qg[h * kHeadDim + d] : (uint16_t)0;
+    }
+  }
   __syncthreads();
   topk::score_slice<8>(qs, p.M + (size_t)unit * Cmax * kHeadDim, c0, c1, a, Cmax);
   __syncthreads();
@@ -215,6 +267,28 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
     mbar_arrive_expect_tx(&bar_full[slot], 2 * bytes);
     bulk_load(dst, Ku + (size_t)y * kHeadDim, bytes, &bar_full[slot]);
     bulk_load(dst + 2048, Vu + (size_t)y * kHeadDim, bytes, &bar_full[slot]);
+  };
+  // The same for the tensor-core consumers, by the whole warp: one 256-byte
+  // copy per row (lanes 0..7 the K rows, 8..15 the V rows) into rows kPitch
+  // apart.
+  auto issue_rows = [&](int slot, int c) {
+    const bool ok = c >= 0 && c < C;
+    const int y = ok ? c * kChunk : 0;
+    int nr = ok ? min(kChunk, L - y) : 0;
+    if (ok && !TF_DBG_OK(nr > 0 && y + nr <= L && L <= p.Lmax, kDbgCacheRow)) nr = 0;
+    const int lane_ = threadIdx.x & 31;
+    if (lane_ == 0) {
+      if (!ok) atomicExch(&s_abort, 1);
+      slot_n[slot] = nr;
+      mbar_arrive_expect_tx(&bar_full[slot], (uint32_t)(2 * nr * kHeadDim * 2));
+    }
+    __syncwarp();
+    if (lane_ < 2 * kChunk && (lane_ & (kChunk - 1)) < nr) {
+      const int row = lane_ & (kChunk - 1);
+      fence_proxy_async_smem();  // this slot's earlier generic reads and writes before the copy
+      bulk_load(ring + slot * kSlotBytes + (lane_ >= kChunk ? kVOff : 0) + row * kPitch,
+                (lane_ >= kChunk ? Vu : Ku) + (size_t)(y + row) * kHeadDim, kHeadDim * 2, &bar_full[slot]);
+    }
   };
 
   int32_t* out_idx = p.idx + (size_t)unit * p.kc;
@@ -285,6 +359,15 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
   // ---------------------------------------------------------------- attention
   const int rows = G < NQ ? G : NQ;
   float m[NQ], l[NQ], o[NQ][4];
+  // two to four heads (tensor-core consumers): lane (g, t) = (lane / 4, lane % 4)
+  // keeps the running max and sum of head g, and oc[bk] the output of dims
+  // 16 bk + g and 16 bk + g + 8 for heads 2t and 2t + 1
+  float mh = -INFINITY, lh = 0.0f;
+  float oc[NQ >= 2 ? 8 : 1][4];
+#pragma unroll
+  for (int bk = 0; bk < (NQ >= 2 ? 8 : 1); ++bk)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) oc[bk][i] = 0.0f;
 #pragma unroll
   for (int h = 0; h < NQ; ++h) {
     m[h] = -INFINITY;
@@ -350,13 +433,14 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
             if (i < min(*(volatile int*)&s_ntot, kMaxList)) c = alist[i];
           }
         }
-        if (c != kNoChunk) {
+        if (NQ == 1 && c != kNoChunk) {
           fence_proxy_async_smem();  // the slot's earlier generic reads and writes before the copy
           issue(slot, c);
         }
       }
       c = __shfl_sync(0xffffffffu, c, 0);
       if (c == kNoChunk) break;
+      if constexpr (NQ >= 2) issue_rows(slot, c);
       const uint32_t ph = u & 1;
       ++u;
       if (!mbar_wait(&bar_full[slot], ph)) {
@@ -364,67 +448,131 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
         break;
       }
       const int nr = slot_n[slot];
-      float sa[NQ], sb[NQ];  // two independent partial sums per head
+      if constexpr (NQ == 1) {
+        float sa[NQ], sb[NQ];  // two independent partial sums per head
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int jr = (j + rot) & 3;
-        const uint4 kv = *reinterpret_cast<const uint4*>(kb + r * 256 + dq * 64 + jr * 16);
-        float f[8];
-        unpack8(kv, f);
+        for (int j = 0; j < 4; ++j) {
+          const int jr = (j + rot) & 3;
+          const uint4 kv = *reinterpret_cast<const uint4*>(kb + r * 256 + dq * 64 + jr * 16);
+          float f[8];
+          unpack8(kv, f);
 #pragma unroll
-        for (int h = 0; h < NQ; ++h) {
-          const float4 qa = q4[h * 32 + 4 * dq + jr];
-          const float4 qb = q4[h * 32 + 16 + 4 * dq + jr];
-          float t = qa.x * f[0];
-          t = fmaf(qa.y, f[1], t);
-          t = fmaf(qa.z, f[2], t);
-          t = fmaf(qa.w, f[3], t);
-          t = fmaf(qb.x, f[4], t);
-          t = fmaf(qb.y, f[5], t);
-          t = fmaf(qb.z, f[6], t);
-          t = fmaf(qb.w, f[7], t);
-          if (j == 0) sa[h] = t;
-          else if (j == 1) sb[h] = t;
-          else if (j == 2) sa[h] += t;
-          else sb[h] += t;
+          for (int h = 0; h < NQ; ++h) {
+            const float4 qa = q4[h * 32 + 4 * dq + jr];
+            const float4 qb = q4[h * 32 + 16 + 4 * dq + jr];
+            float t = qa.x * f[0];
+            t = fmaf(qa.y, f[1], t);
+            t = fmaf(qa.z, f[2], t);
+            t = fmaf(qa.w, f[3], t);
+            t = fmaf(qb.x, f[4], t);
+            t = fmaf(qb.y, f[5], t);
+            t = fmaf(qb.z, f[6], t);
+            t = fmaf(qb.w, f[7], t);
+            if (j == 0) sa[h] = t;
+            else if (j == 1) sb[h] = t;
+            else if (j == 2) sa[h] += t;
+            else sb[h] += t;
+          }
         }
-      }
-      const bool valid = r < nr;
-      float pr[NQ];
-#pragma unroll
-      for (int h = 0; h < NQ; ++h) {
-        float s = sa[h] + sb[h];
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        s += __shfl_xor_sync(0xffffffffu, s, 2);
-        s = valid ? s : -INFINITY;
-        float cmx = s;
-        cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 4));
-        cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 8));
-        cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 16));
-        const float mn = fmaxf(m[h], cmx);
-        const float alpha = merge_scale(m[h], mn);
-        pr[h] = (s == -INFINITY) ? 0.0f : exp2f(s - mn);
-        float ps = pr[h];
-        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-        l[h] = l[h] * alpha + ps;
-        m[h] = mn;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[h][i] *= alpha;
-      }
-      // P V: lane owns head dims [4 lane, 4 lane + 4) of every row
-      for (int rr = 0; rr < nr; ++rr) {
-        const uint2 vv = *reinterpret_cast<const uint2*>(vb + rr * 256 + lane * 8);
-        const float v0 = __uint_as_float(vv.x << 16), v1 = __uint_as_float(vv.x & 0xffff0000u);
-        const float v2 = __uint_as_float(vv.y << 16), v3 = __uint_as_float(vv.y & 0xffff0000u);
+        const bool valid = r < nr;
+        float pr[NQ];
 #pragma unroll
         for (int h = 0; h < NQ; ++h) {
-          const float pw = __shfl_sync(0xffffffffu, pr[h], rr * 4);  // lane 4 rr holds row rr
-          o[h][0] = fmaf(pw, v0, o[h][0]);
-          o[h][1] = fmaf(pw, v1, o[h][1]);
-          o[h][2] = fmaf(pw, v2, o[h][2]);
-          o[h][3] = fmaf(pw, v3, o[h][3]);
+          float s = sa[h] + sb[h];
+          s += __shfl_xor_sync(0xffffffffu, s, 1);
+          s += __shfl_xor_sync(0xffffffffu, s, 2);
+          s = valid ? s : -INFINITY;
+          float cmx = s;
+          cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 4));
+          cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 8));
+          cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 16));
+          const float mn = fmaxf(m[h], cmx);
+          const float alpha = merge_scale(m[h], mn);
+          pr[h] = (s == -INFINITY) ? 0.0f : exp2f(s - mn);
+          float ps = pr[h];
+          ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+          ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+          ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+          l[h] = l[h] * alpha + ps;
+          m[h] = mn;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[h][i] *= alpha;
+        }
+        // P V: lane owns head dims [4 lane, 4 lane + 4) of every row
+        for (int rr = 0; rr < nr; ++rr) {
+          const uint2 vv = *reinterpret_cast<const uint2*>(vb + rr * 256 + lane * 8);
+          const float v0 = __uint_as_float(vv.x << 16), v1 = __uint_as_float(vv.x & 0xffff0000u);
+          const float v2 = __uint_as_float(vv.y << 16), v3 = __uint_as_float(vv.y & 0xffff0000u);
+#pragma unroll
+          for (int h = 0; h < NQ; ++h) {
+            const float pw = __shfl_sync(0xffffffffu, pr[h], rr * 4);  // lane 4 rr holds row rr
+            o[h][0] = fmaf(pw, v0, o[h][0]);
+            o[h][1] = fmaf(pw, v1, o[h][1]);
+            o[h][2] = fmaf(pw, v2, o[h][2]);
+            o[h][3] = fmaf(pw, v3, o[h][3]);
+          }
+        }
+      } else if (nr > 0) {
+        // S[h][key] = q_h . K_key on the tensor cores (heads as rows, zero past
+        // G), then the online softmax per head and O^T += V^T P^T with P split
+        // into bf16 hi and lo parts (P to 2^-17, as the verify kernel does)
+        const int t4 = lane & 3;
+        const uint32_t kaddr = smem_u32(ring + slot * kSlotBytes);
+        const uint32_t vaddr = kaddr + kVOff;
+        const uint32_t qaddr = smem_u32(qbf);
+        if (nr < kChunk) {
+          // rows past the chunk's end may hold anything: zero them in V so
+          // that 0 * V stays 0 (their scores are masked below)
+          uint8_t* vrow = ring + slot * kSlotBytes + kVOff;
+          for (int e = lane; e < (kChunk - nr) * 16; e += 32)
+            *reinterpret_cast<uint4*>(vrow + (nr + (e >> 4)) * kPitch + (e & 15) * 16) = make_uint4(0, 0, 0, 0);
+          __syncwarp();
+        }
+        const uint32_t row_off = (uint32_t)((lane & 7) * kPitch + (lane >> 3) * 16);
+        float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int ks = 0; ks < kHeadDim / 16; ks += 2) {  // 32 dims per step
+          uint32_t qa[4], kf[4];
+          ldsm_x4(qa, qaddr + row_off + ks * 32);
+          ldsm_x4(kf, kaddr + row_off + ks * 32);
+          mma_s(sc, qa[0], qa[1], kf[0], kf[1]);
+          mma_s(sc, qa[2], qa[3], kf[2], kf[3]);
+        }
+        // this lane: head g8, keys 2 t4 and 2 t4 + 1
+        const float s0 = (2 * t4 < nr) ? sc[0] * p.scale_log2 : -INFINITY;
+        const float s1 = (2 * t4 + 1 < nr) ? sc[1] * p.scale_log2 : -INFINITY;
+        float cmx = fmaxf(s0, s1);
+        cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 1));
+        cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 2));
+        const float mn = fmaxf(mh, cmx);
+        const float alpha = merge_scale(mh, mn);
+        const float p0 = (s0 == -INFINITY) ? 0.0f : exp2f(s0 - mn);
+        const float p1 = (s1 == -INFINITY) ? 0.0f : exp2f(s1 - mn);
+        float ps = p0 + p1;
+        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        lh = lh * alpha + ps;
+        mh = mn;
+        // this lane's outputs belong to heads 2 t4 and 2 t4 + 1
+        const float ae = __shfl_sync(0xffffffffu, alpha, 8 * t4);
+        const float ao = __shfl_sync(0xffffffffu, alpha, 8 * t4 + 4);
+        const __nv_bfloat162 ph2 = __floats2bfloat162_rn(p0, p1);
+        const __nv_bfloat162 pl2 = __floats2bfloat162_rn(p0 - __low2float(ph2), p1 - __high2float(ph2));
+        const uint32_t bh = bf16x2_bits(ph2), bl = bf16x2_bits(pl2);
+#pragma unroll
+        for (int bk = 0; bk < 8; bk += 2) {  // 32 dims per step
+          uint32_t va[4];
+          ldsm_x4_t(va, vaddr + row_off + bk * 32);
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            float (&cc)[4] = oc[bk + hb];
+            cc[0] *= ae;
+            cc[1] *= ao;
+            cc[2] *= ae;
+            cc[3] *= ao;
+            mma_pv(cc, va[2 * hb], va[2 * hb + 1], bh);
+            mma_pv(cc, va[2 * hb], va[2 * hb + 1], bl);
+          }
         }
       }
       __syncwarp();
@@ -441,14 +589,32 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
   }
   __syncthreads();
   float* wo = reinterpret_cast<float*>(ring);  // [kComputeWarps][NQ][128]
+  if constexpr (NQ == 1) {
 #pragma unroll
-  for (int h = 0; h < NQ; ++h) {
-    if (lane == 0) {
-      wm[warp][h] = m[h];
-      wl[warp][h] = l[h];
+    for (int h = 0; h < NQ; ++h) {
+      if (lane == 0) {
+        wm[warp][h] = m[h];
+        wl[warp][h] = l[h];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) wo[(warp * NQ + h) * kHeadDim + lane * 4 + i] = o[h][i];
+    }
+  } else {
+    const int g8 = lane >> 2, t4 = lane & 3;
+    if (t4 == 0 && g8 < NQ) {
+      wm[warp][g8] = mh;
+      wl[warp][g8] = lh;
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) wo[(warp * NQ + h) * kHeadDim + lane * 4 + i] = o[h][i];
+    for (int bk = 0; bk < 8; ++bk)
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const int h = 2 * t4 + hb;
+        if (h < NQ) {
+          wo[(warp * NQ + h) * kHeadDim + 16 * bk + g8] = oc[bk][hb];
+          wo[(warp * NQ + h) * kHeadDim + 16 * bk + g8 + 8] = oc[bk][2 + hb];
+        }
+      }
   }
   __syncthreads();
 
