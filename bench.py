@@ -333,6 +333,17 @@ def graph_loop_ms(calls, stream, replays=5):
     return ms
 
 
+def window_launches(G, T):
+    """Launches tf_verify_window_attn makes for G query heads per KV head and T
+    verify tokens: one when the G window rows fill padding rows of the verify
+    kernel (no more 32-row groups, no wider group rounded up to 8 rows), else
+    two (the library's rule; tests compare it with the workspace sizes)."""
+    groups = lambda r: -(-r // 32)
+    width = lambda r: -(-min(r, 32) // 8)
+    fits = groups(G * (T + 1)) == groups(G * T) and width(G * (T + 1)) == width(G * T)
+    return 1 if fits else 2
+
+
 N_QUERY_SETS = 4   # consecutive steps cycle through this many seeded query sets
 HINT_SCALE = 0.7  # the draft's cut bound: the previous step's cut of the layer x 0.7
 
@@ -381,10 +392,7 @@ class StepState:
         self.ws_win = tf.workspace(tf.tf_stream_window_attn_workspace(B, Hq, Hkv, w.n_sink, w.window), dev)
         self.ws_ver = tf.workspace(tf.tf_verify_attn_workspace(B, Hq, Hkv, L, T), dev)
         self.ws_vw = tf.workspace(tf.tf_verify_window_attn_workspace(B, Hq, Hkv, L, T, w.n_sink, w.window), dev)
-        G = Hq // Hkv
-        # one launch when the window rows fill padding rows of the verify kernel (the library's rule)
-        fits = (-(-G * (T + 1) // 32) == -(-G * T // 32)) and (-(-min(G * (T + 1), 32) // 8) == -(-min(G * T, 32) // 8))
-        self.vw_launches = 1 if fits else 2
+        self.vw_launches = window_launches(Hq // Hkv, T)
         torch.cuda.synchronize()
 
     def bytes_per_launch(self):

@@ -7,6 +7,7 @@ the ABI version, workspace-size queries and host-side argument validation.
 import ctypes
 import os
 import re
+import sys
 
 import pytest
 
@@ -197,3 +198,19 @@ def test_binding_rejects_cpu_tensors():
     with pytest.raises(TypeError, match="CUDA"):
         binding.tf_build_chunk_means(K, torch.zeros(1, dtype=torch.int32), torch.zeros((1, 1, 1, 128),
                                                                                       dtype=torch.bfloat16))
+
+
+def test_bench_mirrors_the_one_launch_rule(lib):
+    """bench.py counts tf_verify_window_attn's launches with its own copy of the
+    library's rule; the workspace query tells the two paths apart (one launch:
+    the verify scratch of G*(T+1) rows; two: the verify scratch of G*T rows plus
+    the window's)."""
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    for G in (1, 2, 3, 4, 5, 6, 8):
+        for T in range(1, 17):
+            one = lib.tf_verify_window_attn_workspace(1, 2 * G, 2, 64, T, 4, 252) == \
+                lib.tf_verify_attn_workspace(1, 2 * G, 2, 64, T + 1)
+            assert one == (bench.window_launches(G, T) == 1), (G, T)
+    assert bench.window_launches(1, 6) == 1 and bench.window_launches(4, 6) == 2

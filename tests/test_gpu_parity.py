@@ -270,13 +270,14 @@ def test_stream_window_attn(cuda_lib, w):
 
 
 @pytest.mark.parametrize("w", [synth.TINY, small_workload(), small_workload(Hkv=8, T=6, L=3000, L_min=2000),
-                               small_workload(T=5),
+                               small_workload(T=5), small_workload(Hq=8, Hkv=4, T=5),
                                small_workload(B=1, Hq=16, Hkv=2, T=4, L=900, ragged=False),
                                small_workload(B=2, Hq=8, Hkv=2, T=16, L=700, L_min=100),
                                small_workload(T=5, L=40000, L_min=30000),
                                small_workload(B=2, Hq=16, Hkv=2, T=5, L=40000, L_min=30000),
                                small_workload(B=2, Hq=16, Hkv=2, T=4, L=40000, L_min=30000)],
-                         ids=["tiny", "gqa-two-launches", "mha-6", "gqa-t5-padding-rows", "own-group-two-launches",
+                         ids=["tiny", "gqa-two-launches", "mha-6", "gqa-t5-padding-rows", "g2-t5-padding-rows",
+                              "own-group-two-launches",
                               "three-groups-two-launches", "split", "window-warpgroup-split",
                               "own-group-two-launches-split"])
 def test_verify_window_attn(cuda_lib, w):
