@@ -90,7 +90,9 @@ TF_API int tf_abi_version(void);
  * workspace again, in `stream` order, so the workspace can be reused, and
  * returns TF_ERR_DEVICE_DATA.  ws is device memory of ws_bytes >= 4 bytes
  * (TF_ERR_INVALID_ARG otherwise, nothing read); TF_ERR_CUDA if the copy, the
- * clearing or the wait fails. */
+ * clearing or the wait fails.  It takes the workspace, not only the stream:
+ * the library keeps no global state, so the status lives in the caller's
+ * workspace. */
 TF_API tf_status tf_check_status(void* ws, size_t ws_bytes, tf_stream_t stream);
 
 /* Bounds violations recorded by the checked build of this library
