@@ -124,6 +124,8 @@ def test_host_validation_rejects_before_launch(lib):
     vsz = lib.tf_verify_attn_workspace(1, 8, 2, 64, 8)
     assert vw(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 4, 252, 0.1, fake, fake, fake, vsz,
               None) == WORKSPACE  # room for the verify scratch only
+    assert vw(fake, fake, fake, fake, fake, 0, 8, 2, 64, 128, 6, 4, 252, 0.1, fake, fake, null, 0,
+              None) == 0  # empty batch: nothing to do, nothing launched
     assert lib.tf_verify_window_attn_workspace(1, 8, 2, 64, 6, -1, 252) == 0
     # the same with a cut hint (before idx): required, and the same limits
     hd = lib.tf_retrieval_draft_attn_hinted
