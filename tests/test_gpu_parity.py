@@ -490,3 +490,26 @@ def test_verify_tree_special_shapes(cuda_lib):
     c["seq_cpu"] = torch.tensor([5, 1200], dtype=torch.int32)
     tree = random_tree(w.B, w.T, seed=1)
     assert np.abs(run(tree).cpu().double().numpy() - want_of(tree)).max() <= ATOL
+
+
+@pytest.mark.parametrize("w", [small_workload(), small_workload(Hkv=8, T=6, L=3000, L_min=2000)],
+                         ids=["gqa-two-launches", "mha-one-launch"])
+def test_verify_window_attn_in_cuda_graph(cuda_lib, w):
+    """Captured once and replayed, the call (one launch, or the window launch
+    and the verify launch on one workspace) gives the eager call's outputs bit
+    for bit."""
+    c = make_case(w)
+    ws = cuda_lib.workspace(cuda_lib.tf_verify_window_attn_workspace(w.B, w.Hq, w.Hkv, w.L, w.T, w.n_sink, w.window),
+                            "cuda")
+    out, wout = cuda_lib.tf_verify_window_attn(c["Q"], c["q"], c["K"], c["V"], c["seq"], w.n_sink, w.window, 0.1, ws=ws)
+    g_out, g_wout = torch.empty_like(out), torch.empty_like(wout)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cuda_lib.tf_verify_window_attn(c["Q"], c["q"], c["K"], c["V"], c["seq"], w.n_sink, w.window, 0.1, out=g_out,
+                                       wout=g_wout, ws=ws)
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(g_out, out) and torch.equal(g_wout, wout)
+    assert cuda_lib.tf_check_status(ws) == 0
