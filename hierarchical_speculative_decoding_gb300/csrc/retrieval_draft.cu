@@ -690,10 +690,9 @@ tf_status launch_draft(const DraftParams& p, int units, int Cmax, cudaStream_t s
   // Cluster size: the largest S <= 16 (at most one CTA per 64 chunks) for
   // which every unit's cluster is resident at once, as the occupancy query for
   // that cluster shape and slice size reports; at least enough CTAs that every
-  // slice fits on chip.  With 32 units that is S = 9: 288 CTAs, two on each of
-  // 144 SMs, so every slice streams at the same rate (S = 8 leaves some CTAs
-  // alone on an SM and the others paired, and each cluster waits for its
-  // paired members).
+  // slice fits on chip.  On a GB300 (two CTAs per SM) 36 clusters of 8, 30 of
+  // 9 and 14 of 16 are resident at once, so 32 units take S = 8 (256 CTAs on
+  // 128 SMs).
   const int need = (Cmax + kMaxSliceKeys - 1) / kMaxSliceKeys;
   if (need > kMaxCluster) return TF_ERR_UNSUPPORTED;
   int most = (Cmax + 63) / 64;
