@@ -5,7 +5,8 @@ Same launch configuration as the benchmark: the whole layer (every unit) goes
 through each call; the oracle recomputes a few units, always including the
 first and last KV head and, for ragged batches, the longest and the shortest
 sequence.  The offloaded verify streams the same cache from pinned host
-memory in the benchmark's 16K-position segments.  Tolerances as in test_gpu_parity.py.
+memory in the benchmark's 16K-position segments; the window + verify call runs as
+the benchmark's step runs it.  Tolerances as in test_gpu_parity.py.
 """
 
 import numpy as np
@@ -51,6 +52,7 @@ def test_full_size_layer(cuda_lib, w):
     sp = cuda_lib.tf_sparse_decode_attn(q, K, V, seq, idx, nsel, scale)
     wi = cuda_lib.tf_stream_window_attn(q, K, V, seq, w.n_sink, w.window, scale)
     ve = cuda_lib.tf_verify_attn(Q, K, V, seq, scale)
+    vw_v, vw_w = cuda_lib.tf_verify_window_attn(Q, q, K, V, seq, w.n_sink, w.window, scale)  # as the bench step
     fidx, fnsel, fsp = cuda_lib.tf_retrieval_draft_attn(q, M, K, V, seq, w.kc, scale)
     sv = cuda_lib.tf_sparse_verify_attn(Q, K, V, seq, idx, nsel, scale)
     # offloaded verify as timed: pinned host K/V, 16K-position segments, copies on a side stream
@@ -69,6 +71,7 @@ def test_full_size_layer(cuda_lib, w):
     M_h, idx_h, nsel_h = bits(M), idx.cpu().numpy(), nsel.cpu().numpy()
     sp_h, wi_h, ve_h = sp.cpu().double().numpy(), wi.cpu().double().numpy(), ve.cpu().double().numpy()
     sv_h, off_h = sv.cpu().double().numpy(), off.cpu().double().numpy()
+    vwv_h, vww_h = vw_v.cpu().double().numpy(), vw_w.cpu().double().numpy()
     q_h, Q_h = bits(q), bits(Q)
     G = w.G
     near_ties = 0
@@ -96,10 +99,12 @@ def test_full_size_layer(cuda_lib, w):
         # a6
         wi_o = O.stream_window_attn(qg, Kb, Vb, sl, w.n_sink, w.window, scale)
         assert np.abs(wi_h[b, g * G : (g + 1) * G] - wi_o[0]).max() <= ATOL
+        assert np.abs(vww_h[b, g * G : (g + 1) * G] - wi_o[0]).max() <= ATOL
         # a7
         ve_o = O.verify_attn(Q_h[b : b + 1, g * G : (g + 1) * G], Kb, Vb, sl, scale)
         assert np.abs(ve_h[b, g * G : (g + 1) * G] - ve_o[0]).max() <= ATOL
         assert np.abs(off_h[b, g * G : (g + 1) * G] - ve_o[0]).max() <= ATOL
+        assert np.abs(vwv_h[b, g * G : (g + 1) * G] - ve_o[0]).max() <= ATOL
         # level-1 verify over the GPU's own selection
         sv_o = O.sparse_verify_attn(Q_h[b : b + 1, g * G : (g + 1) * G], Kb, Vb, sl,
                                     idx_h[b : b + 1, g : g + 1], nsel_h[b : b + 1, g : g + 1], w.chunk, scale)
