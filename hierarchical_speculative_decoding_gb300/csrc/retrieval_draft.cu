@@ -36,6 +36,7 @@
 // leaves NaN in the outputs.
 #include <cuda_bf16.h>
 
+#include "tma_host.cuh"
 #include "topk_select.cuh"
 
 namespace tf {
@@ -51,22 +52,24 @@ constexpr int kComputeWarps = kWarps;                   // every warp attends
 constexpr int kCutWarps = 8;                            // warps 0..7 finish the cut
 constexpr int kRingSlots = kComputeWarps;               // one slot per warp
 constexpr int kEarlySlots = kComputeWarps - kCutWarps;  // slots of warps 8..15
-// A ring slot holds one chunk's 8 K rows and 8 V rows.  One query head: K
-// rows at [0, 2 KB), V rows at [2 KB, 4 KB), 256 bytes apart.  Two to four
-// heads (tensor-core consumers): rows 272 bytes apart, K from 0 and V from
-// kVOff, so that the eight rows an ldmatrix reads fall in distinct banks.
-constexpr int kPitch = 272;
-constexpr int kVOff = kChunk * kPitch;  // 2176
-constexpr int kSlotBytes = 2 * kVOff;   // 4352
+// A ring slot holds one chunk's 8 K rows at [0, 2 KB) and its 8 V rows at
+// [2 KB, 4 KB).  One query head: rows 256 bytes apart (one bulk copy each).
+// Two to four heads (tensor-core consumers): each 2 KB piece is two 1 KB
+// swizzle atoms (dims 0..63, 64..127; 16-byte unit u of row r at
+// r * 128 + ((u ^ r) * 16)), written by one TMA box, so that the eight rows an
+// ldmatrix reads fall in distinct banks.
+constexpr int kSlotBytes = 4096;
+constexpr int kQPitch = 272;  // bytes between the bf16 query rows (conflict-free ldmatrix)
 constexpr int kCandCap = 2048;    // keys of the threshold bin gathered on every CTA
 constexpr int kHintCap = 4096;    // keys above a cut bound gathered on every CTA (over gcand and hist1)
 constexpr int kMaxList = 2048;    // selected chunks per CTA (kc <= kMaxList)
 constexpr uint32_t kIdleLimit = 1u << 22;  // polls for the final list before a warp gives up
 
 // Dynamic shared memory (bytes).
-//  [0, 34816)      ring slots 0..7 (warps 8..15); during round 1 they hold
+// (from a 1 KB-aligned base, so that every slot starts a swizzle atom)
+//  [0, 32768)      ring slots 0..7 (warps 8..15); during round 1 they hold
 //                  tot, which only this CTA reads
-//  [34816, 69632)  ring slots 8..15 (warps 0..7) once the cut is done;
+//  [32768, 65536)  ring slots 8..15 (warps 0..7) once the cut is done;
 //                  until then hist2, hist3, gcand (the cut group's scratch)
 //                  and hist1 (read by the other CTAs in round 1, which they
 //                  finish before the cut's cluster barrier; with a cut bound
@@ -75,13 +78,13 @@ constexpr uint32_t kIdleLimit = 1u << 22;  // polls for the final list before a 
 //  alist           this CTA's selected chunks (certain ones first)
 //  keys            this CTA's score keys
 constexpr int kOffTot = 0;
-constexpr int kOffHist2 = kEarlySlots * kSlotBytes;  // 34816
-constexpr int kOffHist3 = kOffHist2 + 2048 * 4;      // 43008
-constexpr int kOffGcand = kOffHist3 + 1024 * 4;      // 47104
-constexpr int kOffHist1 = kOffGcand + kCandCap * 4;  // 55296
-constexpr int kOffCand = kRingSlots * kSlotBytes;    // 69632
-constexpr int kOffList = kOffCand + kCandCap * 4;    // 77824
-constexpr int kOffKeys = kOffList + kMaxList * 4;    // 86016
+constexpr int kOffHist2 = kEarlySlots * kSlotBytes;  // 32768
+constexpr int kOffHist3 = kOffHist2 + 2048 * 4;      // 40960
+constexpr int kOffGcand = kOffHist3 + 1024 * 4;      // 45056
+constexpr int kOffHist1 = kOffGcand + kCandCap * 4;  // 53248
+constexpr int kOffCand = kRingSlots * kSlotBytes;    // 65536
+constexpr int kOffList = kOffCand + kCandCap * 4;    // 73728
+constexpr int kOffKeys = kOffList + kMaxList * 4;    // 81920
 static_assert(kOffHist1 + 2048 * 4 <= kOffCand, "the cut's scratch must fit the late slots");
 static_assert(kOffGcand + kHintCap * 4 <= kOffCand, "the hinted gather must fit the late slots");
 static_assert(kOffTot + 2048 * 4 <= kOffHist2, "tot must stay inside the early slots");
@@ -101,9 +104,11 @@ struct DraftParams {
   const float* hint;  // [B, Hkv] lower bounds on the cut scores, or null (NaN: none for that unit)
   int nseq;           // B
   int longest_first;  // 1: block row r serves the sequence with the r-th longest context (B <= 64)
+  CUtensorMap mapK, mapV;  // two to four heads: 8-row pieces of K and V as [B * Hkv * Lmax, 128] boxes
 };
 
-size_t draft_smem(int slice) { return (size_t)kOffKeys + (size_t)slice * sizeof(uint32_t); }
+// + 1 KB to align the base
+size_t draft_smem(int slice) { return 1024 + (size_t)kOffKeys + (size_t)slice * sizeof(uint32_t); }
 
 // Warp-level tensor-core fragments (mma.sync: a chunk of 8 keys is far below
 // the 64-row minimum of a tcgen05 tile).  ldsm_x4 / ldsm_x4_t: four 8 x 8
@@ -146,12 +151,13 @@ __device__ __forceinline__ void mma_pv(float (&c)[4], uint32_t a0, uint32_t a1, 
 __device__ __forceinline__ int slot_of(int warp) { return (warp + kEarlySlots) % kRingSlots; }
 
 template <int NQ>
-__global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __grid_constant__ DraftParams p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* const smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(16) float qsm[NQ * kHeadDim];  // scaled query rows, permuted (see below)
   __shared__ float qs[kHeadDim];                      // the group's summed query (scores)
   // two to four heads: the query rows as bf16, 8 rows (heads past G zero) 272 bytes apart
-  __shared__ __align__(16) uint16_t qbf[NQ >= 2 ? kChunk * kPitch / 2 : 8];
+  __shared__ __align__(16) uint16_t qbf[NQ >= 2 ? kChunk * kQPitch / 2 : 8];
   __shared__ __align__(8) uint64_t bar_full[kRingSlots];
   __shared__ int slot_n[kRingSlots], slot_uses[kRingSlots];
   __shared__ float wm[kComputeWarps][NQ], wl[kComputeWarps][NQ];
@@ -236,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
     qsm[h * kHeadDim + u * 4 + (d & 3)] = v;
   }
   if constexpr (NQ >= 2) {
-    for (int e = threadIdx.x; e < kChunk * kPitch / 2; e += kThreads) {
-      const int h = e / (kPitch / 2), d = e % (kPitch / 2);
+    for (int e = threadIdx.x; e < kChunk * kQPitch / 2; e += kThreads) {
+      const int h = e / (kQPitch / 2), d = e % (kQPitch / 2);
       qbf[e] = (h < G && d < kHeadDim) ? qg[h * kHeadDim + d] : (uint16_t)0;
     }
   }
@@ -268,27 +274,25 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
     bulk_load(dst, Ku + (size_t)y * kHeadDim, bytes, &bar_full[slot]);
     bulk_load(dst + 2048, Vu + (size_t)y * kHeadDim, bytes, &bar_full[slot]);
   };
-  // The same for the tensor-core consumers, by the whole warp: one 256-byte
-  // copy per row (lanes 0..7 the K rows, 8..15 the V rows) into rows kPitch
-  // apart.
-  auto issue_rows = [&](int slot, int c) {
+  // The same for the tensor-core consumers (lane 0): one TMA box for the K
+  // piece and one for the V piece, always 8 rows (rows past the context hold
+  // whatever the cache holds there, zero past its end; they are masked below)
+  auto issue_tma = [&](int slot, int c) {
     const bool ok = c >= 0 && c < C;
     const int y = ok ? c * kChunk : 0;
     int nr = ok ? min(kChunk, L - y) : 0;
     if (ok && !TF_DBG_OK(nr > 0 && y + nr <= L && L <= p.Lmax, kDbgCacheRow)) nr = 0;
-    const int lane_ = threadIdx.x & 31;
-    if (lane_ == 0) {
-      if (!ok) atomicExch(&s_abort, 1);
-      slot_n[slot] = nr;
-      mbar_arrive_expect_tx(&bar_full[slot], (uint32_t)(2 * nr * kHeadDim * 2));
+    if (!ok) atomicExch(&s_abort, 1);
+    slot_n[slot] = nr;
+    if (nr == 0) {
+      mbar_arrive(&bar_full[slot]);
+      return;
     }
-    __syncwarp();
-    if (lane_ < 2 * kChunk && (lane_ & (kChunk - 1)) < nr) {
-      const int row = lane_ & (kChunk - 1);
-      fence_proxy_async_smem();  // this slot's earlier generic reads and writes before the copy
-      bulk_load(ring + slot * kSlotBytes + (lane_ >= kChunk ? kVOff : 0) + row * kPitch,
-                (lane_ >= kChunk ? Vu : Ku) + (size_t)(y + row) * kHeadDim, kHeadDim * 2, &bar_full[slot]);
-    }
+    uint8_t* dst = ring + slot * kSlotBytes;
+    const int row = (int)((size_t)unit * p.Lmax + y);
+    mbar_arrive_expect_tx(&bar_full[slot], (uint32_t)kSlotBytes);
+    tma_load_3d(dst, &p.mapK, &bar_full[slot], 0, row, 0);
+    tma_load_3d(dst + 2048, &p.mapV, &bar_full[slot], 0, row, 0);
   };
 
   int32_t* out_idx = p.idx + (size_t)unit * p.kc;
@@ -433,14 +437,14 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
             if (i < min(*(volatile int*)&s_ntot, kMaxList)) c = alist[i];
           }
         }
-        if (NQ == 1 && c != kNoChunk) {
+        if (c != kNoChunk) {
           fence_proxy_async_smem();  // the slot's earlier generic reads and writes before the copy
-          issue(slot, c);
+          if constexpr (NQ == 1) issue(slot, c);
+          else issue_tma(slot, c);
         }
       }
       c = __shfl_sync(0xffffffffu, c, 0);
       if (c == kNoChunk) break;
-      if constexpr (NQ >= 2) issue_rows(slot, c);
       const uint32_t ph = u & 1;
       ++u;
       if (!mbar_wait(&bar_full[slot], ph)) {
@@ -518,23 +522,30 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
         // into bf16 hi and lo parts (P to 2^-17, as the verify kernel does)
         const int t4 = lane & 3;
         const uint32_t kaddr = smem_u32(ring + slot * kSlotBytes);
-        const uint32_t vaddr = kaddr + kVOff;
+        const uint32_t vaddr = kaddr + 2048;
         const uint32_t qaddr = smem_u32(qbf);
         if (nr < kChunk) {
           // rows past the chunk's end may hold anything: zero them in V so
           // that 0 * V stays 0 (their scores are masked below)
-          uint8_t* vrow = ring + slot * kSlotBytes + kVOff;
+          uint8_t* vp = ring + slot * kSlotBytes + 2048;
           for (int e = lane; e < (kChunk - nr) * 16; e += 32)
-            *reinterpret_cast<uint4*>(vrow + (nr + (e >> 4)) * kPitch + (e & 15) * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vp + ((e >> 3) & 1) * 1024 + (nr + (e >> 4)) * 128 + (e & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
           __syncwarp();
         }
-        const uint32_t row_off = (uint32_t)((lane & 7) * kPitch + (lane >> 3) * 16);
+        // ldmatrix row addresses: lane = (matrix m = lane / 8, row r = lane % 8);
+        // 16-byte unit u of a piece row sits in atom u / 8 at ((u % 8) ^ r) * 16
+        const int lr = lane & 7, lm = lane >> 3;
+        auto piece_addr = [&](uint32_t base, int u) -> uint32_t {
+          return base + (uint32_t)((u >> 3) * 1024 + lr * 128 + (((u & 7) ^ lr) << 4));
+        };
+        const uint32_t q_off = (uint32_t)(lr * kQPitch + lm * 16);
         float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int ks = 0; ks < kHeadDim / 16; ks += 2) {  // 32 dims per step
           uint32_t qa[4], kf[4];
-          ldsm_x4(qa, qaddr + row_off + ks * 32);
-          ldsm_x4(kf, kaddr + row_off + ks * 32);
+          ldsm_x4(qa, qaddr + q_off + ks * 32);
+          ldsm_x4(kf, piece_addr(kaddr, 2 * ks + lm));
           mma_s(sc, qa[0], qa[1], kf[0], kf[1]);
           mma_s(sc, qa[2], qa[3], kf[2], kf[3]);
         }
@@ -562,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(DraftParam
 #pragma unroll
         for (int bk = 0; bk < 8; bk += 2) {  // 32 dims per step
           uint32_t va[4];
-          ldsm_x4_t(va, vaddr + row_off + bk * 32);
+          ldsm_x4_t(va, piece_addr(vaddr, 2 * bk + lm));
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb) {
             float (&cc)[4] = oc[bk + hb];
@@ -767,6 +778,11 @@ tf_status draft_entry(const uint16_t* q, const uint16_t* M, const uint16_t* K, c
   DraftParams p{q, M, K, V, seq_lens, Hq, Hkv, Lmax, kc, scale * kLog2e, idx, n_sel, s_cut, out, hint,
                 B, (B > 1 && B <= 64) ? 1 : 0};
   const int G = Hq / Hkv;
+  if (G >= 2 && Lmax > 0) {
+    const long long rows_total = (long long)units * Lmax;
+    if (rows_total >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
+    if (!make_piece_map(&p.mapK, K, rows_total) || !make_piece_map(&p.mapV, V, rows_total)) return TF_ERR_CUDA;
+  }
   switch (G) {
     case 1: return launch_draft<1>(p, units, Cmax < 1 ? 1 : Cmax, stream);
     case 2: return launch_draft<2>(p, units, Cmax < 1 ? 1 : Cmax, stream);

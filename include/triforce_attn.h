@@ -209,7 +209,8 @@ TF_API tf_status tf_sparse_decode_attn_noalloc(const uint16_t* q, const uint16_t
  *   out [B, Hq, D] float32  as tf_sparse_decode_attn over that selection.
  * Scores, the selection and the split-K partial states stay on chip (one
  * thread-block cluster per (b, g)), so there is no workspace.  Limits:
- * kc <= 2048, Hq / Hkv <= 4, contexts up to 8 x 16384 chunks (else
+ * kc <= 2048, Hq / Hkv <= 4, contexts up to 8 x 16384 chunks, and for
+ * Hq / Hkv >= 2 (chunks loaded by TMA) B * Hkv * Lmax < 2^31 (else
  * TF_ERR_UNSUPPORTED; the two separate calls have no such limits).  Device
  * pointers, 16-byte aligned q, M, K, V and out.
  */
