@@ -21,14 +21,16 @@
 //    streaming while the cut is resolved.
 //  * Each warp owns one 4 KB ring slot and stages its own chunks: lane 0
 //    claims the next list entry (a shared counter), copies the chunk's K and V
-//    rows into the slot (cp.async.bulk) and the warp waits for them; entries
-//    past the certain ones are read once the cut group has published the final
+//    rows into the slot (one query head: cp.async.bulk; two to four: two TMA
+//    boxes in the 128-byte swizzle) and the warp waits for them; entries past
+//    the certain ones are read once the cut group has published the final
 //    list.  No hand-over between warps: a slot is free again as soon as its
 //    warp has read it.
-//  * Consumer lane (row r, quarter dq) forms 32-dim dot products with the
-//    query rows held in shared memory in a bank-conflict-free permuted layout;
-//    the online softmax runs in the log2 domain in fp32 and each lane owns 4
-//    head dims of P V.
+//  * One query head: consumer lane (row r, quarter dq) forms 32-dim dot
+//    products with the query row held in shared memory in a bank-conflict-free
+//    permuted layout, and owns 4 head dims of P V.  Two to four heads: the
+//    warp runs Q K^T and P V on the tensor cores (mma.sync fragments).  The
+//    online softmax runs in the log2 domain in fp32.
 //  * Warps merge in shared memory, then CTA rank 0 merges the S partial states
 //    of the cluster through distributed shared memory (log-sum-exp identity)
 //    and writes the output.
