@@ -54,6 +54,11 @@ def test_full_size_layer(cuda_lib, w):
     ve = cuda_lib.tf_verify_attn(Q, K, V, seq, scale)
     vw_v, vw_w = cuda_lib.tf_verify_window_attn(Q, q, K, V, seq, w.n_sink, w.window, scale)  # as the bench step
     fidx, fnsel, fsp = cuda_lib.tf_retrieval_draft_attn(q, M, K, V, seq, w.kc, scale)
+    # the benchmark's bound: 0.7 x the cut of another seeded query set
+    q_other, _ = synth.decode_queries(w, 1000, device="cuda")
+    cut_other = torch.empty((w.B, w.Hkv), dtype=torch.float32, device="cuda")
+    cuda_lib.tf_retrieval_draft_attn(q_other, M, K, V, seq, w.kc, scale, s_cut=cut_other)
+    hidx, hnsel, hsp = cuda_lib.tf_retrieval_draft_attn(q, M, K, V, seq, w.kc, scale, cut_hint=cut_other * 0.7)
     sv = cuda_lib.tf_sparse_verify_attn(Q, K, V, seq, idx, nsel, scale)
     # offloaded verify as timed: pinned host K/V, 16K-position segments, copies on a side stream
     K_host = torch.empty(K.shape, dtype=K.dtype, pin_memory=True).copy_(K)
@@ -67,6 +72,10 @@ def test_full_size_layer(cuda_lib, w):
     # the fused retrieval drafter selects exactly what the top-k call selects
     assert np.array_equal(fidx.cpu().numpy(), idx.cpu().numpy())
     assert np.array_equal(fnsel.cpu().numpy(), nsel.cpu().numpy())
+    # ... with or without the bound
+    assert np.array_equal(hidx.cpu().numpy(), idx.cpu().numpy())
+    assert np.array_equal(hnsel.cpu().numpy(), nsel.cpu().numpy())
+    hsp_h = hsp.cpu().double().numpy()
     fsp_h = fsp.cpu().double().numpy()
     M_h, idx_h, nsel_h = bits(M), idx.cpu().numpy(), nsel.cpu().numpy()
     sp_h, wi_h, ve_h = sp.cpu().double().numpy(), wi.cpu().double().numpy(), ve.cpu().double().numpy()
@@ -96,6 +105,7 @@ def test_full_size_layer(cuda_lib, w):
                                     w.chunk, scale)
         assert np.abs(sp_h[b, g * G : (g + 1) * G] - sp_o[0]).max() <= ATOL
         assert np.abs(fsp_h[b, g * G : (g + 1) * G] - sp_o[0]).max() <= ATOL
+        assert np.abs(hsp_h[b, g * G : (g + 1) * G] - sp_o[0]).max() <= ATOL
         # a6
         wi_o = O.stream_window_attn(qg, Kb, Vb, sl, w.n_sink, w.window, scale)
         assert np.abs(wi_h[b, g * G : (g + 1) * G] - wi_o[0]).max() <= ATOL
