@@ -393,6 +393,9 @@ class StepState:
         self.ws_ver = tf.workspace(tf.tf_verify_attn_workspace(B, Hq, Hkv, L, T), dev)
         self.ws_vw = tf.workspace(tf.tf_verify_window_attn_workspace(B, Hq, Hkv, L, T, w.n_sink, w.window), dev)
         self.vw_launches = window_launches(Hq // Hkv, T)
+        # where the window rows do not fit the verify launch, two to four query heads take the window
+        # attention in the drafter's launch instead (tf_retrieval_window_draft_attn)
+        self.window_in_draft = self.vw_launches == 2 and 2 <= Hq // Hkv <= 4
         torch.cuda.synchronize()
 
     def bytes_per_launch(self):
@@ -418,7 +421,9 @@ class StepState:
         return {
             "topk": means + B * Hq * D * 2 + ids,
             "sparse": 2 * sel_rows * row + ids + q_io,
-            "draft": means + ids + 2 * sel_rows * row + q_io,
+            "draft": means + ids + 2 * sel_rows * row + q_io + (
+                sum(2 * Hkv * min(x, w.n_sink + w.window) * row for x in lens) + B * Hq * D * 4
+                if self.window_in_draft else 0),
             "window": sum(2 * Hkv * min(x, w.n_sink + w.window) * row for x in lens) + q_io,
             # in one launch the window rows read keys the verify rows read anyway: only their queries
             # and outputs add
@@ -438,7 +443,8 @@ def make_step(st, tf, two_call, stream, hinted=True, split_window=False):
     import torch
 
     w = st.w
-    split = split_window and st.vw_launches == 2
+    wid = st.window_in_draft and not two_call  # the window attention in the drafter's launch
+    split = split_window and st.vw_launches == 2 and not wid
     kinds = ("draft", "window", "verify") if split else ("draft", "verify")
     hinted = hinted and not two_call
 
@@ -448,6 +454,11 @@ def make_step(st, tf, two_call, stream, hinted=True, split_window=False):
             tf.tf_chunk_scores_topk(q[l], st.M[l], st.seq, w.L, w.kc, st.idx[l], st.nsel[l], ws=st.ws_topk)
             tf.tf_sparse_decode_attn(q[l], st.K[l], st.V[l], st.seq, st.idx[l], st.nsel[l], st.scale,
                                      out=st.o_sp[l], ws=st.ws_sp)
+        elif wid:
+            tf.tf_retrieval_window_draft_attn(q[l], st.M[l], st.K[l], st.V[l], st.seq, w.kc, st.scale, w.n_sink,
+                                              w.window, idx=st.idx[l], n_sel=st.nsel[l], out=st.o_sp[l],
+                                              wout=st.o_win[l], s_cut=st.cut[l],
+                                              cut_hint=st.hint[l] if hinted else None)
         else:
             tf.tf_retrieval_draft_attn(q[l], st.M[l], st.K[l], st.V[l], st.seq, w.kc, st.scale, idx=st.idx[l],
                                        n_sel=st.nsel[l], out=st.o_sp[l], s_cut=st.cut[l],
@@ -469,6 +480,8 @@ def make_step(st, tf, two_call, stream, hinted=True, split_window=False):
                                          out=st.o_win[l], ws=st.ws_win)
                 if evs is not None:
                     evs[l][2].record(stream)
+                tf.tf_verify_attn(Q[l], st.K[l], st.V[l], st.seq, st.scale, out=st.o_ver[l], ws=st.ws_ver)
+            elif wid:
                 tf.tf_verify_attn(Q[l], st.K[l], st.V[l], st.seq, st.scale, out=st.o_ver[l], ws=st.ws_ver)
             else:
                 tf.tf_verify_window_attn(Q[l], q[l], st.K[l], st.V[l], st.seq, w.n_sink, w.window, st.scale,
@@ -559,8 +572,25 @@ def breakdown_cycle(st, tf, args, stream, k):
 
 
 def verify_label(st):
-    return ("tf_verify_window_attn (one launch: the window rows inside the verify launch)" if st.vw_launches == 1
-            else "tf_verify_attn, after tf_stream_window_attn (the two launches tf_verify_window_attn makes here)")
+    if st.vw_launches == 1:
+        return "tf_verify_window_attn (one launch: the window rows inside the verify launch)"
+    if st.window_in_draft:
+        return "tf_verify_attn (the window attention rides in the drafter's launch)"
+    return "tf_verify_attn, after tf_stream_window_attn (the two launches tf_verify_window_attn makes here)"
+
+
+def draft_label(st, two_call):
+    if two_call:
+        return "tf_chunk_scores_topk + tf_sparse_decode_attn"
+    if st.window_in_draft:
+        return "tf_retrieval_window_draft_attn (scores, top-k, sparse and window attention in one launch)"
+    return "tf_retrieval_draft_attn"
+
+
+def launches_per_layer(st, two_call):
+    if two_call:
+        return 2 + st.vw_launches
+    return 2 if st.window_in_draft else 1 + st.vw_launches
 
 
 def per_kernel_times(step, layers, k_steps, kinds):
@@ -672,6 +702,7 @@ def measure_extra_workload(w, args, tf, synth, dev, stream, world, local, peak):
         name = "retrieval_draft" if k == "draft" else k
         kern[name] = kernel_entry(nb[k], statistics.mean(per_kind[k]), peak)
     kern["verify"]["calls"] = verify_label(st)
+    kern["retrieval_draft"]["calls"] = draft_label(st, args.two_call_draft)
     kern["retrieval_draft"]["back_to_back"] = kernel_entry(nb["draft"], draft_back_to_back_ms(st, draft, cyc, stream),
                                                            peak)
     kern["sparse_verify_level1"] = measure_level1(st, w, tf, dev, stream, peak)
@@ -686,7 +717,7 @@ def measure_extra_workload(w, args, tf, synth, dev, stream, world, local, peak):
                         "unit": "GB/s", "frac": ver["frac_hbm"], "algorithmic_bytes": nb["verify"],
                         "traffic": recorded_traffic("verify_attn.cu", w.name)},
            "kernels": kern, "clocks": clocks,
-           "gpu_launches": steps * st.layers * ((2 if args.two_call_draft else 1) + st.vw_launches)}
+           "gpu_launches": steps * st.layers * launches_per_layer(st, args.two_call_draft)}
     if cold is not None:
         out["cold_start"] = cold
     kern["retrieval_draft"]["traffic"] = None if args.two_call_draft else recorded_traffic("retrieval_draft.cu",
@@ -867,8 +898,7 @@ def run_gpu(args):
     for k in kinds_k:
         name = "retrieval_draft" if k == "draft" else k
         kernels[name] = kernel_entry(nb[k], statistics.mean(per_kind[k]), peak)
-    kernels["retrieval_draft"]["calls"] = ("tf_chunk_scores_topk + tf_sparse_decode_attn" if args.two_call_draft
-                                           else "tf_retrieval_draft_attn")
+    kernels["retrieval_draft"]["calls"] = draft_label(st, args.two_call_draft)
     kernels["retrieval_draft"]["traffic"] = (None if args.two_call_draft
                                              else recorded_traffic("retrieval_draft.cu", w.name))
     # the two-call form of the retrieval drafter, for comparison: each call back to back over the
@@ -944,7 +974,7 @@ def run_gpu(args):
                      "algorithmic_bytes": nb["verify"], "peak_source": peak_kind},
         "kernels": kernels,
         "kernel_timing": f"CUDA events around every launch, {k_steps} further steps after the timed region",
-        "gpu_launches": args.steps * layers * ((2 if args.two_call_draft else 1) + st.vw_launches),
+        "gpu_launches": args.steps * layers * launches_per_layer(st, args.two_call_draft),
         "clocks": clocks,
     }
 

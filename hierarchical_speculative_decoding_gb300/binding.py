@@ -39,6 +39,8 @@ _SIGS = {
     "tf_verify_window_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _S, _P]),
     "tf_retrieval_draft_attn_hinted": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P,
                                             _P]),
+    "tf_retrieval_window_draft_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _I, _I, _P, _P,
+                                            _P, _P, _P, _P]),
     "tf_stream_window_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
     "tf_stream_window_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _S, _P]),
     "tf_sparse_verify_attn_workspace": (_S, [_I, _I, _I, _I, _I]),
@@ -337,6 +339,49 @@ def tf_retrieval_draft_attn(q, M, K, V, seq_lens, kc, scale, idx=None, n_sel=Non
                                                      _ptr(n_sel), _ptr(s_cut), _ptr(out), _stream(stream)),
                "tf_retrieval_draft_attn_hinted")
     return idx, n_sel, out
+
+
+def tf_retrieval_window_draft_attn(q, M, K, V, seq_lens, kc, scale, n_sink, window, idx=None, n_sel=None,
+                                   s_cut=None, out=None, wout=None, chunk=8, stream=None, cut_hint=None):
+    """The retrieval drafter (as tf_retrieval_draft_attn, cut_hint optional) and
+    the sink + window attention of the same queries in one launch, for 2 to 4
+    query heads per KV head.  Returns (idx, n_sel, out, wout [B, Hq, D])."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(M, torch.bfloat16, "M", 4)
+    _need(K, torch.bfloat16, "K", 4)
+    _need(V, torch.bfloat16, "V", 4)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, Hq, D = q.shape
+    _, Hkv, Lmax, _ = K.shape
+    if idx is None:
+        idx = torch.empty((B, Hkv, kc), dtype=torch.int32, device=q.device)
+    if n_sel is None:
+        n_sel = torch.empty((B, Hkv), dtype=torch.int32, device=q.device)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if wout is None:
+        wout = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    _need(idx, torch.int32, "idx", 3)
+    _need(n_sel, torch.int32, "n_sel", 2)
+    _need(out, torch.float32, "out", 3)
+    _need(wout, torch.float32, "wout", 3)
+    if s_cut is not None:
+        _need(s_cut, torch.float32, "s_cut", 2)
+    if cut_hint is not None:
+        _need(cut_hint, torch.float32, "cut_hint", 2)
+    _kv_shapes(K, V, seq_lens, B, D)
+    _shape(M, (B, Hkv, -(-Lmax // chunk), D), "M")
+    _shape(idx, (B, Hkv, kc), "idx")
+    _shape(n_sel, (B, Hkv), "n_sel")
+    _shape(s_cut, (B, Hkv), "s_cut")
+    _shape(cut_hint, (B, Hkv), "cut_hint")
+    _shape(out, (B, Hq, D), "out")
+    _shape(wout, (B, Hq, D), "wout")
+    _check(load().tf_retrieval_window_draft_attn(_ptr(q), _ptr(M), _ptr(K), _ptr(V), _ptr(seq_lens), B, Hq, Hkv,
+                                                 Lmax, D, chunk, kc, float(scale), _ptr(cut_hint), int(n_sink),
+                                                 int(window), _ptr(idx), _ptr(n_sel), _ptr(s_cut), _ptr(out),
+                                                 _ptr(wout), _stream(stream)), "tf_retrieval_window_draft_attn")
+    return idx, n_sel, out, wout
 
 
 def tf_sparse_verify_attn_workspace(B, Hq, Hkv, kc, T):

@@ -107,6 +107,10 @@ struct DraftParams {
   int nseq;           // B
   int longest_first;  // 1: block row r serves the sequence with the r-th longest context (B <= 64)
   CUtensorMap mapK, mapV;  // two to four heads: 8-row pieces of K and V as [B * Hkv * Lmax, 128] boxes
+  // optional, two to four heads: the sink + window attention of the same
+  // queries, written to wout [B, Hq, 128] (null: none)
+  float* wout;
+  int n_sink, window;
 };
 
 // + 1 KB to align the base
@@ -162,8 +166,12 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
   __shared__ __align__(16) uint16_t qbf[NQ >= 2 ? kChunk * kQPitch / 2 : 8];
   __shared__ __align__(8) uint64_t bar_full[kRingSlots];
   __shared__ int slot_n[kRingSlots], slot_uses[kRingSlots];
-  __shared__ float wm[kComputeWarps][NQ], wl[kComputeWarps][NQ];
-  __shared__ float cpart[NQ][kHeadDim], cm[NQ], cl[NQ];
+  // rows of a warp's state: the heads (NQ), or for the tensor-core consumers
+  // the 8 fragment rows: heads 0..3, then the window rows 4..7
+  constexpr int kRowsW = NQ >= 2 ? 8 : NQ;
+  __shared__ float wm[kComputeWarps][kRowsW], wl[kComputeWarps][kRowsW];
+  __shared__ float cpart[kRowsW][kHeadDim], cm[kRowsW], cl[kRowsW];
+  __shared__ uint8_t slot_win[kRingSlots];  // 1: the slot holds a window piece
   __shared__ uint32_t s_min;
   __shared__ int s_na, s_ntot, s_abort, s_hcnt, s_next;
   __shared__ int s_hroff[kMaxCluster + 1];
@@ -246,7 +254,9 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
   if constexpr (NQ >= 2) {
     for (int e = threadIdx.x; e < kChunk * kQPitch / 2; e += kThreads) {
       const int h = e / (kQPitch / 2), d = e % (kQPitch / 2);
-      qbf[e] = (h < G && d < kHeadDim) ? qg[h * kHeadDim + d] : (uint16_t)0;
+      // rows 0..G-1 the heads; with a window output rows 4..4+G-1 the same heads again
+      const int hq = h < G ? h : ((p.wout && h >= 4 && h - 4 < G) ? h - 4 : -1);
+      qbf[e] = (hq >= 0 && d < kHeadDim) ? qg[hq * kHeadDim + d] : (uint16_t)0;
     }
   }
   __syncthreads();
@@ -255,6 +265,23 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
 
   const uint16_t* Ku = p.K + (size_t)unit * p.Lmax * kHeadDim;
   const uint16_t* Vu = p.V + (size_t)unit * p.Lmax * kHeadDim;
+  // window pieces of this unit (with a window output): the sinks
+  // [0, ns_eff) and the recent keys [w0, L) in pieces of up to 8 rows; list
+  // entry -1 - k is piece k
+  const bool win = NQ >= 2 && p.wout != nullptr;
+  const int ns_eff = min(p.n_sink, L), w0 = max(p.n_sink, L - p.window);
+  const int n_sp = (ns_eff + kChunk - 1) / kChunk;
+  const int n_pw = win ? n_sp + (max(L - w0, 0) + kChunk - 1) / kChunk : 0;
+  auto piece = [&](int k, int& y, int& nr) {
+    if (k < n_sp) {
+      y = k * kChunk;
+      nr = min(kChunk, ns_eff - y);
+    } else {
+      y = w0 + (k - n_sp) * kChunk;
+      nr = min(kChunk, L - y);
+    }
+  };
+
   // Stage chunk c (its valid rows of K and of V) into a ring slot.  An id
   // outside [0, C) cannot come out of the selection; it is refused all the
   // same (the slot completes empty and the outputs are poisoned) rather than
@@ -280,12 +307,21 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
   // piece and one for the V piece, always 8 rows (rows past the context hold
   // whatever the cache holds there, zero past its end; they are masked below)
   auto issue_tma = [&](int slot, int c) {
-    const bool ok = c >= 0 && c < C;
-    const int y = ok ? c * kChunk : 0;
-    int nr = ok ? min(kChunk, L - y) : 0;
-    if (ok && !TF_DBG_OK(nr > 0 && y + nr <= L && L <= p.Lmax, kDbgCacheRow)) nr = 0;
+    // a chunk id, or -1 - k for window piece k
+    int y = 0, nr = 0;
+    const bool ok = c >= 0 ? c < C : (-1 - c) < n_pw;
+    if (ok) {
+      if (c >= 0) {
+        y = c * kChunk;
+        nr = min(kChunk, L - y);
+      } else {
+        piece(-1 - c, y, nr);
+      }
+    }
+    if (ok && !TF_DBG_OK(nr > 0 && y >= 0 && y + nr <= L && L <= p.Lmax, kDbgCacheRow)) nr = 0;
     if (!ok) atomicExch(&s_abort, 1);
     slot_n[slot] = nr;
+    slot_win[slot] = c < 0 ? 1 : 0;
     if (nr == 0) {
       mbar_arrive(&bar_full[slot]);
       return;
@@ -358,6 +394,24 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
           if (at < kMaxList) alist[at] = c0 + i;
         }
       });
+    }
+  }
+  if (win) {
+    // this CTA's window pieces (k = rank, rank + S, ...), known before the cut:
+    // appended to the certain entries while the cut runs (split), else to
+    // the final list
+    __syncthreads();
+    const int base = split ? s_na : s_ntot;
+    const int mine = n_pw > (int)rank ? (n_pw - (int)rank + S - 1) / S : 0;
+    if (base + mine > kMaxList) {
+      if (threadIdx.x == 0) atomicExch(&s_abort, 1);  // cannot happen within the host's limits
+    } else {
+      for (int j = threadIdx.x; j < mine; j += kThreads) alist[base + j] = -1 - ((int)rank + j * S);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && base + mine <= kMaxList) {
+      if (split) s_na = base + mine;
+      s_ntot = base + mine;
     }
   }
   __syncthreads();
@@ -551,9 +605,11 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
           mma_s(sc, qa[0], qa[1], kf[0], kf[1]);
           mma_s(sc, qa[2], qa[3], kf[2], kf[3]);
         }
-        // this lane: head g8, keys 2 t4 and 2 t4 + 1
-        const float s0 = (2 * t4 < nr) ? sc[0] * p.scale_log2 : -INFINITY;
-        const float s1 = (2 * t4 + 1 < nr) ? sc[1] * p.scale_log2 : -INFINITY;
+        // this lane: row g8 (heads 0..3, window rows 4..7), keys 2 t4 and 2 t4 + 1;
+        // a chunk feeds the head rows, a window piece the window rows
+        const bool row_on = slot_win[slot] ? (lane >> 2) >= 4 : (lane >> 2) < 4;
+        const float s0 = (row_on && 2 * t4 < nr) ? sc[0] * p.scale_log2 : -INFINITY;
+        const float s1 = (row_on && 2 * t4 + 1 < nr) ? sc[1] * p.scale_log2 : -INFINITY;
         float cmx = fmaxf(s0, s1);
         cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 1));
         cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 2));
@@ -610,11 +666,11 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
         wl[warp][h] = l[h];
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) wo[(warp * NQ + h) * kHeadDim + lane * 4 + i] = o[h][i];
+      for (int i = 0; i < 4; ++i) wo[(warp * kRowsW + h) * kHeadDim + lane * 4 + i] = o[h][i];
     }
   } else {
     const int g8 = lane >> 2, t4 = lane & 3;
-    if (t4 == 0 && g8 < NQ) {
+    if (t4 == 0) {
       wm[warp][g8] = mh;
       wl[warp][g8] = lh;
     }
@@ -623,24 +679,25 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {
         const int h = 2 * t4 + hb;
-        if (h < NQ) {
-          wo[(warp * NQ + h) * kHeadDim + 16 * bk + g8] = oc[bk][hb];
-          wo[(warp * NQ + h) * kHeadDim + 16 * bk + g8 + 8] = oc[bk][2 + hb];
-        }
+        wo[(warp * kRowsW + h) * kHeadDim + 16 * bk + g8] = oc[bk][hb];
+        wo[(warp * kRowsW + h) * kHeadDim + 16 * bk + g8 + 8] = oc[bk][2 + hb];
       }
   }
   __syncthreads();
 
-  // ---- this CTA's partial state: merge the compute warps
-  for (int e = threadIdx.x; e < rows * kHeadDim; e += kThreads) {
-    const int h = e / kHeadDim, d = e % kHeadDim;
+  // ---- this CTA's partial state: merge the compute warps (the head rows,
+  // then with a window output the window rows 4..)
+  const int nrows = win ? 2 * rows : rows;
+  auto row_of = [&](int i) { return i < rows ? i : 4 + (i - rows); };
+  for (int e = threadIdx.x; e < nrows * kHeadDim; e += kThreads) {
+    const int h = row_of(e / kHeadDim), d = e % kHeadDim;
     float mx = -INFINITY;
     for (int w = 0; w < kComputeWarps; ++w) mx = fmaxf(mx, wm[w][h]);
     float ls = 0.0f, os = 0.0f;
     for (int w = 0; w < kComputeWarps; ++w) {
       const float f = merge_scale(wm[w][h], mx);
       ls = fmaf(f, wl[w][h], ls);
-      os = fmaf(f, wo[(w * NQ + h) * kHeadDim + d], os);
+      os = fmaf(f, wo[(w * kRowsW + h) * kHeadDim + d], os);
     }
     cpart[h][d] = os;
     if (d == 0) {
@@ -654,9 +711,9 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
   if (rank == 0) {
     bool bad = false;
     for (int rr = 0; rr < S; ++rr) bad |= dsmem_ld_u32(&s_abort, (uint32_t)rr) != 0;
-    float* outp = p.out + ((size_t)b * p.Hq + (size_t)g * G) * kHeadDim;
-    for (int e = threadIdx.x; e < rows * kHeadDim; e += kThreads) {
-      const int h = e / kHeadDim, d = e % kHeadDim;
+    const size_t orow = ((size_t)b * p.Hq + (size_t)g * G) * kHeadDim;
+    for (int e = threadIdx.x; e < nrows * kHeadDim; e += kThreads) {
+      const int h = row_of(e / kHeadDim), d = e % kHeadDim;
       float mr[kMaxCluster];
 #pragma unroll
       for (int rr = 0; rr < kMaxCluster; ++rr)
@@ -673,7 +730,8 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
           os = fmaf(f, __uint_as_float(dsmem_ld_u32(&cpart[h][d], (uint32_t)rr)), os);
         }
       }
-      outp[h * kHeadDim + d] = bad ? NAN : (ls > 0.0f ? os / ls : 0.0f);
+      float* dst = h < 4 ? p.out + orow + (size_t)h * kHeadDim : p.wout + orow + (size_t)(h - 4) * kHeadDim;
+      dst[d] = bad ? NAN : (ls > 0.0f ? os / ls : 0.0f);
     }
     if (threadIdx.x == 0) {
       if (C <= p.kc) {
@@ -767,7 +825,7 @@ namespace {
 tf_status draft_entry(const uint16_t* q, const uint16_t* M, const uint16_t* K, const uint16_t* V,
                       const int32_t* seq_lens, int B, int Hq, int Hkv, int Lmax, int D, int chunk, int kc, float scale,
                       int32_t* idx, int32_t* n_sel, float* s_cut, float* out, const float* hint,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, float* wout = nullptr, int n_sink = 0, int window = 0) {
   if (!q || !M || !K || !V || !seq_lens || !idx || !n_sel || !out) return TF_ERR_INVALID_ARG;
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || kc <= 0 || Hq % Hkv != 0) return TF_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(M) || !aligned16(K) || !aligned16(V) || !aligned16(out)) return TF_ERR_INVALID_ARG;
@@ -779,6 +837,9 @@ tf_status draft_entry(const uint16_t* q, const uint16_t* M, const uint16_t* K, c
   const int Cmax = (Lmax + kChunk - 1) / kChunk;
   DraftParams p{q, M, K, V, seq_lens, Hq, Hkv, Lmax, kc, scale * kLog2e, idx, n_sel, s_cut, out, hint,
                 B, (B > 1 && B <= 64) ? 1 : 0};
+  p.wout = wout;
+  p.n_sink = n_sink;
+  p.window = window;
   const int G = Hq / Hkv;
   if (G >= 2 && Lmax > 0) {
     const long long rows_total = (long long)units * Lmax;
@@ -801,6 +862,23 @@ extern "C" tf_status tf_retrieval_draft_attn(const uint16_t* q, const uint16_t* 
                                              int32_t* n_sel, float* s_cut, float* out, tf_stream_t stream) {
   return tf::draft_entry(q, M, K, V, seq_lens, B, Hq, Hkv, Lmax, D, chunk, kc, scale, idx, n_sel, s_cut, out,
                          nullptr, (cudaStream_t)stream);
+}
+
+extern "C" tf_status tf_retrieval_window_draft_attn(const uint16_t* q, const uint16_t* M, const uint16_t* K,
+                                                    const uint16_t* V, const int32_t* seq_lens, int B, int Hq,
+                                                    int Hkv, int Lmax, int D, int chunk, int kc, float scale,
+                                                    const float* cut_hint, int n_sink, int window, int32_t* idx,
+                                                    int32_t* n_sel, float* s_cut, float* out, float* wout,
+                                                    tf_stream_t stream) {
+  using namespace tf;
+  if (!wout || !aligned16(wout) || n_sink < 0 || window < 0) return TF_ERR_INVALID_ARG;
+  if (Hkv <= 0 || Hq % Hkv != 0) return TF_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  // a CTA lists its selected chunks and its share of the window pieces
+  const long long pieces = ((long long)n_sink + kChunk - 1) / kChunk + ((long long)window + kChunk - 1) / kChunk + 1;
+  if (G < 2 || G > 4 || (long long)kc + pieces > kMaxList) return TF_ERR_UNSUPPORTED;
+  return draft_entry(q, M, K, V, seq_lens, B, Hq, Hkv, Lmax, D, chunk, kc, scale, idx, n_sel, s_cut, out, cut_hint,
+                     (cudaStream_t)stream, wout, n_sink, window);
 }
 
 extern "C" tf_status tf_retrieval_draft_attn_hinted(const uint16_t* q, const uint16_t* M, const uint16_t* K,

@@ -245,6 +245,30 @@ TF_API tf_status tf_retrieval_draft_attn_hinted(const uint16_t* q, const uint16_
                                                 float* s_cut, float* out, tf_stream_t stream);
 
 /*
+ * a2 + a3 + a4 and a6 in one launch, for GQA groups (2 <= Hq / Hkv <= 4):
+ * tf_retrieval_draft_attn (cut_hint as tf_retrieval_draft_attn_hinted; NULL:
+ * no bound) plus tf_stream_window_attn of the same decode queries q over the
+ * same cache ("TriForce: Hierarchical Speculative Decoding for LLMs", "The
+ * Three Forces of TriForce": Force 1's sinks + recent window and Force 2's
+ * retrieved blocks, both drafters' attention for the same token).  The
+ * window's keys, [0, min(n_sink, L)) and [max(n_sink, L - window), L), enter
+ * the drafter's chunk lists as 8-row pieces, and its rows ride in the spare
+ * rows of the drafter's tensor-core fragments, so the window needs no launch
+ * of its own.  Outputs: idx, n_sel, s_cut, out as tf_retrieval_draft_attn;
+ * wout [B, Hq, 128] fp32 as tf_stream_window_attn (within the attention
+ * tolerance).  Limits: those of tf_retrieval_draft_attn, Hq / Hkv from 2 to
+ * 4, and kc + ceil(n_sink / 8) + ceil(window / 8) + 1 <= 2048 (else
+ * TF_ERR_UNSUPPORTED).  Errors: NULL or misaligned wout, negative n_sink or
+ * window -> TF_ERR_INVALID_ARG; otherwise as tf_retrieval_draft_attn.
+ */
+TF_API tf_status tf_retrieval_window_draft_attn(const uint16_t* q, const uint16_t* M, const uint16_t* K,
+                                  const uint16_t* V, const int32_t* seq_lens,
+                                  int B, int Hq, int Hkv, int Lmax, int D, int chunk, int kc,
+                                  float scale, const float* cut_hint, int n_sink, int window,
+                                  int32_t* idx, int32_t* n_sel, float* s_cut, float* out,
+                                  float* wout, tf_stream_t stream);
+
+/*
  * Level-1 verification over the retrieval cache:
  * the retrieval drafter -- the target model over the retrieved KV blocks --
  * checks the tiny drafter's candidates in one pass ("TriForce: Hierarchical

@@ -127,6 +127,18 @@ def test_host_validation_rejects_before_launch(lib):
     assert vw(fake, fake, fake, fake, fake, 0, 8, 2, 64, 128, 6, 4, 252, 0.1, fake, fake, null, 0,
               None) == 0  # empty batch: nothing to do, nothing launched
     assert lib.tf_verify_window_attn_workspace(1, 8, 2, 64, 6, -1, 252) == 0
+    # retrieval draft + window in one launch: ... scale, hint, n_sink, window, idx, n_sel, s_cut, out, wout, stream
+    wd = lib.tf_retrieval_window_draft_attn
+    assert wd(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 64, 0.1, null, 4, 252, fake, fake, null, fake,
+              null, None) == INVALID  # no window output
+    assert wd(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 64, 0.1, null, -1, 252, fake, fake, null, fake,
+              fake, None) == INVALID  # negative sink count
+    assert wd(fake, fake, fake, fake, fake, 1, 8, 8, 64, 128, 8, 64, 0.1, null, 4, 252, fake, fake, null, fake,
+              fake, None) == UNSUPPORTED  # one query head: the window rides in the verify launch instead
+    assert wd(fake, fake, fake, fake, fake, 1, 16, 2, 64, 128, 8, 64, 0.1, null, 4, 252, fake, fake, null, fake,
+              fake, None) == UNSUPPORTED  # eight query heads per KV head
+    assert wd(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 2020, 0.1, null, 4, 252, fake, fake, null, fake,
+              fake, None) == UNSUPPORTED  # the chunk list cannot take kc chunks plus the window pieces
     # the same with a cut hint (before idx): required, and the same limits
     hd = lib.tf_retrieval_draft_attn_hinted
     assert hd(fake, fake, fake, fake, fake, 1, 8, 2, 64, 128, 8, 64, 0.1, null, fake, fake, null, fake,

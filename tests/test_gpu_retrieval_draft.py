@@ -264,3 +264,59 @@ def test_retrieval_draft_cut_hint_one_cta_over_its_list(cuda_lib):
     idx, nsel, cut, out = _hinted(cuda_lib, w, c, M, torch.full((1, 1), float(bound)).cuda(), 512)
     assert np.array_equal(idx, idx0) and np.array_equal(cut.view(np.uint32), cut0.view(np.uint32))
     assert np.abs(out - out0).max() <= ATOL
+
+
+@pytest.mark.parametrize("w", [
+    small_workload(),
+    small_workload(B=2, Hq=8, Hkv=4, L=20000, budget=8 * 512, L_min=17000),
+    small_workload(B=3, Hq=6, Hkv=2, L=5000, budget=8 * 37, L_min=9),
+    small_workload(B=2, Hq=8, Hkv=2, L=600, budget=8 * 100, ragged=False),
+], ids=["gqa4-ragged", "g2", "g3-short", "all-selected"])
+@pytest.mark.parametrize("hinted", [False, True], ids=["cold", "bounded"])
+def test_retrieval_window_draft(cuda_lib, w, hinted):
+    """The drafter and the window in one launch: the selection is the plain
+    call's bit for bit, the attention over it and the window attention match
+    the oracle."""
+    c = make_case(w, fill_invalid=float("nan") if w.ragged else None)
+    scale = scale_for(w.D)
+    M = torch.empty((w.B, w.Hkv, -(-w.L // w.chunk), w.D), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.tf_build_chunk_means(c["K"], c["seq"], M)
+    s_cut = torch.empty((w.B, w.Hkv), dtype=torch.float32, device="cuda")
+    idx0, nsel0, _ = cuda_lib.tf_retrieval_draft_attn(c["q"], M, c["K"], c["V"], c["seq"], w.kc, scale, s_cut=s_cut)
+    hint = (s_cut - 0.3 * s_cut.abs()) if hinted else None
+    idx, nsel, out, wout = cuda_lib.tf_retrieval_window_draft_attn(c["q"], M, c["K"], c["V"], c["seq"], w.kc, scale,
+                                                                   w.n_sink, w.window, cut_hint=hint)
+    torch.cuda.synchronize()
+    idx_h, nsel_h = idx.cpu().numpy(), nsel.cpu().numpy()
+    assert np.array_equal(idx_h, idx0.cpu().numpy()) and np.array_equal(nsel_h, nsel0.cpu().numpy())
+    seq = c["seq_cpu"].numpy()
+    want = O.sparse_decode_attn(bits(c["q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), seq, idx_h, nsel_h, w.chunk,
+                                scale)
+    assert np.abs(out.cpu().double().numpy() - want).max() <= ATOL
+    wwant = O.stream_window_attn(bits(c["q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), seq, w.n_sink, w.window,
+                                 scale)
+    assert np.abs(wout.cpu().double().numpy() - wwant).max() <= ATOL
+
+
+def test_retrieval_window_draft_short_contexts(cuda_lib):
+    """Contexts shorter than a chunk, than the sinks plus the window, and empty."""
+    w = small_workload(B=4, Hq=8, Hkv=2, L=700, budget=8 * 16, ragged=False)
+    c = make_case(w)
+    seq = np.array([3, 0, 50, 700], dtype=np.int32)
+    c["seq"] = torch.from_numpy(seq).cuda()
+    scale = scale_for(w.D)
+    M = torch.empty((w.B, w.Hkv, -(-w.L // w.chunk), w.D), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.tf_build_chunk_means(c["K"], c["seq"], M)
+    idx0, nsel0, _ = cuda_lib.tf_retrieval_draft_attn(c["q"], M, c["K"], c["V"], c["seq"], w.kc, scale)
+    idx, nsel, out, wout = cuda_lib.tf_retrieval_window_draft_attn(c["q"], M, c["K"], c["V"], c["seq"], w.kc, scale,
+                                                                   w.n_sink, w.window)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), idx0.cpu().numpy()) and np.array_equal(nsel.cpu().numpy(),
+                                                                                     nsel0.cpu().numpy())
+    want = O.sparse_decode_attn(bits(c["q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), seq, idx.cpu().numpy(),
+                                nsel.cpu().numpy(), w.chunk, scale)
+    assert np.abs(out.cpu().double().numpy() - want).max() <= ATOL
+    wwant = O.stream_window_attn(bits(c["q_cpu"]), bits(c["K_cpu"]), bits(c["V_cpu"]), seq, w.n_sink, w.window,
+                                 scale)
+    assert np.abs(wout.cpu().double().numpy() - wwant).max() <= ATOL
+    assert np.all(wout.cpu().numpy()[1] == 0)
