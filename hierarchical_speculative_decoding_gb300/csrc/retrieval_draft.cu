@@ -156,8 +156,9 @@ __device__ __forceinline__ void mma_pv(float (&c)[4], uint32_t a0, uint32_t a1, 
 // group) slots 8..15.
 __device__ __forceinline__ int slot_of(int warp) { return (warp + kEarlySlots) % kRingSlots; }
 
-template <int NQ>
+template <int NQ, bool WIN>
 __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __grid_constant__ DraftParams p) {
+  static_assert(!WIN || NQ >= 2, "the window rows ride in the tensor-core consumers' fragments");
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* const smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(16) float qsm[NQ * kHeadDim];  // scaled query rows, permuted (see below)
@@ -166,14 +167,16 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
   __shared__ __align__(16) uint16_t qbf[NQ >= 2 ? kChunk * kQPitch / 2 : 8];
   __shared__ __align__(8) uint64_t bar_full[kRingSlots];
   __shared__ int slot_n[kRingSlots], slot_uses[kRingSlots];
-  // rows of a warp's state: the heads (NQ), or for the tensor-core consumers
-  // the 8 fragment rows: heads 0..3, then the window rows 4..7
-  constexpr int kRowsW = NQ >= 2 ? 8 : NQ;
+  // rows of a warp's state: the heads (NQ), or with a window output all 8
+  // fragment rows: heads 0..3, then the window rows 4..7
+  constexpr int kRowsW = WIN ? 8 : NQ;
   __shared__ float wm[kComputeWarps][kRowsW], wl[kComputeWarps][kRowsW];
-  __shared__ float cpart[kRowsW][kHeadDim], cm[kRowsW], cl[kRowsW];
+  __shared__ __align__(16) float cpart[kRowsW][kHeadDim];
+  __shared__ float cm[kRowsW], cl[kRowsW];
   __shared__ uint8_t slot_win[kRingSlots];  // 1: the slot holds a window piece
   __shared__ uint32_t s_min;
   __shared__ int s_na, s_ntot, s_abort, s_hcnt, s_next;
+  __shared__ int s_wg[4];  // window geometry: sinks kept, first window key, sink pieces, pieces
   __shared__ int s_hroff[kMaxCluster + 1];
   __shared__ volatile int s_cut_done;
 
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
     for (int e = threadIdx.x; e < kChunk * kQPitch / 2; e += kThreads) {
       const int h = e / (kQPitch / 2), d = e % (kQPitch / 2);
       // rows 0..G-1 the heads; with a window output rows 4..4+G-1 the same heads again
-      const int hq = h < G ? h : ((p.wout && h >= 4 && h - 4 < G) ? h - 4 : -1);
+      const int hq = h < G ? h : ((WIN && h >= 4 && h - 4 < G) ? h - 4 : -1);
       qbf[e] = (hq >= 0 && d < kHeadDim) ? qg[hq * kHeadDim + d] : (uint16_t)0;
     }
   }
@@ -267,17 +270,27 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
   const uint16_t* Vu = p.V + (size_t)unit * p.Lmax * kHeadDim;
   // window pieces of this unit (with a window output): the sinks
   // [0, ns_eff) and the recent keys [w0, L) in pieces of up to 8 rows; list
-  // entry -1 - k is piece k
-  const bool win = NQ >= 2 && p.wout != nullptr;
-  const int ns_eff = min(p.n_sink, L), w0 = max(p.n_sink, L - p.window);
-  const int n_sp = (ns_eff + kChunk - 1) / kChunk;
-  const int n_pw = win ? n_sp + (max(L - w0, 0) + kChunk - 1) / kChunk : 0;
+  // entry -1 - k is piece k.  Lane 0 reads the geometry from shared memory
+  // when it stages a window piece.
+  constexpr bool win = WIN;
+  int n_pw = 0;
+  if (win) {
+    const int ns_eff = min(p.n_sink, L), w0 = max(p.n_sink, L - p.window);
+    const int n_sp = (ns_eff + kChunk - 1) / kChunk;
+    n_pw = n_sp + (max(L - w0, 0) + kChunk - 1) / kChunk;
+    if (threadIdx.x == 0) {
+      s_wg[0] = ns_eff;
+      s_wg[1] = w0;
+      s_wg[2] = n_sp;
+      s_wg[3] = n_pw;
+    }
+  }
   auto piece = [&](int k, int& y, int& nr) {
-    if (k < n_sp) {
+    if (k < s_wg[2]) {
       y = k * kChunk;
-      nr = min(kChunk, ns_eff - y);
+      nr = min(kChunk, s_wg[0] - y);
     } else {
-      y = w0 + (k - n_sp) * kChunk;
+      y = s_wg[1] + (k - s_wg[2]) * kChunk;
       nr = min(kChunk, L - y);
     }
   };
@@ -309,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
   auto issue_tma = [&](int slot, int c) {
     // a chunk id, or -1 - k for window piece k
     int y = 0, nr = 0;
-    const bool ok = c >= 0 ? c < C : (-1 - c) < n_pw;
+    bool ok = c >= 0 && c < C;
+    if constexpr (WIN) ok = c >= 0 ? c < C : (-1 - c) < s_wg[3];
     if (ok) {
       if (c >= 0) {
         y = c * kChunk;
@@ -321,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
     if (ok && !TF_DBG_OK(nr > 0 && y >= 0 && y + nr <= L && L <= p.Lmax, kDbgCacheRow)) nr = 0;
     if (!ok) atomicExch(&s_abort, 1);
     slot_n[slot] = nr;
-    slot_win[slot] = c < 0 ? 1 : 0;
+    if constexpr (WIN) slot_win[slot] = c < 0 ? 1 : 0;
     if (nr == 0) {
       mbar_arrive(&bar_full[slot]);
       return;
@@ -607,7 +621,8 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
         }
         // this lane: row g8 (heads 0..3, window rows 4..7), keys 2 t4 and 2 t4 + 1;
         // a chunk feeds the head rows, a window piece the window rows
-        const bool row_on = slot_win[slot] ? (lane >> 2) >= 4 : (lane >> 2) < 4;
+        bool row_on = true;  // without a window output rows past G hold zero queries, discarded
+        if constexpr (WIN) row_on = slot_win[slot] ? (lane >> 2) >= 4 : (lane >> 2) < 4;
         const float s0 = (row_on && 2 * t4 < nr) ? sc[0] * p.scale_log2 : -INFINITY;
         const float s1 = (row_on && 2 * t4 + 1 < nr) ? sc[1] * p.scale_log2 : -INFINITY;
         float cmx = fmaxf(s0, s1);
@@ -657,81 +672,120 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
       if (slot_uses[sl] > 0) mbar_wait(&bar_full[sl], (slot_uses[sl] - 1) & 1, 1u << 8);
   }
   __syncthreads();
-  float* wo = reinterpret_cast<float*>(ring);  // [kComputeWarps][NQ][128]
+  // Each warp's state: wo [kComputeWarps][kRowsW][128] over the idle ring.
+  // The tensor-core consumers' fragment rows 2 t4 and 2 t4 + 1 store with the
+  // column XOR-ed by 8 t4 (the four lanes of a quarter then write four bank
+  // groups); groups of four columns stay contiguous, so reads take float4s.
+  float* wo = reinterpret_cast<float*>(ring);
+  auto wo_col = [](int h, int d) { return NQ >= 2 ? d ^ (((h >> 1) & 3) << 3) : d; };
+  const int nrows = win ? 2 * rows : rows;  // merged rows: the heads, then the window rows
+  auto row_of = [&](int i) { return i < rows ? i : 4 + (i - rows); };
   if constexpr (NQ == 1) {
-#pragma unroll
-    for (int h = 0; h < NQ; ++h) {
-      if (lane == 0) {
-        wm[warp][h] = m[h];
-        wl[warp][h] = l[h];
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) wo[(warp * kRowsW + h) * kHeadDim + lane * 4 + i] = o[h][i];
+    if (lane == 0) {
+      wm[warp][0] = m[0];
+      wl[warp][0] = l[0];
     }
+    *reinterpret_cast<float4*>(wo + warp * kRowsW * kHeadDim + lane * 4) = make_float4(o[0][0], o[0][1], o[0][2], o[0][3]);
   } else {
     const int g8 = lane >> 2, t4 = lane & 3;
-    if (t4 == 0) {
+    if (t4 == 0 && g8 < kRowsW) {
       wm[warp][g8] = mh;
       wl[warp][g8] = lh;
     }
+    if (2 * t4 < kRowsW) {  // rows 2 t4 and 2 t4 + 1
 #pragma unroll
-    for (int bk = 0; bk < 8; ++bk)
+      for (int bk = 0; bk < 8; ++bk)
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        const int h = 2 * t4 + hb;
-        wo[(warp * kRowsW + h) * kHeadDim + 16 * bk + g8] = oc[bk][hb];
-        wo[(warp * kRowsW + h) * kHeadDim + 16 * bk + g8 + 8] = oc[bk][2 + hb];
-      }
+        for (int hb = 0; hb < 2; ++hb) {
+          const int h = 2 * t4 + hb;
+          float* row = wo + (warp * kRowsW + h) * kHeadDim;
+          row[wo_col(h, 16 * bk + g8)] = oc[bk][hb];
+          row[wo_col(h, 16 * bk + g8 + 8)] = oc[bk][2 + hb];
+        }
+    }
   }
   __syncthreads();
 
-  // ---- this CTA's partial state: merge the compute warps (the head rows,
-  // then with a window output the window rows 4..)
-  const int nrows = win ? 2 * rows : rows;
-  auto row_of = [&](int i) { return i < rows ? i : 4 + (i - rows); };
-  for (int e = threadIdx.x; e < nrows * kHeadDim; e += kThreads) {
-    const int h = row_of(e / kHeadDim), d = e % kHeadDim;
+  // ---- this CTA's partial state: merge the compute warps.  The scale of
+  // (warp, row) is computed once; the outputs are float4 weighted sums.
+  __shared__ float wf[kComputeWarps][kRowsW];
+  if (threadIdx.x < nrows) {
+    const int h = row_of(threadIdx.x);
     float mx = -INFINITY;
     for (int w = 0; w < kComputeWarps; ++w) mx = fmaxf(mx, wm[w][h]);
-    float ls = 0.0f, os = 0.0f;
+    cm[h] = mx;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < kComputeWarps * nrows; e += kThreads) {
+    const int w = e / nrows, h = row_of(e % nrows);
+    wf[w][h] = merge_scale(wm[w][h], cm[h]);
+  }
+  __syncthreads();
+  if (threadIdx.x < nrows) {
+    const int h = row_of(threadIdx.x);
+    float ls = 0.0f;
+    for (int w = 0; w < kComputeWarps; ++w) ls = fmaf(wf[w][h], wl[w][h], ls);
+    cl[h] = ls;
+  }
+  for (int e = threadIdx.x; e < nrows * (kHeadDim / 4); e += kThreads) {
+    const int h = row_of(e / (kHeadDim / 4)), d = 4 * (e % (kHeadDim / 4));
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     for (int w = 0; w < kComputeWarps; ++w) {
-      const float f = merge_scale(wm[w][h], mx);
-      ls = fmaf(f, wl[w][h], ls);
-      os = fmaf(f, wo[(w * kRowsW + h) * kHeadDim + d], os);
+      const float f = wf[w][h];
+      const float4 v = *reinterpret_cast<const float4*>(wo + (w * kRowsW + h) * kHeadDim + wo_col(h, d));
+      acc.x = fmaf(f, v.x, acc.x);
+      acc.y = fmaf(f, v.y, acc.y);
+      acc.z = fmaf(f, v.z, acc.z);
+      acc.w = fmaf(f, v.w, acc.w);
     }
-    cpart[h][d] = os;
-    if (d == 0) {
-      cm[h] = mx;
-      cl[h] = ls;
-    }
+    *reinterpret_cast<float4*>(&cpart[h][d]) = acc;
   }
   cluster_sync();
 
-  // ---- rank 0 merges the cluster's partial states and writes the outputs
+  // ---- rank 0 merges the cluster's partial states and writes the outputs:
+  // the scale of (rank, row), divided by the row's total, once; then 16-byte
+  // loads of every rank's partial outputs
   if (rank == 0) {
-    bool bad = false;
-    for (int rr = 0; rr < S; ++rr) bad |= dsmem_ld_u32(&s_abort, (uint32_t)rr) != 0;
-    const size_t orow = ((size_t)b * p.Hq + (size_t)g * G) * kHeadDim;
-    for (int e = threadIdx.x; e < nrows * kHeadDim; e += kThreads) {
-      const int h = row_of(e / kHeadDim), d = e % kHeadDim;
-      float mr[kMaxCluster];
-#pragma unroll
-      for (int rr = 0; rr < kMaxCluster; ++rr)
-        mr[rr] = rr < S ? __uint_as_float(dsmem_ld_u32(&cm[h], (uint32_t)rr)) : -INFINITY;
+    __shared__ float rf[kMaxCluster][kRowsW];
+    __shared__ int s_bad;
+    if (threadIdx.x == 0) s_bad = 0;
+    for (int e = threadIdx.x; e < S * nrows; e += kThreads) {
+      const int rr = e / nrows, h = row_of(e % nrows);
+      rf[rr][h] = __uint_as_float(dsmem_ld_u32(&cm[h], (uint32_t)rr));
+    }
+    __syncthreads();
+    if (threadIdx.x < S && dsmem_ld_u32(&s_abort, threadIdx.x) != 0) s_bad = 1;
+    if (threadIdx.x < nrows) {
+      const int h = row_of(threadIdx.x);
       float mx = -INFINITY;
-#pragma unroll
-      for (int rr = 0; rr < kMaxCluster; ++rr) mx = fmaxf(mx, mr[rr]);
-      float ls = 0.0f, os = 0.0f;
-#pragma unroll
-      for (int rr = 0; rr < kMaxCluster; ++rr) {
-        if (rr < S) {
-          const float f = merge_scale(mr[rr], mx);
-          ls = fmaf(f, __uint_as_float(dsmem_ld_u32(&cl[h], (uint32_t)rr)), ls);
-          os = fmaf(f, __uint_as_float(dsmem_ld_u32(&cpart[h][d], (uint32_t)rr)), os);
-        }
+      for (int rr = 0; rr < S; ++rr) mx = fmaxf(mx, rf[rr][h]);
+      float ls = 0.0f;
+      for (int rr = 0; rr < S; ++rr) {
+        const float f = merge_scale(rf[rr][h], mx);
+        rf[rr][h] = f;
+        ls = fmaf(f, __uint_as_float(dsmem_ld_u32(&cl[h], (uint32_t)rr)), ls);
       }
+      // 0 for a row with no keys at all
+      const float inv = ls > 0.0f ? 1.0f / ls : 0.0f;
+      for (int rr = 0; rr < S; ++rr) rf[rr][h] *= inv;
+    }
+    __syncthreads();
+    const bool bad = s_bad != 0;
+    const size_t orow = ((size_t)b * p.Hq + (size_t)g * G) * kHeadDim;
+    for (int e = threadIdx.x; e < nrows * (kHeadDim / 4); e += kThreads) {
+      const int h = row_of(e / (kHeadDim / 4)), d = 4 * (e % (kHeadDim / 4));
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int rr = 0; rr < S; ++rr) {
+        const float f = rf[rr][h];
+        const uint4 u = dsmem_ld_v4(&cpart[h][d], (uint32_t)rr);
+        acc.x = fmaf(f, __uint_as_float(u.x), acc.x);
+        acc.y = fmaf(f, __uint_as_float(u.y), acc.y);
+        acc.z = fmaf(f, __uint_as_float(u.z), acc.z);
+        acc.w = fmaf(f, __uint_as_float(u.w), acc.w);
+      }
+      if (bad) acc = make_float4(NAN, NAN, NAN, NAN);
       float* dst = h < 4 ? p.out + orow + (size_t)h * kHeadDim : p.wout + orow + (size_t)(h - 4) * kHeadDim;
-      dst[d] = bad ? NAN : (ls > 0.0f ? os / ls : 0.0f);
+      *reinterpret_cast<float4*>(dst + d) = acc;
     }
     if (threadIdx.x == 0) {
       if (C <= p.kc) {
@@ -748,13 +802,13 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
   cluster_sync();  // keep shared memory alive until rank 0 has read it
 }
 
-template <int NQ>
+template <int NQ, bool WIN>
 tf_status launch_draft(const DraftParams& p, int units, int Cmax, cudaStream_t stream) {
   static DeviceCache configured;
   if (!configured.get([] {
-        return cudaFuncSetAttribute(retrieval_draft_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(retrieval_draft_kernel<NQ, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)draft_smem(kMaxSliceKeys)) == cudaSuccess &&
-               cudaFuncSetAttribute(retrieval_draft_kernel<NQ>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+               cudaFuncSetAttribute(retrieval_draft_kernel<NQ, WIN>, cudaFuncAttributeNonPortableClusterSizeAllowed,
                                     1) == cudaSuccess;
       }))
     return TF_ERR_CUDA;
@@ -783,7 +837,7 @@ tf_status launch_draft(const DraftParams& p, int units, int Cmax, cudaStream_t s
     qc.attrs = qa;
     qc.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, retrieval_draft_kernel<NQ>, &qc) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, retrieval_draft_kernel<NQ, WIN>, &qc) != cudaSuccess) {
       (void)cudaGetLastError();  // this shape is not available: try a smaller one
       continue;
     }
@@ -809,7 +863,7 @@ tf_status launch_draft(const DraftParams& p, int units, int Cmax, cudaStream_t s
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, retrieval_draft_kernel<NQ>, p) != cudaSuccess) return TF_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, retrieval_draft_kernel<NQ, WIN>, p) != cudaSuccess) return TF_ERR_CUDA;
   return launch_status();
 }
 
@@ -846,10 +900,15 @@ tf_status draft_entry(const uint16_t* q, const uint16_t* M, const uint16_t* K, c
     if (rows_total >= (1ll << 31)) return TF_ERR_UNSUPPORTED;
     if (!make_piece_map(&p.mapK, K, rows_total) || !make_piece_map(&p.mapV, V, rows_total)) return TF_ERR_CUDA;
   }
+  const int cm = Cmax < 1 ? 1 : Cmax;
+  if (wout) {  // two to four heads (the window entry point refuses the rest)
+    if (G < 2) return TF_ERR_UNSUPPORTED;
+    return G == 2 ? launch_draft<2, true>(p, units, cm, stream) : launch_draft<4, true>(p, units, cm, stream);
+  }
   switch (G) {
-    case 1: return launch_draft<1>(p, units, Cmax < 1 ? 1 : Cmax, stream);
-    case 2: return launch_draft<2>(p, units, Cmax < 1 ? 1 : Cmax, stream);
-    default: return launch_draft<4>(p, units, Cmax < 1 ? 1 : Cmax, stream);
+    case 1: return launch_draft<1, false>(p, units, cm, stream);
+    case 2: return launch_draft<2, false>(p, units, cm, stream);
+    default: return launch_draft<4, false>(p, units, cm, stream);
   }
 }
 
