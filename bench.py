@@ -43,7 +43,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "draft+verify attn steps/s at 128K (Llama2-7B shape); achieved HBM GB/s vs peak"
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -59,7 +59,7 @@ def parse():
                     help="run the retrieval drafter as tf_chunk_scores_topk + tf_sparse_decode_attn")
     ap.add_argument("--extra-workloads", default="llama3-8b-gqa-128k-b4,mixed-b8-gqa-16k-128k",
                     help="comma-separated workloads timed after the headline one ('none': skip)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 # ---------------------------------------------------------------- helpers
@@ -344,6 +344,14 @@ def window_launches(G, T):
     return 1 if fits else 2
 
 
+def window_in_draft(G, T):
+    """Whether the step gives the window attention to the drafter: where the
+    window rows would widen the verify launch (two launches), the fused draft
+    carries them for two to four query heads per KV head
+    (tf_retrieval_window_draft_attn), so a layer stays two launches."""
+    return window_launches(G, T) == 2 and 2 <= G <= 4
+
+
 N_QUERY_SETS = 4   # consecutive steps cycle through this many seeded query sets
 HINT_SCALE = 0.7  # the draft's cut bound: the previous step's cut of the layer x 0.7
 
@@ -393,9 +401,7 @@ class StepState:
         self.ws_ver = tf.workspace(tf.tf_verify_attn_workspace(B, Hq, Hkv, L, T), dev)
         self.ws_vw = tf.workspace(tf.tf_verify_window_attn_workspace(B, Hq, Hkv, L, T, w.n_sink, w.window), dev)
         self.vw_launches = window_launches(Hq // Hkv, T)
-        # where the window rows do not fit the verify launch, two to four query heads take the window
-        # attention in the drafter's launch instead (tf_retrieval_window_draft_attn)
-        self.window_in_draft = self.vw_launches == 2 and 2 <= Hq // Hkv <= 4
+        self.window_in_draft = window_in_draft(Hq // Hkv, T)
         torch.cuda.synchronize()
 
     def bytes_per_launch(self):

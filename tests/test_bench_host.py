@@ -1,7 +1,7 @@
 """Host logic of bench.py that needs no GPU: the clock sampler's summary of
-nvidia-smi rows (throttle reasons that reject a run), the peak fallback, and
-the rule that recorded ncu traffic is used only for the kernel source it was
-captured on."""
+nvidia-smi rows (throttle reasons that reject a run), the peak fallback, the
+rule that recorded ncu traffic is used only for the kernel source it was
+captured on, and the step's launch shape on each benchmark workload."""
 
 import json
 import os
@@ -71,3 +71,29 @@ def test_committed_traffic_lines_name_existing_kernels():
     for parts in lines:
         assert len(parts) == 4 and len(parts[1]) == 16 and float(parts[3]) > 0
         assert os.path.exists(os.path.join(ROOT, "hierarchical_speculative_decoding_gb300", "csrc", parts[0]))
+
+
+def test_every_benchmark_workload_runs_two_launches_per_layer():
+    """The step's launch shape per workload: the window rows ride in the verify
+    launch where they fit (Llama2-7B: one query head per KV head), else in the
+    fused draft (GQA groups of two to four heads); either way a layer is two
+    launches.  Groups beyond four heads keep the separate window launch."""
+    from types import SimpleNamespace
+
+    from hierarchical_speculative_decoding_gb300 import synth
+
+    names = ["llama2-7b-128k-32layer", "llama3-8b-gqa-128k-b4", "mixed-b8-gqa-16k-128k"]
+    assert bench.parse([]).workload == names[0]
+    assert bench.parse([]).extra_workloads.split(",") == names[1:]
+    expect = {names[0]: (1, False), names[1]: (2, True), names[2]: (2, True)}
+    for name in names:
+        w = synth.WORKLOADS[name]
+        G = w.Hq // w.Hkv
+        st = SimpleNamespace(vw_launches=bench.window_launches(G, w.T), window_in_draft=bench.window_in_draft(G, w.T))
+        assert (st.vw_launches, st.window_in_draft) == expect[name], name
+        assert bench.launches_per_layer(st, two_call=False) == 2, name
+    for G, T in ((1, 6), (8, 6), (5, 3)):
+        assert not bench.window_in_draft(G, T)
+    for G in (2, 3, 4):
+        for T in range(1, 17):
+            assert bench.window_in_draft(G, T) == (bench.window_launches(G, T) == 2), (G, T)
