@@ -1,6 +1,7 @@
 // a2 + a3 + a4 (+ a5) fused -- the Force 2 retrieval drafter's decode attention
 // in one launch: chunk scores, top-k selection and attention over the selected
-// chunks.
+// chunks; optionally (a6) the Force 1 drafter's sink + window attention of the
+// same queries in the same launch.
 //
 // "TriForce: Hierarchical Speculative Decoding for LLMs", "The Three Forces of
 // TriForce": the retrieval drafter is the target model attending only to the
@@ -8,7 +9,7 @@
 // Outputs are those of the top-k call (idx, n_sel, s_cut) and of the sparse
 // attention call over that selection (out), computed in one pass.
 //
-// Design: the top-k cluster (one cluster of S <= 8 CTAs per (b, g) unit, CTA r
+// Design: the top-k cluster (one cluster of S <= 16 CTAs per (b, g) unit, CTA r
 // scoring the r-th slice of the chunk means; see topk_select.cuh) keeps going
 // after the cut: each CTA attends the chunks it selected itself, so no chunk
 // list goes through global memory and no second launch waits for the first.
@@ -31,9 +32,15 @@
 //    permuted layout, and owns 4 head dims of P V.  Two to four heads: the
 //    warp runs Q K^T and P V on the tensor cores (mma.sync fragments).  The
 //    online softmax runs in the log2 domain in fp32.
+//  * The window form (template WIN, two to four heads): the sink and window
+//    keys join the certain entries as pieces of up to 8 rows, and the MMA
+//    tile's B-fragment rows 4..7, idle with at most four heads, carry the same
+//    queries masked to those pieces; rows 0..3 are masked to the retrieved
+//    chunks.  The merges carry all 8 rows; rows 4.. go to the window output.
 //  * Warps merge in shared memory, then CTA rank 0 merges the S partial states
 //    of the cluster through distributed shared memory (log-sum-exp identity)
-//    and writes the output.
+//    and writes the output; both merges compute each (warp or rank, row)
+//    scale once and then sum float4s.
 // All waits are bounded; a timeout (only a hardware fault can cause one)
 // leaves NaN in the outputs.
 #include <cuda_bf16.h>
@@ -434,8 +441,9 @@ __global__ void __launch_bounds__(kThreads, 2) retrieval_draft_kernel(const __gr
   const int rows = G < NQ ? G : NQ;
   float m[NQ], l[NQ], o[NQ][4];
   // two to four heads (tensor-core consumers): lane (g, t) = (lane / 4, lane % 4)
-  // keeps the running max and sum of head g, and oc[bk] the output of dims
-  // 16 bk + g and 16 bk + g + 8 for heads 2t and 2t + 1
+  // keeps the running max and sum of fragment row g (head g; in the window
+  // form rows 4..7 are the window rows), and oc[bk] the output of dims
+  // 16 bk + g and 16 bk + g + 8 for rows 2t and 2t + 1
   float mh = -INFINITY, lh = 0.0f;
   float oc[NQ >= 2 ? 8 : 1][4];
 #pragma unroll
