@@ -39,6 +39,14 @@ def test_attention_calls_refuse_mismatched_shapes(cuda_lib):
         tf.tf_retrieval_draft_attn(q, M[:, :, :-1].contiguous(), K, V, seq, 8, 0.1)
     with pytest.raises(ValueError, match="M must be"):
         tf.tf_chunk_scores_topk(q, M[:, :, :-1].contiguous(), seq, w.L, 8)
+    out_sentinel = torch.full((w.B, w.Hq, w.D), 7.0, device="cuda")
+    with pytest.raises(ValueError, match="wout must be"):
+        tf.tf_retrieval_window_draft_attn(q, M, K, V, seq, 8, 0.1, w.n_sink, w.window, out=out_sentinel,
+                                          wout=torch.empty((w.B, w.Hq - 1, w.D), device="cuda"))
+    with pytest.raises(ValueError, match="cut_hint must be"):
+        tf.tf_retrieval_window_draft_attn(q, M, K, V, seq, 8, 0.1, w.n_sink, w.window, out=out_sentinel,
+                                          cut_hint=torch.zeros((w.B, w.Hkv + 1), device="cuda"))
+    assert bool((out_sentinel == 7.0).all())
     idx = torch.zeros((w.B, w.Hkv, 8), dtype=torch.int32, device="cuda")
     n_sel = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device="cuda")
     with pytest.raises(ValueError, match="n_sel must be"):
