@@ -97,3 +97,43 @@ def test_every_benchmark_workload_runs_two_launches_per_layer():
     for G in (2, 3, 4):
         for T in range(1, 17):
             assert bench.window_in_draft(G, T) == (bench.window_launches(G, T) == 2), (G, T)
+
+
+def test_algorithmic_bytes_match_hand_counts():
+    """The byte counts behind the roofline's `achieved`, on the two full-length
+    128K workloads with kc full chunks selected per (b, g), against counts done
+    by hand from the cache sizes:
+    - Llama2-7B verify: K + V of one layer, 32 heads x 131072 x 128 x 2 B x 2
+      = 2 GiB, + the 6 verify queries in (bf16) and out (fp32) per head
+      (32 x 6 x 128 x 6 B = 147456), + the window row's query and output that
+      ride in the launch (32 x 128 x 6 B = 24576);
+    - Llama2-7B draft: the chunk means (32 x 16384 x 256 B = 128 MiB), the ids
+      (32 x 512 x 4 B), the selected K + V (32 x 512 x 8 rows x 512 B = 64 MiB),
+      the query in and the output out (24576);
+    - GQA batch 4 verify: 2 GiB + 4 x 32 x 6 x 128 x 6 B (589824);
+    - GQA batch 4 draft with the window rows: 128 MiB + 4 x 8 x 512 x 4 B +
+      64 MiB + 4 x 32 x 128 x 6 B, + the 256 sink and window keys' K + V
+      (4 x 8 x 256 x 512 B = 4 MiB) and the window output (4 x 32 x 128 x 4 B)."""
+    import torch
+
+    from hierarchical_speculative_decoding_gb300 import synth
+
+    expect = {
+        "llama2-7b-128k-32layer": {"verify": 2**31 + 147456 + 24576,
+                                   "draft": 2**27 + 65536 + 2**26 + 24576},
+        "llama3-8b-gqa-128k-b4": {"verify": 2**31 + 589824,
+                                  "draft": 2**27 + 65536 + 2**26 + 98304 + 2**22 + 65536},
+    }
+    for name, want in expect.items():
+        w = synth.WORKLOADS[name]
+        G = w.Hq // w.Hkv
+        st = object.__new__(bench.StepState)  # the byte count needs no device state
+        st.w = w
+        st.seq_cpu = synth.seq_lens_for(w)
+        st.vw_launches = bench.window_launches(G, w.T)
+        st.window_in_draft = bench.window_in_draft(G, w.T)
+        st.idx = torch.arange(w.kc, dtype=torch.int32).expand(1, w.B, w.Hkv, w.kc).clone()
+        st.nsel = torch.full((1, w.B, w.Hkv), w.kc, dtype=torch.int32)
+        nb = st.bytes_per_launch()
+        assert nb["verify"] == want["verify"], name
+        assert nb["draft"] == want["draft"], name
