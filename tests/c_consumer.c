@@ -34,6 +34,12 @@ int main(void) {
   expect(tf_pack_retrieval_cache(fake, fake, ifake, ifake, ifake, 1, 2, 64, 128, 8, 4097, fake, fake, ifake, ifake,
                                  NULL),
          TF_ERR_UNSUPPORTED, "packing with kc above 4096");
+  expect(tf_retrieval_window_draft_attn(fake, fake, fake, fake, ifake, 1, 8, 2, 64, 128, 8, 4, 0.1f, NULL, 4, 60,
+                                        ifake, ifake, NULL, ffake, NULL, NULL),
+         TF_ERR_INVALID_ARG, "window draft without a window output");
+  expect(tf_retrieval_window_draft_attn(fake, fake, fake, fake, ifake, 1, 2, 2, 64, 128, 8, 4, 0.1f, NULL, 4, 60,
+                                        ifake, ifake, NULL, ffake, ffake, NULL),
+         TF_ERR_UNSUPPORTED, "window draft with one query head per KV head");
   expect(tf_check_status(NULL, 4096, NULL), TF_ERR_INVALID_ARG, "status of a missing workspace");
   expect(tf_chunk_scores_topk_workspace(1, 32, 131072, 8) == 0, 1, "top-k needs no workspace");
 
