@@ -59,6 +59,11 @@ def test_full_size_layer(cuda_lib, w):
     cut_other = torch.empty((w.B, w.Hkv), dtype=torch.float32, device="cuda")
     cuda_lib.tf_retrieval_draft_attn(q_other, M, K, V, seq, w.kc, scale, s_cut=cut_other)
     hidx, hnsel, hsp = cuda_lib.tf_retrieval_draft_attn(q, M, K, V, seq, w.kc, scale, cut_hint=cut_other * 0.7)
+    # two to four heads per KV head: the step's draft carries the window rows (tf_retrieval_window_draft_attn)
+    in_draft = 2 <= w.G <= 4
+    if in_draft:
+        widx, wnsel, wsp, wwi = cuda_lib.tf_retrieval_window_draft_attn(q, M, K, V, seq, w.kc, scale, w.n_sink,
+                                                                        w.window, cut_hint=cut_other * 0.7)
     sv = cuda_lib.tf_sparse_verify_attn(Q, K, V, seq, idx, nsel, scale)
     # offloaded verify as timed: pinned host K/V, 16K-position segments, copies on a side stream
     K_host = torch.empty(K.shape, dtype=K.dtype, pin_memory=True).copy_(K)
@@ -75,6 +80,10 @@ def test_full_size_layer(cuda_lib, w):
     # ... with or without the bound
     assert np.array_equal(hidx.cpu().numpy(), idx.cpu().numpy())
     assert np.array_equal(hnsel.cpu().numpy(), nsel.cpu().numpy())
+    if in_draft:
+        assert np.array_equal(widx.cpu().numpy(), idx.cpu().numpy())
+        assert np.array_equal(wnsel.cpu().numpy(), nsel.cpu().numpy())
+        wsp_h, wwi_h = wsp.cpu().double().numpy(), wwi.cpu().double().numpy()
     hsp_h = hsp.cpu().double().numpy()
     fsp_h = fsp.cpu().double().numpy()
     M_h, idx_h, nsel_h = bits(M), idx.cpu().numpy(), nsel.cpu().numpy()
@@ -106,10 +115,14 @@ def test_full_size_layer(cuda_lib, w):
         assert np.abs(sp_h[b, g * G : (g + 1) * G] - sp_o[0]).max() <= ATOL
         assert np.abs(fsp_h[b, g * G : (g + 1) * G] - sp_o[0]).max() <= ATOL
         assert np.abs(hsp_h[b, g * G : (g + 1) * G] - sp_o[0]).max() <= ATOL
+        if in_draft:
+            assert np.abs(wsp_h[b, g * G : (g + 1) * G] - sp_o[0]).max() <= ATOL
         # a6
         wi_o = O.stream_window_attn(qg, Kb, Vb, sl, w.n_sink, w.window, scale)
         assert np.abs(wi_h[b, g * G : (g + 1) * G] - wi_o[0]).max() <= ATOL
         assert np.abs(vww_h[b, g * G : (g + 1) * G] - wi_o[0]).max() <= ATOL
+        if in_draft:
+            assert np.abs(wwi_h[b, g * G : (g + 1) * G] - wi_o[0]).max() <= ATOL
         # a7
         ve_o = O.verify_attn(Q_h[b : b + 1, g * G : (g + 1) * G], Kb, Vb, sl, scale)
         assert np.abs(ve_h[b, g * G : (g + 1) * G] - ve_o[0]).max() <= ATOL
